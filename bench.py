@@ -1,0 +1,281 @@
+#!/usr/bin/env python
+"""Bench of the packed lookahead call on one GB300 (or N independent replicas).
+
+Workload (one bench step = one request): Llama-7B-shape random-init bf16
+model (32 layers, d 4096, 32 heads of 128, FFN 11008, vocab 32000, weights
+N(0, 0.02) seed 0), batch 1, a 512-token prompt from a seeded order-2 Markov
+chain with Zipf(1.1) next-token ranks (seed 2), greedy, 256 new tokens,
+W=15, N=5, G=15.
+
+Reported (one JSON line on rank 0):
+  value        committed tokens/s of the decode phase: tokens produced by the
+               packed calls / their device time (CUDA events on the library's
+               stream), summed over the timed requests and all ranks
+  e2e          tokens/s of the same requests through la_generate with host
+               prompt and host output (prompt H2D, prefill, decode, D2H)
+  roofline     the packed call against HBM: algorithmic bytes per call
+               (weights read once + committed K/V read + temporary K/V
+               written) / measured call time, peak = measured copy bandwidth
+  cpu_baseline the CPU oracle on this host's cores on a bounded sample
+Inputs are larger than L2 (13 GB of weights stream every call), so no L2
+flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+W_, N_, G_ = 15, 5, 15
+PROMPT_LEN, MAX_NEW = 512, 256
+
+
+def algorithmic_bytes_per_call(cfg, K_in: float, Q: float) -> float:
+    """Weights read once + committed K/V read + temporary K/V written, bf16."""
+    d, F, V, L = cfg.d_model, cfg.d_ffn, cfg.vocab, cfg.n_layers
+    HD = cfg.n_heads * cfg.head_dim
+    weights = L * (d * 3 * HD + HD * d + 3 * d * F) * 2 + V * d * 2 + (2 * L + 1) * d * 2
+    kv_read = K_in * L * 2 * HD * 2
+    kv_write = Q * L * 2 * HD * 2
+    return weights + kv_read + kv_write
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(cfg, weights, n_calls: int = 2, prompt_len: int = 24):
+    """The oracle (as it stands) on the host cores: a bounded sample of the same
+    workload — prefill of a short Markov prompt, then `n_calls` packed lookahead
+    calls at W=15, N=5, G=15; returns committed tokens/s of those calls."""
+    import numpy as np
+    import synth
+    from oracle import lookahead as la
+    from oracle.model import OracleModel, argmax_lowest
+    m = OracleModel(cfg, weights, compute_dtype=np.float32, store="bf16", cache_weights=True)
+    p = synth.markov_zipf_prompt(cfg.vocab, prompt_len, 2).tolist()
+    cache, lg = m.prefill(p)                    # also converts and caches the weights (not timed)
+    st = la.LookaheadState(p, argmax_lowest(lg[-1]), W_, N_, G_)
+    run = la.make_runner(m, cache, "meta")
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(n_calls):
+        rows, g = st.plan()
+        out = run.run(rows)
+        info = st.publish(rows, g, [argmax_lowest(x) for x in out])
+        run.commit(rows, info.commit_rows)
+        toks += len(info.emitted)
+    dt = time.perf_counter() - t0
+    return {"value": toks / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"oracle fp32 arithmetic, bf16 storage emulation; {n_calls} packed calls (W=15,N=5,G=15) "
+                      f"after a {prompt_len}-token prompt on the 7B shape; {toks} tokens in {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ar-steps", type=int, default=1)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import torch
+    import synth
+    cfg = synth.LLAMA_7B
+    config = {"workload": "llama-7b-shape bf16, batch 1, prompt 512 Markov/Zipf(1.1), 256 new tokens, greedy, "
+                          "W=15 N=5 G=15", "model": "llama-7b-shape (random init)", "global_batch": world,
+              "seq_len": PROMPT_LEN + MAX_NEW, "parallelism": f"replicas{world}",
+              "l2": "inputs larger than L2 (13 GB weights per call); no flush"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+        w = synth.llama_weights(cfg, 0, device=dev)
+        vals = []
+        for _ in range(max(1, args.warmup)):
+            pass          # the oracle has no warm-up state; warm-up runs would only repeat the sample
+        samples = [cpu_oracle_sample(cfg, w, n_calls=1) for _ in range(max(1, args.steps))]
+        v = statistics.mean(s["value"] for s in samples)
+        line = {"impl": "reference", "metric": "committed tokens/s", "value": v, "unit": "tokens/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+                "cpu_baseline": dict(samples[-1], value=v),
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from lookahead_decoding_gb300 import build
+    build()
+    from lookahead_decoding_gb300 import lib
+    L = lib()
+    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}")
+    ctx = L.Context(cfg, w, max_ctx=1024, max_W=W_, max_N=N_, max_G=G_)
+    prompt = synth.markov_zipf_prompt(cfg.vocab, PROMPT_LEN, 2).tolist()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        L.la_generate(ctx.ctx, prompt, MAX_NEW, W_, N_, G_)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    barrier()
+    t0 = time.perf_counter()
+    stats = []
+    outs = []
+    for _ in range(args.steps):
+        st = L.la_stats()
+        outs.append(L.la_generate(ctx.ctx, prompt, MAX_NEW, W_, N_, G_, stats=st))
+        stats.append(st)
+    barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+
+    decode_s = sum(s.decode_ns for s in stats) * 1e-9
+    calls = sum(s.steps for s in stats)
+    new_tokens = sum(s.tokens - 1 for s in stats)      # tokens of the packed calls (the first comes from the prefill)
+    tps = new_tokens / decode_s
+    call_ms = decode_s / calls * 1e3
+    # aggregate over ranks: total tokens / max time
+    if world > 1:
+        t = torch.tensor([new_tokens, decode_s, wall], dtype=torch.float64, device=f"cuda:{local}")
+        g = [torch.zeros_like(t) for _ in range(world)]
+        torch.distributed.all_gather(g, t)
+        tot_tok = sum(float(x[0]) for x in g)
+        max_dec = max(float(x[1]) for x in g)
+        wall = max(float(x[2]) for x in g)
+        tps = tot_tok / max_dec
+
+    # autoregressive decode on the same kernels
+    ar_stats = []
+    for _ in range(args.ar_steps):
+        st = L.la_stats()
+        ar = L.la_generate_ar(ctx.ctx, prompt, MAX_NEW, stats=st)
+        ar_stats.append(st)
+    ar_tps = sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)
+    same = all(o == ar for o in outs)
+
+    # kernels of ours launched in the timed region: per request the prefill
+    # (2 chunks x (rows + embed + 8 per layer) + need + head 3 + finish), begin,
+    # and per packed call pack + embed + 8 per layer + head 3 + publish + commit
+    chunks = (PROMPT_LEN + 255) // 256
+    per_call = 2 + 8 * cfg.n_layers + 3 + 2
+    per_request = chunks * (2 + 8 * cfg.n_layers) + 1 + 3 + 1 + 1
+    launches = args.steps * per_request + calls * per_call
+    peaks, src = measured_peaks()
+    mean_K = PROMPT_LEN + MAX_NEW / 2.0
+    mean_Q = statistics.mean(s.mean_rows for s in stats)
+    bytes_call = algorithmic_bytes_per_call(cfg, mean_K, mean_Q)
+    achieved = bytes_call / (call_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    line = {
+        "metric": "committed tokens/s @ batch 1 (7B-shape bf16)",
+        "value": tps * (1 if world == 1 else 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config,
+        "tokens_per_call": new_tokens / calls,
+        "call_latency_ms": call_ms,
+        "prefill_ms": statistics.mean(s.prefill_ns for s in stats) * 1e-6,
+        "mean_rows_per_call": mean_Q,
+        "ar_tokens_per_s": ar_tps,
+        "speedup_vs_ar": tps / ar_tps if world == 1 else None,
+        "lookahead_equals_ar": same,
+        "e2e": {"value": (MAX_NEW * args.steps * world) / wall, "unit": "tokens/s",
+                "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": MAX_NEW * 4},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "whole packed call (all kernels of one step)",
+                     "algorithmic_bytes_per_call": bytes_call, "peak_source": src},
+        "step_roofline_frac": (bytes_call / (peak * 1e9)) / (call_ms * 1e-3),
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, w, n_calls=1)
+    ctx.close()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * liblookahead — C ABI of the packed per-step target call of Lookahead decoding
+ * on one GB300 (sm_103a).
+ *
+ * The method (Fu, Bailis, Stoica, Zhang, "Break the Sequential Dependency of
+ * LLM Inference Using Lookahead Decoding", §3; "M7.3 – Lookahead Decoding",
+ * §0x03–§0x07): every call runs one unchanged causal decoder over
+ *   - the ordinary row (the last committed token x_t),
+ *   - a lookahead branch: W window columns over N-1 Jacobi trajectory levels,
+ *   - a verification branch: up to G candidate suffixes of N-1 tokens looked up
+ *     in an n-gram pool under the key x_t,
+ * packed into one batch of rows with a branch-structured attention mask; the
+ * outputs feed a verifier (greedy, or exact sampling over disjoint one-hot
+ * proposals), the n-gram pool update, the K/V commit and the window shift.
+ *
+ * Conventions for every entry point
+ *   - Return value: LA_OK (0) or one of the LA_E* codes below.  la_strerror()
+ *     names it.  Every call is fail-closed (M7.3 §0x07 "publication order
+ *     should be fail-closed"): on any error no token is appended and the
+ *     committed K/V length, the window and the pool keep their previous
+ *     contents.
+ *   - "host" pointers are ordinary CPU memory owned by the caller; the
+ *     library copies from/into them before returning.  "device" pointers are
+ *     CUDA global memory on the context's device, owned by the caller and
+ *     borrowed for the lifetime of the context (weights).
+ *   - All GPU work is enqueued on the CUDA stream given to la_init.  Calls
+ *     that return host results (la_prefill, la_step, la_generate*,
+ *     la_debug_*) synchronise that stream before returning.
+ *   - A context is not thread-safe; use one context per thread.
+ */
+#ifndef LOOKAHEAD_H
+#define LOOKAHEAD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define LA_OK        0
+#define LA_EINVAL    1  /* bad argument: null pointer, N < 3, W < 1, G < 0, id out of range */
+#define LA_ECAPACITY 2  /* exceeds a size fixed at la_init (context length, W, N, G, prompt) */
+#define LA_ESTATE    3  /* call out of order: step before prefill, W/N/G changed without re-prefill */
+#define LA_ECUDA     4  /* a CUDA runtime/driver call failed (details: la_last_cuda_error) */
+#define LA_EDEVICE   5  /* a kernel set the device error word (bounds or invariant check) */
+#define LA_ETIMEOUT  6  /* a bounded device wait ran out; the step's results were discarded */
+#define LA_ENOTSUP   7  /* configuration not supported by this build (dtype, head_dim, ...) */
+
+/* ---- element types ------------------------------------------------------- */
+#define LA_F32  0       /* fp32 weights, activations and K/V */
+#define LA_BF16 1       /* bf16 weights, activations and K/V; fp32 accumulation */
+
+typedef struct la_ctx la_ctx;
+
+/* Decoder-only Llama-style model: RMSNorm, RoPE (rotate-half, theta), SwiGLU
+ * MLP, multi-head attention with n_kv_heads == n_heads, untied LM head, no
+ * biases.  head_dim must be 32 or 128; d_model == n_heads * head_dim. */
+typedef struct {
+    int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ffn, vocab;
+    float   rms_eps;     /* e.g. 1e-5 */
+    float   rope_theta;  /* e.g. 10000 */
+    int32_t dtype;       /* LA_F32 or LA_BF16 */
+} la_model_cfg;
+
+/* Device pointers to the weights, row-major, element type cfg.dtype.
+ *   tok_emb [vocab][d_model]   lm_head [vocab][d_model]   final_norm [d_model]
+ * Per layer l (host arrays of n_layers device pointers):
+ *   attn_norm[l], mlp_norm[l]  [d_model]
+ *   wq[l], wk[l], wv[l]        [n_heads*head_dim][d_model]
+ *   wo[l]                      [d_model][n_heads*head_dim]
+ *   w_gate[l], w_up[l]         [d_ffn][d_model]
+ *   w_down[l]                  [d_model][d_ffn]
+ * Every matrix must be 16-byte aligned.  The caller keeps them alive and
+ * unchanged until la_free.  The host pointer arrays are copied by la_init. */
+typedef struct {
+    const void* tok_emb;
+    const void* lm_head;
+    const void* final_norm;
+    const void* const* attn_norm;
+    const void* const* wq;
+    const void* const* wk;
+    const void* const* wv;
+    const void* const* wo;
+    const void* const* mlp_norm;
+    const void* const* w_gate;
+    const void* const* w_up;
+    const void* const* w_down;
+} la_weights;
+
+/* Sampling policy (break the sequential dependency §2, §3.2; M7.3 §0x05B):
+ * target p = softmax(logits / temperature) restricted to the top-p nucleus
+ * (probability descending, ties by lower id, the crossing token kept),
+ * renormalised.  Uniforms come from Philox4x32-10 keyed by seed with the
+ * counter (step, offset, test, purpose).  Pass NULL for greedy decoding. */
+typedef struct {
+    float    temperature;  /* > 0 */
+    float    top_p;        /* (0, 1] */
+    uint64_t seed;
+} la_sampling;
+
+/* Counters of the last la_generate / la_generate_ar call. */
+typedef struct {
+    int64_t steps;              /* packed target calls after the prefill */
+    int64_t tokens;             /* tokens returned (including the prefill's) */
+    int64_t prefill_ns;         /* device time of the prefill */
+    int64_t decode_ns;          /* device time of all steps */
+    int32_t emitted_hist[16];   /* calls that emitted 1, 2, ... tokens (E_t = a+1) */
+    double  mean_candidates;    /* mean C_t over steady calls */
+    double  mean_rows;          /* mean Q over calls */
+} la_stats;
+
+/* Create a context on the current CUDA device.
+ *   cfg, w        : model (see above); weights are borrowed device memory.
+ *   max_ctx       : largest committed length (prompt + generated tokens).
+ *   max_W, max_N, max_G : largest lookahead knobs any later call may use
+ *                   (max_N >= 3, max_W >= 1, max_G >= 0); they size the
+ *                   row buffers: Q <= (max_W + max_G) * (max_N - 1) + max_N.
+ *   stream        : cudaStream_t to enqueue on (NULL = the legacy default).
+ *   out           : receives the context.
+ * Allocates the K/V cache, the call's temporary K/V rows, the n-gram pool
+ * ([vocab][max_G][max_N-1] ids), the window, the activations and scratch
+ * with cudaMalloc.  Errors: LA_EINVAL, LA_ENOTSUP, LA_ECUDA. */
+int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
+            int max_W, int max_N, int max_G, void* stream, la_ctx** out);
+
+/* Prefill the prompt (host ids, n >= 1, each in [0, vocab)) with one causal
+ * forward; resets the K/V cache, the window, the pool and the step counter.
+ * *first_token (host) receives the first generated token (argmax of the last
+ * prompt row, or a draw from it when `s` is not NULL).  Errors: LA_EINVAL,
+ * LA_ECAPACITY (n > max_ctx - 1), LA_ECUDA, LA_EDEVICE. */
+int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s,
+               int32_t* first_token);
+
+/* One packed target call (M7.3 §0x03A steady-state lifecycle, steps 1-8):
+ * lookup, pack, forward, verify, K/V commit, pool update, window shift.
+ * The first call after la_prefill fixes W, N, G (1 <= W <= max_W,
+ * 3 <= N <= max_N, 0 <= G <= max_G) and seeds window level 0 with
+ * W+N-3 prompt tokens (cyclically); the first N-2 calls are warm-up fills
+ * without a verification branch.  Later calls must pass the same W, N, G
+ * (LA_ESTATE otherwise).  out (host, capacity >= N) receives the emitted
+ * tokens, *n_out their number (1..N). */
+int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s,
+            int32_t* out, int* n_out);
+
+/* Prefill + lookahead steps until max_new tokens (the prefill's token
+ * included) have been produced; out (host, capacity >= max_new) receives
+ * exactly max_new tokens (*n_out = max_new).  Steps run as captured CUDA
+ * graphs without host synchronisation between them.  stats may be NULL. */
+int la_generate(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
+                int W, int N, int G, const la_sampling* s,
+                int32_t* out, int* n_out, la_stats* stats);
+
+/* The same as la_generate but with plain autoregressive decoding (one row
+ * per call) on the same kernels: the baseline the method must equal
+ * (greedy) and beat. */
+int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
+                   const la_sampling* s, int32_t* out, int* n_out, la_stats* stats);
+
+/* ---- inspection (tests) -------------------------------------------------- */
+
+/* Keep fp32 logits of the rows whose outputs the verifier reads (the
+ * ordinary row, the deepest trajectory level, every verification row) for
+ * la_debug_logits.  flags: bit 0 = keep logits. */
+int la_set_debug(la_ctx* ctx, int flags);
+
+/* fp32 logits [*n_rows][vocab] of the last call's needed rows and their
+ * packed row indices.  host buffers of capacity cap_rows rows. */
+int la_debug_logits(la_ctx* ctx, float* logits, int32_t* rows, int cap_rows, int* n_rows);
+
+/* Snapshot of the request state after the last call (host buffers):
+ *   hdr[16]        : K (committed length), x_t, W, N, G, n_levels, step,
+ *                    Q, C_t, a, winner, n_out, err, steady, n_need, n_deep
+ *   levels         : [max_N-1][max_W+max_N-3] window ids, level_len[max_N-1]
+ *   row_tok/pos/meta : [Qmax] ids, logical positions and metadata of the
+ *                    last packed call (meta = role | level<<2 | column<<8 |
+ *                    candidate<<16 | offset<<24; role 0 ordinary,
+ *                    1 lookahead, 2 verify)
+ * Any pointer may be NULL. */
+int la_debug_state(la_ctx* ctx, int32_t* hdr, int32_t* levels, int32_t* level_len,
+                   int32_t* row_tok, int32_t* row_pos, int32_t* row_meta);
+
+/* The pool bucket of `key`: up to max_G suffixes of N-1 ids, oldest first
+ * (host buffer [max_G][max_N-1]); *count receives the bucket size. */
+int la_debug_pool(la_ctx* ctx, int key, int32_t* suffixes, int* count);
+
+/* One call of the state machine with the model forward replaced by given
+ * per-row outputs (host): argmax[q] for every packed row q of this call and,
+ * in sampling mode, fp32 logits[q][vocab] (else NULL).  Q must equal the row
+ * count the call packs (LA_ESTATE otherwise).  Everything else — lookup,
+ * pack, verification, pool, window, out ring — is the product path; the K/V
+ * commit copies whatever the temporary rows hold. */
+int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q,
+                   const int32_t* argmax, const float* logits, int32_t* out, int* n_out);
+
+/* Sizes fixed at la_init: [0]=Qmax [1]=max_W [2]=max_N [3]=max_G [4]=max_ctx
+ * [5]=vocab [6]=window row length (max_W+max_N-3) [7]=path length bound. */
+int la_query(la_ctx* ctx, int32_t* sizes8);
+
+void        la_free(la_ctx* ctx);
+const char* la_strerror(int code);
+/* The last CUDA error string seen by this context (or "" if none). */
+const char* la_last_cuda_error(la_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LOOKAHEAD_H */

@@ -1,0 +1,277 @@
+"""ctypes binding of liblookahead (argument marshalling only).
+
+Every function named ``la_*`` here calls the C entry point of the same name
+declared in include/lookahead.h; all computation happens in the library's
+CUDA kernels.  Importing this module loads ``liblookahead.so`` from the
+package directory and raises if it is missing — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblookahead.so")
+
+LA_OK, LA_EINVAL, LA_ECAPACITY, LA_ESTATE, LA_ECUDA, LA_EDEVICE, LA_ETIMEOUT, LA_ENOTSUP = range(8)
+LA_F32, LA_BF16 = 0, 1
+
+EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
+           "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
+           "la_last_cuda_error"]
+
+
+class la_model_cfg(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("d_ffn", C.c_int32), ("vocab", C.c_int32), ("rms_eps", C.c_float),
+                ("rope_theta", C.c_float), ("dtype", C.c_int32)]
+
+
+_PP = C.POINTER(C.c_void_p)
+
+
+class la_weights(C.Structure):
+    _fields_ = [("tok_emb", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
+                ("attn_norm", _PP), ("wq", _PP), ("wk", _PP), ("wv", _PP), ("wo", _PP),
+                ("mlp_norm", _PP), ("w_gate", _PP), ("w_up", _PP), ("w_down", _PP)]
+
+
+class la_sampling(C.Structure):
+    _fields_ = [("temperature", C.c_float), ("top_p", C.c_float), ("seed", C.c_uint64)]
+
+
+class la_stats(C.Structure):
+    _fields_ = [("steps", C.c_int64), ("tokens", C.c_int64), ("prefill_ns", C.c_int64), ("decode_ns", C.c_int64),
+                ("emitted_hist", C.c_int32 * 16), ("mean_candidates", C.c_double), ("mean_rows", C.c_double)]
+
+
+class LaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {code} ({strerror(code)})")
+        self.code = code
+
+
+def _load() -> C.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with lookahead_decoding_gb300.build.build()")
+    lib = C.CDLL(LIB_PATH)
+    i32p = C.POINTER(C.c_int32)
+    f32p = C.POINTER(C.c_float)
+    vp = C.c_void_p
+    sig = {
+        "la_init": (C.c_int, [C.POINTER(la_model_cfg), C.POINTER(la_weights), C.c_int, C.c_int, C.c_int, C.c_int, vp,
+                              C.POINTER(vp)]),
+        "la_prefill": (C.c_int, [vp, i32p, C.c_int, C.POINTER(la_sampling), i32p]),
+        "la_step": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), i32p, C.POINTER(C.c_int)]),
+        "la_generate": (C.c_int, [vp, i32p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), i32p,
+                                  C.POINTER(C.c_int), C.POINTER(la_stats)]),
+        "la_generate_ar": (C.c_int, [vp, i32p, C.c_int, C.c_int, C.POINTER(la_sampling), i32p, C.POINTER(C.c_int),
+                                     C.POINTER(la_stats)]),
+        "la_set_debug": (C.c_int, [vp, C.c_int]),
+        "la_debug_logits": (C.c_int, [vp, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
+        "la_debug_state": (C.c_int, [vp, i32p, i32p, i32p, i32p, i32p, i32p]),
+        "la_debug_pool": (C.c_int, [vp, C.c_int, i32p, C.POINTER(C.c_int)]),
+        "la_step_inject": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), C.c_int, i32p, f32p, i32p,
+                                     C.POINTER(C.c_int)]),
+        "la_query": (C.c_int, [vp, i32p]),
+        "la_free": (None, [vp]),
+        "la_strerror": (C.c_char_p, [C.c_int]),
+        "la_last_cuda_error": (C.c_char_p, [vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def strerror(code: int) -> str:
+    return LIB.la_strerror(code).decode()
+
+
+def _i32(a) -> Tuple[np.ndarray, C.POINTER(C.c_int32)]:
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return arr, arr.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def _check(code: int, what: str, ctx=None) -> None:
+    if code != LA_OK:
+        msg = what
+        if ctx is not None and code == LA_ECUDA:
+            msg += " [" + LIB.la_last_cuda_error(ctx).decode() + "]"
+        raise LaError(code, msg)
+
+
+def _sampling(s) -> Optional[la_sampling]:
+    if s is None:
+        return None
+    if isinstance(s, la_sampling):
+        return s
+    t, p, seed = s
+    return la_sampling(float(t), float(p), int(seed))
+
+
+# ---------------------------------------------------------------------------
+# entry points with the C names
+# ---------------------------------------------------------------------------
+
+def la_init(cfg: la_model_cfg, weights: la_weights, max_ctx: int, max_W: int, max_N: int, max_G: int,
+            stream: int = 0):
+    ctx = C.c_void_p()
+    code = LIB.la_init(C.byref(cfg), C.byref(weights), max_ctx, max_W, max_N, max_G, C.c_void_p(stream or None),
+                       C.byref(ctx))
+    _check(code, "la_init")
+    return ctx
+
+
+def la_prefill(ctx, prompt: Sequence[int], sampling=None) -> int:
+    arr, p = _i32(prompt)
+    tok = C.c_int32()
+    s = _sampling(sampling)
+    _check(LIB.la_prefill(ctx, p, len(arr), C.byref(s) if s else None, C.byref(tok)), "la_prefill", ctx)
+    return int(tok.value)
+
+
+def la_step(ctx, W: int, N: int, G: int, sampling=None) -> List[int]:
+    out = (C.c_int32 * 16)()
+    n = C.c_int()
+    s = _sampling(sampling)
+    _check(LIB.la_step(ctx, W, N, G, C.byref(s) if s else None, out, C.byref(n)), "la_step", ctx)
+    return [int(out[i]) for i in range(n.value)]
+
+
+def la_generate(ctx, prompt, max_new: int, W: int, N: int, G: int, sampling=None, stats: Optional[la_stats] = None):
+    arr, p = _i32(prompt)
+    out = np.zeros(max_new, dtype=np.int32)
+    n = C.c_int()
+    s = _sampling(sampling)
+    _check(LIB.la_generate(ctx, p, len(arr), max_new, W, N, G, C.byref(s) if s else None,
+                           out.ctypes.data_as(C.POINTER(C.c_int32)), C.byref(n),
+                           C.byref(stats) if stats is not None else None), "la_generate", ctx)
+    return out[: n.value].tolist()
+
+
+def la_generate_ar(ctx, prompt, max_new: int, sampling=None, stats: Optional[la_stats] = None):
+    arr, p = _i32(prompt)
+    out = np.zeros(max_new, dtype=np.int32)
+    n = C.c_int()
+    s = _sampling(sampling)
+    _check(LIB.la_generate_ar(ctx, p, len(arr), max_new, C.byref(s) if s else None,
+                              out.ctypes.data_as(C.POINTER(C.c_int32)), C.byref(n),
+                              C.byref(stats) if stats is not None else None), "la_generate_ar", ctx)
+    return out[: n.value].tolist()
+
+
+def la_query(ctx) -> Dict[str, int]:
+    v = (C.c_int32 * 8)()
+    _check(LIB.la_query(ctx, v), "la_query")
+    keys = ["Qmax", "max_W", "max_N", "max_G", "max_ctx", "vocab", "LMAX", "PMAX"]
+    return {k: int(v[i]) for i, k in enumerate(keys)}
+
+
+def la_set_debug(ctx, flags: int) -> None:
+    _check(LIB.la_set_debug(ctx, flags), "la_set_debug")
+
+
+def la_debug_logits(ctx, cap_rows: int, vocab: int):
+    logits = np.zeros((cap_rows, vocab), dtype=np.float32)
+    rows = np.zeros(cap_rows, dtype=np.int32)
+    n = C.c_int()
+    _check(LIB.la_debug_logits(ctx, logits.ctypes.data_as(C.POINTER(C.c_float)),
+                               rows.ctypes.data_as(C.POINTER(C.c_int32)), cap_rows, C.byref(n)), "la_debug_logits", ctx)
+    return logits[: n.value], rows[: n.value]
+
+
+HDR_KEYS = ["K", "x_t", "W", "N", "G", "n_levels", "step", "Q", "C_t", "a", "winner", "n_out", "err", "steady",
+            "n_need", "n_deep"]
+
+
+def la_debug_state(ctx):
+    q = la_query(ctx)
+    R = q["max_N"] - 1
+    hdr = np.zeros(16, dtype=np.int32)
+    levels = np.zeros((R, q["LMAX"]), dtype=np.int32)
+    lens = np.zeros(R, dtype=np.int32)
+    tok = np.zeros(q["Qmax"], dtype=np.int32)
+    pos = np.zeros(q["Qmax"], dtype=np.int32)
+    meta = np.zeros(q["Qmax"], dtype=np.int32)
+    P = lambda a: a.ctypes.data_as(C.POINTER(C.c_int32))
+    _check(LIB.la_debug_state(ctx, P(hdr), P(levels), P(lens), P(tok), P(pos), P(meta)), "la_debug_state", ctx)
+    h = dict(zip(HDR_KEYS, hdr.tolist()))
+    lv = [levels[r, : lens[r]].tolist() if r < h["n_levels"] else None for r in range(R)]
+    Q = h["Q"]
+    return h, lv, tok[:Q].tolist(), pos[:Q].tolist(), meta[:Q].tolist()
+
+
+def la_debug_pool(ctx, key: int):
+    q = la_query(ctx)
+    G, S = max(1, q["max_G"]), q["max_N"] - 1
+    buf = np.zeros((G, S), dtype=np.int32)
+    n = C.c_int()
+    _check(LIB.la_debug_pool(ctx, key, buf.ctypes.data_as(C.POINTER(C.c_int32)), C.byref(n)), "la_debug_pool", ctx)
+    return [tuple(r) for r in buf[: n.value].tolist()]
+
+
+def la_step_inject(ctx, W: int, N: int, G: int, argmax: Sequence[int], sampling=None, logits=None) -> List[int]:
+    arr, p = _i32(argmax)
+    out = (C.c_int32 * 16)()
+    n = C.c_int()
+    s = _sampling(sampling)
+    lp = None
+    if logits is not None:
+        lg = np.ascontiguousarray(logits, dtype=np.float32)
+        lp = lg.ctypes.data_as(C.POINTER(C.c_float))
+    _check(LIB.la_step_inject(ctx, W, N, G, C.byref(s) if s else None, len(arr), p, lp, out, C.byref(n)),
+           "la_step_inject", ctx)
+    return [int(out[i]) for i in range(n.value)]
+
+
+def la_free(ctx) -> None:
+    LIB.la_free(ctx)
+
+
+# ---------------------------------------------------------------------------
+# convenience: a context built from a dict of torch weight tensors
+# ---------------------------------------------------------------------------
+
+class Context:
+    """Owns one la_ctx; ``weights`` maps the tensor names tok_emb, lm_head,
+    final_norm and l{i}.{attn_norm,wq,wk,wv,wo,mlp_norm,w_gate,w_up,w_down} to
+    CUDA tensors in the model dtype (kept referenced for the context's life)."""
+
+    def __init__(self, cfg, weights: Dict[str, "object"], max_ctx: int, max_W: int, max_N: int, max_G: int,
+                 stream: int = 0):
+        dt = LA_F32 if cfg.dtype == "f32" else LA_BF16
+        self.cfg = la_model_cfg(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.d_ffn,
+                                cfg.vocab, cfg.rms_eps, cfg.rope_theta, dt)
+        self._keep = weights
+        L = cfg.n_layers
+
+        def ptrs(name):
+            arr = (C.c_void_p * L)(*[weights[f"l{l}.{name}"].data_ptr() for l in range(L)])
+            self._arrays.append(arr)
+            return C.cast(arr, _PP)
+
+        self._arrays = []
+        self.w = la_weights(weights["tok_emb"].data_ptr(), weights["lm_head"].data_ptr(),
+                            weights["final_norm"].data_ptr(), ptrs("attn_norm"), ptrs("wq"), ptrs("wk"), ptrs("wv"),
+                            ptrs("wo"), ptrs("mlp_norm"), ptrs("w_gate"), ptrs("w_up"), ptrs("w_down"))
+        self.ctx = la_init(self.cfg, self.w, max_ctx, max_W, max_N, max_G, stream)
+        self.vocab = cfg.vocab
+
+    def close(self):
+        if self.ctx:
+            la_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,687 @@
+// C ABI of liblookahead: context, device state, the step orchestrator and
+// the CUDA-graph driven generate loop.  See include/lookahead.h for the
+// contract of every entry point.
+#include "la_common.cuh"
+#include "la_kernels.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+namespace {
+
+constexpr int PREFILL_CHUNK = 256;
+
+struct Graph {
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t x = nullptr;
+};
+
+}  // namespace
+
+struct la_ctx {
+    la_model_cfg cfg{};
+    int bf16 = 0;
+    int tc = 0;                       // tensor-core GEMMs (bf16 models unless LA_GEMM=ffma)
+    size_t esz = 4;
+    int max_ctx = 0, max_W = 0, max_N = 0, max_G = 0;
+    int Qmax = 0, Qcap = 0, PMAX = 0, LMAX = 0, Rmax = 0, Smax = 0, Gmax = 0, rope_len = 0, out_cap = 0;
+    int HD = 0;
+    cudaStream_t st = nullptr;
+    bool own_stream = false;
+    std::string last_err;
+
+    // weights (borrowed)
+    const void *emb = nullptr, *head = nullptr, *fnorm = nullptr;
+    std::vector<const void*> attn_norm, wq, wk, wv, wo, mlp_norm, wg, wu, wd;
+
+    // device state
+    LaDev d{};
+    std::vector<void*> allocs;
+    float* x = nullptr;
+    void *xn = nullptr, *qkv = nullptr, *qbuf = nullptr, *attn = nullptr, *act = nullptr, *hn = nullptr;
+    void *cache = nullptr, *temp = nullptr;
+    float *rcos = nullptr, *rsin = nullptr;
+    float* logits = nullptr;          // [Qcap][V] fp32
+    float* logits_in = nullptr;       // [Qmax][V] staging for injected logits
+    int32_t* argmax_in = nullptr;     // [Qcap]
+    TcWork work{};
+
+    // tensor-core GEMM descriptors (bf16 models)
+    std::vector<TcGemm> g_qkv, g_o, g_gu, g_down;
+    TcGemm g_head{};
+
+    // request state on the host side
+    bool prefilled = false, begun = false;
+    int W = 0, N = 0, G = 0, mode = 0, sampling = 0;
+    int prompt_len = 0;
+    int debug = 0;
+    std::map<int, Graph> graphs;
+};
+
+// ---------------------------------------------------------------------------
+// helpers
+// ---------------------------------------------------------------------------
+#define CK(expr)                                          \
+    do {                                                  \
+        cudaError_t _e = (expr);                          \
+        if (_e != cudaSuccess) {                          \
+            ctx->last_err = cudaGetErrorString(_e);       \
+            return LA_ECUDA;                              \
+        }                                                 \
+    } while (0)
+
+static int dalloc(la_ctx* ctx, void** p, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) { ctx->last_err = cudaGetErrorString(e); return LA_ECUDA; }
+    ctx->allocs.push_back(*p);
+    e = cudaMemset(*p, 0, bytes);
+    if (e != cudaSuccess) { ctx->last_err = cudaGetErrorString(e); return LA_ECUDA; }
+    return LA_OK;
+}
+
+static void* layer_plane(la_ctx* ctx, void* base, int l, int kv, int rows) {
+    size_t plane = (size_t)ctx->cfg.n_heads * rows * ctx->cfg.head_dim * ctx->esz;
+    return (char*)base + ((size_t)l * 2 + kv) * plane;
+}
+
+static int read_hdr(la_ctx* ctx, LaHdr* h) {
+    CK(cudaMemcpyAsync(h, ctx->d.hdr, sizeof(LaHdr), cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    return LA_OK;
+}
+
+static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const void* w2, const void* w3, int n_seg,
+                     int Nout_seg, int K, void* X, void* out, int ldo) {
+    memset(g, 0, sizeof(*g));
+    if (la_tc_make_map(&g->tmA, w1, Nout_seg, K, 128)) return LA_ECUDA;
+    if (la_tc_make_map(&g->tmA2, w2 ? w2 : w1, Nout_seg, K, 128)) return LA_ECUDA;
+    if (la_tc_make_map(&g->tmA3, w3 ? w3 : w1, Nout_seg, K, 128)) return LA_ECUDA;
+    if (la_tc_make_map(&g->tmB, X, ctx->Qcap, K, 16)) return LA_ECUDA;
+    g->mode = mode;
+    g->K = K;
+    g->Nout = Nout_seg * n_seg;
+    g->seg_tiles = n_seg > 1 ? Nout_seg / 128 : 0;
+    g->splits = la_tc_split_for(g->Nout / 128, K / 64);
+    const char* env = getenv("LA_SPLITK");   // tuning override: fixed split for every GEMM
+    if (env) g->splits = std::max(1, std::min(atoi(env), K / 64));
+    g->rows_cap = ctx->Qcap;
+    g->out = out;
+    g->ldo = ldo;
+    return LA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// forward passes
+// ---------------------------------------------------------------------------
+static int enqueue_forward(la_ctx* ctx, int sel) {
+    const la_model_cfg& c = ctx->cfg;
+    const LaDev& d = ctx->d;
+    cudaStream_t st = ctx->st;
+    const int rc = (sel == SEL_PREFILL) ? PREFILL_CHUNK : ctx->Qmax;
+    const int dm = c.d_model, HD = ctx->HD, F = c.d_ffn, H = c.n_heads, dh = c.head_dim;
+    la_launch_embed(d, st, c.dtype, ctx->emb, ctx->x, dm, sel, rc);
+    for (int l = 0; l < c.n_layers; ++l) {
+        la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->attn_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc);
+        if (ctx->tc) {
+            CK(la_launch_gemm_tc(d, st, ctx->g_qkv[l], ctx->work, sel));
+        } else {
+            char* q = (char*)ctx->qkv;
+            la_launch_gemm_ffma(d, st, c.dtype, GEMM_STORE, ctx->xn, dm, ctx->wq[l], nullptr, dm, HD, q, 3 * HD, sel, rc);
+            la_launch_gemm_ffma(d, st, c.dtype, GEMM_STORE, ctx->xn, dm, ctx->wk[l], nullptr, dm, HD, q + HD * ctx->esz,
+                                3 * HD, sel, rc);
+            la_launch_gemm_ffma(d, st, c.dtype, GEMM_STORE, ctx->xn, dm, ctx->wv[l], nullptr, dm, HD,
+                                q + 2 * HD * ctx->esz, 3 * HD, sel, rc);
+        }
+        void* kdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx)
+                                          : layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax);
+        void* vdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx)
+                                          : layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax);
+        int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ctx->Qmax;
+        la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
+                          stride, rc);
+        CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
+                               layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
+                               layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax), layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax),
+                               ctx->attn, H, sel, ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc));
+        if (ctx->tc) {
+            CK(la_launch_gemm_tc(d, st, ctx->g_o[l], ctx->work, sel));
+        } else {
+            la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->attn, HD, ctx->wo[l], nullptr, HD, dm, ctx->x, dm, sel, rc);
+        }
+        la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->mlp_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc);
+        if (ctx->tc) {
+            CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel));
+            CK(la_launch_gemm_tc(d, st, ctx->g_down[l], ctx->work, sel));
+        } else {
+            la_launch_gemm_ffma(d, st, c.dtype, GEMM_SWIGLU, ctx->xn, dm, ctx->wg[l], ctx->wu[l], dm, F, ctx->act, F, sel, rc);
+            la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->act, F, ctx->wd[l], nullptr, F, dm, ctx->x, dm, sel, rc);
+        }
+    }
+    CK(cudaGetLastError());
+    return LA_OK;
+}
+
+// final norm on the needed rows, LM head, argmax (and fp32 logits when kept)
+static int enqueue_head(la_ctx* ctx, int keep_logits) {
+    const la_model_cfg& c = ctx->cfg;
+    const LaDev& d = ctx->d;
+    cudaStream_t st = ctx->st;
+    const int rc = ctx->Qmax;
+    la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->fnorm, ctx->hn, c.d_model, c.rms_eps, SEL_NEED, 1, rc);
+    if (ctx->tc) {
+        TcGemm g = ctx->g_head;
+        g.logits = keep_logits ? ctx->logits : nullptr;
+        CK(la_launch_gemm_tc(d, st, g, ctx->work, SEL_NEED));
+        la_launch_argmax_reduce(d, st, ctx->work.part_v, ctx->work.part_i, c.vocab / 128, ctx->work.part_stride,
+                                SEL_NEED, rc);
+    } else {
+        la_launch_gemm_ffma(d, st, c.dtype, GEMM_LOGITS, ctx->hn, c.d_model, ctx->head, nullptr, c.d_model, c.vocab,
+                            ctx->logits, c.vocab, SEL_NEED, rc);
+        la_launch_argmax_rows(d, st, ctx->logits, c.vocab, SEL_NEED, rc);
+    }
+    CK(cudaGetLastError());
+    return LA_OK;
+}
+
+static int enqueue_publish_commit(la_ctx* ctx, int verdict_given) {
+    const la_model_cfg& c = ctx->cfg;
+    la_launch_publish(ctx->d, ctx->st, verdict_given);
+    la_launch_commit(ctx->d, ctx->st, ctx->cache, ctx->temp, c.n_layers * 2 * c.n_heads, c.n_heads,
+                     (int)(c.head_dim * ctx->esz), ctx->max_ctx, ctx->Qmax);
+    CK(cudaGetLastError());
+    return LA_OK;
+}
+
+static int enqueue_step(la_ctx* ctx) {
+    la_launch_pack(ctx->d, ctx->st);
+    int r = enqueue_forward(ctx, SEL_CALL);
+    if (r) return r;
+    r = enqueue_head(ctx, ctx->debug & 1);
+    if (r) return r;
+    return enqueue_publish_commit(ctx, 0);
+}
+
+static int get_graph(la_ctx* ctx, Graph** out) {
+    int key = (ctx->debug & 1);
+    auto it = ctx->graphs.find(key);
+    if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
+    Graph g;
+    CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
+    int r = enqueue_step(ctx);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
+    if (r) { if (graph) cudaGraphDestroy(graph); return r; }
+    CK(e);
+    g.g = graph;
+    CK(cudaGraphInstantiate(&g.x, graph, 0));
+    ctx->graphs[key] = g;
+    *out = &ctx->graphs[key];
+    return LA_OK;
+}
+
+static int check_err_word(la_ctx* ctx, const LaHdr& h) {
+    if (h.err) return h.err;
+    return LA_OK;
+}
+
+// Clears the device error word before a call.  A GEMM CTA that gave up on a
+// bounded wait may have left a split-K arrival counter short, so the counters
+// are zeroed too.
+static int clear_err(la_ctx* ctx) {
+    CK(cudaMemsetAsync(&ctx->d.hdr->err, 0, sizeof(int32_t), ctx->st));
+    if (ctx->work.counters) CK(cudaMemsetAsync(ctx->work.counters, 0, sizeof(int) * ctx->work.n_counters, ctx->st));
+    return LA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* la_strerror(int code) {
+    switch (code) {
+        case LA_OK: return "ok";
+        case LA_EINVAL: return "invalid argument";
+        case LA_ECAPACITY: return "capacity exceeded";
+        case LA_ESTATE: return "call out of order";
+        case LA_ECUDA: return "CUDA error";
+        case LA_EDEVICE: return "device check failed";
+        case LA_ETIMEOUT: return "device wait timed out";
+        case LA_ENOTSUP: return "not supported";
+        default: return "unknown error";
+    }
+}
+
+const char* la_last_cuda_error(la_ctx* ctx) { return ctx ? ctx->last_err.c_str() : ""; }
+
+void la_free(la_ctx* ctx) {
+    if (!ctx) return;
+    if (ctx->st) cudaStreamSynchronize(ctx->st);
+    for (auto& kv : ctx->graphs) {
+        if (kv.second.x) cudaGraphExecDestroy(kv.second.x);
+        if (kv.second.g) cudaGraphDestroy(kv.second.g);
+    }
+    for (void* p : ctx->allocs) cudaFree(p);
+    if (ctx->own_stream && ctx->st) cudaStreamDestroy(ctx->st);
+    delete ctx;
+}
+
+int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W, int max_N, int max_G, void* stream,
+            la_ctx** out) {
+    if (!cfg || !w || !out) return LA_EINVAL;
+    *out = nullptr;
+    const la_model_cfg& c = *cfg;
+    if (c.n_layers < 1 || c.n_heads < 1 || c.vocab < 2 || c.d_model != c.n_heads * c.head_dim ||
+        c.n_kv_heads != c.n_heads || !(c.rms_eps > 0.f) || !(c.rope_theta > 0.f))
+        return LA_EINVAL;
+    if (c.dtype != LA_F32 && c.dtype != LA_BF16) return LA_ENOTSUP;
+    if (c.head_dim != 32 && c.head_dim != 128) return LA_ENOTSUP;
+    if (c.dtype == LA_F32 && (c.d_model % 64 || c.d_ffn % 64 || c.vocab % 64)) return LA_ENOTSUP;
+    if (c.dtype == LA_BF16 && (c.d_model % 128 || c.d_ffn % 128 || c.vocab % 128)) return LA_ENOTSUP;
+    if (max_N < 3 || max_N > LA_MAX_R + 1 || max_W < 1 || max_W > LA_MAX_W || max_G < 0 || max_G > LA_MAX_G ||
+        max_ctx < 2)
+        return LA_EINVAL;
+    if (!w->tok_emb || !w->lm_head || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
+        !w->mlp_norm || !w->w_gate || !w->w_up || !w->w_down)
+        return LA_EINVAL;
+
+    la_ctx* ctx = new la_ctx();
+    ctx->cfg = c;
+    ctx->bf16 = (c.dtype == LA_BF16);
+    {
+        const char* gsel = getenv("LA_GEMM");    // "ffma": CUDA-core reference GEMMs for every dtype
+        ctx->tc = ctx->bf16 && !(gsel && strcmp(gsel, "ffma") == 0);
+    }
+    ctx->esz = ctx->bf16 ? 2 : 4;
+    ctx->max_ctx = max_ctx;
+    ctx->max_W = max_W;
+    ctx->max_N = max_N;
+    ctx->max_G = max_G;
+    ctx->HD = c.n_heads * c.head_dim;
+    ctx->Rmax = max_N - 1;
+    ctx->Smax = max_N - 1;
+    ctx->Gmax = std::max(1, max_G);
+    ctx->LMAX = std::max(1, max_W + max_N - 3);
+    ctx->PMAX = max_W + 2 * max_N;
+    int steadyQ = (max_W + max_G) * (max_N - 1);
+    int warmQ = 1 + (max_N - 1) * (max_W + max_N - 3);
+    ctx->Qmax = std::max(steadyQ, warmQ) + 16;
+    ctx->Qcap = ((std::max(ctx->Qmax, PREFILL_CHUNK) + 255) / 256) * 256;
+    ctx->rope_len = max_ctx + ctx->PMAX + 1;
+    ctx->out_cap = max_ctx + 32;
+
+    if (stream) ctx->st = (cudaStream_t)stream;
+    else {
+        if (cudaStreamCreateWithFlags(&ctx->st, cudaStreamNonBlocking) != cudaSuccess) { delete ctx; return LA_ECUDA; }
+        ctx->own_stream = true;
+    }
+    ctx->emb = w->tok_emb;
+    ctx->head = w->lm_head;
+    ctx->fnorm = w->final_norm;
+    for (int l = 0; l < c.n_layers; ++l) {
+        ctx->attn_norm.push_back(w->attn_norm[l]);
+        ctx->wq.push_back(w->wq[l]);
+        ctx->wk.push_back(w->wk[l]);
+        ctx->wv.push_back(w->wv[l]);
+        ctx->wo.push_back(w->wo[l]);
+        ctx->mlp_norm.push_back(w->mlp_norm[l]);
+        ctx->wg.push_back(w->w_gate[l]);
+        ctx->wu.push_back(w->w_up[l]);
+        ctx->wd.push_back(w->w_down[l]);
+    }
+
+    int r = LA_OK;
+    LaDev& d = ctx->d;
+    auto A = [&](void** p, size_t bytes) { if (r == LA_OK) r = dalloc(ctx, p, bytes); };
+    const size_t V = c.vocab;
+    A((void**)&d.hdr, sizeof(LaHdr));
+    A((void**)&d.window, sizeof(int32_t) * ctx->Rmax * ctx->LMAX);
+    A((void**)&d.pool_tok, sizeof(int32_t) * V * ctx->Gmax * ctx->Smax);
+    A((void**)&d.pool_cnt, sizeof(int32_t) * V);
+    A((void**)&d.prompt, sizeof(int32_t) * max_ctx);
+    A((void**)&d.row_tok, sizeof(int32_t) * ctx->Qcap);
+    A((void**)&d.row_pos, sizeof(int32_t) * ctx->Qcap);
+    A((void**)&d.row_meta, sizeof(int32_t) * ctx->Qcap);
+    A((void**)&d.row_path, sizeof(int32_t) * ctx->Qcap * ctx->PMAX);
+    A((void**)&d.need, sizeof(int32_t) * ctx->Qcap);
+    A((void**)&d.argmax, sizeof(int32_t) * ctx->Qcap);
+    A((void**)&d.out, sizeof(int32_t) * ctx->out_cap);
+    A((void**)&d.commit_rows, sizeof(int32_t) * 16);
+    A((void**)&ctx->argmax_in, sizeof(int32_t) * ctx->Qcap);
+    d.V = c.vocab;
+    d.Gmax = ctx->Gmax;
+    d.Smax = ctx->Smax;
+    d.Rmax = ctx->Rmax;
+    d.LMAX = ctx->LMAX;
+    d.PMAX = ctx->PMAX;
+    d.Qmax = ctx->Qmax;
+    d.Qcap = ctx->Qcap;
+    d.max_ctx = max_ctx;
+    d.out_cap = ctx->out_cap;
+
+    const size_t dm = c.d_model, HD = ctx->HD, F = c.d_ffn, Qc = ctx->Qcap, es = ctx->esz;
+    A((void**)&ctx->x, sizeof(float) * Qc * dm);
+    A(&ctx->xn, es * Qc * dm);
+    A(&ctx->qkv, es * Qc * 3 * HD);
+    A(&ctx->qbuf, es * Qc * HD);
+    A(&ctx->attn, es * Qc * HD);
+    A(&ctx->act, es * Qc * F);
+    A(&ctx->hn, es * Qc * dm);
+    A(&ctx->cache, es * (size_t)c.n_layers * 2 * HD * max_ctx);
+    A(&ctx->temp, es * (size_t)c.n_layers * 2 * HD * ctx->Qmax);
+    A((void**)&ctx->rcos, sizeof(float) * (size_t)ctx->rope_len * (c.head_dim / 2));
+    A((void**)&ctx->rsin, sizeof(float) * (size_t)ctx->rope_len * (c.head_dim / 2));
+    A((void**)&ctx->logits, sizeof(float) * Qc * V);
+    A((void**)&ctx->logits_in, sizeof(float) * (size_t)ctx->Qmax * V);
+    if (r) { la_free(ctx); return r; }
+    la_launch_rope_table(ctx->rcos, ctx->rsin, ctx->rope_len, c.head_dim, (double)c.rope_theta, ctx->st);
+
+    if (ctx->tc) {
+        // tensor-core GEMM descriptors and scratch
+        ctx->g_qkv.resize(c.n_layers);
+        ctx->g_o.resize(c.n_layers);
+        ctx->g_gu.resize(c.n_layers);
+        ctx->g_down.resize(c.n_layers);
+        for (int l = 0; l < c.n_layers && !r; ++l) {
+            r = make_gemm(ctx, &ctx->g_qkv[l], GEMM_STORE, ctx->wq[l], ctx->wk[l], ctx->wv[l], 3, (int)HD, (int)dm,
+                          ctx->xn, ctx->qkv, (int)(3 * HD));
+            if (!r) r = make_gemm(ctx, &ctx->g_o[l], GEMM_RESID, ctx->wo[l], nullptr, nullptr, 1, (int)dm, (int)HD,
+                                  ctx->attn, ctx->x, (int)dm);
+            if (!r) r = make_gemm(ctx, &ctx->g_gu[l], GEMM_SWIGLU, ctx->wg[l], ctx->wu[l], nullptr, 1, (int)F, (int)dm,
+                                  ctx->xn, ctx->act, (int)F);
+            if (!r) r = make_gemm(ctx, &ctx->g_down[l], GEMM_RESID, ctx->wd[l], nullptr, nullptr, 1, (int)dm, (int)F,
+                                  ctx->act, ctx->x, (int)dm);
+        }
+        if (!r) r = make_gemm(ctx, &ctx->g_head, GEMM_LOGITS, ctx->head, nullptr, nullptr, 1, (int)V, (int)dm, ctx->hn,
+                              nullptr, 0);
+        if (r) { la_free(ctx); return r; }
+        ctx->g_head.splits = 1;     // argmax partials need whole-K tiles
+        ctx->g_head.ld_logits = (int)V;
+        size_t wsf = 0;
+        int qchunks = ctx->Qcap / 256;
+        auto need_ws = [&](const TcGemm& g) {
+            if (g.splits > 1) wsf = std::max(wsf, (size_t)(g.Nout / 128) * qchunks * g.splits * 2 * 256 * 128);
+        };
+        need_ws(ctx->g_qkv[0]);
+        need_ws(ctx->g_o[0]);
+        need_ws(ctx->g_gu[0]);
+        need_ws(ctx->g_down[0]);
+        ctx->work.ws_floats = wsf;
+        A((void**)&ctx->work.ws, sizeof(float) * std::max<size_t>(wsf, 4));
+        ctx->work.n_counters = (int)((std::max(3 * HD, std::max(F, V)) / 128) * qchunks);
+        A((void**)&ctx->work.counters, sizeof(int) * ctx->work.n_counters);
+        ctx->work.part_stride = ctx->Qcap;
+        A((void**)&ctx->work.part_v, sizeof(float) * (V / 128) * ctx->Qcap);
+        A((void**)&ctx->work.part_i, sizeof(int) * (V / 128) * ctx->Qcap);
+        if (r) { la_free(ctx); return r; }
+    }
+    if (cudaStreamSynchronize(ctx->st) != cudaSuccess) {
+        ctx->last_err = cudaGetErrorString(cudaGetLastError());
+        la_free(ctx);
+        return LA_ECUDA;
+    }
+    *out = ctx;
+    return LA_OK;
+}
+
+int la_query(la_ctx* ctx, int32_t* s) {
+    if (!ctx || !s) return LA_EINVAL;
+    s[0] = ctx->Qmax; s[1] = ctx->max_W; s[2] = ctx->max_N; s[3] = ctx->max_G;
+    s[4] = ctx->max_ctx; s[5] = ctx->cfg.vocab; s[6] = ctx->LMAX; s[7] = ctx->PMAX;
+    return LA_OK;
+}
+
+int la_set_debug(la_ctx* ctx, int flags) {
+    if (!ctx) return LA_EINVAL;
+    ctx->debug = flags;
+    return LA_OK;
+}
+
+static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n) {
+    const la_model_cfg& c = ctx->cfg;
+    if (!prompt || n < 1) return LA_EINVAL;
+    if (n > ctx->max_ctx - 1) return LA_ECAPACITY;
+    for (int i = 0; i < n; ++i)
+        if (prompt[i] < 0 || prompt[i] >= c.vocab) return LA_EINVAL;
+    ctx->prefilled = false;
+    ctx->begun = false;
+    CK(cudaMemcpyAsync(ctx->d.prompt, prompt, sizeof(int32_t) * n, cudaMemcpyHostToDevice, ctx->st));
+    LaHdr h0;
+    memset(&h0, 0, sizeof(h0));
+    h0.prompt_len = n;
+    h0.max_out = 1;
+    CK(cudaMemcpyAsync(ctx->d.hdr, &h0, sizeof(h0), cudaMemcpyHostToDevice, ctx->st));
+    CK(cudaMemsetAsync(ctx->d.pool_cnt, 0, sizeof(int32_t) * c.vocab, ctx->st));
+    for (int c0 = 0; c0 < n; c0 += PREFILL_CHUNK) {
+        int m = std::min(PREFILL_CHUNK, n - c0);
+        la_launch_prefill_rows(ctx->d, ctx->st, c0, m);
+        int r = enqueue_forward(ctx, SEL_PREFILL);
+        if (r) return r;
+    }
+    la_launch_prefill_need(ctx->d, ctx->st, (n - 1) % PREFILL_CHUNK);
+    int r = enqueue_head(ctx, ctx->debug & 1);
+    if (r) return r;
+    la_launch_prefill_finish(ctx->d, ctx->st, n);
+    CK(cudaGetLastError());
+    ctx->prompt_len = n;
+    return LA_OK;
+}
+
+int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, int32_t* first_token) {
+    if (!ctx || !first_token) return LA_EINVAL;
+    if (s) return LA_ENOTSUP;
+    int r = do_prefill(ctx, prompt, n);
+    if (r) return r;
+    LaHdr h;
+    r = read_hdr(ctx, &h);
+    if (r) return r;
+    if (h.err) return h.err;
+    *first_token = h.x_t;
+    ctx->prefilled = true;
+    return LA_OK;
+}
+
+static int begin_request(la_ctx* ctx, int mode, int W, int N, int G, const la_sampling* s, int max_out) {
+    if (mode == MODE_LOOKAHEAD) {
+        if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
+        if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    }
+    ctx->mode = mode;
+    ctx->W = W; ctx->N = N; ctx->G = G;
+    ctx->sampling = s ? 1 : 0;
+    la_launch_begin(ctx->d, ctx->st, mode, W, N, G, ctx->sampling, s ? s->temperature : 1.f, s ? s->top_p : 1.f,
+                    s ? s->seed : 0, max_out);
+    CK(cudaGetLastError());
+    ctx->begun = true;
+    return LA_OK;
+}
+
+int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int32_t* out, int* n_out) {
+    if (!ctx || !out || !n_out) return LA_EINVAL;
+    if (s) return LA_ENOTSUP;
+    if (!ctx->prefilled) return LA_ESTATE;
+    if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
+    if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    int r;
+    if (!ctx->begun) {
+        r = begin_request(ctx, MODE_LOOKAHEAD, W, N, G, s, ctx->out_cap);
+        if (r) return r;
+    } else if (ctx->mode != MODE_LOOKAHEAD || W != ctx->W || N != ctx->N || G != ctx->G) {
+        return LA_ESTATE;
+    }
+    r = clear_err(ctx);
+    if (r) return r;
+    r = enqueue_step(ctx);
+    if (r) return r;
+    LaHdr h;
+    r = read_hdr(ctx, &h);
+    if (r) return r;
+    if (h.err) return h.err;
+    for (int i = 0; i < h.E; ++i) out[i] = h.emitted[i];
+    *n_out = h.E;
+    return LA_OK;
+}
+
+int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q, const int32_t* argmax,
+                   const float* logits, int32_t* out, int* n_out) {
+    if (!ctx || !out || !n_out || !argmax) return LA_EINVAL;
+    if (s || logits) return LA_ENOTSUP;
+    if (!ctx->prefilled) return LA_ESTATE;
+    if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
+    if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    int r;
+    if (!ctx->begun) {
+        r = begin_request(ctx, MODE_LOOKAHEAD, W, N, G, s, ctx->out_cap);
+        if (r) return r;
+    } else if (ctx->mode != MODE_LOOKAHEAD || W != ctx->W || N != ctx->N || G != ctx->G) {
+        return LA_ESTATE;
+    }
+    r = clear_err(ctx);
+    if (r) return r;
+    la_launch_pack(ctx->d, ctx->st);
+    LaHdr h;
+    r = read_hdr(ctx, &h);
+    if (r) return r;
+    if (h.err) return h.err;
+    if (h.Q != Q || Q > ctx->Qcap) return LA_ESTATE;
+    for (int q = 0; q < Q; ++q)
+        if (argmax[q] < 0 || argmax[q] >= ctx->cfg.vocab) return LA_EINVAL;
+    CK(cudaMemcpyAsync(ctx->argmax_in, argmax, sizeof(int32_t) * Q, cudaMemcpyHostToDevice, ctx->st));
+    la_launch_inject_map(ctx->d, ctx->st, ctx->argmax_in, nullptr, nullptr, ctx->cfg.vocab);
+    r = enqueue_publish_commit(ctx, 0);
+    if (r) return r;
+    r = read_hdr(ctx, &h);
+    if (r) return r;
+    if (h.err) return h.err;
+    for (int i = 0; i < h.E; ++i) out[i] = h.emitted[i];
+    *n_out = h.E;
+    return LA_OK;
+}
+
+static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int max_new, int W, int N, int G,
+                        const la_sampling* s, int32_t* out, int* n_out, la_stats* stats) {
+    if (!ctx || !out || !n_out || max_new < 1) return LA_EINVAL;
+    if (s) return LA_ENOTSUP;
+    if (mode == MODE_LOOKAHEAD) {
+        if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
+        if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    }
+    if (n + max_new > ctx->max_ctx) return LA_ECAPACITY;
+    cudaEvent_t e0, e1, e2;
+    CK(cudaEventCreate(&e0));
+    CK(cudaEventCreate(&e1));
+    CK(cudaEventCreate(&e2));
+    CK(cudaEventRecord(e0, ctx->st));
+    int r = do_prefill(ctx, prompt, n);
+    if (r) return r;
+    ctx->prefilled = true;
+    CK(cudaEventRecord(e1, ctx->st));
+    r = begin_request(ctx, mode, W, N, G, s, max_new);
+    if (r) return r;
+    r = clear_err(ctx);
+    if (r) return r;
+    Graph* g = nullptr;
+    r = get_graph(ctx, &g);
+    if (r) return r;
+    const int per_step_max = (mode == MODE_LOOKAHEAD) ? N : 1;
+    LaHdr h;
+    r = read_hdr(ctx, &h);
+    if (r) return r;
+    int guard = 0;
+    while (!h.done && !h.err) {
+        int remaining = max_new - h.n_out;
+        int launches = std::max(1, (remaining + per_step_max - 1) / per_step_max);
+        for (int i = 0; i < launches; ++i) CK(cudaGraphLaunch(g->x, ctx->st));
+        r = read_hdr(ctx, &h);
+        if (r) return r;
+        if (++guard > 4 * max_new + 16) return LA_EDEVICE;
+    }
+    CK(cudaEventRecord(e2, ctx->st));
+    if (h.err) return h.err;
+    CK(cudaMemcpyAsync(out, ctx->d.out, sizeof(int32_t) * max_new, cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    *n_out = max_new;
+    if (stats) {
+        float ms0 = 0, ms1 = 0;
+        cudaEventElapsedTime(&ms0, e0, e1);
+        cudaEventElapsedTime(&ms1, e1, e2);
+        memset(stats, 0, sizeof(*stats));
+        stats->steps = h.n_steps;
+        stats->tokens = max_new;
+        stats->prefill_ns = (int64_t)(ms0 * 1e6);
+        stats->decode_ns = (int64_t)(ms1 * 1e6);
+        for (int i = 0; i < 16; ++i) stats->emitted_hist[i] = h.hist[i];
+        stats->mean_candidates = h.n_steady ? (double)h.sum_Ct / h.n_steady : 0.0;
+        stats->mean_rows = h.n_steps ? (double)h.sum_Q / h.n_steps : 0.0;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaEventDestroy(e2);
+    return LA_OK;
+}
+
+int la_generate(la_ctx* ctx, const int32_t* prompt, int n, int max_new, int W, int N, int G, const la_sampling* s,
+                int32_t* out, int* n_out, la_stats* stats) {
+    return run_generate(ctx, MODE_LOOKAHEAD, prompt, n, max_new, W, N, G, s, out, n_out, stats);
+}
+
+int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new, const la_sampling* s, int32_t* out,
+                   int* n_out, la_stats* stats) {
+    return run_generate(ctx, MODE_AR, prompt, n, max_new, 1, 3, 0, s, out, n_out, stats);
+}
+
+int la_debug_logits(la_ctx* ctx, float* logits, int32_t* rows, int cap_rows, int* n_rows) {
+    if (!ctx || !n_rows) return LA_EINVAL;
+    if (!(ctx->debug & 1)) return LA_ESTATE;
+    LaHdr h;
+    int r = read_hdr(ctx, &h);
+    if (r) return r;
+    int n = h.n_need;
+    *n_rows = n;
+    if (n > cap_rows) return LA_ECAPACITY;
+    if (logits) CK(cudaMemcpyAsync(logits, ctx->logits, sizeof(float) * n * ctx->cfg.vocab, cudaMemcpyDeviceToHost, ctx->st));
+    if (rows) CK(cudaMemcpyAsync(rows, ctx->d.need, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    return LA_OK;
+}
+
+int la_debug_state(la_ctx* ctx, int32_t* hdr, int32_t* levels, int32_t* level_len, int32_t* row_tok, int32_t* row_pos,
+                   int32_t* row_meta) {
+    if (!ctx) return LA_EINVAL;
+    LaHdr h;
+    int r = read_hdr(ctx, &h);
+    if (r) return r;
+    if (hdr) {
+        int32_t v[16] = {h.K, h.x_t, h.W, h.N, h.G, h.n_levels, h.step, h.Q, h.C_t, h.a, h.winner, h.n_out,
+                         h.err, h.steady, h.n_need, h.n_deep};
+        memcpy(hdr, v, sizeof(v));
+    }
+    if (levels) CK(cudaMemcpyAsync(levels, ctx->d.window, sizeof(int32_t) * ctx->Rmax * ctx->LMAX, cudaMemcpyDeviceToHost, ctx->st));
+    if (level_len)
+        for (int i = 0; i < ctx->Rmax; ++i) level_len[i] = h.level_len[i];
+    if (row_tok) CK(cudaMemcpyAsync(row_tok, ctx->d.row_tok, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
+    if (row_pos) CK(cudaMemcpyAsync(row_pos, ctx->d.row_pos, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
+    if (row_meta) CK(cudaMemcpyAsync(row_meta, ctx->d.row_meta, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    return LA_OK;
+}
+
+int la_debug_pool(la_ctx* ctx, int key, int32_t* suffixes, int* count) {
+    if (!ctx || !count || key < 0 || key >= ctx->cfg.vocab) return LA_EINVAL;
+    int32_t cnt = 0;
+    CK(cudaMemcpyAsync(&cnt, ctx->d.pool_cnt + key, sizeof(int32_t), cudaMemcpyDeviceToHost, ctx->st));
+    if (suffixes)
+        CK(cudaMemcpyAsync(suffixes, ctx->d.pool_tok + (size_t)key * ctx->Gmax * ctx->Smax,
+                           sizeof(int32_t) * ctx->Gmax * ctx->Smax, cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    *count = cnt;
+    return LA_OK;
+}
+
+}  // extern "C"

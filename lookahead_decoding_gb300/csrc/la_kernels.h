@@ -1,0 +1,69 @@
+// Host-side launchers of the liblookahead kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include <stdint.h>
+
+struct LaDev;
+
+// epilogues of the GEMMs
+#define GEMM_STORE 0   // out[q][n] = acc                       (element type of the model)
+#define GEMM_RESID 1   // out[q][n] += acc                      (fp32 residual stream)
+#define GEMM_SWIGLU 2  // out[q][n] = silu(acc_gate) * acc_up   (element type of the model)
+#define GEMM_LOGITS 3  // out[q][n] = acc (fp32); tensor-core variant adds argmax partials
+
+// row-count selectors read from the device header
+#define SEL_CALL 0     // rows of the packed call (Q)
+#define SEL_PREFILL 1  // rows of the current prefill chunk
+#define SEL_NEED 2     // rows whose logits are read
+
+void la_launch_begin(const LaDev& d, cudaStream_t st, int mode, int W, int N, int G, int sampling,
+                     float temperature, float top_p, uint64_t seed, int max_out);
+void la_launch_pack(const LaDev& d, cudaStream_t st);
+void la_launch_publish(const LaDev& d, cudaStream_t st, int verdict_given);
+void la_launch_commit(const LaDev& d, cudaStream_t st, void* cache, void* temp, int planes, int n_heads,
+                      int head_bytes, int max_ctx, int Qmax);
+void la_launch_inject_map(const LaDev& d, cudaStream_t st, const int32_t* argmax_rows, const float* logits_rows,
+                          float* logits_need, int V);
+void la_launch_prefill_rows(const LaDev& d, cudaStream_t st, int c0, int n);
+void la_launch_prefill_need(const LaDev& d, cudaStream_t st, int last_local);
+void la_launch_prefill_finish(const LaDev& d, cudaStream_t st, int P);
+
+void la_launch_rope_table(float* rcos, float* rsin, int n_pos, int dh, double theta, cudaStream_t st);
+void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb, float* x, int dm, int sel, int rows_cap);
+void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, const float* x, const void* g, void* y, int dm,
+                       float eps, int sel, int gather, int rows_cap);
+void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
+                       void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap);
+cudaError_t la_launch_attention(const LaDev& d, cudaStream_t st, int dtype, int dh, const void* qbuf, const void* kc,
+                                const void* vc, const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
+                                int max_ctx, int Qmax, int rows_cap);
+void la_launch_gemm_ffma(const LaDev& d, cudaStream_t st, int dtype, int mode, const void* X, int ldx, const void* Wm,
+                         const void* W2, int K, int Nout, void* out, int ldo, int sel, int rows_cap);
+void la_launch_argmax_rows(const LaDev& d, cudaStream_t st, const float* logits, int V, int sel, int rows_cap);
+void la_launch_argmax_reduce(const LaDev& d, cudaStream_t st, const float* pv, const int* pi, int n_tiles, int stride,
+                             int sel, int rows_cap);
+
+// tensor-core (tcgen05) bf16 GEMM: Y[q][n] = sum_k X[q][k] W[n][k]
+struct TcGemm {
+    CUtensorMap tmA;      // weights [Nout][K], box 64 x 128, 128B swizzle
+    CUtensorMap tmA2;     // second weight matrix (SwiGLU up, or segment 1), else a copy of tmA
+    CUtensorMap tmA3;     // segment 2 (QKV), else a copy of tmA
+    CUtensorMap tmB;      // activations [rows_alloc][K], box 64 x 16, 128B swizzle
+    int mode, K, Nout, splits, rows_cap;
+    int seg_tiles;        // >0: tiles per weight segment (output columns concatenate the segments)
+    void* out; int ldo;
+    float* logits; int ld_logits;   // GEMM_LOGITS: optional fp32 logits
+};
+struct TcWork {
+    float* ws;            // split-K partials
+    size_t ws_floats;
+    int* counters;        // per (tile, q-chunk) arrival counters, zero-initialised
+    int n_counters;
+    float* part_v;        // argmax partials [n_tiles][part_stride]
+    int* part_i;
+    int part_stride;
+};
+int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
+cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
+int la_tc_split_for(int n_tiles, int k_tiles);

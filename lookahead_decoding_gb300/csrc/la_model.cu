@@ -1,0 +1,483 @@
+// Model kernels of the packed target call: embedding, RMSNorm, RoPE + K/V
+// write, masked attention, the CUDA-core GEMM (fp32 model and reference
+// path), and the LM-head argmax reductions.
+//
+// Row invariance: every kernel computes a row's result with an arithmetic
+// order that depends only on that row's inputs and logical position, never
+// on how many rows share the call or where the row sits in the batch.  This
+// makes a row packed with others bit-identical to the same token decoded
+// alone, which is what lets the lookahead output equal autoregressive
+// greedy decoding exactly (M7.3 §0x02A: the method's fixed point is the
+// autoregressive result; the equality needs the same selector on the same
+// logits).
+#include "la_common.cuh"
+#include "la_kernels.h"
+
+#include <math.h>
+
+// ---------------------------------------------------------------------------
+// RoPE table: cos/sin(pos * theta^(-2i/dh)) evaluated in fp64, stored fp32
+// ---------------------------------------------------------------------------
+__global__ void k_rope_table(float* rcos, float* rsin, int n_pos, int half, double theta, int dh) {
+    int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_pos * half) return;
+    int p = idx / half, i = idx % half;
+    double inv = pow(theta, -2.0 * (double)i / (double)dh);
+    double ang = (double)p * inv;
+    rcos[idx] = (float)cos(ang);
+    rsin[idx] = (float)sin(ang);
+}
+
+__device__ __forceinline__ int rows_of(const LaHdr* h, int sel) {
+    // sel: 0 = packed rows of the call, 1 = prefill chunk rows, 2 = needed rows
+    return sel == 0 ? h->Q : (sel == 1 ? h->prefill_rows : h->n_need);
+}
+__device__ __forceinline__ bool skip_call(const LaHdr* h, int sel) {
+    return h->err != 0 || (sel != 1 && h->done != 0);
+}
+
+// ---------------------------------------------------------------------------
+// embedding: x[q][:] = E[tok[q]]  (fp32 residual stream)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    int q = blockIdx.x;
+    if (q >= rows_of(h, sel)) return;
+    int tok = d.row_tok[q];
+    if (tok < 0 || tok >= d.V) { la_set_err(d.hdr, LA_EDEVICE); return; }
+    const T* e = emb + (size_t)tok * dm;
+    for (int i = threadIdx.x; i < dm; i += blockDim.x) x[(size_t)q * dm + i] = to_f(e[i]);
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, one block per row, fixed
+// reduction order.  gather=1 reads row need[i] and writes row i.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void k_rmsnorm(LaDev d, const float* x, const T* g, T* y, int dm, float eps, int sel, int gather) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    int row = blockIdx.x;
+    if (row >= rows_of(h, sel)) return;
+    int src = gather ? d.need[row] : row;
+    const float* xr = x + (size_t)src * dm;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < dm; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    __shared__ float red[32];
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = ss;
+    __syncthreads();
+    if (w == 0) {
+        float v = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (l == 0) red[0] = v;
+    }
+    __syncthreads();
+    float r = 1.0f / sqrtf(red[0] / (float)dm + eps);
+    for (int i = threadIdx.x; i < dm; i += blockDim.x)
+        y[(size_t)row * dm + i] = from_f<T>(xr[i] * r * to_f(g[i]));
+}
+
+// ---------------------------------------------------------------------------
+// RoPE (rotate-half) on q and k at each row's logical position; q goes to
+// qbuf [H][Qcap][dh]; k, v go to kdst/vdst [H][stride][dh] at the row's
+// packed index (temporary rows of the call) or, in a prefill, at its
+// position in the cache.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float* rsin, T* qbuf, T* kdst, T* vdst,
+                          int H, int dh, int sel, int Qcap, int stride) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    int q = blockIdx.x;
+    if (q >= rows_of(h, sel)) return;
+    int hh = blockIdx.y, i = threadIdx.x, half = dh >> 1;
+    if (i >= half) return;
+    int pos = d.row_pos[q];
+    float c = rcos[(size_t)pos * half + i], s = rsin[(size_t)pos * half + i];
+    const int HD = H * dh;
+    const T* base = qkv + (size_t)q * 3 * HD + hh * dh;
+    float qa = to_f(base[i]), qb = to_f(base[i + half]);
+    float ka = to_f(base[HD + i]), kb = to_f(base[HD + i + half]);
+    T* qo = qbuf + ((size_t)hh * Qcap + q) * dh;
+    qo[i] = from_f<T>(qa * c - qb * s);
+    qo[i + half] = from_f<T>(qb * c + qa * s);
+    int slot = (sel == 1) ? pos : q;
+    T* ko = kdst + ((size_t)hh * stride + slot) * dh;
+    T* vo = vdst + ((size_t)hh * stride + slot) * dh;
+    ko[i] = from_f<T>(ka * c - kb * s);
+    ko[i + half] = from_f<T>(kb * c + ka * s);
+    vo[i] = base[2 * HD + i];
+    vo[i + half] = base[2 * HD + i + half];
+}
+
+// ---------------------------------------------------------------------------
+// Masked attention (CUDA cores).  One CTA per (head, block of rows).  Every
+// row sees one key per logical position 0..pos: positions below the
+// committed length K come from the cache, positions K..pos from the call's
+// temporary rows on the row's own path (row_path), which encodes the
+// branch visibility of M7.3 §0x04A without a mask tensor.  Keys are taken in
+// chunks of 32 aligned to absolute positions; chunks below every row's
+// frontier are staged once in shared memory for all rows of the CTA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int DPL, int RPW>
+struct AttnState {
+    float m[RPW], l[RPW], o[RPW][DPL];
+};
+
+// One online-softmax step over a chunk of 32 keys (lane j holds key j's
+// score).  Both the shared-chunk and the gathered-key paths call this one
+// function, and it uses only explicitly rounded operations, so a row's
+// result does not depend on which path delivered its keys.
+template <int DPL, typename VGet>
+__device__ __forceinline__ void softmax_chunk(float s, bool valid, float& m, float& l, float (&o)[DPL], VGet vget) {
+    const float cmax = warp_max(valid ? s : -INFINITY);
+    const float mn = fmaxf(m, cmax);
+    const float p = valid ? expf(__fsub_rn(s, mn)) : 0.f;
+    const float corr = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
+    l = fmaf(l, corr, warp_sum(p));
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = __fmul_rn(o[e], corr);
+    for (int j = 0; j < 32; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+        if (pj != 0.f) {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[e] = fmaf(pj, vget(j, e), o[e]);
+        }
+    }
+    m = mn;
+}
+
+template <typename T, int DH, int RPW>
+__global__ void __launch_bounds__(256) k_attention(LaDev d, const T* qbuf, const T* kc, const T* vc, const T* kt,
+                                                   const T* vt, T* out, int H, int sel, int Qcap, int max_ctx,
+                                                   int Qmax, float scale) {
+    constexpr int DPL = DH / 32;
+    constexpr int NW = 8;
+    constexpr int RPC = NW * RPW;
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    const int rows = rows_of(h, sel);
+    const int hh = blockIdx.x;
+    const int r0 = blockIdx.y * RPC;
+    if (r0 >= rows) return;
+    const int prefill = (sel == 1);
+    const int K = prefill ? 0 : h->K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    extern __shared__ float sm[];
+    float* q_s = sm;                       // [RPC][DH]
+    float* kt_s = q_s + RPC * DH;          // [DH][33]
+    float* v_s = kt_s + DH * 33;           // [32][DH]
+
+    const T* kc_h = kc + (size_t)hh * max_ctx * DH;
+    const T* vc_h = vc + (size_t)hh * max_ctx * DH;
+    const T* kt_h = kt + (size_t)hh * Qmax * DH;
+    const T* vt_h = vt + (size_t)hh * Qmax * DH;
+
+    int minpos = 0x7fffffff, maxpos = -1;
+    for (int r = r0; r < min(rows, r0 + RPC); ++r) {
+        int p = d.row_pos[r];
+        minpos = min(minpos, p);
+        maxpos = max(maxpos, p);
+    }
+    // queries into shared memory (fp32)
+    for (int i = threadIdx.x; i < RPC * DH; i += blockDim.x) {
+        int r = r0 + i / DH;
+        q_s[i] = (r < rows) ? to_f(qbuf[((size_t)hh * Qcap + r) * DH + (i % DH)]) : 0.f;
+    }
+    // chunks below `shared_end` hold committed keys visible to every row here
+    const int shared_end = prefill ? (minpos + 1) : K;
+    const int n_shared = shared_end / 32;
+
+    AttnState<DPL, RPW> st;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        st.m[i] = -INFINITY; st.l[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) st.o[i][j] = 0.f;
+    }
+    int myrow[RPW], mypos[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        int r = r0 + warp + i * NW;
+        myrow[i] = r;
+        mypos[i] = (r < rows) ? d.row_pos[r] : -1;
+    }
+
+    for (int c = 0; c < n_shared; ++c) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < 32 * DH; i += blockDim.x) {
+            int j = i / DH, dd = i % DH;
+            size_t src = (size_t)(c * 32 + j) * DH + dd;
+            kt_s[dd * 33 + j] = to_f(kc_h[src]);
+            v_s[j * DH + dd] = to_f(vc_h[src]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            if (mypos[i] < 0) continue;
+            const float* qv = q_s + (myrow[i] - r0) * DH;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int dd = 0; dd < DH; ++dd) acc = fmaf(qv[dd], kt_s[dd * 33 + lane], acc);
+            softmax_chunk<DPL>(__fmul_rn(acc, scale), true, st.m[i], st.l[i], st.o[i],
+                               [&](int j, int e) { return v_s[j * DH + lane * DPL + e]; });
+        }
+    }
+    // remaining chunks: keys gathered per row (committed or the row's own path)
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        if (mypos[i] < 0) continue;
+        const int r = myrow[i], pos = mypos[i];
+        const int Kr = prefill ? pos + 1 : K;       // keys below Kr are in the cache
+        const int* path = d.row_path + (size_t)r * d.PMAX;
+        const float* qv = q_s + (r - r0) * DH;
+        for (int c = n_shared; c * 32 <= pos; ++c) {
+            int p = c * 32 + lane;
+            bool valid = p <= pos;
+            const T* kp = nullptr;
+            const T* vp = nullptr;
+            if (valid) {
+                if (p < Kr) { kp = kc_h + (size_t)p * DH; vp = vc_h + (size_t)p * DH; }
+                else {
+                    int src = path[p - K];
+                    kp = kt_h + (size_t)src * DH; vp = vt_h + (size_t)src * DH;
+                }
+            }
+            float s = -INFINITY;
+            if (valid) {
+                float acc = 0.f;
+#pragma unroll 8
+                for (int dd = 0; dd < DH; ++dd) acc = fmaf(qv[dd], to_f(kp[dd]), acc);
+                s = __fmul_rn(acc, scale);
+            }
+            softmax_chunk<DPL>(s, valid, st.m[i], st.l[i], st.o[i], [&](int j, int e) {
+                const T* vj = (const T*)__shfl_sync(0xffffffffu, (unsigned long long)vp, j);
+                return to_f(vj[lane * DPL + e]);
+            });
+        }
+        float inv = 1.0f / st.l[i];
+        T* op = out + (size_t)r * H * DH + hh * DH + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) op[e] = from_f<T>(__fmul_rn(st.o[i][e], inv));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core GEMM: Y[q][n] = sum_k X[q][k] W[n][k], k ascending per output
+// (one FMA chain), tile 64 n x 32 q, fp32 accumulation.  Used for the fp32
+// model and as the reference kernel of the tensor-core GEMM.
+// ---------------------------------------------------------------------------
+template <typename T, int MODE>
+__global__ void __launch_bounds__(256) k_gemm_ffma(LaDev d, const T* X, int ldx, const T* Wm, const T* W2, int K,
+                                                   int Nout, void* out, int ldo, int sel) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    const int rows = rows_of(h, sel);
+    const int n0 = blockIdx.x * 64, q0 = blockIdx.y * 32;
+    if (q0 >= rows) return;
+    __shared__ float Ws[32][65];
+    __shared__ float W2s[MODE == GEMM_SWIGLU ? 32 : 1][65];
+    __shared__ float Xs[32][33];
+    const int tid = threadIdx.x, nl = tid & 63, qg = tid >> 6;
+    float acc[8], acc2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { acc[i] = 0.f; acc2[i] = 0.f; }
+    for (int k0 = 0; k0 < K; k0 += 32) {
+        for (int i = tid; i < 64 * 32; i += 256) {
+            int n = i >> 5, k = i & 31;
+            Ws[k][n] = to_f(Wm[(size_t)(n0 + n) * K + k0 + k]);
+            if (MODE == GEMM_SWIGLU) W2s[k][n] = to_f(W2[(size_t)(n0 + n) * K + k0 + k]);
+        }
+        for (int i = tid; i < 32 * 32; i += 256) {
+            int q = i >> 5, k = i & 31;
+            Xs[q][k] = (q0 + q < rows) ? to_f(X[(size_t)(q0 + q) * ldx + k0 + k]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < 32; ++kk) {
+            float w = Ws[kk][nl];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, Xs[qg * 8 + i][kk], acc[i]);
+            if (MODE == GEMM_SWIGLU) {
+                float w2 = W2s[kk][nl];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc2[i] = fmaf(w2, Xs[qg * 8 + i][kk], acc2[i]);
+            }
+        }
+        __syncthreads();
+    }
+    const int n = n0 + nl;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int q = q0 + qg * 8 + i;
+        if (q >= rows) continue;
+        size_t o = (size_t)q * ldo + n;
+        if (MODE == GEMM_STORE) ((T*)out)[o] = from_f<T>(acc[i]);
+        else if (MODE == GEMM_RESID) ((float*)out)[o] += acc[i];
+        else if (MODE == GEMM_SWIGLU) {
+            float g = acc[i];
+            ((T*)out)[o] = from_f<T>(g / (1.0f + expf(-g)) * acc2[i]);
+        } else if (MODE == GEMM_LOGITS) ((float*)out)[o] = acc[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// argmax over fp32 logit rows, lowest id among maxima
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
+    if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
+}
+__global__ void k_argmax_rows(LaDev d, const float* logits, int V, int sel) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    int row = blockIdx.x;
+    if (row >= rows_of(h, sel)) return;
+    const float* x = logits + (size_t)row * V;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) better(bv, bi, x[v], v);
+    for (int o = 16; o > 0; o >>= 1) {
+        float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        better(bv, bi, v2, i2);
+    }
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) { sv[w] = bv; si[w] = bi; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int k = 1; k < (int)(blockDim.x >> 5); ++k) better(bv, bi, sv[k], si[k]);
+        d.argmax[row] = bi;
+    }
+}
+
+// partial (value, index) per (vocab tile, row) -> argmax per row
+__global__ void k_argmax_reduce(LaDev d, const float* pv, const int* pi, int n_tiles, int stride, int sel) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    int row = blockIdx.x;
+    if (row >= rows_of(h, sel)) return;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) better(bv, bi, pv[(size_t)t * stride + row], pi[(size_t)t * stride + row]);
+    for (int o = 16; o > 0; o >>= 1) {
+        float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        better(bv, bi, v2, i2);
+    }
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) { sv[w] = bv; si[w] = bi; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int k = 1; k < (int)(blockDim.x >> 5); ++k) better(bv, bi, sv[k], si[k]);
+        d.argmax[row] = bi;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+void la_launch_rope_table(float* rcos, float* rsin, int n_pos, int dh, double theta, cudaStream_t st) {
+    int half = dh / 2, n = n_pos * half;
+    k_rope_table<<<(n + 255) / 256, 256, 0, st>>>(rcos, rsin, n_pos, half, theta, dh);
+}
+
+template <typename T>
+void la_launch_embed_t(const LaDev& d, cudaStream_t st, const void* emb, float* x, int dm, int sel, int rows_cap) {
+    k_embed<T><<<rows_cap, 128, 0, st>>>(d, (const T*)emb, x, dm, sel);
+}
+void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb, float* x, int dm, int sel, int rows_cap) {
+    if (dtype == LA_F32) la_launch_embed_t<float>(d, st, emb, x, dm, sel, rows_cap);
+    else la_launch_embed_t<__nv_bfloat16>(d, st, emb, x, dm, sel, rows_cap);
+}
+
+void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, const float* x, const void* g, void* y, int dm,
+                       float eps, int sel, int gather, int rows_cap) {
+    if (dtype == LA_F32) k_rmsnorm<float><<<rows_cap, 256, 0, st>>>(d, x, (const float*)g, (float*)y, dm, eps, sel, gather);
+    else k_rmsnorm<__nv_bfloat16><<<rows_cap, 256, 0, st>>>(d, x, (const __nv_bfloat16*)g, (__nv_bfloat16*)y, dm, eps, sel, gather);
+}
+
+void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
+                       void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap) {
+    dim3 g(rows_cap, H);
+    if (dtype == LA_F32)
+        k_rope_kv<float><<<g, dh / 2, 0, st>>>(d, (const float*)qkv, rcos, rsin, (float*)qbuf, (float*)kdst, (float*)vdst,
+                                               H, dh, sel, Qcap, stride);
+    else
+        k_rope_kv<__nv_bfloat16><<<g, dh / 2, 0, st>>>(d, (const __nv_bfloat16*)qkv, rcos, rsin, (__nv_bfloat16*)qbuf,
+                                                       (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride);
+}
+
+template <typename T, int DH, int RPW>
+static cudaError_t attn_t(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
+                          const void* kt, const void* vt, void* out, int H, int sel, int Qcap, int max_ctx, int Qmax,
+                          int rows_cap) {
+    constexpr int RPC = 8 * RPW;
+    size_t smem = (size_t)(RPC * DH + DH * 33 + 32 * DH) * sizeof(float);
+    auto kern = k_attention<T, DH, RPW>;
+    static bool attr_done = false;     // set once, before any stream capture
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    dim3 g(H, (rows_cap + RPC - 1) / RPC);
+    kern<<<g, 256, smem, st>>>(d, (const T*)qbuf, (const T*)kc, (const T*)vc, (const T*)kt, (const T*)vt, (T*)out, H,
+                                sel, Qcap, max_ctx, Qmax, 1.0f / sqrtf((float)DH));
+    return cudaGetLastError();
+}
+
+cudaError_t la_launch_attention(const LaDev& d, cudaStream_t st, int dtype, int dh, const void* qbuf, const void* kc,
+                                const void* vc, const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
+                                int max_ctx, int Qmax, int rows_cap) {
+    if (dtype == LA_F32) {
+        if (dh == 32) return attn_t<float, 32, 4>(d, st, qbuf, kc, vc, kt, vt, out, H, sel, Qcap, max_ctx, Qmax, rows_cap);
+        if (dh == 128) return attn_t<float, 128, 4>(d, st, qbuf, kc, vc, kt, vt, out, H, sel, Qcap, max_ctx, Qmax, rows_cap);
+    } else {
+        if (dh == 32) return attn_t<__nv_bfloat16, 32, 4>(d, st, qbuf, kc, vc, kt, vt, out, H, sel, Qcap, max_ctx, Qmax, rows_cap);
+        if (dh == 128) return attn_t<__nv_bfloat16, 128, 4>(d, st, qbuf, kc, vc, kt, vt, out, H, sel, Qcap, max_ctx, Qmax, rows_cap);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+static void gemm_ffma_t(const LaDev& d, cudaStream_t st, int mode, const void* X, int ldx, const void* Wm, const void* W2,
+                        int K, int Nout, void* out, int ldo, int sel, int rows_cap) {
+    dim3 g(Nout / 64, (rows_cap + 31) / 32);
+    switch (mode) {
+        case GEMM_STORE: k_gemm_ffma<T, GEMM_STORE><<<g, 256, 0, st>>>(d, (const T*)X, ldx, (const T*)Wm, nullptr, K, Nout, out, ldo, sel); break;
+        case GEMM_RESID: k_gemm_ffma<T, GEMM_RESID><<<g, 256, 0, st>>>(d, (const T*)X, ldx, (const T*)Wm, nullptr, K, Nout, out, ldo, sel); break;
+        case GEMM_SWIGLU: k_gemm_ffma<T, GEMM_SWIGLU><<<g, 256, 0, st>>>(d, (const T*)X, ldx, (const T*)Wm, (const T*)W2, K, Nout, out, ldo, sel); break;
+        case GEMM_LOGITS: k_gemm_ffma<T, GEMM_LOGITS><<<g, 256, 0, st>>>(d, (const T*)X, ldx, (const T*)Wm, nullptr, K, Nout, out, ldo, sel); break;
+    }
+}
+void la_launch_gemm_ffma(const LaDev& d, cudaStream_t st, int dtype, int mode, const void* X, int ldx, const void* Wm,
+                         const void* W2, int K, int Nout, void* out, int ldo, int sel, int rows_cap) {
+    if (dtype == LA_F32) gemm_ffma_t<float>(d, st, mode, X, ldx, Wm, W2, K, Nout, out, ldo, sel, rows_cap);
+    else gemm_ffma_t<__nv_bfloat16>(d, st, mode, X, ldx, Wm, W2, K, Nout, out, ldo, sel, rows_cap);
+}
+
+void la_launch_argmax_rows(const LaDev& d, cudaStream_t st, const float* logits, int V, int sel, int rows_cap) {
+    k_argmax_rows<<<rows_cap, 256, 0, st>>>(d, logits, V, sel);
+}
+void la_launch_argmax_reduce(const LaDev& d, cudaStream_t st, const float* pv, const int* pi, int n_tiles, int stride,
+                             int sel, int rows_cap) {
+    k_argmax_reduce<<<rows_cap, 256, 0, st>>>(d, pv, pi, n_tiles, stride, sel);
+}
