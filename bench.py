@@ -136,6 +136,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ar-steps", type=int, default=1)
+    ap.add_argument("--max-new", type=int, default=MAX_NEW, help="new tokens per request (profiling runs)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -186,7 +187,7 @@ def main():
             torch.distributed.barrier()
 
     for _ in range(args.warmup):
-        L.la_generate(ctx.ctx, prompt, MAX_NEW, W_, N_, G_)
+        L.la_generate(ctx.ctx, prompt, args.max_new, W_, N_, G_)
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
     barrier()
@@ -195,7 +196,7 @@ def main():
     outs = []
     for _ in range(args.steps):
         st = L.la_stats()
-        outs.append(L.la_generate(ctx.ctx, prompt, MAX_NEW, W_, N_, G_, stats=st))
+        outs.append(L.la_generate(ctx.ctx, prompt, args.max_new, W_, N_, G_, stats=st))
         stats.append(st)
     barrier()
     wall = time.perf_counter() - t0
@@ -220,10 +221,10 @@ def main():
     ar_stats = []
     for _ in range(args.ar_steps):
         st = L.la_stats()
-        ar = L.la_generate_ar(ctx.ctx, prompt, MAX_NEW, stats=st)
+        ar = L.la_generate_ar(ctx.ctx, prompt, args.max_new, stats=st)
         ar_stats.append(st)
-    ar_tps = sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)
-    same = all(o == ar for o in outs)
+    ar_tps = (sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)) if ar_stats else None
+    same = all(o == ar for o in outs) if ar_stats else None
 
     # kernels of ours launched in the timed region: per request the prefill
     # (2 chunks x (rows + embed + 8 per layer) + need + head 3 + finish), begin,
@@ -233,7 +234,7 @@ def main():
     per_request = chunks * (2 + 8 * cfg.n_layers) + 1 + 3 + 1 + 1
     launches = args.steps * per_request + calls * per_call
     peaks, src = measured_peaks()
-    mean_K = PROMPT_LEN + MAX_NEW / 2.0
+    mean_K = PROMPT_LEN + args.max_new / 2.0
     mean_Q = statistics.mean(s.mean_rows for s in stats)
     bytes_call = algorithmic_bytes_per_call(cfg, mean_K, mean_Q)
     achieved = bytes_call / (call_ms * 1e-3) / 1e9
@@ -257,10 +258,10 @@ def main():
         "prefill_ms": statistics.mean(s.prefill_ns for s in stats) * 1e-6,
         "mean_rows_per_call": mean_Q,
         "ar_tokens_per_s": ar_tps,
-        "speedup_vs_ar": tps / ar_tps if world == 1 else None,
+        "speedup_vs_ar": tps / ar_tps if (world == 1 and ar_tps) else None,
         "lookahead_equals_ar": same,
-        "e2e": {"value": (MAX_NEW * args.steps * world) / wall, "unit": "tokens/s",
-                "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": MAX_NEW * 4},
+        "e2e": {"value": (args.max_new * args.steps * world) / wall, "unit": "tokens/s",
+                "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": args.max_new * 4},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "kernel": "whole packed call (all kernels of one step)",
                      "algorithmic_bytes_per_call": bytes_call, "peak_source": src},

@@ -116,11 +116,16 @@ typedef struct {
  *   max_W, max_N, max_G : largest lookahead knobs any later call may use
  *                   (max_N >= 3, max_W >= 1, max_G >= 0); they size the
  *                   row buffers: Q <= (max_W + max_G) * (max_N - 1) + max_N.
- *   stream        : cudaStream_t to enqueue on (NULL = the legacy default).
+ *   stream        : cudaStream_t to enqueue on (NULL: the context creates and
+ *                   owns a non-blocking stream).
  *   out           : receives the context.
  * Allocates the K/V cache, the call's temporary K/V rows, the n-gram pool
  * ([vocab][max_G][max_N-1] ids), the window, the activations and scratch
- * with cudaMalloc.  Errors: LA_EINVAL, LA_ENOTSUP, LA_ECUDA. */
+ * with cudaMalloc.  la_init first waits for all work already issued on the
+ * device, so weights still being written by another stream are complete
+ * before any kernel of the context reads them; later writes to the weights
+ * must be ordered before the context's calls by the caller.
+ * Errors: LA_EINVAL, LA_ENOTSUP, LA_ECUDA. */
 int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
             int max_W, int max_N, int max_G, void* stream, la_ctx** out);
 
@@ -192,6 +197,35 @@ int la_debug_pool(la_ctx* ctx, int key, int32_t* suffixes, int* count);
  * commit copies whatever the temporary rows hold. */
 int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q,
                    const int32_t* argmax, const float* logits, int32_t* out, int* n_out);
+
+/* The exact sampling verifier alone (M7.3 §0x05B), for distribution tests:
+ * n_trials independent verifications of the same rows, trial i drawing its
+ * uniforms with Philox step index i.
+ *   logits (host) [rows][V] fp32: row 0 the ordinary row, row 1 + c*S + s the
+ *                  row whose input is candidate c's token s (rows >= 1 + Ct*S)
+ *   cand   (host) [Ct][S] candidate suffix ids (Ct <= 32, 1 <= S <= 15)
+ *   s      sampling policy (required)
+ *   out    (host) [n_trials][S+3]: E (tokens emitted), a (accepted
+ *                  candidate tokens), then the S+1 emitted ids (-1 padded).
+ * Uses the current device; allocates its own temporary device buffers.
+ * Errors: LA_EINVAL, LA_ENOTSUP (V * 4 bytes > 200 KB), LA_ECUDA. */
+int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* cand, int Ct, int S,
+                           const la_sampling* s, int n_trials, int32_t* out);
+
+/* The tensor-core GEMM alone, for kernel tests: acc[q][n] = sum_k x[q][k] w[n][k]
+ * with bf16 inputs (host, raw bf16 bit patterns) and fp32 accumulation, split
+ * into `splits` K ranges reduced in fixed order, followed by one epilogue:
+ *   mode 0 store   y[q][n] = bf16(acc)                (w: n_seg stacked segments)
+ *   mode 1 resid   y[q][n] += acc                     (y holds the input, fp32)
+ *   mode 2 swiglu  y[q][n] = bf16(silu(acc_w) * acc_w2)
+ *   mode 3 logits  y[q][n] = acc (fp32)
+ * w [n_out][K], w2 [n_out][K] (swiglu only), x [rows][K]; y (host)
+ * [rows][n_out] fp32 (bf16 results widened).  n_out a multiple of
+ * 128 * n_seg (n_seg 1..3), K of 64, 1 <= rows <= 1024, 1 <= splits <= K/64.
+ * Uses the current device and allocates its own temporary device buffers.
+ * Errors: LA_EINVAL, LA_ECUDA, LA_ETIMEOUT. */
+int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K,
+                  const uint16_t* x, int rows, int splits, float* y);
 
 /* Sizes fixed at la_init: [0]=Qmax [1]=max_W [2]=max_N [3]=max_G [4]=max_ctx
  * [5]=vocab [6]=window row length (max_W+max_N-3) [7]=path length bound. */

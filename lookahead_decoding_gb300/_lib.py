@@ -21,7 +21,7 @@ LA_F32, LA_BF16 = 0, 1
 
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
-           "la_last_cuda_error"]
+           "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm"]
 
 
 class la_model_cfg(C.Structure):
@@ -77,6 +77,10 @@ def _load() -> C.CDLL:
         "la_step_inject": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), C.c_int, i32p, f32p, i32p,
                                      C.POINTER(C.c_int)]),
         "la_query": (C.c_int, [vp, i32p]),
+        "la_debug_gemm": (C.c_int, [C.c_int, C.POINTER(C.c_uint16), C.POINTER(C.c_uint16), C.c_int, C.c_int, C.c_int,
+                                    C.POINTER(C.c_uint16), C.c_int, C.c_int, f32p]),
+        "la_debug_sample_verify": (C.c_int, [f32p, C.c_int, C.c_int, i32p, C.c_int, C.c_int, C.POINTER(la_sampling),
+                                             C.c_int, i32p]),
         "la_free": (None, [vp]),
         "la_strerror": (C.c_char_p, [C.c_int]),
         "la_last_cuda_error": (C.c_char_p, [vp]),
@@ -210,12 +214,15 @@ def la_debug_state(ctx):
 
 
 def la_debug_pool(ctx, key: int):
+    """The bucket of `key`, oldest first, as tuples of the request's N-1 ids."""
     q = la_query(ctx)
     G, S = max(1, q["max_G"]), q["max_N"] - 1
+    h = la_debug_state(ctx)[0]
+    s_req = h["N"] - 1 if h["N"] >= 3 else S
     buf = np.zeros((G, S), dtype=np.int32)
     n = C.c_int()
     _check(LIB.la_debug_pool(ctx, key, buf.ctypes.data_as(C.POINTER(C.c_int32)), C.byref(n)), "la_debug_pool", ctx)
-    return [tuple(r) for r in buf[: n.value].tolist()]
+    return [tuple(r[:s_req]) for r in buf[: n.value].tolist()]
 
 
 def la_step_inject(ctx, W: int, N: int, G: int, argmax: Sequence[int], sampling=None, logits=None) -> List[int]:
@@ -230,6 +237,47 @@ def la_step_inject(ctx, W: int, N: int, G: int, argmax: Sequence[int], sampling=
     _check(LIB.la_step_inject(ctx, W, N, G, C.byref(s) if s else None, len(arr), p, lp, out, C.byref(n)),
            "la_step_inject", ctx)
     return [int(out[i]) for i in range(n.value)]
+
+
+def la_debug_sample_verify(logits, cands, sampling, n_trials: int):
+    """n_trials verifications of the same rows; returns an int32 array [n_trials][S+3]
+    of (E, a, emitted ids padded with -1)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    rows, V = lg.shape
+    c = np.ascontiguousarray(np.asarray(cands, dtype=np.int32).reshape(len(cands), -1)) if len(cands) else \
+        np.zeros((0, 1), dtype=np.int32)
+    Ct, S = c.shape[0], (c.shape[1] if len(cands) else 1)
+    out = np.zeros((n_trials, S + 3), dtype=np.int32)
+    s = _sampling(sampling)
+    _check(LIB.la_debug_sample_verify(lg.ctypes.data_as(C.POINTER(C.c_float)), rows, V,
+                                      c.ctypes.data_as(C.POINTER(C.c_int32)), Ct, S, C.byref(s), n_trials,
+                                      out.ctypes.data_as(C.POINTER(C.c_int32))), "la_debug_sample_verify")
+    return out
+
+
+def _bf16_bits(a):
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+        return np.ascontiguousarray(a.contiguous().view(torch.int16).numpy().view(np.uint16))
+    return np.ascontiguousarray(np.asarray(a, dtype=np.uint16))
+
+
+GEMM_STORE, GEMM_RESID, GEMM_SWIGLU, GEMM_LOGITS = 0, 1, 2, 3
+
+
+def la_debug_gemm(w_bf16, x_bf16, splits: int = 1, mode: int = GEMM_LOGITS, w2_bf16=None, n_seg: int = 1,
+                  y_in=None):
+    """The tensor-core GEMM with one epilogue on bf16 CPU tensors (see the header)."""
+    wb, xb = _bf16_bits(w_bf16), _bf16_bits(x_bf16)
+    n_out, K = wb.shape
+    rows = xb.shape[0]
+    y = np.zeros((rows, n_out), dtype=np.float32) if y_in is None else np.array(y_in, dtype=np.float32, order="C")
+    w2b = _bf16_bits(w2_bf16) if w2_bf16 is not None else None
+    P16 = C.POINTER(C.c_uint16)
+    _check(LIB.la_debug_gemm(mode, wb.ctypes.data_as(P16), w2b.ctypes.data_as(P16) if w2b is not None else None,
+                             n_seg, n_out, K, xb.ctypes.data_as(P16), rows, splits,
+                             y.ctypes.data_as(C.POINTER(C.c_float))), "la_debug_gemm")
+    return y
 
 
 def la_free(ctx) -> None:

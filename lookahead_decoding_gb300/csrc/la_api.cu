@@ -75,12 +75,15 @@ struct la_ctx {
         }                                                 \
     } while (0)
 
+// Allocates and zeroes on the context's stream: the zeroing must be ordered
+// before the first kernel of that stream (a non-blocking stream does not
+// order against the legacy default stream).
 static int dalloc(la_ctx* ctx, void** p, size_t bytes) {
     if (bytes == 0) bytes = 16;
     cudaError_t e = cudaMalloc(p, bytes);
     if (e != cudaSuccess) { ctx->last_err = cudaGetErrorString(e); return LA_ECUDA; }
     ctx->allocs.push_back(*p);
-    e = cudaMemset(*p, 0, bytes);
+    e = cudaMemsetAsync(*p, 0, bytes, ctx->st);
     if (e != cudaSuccess) { ctx->last_err = cudaGetErrorString(e); return LA_ECUDA; }
     return LA_OK;
 }
@@ -202,13 +205,14 @@ static int enqueue_step(la_ctx* ctx) {
     la_launch_pack(ctx->d, ctx->st);
     int r = enqueue_forward(ctx, SEL_CALL);
     if (r) return r;
-    r = enqueue_head(ctx, ctx->debug & 1);
+    r = enqueue_head(ctx, (ctx->debug & 1) | ctx->sampling);
     if (r) return r;
-    return enqueue_publish_commit(ctx, 0);
+    if (ctx->sampling) CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, ctx->cfg.vocab, 0));
+    return enqueue_publish_commit(ctx, ctx->sampling);
 }
 
 static int get_graph(la_ctx* ctx, Graph** out) {
-    int key = (ctx->debug & 1);
+    int key = (ctx->debug & 1) | (ctx->sampling << 1);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     Graph g;
@@ -291,6 +295,9 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
         !w->mlp_norm || !w->w_gate || !w->w_up || !w->w_down)
         return LA_EINVAL;
 
+    // The weights may still be in flight on another stream (the caller's
+    // allocator or generator): wait for all work already issued on the device.
+    if (cudaDeviceSynchronize() != cudaSuccess) return LA_ECUDA;
     la_ctx* ctx = new la_ctx();
     ctx->cfg = c;
     ctx->bf16 = (c.dtype == LA_BF16);
@@ -443,7 +450,13 @@ int la_set_debug(la_ctx* ctx, int flags) {
     return LA_OK;
 }
 
-static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n) {
+static int check_sampling(const la_sampling* s) {
+    if (!s) return LA_OK;
+    if (!(s->temperature > 0.f) || !(s->top_p > 0.f) || !(s->top_p <= 1.f)) return LA_EINVAL;
+    return LA_OK;
+}
+
+static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s) {
     const la_model_cfg& c = ctx->cfg;
     if (!prompt || n < 1) return LA_EINVAL;
     if (n > ctx->max_ctx - 1) return LA_ECAPACITY;
@@ -456,6 +469,14 @@ static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n) {
     memset(&h0, 0, sizeof(h0));
     h0.prompt_len = n;
     h0.max_out = 1;
+    h0.S = 1;
+    if (s) {
+        h0.sampling = 1;
+        h0.temperature = s->temperature;
+        h0.top_p = s->top_p;
+        h0.seed_lo = (uint32_t)(s->seed & 0xffffffffu);
+        h0.seed_hi = (uint32_t)(s->seed >> 32);
+    }
     CK(cudaMemcpyAsync(ctx->d.hdr, &h0, sizeof(h0), cudaMemcpyHostToDevice, ctx->st));
     CK(cudaMemsetAsync(ctx->d.pool_cnt, 0, sizeof(int32_t) * c.vocab, ctx->st));
     for (int c0 = 0; c0 < n; c0 += PREFILL_CHUNK) {
@@ -465,8 +486,9 @@ static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n) {
         if (r) return r;
     }
     la_launch_prefill_need(ctx->d, ctx->st, (n - 1) % PREFILL_CHUNK);
-    int r = enqueue_head(ctx, ctx->debug & 1);
+    int r = enqueue_head(ctx, (ctx->debug & 1) | (s ? 1 : 0));
     if (r) return r;
+    if (s) CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, c.vocab, 1));
     la_launch_prefill_finish(ctx->d, ctx->st, n);
     CK(cudaGetLastError());
     ctx->prompt_len = n;
@@ -475,8 +497,9 @@ static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n) {
 
 int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, int32_t* first_token) {
     if (!ctx || !first_token) return LA_EINVAL;
-    if (s) return LA_ENOTSUP;
-    int r = do_prefill(ctx, prompt, n);
+    int r = check_sampling(s);
+    if (r) return r;
+    r = do_prefill(ctx, prompt, n, s);
     if (r) return r;
     LaHdr h;
     r = read_hdr(ctx, &h);
@@ -504,7 +527,7 @@ static int begin_request(la_ctx* ctx, int mode, int W, int N, int G, const la_sa
 
 int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int32_t* out, int* n_out) {
     if (!ctx || !out || !n_out) return LA_EINVAL;
-    if (s) return LA_ENOTSUP;
+    if (check_sampling(s)) return LA_EINVAL;
     if (!ctx->prefilled) return LA_ESTATE;
     if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
     if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
@@ -512,7 +535,8 @@ int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int32_t* out
     if (!ctx->begun) {
         r = begin_request(ctx, MODE_LOOKAHEAD, W, N, G, s, ctx->out_cap);
         if (r) return r;
-    } else if (ctx->mode != MODE_LOOKAHEAD || W != ctx->W || N != ctx->N || G != ctx->G) {
+    } else if (ctx->mode != MODE_LOOKAHEAD || W != ctx->W || N != ctx->N || G != ctx->G ||
+               ctx->sampling != (s ? 1 : 0)) {
         return LA_ESTATE;
     }
     r = clear_err(ctx);
@@ -531,7 +555,7 @@ int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int32_t* out
 int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q, const int32_t* argmax,
                    const float* logits, int32_t* out, int* n_out) {
     if (!ctx || !out || !n_out || !argmax) return LA_EINVAL;
-    if (s || logits) return LA_ENOTSUP;
+    if (check_sampling(s) || (s && !logits)) return LA_EINVAL;
     if (!ctx->prefilled) return LA_ESTATE;
     if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
     if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
@@ -539,7 +563,8 @@ int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q
     if (!ctx->begun) {
         r = begin_request(ctx, MODE_LOOKAHEAD, W, N, G, s, ctx->out_cap);
         if (r) return r;
-    } else if (ctx->mode != MODE_LOOKAHEAD || W != ctx->W || N != ctx->N || G != ctx->G) {
+    } else if (ctx->mode != MODE_LOOKAHEAD || W != ctx->W || N != ctx->N || G != ctx->G ||
+               ctx->sampling != (s ? 1 : 0)) {
         return LA_ESTATE;
     }
     r = clear_err(ctx);
@@ -553,8 +578,14 @@ int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q
     for (int q = 0; q < Q; ++q)
         if (argmax[q] < 0 || argmax[q] >= ctx->cfg.vocab) return LA_EINVAL;
     CK(cudaMemcpyAsync(ctx->argmax_in, argmax, sizeof(int32_t) * Q, cudaMemcpyHostToDevice, ctx->st));
-    la_launch_inject_map(ctx->d, ctx->st, ctx->argmax_in, nullptr, nullptr, ctx->cfg.vocab);
-    r = enqueue_publish_commit(ctx, 0);
+    if (s) {
+        if (Q > ctx->Qmax) return LA_ECAPACITY;
+        CK(cudaMemcpyAsync(ctx->logits_in, logits, sizeof(float) * (size_t)Q * ctx->cfg.vocab, cudaMemcpyHostToDevice,
+                           ctx->st));
+    }
+    la_launch_inject_map(ctx->d, ctx->st, ctx->argmax_in, s ? ctx->logits_in : nullptr, ctx->logits, ctx->cfg.vocab);
+    if (s) CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, ctx->cfg.vocab, 0));
+    r = enqueue_publish_commit(ctx, s ? 1 : 0);
     if (r) return r;
     r = read_hdr(ctx, &h);
     if (r) return r;
@@ -567,7 +598,7 @@ int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q
 static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int max_new, int W, int N, int G,
                         const la_sampling* s, int32_t* out, int* n_out, la_stats* stats) {
     if (!ctx || !out || !n_out || max_new < 1) return LA_EINVAL;
-    if (s) return LA_ENOTSUP;
+    if (check_sampling(s)) return LA_EINVAL;
     if (mode == MODE_LOOKAHEAD) {
         if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
         if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
@@ -578,7 +609,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
     CK(cudaEventCreate(&e1));
     CK(cudaEventCreate(&e2));
     CK(cudaEventRecord(e0, ctx->st));
-    int r = do_prefill(ctx, prompt, n);
+    int r = do_prefill(ctx, prompt, n, s);
     if (r) return r;
     ctx->prefilled = true;
     CK(cudaEventRecord(e1, ctx->st));
@@ -682,6 +713,130 @@ int la_debug_pool(la_ctx* ctx, int key, int32_t* suffixes, int* count) {
     CK(cudaStreamSynchronize(ctx->st));
     *count = cnt;
     return LA_OK;
+}
+
+int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* cand, int Ct, int S,
+                           const la_sampling* s, int n_trials, int32_t* out) {
+    if (!logits || !s || !out || rows < 1 || V < 2 || Ct < 0 || Ct > LA_MAX_G || S < 1 || S > 15 || n_trials < 1)
+        return LA_EINVAL;
+    if (check_sampling(s)) return LA_EINVAL;
+    if (Ct > 0 && !cand) return LA_EINVAL;
+    if (rows < 1 + Ct * S) return LA_EINVAL;
+    if ((size_t)V * sizeof(float) > 200 * 1024) return LA_ENOTSUP;
+    for (int i = 0; i < Ct * S; ++i)
+        if (cand[i] < 0 || cand[i] >= V) return LA_EINVAL;
+    float* dl = nullptr;
+    int32_t *dc = nullptr, *dout = nullptr;
+    int rc = LA_OK;
+    const size_t out_n = (size_t)n_trials * (S + 3);
+    if (cudaMalloc(&dl, sizeof(float) * (size_t)rows * V) != cudaSuccess ||
+        cudaMalloc(&dc, sizeof(int32_t) * (size_t)std::max(1, Ct * S)) != cudaSuccess ||
+        cudaMalloc(&dout, sizeof(int32_t) * out_n) != cudaSuccess) {
+        rc = LA_ECUDA;
+    }
+    if (!rc && cudaMemcpy(dl, logits, sizeof(float) * (size_t)rows * V, cudaMemcpyHostToDevice) != cudaSuccess) rc = LA_ECUDA;
+    if (!rc && Ct > 0 && cudaMemcpy(dc, cand, sizeof(int32_t) * Ct * S, cudaMemcpyHostToDevice) != cudaSuccess) rc = LA_ECUDA;
+    if (!rc && la_launch_sample_trials(0, dl, V, dc, Ct, S, s->temperature, s->top_p, s->seed, n_trials, dout) != cudaSuccess)
+        rc = LA_ECUDA;
+    if (!rc && cudaMemcpy(out, dout, sizeof(int32_t) * out_n, cudaMemcpyDeviceToHost) != cudaSuccess) rc = LA_ECUDA;
+    cudaFree(dl);
+    cudaFree(dc);
+    cudaFree(dout);
+    return rc;
+}
+
+int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K, const uint16_t* x,
+                  int rows, int splits, float* y) {
+    if (!w || !x || !y || mode < GEMM_STORE || mode > GEMM_LOGITS || n_seg < 1 || n_seg > 3 || n_out < 128 ||
+        n_out % (128 * n_seg) || K < 64 || K % 64 || rows < 1 || rows > 1024 || splits < 1 || splits > K / 64)
+        return LA_EINVAL;
+    if (mode == GEMM_SWIGLU && (!w2 || n_seg != 1)) return LA_EINVAL;
+    if (mode == GEMM_LOGITS && n_seg != 1) return LA_EINVAL;
+    const int rows_cap = ((rows + 255) / 256) * 256;
+    const int n_seg_out = n_out / n_seg;
+    void* dw[3] = {nullptr, nullptr, nullptr};
+    void *dw2 = nullptr, *dx = nullptr, *dout = nullptr;
+    float *ws = nullptr, *pv = nullptr;
+    int *cnt = nullptr, *pi = nullptr;
+    LaHdr* hdr = nullptr;
+    int rc = LA_OK;
+    const int tiles = n_out / 128, qchunks = rows_cap / 256;
+    auto M = [&](void** p, size_t b) { if (!rc && cudaMalloc(p, b) != cudaSuccess) rc = LA_ECUDA; };
+    for (int sgi = 0; sgi < n_seg; ++sgi) M(&dw[sgi], (size_t)n_seg_out * K * 2);
+    if (mode == GEMM_SWIGLU) M(&dw2, (size_t)n_out * K * 2);
+    M(&dx, (size_t)rows_cap * K * 2);
+    M(&dout, (size_t)rows_cap * n_out * 4);
+    M((void**)&ws, (size_t)tiles * qchunks * splits * 2 * 256 * 128 * 4);
+    M((void**)&cnt, (size_t)tiles * qchunks * 4);
+    M((void**)&pv, (size_t)tiles * rows_cap * 4);
+    M((void**)&pi, (size_t)tiles * rows_cap * 4);
+    M((void**)&hdr, sizeof(LaHdr));
+    const bool f32out = (mode == GEMM_RESID || mode == GEMM_LOGITS);
+    if (!rc) {
+        LaHdr h;
+        memset(&h, 0, sizeof(h));
+        h.n_need = rows;
+        bool ok = cudaMemcpy(hdr, &h, sizeof(h), cudaMemcpyHostToDevice) == cudaSuccess;
+        for (int sgi = 0; sgi < n_seg; ++sgi)
+            ok = ok && cudaMemcpy(dw[sgi], w + (size_t)sgi * n_seg_out * K, (size_t)n_seg_out * K * 2,
+                                  cudaMemcpyHostToDevice) == cudaSuccess;
+        if (dw2) ok = ok && cudaMemcpy(dw2, w2, (size_t)n_out * K * 2, cudaMemcpyHostToDevice) == cudaSuccess;
+        ok = ok && cudaMemset(dx, 0, (size_t)rows_cap * K * 2) == cudaSuccess;
+        ok = ok && cudaMemcpy(dx, x, (size_t)rows * K * 2, cudaMemcpyHostToDevice) == cudaSuccess;
+        ok = ok && cudaMemset(cnt, 0, (size_t)tiles * qchunks * 4) == cudaSuccess;
+        ok = ok && cudaMemset(dout, 0, (size_t)rows_cap * n_out * 4) == cudaSuccess;
+        if (mode == GEMM_RESID) ok = ok && cudaMemcpy(dout, y, (size_t)rows * n_out * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+        if (!ok) rc = LA_ECUDA;
+    }
+    if (!rc) {
+        TcGemm g;
+        memset(&g, 0, sizeof(g));
+        if (la_tc_make_map(&g.tmA, dw[0], n_seg_out, K, 128) ||
+            la_tc_make_map(&g.tmA2, mode == GEMM_SWIGLU ? dw2 : (n_seg > 1 ? dw[1] : dw[0]), n_seg_out, K, 128) ||
+            la_tc_make_map(&g.tmA3, n_seg > 2 ? dw[2] : dw[0], n_seg_out, K, 128) ||
+            la_tc_make_map(&g.tmB, dx, rows_cap, K, 16))
+            rc = LA_ECUDA;
+        g.mode = mode;
+        g.K = K;
+        g.Nout = n_out;
+        g.seg_tiles = n_seg > 1 ? n_seg_out / 128 : 0;
+        g.splits = splits;
+        g.rows_cap = rows_cap;
+        g.out = dout;
+        g.ldo = n_out;
+        g.logits = mode == GEMM_LOGITS ? (float*)dout : nullptr;
+        g.ld_logits = n_out;
+        TcWork wk;
+        memset(&wk, 0, sizeof(wk));
+        wk.ws = ws;
+        wk.counters = cnt;
+        wk.part_v = pv;
+        wk.part_i = pi;
+        wk.part_stride = rows_cap;
+        LaDev d;
+        memset(&d, 0, sizeof(d));
+        d.hdr = hdr;
+        if (!rc && la_launch_gemm_tc(d, 0, g, wk, SEL_NEED) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && cudaDeviceSynchronize() != cudaSuccess) rc = LA_ECUDA;
+        LaHdr h;
+        if (!rc && cudaMemcpy(&h, hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && h.err) rc = h.err;
+        if (!rc) {
+            if (f32out) {
+                if (cudaMemcpy(y, dout, (size_t)rows * n_out * 4, cudaMemcpyDeviceToHost) != cudaSuccess) rc = LA_ECUDA;
+            } else {
+                std::vector<uint16_t> tmpb((size_t)rows * n_out);
+                if (cudaMemcpy(tmpb.data(), dout, tmpb.size() * 2, cudaMemcpyDeviceToHost) != cudaSuccess) rc = LA_ECUDA;
+                for (size_t i = 0; i < tmpb.size() && !rc; ++i) {
+                    uint32_t u = (uint32_t)tmpb[i] << 16;
+                    memcpy(&y[i], &u, 4);
+                }
+            }
+        }
+    }
+    for (int sgi = 0; sgi < 3; ++sgi) cudaFree(dw[sgi]);
+    cudaFree(dw2); cudaFree(dx); cudaFree(dout); cudaFree(ws); cudaFree(cnt); cudaFree(pv); cudaFree(pi); cudaFree(hdr);
+    return rc;
 }
 
 }  // extern "C"

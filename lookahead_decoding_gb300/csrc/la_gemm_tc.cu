@@ -280,8 +280,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     float a = 0.f, b = 0.f;
                     for (int s = 0; s < p.splits; ++s) {
                         const float* w = wst + (size_t)s * (2 * BN_MAX * BM);
-                        a = __fadd_rn(a, w[(size_t)(c0 + j) * BM + n_local]);
-                        if (swiglu) b = __fadd_rn(b, w[(size_t)(BN_MAX + c0 + j) * BM + n_local]);
+                        a = __fadd_rn(a, __ldcg(w + (size_t)(c0 + j) * BM + n_local));
+                        if (swiglu) b = __fadd_rn(b, __ldcg(w + (size_t)(BN_MAX + c0 + j) * BM + n_local));
                     }
                     v[j] = a; u[j] = b;
                 }

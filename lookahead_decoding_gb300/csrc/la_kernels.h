@@ -67,3 +67,10 @@ struct TcWork {
 int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
 int la_tc_split_for(int n_tiles, int k_tiles);
+
+// exact sampling verifier (one CTA): reads the needed rows' fp32 logits and
+// writes the verdict (a, winner, E, emitted) into the header; prefill=1 draws
+// the first token of a request from row 0 (Philox step 0xFFFFFFFF)
+cudaError_t la_launch_sample_verify(const LaDev& d, cudaStream_t st, const float* logits, int V, int prefill);
+cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V, const int32_t* cand, int Ct, int S,
+                                    float T, float top_p, uint64_t seed, int n_trials, int32_t* out);

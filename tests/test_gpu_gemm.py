@@ -1,0 +1,69 @@
+"""The tcgen05 GEMM alone against a float64 matmul of the same bf16 inputs:
+shapes with many K tiles per CTA (the shared-memory ring wraps), split-K,
+ragged row counts, several row chunks; plus split and row-count invariance."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def L():
+    from lookahead_decoding_gb300 import lib
+    return lib()
+
+
+def case(n_out, K, rows, seed):
+    g = torch.Generator().manual_seed(seed)
+    w = (torch.randn(n_out, K, generator=g) * 0.05).to(torch.bfloat16)
+    x = torch.randn(rows, K, generator=g).to(torch.bfloat16)
+    ref = x.double().numpy() @ w.double().numpy().T
+    return w, x, ref
+
+
+@pytest.mark.parametrize("n_out,K,rows,splits", [
+    (128, 64, 1, 1), (256, 512, 16, 1), (128, 4096, 76, 1), (384, 4096, 120, 1), (256, 4096, 33, 4),
+    (128, 11008, 7, 4), (256, 1024, 256, 2), (128, 2048, 300, 3), (128, 640, 512, 1),
+])
+def test_gemm_matches_float64(n_out, K, rows, splits):
+    w, x, ref = case(n_out, K, rows, n_out + K + rows)
+    y = L().la_debug_gemm(w, x, splits)
+    err = np.max(np.abs(y - ref)) / (np.max(np.abs(ref)) + 1e-9)
+    assert err < 2e-5, err
+
+
+def bf16(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("K,rows,splits", [(4096, 24, 1), (4096, 60, 4), (512, 7, 8), (11008, 76, 2)])
+def test_store_segments(K, rows, splits):
+    w, x, ref = case(3 * 256, K, rows, 3 + K)
+    y = L().la_debug_gemm(w, x, splits, mode=0, n_seg=3)
+    assert np.max(np.abs(y - bf16(ref))) <= np.max(np.abs(ref)) * 2 ** -7
+
+
+@pytest.mark.parametrize("K,rows,splits", [(4096, 24, 1), (4096, 60, 4), (512, 7, 8), (1408, 300, 2)])
+def test_swiglu(K, rows, splits):
+    w, x, g = case(256, K, rows, 5 + K)
+    w2, _, _ = case(256, K, rows, 6 + K)
+    u = x.double().numpy() @ w2.double().numpy().T
+    ref = g / (1 + np.exp(-g)) * u
+    y = L().la_debug_gemm(w, x, splits, mode=2, w2_bf16=w2)
+    assert np.max(np.abs(y - ref)) <= np.max(np.abs(ref)) * 2 ** -7
+
+
+@pytest.mark.parametrize("K,rows,splits", [(4096, 24, 1), (11008, 60, 4), (512, 7, 8)])
+def test_resid(K, rows, splits):
+    w, x, ref = case(256, K, rows, 7 + K)
+    y0 = np.random.default_rng(1).normal(size=ref.shape).astype(np.float32)
+    y = L().la_debug_gemm(w, x, splits, mode=1, y_in=y0)
+    assert np.max(np.abs(y - (y0 + ref))) < 1e-4 * (np.max(np.abs(ref)) + 1)
+
+
+def test_rows_do_not_change_other_rows_bits():
+    w, x, _ = case(256, 4096, 200, 1)
+    full = L().la_debug_gemm(w, x, 4)
+    for r in (1, 13, 64, 199):
+        part = L().la_debug_gemm(w, x[:r].clone(), 4)
+        assert np.array_equal(part.view(np.uint32), full[:r].view(np.uint32))

@@ -1,0 +1,171 @@
+"""GPU exact-sampling verifier against the oracle and against the target law.
+
+* the 3-token toy p = (0.5, 0.3, 0.2) of the speculative-decoding lesson
+  (Ch. 1) with one-hot candidates B, B, C: the emitted token's law over 1e6
+  verifier runs equals p (chi-square, df 2, alpha 0.001);
+* a two-offset candidate set with shared first tokens: the joint law of the
+  first two output tokens over 1e6 runs equals autoregressive sampling;
+* the same rows and Philox counters give the oracle's decisions exactly;
+* the whole state machine in sampling mode with injected logits follows the
+  oracle call by call.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import lookahead as la
+from oracle import philox
+from oracle import sampling as smp
+from tests.gpu_util import context
+
+pytestmark = pytest.mark.gpu
+
+CHI2_DF2_001 = 13.816
+CHI2_DF8_001 = 26.124
+
+
+def L():
+    from lookahead_decoding_gb300 import lib
+    return lib()
+
+
+def test_toy_three_token_law_1e6():
+    p = np.array([0.5, 0.3, 0.2])
+    logits = np.zeros((4, 3), dtype=np.float32)
+    logits[:] = np.log(p).astype(np.float32)
+    cands = [[1], [1], [2]]                       # B, B, C
+    n = 1_000_000
+    out = L().la_debug_sample_verify(logits, cands, (1.0, 1.0, 20240), n)
+    first = out[:, 2]
+    counts = np.bincount(first, minlength=3)[:3]
+    chi2 = float(((counts - n * p) ** 2 / (n * p)).sum())
+    assert chi2 < CHI2_DF2_001, (counts, chi2)
+    # accepted candidate tokens carry their own mass, the residual the rest
+    acc = out[:, 1] == 1
+    assert abs(acc.mean() - 0.5) < 0.005          # P(accept B or C) = p(B) + p(C)
+
+
+def test_two_offset_joint_law_1e6():
+    V = 3
+    rng = np.random.default_rng(4)
+    p0 = np.array([0.45, 0.35, 0.2])
+    cond = {t: rng.dirichlet(np.ones(V)) for t in range(V)}      # law of the 2nd token after token t
+    cands = [[0, 1], [0, 2], [1, 1]]
+    S = 2
+    rows = np.zeros((1 + 3 * S, V), dtype=np.float32)
+    rows[0] = np.log(p0)
+    for c, g in enumerate(cands):
+        rows[1 + c * S + 0] = np.log(cond[g[0]])
+        rows[1 + c * S + 1] = np.log(np.ones(V) / V)             # bonus rows (not tested here)
+    n = 1_000_000
+    out = L().la_debug_sample_verify(rows, cands, (1.0, 1.0, 777), n)
+    t1 = out[:, 2]
+    t2 = out[:, 3].copy()
+    # when the call stopped after one token, the next call would read cond[t1]
+    short = out[:, 0] == 1
+    for t in range(V):
+        m = short & (t1 == t)
+        t2[m] = rng.choice(V, size=int(m.sum()), p=cond[t])
+    joint = np.zeros((V, V))
+    np.add.at(joint, (t1, t2), 1)
+    exp = n * np.array([[p0[a] * cond[a][b] for b in range(V)] for a in range(V)], dtype=np.float64)
+    chi2 = float(((joint - exp) ** 2 / exp).sum())
+    assert chi2 < CHI2_DF8_001, (joint, exp, chi2)
+
+
+@pytest.mark.parametrize("T,top_p", [(1.0, 1.0), (0.8, 0.9), (0.5, 0.6)])
+def test_decisions_match_oracle(T, top_p):
+    V, S = 16, 3
+    rng = np.random.default_rng(9)
+    cands = [[3, 5, 1], [3, 5, 2], [7, 1, 1], [3, 4, 4], [0, 0, 0]]
+    rows = rng.normal(size=(1 + len(cands) * S, V)).astype(np.float32) * 1.5
+    # survivors with one accepted prefix must read identical rows
+    for c, g in enumerate(cands):
+        for c2, g2 in enumerate(cands):
+            for s in range(S):
+                if list(g[: s + 1]) == list(g2[: s + 1]):
+                    rows[1 + c2 * S + s] = rows[1 + c * S + s]
+    seed, n = 31337, 3000
+    out = L().la_debug_sample_verify(rows, cands, (T, top_p, seed), n)
+    lg = rows.astype(np.float64)
+    mism = 0
+    for i in range(n):
+        ch = smp.PhiloxChooser(seed, i)
+        em, a, w = smp.sample_verify(cands, smp.warp(lg[0], T, top_p),
+                                     lambda c, s: smp.warp(lg[1 + c * S + s], T, top_p), ch)
+        got = [int(x) for x in out[i, 2: 2 + out[i, 0]]]
+        if got != em or int(out[i, 1]) != a:
+            mism += 1
+    assert mism <= 1, mism
+
+
+def fake_logits(rows, V, seed=5):
+    """A stand-in model for the sampling state machine: each row's logits are a
+    fixed random vector chosen by the last two tokens of its visible path,
+    peaked on a few tokens so that pool hits and acceptances are frequent."""
+    sets = la.vis_sets(rows)
+    out = np.zeros((len(rows), V), dtype=np.float32)
+    for i, (rw, s) in enumerate(zip(rows, sets)):
+        path = [rows[j].token for j in sorted(s, key=lambda j: rows[j].position)]
+        a = path[-1]
+        b = path[-2] if len(path) > 1 else 0
+        r = np.random.default_rng(seed * 1000003 + a * 1009 + b)
+        v = np.full(V, -8.0, dtype=np.float32)
+        hot = r.choice(8, size=3, replace=False)
+        v[hot] = r.normal(size=3).astype(np.float32) * 0.7 + 2.0
+        out[i] = v
+    return out
+
+
+@pytest.mark.parametrize("W,N,G", [(5, 3, 5), (3, 4, 2), (6, 5, 6)])
+def test_sampling_state_machine_with_injected_logits(W, N, G):
+    cfg = synth.TINY
+    w = {k: v.to("cuda:0") for k, v in synth.llama_weights(cfg, 0).items()}
+    ctx = context(cfg, w, max_ctx=512, W=8, N=5, G=8)
+    Lb = L()
+    try:
+        T, top_p, seed = 0.9, 0.95, 4242
+        p = [1, 2, 3, 4, 5, 6, 7, 0]
+        first = Lb.la_prefill(ctx.ctx, p, sampling=(T, top_p, seed))
+        st = la.LookaheadState(p, first, W, N, G)
+        samp = la.Sampling(T, top_p, seed)
+        mism = 0
+        total_a = 0
+        for step in range(40):
+            rows, guesses = st.plan()
+            lg = fake_logits(rows, cfg.vocab)
+            argmax = [int(np.argmax(x)) for x in lg]
+            em = Lb.la_step_inject(ctx.ctx, W, N, G, argmax, sampling=(T, top_p, seed), logits=lg)
+            verdict = la.sample_step(lg.astype(np.float64), rows, guesses, st, samp)
+            if em != verdict[0]:
+                mism += 1
+                # follow the GPU (a decision within rounding of a boundary)
+                h = Lb.la_debug_state(ctx.ctx)[0]
+                verdict = (em, h["a"], h["winner"])
+            info = st.publish(rows, guesses, argmax, verdict)
+            total_a += info.a
+            h, lv, _, _, _ = Lb.la_debug_state(ctx.ctx)
+            assert h["K"] == st.p and h["x_t"] == st.x_t
+            assert lv[: N - 1] == [None if l is None else list(l) for l in st.levels]
+        assert mism <= 1
+        assert total_a > 0
+    finally:
+        ctx.close()
+
+
+def test_generate_sampling_runs_and_is_seeded():
+    cfg = synth.TINY
+    w = {k: v.to("cuda:0") for k, v in synth.llama_weights(cfg, 0).items()}
+    ctx = context(cfg, w, max_ctx=256, W=5, N=3, G=5)
+    Lb = L()
+    try:
+        p = synth.uniform_prompt(cfg.vocab, 32, 1).tolist()
+        a = Lb.la_generate(ctx.ctx, p, 48, 5, 3, 5, sampling=(0.8, 0.9, 1))
+        b = Lb.la_generate(ctx.ctx, p, 48, 5, 3, 5, sampling=(0.8, 0.9, 1))
+        c = Lb.la_generate(ctx.ctx, p, 48, 5, 3, 5, sampling=(0.8, 0.9, 2))
+        assert a == b and a != c
+        assert all(0 <= t < cfg.vocab for t in a)
+        ar = Lb.la_generate_ar(ctx.ctx, p, 48, sampling=(0.8, 0.9, 1))
+        assert len(ar) == 48
+    finally:
+        ctx.close()

@@ -20,7 +20,7 @@ def setup():
     from lookahead_decoding_gb300 import lib
     w_cpu = synth.llama_weights(CFG, 0)
     w = {k: v.to("cuda:0") for k, v in w_cpu.items()}
-    ctx = context(CFG, w, max_ctx=256, W=8, N=5, G=8)
+    ctx = context(CFG, w, max_ctx=512, W=8, N=5, G=8)
     oracle = OracleModel(CFG, w_cpu)
     yield lib(), ctx, oracle, w_cpu
     ctx.close()
