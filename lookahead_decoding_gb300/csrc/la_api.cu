@@ -47,6 +47,8 @@ struct la_ctx {
     void *cache = nullptr, *temp = nullptr;
     float *rcos = nullptr, *rsin = nullptr;
     float* logits = nullptr;          // [Qcap][V] fp32
+    float* attn_part = nullptr;       // bf16 attention block partials [Qcap][H][blocks][dh+2]
+    int attn_TB = 0;
     float* logits_in = nullptr;       // [Qmax][V] staging for injected logits
     int32_t* argmax_in = nullptr;     // [Qcap]
     TcWork work{};
@@ -148,10 +150,19 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
         int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ctx->Qmax;
         la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
                           stride, rc);
-        CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
-                               layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
-                               layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax), layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax),
-                               ctx->attn, H, sel, ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc));
+        if (ctx->bf16) {
+            CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
+                                        layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
+                                        layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax),
+                                        layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, ctx->attn_part, H, sel,
+                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB));
+        } else {
+            CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
+                                   layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
+                                   layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax),
+                                   layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, H, sel, ctx->Qcap,
+                                   ctx->max_ctx, ctx->Qmax, rc));
+        }
         if (ctx->tc) {
             CK(la_launch_gemm_tc(d, st, ctx->g_o[l], ctx->work, sel));
         } else {
@@ -286,8 +297,9 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
         return LA_EINVAL;
     if (c.dtype != LA_F32 && c.dtype != LA_BF16) return LA_ENOTSUP;
     if (c.head_dim != 32 && c.head_dim != 128) return LA_ENOTSUP;
+    if (c.d_model > 8192) return LA_ENOTSUP;
     if (c.dtype == LA_F32 && (c.d_model % 64 || c.d_ffn % 64 || c.vocab % 64)) return LA_ENOTSUP;
-    if (c.dtype == LA_BF16 && (c.d_model % 128 || c.d_ffn % 128 || c.vocab % 128)) return LA_ENOTSUP;
+    if (c.dtype == LA_BF16 && (c.d_model % 128 || c.d_ffn % 128 || c.vocab % 128 || c.head_dim != 128)) return LA_ENOTSUP;
     if (max_N < 3 || max_N > LA_MAX_R + 1 || max_W < 1 || max_W > LA_MAX_W || max_G < 0 || max_G > LA_MAX_G ||
         max_ctx < 2)
         return LA_EINVAL;
@@ -386,6 +398,11 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
     A((void**)&ctx->rsin, sizeof(float) * (size_t)ctx->rope_len * (c.head_dim / 2));
     A((void**)&ctx->logits, sizeof(float) * Qc * V);
     A((void**)&ctx->logits_in, sizeof(float) * (size_t)ctx->Qmax * V);
+    if (ctx->bf16) {
+        ctx->attn_TB = la_attn_tail_blocks(ctx->PMAX);
+        A((void**)&ctx->attn_part,
+          sizeof(float) * Qc * c.n_heads * (size_t)la_attn_nblocks(max_ctx) * (c.head_dim + 2));
+    }
     if (r) { la_free(ctx); return r; }
     la_launch_rope_table(ctx->rcos, ctx->rsin, ctx->rope_len, c.head_dim, (double)c.rope_theta, ctx->st);
 

@@ -74,3 +74,10 @@ int la_tc_split_for(int n_tiles, int k_tiles);
 cudaError_t la_launch_sample_verify(const LaDev& d, cudaStream_t st, const float* logits, int V, int prefill);
 cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V, const int32_t* cand, int Ct, int S,
                                     float T, float top_p, uint64_t seed, int n_trials, int32_t* out);
+
+// bf16 attention: committed 128-position blocks on tensor cores + combine/tail
+int la_attn_tail_blocks(int pmax);
+int la_attn_nblocks(int max_ctx);
+cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
+                                     const void* kt, const void* vt, void* out, float* part, int H, int sel, int Qcap,
+                                     int max_ctx, int Qmax, int rows_cap, int TB);

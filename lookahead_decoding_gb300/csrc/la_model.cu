@@ -56,29 +56,52 @@ __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
 // reduction order.  gather=1 reads row need[i] and writes row i.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void k_rmsnorm(LaDev d, const float* x, const T* g, T* y, int dm, float eps, int sel, int gather) {
+__global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const T* g, T* y, int dm, float eps, int sel,
+                                                 int gather) {
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     int row = blockIdx.x;
     if (row >= rows_of(h, sel)) return;
     int src = gather ? d.need[row] : row;
     const float* xr = x + (size_t)src * dm;
+    // the row stays in registers: up to 8 float4 per thread (d_model <= 8192)
+    constexpr int MAXV = 8;
+    float4 v[MAXV];
     float ss = 0.f;
-    for (int i = threadIdx.x; i < dm; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+#pragma unroll
+    for (int k = 0; k < MAXV; ++k) {
+        const int i = (k * blockDim.x + threadIdx.x) * 4;
+        if (i < dm) {
+            v[k] = *reinterpret_cast<const float4*>(xr + i);
+            ss = fmaf(v[k].x, v[k].x, ss);
+            ss = fmaf(v[k].y, v[k].y, ss);
+            ss = fmaf(v[k].z, v[k].z, ss);
+            ss = fmaf(v[k].w, v[k].w, ss);
+        }
+    }
     __shared__ float red[32];
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     if (l == 0) red[w] = ss;
     __syncthreads();
     if (w == 0) {
-        float v = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (l == 0) red[0] = v;
+        float t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (l == 0) red[0] = t;
     }
     __syncthreads();
-    float r = 1.0f / sqrtf(red[0] / (float)dm + eps);
-    for (int i = threadIdx.x; i < dm; i += blockDim.x)
-        y[(size_t)row * dm + i] = from_f<T>(xr[i] * r * to_f(g[i]));
+    const float r = 1.0f / sqrtf(red[0] / (float)dm + eps);
+    T* yr = y + (size_t)row * dm;
+#pragma unroll
+    for (int k = 0; k < MAXV; ++k) {
+        const int i = (k * blockDim.x + threadIdx.x) * 4;
+        if (i < dm) {
+            yr[i + 0] = from_f<T>(v[k].x * r * to_f(g[i + 0]));
+            yr[i + 1] = from_f<T>(v[k].y * r * to_f(g[i + 1]));
+            yr[i + 2] = from_f<T>(v[k].z * r * to_f(g[i + 2]));
+            yr[i + 3] = from_f<T>(v[k].w * r * to_f(g[i + 3]));
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
