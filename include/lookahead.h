@@ -213,19 +213,21 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
                            const la_sampling* s, int n_trials, int32_t* out);
 
 /* The tensor-core GEMM alone, for kernel tests: acc[q][n] = sum_k x[q][k] w[n][k]
- * with bf16 inputs (host, raw bf16 bit patterns) and fp32 accumulation, split
- * into `splits` K ranges reduced in fixed order, followed by one epilogue:
+ * with bf16 inputs (host, raw bf16 bit patterns) and fp32 accumulation on
+ * n_cta persistent CTAs (0: one per SM; the (tile, K slice) units are split
+ * evenly over them and a tile shared by several CTAs is reduced in K order),
+ * followed by one epilogue:
  *   mode 0 store   y[q][n] = bf16(acc)                (w: n_seg stacked segments)
  *   mode 1 resid   y[q][n] += acc                     (y holds the input, fp32)
  *   mode 2 swiglu  y[q][n] = bf16(silu(acc_w) * acc_w2)
  *   mode 3 logits  y[q][n] = acc (fp32)
  * w [n_out][K], w2 [n_out][K] (swiglu only), x [rows][K]; y (host)
  * [rows][n_out] fp32 (bf16 results widened).  n_out a multiple of
- * 128 * n_seg (n_seg 1..3), K of 64, 1 <= rows <= 1024, 1 <= splits <= K/64.
+ * 128 * n_seg (n_seg 1..3), K of 64, 1 <= rows <= 1024, 0 <= n_cta <= 4096.
  * Uses the current device and allocates its own temporary device buffers.
  * Errors: LA_EINVAL, LA_ECUDA, LA_ETIMEOUT. */
 int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K,
-                  const uint16_t* x, int rows, int splits, float* y);
+                  const uint16_t* x, int rows, int n_cta, float* y);
 
 /* Sizes fixed at la_init: [0]=Qmax [1]=max_W [2]=max_N [3]=max_G [4]=max_ctx
  * [5]=vocab [6]=window row length (max_W+max_N-3) [7]=path length bound. */

@@ -265,9 +265,10 @@ def _bf16_bits(a):
 GEMM_STORE, GEMM_RESID, GEMM_SWIGLU, GEMM_LOGITS = 0, 1, 2, 3
 
 
-def la_debug_gemm(w_bf16, x_bf16, splits: int = 1, mode: int = GEMM_LOGITS, w2_bf16=None, n_seg: int = 1,
+def la_debug_gemm(w_bf16, x_bf16, n_cta: int = 0, mode: int = GEMM_LOGITS, w2_bf16=None, n_seg: int = 1,
                   y_in=None):
-    """The tensor-core GEMM with one epilogue on bf16 CPU tensors (see the header)."""
+    """The tensor-core GEMM with one epilogue on bf16 CPU tensors (see the header);
+    n_cta persistent CTAs (0 = one per SM)."""
     wb, xb = _bf16_bits(w_bf16), _bf16_bits(x_bf16)
     n_out, K = wb.shape
     rows = xb.shape[0]
@@ -275,7 +276,7 @@ def la_debug_gemm(w_bf16, x_bf16, splits: int = 1, mode: int = GEMM_LOGITS, w2_b
     w2b = _bf16_bits(w2_bf16) if w2_bf16 is not None else None
     P16 = C.POINTER(C.c_uint16)
     _check(LIB.la_debug_gemm(mode, wb.ctypes.data_as(P16), w2b.ctypes.data_as(P16) if w2b is not None else None,
-                             n_seg, n_out, K, xb.ctypes.data_as(P16), rows, splits,
+                             n_seg, n_out, K, xb.ctypes.data_as(P16), rows, n_cta,
                              y.ctypes.data_as(C.POINTER(C.c_float))), "la_debug_gemm")
     return y
 

@@ -112,9 +112,8 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     g->K = K;
     g->Nout = Nout_seg * n_seg;
     g->seg_tiles = n_seg > 1 ? Nout_seg / 128 : 0;
-    g->splits = la_tc_split_for(g->Nout / 128, K / 64);
-    const char* env = getenv("LA_SPLITK");   // tuning override: fixed split for every GEMM
-    if (env) g->splits = std::max(1, std::min(atoi(env), K / 64));
+    g->n_cta = la_tc_ctas();
+    g->max_seg = la_tc_max_segments(g->Nout / 128, K / 64, g->n_cta);
     g->rows_cap = ctx->Qcap;
     g->out = out;
     g->ldo = ldo;
@@ -425,17 +424,18 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
         if (!r) r = make_gemm(ctx, &ctx->g_head, GEMM_LOGITS, ctx->head, nullptr, nullptr, 1, (int)V, (int)dm, ctx->hn,
                               nullptr, 0);
         if (r) { la_free(ctx); return r; }
-        ctx->g_head.splits = 1;     // argmax partials need whole-K tiles
         ctx->g_head.ld_logits = (int)V;
         size_t wsf = 0;
         int qchunks = ctx->Qcap / 256;
         auto need_ws = [&](const TcGemm& g) {
-            if (g.splits > 1) wsf = std::max(wsf, (size_t)(g.Nout / 128) * qchunks * g.splits * 2 * 256 * 128);
+            const size_t planes = (g.mode == GEMM_SWIGLU) ? 2 : 1;
+            if (g.max_seg > 1) wsf = std::max(wsf, (size_t)(g.Nout / 128) * qchunks * g.max_seg * planes * 256 * 128);
         };
         need_ws(ctx->g_qkv[0]);
         need_ws(ctx->g_o[0]);
         need_ws(ctx->g_gu[0]);
         need_ws(ctx->g_down[0]);
+        need_ws(ctx->g_head);
         ctx->work.ws_floats = wsf;
         A((void**)&ctx->work.ws, sizeof(float) * std::max<size_t>(wsf, 4));
         ctx->work.n_counters = (int)((std::max(3 * HD, std::max(F, V)) / 128) * qchunks);
@@ -763,10 +763,12 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
 }
 
 int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K, const uint16_t* x,
-                  int rows, int splits, float* y) {
+                  int rows, int n_cta, float* y) {
     if (!w || !x || !y || mode < GEMM_STORE || mode > GEMM_LOGITS || n_seg < 1 || n_seg > 3 || n_out < 128 ||
-        n_out % (128 * n_seg) || K < 64 || K % 64 || rows < 1 || rows > 1024 || splits < 1 || splits > K / 64)
+        n_out % (128 * n_seg) || K < 64 || K % 64 || rows < 1 || rows > 1024 || n_cta < 0 || n_cta > 4096)
         return LA_EINVAL;
+    if (n_cta == 0) n_cta = la_tc_ctas();
+    const int max_seg = la_tc_max_segments(n_out / 128, K / 64, n_cta);
     if (mode == GEMM_SWIGLU && (!w2 || n_seg != 1)) return LA_EINVAL;
     if (mode == GEMM_LOGITS && n_seg != 1) return LA_EINVAL;
     const int rows_cap = ((rows + 255) / 256) * 256;
@@ -783,7 +785,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
     if (mode == GEMM_SWIGLU) M(&dw2, (size_t)n_out * K * 2);
     M(&dx, (size_t)rows_cap * K * 2);
     M(&dout, (size_t)rows_cap * n_out * 4);
-    M((void**)&ws, (size_t)tiles * qchunks * splits * 2 * 256 * 128 * 4);
+    M((void**)&ws, (size_t)tiles * qchunks * max_seg * 2 * 256 * 128 * 4);
     M((void**)&cnt, (size_t)tiles * qchunks * 4);
     M((void**)&pv, (size_t)tiles * rows_cap * 4);
     M((void**)&pi, (size_t)tiles * rows_cap * 4);
@@ -817,7 +819,8 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         g.K = K;
         g.Nout = n_out;
         g.seg_tiles = n_seg > 1 ? n_seg_out / 128 : 0;
-        g.splits = splits;
+        g.n_cta = n_cta;
+        g.max_seg = max_seg;
         g.rows_cap = rows_cap;
         g.out = dout;
         g.ldo = n_out;

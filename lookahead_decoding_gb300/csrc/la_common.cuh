@@ -87,4 +87,4 @@ __device__ __forceinline__ void la_set_err(LaHdr* h, int code) { atomicCAS(&h->e
 
 // Spin limit of every bounded device wait (iterations of mbarrier.try_wait,
 // each of which suspends for a hardware-defined interval).
-#define LA_SPIN_LIMIT (1u << 24)
+#define LA_SPIN_LIMIT (1u << 22)

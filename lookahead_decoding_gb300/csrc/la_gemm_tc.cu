@@ -1,22 +1,27 @@
 // Tensor-core GEMM of the packed call on sm_103a: Y[q][n] = sum_k X[q][k] W[n][k]
 // for the QKV, O, gate/up (SwiGLU) and down projections and the LM head.
 //
-// The call is a skinny contraction (Q packed rows against a weight matrix
-// that is read once per call), so the weights take the MMA's M side:
-//   - one CTA owns BM = 128 weight rows (n) and up to 256 packed rows (q);
-//   - TMA streams 128 x 64 bf16 weight tiles and q x 64 activation tiles,
-//     both 128-byte swizzled, through a multi-stage mbarrier pipeline;
-//   - one thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in
-//     TMEM, M = 128, N = q rounded up to 16, K = 16 per instruction);
-//   - four warps read the accumulator back with tcgen05.ld and run the
-//     epilogue (store, residual add, SwiGLU, or logits + argmax partials).
-// Split-K is fixed per weight shape (never by Q) and reduced by the last
-// arriving CTA in split order, so a row's result is independent of how many
-// rows share the call.
+// The call is a skinny contraction: Q packed rows against a weight matrix
+// that streams from HBM once per call, so the kernel is built to keep every
+// SM streaming weights:
+//   - persistent stream-K: one CTA per SM; the (128-row weight tile, 64-wide
+//     K slice) units of the whole matrix are split into equal contiguous
+//     ranges, one per CTA, so every SM moves the same number of bytes;
+//   - warp 0 streams units through a multi-stage TMA + mbarrier ring
+//     (128 x 64 bf16 weight tiles and q x 64 activation tiles, 128-byte
+//     swizzle); warp 1 issues tcgen05.mma (kind::f16, bf16 in, fp32 in TMEM,
+//     M = 128 weight rows, N = q rounded up to 16); warps 2-5 drain the
+//     accumulator with tcgen05.ld;
+//   - two TMEM accumulators alternate between the K segments a CTA owns, so
+//     the MMA warp starts the next tile while the epilogue drains the last;
+//   - a tile whose K range spans several CTAs is finished by the last CTA to
+//     arrive, which adds the fp32 partials in segment (K) order.
+// The partition depends only on the weight shape and the SM count, never on
+// Q, so a row's result does not depend on how many rows share the call.
 //
 // Every wait on an mbarrier is bounded; a wait that runs out sets the device
-// error word (LA_ETIMEOUT) and the CTA skips its outputs, frees its TMEM and
-// returns.
+// error word (LA_ETIMEOUT); the CTA then skips its outputs, frees its TMEM
+// and returns.
 #include "la_common.cuh"
 #include "la_kernels.h"
 
@@ -29,14 +34,15 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN_MAX = 256;
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB
-constexpr int ROW_BYTES = BK * 2;         // 128 B per activation row per stage
+constexpr int ROW_BYTES = BK * 2;         // 128 B per activation row per unit
 constexpr int BOX_ROWS = 16;
-constexpr int MAX_STAGES = 8;
+constexpr int MAX_STAGES = 12;
 constexpr int SMEM_BYTES = 200 * 1024;
+constexpr int NTHREADS = 192;             // producer, MMA, 4 epilogue warps
 
 struct TcParams {
     LaHdr* hdr;
-    int sel, mode, K, Nout, k_tiles, splits, n_tiles, seg_tiles;
+    int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg;
     void* out; int ldo;
     float* logits; int ld_logits;
     float* ws; int* counters;
@@ -50,6 +56,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -119,55 +128,72 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// named barrier among the four epilogue warps
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
 }
 
-__global__ void __launch_bounds__(128, 1)
+// the CTA that owns unit x when T units are split evenly over P CTAs
+__device__ __forceinline__ int cta_of(long long x, long long T, int P) { return (int)(((x + 1) * P - 1) / T); }
+
+__global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
           const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB, TcParams p) {
     LaHdr* h = p.hdr;
     if (h->err != 0 || (p.sel != SEL_PREFILL && h->done != 0)) return;
     const int rows = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
-    const int q0 = blockIdx.z * BN_MAX;
+    const int q0 = blockIdx.y * BN_MAX;
     if (q0 >= rows) return;
     const int nq = min(BN_MAX, rows - q0);
     const int BN = (nq + 15) & ~15;
-    const int tile = blockIdx.x, split = blockIdx.y;
     const int swiglu = (p.mode == GEMM_SWIGLU);
     const int nA = swiglu ? 2 : 1;
-    const int kt0 = (int)((long long)p.k_tiles * split / p.splits);
-    const int kt1 = (int)((long long)p.k_tiles * (split + 1) / p.splits);
-    const int nk = kt1 - kt0;
+    const long long T = (long long)p.n_tiles * p.k_tiles;
+    // never more CTAs than units: every CTA then owns at least one unit and the
+    // owners of one tile are consecutive CTAs
+    const int P = (int)(T < (long long)p.n_cta ? T : (long long)p.n_cta), c = blockIdx.x;
+    if (c >= P) return;
+    const long long u_begin = T * c / P, u_end = T * (c + 1) / P;
+    const int n_units = (int)(u_end - u_begin);
+    if (n_units <= 0) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // layout: [barriers 1 KB][stages ...]
+    // [barriers][flags][reduction scratch 8 KB][stages ...]
     const uint32_t bar_full = base;                        // MAX_STAGES x 8 B
     const uint32_t bar_empty = base + 8 * MAX_STAGES;
-    const uint32_t bar_acc = base + 16 * MAX_STAGES;
-    uint32_t* tmem_slot = (uint32_t*)(gbase + 16 * MAX_STAGES + 8);
-    int* s_flag = (int*)(gbase + 16 * MAX_STAGES + 16);
-    float* red_v = (float*)(gbase + 1024 + 0);             // reuses stage memory after the mainloop
-    const uint32_t stage0 = base + 1024;
+    const uint32_t bar_accf = base + 16 * MAX_STAGES;      // 2 x 8 B
+    const uint32_t bar_acce = bar_accf + 16;               // 2 x 8 B
+    uint32_t* tmem_slot = (uint32_t*)(gbase + 16 * MAX_STAGES + 32);
+    int* s_flag = (int*)(gbase + 16 * MAX_STAGES + 40);
+    float* rv = (float*)(gbase + 1024);                    // [4][BN_MAX] argmax values
+    int* ri = (int*)(gbase + 1024 + 4 * BN_MAX * 4);       // [4][BN_MAX] argmax ids
+    const uint32_t stage0 = base + 1024 + 8192;
     const uint32_t b_bytes = (uint32_t)BN * ROW_BYTES;
     const uint32_t stage_bytes = (((uint32_t)nA * A_BYTES + b_bytes) + 1023u) & ~1023u;
-    int ns = (int)((SMEM_BYTES - 2048) / stage_bytes);
+    int ns = (int)((SMEM_BYTES - 1024 - 8192) / stage_bytes);
     ns = ns > MAX_STAGES ? MAX_STAGES : ns;
     const uint32_t tx_bytes = (uint32_t)nA * A_BYTES + b_bytes;
-    const uint32_t ncols = swiglu ? 512u : 256u;
+    const int acc_cols = nA * BN;                          // one accumulator: nA x BN fp32 columns
+    const int nbuf = (2 * acc_cols <= 512) ? 2 : 1;
+    uint32_t ncols = 32;
+    while (ncols < (uint32_t)(nbuf * acc_cols)) ncols <<= 1;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < ns; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        mbar_init(bar_acc, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_accf + 8 * b, 1);
+            mbar_init(bar_acce + 8 * b, 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        *s_flag = 0;
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -179,156 +205,201 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    bool ok = true;
 
-    if (warp == 0 && lane == 0) {
-        // TMA producer
-        // weight rows of this tile (segmented launches concatenate up to three matrices)
-        const CUtensorMap* wmap = &tmA;
-        int wrow = tile * BM;
-        if (p.seg_tiles > 0) {
-            const int seg = tile / p.seg_tiles;
-            wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
-            wrow = (tile - seg * p.seg_tiles) * BM;
+    if (warp == 0) {
+        if (lane == 0) {
+            // TMA producer: every unit of this CTA, in order
+            uint64_t pol_w, pol_x;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+            bool ok = true;
+            for (int it = 0; it < n_units && ok; ++it) {
+                const long long u = u_begin + it;
+                const int tile = (int)(u / p.k_tiles), kt = (int)(u % p.k_tiles);
+                const int s = it % ns, r = it / ns;
+                if (r > 0 && !mbar_wait(bar_empty + 8 * s, (uint32_t)((r - 1) & 1))) { ok = false; break; }
+                const uint32_t st = stage0 + (uint32_t)s * stage_bytes;
+                const uint32_t fb = bar_full + 8 * s;
+                mbar_expect_tx(fb, tx_bytes);
+                const CUtensorMap* wmap = &tmA;
+                int wrow = tile * BM;
+                if (p.seg_tiles > 0) {
+                    const int seg = tile / p.seg_tiles;
+                    wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
+                    wrow = (tile - seg * p.seg_tiles) * BM;
+                }
+                const int kx = kt * BK;
+                tma_load_2d(st, wmap, fb, kx, wrow, pol_w);
+                if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kx, wrow, pol_w);
+                const uint32_t bst = st + (uint32_t)nA * A_BYTES;
+                for (int rr = 0; rr < BN; rr += BOX_ROWS)
+                    tma_load_2d(bst + (uint32_t)rr * ROW_BYTES, &tmB, fb, kx, q0 + rr, pol_x);
+            }
+            if (!ok) la_set_err(h, LA_ETIMEOUT);
         }
-        uint64_t pol_w, pol_x;
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-        for (int it = 0; it < nk; ++it) {
-            const int s = it % ns, u = it / ns;
-            if (u > 0 && !mbar_wait(bar_empty + 8 * s, (uint32_t)((u - 1) & 1))) { ok = false; break; }
-            const uint32_t st = stage0 + (uint32_t)s * stage_bytes;
-            const uint32_t fb = bar_full + 8 * s;
-            mbar_expect_tx(fb, tx_bytes);
-            const int kx = (kt0 + it) * BK;
-            tma_load_2d(st, wmap, fb, kx, wrow, pol_w);
-            if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kx, tile * BM, pol_w);
-            const uint32_t bst = st + (uint32_t)nA * A_BYTES;
-            for (int r = 0; r < BN; r += BOX_ROWS) tma_load_2d(bst + (uint32_t)r * ROW_BYTES, &tmB, fb, kx, q0 + r, pol_x);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer: one accumulator per K segment, alternating buffers
+            const uint32_t id = idesc_bf16(BN);
+            bool ok = true;
+            int seg_i = 0;
+            int it = 0;
+            while (it < n_units && ok) {
+                const long long u = u_begin + it;
+                const int tile = (int)(u / p.k_tiles);
+                const int seg_end = min(n_units, (int)((long long)(tile + 1) * p.k_tiles - u_begin));
+                const int b = seg_i % nbuf, ub = seg_i / nbuf;
+                if (ub > 0 && !mbar_wait(bar_acce + 8 * b, (uint32_t)((ub - 1) & 1))) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * acc_cols);
+                for (int first = 1; it < seg_end; ++it, first = 0) {
+                    const int s = it % ns, r = it / ns;
+                    if (!mbar_wait(bar_full + 8 * s, (uint32_t)(r & 1))) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t st = stage0 + (uint32_t)s * stage_bytes;
+                    const uint32_t bst = st + (uint32_t)nA * A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t bdesc = sdesc(bst + kk * 32);
+                        const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+                        mma_bf16(acc, sdesc(st + kk * 32), bdesc, id, accum);
+                        if (swiglu) mma_bf16(acc + (uint32_t)BN, sdesc(st + A_BYTES + kk * 32), bdesc, id, accum);
+                    }
+                    mma_commit(bar_empty + 8 * s);
+                }
+                mma_commit(bar_accf + 8 * b);
+                ++seg_i;
+            }
+            if (!ok) la_set_err(h, LA_ETIMEOUT);
         }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer
-        const uint32_t id = idesc_bf16(BN);
-        for (int it = 0; it < nk; ++it) {
-            const int s = it % ns, u = it / ns;
-            if (!mbar_wait(bar_full + 8 * s, (uint32_t)(u & 1))) { ok = false; break; }
+    } else {
+        // epilogue warps 2-5: TMEM lane quarter (warp % 4)
+        const int quarter = warp & 3;
+        const int et = quarter * 32 + lane;                // 0..127: the weight row within the tile
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        int seg_i = 0;
+        int it = 0;
+        bool alive = true;
+        while (it < n_units) {
+            const long long u = u_begin + it;
+            const int tile = (int)(u / p.k_tiles);
+            const long long tile_u0 = (long long)tile * p.k_tiles, tile_u1 = tile_u0 + p.k_tiles;
+            const int seg_end = min(n_units, (int)(tile_u1 - u_begin));
+            it = seg_end;
+            const int b = seg_i % nbuf, ub = seg_i / nbuf;
+            ++seg_i;
+            const bool got = alive && mbar_wait(bar_accf + 8 * b, (uint32_t)(ub & 1));
+            if (!got && alive) { alive = false; la_set_err(h, LA_ETIMEOUT); }
             tc_fence_after();
-            const uint32_t st = stage0 + (uint32_t)s * stage_bytes;
-            const uint32_t bst = st + (uint32_t)nA * A_BYTES;
+            const uint32_t acc = tmem + lane_base + (uint32_t)(b * acc_cols);
+            const int c_first = cta_of(tile_u0, T, P), c_last = cta_of(tile_u1 - 1, T, P);
+            const int nseg = c_last - c_first + 1;
+            const int n = tile * BM + et;
+            const float* wst = nullptr;
+            if (nseg > 1) {
+                // publish this segment's partial; the last CTA to arrive finishes the tile
+                const int sg = c - c_first;
+                float* wsb = p.ws + (((size_t)(tile + (size_t)blockIdx.y * p.n_tiles) * p.max_seg + sg) * nA) *
+                                        (size_t)(BN_MAX * BM);
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(acc + c0, v);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                const uint64_t bdesc = sdesc(bst + kk * 32);
-                mma_bf16(tmem, sdesc(st + kk * 32), bdesc, id, (it > 0 || kk > 0) ? 1u : 0u);
-                if (swiglu) mma_bf16(tmem + (uint32_t)BN_MAX, sdesc(st + A_BYTES + kk * 32), bdesc, id,
-                                     (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int j = 0; j < 16; ++j) __stcg(wsb + (size_t)(c0 + j) * BM + et, got ? v[j] : 0.f);
+                    if (swiglu) {
+                        tmem_ld16(acc + BN + c0, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            __stcg(wsb + (size_t)(BN_MAX + c0 + j) * BM + et, got ? v[j] : 0.f);
+                    }
+                }
+                tc_fence_before();
+                __threadfence();
+                epi_sync();
+                if (quarter == 0 && lane == 0) {
+                    mbar_arrive(bar_acce + 8 * b);      // the accumulator is free again
+                    int* ctr = p.counters + tile + blockIdx.y * p.n_tiles;
+                    const int old = atomicAdd(ctr, 1);
+                    const int last = (old == nseg - 1);
+                    if (last) *ctr = 0;
+                    *s_flag = last;
+                }
+                epi_sync();
+                const bool final_here = (*s_flag != 0);
+                epi_sync();                              // everyone read the flag before it is reused
+                if (!final_here) continue;
+                __threadfence();
+                wst = p.ws + ((size_t)(tile + (size_t)blockIdx.y * p.n_tiles) * p.max_seg * nA) * (size_t)(BN_MAX * BM);
             }
-            mma_commit(bar_empty + 8 * s);
-        }
-        mma_commit(bar_acc);
-    }
-    __syncwarp();
-    if (!__all_sync(0xffffffffu, ok)) la_set_err(h, LA_ETIMEOUT);
-    // every thread waits for the accumulator
-    bool acc_ok = mbar_wait(bar_acc, 0u);
-    if (!acc_ok) la_set_err(h, LA_ETIMEOUT);
-    tc_fence_after();
-
-    const int n_local = warp * 32 + lane;
-    const int n = tile * BM + n_local;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const int is_split = p.splits > 1;
-    const bool last_ok = acc_ok && nk > 0;
-
-    // ---- split-K: publish partial, let the last CTA of the tile finish
-    if (is_split) {
-        float* wsb = p.ws + ((size_t)(tile + (size_t)blockIdx.z * p.n_tiles) * p.splits + split) * (2 * BN_MAX * BM);
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-            float v[16];
-            tmem_ld16(trow + c0, v);
+            // final epilogue, 16 packed rows at a time
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                float v[16], w2[16];
+                if (nseg > 1) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) wsb[(size_t)(c0 + j) * BM + n_local] = last_ok ? v[j] : 0.f;
-            if (swiglu) {
-                tmem_ld16(trow + BN_MAX + c0, v);
+                    for (int j = 0; j < 16; ++j) { v[j] = 0.f; w2[j] = 0.f; }
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const float* w = wst + (size_t)sg * nA * (BN_MAX * BM);
+                        float t1[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) wsb[(size_t)(BN_MAX + c0 + j) * BM + n_local] = last_ok ? v[j] : 0.f;
-            }
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            int* ctr = p.counters + tile + blockIdx.z * p.n_tiles;
-            int old = atomicAdd(ctr, 1);
-            int last = (old == p.splits - 1);
-            if (last) *ctr = 0;
-            *s_flag = last;
-        }
-        __syncthreads();
-        if (!*s_flag) goto done;
-        __threadfence();
-    }
-
-    // ---- final epilogue, 16 packed rows at a time
-    {
-        const float* wst = p.ws + (size_t)(tile + (size_t)blockIdx.z * p.n_tiles) * p.splits * (2 * BN_MAX * BM);
-        float* rv = (float*)red_v;                 // [4][BN] values
-        int* ri = (int*)(red_v + 4 * BN_MAX);      // [4][BN] indices
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-            float v[16], u[16];
-            if (is_split) {
+                        for (int j = 0; j < 16; ++j) t1[j] = __ldcg(w + (size_t)(c0 + j) * BM + et);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], t1[j]);
+                        if (swiglu) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) t1[j] = __ldcg(w + (size_t)(BN_MAX + c0 + j) * BM + et);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) w2[j] = __fadd_rn(w2[j], t1[j]);
+                        }
+                    }
+                } else {
+                    tmem_ld16(acc + c0, v);
+                    if (swiglu) tmem_ld16(acc + BN + c0, w2);
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    float a = 0.f, b = 0.f;
-                    for (int s = 0; s < p.splits; ++s) {
-                        const float* w = wst + (size_t)s * (2 * BN_MAX * BM);
-                        a = __fadd_rn(a, __ldcg(w + (size_t)(c0 + j) * BM + n_local));
-                        if (swiglu) b = __fadd_rn(b, __ldcg(w + (size_t)(BN_MAX + c0 + j) * BM + n_local));
-                    }
-                    v[j] = a; u[j] = b;
-                }
-            } else {
-                tmem_ld16(trow + c0, v);
-                if (swiglu) tmem_ld16(trow + BN_MAX + c0, u);
-            }
-            if (!acc_ok) continue;
+                    const int q = q0 + c0 + j;
+                    const bool in = got && q < rows;
+                    const size_t o = (size_t)q * p.ldo + n;
+                    if (p.mode == GEMM_STORE) {
+                        if (in) ((__nv_bfloat16*)p.out)[o] = __float2bfloat16_rn(v[j]);
+                    } else if (p.mode == GEMM_RESID) {
+                        if (in) ((float*)p.out)[o] += v[j];
+                    } else if (p.mode == GEMM_SWIGLU) {
+                        if (in) ((__nv_bfloat16*)p.out)[o] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * w2[j]);
+                    } else {   // logits + argmax partials over this tile's 128 vocab entries
+                        if (in && p.logits) p.logits[(size_t)q * p.ld_logits + n] = v[j];
+                        float bv = v[j];
+                        int bi = n;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int q = q0 + c0 + j;
-                const bool in = q < rows;
-                const size_t o = (size_t)q * p.ldo + n;
-                if (p.mode == GEMM_STORE) {
-                    if (in) ((__nv_bfloat16*)p.out)[o] = __float2bfloat16_rn(v[j]);
-                } else if (p.mode == GEMM_RESID) {
-                    if (in) ((float*)p.out)[o] += v[j];
-                } else if (p.mode == GEMM_SWIGLU) {
-                    if (in) ((__nv_bfloat16*)p.out)[o] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * u[j]);
-                } else {   // logits + argmax partials over this tile's 128 vocab entries
-                    if (in && p.logits) p.logits[(size_t)q * p.ld_logits + n] = v[j];
-                    float bv = v[j];
-                    int bi = n;
-#pragma unroll
-                    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-                        float v2 = __shfl_xor_sync(0xffffffffu, bv, o2);
-                        int i2 = __shfl_xor_sync(0xffffffffu, bi, o2);
-                        better(bv, bi, v2, i2);
+                        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                            const float vv = __shfl_xor_sync(0xffffffffu, bv, o2);
+                            const int ii = __shfl_xor_sync(0xffffffffu, bi, o2);
+                            better(bv, bi, vv, ii);
+                        }
+                        if (lane == 0) { rv[quarter * BN_MAX + c0 + j] = bv; ri[quarter * BN_MAX + c0 + j] = bi; }
                     }
-                    if (lane == 0) { rv[warp * BN_MAX + c0 + j] = bv; ri[warp * BN_MAX + c0 + j] = bi; }
                 }
             }
-        }
-        if (p.mode == GEMM_LOGITS) {
-            __syncthreads();
-            for (int c = tid; c < nq; c += blockDim.x) {
-                float bv = rv[c];
-                int bi = ri[c];
-                for (int w = 1; w < 4; ++w) better(bv, bi, rv[w * BN_MAX + c], ri[w * BN_MAX + c]);
-                if (acc_ok) {
-                    p.part_v[(size_t)tile * p.part_stride + q0 + c] = bv;
-                    p.part_i[(size_t)tile * p.part_stride + q0 + c] = bi;
+            if (nseg == 1) {
+                tc_fence_before();
+                epi_sync();
+                if (quarter == 0 && lane == 0) mbar_arrive(bar_acce + 8 * b);
+            }
+            if (p.mode == GEMM_LOGITS) {
+                epi_sync();
+                for (int cc = et; cc < nq; cc += 128) {
+                    float bv = rv[cc];
+                    int bi = ri[cc];
+                    for (int w = 1; w < 4; ++w) better(bv, bi, rv[w * BN_MAX + cc], ri[w * BN_MAX + cc]);
+                    if (got) {
+                        p.part_v[(size_t)tile * p.part_stride + q0 + cc] = bv;
+                        p.part_i[(size_t)tile * p.part_stride + q0 + cc] = bi;
+                    }
                 }
+                epi_sync();
             }
         }
     }
-done:
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -363,14 +434,26 @@ int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_ro
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-// Fixed split-K per weight shape: enough CTAs to cover the SMs once.
-int la_tc_split_for(int n_tiles, int k_tiles) {
-    const int sms = 148;
-    int s = sms / n_tiles;
-    if (s < 1) s = 1;
-    if (s > 8) s = 8;
-    if (s > k_tiles) s = k_tiles;
-    return s;
+// CTAs of the persistent kernel: one per SM of the current device
+int la_tc_ctas() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+    return sms;
+}
+
+// The largest number of CTAs that share one tile's K range (the partial
+// segments the workspace must hold per tile).
+int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta) {
+    const long long T = (long long)n_tiles * k_tiles;
+    if ((long long)n_cta > T) n_cta = (int)T;
+    int best = 1;
+    for (int t = 0; t < n_tiles; ++t) {
+        const long long u0 = (long long)t * k_tiles, u1 = u0 + k_tiles - 1;
+        const int c0 = (int)(((u0 + 1) * n_cta - 1) / T), c1 = (int)(((u1 + 1) * n_cta - 1) / T);
+        best = std::max(best, c1 - c0 + 1);
+    }
+    return best;
 }
 
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel) {
@@ -387,9 +470,10 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.K = g.K;
     p.Nout = g.Nout;
     p.k_tiles = g.K / BK;
-    p.splits = g.splits;
     p.n_tiles = g.Nout / BM;
     p.seg_tiles = g.seg_tiles;
+    p.n_cta = g.n_cta;
+    p.max_seg = g.max_seg;
     p.out = g.out;
     p.ldo = g.ldo;
     p.logits = g.logits;
@@ -399,7 +483,7 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.part_v = w.part_v;
     p.part_i = w.part_i;
     p.part_stride = w.part_stride;
-    dim3 grid(p.n_tiles, g.splits, (g.rows_cap + BN_MAX - 1) / BN_MAX);
-    k_gemm_tc<<<grid, 128, SMEM_BYTES + 1024, st>>>(g.tmA, g.tmA2, g.tmA3, g.tmB, p);
+    dim3 grid(g.n_cta, (g.rows_cap + BN_MAX - 1) / BN_MAX);
+    k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES + 1024, st>>>(g.tmA, g.tmA2, g.tmA3, g.tmB, p);
     return cudaGetLastError();
 }

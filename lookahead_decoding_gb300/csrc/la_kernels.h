@@ -50,13 +50,15 @@ struct TcGemm {
     CUtensorMap tmA2;     // second weight matrix (SwiGLU up, or segment 1), else a copy of tmA
     CUtensorMap tmA3;     // segment 2 (QKV), else a copy of tmA
     CUtensorMap tmB;      // activations [rows_alloc][K], box 64 x 16, 128B swizzle
-    int mode, K, Nout, splits, rows_cap;
+    int mode, K, Nout, rows_cap;
     int seg_tiles;        // >0: tiles per weight segment (output columns concatenate the segments)
+    int n_cta;            // persistent CTAs (one per SM)
+    int max_seg;          // largest number of CTAs sharing one tile's K range
     void* out; int ldo;
     float* logits; int ld_logits;   // GEMM_LOGITS: optional fp32 logits
 };
 struct TcWork {
-    float* ws;            // split-K partials
+    float* ws;            // partial tiles of K ranges shared by several CTAs
     size_t ws_floats;
     int* counters;        // per (tile, q-chunk) arrival counters, zero-initialised
     int n_counters;
@@ -66,7 +68,8 @@ struct TcWork {
 };
 int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
-int la_tc_split_for(int n_tiles, int k_tiles);
+int la_tc_ctas();
+int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
 
 // exact sampling verifier (one CTA): reads the needed rows' fp32 logits and
 // writes the verdict (a, winner, E, emitted) into the header; prefill=1 draws

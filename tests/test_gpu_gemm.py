@@ -1,6 +1,7 @@
 """The tcgen05 GEMM alone against a float64 matmul of the same bf16 inputs:
-shapes with many K tiles per CTA (the shared-memory ring wraps), split-K,
-ragged row counts, several row chunks; plus split and row-count invariance."""
+shapes with many K slices per CTA (the shared-memory ring wraps), tiles
+shared by several persistent CTAs, CTAs that own several tiles, ragged row
+counts, several row chunks; plus row-count invariance."""
 import numpy as np
 import pytest
 import torch
@@ -21,13 +22,14 @@ def case(n_out, K, rows, seed):
     return w, x, ref
 
 
-@pytest.mark.parametrize("n_out,K,rows,splits", [
-    (128, 64, 1, 1), (256, 512, 16, 1), (128, 4096, 76, 1), (384, 4096, 120, 1), (256, 4096, 33, 4),
-    (128, 11008, 7, 4), (256, 1024, 256, 2), (128, 2048, 300, 3), (128, 640, 512, 1),
+@pytest.mark.parametrize("n_out,K,rows,n_cta", [
+    (128, 64, 1, 1), (256, 512, 16, 0), (128, 4096, 76, 1), (384, 4096, 120, 0), (256, 4096, 33, 4),
+    (128, 11008, 7, 0), (256, 1024, 256, 3), (128, 2048, 300, 7), (128, 640, 512, 0), (4096, 4096, 60, 0),
+    (1024, 4096, 60, 148), (32000 // 125 * 4, 4096, 1, 0),
 ])
-def test_gemm_matches_float64(n_out, K, rows, splits):
+def test_gemm_matches_float64(n_out, K, rows, n_cta):
     w, x, ref = case(n_out, K, rows, n_out + K + rows)
-    y = L().la_debug_gemm(w, x, splits)
+    y = L().la_debug_gemm(w, x, n_cta)
     err = np.max(np.abs(y - ref)) / (np.max(np.abs(ref)) + 1e-9)
     assert err < 2e-5, err
 
@@ -36,34 +38,34 @@ def bf16(a):
     return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
 
 
-@pytest.mark.parametrize("K,rows,splits", [(4096, 24, 1), (4096, 60, 4), (512, 7, 8), (11008, 76, 2)])
-def test_store_segments(K, rows, splits):
+@pytest.mark.parametrize("K,rows,n_cta", [(4096, 24, 0), (4096, 60, 5), (512, 7, 0), (11008, 76, 2)])
+def test_store_segments(K, rows, n_cta):
     w, x, ref = case(3 * 256, K, rows, 3 + K)
-    y = L().la_debug_gemm(w, x, splits, mode=0, n_seg=3)
+    y = L().la_debug_gemm(w, x, n_cta, mode=0, n_seg=3)
     assert np.max(np.abs(y - bf16(ref))) <= np.max(np.abs(ref)) * 2 ** -7
 
 
-@pytest.mark.parametrize("K,rows,splits", [(4096, 24, 1), (4096, 60, 4), (512, 7, 8), (1408, 300, 2)])
-def test_swiglu(K, rows, splits):
+@pytest.mark.parametrize("K,rows,n_cta", [(4096, 24, 0), (4096, 60, 4), (512, 7, 0), (1408, 300, 2)])
+def test_swiglu(K, rows, n_cta):
     w, x, g = case(256, K, rows, 5 + K)
     w2, _, _ = case(256, K, rows, 6 + K)
     u = x.double().numpy() @ w2.double().numpy().T
     ref = g / (1 + np.exp(-g)) * u
-    y = L().la_debug_gemm(w, x, splits, mode=2, w2_bf16=w2)
+    y = L().la_debug_gemm(w, x, n_cta, mode=2, w2_bf16=w2)
     assert np.max(np.abs(y - ref)) <= np.max(np.abs(ref)) * 2 ** -7
 
 
-@pytest.mark.parametrize("K,rows,splits", [(4096, 24, 1), (11008, 60, 4), (512, 7, 8)])
-def test_resid(K, rows, splits):
+@pytest.mark.parametrize("K,rows,n_cta", [(4096, 24, 0), (11008, 60, 4), (512, 7, 0)])
+def test_resid(K, rows, n_cta):
     w, x, ref = case(256, K, rows, 7 + K)
     y0 = np.random.default_rng(1).normal(size=ref.shape).astype(np.float32)
-    y = L().la_debug_gemm(w, x, splits, mode=1, y_in=y0)
+    y = L().la_debug_gemm(w, x, n_cta, mode=1, y_in=y0)
     assert np.max(np.abs(y - (y0 + ref))) < 1e-4 * (np.max(np.abs(ref)) + 1)
 
 
 def test_rows_do_not_change_other_rows_bits():
     w, x, _ = case(256, 4096, 200, 1)
-    full = L().la_debug_gemm(w, x, 4)
+    full = L().la_debug_gemm(w, x, 0)
     for r in (1, 13, 64, 199):
-        part = L().la_debug_gemm(w, x[:r].clone(), 4)
+        part = L().la_debug_gemm(w, x[:r].clone(), 0)
         assert np.array_equal(part.view(np.uint32), full[:r].view(np.uint32))
