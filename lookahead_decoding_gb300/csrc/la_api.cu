@@ -47,7 +47,7 @@ struct la_ctx {
     void *cache = nullptr, *temp = nullptr;
     float *rcos = nullptr, *rsin = nullptr;
     float* logits = nullptr;          // [Qcap][V] fp32
-    float* attn_part = nullptr;       // bf16 attention block partials [Qcap][H][blocks][dh+2]
+    float* attn_part = nullptr;       // bf16 attention block partials [Qcap][H][blocks][record]
     int attn_TB = 0;
     float* logits_in = nullptr;       // [Qmax][V] staging for injected logits
     int32_t* argmax_in = nullptr;     // [Qcap]
@@ -400,7 +400,7 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
     if (ctx->bf16) {
         ctx->attn_TB = la_attn_tail_blocks(ctx->PMAX);
         A((void**)&ctx->attn_part,
-          sizeof(float) * Qc * c.n_heads * (size_t)la_attn_nblocks(max_ctx) * (c.head_dim + 2));
+          sizeof(float) * Qc * c.n_heads * (size_t)la_attn_nblocks(max_ctx) * la_attn_record_floats());
     }
     if (r) { la_free(ctx); return r; }
     la_launch_rope_table(ctx->rcos, ctx->rsin, ctx->rope_len, c.head_dim, (double)c.rope_theta, ctx->st);

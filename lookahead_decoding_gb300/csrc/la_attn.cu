@@ -2,7 +2,7 @@
 //
 // Every row attends to one key per logical position 0..pos (M7.3 §0x04A:
 // the committed prefix, then the row's own branch path).  The positions are
-// split at t0(pos) = max(0, (floor(pos/64) - TB) * 64), a function of the
+// split at t0(pos) = max(0, (floor(pos/32) - TB) * 32), a function of the
 // row's position alone (TB is fixed per context so that pos - t0 covers
 // every in-call offset):
 //   * k_attn_blocks — keys [0, t0) are committed K/V; one CTA per (head,
@@ -32,11 +32,12 @@ constexpr int RG = 128;           // rows per CTA (8 warps x 16)
 constexpr int PAD = 8;            // bf16 padding per smem row (16 B): conflict-free fragment loads
 constexpr int LDK = DH + PAD;     // K tile [key][dim]
 constexpr int LDV = BLK + PAD;    // V tile transposed [dim][key]
-constexpr int PSTR = DH + 2;      // partial record: m, l, o[DH]
+constexpr int OOFF = 4;           // partial record: m, l, 2 pad, o[DH] (o 16-byte aligned)
+constexpr int PSTR = DH + OOFF;
 
 __device__ __forceinline__ int t0_of(int pos, int TB) {
-    int b = (pos >> 6) - TB;
-    return b > 0 ? (b << 6) : 0;
+    int b = (pos >> 5) - TB;
+    return b > 0 ? (b << 5) : 0;
 }
 
 __device__ __forceinline__ int rows_sel(const LaHdr* h, int sel) {
@@ -196,13 +197,13 @@ __global__ void __launch_bounds__(256) k_attn_blocks(LaDev d, const __nv_bfloat1
         float* pr = part + (((size_t)ra * H + hh) * NS + blk) * PSTR;
         if (t == 0) { pr[0] = ma; pr[1] = la; }
 #pragma unroll
-        for (int n = 0; n < 16; ++n) { pr[2 + n * 8 + 2 * t] = o[n][0]; pr[2 + n * 8 + 2 * t + 1] = o[n][1]; }
+        for (int n = 0; n < 16; ++n) { pr[OOFF + n * 8 + 2 * t] = o[n][0]; pr[OOFF + n * 8 + 2 * t + 1] = o[n][1]; }
     }
     if (rb < r1 && tb > key0) {
         float* pr = part + (((size_t)rb * H + hh) * NS + blk) * PSTR;
         if (t == 0) { pr[0] = mb; pr[1] = lb; }
 #pragma unroll
-        for (int n = 0; n < 16; ++n) { pr[2 + n * 8 + 2 * t] = o[n][2]; pr[2 + n * 8 + 2 * t + 1] = o[n][3]; }
+        for (int n = 0; n < 16; ++n) { pr[OOFF + n * 8 + 2 * t] = o[n][2]; pr[OOFF + n * 8 + 2 * t + 1] = o[n][3]; }
     }
 }
 
@@ -215,7 +216,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part, const __nv_bfloat16* qbuf,
+// CW warps per CTA, one (row, head) per warp; each warp stages its row's
+// 32-key chunks in shared memory with coalesced 16-byte loads.
+constexpr int CW = 4;                 // warps per combine CTA
+constexpr int LDC = DH + 8;           // staged key/value row (bf16), conflict-free 16-byte reads
+
+__global__ void __launch_bounds__(CW * 32) k_attn_combine(LaDev d, const float* part, const __nv_bfloat16* qbuf,
                                                       const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                                                       const __nv_bfloat16* kt, const __nv_bfloat16* vt,
                                                       __nv_bfloat16* out, int sel, int Qcap, int max_ctx, int Qmax,
@@ -225,12 +231,15 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
     const int rows = rows_sel(h, sel);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hh = blockIdx.x;
-    const int r = blockIdx.y * 8 + warp;
-    __shared__ float q_s[8][DH];
-    if (r < rows)
-        for (int i = lane; i < DH; i += 32) q_s[warp][i] = __bfloat162float(qbuf[((size_t)hh * Qcap + r) * DH + i]);
-    __syncwarp();
+    const int r = blockIdx.y * CW + warp;
+    extern __shared__ __align__(16) uint8_t csm[];
+    float (*q_s)[DH] = reinterpret_cast<float (*)[DH]>(csm);                                       // [CW][DH]
+    __nv_bfloat16 (*k_s)[32][LDC] = reinterpret_cast<__nv_bfloat16 (*)[32][LDC]>(csm + CW * DH * 4);  // [CW][32][LDC]
+    __nv_bfloat16 (*v_s)[32][DH] =
+        reinterpret_cast<__nv_bfloat16 (*)[32][DH]>(csm + CW * DH * 4 + CW * 32 * LDC * 2);           // [CW][32][DH]
     if (r >= rows) return;
+    for (int i = lane; i < DH; i += 32) q_s[warp][i] = __bfloat162float(qbuf[((size_t)hh * Qcap + r) * DH + i]);
+    __syncwarp();
     const int prefill = (sel == SEL_PREFILL);
     const int pos = d.row_pos[r];
     const int t0 = t0_of(pos, TB);
@@ -242,12 +251,15 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
     for (int b = 0; b < nb; ++b) {
         const float* pr = part + (((size_t)r * H + hh) * NS + b) * PSTR;
         const float mj = pr[0], lj = pr[1];
+        const float4 oj = *reinterpret_cast<const float4*>(pr + OOFF + lane * 4);
         const float mn = fmaxf(m, mj);
         const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
         const float cb = expf(__fsub_rn(mj, mn));
         l = fmaf(l, ca, __fmul_rn(lj, cb));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = fmaf(o[e], ca, __fmul_rn(pr[2 + lane * 4 + e], cb));
+        o[0] = fmaf(o[0], ca, __fmul_rn(oj.x, cb));
+        o[1] = fmaf(o[1], ca, __fmul_rn(oj.y, cb));
+        o[2] = fmaf(o[2], ca, __fmul_rn(oj.z, cb));
+        o[3] = fmaf(o[3], ca, __fmul_rn(oj.w, cb));
         m = mn;
     }
     // the remaining positions [t0, pos], 32 at a time
@@ -258,6 +270,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
     const int* path = d.row_path + (size_t)r * d.PMAX;
     const float scale = 0.08838834764831845f;
     for (int c0 = t0; c0 <= pos; c0 += 32) {
+        // stage the chunk: key j's source row (cache or the row's path), 16 bytes per lane per step
         const int p = c0 + lane;
         const bool valid = p <= pos;
         const __nv_bfloat16* kp = nullptr;
@@ -269,14 +282,30 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
                 kp = kth + (size_t)src * DH; vp = vth + (size_t)src * DH;
             }
         }
+        const int nvalid = min(32, pos - c0 + 1);
+#pragma unroll 4
+        for (int i = lane; i < 32 * (DH / 8); i += 32) {
+            const int j = i >> 4, c8 = (i & 15) * 8;
+            const __nv_bfloat16* kj = (const __nv_bfloat16*)__shfl_sync(0xffffffffu, (unsigned long long)kp, j);
+            const __nv_bfloat16* vj = (const __nv_bfloat16*)__shfl_sync(0xffffffffu, (unsigned long long)vp, j);
+            if (j < nvalid) {
+                *reinterpret_cast<int4*>(&k_s[warp][j][c8]) = *reinterpret_cast<const int4*>(kj + c8);
+                *reinterpret_cast<int4*>(&v_s[warp][j][c8]) = *reinterpret_cast<const int4*>(vj + c8);
+            }
+        }
+        __syncwarp();
         float s = -INFINITY;
         if (valid) {
             float acc = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < DH; i += 2) {
-                const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(kp + i);
-                acc = fmaf(q_s[warp][i], __low2float(k2), acc);
-                acc = fmaf(q_s[warp][i + 1], __high2float(k2), acc);
+#pragma unroll
+            for (int i = 0; i < DH; i += 8) {
+                const int4 kv = *reinterpret_cast<const int4*>(&k_s[warp][lane][i]);
+                const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc = fmaf(q_s[warp][i + 2 * e], __low2float(k2[e]), acc);
+                    acc = fmaf(q_s[warp][i + 2 * e + 1], __high2float(k2[e]), acc);
+                }
             }
             s = __fmul_rn(acc, scale);
         }
@@ -287,12 +316,12 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
         l = fmaf(l, corr, warp_sum(pj_own));
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[e] = __fmul_rn(o[e], corr);
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < nvalid; ++j) {
             const float pj = __shfl_sync(0xffffffffu, pj_own, j);
-            const __nv_bfloat16* vj = (const __nv_bfloat16*)__shfl_sync(0xffffffffu, (unsigned long long)vp, j);
             if (pj != 0.f) {
-                const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(vj + lane * 4);
-                const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(vj + lane * 4 + 2);
+                const uint2 vv = *reinterpret_cast<const uint2*>(&v_s[warp][j][lane * 4]);
+                const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&vv.x);
+                const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&vv.y);
                 o[0] = fmaf(pj, __low2float(v01), o[0]);
                 o[1] = fmaf(pj, __high2float(v01), o[1]);
                 o[2] = fmaf(pj, __low2float(v23), o[2]);
@@ -300,6 +329,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
             }
         }
         m = mn;
+        __syncwarp();
     }
     const float inv = 1.0f / l;
     __nv_bfloat16* op = out + (size_t)r * H * DH + hh * DH + lane * 4;
@@ -309,8 +339,9 @@ __global__ void __launch_bounds__(256) k_attn_combine(LaDev d, const float* part
 
 }  // namespace
 
-int la_attn_tail_blocks(int pmax) { return (pmax + 63) / 64; }
+int la_attn_tail_blocks(int pmax) { return (pmax + 31) / 32; }
 int la_attn_nblocks(int max_ctx) { return (max_ctx + BLK - 1) / BLK; }
+int la_attn_record_floats() { return PSTR; }
 
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, float* part, int H, int sel, int Qcap,
@@ -326,8 +357,15 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
     dim3 g1(H, NS, (rows_cap + RG - 1) / RG);
     k_attn_blocks<<<g1, 256, smem, st>>>(d, (const __nv_bfloat16*)qbuf, (const __nv_bfloat16*)kc,
                                          (const __nv_bfloat16*)vc, part, sel, Qcap, max_ctx, TB, NS, H);
-    dim3 g2(H, (rows_cap + 7) / 8);
-    k_attn_combine<<<g2, 256, 0, st>>>(d, part, (const __nv_bfloat16*)qbuf, (const __nv_bfloat16*)kc,
+    const size_t csmem = (size_t)CW * DH * 4 + (size_t)CW * 32 * LDC * 2 + (size_t)CW * 32 * DH * 2;
+    static bool cattr = false;
+    if (!cattr) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+        if (e != cudaSuccess) return e;
+        cattr = true;
+    }
+    dim3 g2(H, (rows_cap + CW - 1) / CW);
+    k_attn_combine<<<g2, CW * 32, csmem, st>>>(d, part, (const __nv_bfloat16*)qbuf, (const __nv_bfloat16*)kc,
                                        (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt, (const __nv_bfloat16*)vt,
                                        (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, NS, H);
     return cudaGetLastError();

@@ -337,18 +337,24 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if (nseg > 1) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) { v[j] = 0.f; w2[j] = 0.f; }
-                    for (int sg = 0; sg < nseg; ++sg) {
-                        const float* w = wst + (size_t)sg * nA * (BN_MAX * BM);
-                        float t1[16];
+                    // segments four at a time: 64 loads in flight, sums kept in segment order
+                    for (int pl = 0; pl < nA; ++pl) {
+                        float* dst = pl ? w2 : v;
+                        for (int sg0 = 0; sg0 < nseg; sg0 += 4) {
+                            float t1[4][16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) t1[j] = __ldcg(w + (size_t)(c0 + j) * BM + et);
+                            for (int k = 0; k < 4; ++k) {
+                                const float* w = wst + (size_t)(sg0 + k) * nA * (BN_MAX * BM) +
+                                                 (size_t)(pl * BN_MAX + c0) * BM + et;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], t1[j]);
-                        if (swiglu) {
+                                for (int j = 0; j < 16; ++j) t1[k][j] = (sg0 + k < nseg) ? __ldcg(w + (size_t)j * BM) : 0.f;
+                            }
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) t1[j] = __ldcg(w + (size_t)(BN_MAX + c0 + j) * BM + et);
+                            for (int k = 0; k < 4; ++k)
+                                if (sg0 + k < nseg) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) w2[j] = __fadd_rn(w2[j], t1[j]);
+                                    for (int j = 0; j < 16; ++j) dst[j] = __fadd_rn(dst[j], t1[k][j]);
+                                }
                         }
                     }
                 } else {

@@ -81,6 +81,7 @@ cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V,
 // bf16 attention: committed 128-position blocks on tensor cores + combine/tail
 int la_attn_tail_blocks(int pmax);
 int la_attn_nblocks(int max_ctx);
+int la_attn_record_floats();
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, float* part, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB);
