@@ -137,6 +137,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ar-steps", type=int, default=1)
     ap.add_argument("--max-new", type=int, default=MAX_NEW, help="new tokens per request (profiling runs)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling runs: a model with this many layers of the same shapes (0 = all 32)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -146,6 +148,9 @@ def main():
     import torch
     import synth
     cfg = synth.LLAMA_7B
+    if args.layers:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_layers=args.layers)
     config = {"workload": "llama-7b-shape bf16, batch 1, prompt 512 Markov/Zipf(1.1), 256 new tokens, greedy, "
                           "W=15 N=5 G=15", "model": "llama-7b-shape (random init)", "global_batch": world,
               "seq_len": PROMPT_LEN + MAX_NEW, "parallelism": f"replicas{world}",

@@ -229,6 +229,15 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
 int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K,
                   const uint16_t* x, int rows, int n_cta, float* y);
 
+/* Timing of the tensor-core GEMM alone (kernel tuning): n_copies weight
+ * matrices of [n_out][K] (filled with small deterministic values) are used in
+ * turn so that weights stream from HBM rather than L2; *us receives the mean
+ * device time of one launch over `reps` launches after three warm-up
+ * launches (CUDA events on the legacy default stream).  Arguments as for
+ * la_debug_gemm; 1 <= n_copies <= 64.  Errors: LA_EINVAL, LA_ECUDA,
+ * LA_ETIMEOUT. */
+int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, float* us);
+
 /* Sizes fixed at la_init: [0]=Qmax [1]=max_W [2]=max_N [3]=max_G [4]=max_ctx
  * [5]=vocab [6]=window row length (max_W+max_N-3) [7]=path length bound. */
 int la_query(la_ctx* ctx, int32_t* sizes8);

@@ -21,7 +21,7 @@ LA_F32, LA_BF16 = 0, 1
 
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
-           "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm"]
+           "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm"]
 
 
 class la_model_cfg(C.Structure):
@@ -77,6 +77,7 @@ def _load() -> C.CDLL:
         "la_step_inject": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), C.c_int, i32p, f32p, i32p,
                                      C.POINTER(C.c_int)]),
         "la_query": (C.c_int, [vp, i32p]),
+        "la_bench_gemm": (C.c_int, [C.c_int] * 7 + [f32p]),
         "la_debug_gemm": (C.c_int, [C.c_int, C.POINTER(C.c_uint16), C.POINTER(C.c_uint16), C.c_int, C.c_int, C.c_int,
                                     C.POINTER(C.c_uint16), C.c_int, C.c_int, f32p]),
         "la_debug_sample_verify": (C.c_int, [f32p, C.c_int, C.c_int, i32p, C.c_int, C.c_int, C.POINTER(la_sampling),
@@ -279,6 +280,14 @@ def la_debug_gemm(w_bf16, x_bf16, n_cta: int = 0, mode: int = GEMM_LOGITS, w2_bf
                              n_seg, n_out, K, xb.ctypes.data_as(P16), rows, n_cta,
                              y.ctypes.data_as(C.POINTER(C.c_float))), "la_debug_gemm")
     return y
+
+
+def la_bench_gemm(mode: int, n_out: int, K: int, rows: int, n_cta: int = 0, n_copies: int = 8,
+                  reps: int = 20) -> float:
+    """Mean device microseconds of one tensor-core GEMM launch (see the header)."""
+    us = C.c_float()
+    _check(LIB.la_bench_gemm(mode, n_out, K, rows, n_cta, n_copies, reps, C.byref(us)), "la_bench_gemm")
+    return float(us.value)
 
 
 def la_free(ctx) -> None:

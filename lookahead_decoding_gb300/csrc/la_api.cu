@@ -107,7 +107,7 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     if (la_tc_make_map(&g->tmA, w1, Nout_seg, K, 128)) return LA_ECUDA;
     if (la_tc_make_map(&g->tmA2, w2 ? w2 : w1, Nout_seg, K, 128)) return LA_ECUDA;
     if (la_tc_make_map(&g->tmA3, w3 ? w3 : w1, Nout_seg, K, 128)) return LA_ECUDA;
-    if (la_tc_make_map(&g->tmB, X, ctx->Qcap, K, 16)) return LA_ECUDA;
+    if (la_tc_make_act_maps(g, X, ctx->Qcap, K)) return LA_ECUDA;
     g->mode = mode;
     g->K = K;
     g->Nout = Nout_seg * n_seg;
@@ -813,7 +813,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         if (la_tc_make_map(&g.tmA, dw[0], n_seg_out, K, 128) ||
             la_tc_make_map(&g.tmA2, mode == GEMM_SWIGLU ? dw2 : (n_seg > 1 ? dw[1] : dw[0]), n_seg_out, K, 128) ||
             la_tc_make_map(&g.tmA3, n_seg > 2 ? dw[2] : dw[0], n_seg_out, K, 128) ||
-            la_tc_make_map(&g.tmB, dx, rows_cap, K, 16))
+            la_tc_make_act_maps(&g, dx, rows_cap, K))
             rc = LA_ECUDA;
         g.mode = mode;
         g.K = K;
@@ -856,6 +856,93 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
     }
     for (int sgi = 0; sgi < 3; ++sgi) cudaFree(dw[sgi]);
     cudaFree(dw2); cudaFree(dx); cudaFree(dout); cudaFree(ws); cudaFree(cnt); cudaFree(pv); cudaFree(pi); cudaFree(hdr);
+    return rc;
+}
+
+// fills a bf16 buffer with small deterministic values (timing inputs)
+__global__ void k_fill_bf16(__nv_bfloat16* p, size_t n, uint32_t seed) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        uint32_t h = (uint32_t)i * 2654435761u ^ seed;
+        h ^= h >> 15;
+        h *= 2246822519u;
+        h ^= h >> 13;
+        p[i] = __float2bfloat16_rn(((float)(h & 0xffff) / 65536.0f - 0.5f) * 0.04f);
+    }
+}
+
+int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, float* us) {
+    if (!us || mode < GEMM_STORE || mode > GEMM_LOGITS || n_out < 128 || n_out % 128 || K < 64 || K % 64 ||
+        rows < 1 || rows > 1024 || n_cta < 0 || n_copies < 1 || n_copies > 64 || reps < 1)
+        return LA_EINVAL;
+    if (n_cta == 0) n_cta = la_tc_ctas();
+    const int max_seg = la_tc_max_segments(n_out / 128, K / 64, n_cta);
+    const int rows_cap = ((rows + 255) / 256) * 256;
+    const int tiles = n_out / 128, qchunks = rows_cap / 256;
+    const int nA = mode == GEMM_SWIGLU ? 2 : 1;
+    std::vector<void*> w(n_copies * nA, nullptr);
+    void *dx = nullptr, *dout = nullptr;
+    float *ws = nullptr, *pv = nullptr;
+    int *cnt = nullptr, *pi = nullptr;
+    LaHdr* hdr = nullptr;
+    int rc = LA_OK;
+    auto M = [&](void** p, size_t b) { if (!rc && cudaMalloc(p, b) != cudaSuccess) rc = LA_ECUDA; };
+    for (auto& p : w) M(&p, (size_t)n_out * K * 2);
+    M(&dx, (size_t)rows_cap * K * 2);
+    M(&dout, (size_t)rows_cap * n_out * 4);
+    M((void**)&ws, (size_t)tiles * qchunks * max_seg * 2 * 256 * 128 * 4);
+    M((void**)&cnt, (size_t)tiles * qchunks * 4);
+    M((void**)&pv, (size_t)tiles * rows_cap * 4);
+    M((void**)&pi, (size_t)tiles * rows_cap * 4);
+    M((void**)&hdr, sizeof(LaHdr));
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (!rc) {
+        for (size_t i = 0; i < w.size(); ++i) k_fill_bf16<<<512, 256>>>((__nv_bfloat16*)w[i], (size_t)n_out * K, 17u + (uint32_t)i);
+        k_fill_bf16<<<512, 256>>>((__nv_bfloat16*)dx, (size_t)rows_cap * K, 99u);
+        LaHdr h;
+        memset(&h, 0, sizeof(h));
+        h.n_need = rows;
+        if (cudaMemcpy(hdr, &h, sizeof(h), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemset(cnt, 0, (size_t)tiles * qchunks * 4) != cudaSuccess || cudaMemset(dout, 0, (size_t)rows_cap * n_out * 4))
+            rc = LA_ECUDA;
+        if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) rc = LA_ECUDA;
+    }
+    std::vector<TcGemm> gs(n_copies);
+    for (int i = 0; i < n_copies && !rc; ++i) {
+        TcGemm& g = gs[i];
+        memset(&g, 0, sizeof(g));
+        void* a1 = w[i * nA];
+        void* a2 = nA == 2 ? w[i * nA + 1] : a1;
+        if (la_tc_make_map(&g.tmA, a1, n_out, K, 128) || la_tc_make_map(&g.tmA2, a2, n_out, K, 128) ||
+            la_tc_make_map(&g.tmA3, a1, n_out, K, 128) || la_tc_make_act_maps(&g, dx, rows_cap, K))
+            rc = LA_ECUDA;
+        g.mode = mode; g.K = K; g.Nout = n_out; g.n_cta = n_cta; g.max_seg = max_seg; g.rows_cap = rows_cap;
+        g.out = dout; g.ldo = n_out; g.logits = nullptr; g.ld_logits = n_out;
+    }
+    TcWork wk;
+    memset(&wk, 0, sizeof(wk));
+    wk.ws = ws; wk.counters = cnt; wk.part_v = pv; wk.part_i = pi; wk.part_stride = rows_cap;
+    LaDev d;
+    memset(&d, 0, sizeof(d));
+    d.hdr = hdr;
+    if (!rc) {
+        for (int i = 0; i < 3 && !rc; ++i)
+            if (la_launch_gemm_tc(d, 0, gs[i % n_copies], wk, SEL_NEED) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && cudaEventRecord(e0, 0) != cudaSuccess) rc = LA_ECUDA;
+        for (int i = 0; i < reps && !rc; ++i)
+            if (la_launch_gemm_tc(d, 0, gs[i % n_copies], wk, SEL_NEED) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && cudaEventRecord(e1, 0) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && cudaEventSynchronize(e1) != cudaSuccess) rc = LA_ECUDA;
+        float ms = 0;
+        if (!rc) cudaEventElapsedTime(&ms, e0, e1);
+        *us = ms * 1000.0f / reps;
+        LaHdr h;
+        if (!rc && cudaMemcpy(&h, hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && h.err) rc = h.err;
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    for (auto p : w) cudaFree(p);
+    cudaFree(dx); cudaFree(dout); cudaFree(ws); cudaFree(cnt); cudaFree(pv); cudaFree(pi); cudaFree(hdr);
     return rc;
 }
 

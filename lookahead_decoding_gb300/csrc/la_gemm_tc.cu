@@ -27,6 +27,7 @@
 
 #include <cudaTypedefs.h>
 #include <algorithm>
+#include <cstdlib>
 
 namespace {
 
@@ -42,7 +43,7 @@ constexpr int NTHREADS = 192;             // producer, MMA, 4 epilogue warps
 
 struct TcParams {
     LaHdr* hdr;
-    int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg;
+    int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg, max_stages;
     void* out; int ldo;
     float* logits; int ld_logits;
     float* ws; int* counters;
@@ -140,7 +141,9 @@ __device__ __forceinline__ int cta_of(long long x, long long T, int P) { return 
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-          const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+          const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB,
+          const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
+          const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB256, TcParams p) {
     LaHdr* h = p.hdr;
     if (h->err != 0 || (p.sel != SEL_PREFILL && h->done != 0)) return;
     const int rows = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
@@ -177,7 +180,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const uint32_t b_bytes = (uint32_t)BN * ROW_BYTES;
     const uint32_t stage_bytes = (((uint32_t)nA * A_BYTES + b_bytes) + 1023u) & ~1023u;
     int ns = (int)((SMEM_BYTES - 1024 - 8192) / stage_bytes);
-    ns = ns > MAX_STAGES ? MAX_STAGES : ns;
+    ns = ns > p.max_stages ? p.max_stages : ns;
     const uint32_t tx_bytes = (uint32_t)nA * A_BYTES + b_bytes;
     const int acc_cols = nA * BN;                          // one accumulator: nA x BN fp32 columns
     const int nbuf = (2 * acc_cols <= 512) ? 2 : 1;
@@ -231,9 +234,17 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int kx = kt * BK;
                 tma_load_2d(st, wmap, fb, kx, wrow, pol_w);
                 if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kx, wrow, pol_w);
+                // activation rows in at most four boxes (256/128/64/32/16 rows)
                 const uint32_t bst = st + (uint32_t)nA * A_BYTES;
-                for (int rr = 0; rr < BN; rr += BOX_ROWS)
-                    tma_load_2d(bst + (uint32_t)rr * ROW_BYTES, &tmB, fb, kx, q0 + rr, pol_x);
+                int rr = 0;
+                while (rr < BN) {
+                    const int left = BN - rr;
+                    const CUtensorMap* bm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128 : left >= 64 ? &tmB64
+                                          : left >= 32 ? &tmB32 : &tmB;
+                    const int hgt = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : left >= 32 ? 32 : 16;
+                    tma_load_2d(bst + (uint32_t)rr * ROW_BYTES, bm, fb, kx, q0 + rr, pol_x);
+                    rr += hgt;
+                }
             }
             if (!ok) la_set_err(h, LA_ETIMEOUT);
         }
@@ -440,6 +451,14 @@ int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_ro
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
+int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K) {
+    if (la_tc_make_map(&g->tmB, base, rows, K, 16) || la_tc_make_map(&g->tmB32, base, rows, K, 32) ||
+        la_tc_make_map(&g->tmB64, base, rows, K, 64) || la_tc_make_map(&g->tmB128, base, rows, K, 128) ||
+        la_tc_make_map(&g->tmB256, base, rows, K, 256))
+        return -1;
+    return 0;
+}
+
 // CTAs of the persistent kernel: one per SM of the current device
 int la_tc_ctas() {
     int dev = 0, sms = 0;
@@ -480,6 +499,14 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.seg_tiles = g.seg_tiles;
     p.n_cta = g.n_cta;
     p.max_seg = g.max_seg;
+    static int stages = -1;
+    if (stages < 0) {
+        const char* e = getenv("LA_TC_STAGES");   // pipeline-depth override for tuning runs
+        stages = e ? atoi(e) : MAX_STAGES;
+        if (stages < 2) stages = 2;
+        if (stages > MAX_STAGES) stages = MAX_STAGES;
+    }
+    p.max_stages = stages;
     p.out = g.out;
     p.ldo = g.ldo;
     p.logits = g.logits;
@@ -490,6 +517,7 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.part_i = w.part_i;
     p.part_stride = w.part_stride;
     dim3 grid(g.n_cta, (g.rows_cap + BN_MAX - 1) / BN_MAX);
-    k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES + 1024, st>>>(g.tmA, g.tmA2, g.tmA3, g.tmB, p);
+    k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES + 1024, st>>>(g.tmA, g.tmA2, g.tmA3, g.tmB, g.tmB32, g.tmB64, g.tmB128,
+                                                         g.tmB256, p);
     return cudaGetLastError();
 }

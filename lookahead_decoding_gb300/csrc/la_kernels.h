@@ -50,6 +50,7 @@ struct TcGemm {
     CUtensorMap tmA2;     // second weight matrix (SwiGLU up, or segment 1), else a copy of tmA
     CUtensorMap tmA3;     // segment 2 (QKV), else a copy of tmA
     CUtensorMap tmB;      // activations [rows_alloc][K], box 64 x 16, 128B swizzle
+    CUtensorMap tmB32, tmB64, tmB128, tmB256;   // the same activations with taller boxes
     int mode, K, Nout, rows_cap;
     int seg_tiles;        // >0: tiles per weight segment (output columns concatenate the segments)
     int n_cta;            // persistent CTAs (one per SM)
@@ -67,6 +68,7 @@ struct TcWork {
     int part_stride;
 };
 int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
+int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K);
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
 int la_tc_ctas();
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
