@@ -238,6 +238,37 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
  * LA_ETIMEOUT. */
 int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, float* us);
 
+/* The tensor-core GEMM for callers that cannot allocate device memory.  The
+ * lookahead decoding pages have no counterpart to this call: it is a service
+ * of this library.  Callers that cannot allocate: an engine whose own pool (a
+ * KV-cache arena, a caching allocator) already holds all free device memory,
+ * and callers that cannot accept the device-wide synchronisation cudaFree
+ * implies.  The call allocates nothing: its workspace (status word, per-tile
+ * arrival counters, split-tile partial sums) lives in a fixed 64 MiB array
+ * compiled into the library, one per device.
+ *   mode 0 store   y[q][n] = bf16(acc)            y bf16 [rows][n_out]
+ *   mode 1 resid   y[q][n] += acc                 y fp32 [rows][n_out]
+ *   mode 2 swiglu  y[q][n] = bf16(silu(acc_w) * acc_w2)
+ * with acc[q][n] = sum_k x[q][k] w[n][k] (fp32 accumulation, K order, the
+ * same kernel and reduction order as la_debug_gemm with n_cta 0).
+ *   w, w2 (device) bf16 [n_out][K] row-major, 16-byte aligned (w2: swiglu only)
+ *   x     (device) bf16 [rows][K] row-major, 16-byte aligned
+ *   y     (device) as above, 4-byte aligned
+ *   stream  cudaStream_t the work is ordered on (NULL: the legacy stream)
+ * n_out a multiple of 128, K a multiple of 64 (>= 64), rows >= 1.  The call
+ * returns once the result is in y.  The first call on a device (the current
+ * one) looks up the workspace address and sets the kernel's shared-memory
+ * limit there; make it before any stream capture on that device.  The
+ * counters and status word must be zero when the GEMM starts: the call zeroes
+ * them itself on `stream` before each launch.  There is one workspace per
+ * device, so two executions overlapping on a device would race on it; calls
+ * hold a process-wide lock until their work has finished, which keeps them
+ * from overlapping.  Errors: LA_EINVAL (argument, alignment), LA_ECAPACITY
+ * (the problem's partial sums exceed the 64 MiB workspace; checked before any
+ * device work), LA_ENOTSUP (device index >= 64), LA_ECUDA, LA_ETIMEOUT. */
+int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, const void* x, int rows, void* y,
+                    void* stream);
+
 /* Sizes fixed at la_init: [0]=Qmax [1]=max_W [2]=max_N [3]=max_G [4]=max_ctx
  * [5]=vocab [6]=window row length (max_W+max_N-3) [7]=path length bound. */
 int la_query(la_ctx* ctx, int32_t* sizes8);

@@ -21,7 +21,8 @@ LA_F32, LA_BF16 = 0, 1
 
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
-           "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm"]
+           "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
+           "la_gemm_noalloc"]
 
 
 class la_model_cfg(C.Structure):
@@ -78,6 +79,7 @@ def _load() -> C.CDLL:
                                      C.POINTER(C.c_int)]),
         "la_query": (C.c_int, [vp, i32p]),
         "la_bench_gemm": (C.c_int, [C.c_int] * 7 + [f32p]),
+        "la_gemm_noalloc": (C.c_int, [C.c_int, vp, vp, C.c_int, C.c_int, vp, C.c_int, vp, vp]),
         "la_debug_gemm": (C.c_int, [C.c_int, C.POINTER(C.c_uint16), C.POINTER(C.c_uint16), C.c_int, C.c_int, C.c_int,
                                     C.POINTER(C.c_uint16), C.c_int, C.c_int, f32p]),
         "la_debug_sample_verify": (C.c_int, [f32p, C.c_int, C.c_int, i32p, C.c_int, C.c_int, C.POINTER(la_sampling),
@@ -288,6 +290,13 @@ def la_bench_gemm(mode: int, n_out: int, K: int, rows: int, n_cta: int = 0, n_co
     us = C.c_float()
     _check(LIB.la_bench_gemm(mode, n_out, K, rows, n_cta, n_copies, reps, C.byref(us)), "la_bench_gemm")
     return float(us.value)
+
+
+def la_gemm_noalloc(mode: int, w_ptr: int, w2_ptr: Optional[int], n_out: int, K: int, x_ptr: int, rows: int,
+                    y_ptr: int, stream: Optional[int] = None) -> None:
+    """The tensor-core GEMM on caller-owned device buffers (raw device
+    addresses), with no device allocation (see the header)."""
+    _check(LIB.la_gemm_noalloc(mode, w_ptr, w2_ptr, n_out, K, x_ptr, rows, y_ptr, stream), "la_gemm_noalloc")
 
 
 def la_free(ctx) -> None:

@@ -481,6 +481,21 @@ int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta) {
     return best;
 }
 
+// Opt the kernel into its dynamic shared memory on the current device.
+cudaError_t la_tc_prepare_device() {
+    return cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES + 1024);
+}
+
+// Scratch the kernel needs for one problem: the split-tile partial sums
+// (floats) and the per-tile arrival counters (ints).
+void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t* ws_floats, size_t* n_counters) {
+    const int tiles = n_out / BM, k_tiles = K / BK, n_y = (rows + BN_MAX - 1) / BN_MAX;
+    const int nA = mode == GEMM_SWIGLU ? 2 : 1;
+    const int max_seg = la_tc_max_segments(tiles, k_tiles, n_cta);
+    *ws_floats = (size_t)tiles * n_y * max_seg * nA * BN_MAX * BM;
+    *n_counters = (size_t)tiles * n_y;
+}
+
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel) {
     static bool attr_set = false;
     if (!attr_set) {

@@ -72,6 +72,8 @@ int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K);
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
 int la_tc_ctas();
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
+cudaError_t la_tc_prepare_device();
+void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t* ws_floats, size_t* n_counters);
 
 // exact sampling verifier (one CTA): reads the needed rows' fp32 logits and
 // writes the verdict (a, winner, E, emitted) into the header; prefill=1 draws
