@@ -233,10 +233,13 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
  * matrices of [n_out][K] (filled with small deterministic values) are used in
  * turn so that weights stream from HBM rather than L2; *us receives the mean
  * device time of one launch over `reps` launches after three warm-up
- * launches (CUDA events on the legacy default stream).  Arguments as for
- * la_debug_gemm; 1 <= n_copies <= 64.  Errors: LA_EINVAL, LA_ECUDA,
+ * launches (CUDA events on the legacy default stream).  Each launch
+ * prefetches into L2 the first pf_units weight tiles per CTA of the copy
+ * used next (0: no prefetch).  Arguments as for la_debug_gemm;
+ * 1 <= n_copies <= 64, pf_units >= 0.  Errors: LA_EINVAL, LA_ECUDA,
  * LA_ETIMEOUT. */
-int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, float* us);
+int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, int pf_units,
+                  float* us);
 
 /* The tensor-core GEMM for callers that cannot allocate device memory.  The
  * lookahead decoding pages have no counterpart to this call: it is a service
@@ -255,7 +258,7 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
  *   x     (device) bf16 [rows][K] row-major, 16-byte aligned
  *   y     (device) as above, 4-byte aligned
  *   stream  cudaStream_t the work is ordered on (NULL: the legacy stream)
- * n_out a multiple of 128, K a multiple of 64 (>= 64), rows >= 1.  The call
+ * n_out a multiple of 128, K a multiple of 64 (>= 64), 1 <= rows <= 1024.  The call
  * returns once the result is in y.  The first call on a device (the current
  * one) looks up the workspace address and sets the kernel's shared-memory
  * limit there; make it before any stream capture on that device.  The

@@ -78,7 +78,7 @@ def _load() -> C.CDLL:
         "la_step_inject": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), C.c_int, i32p, f32p, i32p,
                                      C.POINTER(C.c_int)]),
         "la_query": (C.c_int, [vp, i32p]),
-        "la_bench_gemm": (C.c_int, [C.c_int] * 7 + [f32p]),
+        "la_bench_gemm": (C.c_int, [C.c_int] * 8 + [f32p]),
         "la_gemm_noalloc": (C.c_int, [C.c_int, vp, vp, C.c_int, C.c_int, vp, C.c_int, vp, vp]),
         "la_debug_gemm": (C.c_int, [C.c_int, C.POINTER(C.c_uint16), C.POINTER(C.c_uint16), C.c_int, C.c_int, C.c_int,
                                     C.POINTER(C.c_uint16), C.c_int, C.c_int, f32p]),
@@ -285,10 +285,10 @@ def la_debug_gemm(w_bf16, x_bf16, n_cta: int = 0, mode: int = GEMM_LOGITS, w2_bf
 
 
 def la_bench_gemm(mode: int, n_out: int, K: int, rows: int, n_cta: int = 0, n_copies: int = 8,
-                  reps: int = 20) -> float:
+                  reps: int = 20, pf_units: int = 0) -> float:
     """Mean device microseconds of one tensor-core GEMM launch (see the header)."""
     us = C.c_float()
-    _check(LIB.la_bench_gemm(mode, n_out, K, rows, n_cta, n_copies, reps, C.byref(us)), "la_bench_gemm")
+    _check(LIB.la_bench_gemm(mode, n_out, K, rows, n_cta, n_copies, reps, pf_units, C.byref(us)), "la_bench_gemm")
     return float(us.value)
 
 

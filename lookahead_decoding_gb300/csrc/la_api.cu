@@ -425,6 +425,18 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
                               nullptr, 0);
         if (r) { la_free(ctx); return r; }
         ctx->g_head.ld_logits = (int)V;
+        // every GEMM prefetches into L2 the first weight tiles of the GEMM launched
+        // after it (the head's successor is the first QKV of the next call)
+        const int pf = la_tc_pf_units();
+        for (int l = 0; l < c.n_layers; ++l) {
+            ctx->g_qkv[l].next = &ctx->g_o[l];
+            ctx->g_o[l].next = &ctx->g_gu[l];
+            ctx->g_gu[l].next = &ctx->g_down[l];
+            ctx->g_down[l].next = l + 1 < c.n_layers ? &ctx->g_qkv[l + 1] : &ctx->g_head;
+            ctx->g_qkv[l].pf_units = ctx->g_o[l].pf_units = ctx->g_gu[l].pf_units = ctx->g_down[l].pf_units = pf;
+        }
+        ctx->g_head.next = &ctx->g_qkv[0];
+        ctx->g_head.pf_units = pf;
         size_t wsf = 0;
         int qchunks = ctx->Qcap / 256;
         auto need_ws = [&](const TcGemm& g) {
@@ -438,7 +450,18 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
         need_ws(ctx->g_head);
         ctx->work.ws_floats = wsf;
         A((void**)&ctx->work.ws, sizeof(float) * std::max<size_t>(wsf, 4));
-        ctx->work.n_counters = (int)((std::max(3 * HD, std::max(F, V)) / 128) * qchunks);
+        // split-tile counters: a region per GEMM (each tile's counter counts
+        // arrivals over all launches of that GEMM)
+        int slots = 0;
+        auto give = [&](TcGemm& g) { g.ctr_off = slots; slots += (g.Nout / 128) * qchunks; };
+        for (int l = 0; l < c.n_layers; ++l) {
+            give(ctx->g_qkv[l]);
+            give(ctx->g_o[l]);
+            give(ctx->g_gu[l]);
+            give(ctx->g_down[l]);
+        }
+        give(ctx->g_head);
+        ctx->work.n_counters = LA_TC_CTR_PER_TILE * slots;
         A((void**)&ctx->work.counters, sizeof(int) * ctx->work.n_counters);
         ctx->work.part_stride = ctx->Qcap;
         A((void**)&ctx->work.part_v, sizeof(float) * (V / 128) * ctx->Qcap);
@@ -786,7 +809,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
     M(&dx, (size_t)rows_cap * K * 2);
     M(&dout, (size_t)rows_cap * n_out * 4);
     M((void**)&ws, (size_t)tiles * qchunks * max_seg * 2 * 256 * 128 * 4);
-    M((void**)&cnt, (size_t)tiles * qchunks * 4);
+    M((void**)&cnt, (size_t)LA_TC_CTR_PER_TILE * tiles * qchunks * 4);
     M((void**)&pv, (size_t)tiles * rows_cap * 4);
     M((void**)&pi, (size_t)tiles * rows_cap * 4);
     M((void**)&hdr, sizeof(LaHdr));
@@ -802,7 +825,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         if (dw2) ok = ok && cudaMemcpy(dw2, w2, (size_t)n_out * K * 2, cudaMemcpyHostToDevice) == cudaSuccess;
         ok = ok && cudaMemset(dx, 0, (size_t)rows_cap * K * 2) == cudaSuccess;
         ok = ok && cudaMemcpy(dx, x, (size_t)rows * K * 2, cudaMemcpyHostToDevice) == cudaSuccess;
-        ok = ok && cudaMemset(cnt, 0, (size_t)tiles * qchunks * 4) == cudaSuccess;
+        ok = ok && cudaMemset(cnt, 0, (size_t)LA_TC_CTR_PER_TILE * tiles * qchunks * 4) == cudaSuccess;
         ok = ok && cudaMemset(dout, 0, (size_t)rows_cap * n_out * 4) == cudaSuccess;
         if (mode == GEMM_RESID) ok = ok && cudaMemcpy(dout, y, (size_t)rows * n_out * 4, cudaMemcpyHostToDevice) == cudaSuccess;
         if (!ok) rc = LA_ECUDA;
@@ -870,9 +893,9 @@ __global__ void k_fill_bf16(__nv_bfloat16* p, size_t n, uint32_t seed) {
     }
 }
 
-int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, float* us) {
+int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, int pf_units, float* us) {
     if (!us || mode < GEMM_STORE || mode > GEMM_LOGITS || n_out < 128 || n_out % 128 || K < 64 || K % 64 ||
-        rows < 1 || rows > 1024 || n_cta < 0 || n_copies < 1 || n_copies > 64 || reps < 1)
+        rows < 1 || rows > 1024 || n_cta < 0 || n_copies < 1 || n_copies > 64 || reps < 1 || pf_units < 0)
         return LA_EINVAL;
     if (n_cta == 0) n_cta = la_tc_ctas();
     const int max_seg = la_tc_max_segments(n_out / 128, K / 64, n_cta);
@@ -890,7 +913,7 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
     M(&dx, (size_t)rows_cap * K * 2);
     M(&dout, (size_t)rows_cap * n_out * 4);
     M((void**)&ws, (size_t)tiles * qchunks * max_seg * 2 * 256 * 128 * 4);
-    M((void**)&cnt, (size_t)tiles * qchunks * 4);
+    M((void**)&cnt, (size_t)LA_TC_CTR_PER_TILE * tiles * qchunks * 4);
     M((void**)&pv, (size_t)tiles * rows_cap * 4);
     M((void**)&pi, (size_t)tiles * rows_cap * 4);
     M((void**)&hdr, sizeof(LaHdr));
@@ -902,7 +925,7 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
         memset(&h, 0, sizeof(h));
         h.n_need = rows;
         if (cudaMemcpy(hdr, &h, sizeof(h), cudaMemcpyHostToDevice) != cudaSuccess ||
-            cudaMemset(cnt, 0, (size_t)tiles * qchunks * 4) != cudaSuccess || cudaMemset(dout, 0, (size_t)rows_cap * n_out * 4))
+            cudaMemset(cnt, 0, (size_t)LA_TC_CTR_PER_TILE * tiles * qchunks * 4) != cudaSuccess || cudaMemset(dout, 0, (size_t)rows_cap * n_out * 4))
             rc = LA_ECUDA;
         if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) rc = LA_ECUDA;
     }
@@ -917,6 +940,10 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
             rc = LA_ECUDA;
         g.mode = mode; g.K = K; g.Nout = n_out; g.n_cta = n_cta; g.max_seg = max_seg; g.rows_cap = rows_cap;
         g.out = dout; g.ldo = n_out; g.logits = nullptr; g.ld_logits = n_out;
+    }
+    for (int i = 0; i < n_copies && !rc; ++i) {
+        gs[i].next = &gs[(i + 1) % n_copies];
+        gs[i].pf_units = pf_units;
     }
     TcWork wk;
     memset(&wk, 0, sizeof(wk));

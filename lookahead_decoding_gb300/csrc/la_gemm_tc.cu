@@ -14,8 +14,14 @@
 //     accumulator with tcgen05.ld;
 //   - two TMEM accumulators alternate between the K segments a CTA owns, so
 //     the MMA warp starts the next tile while the epilogue drains the last;
-//   - a tile whose K range spans several CTAs is finished by the last CTA to
-//     arrive, which adds the fp32 partials in segment (K) order.
+//   - a tile whose K range spans several CTAs: each contributor publishes its
+//     fp32 partial (L2) and goes on streaming; after its last unit it waits
+//     (bounded) for the tile's other partials and finishes its own slice of
+//     the tile's packed rows, adding the partials in segment (K) order, so
+//     the reduction is spread over the contributors instead of one CTA;
+//   - all row chunks of a call (BN_MAX packed rows each) run inside the same
+//     grid of at most one CTA per SM, so the contributors of a tile are
+//     resident together.
 // The partition depends only on the weight shape and the SM count, never on
 // Q, so a row's result does not depend on how many rows share the call.
 //
@@ -40,14 +46,19 @@ constexpr int BOX_ROWS = 16;
 constexpr int MAX_STAGES = 12;
 constexpr int SMEM_BYTES = 200 * 1024;
 constexpr int NTHREADS = 192;             // producer, MMA, 4 epilogue warps
+constexpr int MAX_CHUNKS = 4;
+constexpr uint32_t TMEM_COLS = 512;       // two accumulators of up to 256 fp32 columns             // packed rows per launch <= MAX_CHUNKS * BN_MAX
 
 struct TcParams {
     LaHdr* hdr;
     int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg, max_stages;
     void* out; int ldo;
     float* logits; int ld_logits;
-    float* ws; int* counters;
+    float* ws; unsigned long long* ctr;   // this GEMM's split-tile arrival counters
     float* part_v; int* part_i; int part_stride;
+    int max_chunks;
+    // L2 prefetch of the next GEMM's first units (see la_launch_gemm_tc)
+    int pf_units, pf_n_tiles, pf_k_tiles, pf_seg_tiles, pf_swiglu;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -76,6 +87,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     for (uint32_t i = 0; i < LA_SPIN_LIMIT; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* tm, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm), "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y,
@@ -129,8 +145,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// named barrier among the four epilogue warps
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barrier among the four epilogue warps; the warp reconverges first
+// (bar.sync is warp-aligned: a warp with lanes still in a divergent branch
+// must not reach it)
+__device__ __forceinline__ void epi_sync() {
+    __syncwarp();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
@@ -139,18 +160,50 @@ __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
 // the CTA that owns unit x when T units are split evenly over P CTAs
 __device__ __forceinline__ int cta_of(long long x, long long T, int P) { return (int)(((x + 1) * P - 1) / T); }
 
+// Sum of the partials of columns cb .. cb+NC-1 (clamped to c_hi - 1) over the
+// nseg segments, in segment order.  All NS x NC loads of a group are issued
+// before the first add; clamped indices keep every load on a written entry.
+template <int NS, int NC>
+__device__ __forceinline__ void sum_segments(const float* src0, size_t seg_stride, int nseg, int cb, int c_hi,
+                                             float (&dst)[NC]) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) dst[j] = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += NS) {
+        float t[NS][NC];
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const float* src = src0 + (size_t)min(s0 + k, nseg - 1) * seg_stride;
+#pragma unroll
+            for (int j = 0; j < NC; ++j) t[k][j] = __ldcg(src + (size_t)min(cb + j, c_hi - 1) * BM);
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+            if (s0 + k < nseg) {
+#pragma unroll
+                for (int j = 0; j < NC; ++j) dst[j] = __fadd_rn(dst[j], t[k][j]);
+            }
+    }
+}
+
+// bounded wait until a split-tile arrival counter reaches `target` (acquire)
+__device__ __forceinline__ bool spin_until64(const unsigned long long* ctr, unsigned long long target) {
+    for (uint32_t i = 0; i < LA_SPIN_LIMIT; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        __nanosleep(32);
+    }
+    return false;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
           const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
-          const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB256, TcParams p) {
+          const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB256,
+          const __grid_constant__ CUtensorMap pfA, const __grid_constant__ CUtensorMap pfA2,
+          const __grid_constant__ CUtensorMap pfA3, TcParams p) {
     LaHdr* h = p.hdr;
-    if (h->err != 0 || (p.sel != SEL_PREFILL && h->done != 0)) return;
-    const int rows = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
-    const int q0 = blockIdx.y * BN_MAX;
-    if (q0 >= rows) return;
-    const int nq = min(BN_MAX, rows - q0);
-    const int BN = (nq + 15) & ~15;
     const int swiglu = (p.mode == GEMM_SWIGLU);
     const int nA = swiglu ? 2 : 1;
     const long long T = (long long)p.n_tiles * p.k_tiles;
@@ -160,126 +213,222 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (c >= P) return;
     const long long u_begin = T * c / P, u_end = T * (c + 1) / P;
     const int n_units = (int)(u_end - u_begin);
-    if (n_units <= 0) return;
+    const int tile0 = (int)(u_begin / p.k_tiles), kt0 = (int)(u_begin % p.k_tiles);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // [barriers][flags][reduction scratch 8 KB][stages ...]
+    // [barriers][flags][reduction scratch 8 KB][weight ring][activation ring]
     const uint32_t bar_full = base;                        // MAX_STAGES x 8 B
     const uint32_t bar_empty = base + 8 * MAX_STAGES;
     const uint32_t bar_accf = base + 16 * MAX_STAGES;      // 2 x 8 B
     const uint32_t bar_acce = bar_accf + 16;               // 2 x 8 B
     uint32_t* tmem_slot = (uint32_t*)(gbase + 16 * MAX_STAGES + 32);
     int* s_flag = (int*)(gbase + 16 * MAX_STAGES + 40);
+    int* s_rows = (int*)(gbase + 16 * MAX_STAGES + 44);    // header broadcast: rows, or -1 to skip the call
     float* rv = (float*)(gbase + 1024);                    // [4][BN_MAX] argmax values
     int* ri = (int*)(gbase + 1024 + 4 * BN_MAX * 4);       // [4][BN_MAX] argmax ids
     const uint32_t stage0 = base + 1024 + 8192;
-    const uint32_t b_bytes = (uint32_t)BN * ROW_BYTES;
-    const uint32_t stage_bytes = (((uint32_t)nA * A_BYTES + b_bytes) + 1023u) & ~1023u;
-    int ns = (int)((SMEM_BYTES - 1024 - 8192) / stage_bytes);
-    ns = ns > p.max_stages ? p.max_stages : ns;
-    const uint32_t tx_bytes = (uint32_t)nA * A_BYTES + b_bytes;
-    const int acc_cols = nA * BN;                          // one accumulator: nA x BN fp32 columns
-    const int nbuf = (2 * acc_cols <= 512) ? 2 : 1;
-    uint32_t ncols = 32;
-    while (ncols < (uint32_t)(nbuf * acc_cols)) ncols <<= 1;
-
-    if (warp == 0 && lane == 0) {
-        for (int s = 0; s < ns; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar_accf + 8 * b, 1);
-            mbar_init(bar_acce + 8 * b, 1);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t a_stage = (uint32_t)nA * A_BYTES;
+    // weight tiles issued before the header is read (they depend on nothing);
+    // every stage layout below has at least this many stages
+    const int n_pre = min(swiglu ? 2 : 3, n_units);
 
     if (warp == 0) {
+        int hdr_rows = 0;
         if (lane == 0) {
-            // TMA producer: every unit of this CTA, in order
-            uint64_t pol_w, pol_x;
+            // header words: loaded now, first used after the first weight loads are issued
+            const int h_err = h->err, h_done = h->done;
+            const int h_n = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
+            for (int s = 0; s < MAX_STAGES; ++s) {
+                mbar_init(bar_full + 8 * s, 1);
+                mbar_init(bar_empty + 8 * s, 1);
+            }
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar_accf + 8 * b, 1);
+                mbar_init(bar_acce + 8 * b, 1);
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            uint64_t pol_w;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
-            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-            bool ok = true;
-            for (int it = 0; it < n_units && ok; ++it) {
-                const long long u = u_begin + it;
-                const int tile = (int)(u / p.k_tiles), kt = (int)(u % p.k_tiles);
-                const int s = it % ns, r = it / ns;
-                if (r > 0 && !mbar_wait(bar_empty + 8 * s, (uint32_t)((r - 1) & 1))) { ok = false; break; }
-                const uint32_t st = stage0 + (uint32_t)s * stage_bytes;
-                const uint32_t fb = bar_full + 8 * s;
-                mbar_expect_tx(fb, tx_bytes);
-                const CUtensorMap* wmap = &tmA;
-                int wrow = tile * BM;
-                if (p.seg_tiles > 0) {
-                    const int seg = tile / p.seg_tiles;
-                    wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
-                    wrow = (tile - seg * p.seg_tiles) * BM;
-                }
-                const int kx = kt * BK;
-                tma_load_2d(st, wmap, fb, kx, wrow, pol_w);
-                if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kx, wrow, pol_w);
-                // activation rows in at most four boxes (256/128/64/32/16 rows)
-                const uint32_t bst = st + (uint32_t)nA * A_BYTES;
-                int rr = 0;
-                while (rr < BN) {
-                    const int left = BN - rr;
-                    const CUtensorMap* bm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128 : left >= 64 ? &tmB64
-                                          : left >= 32 ? &tmB32 : &tmB;
-                    const int hgt = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : left >= 32 ? 32 : 16;
-                    tma_load_2d(bst + (uint32_t)rr * ROW_BYTES, bm, fb, kx, q0 + rr, pol_x);
-                    rr += hgt;
+            {
+                int tile = tile0, kt = kt0;
+                for (int i = 0; i < n_pre; ++i) {
+                    const uint32_t fb = bar_full + 8 * i, st = stage0 + (uint32_t)i * a_stage;
+                    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(a_stage) : "memory");
+                    const CUtensorMap* wmap = &tmA;
+                    int wrow = tile * BM;
+                    if (p.seg_tiles > 0) {
+                        const int seg = tile / p.seg_tiles;
+                        wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
+                        wrow = (tile - seg * p.seg_tiles) * BM;
+                    }
+                    tma_load_2d(st, wmap, fb, kt * BK, wrow, pol_w);
+                    if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kt * BK, wrow, pol_w);
+                    if (++kt == p.k_tiles) { kt = 0; ++tile; }
                 }
             }
-            if (!ok) la_set_err(h, LA_ETIMEOUT);
+            int rows = h_n;
+            if (h_err != 0 || (p.sel != SEL_PREFILL && h_done != 0) || rows <= 0) rows = -1;
+            if (rows > 0 && (rows + BN_MAX - 1) / BN_MAX > p.max_chunks) {
+                if (blockIdx.x == 0) la_set_err(h, LA_EDEVICE);
+                rows = -1;
+            }
+            *s_rows = rows;
+            hdr_rows = rows;
         }
-    } else if (warp == 1) {
+        __syncwarp();
+        asm volatile("bar.arrive 2, 192;" ::: "memory");
+        hdr_rows = __shfl_sync(0xffffffffu, hdr_rows, 0);
         if (lane == 0) {
+            const int rows = hdr_rows;
+            if (rows < 0) {
+                // skipped call: let the weight loads already issued land before exiting
+                for (int i = 0; i < n_pre; ++i) {
+                    mbar_arrive(bar_full + 8 * i);
+                    mbar_wait(bar_full + 8 * i, 0);
+                }
+            } else {
+                // TMA producer: every (chunk, unit) of this CTA, in order
+                const int n_chunks = (rows + BN_MAX - 1) / BN_MAX;
+                const int BN0 = (min(BN_MAX, rows) + 15) & ~15;
+                const uint32_t b_stage = (uint32_t)BN0 * ROW_BYTES;
+                int ns = (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage));
+                ns = ns > p.max_stages ? p.max_stages : ns;
+                const uint32_t bbase = stage0 + (uint32_t)ns * a_stage;
+                uint64_t pol_w, pol_x;
+                asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+                asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+                bool ok = true;
+                int y = 0, iu = 0, tile = tile0, kt = kt0, s = 0, r = 0;
+                const int n_items = n_chunks * n_units;
+                for (int it = 0; it < n_items; ++it) {
+                    const int q0 = y * BN_MAX;
+                    const int BN = (min(BN_MAX, rows - q0) + 15) & ~15;
+                    if (r > 0 && !mbar_wait(bar_empty + 8 * s, (uint32_t)((r - 1) & 1))) { ok = false; break; }
+                    const uint32_t st = stage0 + (uint32_t)s * a_stage;
+                    const uint32_t bst = bbase + (uint32_t)s * b_stage;
+                    const uint32_t fb = bar_full + 8 * s;
+                    const int kx = kt * BK;
+                    if (it < n_pre) {
+                        // the weight tile is already on its way
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                                     "r"((uint32_t)BN * ROW_BYTES)
+                                     : "memory");
+                    } else {
+                        mbar_expect_tx(fb, a_stage + (uint32_t)BN * ROW_BYTES);
+                        const CUtensorMap* wmap = &tmA;
+                        int wrow = tile * BM;
+                        if (p.seg_tiles > 0) {
+                            const int seg = tile / p.seg_tiles;
+                            wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
+                            wrow = (tile - seg * p.seg_tiles) * BM;
+                        }
+                        tma_load_2d(st, wmap, fb, kx, wrow, pol_w);
+                        if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kx, wrow, pol_w);
+                    }
+                    // activation rows in at most four boxes (256/128/64/32/16 rows)
+                    int rr = 0;
+                    while (rr < BN) {
+                        const int left = BN - rr;
+                        const CUtensorMap* bm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128 : left >= 64 ? &tmB64
+                                              : left >= 32 ? &tmB32 : &tmB;
+                        const int hgt = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : left >= 32 ? 32 : 16;
+                        tma_load_2d(bst + (uint32_t)rr * ROW_BYTES, bm, fb, kx, q0 + rr, pol_x);
+                        rr += hgt;
+                    }
+                    ++iu;
+                    if (++kt == p.k_tiles) { kt = 0; ++tile; }
+                    if (iu == n_units) { iu = 0; ++y; tile = tile0; kt = kt0; }
+                    if (++s == ns) { s = 0; ++r; }
+                }
+                if (!ok) la_set_err(h, LA_ETIMEOUT);
+                // While this grid drains, pull the first units of the next GEMM's
+                // weights (the ones the same CTA index streams first) into L2.
+                if (ok && p.pf_units > 0) {
+                    const long long T2 = (long long)p.pf_n_tiles * p.pf_k_tiles;
+                    const int P2 = (int)(T2 < (long long)p.n_cta ? T2 : (long long)p.n_cta);
+                    if (c < P2) {
+                        const long long v0 = T2 * c / P2, v1 = T2 * (c + 1) / P2;
+                        const int npf = (int)((long long)p.pf_units < v1 - v0 ? (long long)p.pf_units : v1 - v0);
+                        int ptile = (int)(v0 / p.pf_k_tiles), pkt = (int)(v0 % p.pf_k_tiles);
+                        for (int i = 0; i < npf; ++i) {
+                            const CUtensorMap* m = &pfA;
+                            int row = ptile * BM;
+                            if (p.pf_seg_tiles > 0) {
+                                const int seg = ptile / p.pf_seg_tiles;
+                                m = seg == 0 ? &pfA : (seg == 1 ? &pfA2 : &pfA3);
+                                row = (ptile - seg * p.pf_seg_tiles) * BM;
+                            }
+                            tma_prefetch_l2(m, pkt * BK, row);
+                            if (p.pf_swiglu) tma_prefetch_l2(&pfA2, pkt * BK, row);
+                            if (++pkt == p.pf_k_tiles) { pkt = 0; ++ptile; }
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        if (warp == 1) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+        tc_fence_before();
+        asm volatile("bar.sync 2, 192;" ::: "memory");
+        tc_fence_after();
+    }
+    const int rows = *s_rows;
+    const uint32_t tmem = *tmem_slot;
+    const int n_chunks = rows > 0 ? (rows + BN_MAX - 1) / BN_MAX : 0;
+    const int BN0 = rows > 0 ? (min(BN_MAX, rows) + 15) & ~15 : 16;
+    const uint32_t b_stage = (uint32_t)BN0 * ROW_BYTES;
+    int ns = (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage));
+    ns = ns > p.max_stages ? p.max_stages : ns;
+    const uint32_t bbase = stage0 + (uint32_t)ns * a_stage;
+    const int acc_cols = nA * BN0;                         // one accumulator: nA x BN fp32 columns
+    const int nbuf = (2 * acc_cols <= TMEM_COLS) ? 2 : 1;
+
+    if (warp == 0) {
+        // producer (above)
+    } else if (warp == 1) {
+        if (lane == 0 && n_chunks > 0) {
             // MMA issuer: one accumulator per K segment, alternating buffers
-            const uint32_t id = idesc_bf16(BN);
             bool ok = true;
-            int seg_i = 0;
-            int it = 0;
-            while (it < n_units && ok) {
-                const long long u = u_begin + it;
-                const int tile = (int)(u / p.k_tiles);
-                const int seg_end = min(n_units, (int)((long long)(tile + 1) * p.k_tiles - u_begin));
-                const int b = seg_i % nbuf, ub = seg_i / nbuf;
+            int y = 0, iu = 0, tile = tile0, kt = kt0, s = 0, r = 0, seg_i = 0;
+            while (y < n_chunks && ok) {
+                const int seg_len = min(n_units - iu, p.k_tiles - kt);
+                const int BN = (min(BN_MAX, rows - y * BN_MAX) + 15) & ~15;
+                const uint32_t id = idesc_bf16(BN);
+                const int b = nbuf == 2 ? (seg_i & 1) : 0, ub = nbuf == 2 ? (seg_i >> 1) : seg_i;
                 if (ub > 0 && !mbar_wait(bar_acce + 8 * b, (uint32_t)((ub - 1) & 1))) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t acc = tmem + (uint32_t)(b * acc_cols);
-                for (int first = 1; it < seg_end; ++it, first = 0) {
-                    const int s = it % ns, r = it / ns;
+                for (int j = 0; j < seg_len; ++j) {
                     if (!mbar_wait(bar_full + 8 * s, (uint32_t)(r & 1))) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t st = stage0 + (uint32_t)s * stage_bytes;
-                    const uint32_t bst = st + (uint32_t)nA * A_BYTES;
+                    const uint32_t st = stage0 + (uint32_t)s * a_stage;
+                    const uint32_t bst = bbase + (uint32_t)s * b_stage;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t bdesc = sdesc(bst + kk * 32);
-                        const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+                        const uint32_t accum = (j == 0 && kk == 0) ? 0u : 1u;
                         mma_bf16(acc, sdesc(st + kk * 32), bdesc, id, accum);
                         if (swiglu) mma_bf16(acc + (uint32_t)BN, sdesc(st + A_BYTES + kk * 32), bdesc, id, accum);
                     }
                     mma_commit(bar_empty + 8 * s);
+                    if (++s == ns) { s = 0; ++r; }
                 }
+                if (!ok) break;
                 mma_commit(bar_accf + 8 * b);
                 ++seg_i;
+                iu += seg_len;
+                kt += seg_len;
+                if (kt == p.k_tiles) { kt = 0; ++tile; }
+                if (iu == n_units) { iu = 0; ++y; tile = tile0; kt = kt0; }
             }
             if (!ok) la_set_err(h, LA_ETIMEOUT);
         }
@@ -288,16 +437,91 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const int quarter = warp & 3;
         const int et = quarter * 32 + lane;                // 0..127: the weight row within the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const size_t plane = (size_t)BN_MAX * BM;          // floats of one accumulator in a partial record
+
+        // Results of packed rows q0 + cb .. q0 + cb + ncol - 1 for weight row
+        // tile * BM + et (v: the accumulator, w2: the SwiGLU up accumulator).
+        // Loads of a group are issued together; lanes of a warp hold 32
+        // consecutive weight rows, so every access is one coalesced line.
+        auto emit_group = [&](int tile, int q0, int cb, int ncol, const float (&v)[16], const float (&w2)[16],
+                              bool ok) {
+            const int n = tile * BM + et;
+            if (p.mode == GEMM_STORE) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (ok && j < ncol)
+                        ((__nv_bfloat16*)p.out)[(size_t)(q0 + cb + j) * p.ldo + n] = __float2bfloat16_rn(v[j]);
+            } else if (p.mode == GEMM_RESID) {
+                float old[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    old[j] = ((const float*)p.out)[(size_t)(q0 + cb + min(j, ncol - 1)) * p.ldo + n];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (ok && j < ncol) ((float*)p.out)[(size_t)(q0 + cb + j) * p.ldo + n] = old[j] + v[j];
+            } else if (p.mode == GEMM_SWIGLU) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (ok && j < ncol)
+                        ((__nv_bfloat16*)p.out)[(size_t)(q0 + cb + j) * p.ldo + n] =
+                            __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * w2[j]);
+            } else {   // logits + argmax partials over this tile's 128 vocab entries
+                if (ok && p.logits) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < ncol) p.logits[(size_t)(q0 + cb + j) * p.ld_logits + n] = v[j];
+                }
+                // 16 independent warp reductions, interleaved level by level
+                float bv[16];
+                int bi[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) { bv[j] = v[j]; bi[j] = n; }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float vv = __shfl_xor_sync(0xffffffffu, bv[j], o2);
+                        const int ii = __shfl_xor_sync(0xffffffffu, bi[j], o2);
+                        better(bv[j], bi[j], vv, ii);
+                    }
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < ncol) { rv[quarter * BN_MAX + cb + j] = bv[j]; ri[quarter * BN_MAX + cb + j] = bi[j]; }
+                }
+            }
+        };
+        // logits mode: combine the four lane quarters' argmax of columns [c_lo, c_hi)
+        auto argmax_out = [&](int tile, int q0, int c_lo, int c_hi, bool ok) {
+            if (p.mode != GEMM_LOGITS) return;
+            epi_sync();
+            for (int cc = c_lo + et; cc < c_hi; cc += 128) {
+                float bv = rv[cc];
+                int bi = ri[cc];
+                for (int w = 1; w < 4; ++w) better(bv, bi, rv[w * BN_MAX + cc], ri[w * BN_MAX + cc]);
+                if (ok) {
+                    p.part_v[(size_t)tile * p.part_stride + q0 + cc] = bv;
+                    p.part_i[(size_t)tile * p.part_stride + q0 + cc] = bi;
+                }
+            }
+            epi_sync();
+        };
+
+        // split tiles this CTA contributed to, reduced after its last unit
+        int d_tile[2 * MAX_CHUNKS], d_sg[2 * MAX_CHUNKS], d_nseg[2 * MAX_CHUNKS], d_y[2 * MAX_CHUNKS];
+        unsigned long long d_target[2 * MAX_CHUNKS];         // the arrival count that completes the tile (leader)
+        int nd = 0;
         int seg_i = 0;
-        int it = 0;
         bool alive = true;
-        while (it < n_units) {
-            const long long u = u_begin + it;
-            const int tile = (int)(u / p.k_tiles);
+        int y = 0, iu = 0, tile = tile0, kt = kt0;
+        while (y < n_chunks) {
+            const int seg_len = min(n_units - iu, p.k_tiles - kt);
+            const int q0 = y * BN_MAX;
+            const int nq = min(BN_MAX, rows - q0);
+            const int BN = (nq + 15) & ~15;
             const long long tile_u0 = (long long)tile * p.k_tiles, tile_u1 = tile_u0 + p.k_tiles;
-            const int seg_end = min(n_units, (int)(tile_u1 - u_begin));
-            it = seg_end;
-            const int b = seg_i % nbuf, ub = seg_i / nbuf;
+            const int b = nbuf == 2 ? (seg_i & 1) : 0, ub = nbuf == 2 ? (seg_i >> 1) : seg_i;
             ++seg_i;
             const bool got = alive && mbar_wait(bar_accf + 8 * b, (uint32_t)(ub & 1));
             if (!got && alive) { alive = false; la_set_err(h, LA_ETIMEOUT); }
@@ -305,123 +529,105 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint32_t acc = tmem + lane_base + (uint32_t)(b * acc_cols);
             const int c_first = cta_of(tile_u0, T, P), c_last = cta_of(tile_u1 - 1, T, P);
             const int nseg = c_last - c_first + 1;
-            const int n = tile * BM + et;
-            const float* wst = nullptr;
             if (nseg > 1) {
-                // publish this segment's partial; the last CTA to arrive finishes the tile
+                // publish this segment's partial (valid columns only) and free the accumulator
                 const int sg = c - c_first;
-                float* wsb = p.ws + (((size_t)(tile + (size_t)blockIdx.y * p.n_tiles) * p.max_seg + sg) * nA) *
-                                        (size_t)(BN_MAX * BM);
-                for (int c0 = 0; c0 < BN; c0 += 16) {
+                const size_t slot = (size_t)tile + (size_t)y * p.n_tiles;
+                float* wsb = p.ws + ((slot * p.max_seg + sg) * nA) * plane;
+                for (int c0 = 0; c0 < nq; c0 += 16) {
                     float v[16];
                     tmem_ld16(acc + c0, v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) __stcg(wsb + (size_t)(c0 + j) * BM + et, got ? v[j] : 0.f);
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < nq) __stcg(wsb + (size_t)(c0 + j) * BM + et, got ? v[j] : 0.f);
                     if (swiglu) {
                         tmem_ld16(acc + BN + c0, v);
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            __stcg(wsb + (size_t)(BN_MAX + c0 + j) * BM + et, got ? v[j] : 0.f);
+                            if (c0 + j < nq) __stcg(wsb + plane + (size_t)(c0 + j) * BM + et, got ? v[j] : 0.f);
                     }
                 }
                 tc_fence_before();
-                __threadfence();
                 epi_sync();
                 if (quarter == 0 && lane == 0) {
-                    mbar_arrive(bar_acce + 8 * b);      // the accumulator is free again
-                    int* ctr = p.counters + tile + blockIdx.y * p.n_tiles;
-                    const int old = atomicAdd(ctr, 1);
-                    const int last = (old == nseg - 1);
-                    if (last) *ctr = 0;
-                    *s_flag = last;
+                    mbar_arrive(bar_acce + 8 * b);
+                    // arrival (release: the CTA's partial stores, ordered before it by
+                    // the barrier, are visible to whoever acquires the count).  The
+                    // count only grows: arrival k completes launch k / nseg.
+                    unsigned long long old;
+                    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;"
+                                 : "=l"(old)
+                                 : "l"(p.ctr + slot)
+                                 : "memory");
+                    d_target[nd] = (old / (unsigned long long)nseg + 1ull) * (unsigned long long)nseg;
                 }
-                epi_sync();
-                const bool final_here = (*s_flag != 0);
-                epi_sync();                              // everyone read the flag before it is reused
-                if (!final_here) continue;
-                __threadfence();
-                wst = p.ws + ((size_t)(tile + (size_t)blockIdx.y * p.n_tiles) * p.max_seg * nA) * (size_t)(BN_MAX * BM);
-            }
-            // final epilogue, 16 packed rows at a time
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-                float v[16], w2[16];
-                if (nseg > 1) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) { v[j] = 0.f; w2[j] = 0.f; }
-                    // segments four at a time: 64 loads in flight, sums kept in segment order
-                    for (int pl = 0; pl < nA; ++pl) {
-                        float* dst = pl ? w2 : v;
-                        for (int sg0 = 0; sg0 < nseg; sg0 += 4) {
-                            float t1[4][16];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const float* w = wst + (size_t)(sg0 + k) * nA * (BN_MAX * BM) +
-                                                 (size_t)(pl * BN_MAX + c0) * BM + et;
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) t1[k][j] = (sg0 + k < nseg) ? __ldcg(w + (size_t)j * BM) : 0.f;
-                            }
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                if (sg0 + k < nseg) {
-#pragma unroll
-                                    for (int j = 0; j < 16; ++j) dst[j] = __fadd_rn(dst[j], t1[k][j]);
-                                }
-                        }
-                    }
-                } else {
+                d_tile[nd] = tile; d_sg[nd] = sg; d_nseg[nd] = nseg; d_y[nd] = y;
+                ++nd;
+            } else {
+                // a whole tile: straight from TMEM
+                for (int c0 = 0; c0 < nq; c0 += 16) {
+                    float v[16], w2[16];
                     tmem_ld16(acc + c0, v);
                     if (swiglu) tmem_ld16(acc + BN + c0, w2);
+                    emit_group(tile, q0, c0, min(16, nq - c0), v, w2, got);
                 }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int q = q0 + c0 + j;
-                    const bool in = got && q < rows;
-                    const size_t o = (size_t)q * p.ldo + n;
-                    if (p.mode == GEMM_STORE) {
-                        if (in) ((__nv_bfloat16*)p.out)[o] = __float2bfloat16_rn(v[j]);
-                    } else if (p.mode == GEMM_RESID) {
-                        if (in) ((float*)p.out)[o] += v[j];
-                    } else if (p.mode == GEMM_SWIGLU) {
-                        if (in) ((__nv_bfloat16*)p.out)[o] = __float2bfloat16_rn(v[j] / (1.0f + expf(-v[j])) * w2[j]);
-                    } else {   // logits + argmax partials over this tile's 128 vocab entries
-                        if (in && p.logits) p.logits[(size_t)q * p.ld_logits + n] = v[j];
-                        float bv = v[j];
-                        int bi = n;
-#pragma unroll
-                        for (int o2 = 16; o2 > 0; o2 >>= 1) {
-                            const float vv = __shfl_xor_sync(0xffffffffu, bv, o2);
-                            const int ii = __shfl_xor_sync(0xffffffffu, bi, o2);
-                            better(bv, bi, vv, ii);
-                        }
-                        if (lane == 0) { rv[quarter * BN_MAX + c0 + j] = bv; ri[quarter * BN_MAX + c0 + j] = bi; }
-                    }
-                }
-            }
-            if (nseg == 1) {
                 tc_fence_before();
                 epi_sync();
                 if (quarter == 0 && lane == 0) mbar_arrive(bar_acce + 8 * b);
+                argmax_out(tile, q0, 0, nq, got);
             }
-            if (p.mode == GEMM_LOGITS) {
-                epi_sync();
-                for (int cc = et; cc < nq; cc += 128) {
-                    float bv = rv[cc];
-                    int bi = ri[cc];
-                    for (int w = 1; w < 4; ++w) better(bv, bi, rv[w * BN_MAX + cc], ri[w * BN_MAX + cc]);
-                    if (got) {
-                        p.part_v[(size_t)tile * p.part_stride + q0 + cc] = bv;
-                        p.part_i[(size_t)tile * p.part_stride + q0 + cc] = bi;
-                    }
+            iu += seg_len;
+            kt += seg_len;
+            if (kt == p.k_tiles) { kt = 0; ++tile; }
+            if (iu == n_units) { iu = 0; ++y; tile = tile0; kt = kt0; }
+        }
+
+        // Split tiles: once all nseg partials of this launch have arrived,
+        // contributor sg sums columns [nq*sg/nseg, nq*(sg+1)/nseg) over the
+        // segments in K order.
+        for (int d = 0; d < nd; ++d) {
+            const int tile = d_tile[d], sg = d_sg[d], nseg = d_nseg[d], y = d_y[d];
+            const int q0 = y * BN_MAX;
+            const int nq = min(BN_MAX, rows - q0);
+            const size_t slot = (size_t)tile + (size_t)y * p.n_tiles;
+            if (quarter == 0 && lane == 0) {
+                bool ok = alive && spin_until64(p.ctr + slot, d_target[d]);
+                if (!ok && alive) la_set_err(h, LA_ETIMEOUT);
+                *s_flag = ok ? 1 : 0;
+            }
+            epi_sync();
+            const bool ok = *s_flag != 0;
+            alive = alive && ok;
+            const int c_lo = nq * sg / nseg, c_hi = nq * (sg + 1) / nseg;
+            const float* wst = p.ws + (slot * p.max_seg * nA) * plane + et;
+            const size_t seg_stride = (size_t)nA * plane;
+            for (int cb = c_lo; cb < c_hi; cb += 16) {
+                float v[16], w2[16];
+                if (nseg == 2) {
+                    sum_segments<2, 16>(wst, seg_stride, nseg, cb, c_hi, v);
+                    if (swiglu) sum_segments<2, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
+                } else if (nseg == 3) {
+                    sum_segments<3, 16>(wst, seg_stride, nseg, cb, c_hi, v);
+                    if (swiglu) sum_segments<3, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
+                } else {
+                    sum_segments<4, 16>(wst, seg_stride, nseg, cb, c_hi, v);
+                    if (swiglu) sum_segments<4, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
                 }
-                epi_sync();
+                emit_group(tile, q0, cb, min(16, c_hi - cb), v, w2, ok);
             }
+            argmax_out(tile, q0, c_lo, c_hi, ok);
+            // s_flag is rewritten by the next tile's leader only after this barrier
+            epi_sync();
         }
     }
+    // teardown: every warp reconverges (lane 0 of the producer and MMA warps
+    // may still be finishing) before the CTA-wide barrier that frees TMEM
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
 }
 
@@ -459,6 +665,19 @@ int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K) {
     return 0;
 }
 
+// Weight tiles of the next GEMM each CTA prefetches into L2 (LA_TC_PF
+// overrides the default for tuning runs).
+int la_tc_pf_units() {
+    static int pf = -1;
+    if (pf < 0) {
+        const char* e = getenv("LA_TC_PF");
+        pf = e ? atoi(e) : 0;
+        if (pf < 0) pf = 0;
+        if (pf > 4096) pf = 4096;
+    }
+    return pf;
+}
+
 // CTAs of the persistent kernel: one per SM of the current device
 int la_tc_ctas() {
     int dev = 0, sms = 0;
@@ -493,7 +712,7 @@ void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t*
     const int nA = mode == GEMM_SWIGLU ? 2 : 1;
     const int max_seg = la_tc_max_segments(tiles, k_tiles, n_cta);
     *ws_floats = (size_t)tiles * n_y * max_seg * nA * BN_MAX * BM;
-    *n_counters = (size_t)tiles * n_y;
+    *n_counters = (size_t)LA_TC_CTR_PER_TILE * tiles * n_y;
 }
 
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel) {
@@ -518,7 +737,7 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     if (stages < 0) {
         const char* e = getenv("LA_TC_STAGES");   // pipeline-depth override for tuning runs
         stages = e ? atoi(e) : MAX_STAGES;
-        if (stages < 2) stages = 2;
+        if (stages < 3) stages = 3;   // at least the weight tiles issued before the header
         if (stages > MAX_STAGES) stages = MAX_STAGES;
     }
     p.max_stages = stages;
@@ -527,12 +746,24 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.logits = g.logits;
     p.ld_logits = g.ld_logits;
     p.ws = w.ws;
-    p.counters = w.counters;
+    p.ctr = (unsigned long long*)w.counters + g.ctr_off;
     p.part_v = w.part_v;
     p.part_i = w.part_i;
     p.part_stride = w.part_stride;
-    dim3 grid(g.n_cta, (g.rows_cap + BN_MAX - 1) / BN_MAX);
+    p.max_chunks = (g.rows_cap + BN_MAX - 1) / BN_MAX;
+    const TcGemm* nx = (g.pf_units > 0) ? g.next : nullptr;
+    p.pf_units = nx ? g.pf_units : 0;
+    p.pf_n_tiles = nx ? nx->Nout / BM : 0;
+    p.pf_k_tiles = nx ? nx->K / BK : 0;
+    p.pf_seg_tiles = nx ? nx->seg_tiles : 0;
+    p.pf_swiglu = nx ? (nx->mode == GEMM_SWIGLU) : 0;
+    const CUtensorMap& pf1 = nx ? nx->tmA : g.tmA;
+    const CUtensorMap& pf2 = nx ? nx->tmA2 : g.tmA2;
+    const CUtensorMap& pf3 = nx ? nx->tmA3 : g.tmA3;
+    if (p.max_chunks < 1 || p.max_chunks > MAX_CHUNKS) return cudaErrorInvalidValue;
+    const long long T = (long long)p.n_tiles * p.k_tiles;
+    dim3 grid((unsigned)std::min<long long>(g.n_cta, T), 1);
     k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES + 1024, st>>>(g.tmA, g.tmA2, g.tmA3, g.tmB, g.tmB32, g.tmB64, g.tmB128,
-                                                         g.tmB256, p);
+                                                         g.tmB256, pf1, pf2, pf3, p);
     return cudaGetLastError();
 }

@@ -57,11 +57,16 @@ struct TcGemm {
     int max_seg;          // largest number of CTAs sharing one tile's K range
     void* out; int ldo;
     float* logits; int ld_logits;   // GEMM_LOGITS: optional fp32 logits
+    // the GEMM launched after this one: each CTA prefetches the first pf_units
+    // (128 x 64) weight tiles of its share of `next` into L2 while it drains
+    const TcGemm* next; int pf_units;
+    int ctr_off;          // first split-tile counter of this GEMM (counters are per GEMM)
 };
+#define LA_TC_CTR_PER_TILE 2   // ints per split-tile arrival counter (one 64-bit word)
 struct TcWork {
     float* ws;            // partial tiles of K ranges shared by several CTAs
     size_t ws_floats;
-    int* counters;        // per (tile, q-chunk) arrival counters, zero-initialised
+    int* counters;        // LA_TC_CTR_PER_TILE ints per (GEMM, tile, q-chunk), zero-initialised, 8-byte aligned
     int n_counters;
     float* part_v;        // argmax partials [n_tiles][part_stride]
     int* part_i;
@@ -73,6 +78,7 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
 int la_tc_ctas();
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
 cudaError_t la_tc_prepare_device();
+int la_tc_pf_units();
 void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t* ws_floats, size_t* n_counters);
 
 // exact sampling verifier (one CTA): reads the needed rows' fp32 logits and

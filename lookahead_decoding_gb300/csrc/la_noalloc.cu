@@ -76,7 +76,7 @@ extern "C" {
 int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, const void* x, int rows, void* y,
                     void* stream) {
     if (mode < GEMM_STORE || mode > GEMM_SWIGLU || !w || !x || !y || n_out < 128 || n_out % 128 || K < 64 ||
-        K % 64 || rows < 1 || rows > (1 << 20) || !aligned16(w) || !aligned16(x) || ((uintptr_t)y & 3u))
+        K % 64 || rows < 1 || rows > 1024 || !aligned16(w) || !aligned16(x) || ((uintptr_t)y & 3u))
         return LA_EINVAL;
     if (mode == GEMM_SWIGLU && (!w2 || !aligned16(w2))) return LA_EINVAL;
     const int n_cta = la_tc_ctas();
