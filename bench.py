@@ -48,6 +48,26 @@ def algorithmic_bytes_per_call(cfg, K_in: float, Q: float) -> float:
     return weights + kv_read + kv_write
 
 
+def gemm_bytes_per_call(cfg, Q: float, need_rows: float) -> float:
+    """Algorithmic bytes of the tensor-core GEMMs of one packed call (bf16
+    weights read once, bf16 activations read once, outputs written once;
+    the residual GEMMs read and write the fp32 residual rows)."""
+    d, F, V, L = cfg.d_model, cfg.d_ffn, cfg.vocab, cfg.n_layers
+    HD = cfg.n_heads * cfg.head_dim
+    per_layer = ((3 * HD * d) * 2 + Q * d * 2 + Q * 3 * HD * 2          # QKV: store bf16
+                 + (d * HD) * 2 + Q * HD * 2 + Q * d * 8                # O: residual fp32 read + write
+                 + (2 * F * d) * 2 + Q * d * 2 + Q * F * 2              # gate/up + SwiGLU: store bf16
+                 + (d * F) * 2 + Q * F * 2 + Q * d * 8)                 # down: residual
+    head = V * d * 2 + need_rows * d * 2 + need_rows * (V // 128) * 8   # argmax partials (value, id)
+    return L * per_layer + head
+
+
+# DRAM bytes (read + write) of the GEMM launches of one packed call (32 layers
+# x (QKV + O + gate/up + down) + LM head), from the ncu captures of the current
+# kernel at 60 packed rows summarised in profiles/; None once the kernel changes.
+GEMM_TRAFFIC_PER_CALL = 13.856e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -231,6 +251,15 @@ def main():
     ar_tps = (sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)) if ar_stats else None
     same = all(o == ar for o in outs) if ar_stats else None
 
+    # Live kernel timing of the same workload (one more request, with the
+    # step graph bracketing every launch by CUDA events on the library's
+    # stream): the GEMM family is the dominant kernel.
+    L.la_set_debug(ctx.ctx, 4)
+    st_prof = L.la_stats()
+    L.la_generate(ctx.ctx, prompt, args.max_new, W_, N_, G_, stats=st_prof)
+    prof = L.la_profile_read(ctx.ctx)
+    L.la_set_debug(ctx.ctx, 0)
+
     # kernels of ours launched in the timed region: per request the prefill
     # (2 chunks x (rows + embed + 8 per layer) + need + head 3 + finish), begin,
     # and per packed call pack + embed + 8 per layer + head 3 + publish + commit
@@ -241,9 +270,16 @@ def main():
     peaks, src = measured_peaks()
     mean_K = PROMPT_LEN + args.max_new / 2.0
     mean_Q = statistics.mean(s.mean_rows for s in stats)
+    mean_ct = statistics.mean(s.mean_candidates for s in stats)
     bytes_call = algorithmic_bytes_per_call(cfg, mean_K, mean_Q)
-    achieved = bytes_call / (call_ms * 1e-3) / 1e9
+    step_achieved = bytes_call / (call_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
+    samples = max(1, prof["samples"])
+    gemm_ms_call = prof["ms"]["gemm"] / samples
+    gemm_launches_call = prof["launches"]["gemm"] / samples
+    gemm_bytes = gemm_bytes_per_call(cfg, mean_Q, 1 + W_ + mean_ct * (N_ - 1))
+    gemm_achieved = gemm_bytes / (gemm_ms_call * 1e-3) / 1e9 if gemm_ms_call > 0 else None
+    kernel_ms_call = {k: v / samples for k, v in prof["ms"].items()}
     line = {
         "metric": "committed tokens/s @ batch 1 (7B-shape bf16)",
         "value": tps * (1 if world == 1 else 1),
@@ -267,10 +303,18 @@ def main():
         "lookahead_equals_ar": same,
         "e2e": {"value": (args.max_new * args.steps * world) / wall, "unit": "tokens/s",
                 "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": args.max_new * 4},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "whole packed call (all kernels of one step)",
-                     "algorithmic_bytes_per_call": bytes_call, "peak_source": src},
-        "step_roofline_frac": (bytes_call / (peak * 1e9)) / (call_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": gemm_achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (gemm_achieved / peak) if gemm_achieved else None,
+                     "traffic": GEMM_TRAFFIC_PER_CALL,
+                     "kernel": "k_gemm_tc (tcgen05 GEMMs: QKV, O, gate/up, down per layer + LM head), "
+                               "per call: algorithmic bytes / summed launch time",
+                     "launches_per_call": gemm_launches_call, "ms_per_call": gemm_ms_call,
+                     "algorithmic_bytes_per_call": gemm_bytes, "peak_source": src + " (copy bandwidth)",
+                     "timing": f"CUDA events around each launch in the step graph, {prof['samples']} sampled steps"},
+        "step_roofline": {"achieved": step_achieved, "frac": step_achieved / peak,
+                          "algorithmic_bytes_per_call": bytes_call,
+                          "what": "whole packed call: weights once + committed K/V read + temporary K/V written"},
+        "kernel_ms_per_call": kernel_ms_call,
         "clocks": clk,
         "gpu_launches": launches,
     }

@@ -164,10 +164,24 @@ int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
 
 /* ---- inspection (tests) -------------------------------------------------- */
 
-/* Keep fp32 logits of the rows whose outputs the verifier reads (the
- * ordinary row, the deepest trajectory level, every verification row) for
- * la_debug_logits.  flags: bit 0 = keep logits. */
+/* flags bit 0: keep fp32 logits of the rows whose outputs the verifier reads
+ * (the ordinary row, the deepest trajectory level, every verification row)
+ * for la_debug_logits.
+ * flags bit 2: kernel timing.  The step graph (a separate graph, captured on
+ * first use) brackets every launch with a CUDA event pair on the context's
+ * stream; at each host synchronisation la_generate adds the durations of the
+ * last executed step to per-kind totals read by la_profile_read.  The event
+ * records add a little time to every step: time whole steps with it off. */
 int la_set_debug(la_ctx* ctx, int flags);
+
+/* Per-kind kernel-timing totals since the last read (then reset):
+ *   ms4[k], launches4[k] (host, 4 entries each): k = 0 tensor-core GEMMs,
+ *   1 attention (block and combine kernels, timed together per layer),
+ *   2 row-wise kernels (embedding, RMSNorm, RoPE), 3 state kernels (pack,
+ *   argmax reduction, sampling verifier, publish, K/V commit);
+ *   *samples (host, may be NULL): steps the totals cover.
+ * Errors: LA_EINVAL. */
+int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* samples);
 
 /* fp32 logits [*n_rows][vocab] of the last call's needed rows and their
  * packed row indices.  host buffers of capacity cap_rows rows. */

@@ -22,7 +22,7 @@ LA_F32, LA_BF16 = 0, 1
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
            "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
-           "la_gemm_noalloc"]
+           "la_gemm_noalloc", "la_profile_read"]
 
 
 class la_model_cfg(C.Structure):
@@ -72,6 +72,7 @@ def _load() -> C.CDLL:
         "la_generate_ar": (C.c_int, [vp, i32p, C.c_int, C.c_int, C.POINTER(la_sampling), i32p, C.POINTER(C.c_int),
                                      C.POINTER(la_stats)]),
         "la_set_debug": (C.c_int, [vp, C.c_int]),
+        "la_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
         "la_debug_logits": (C.c_int, [vp, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
         "la_debug_state": (C.c_int, [vp, i32p, i32p, i32p, i32p, i32p, i32p]),
         "la_debug_pool": (C.c_int, [vp, C.c_int, i32p, C.POINTER(C.c_int)]),
@@ -184,6 +185,19 @@ def la_query(ctx) -> Dict[str, int]:
 
 def la_set_debug(ctx, flags: int) -> None:
     _check(LIB.la_set_debug(ctx, flags), "la_set_debug")
+
+
+PROFILE_KINDS = ("gemm", "attention", "rowwise", "state")
+
+
+def la_profile_read(ctx) -> Dict[str, object]:
+    """Kernel-timing totals since the last read (see la_set_debug bit 2)."""
+    ms = (C.c_double * 4)()
+    n = (C.c_int64 * 4)()
+    samples = C.c_int64()
+    _check(LIB.la_profile_read(ctx, ms, n, C.byref(samples)), "la_profile_read", ctx)
+    return {"ms": dict(zip(PROFILE_KINDS, list(ms))), "launches": dict(zip(PROFILE_KINDS, list(n))),
+            "samples": int(samples.value)}
 
 
 def la_debug_logits(ctx, cap_rows: int, vocab: int):

@@ -19,6 +19,15 @@ constexpr int PREFILL_CHUNK = 256;
 struct Graph {
     cudaGraph_t g = nullptr;
     cudaGraphExec_t x = nullptr;
+    int prof_begin = 0, prof_end = 0;   // the graph's timing event pairs (kernel-timing graphs)
+};
+
+// kernel kinds of the kernel-timing mode
+enum { PK_GEMM = 0, PK_ATTN = 1, PK_ROW = 2, PK_STATE = 3, PK_KINDS = 4 };
+
+struct ProfPair {
+    cudaEvent_t a = nullptr, b = nullptr;
+    int kind = 0;
 };
 
 }  // namespace
@@ -63,6 +72,13 @@ struct la_ctx {
     int prompt_len = 0;
     int debug = 0;
     std::map<int, Graph> graphs;
+
+    // kernel-timing mode (debug bit 2): event pairs recorded inside the step graph
+    bool prof_capture = false;
+    std::vector<ProfPair> prof;
+    double prof_ms[PK_KINDS] = {0, 0, 0, 0};
+    long long prof_n[PK_KINDS] = {0, 0, 0, 0};
+    long long prof_samples = 0;
 };
 
 // ---------------------------------------------------------------------------
@@ -101,6 +117,34 @@ static int read_hdr(la_ctx* ctx, LaHdr* h) {
     return LA_OK;
 }
 
+// Kernel-timing mode: while a timing graph is being captured, an event pair
+// brackets each timed launch on the context's stream.
+static int prof_open(la_ctx* ctx, int kind) {
+    if (!ctx->prof_capture) return -1;
+    ProfPair pp;
+    pp.kind = kind;
+    if (cudaEventCreate(&pp.a) != cudaSuccess || cudaEventCreate(&pp.b) != cudaSuccess) return -1;
+    ctx->prof.push_back(pp);
+    const int i = (int)ctx->prof.size() - 1;
+    if (cudaEventRecordWithFlags(ctx->prof[i].a, ctx->st, cudaEventRecordExternal) != cudaSuccess) return -1;
+    return i;
+}
+static void prof_close(la_ctx* ctx, int i) {
+    if (i >= 0) cudaEventRecordWithFlags(ctx->prof[i].b, ctx->st, cudaEventRecordExternal);
+}
+// adds the last execution of graph g to the per-kind totals
+static void prof_collect(la_ctx* ctx, const Graph& g) {
+    if (g.prof_end <= g.prof_begin) return;
+    for (int i = g.prof_begin; i < g.prof_end; ++i) {
+        float ms = 0;
+        if (cudaEventElapsedTime(&ms, ctx->prof[i].a, ctx->prof[i].b) == cudaSuccess) {
+            ctx->prof_ms[ctx->prof[i].kind] += ms;
+            ctx->prof_n[ctx->prof[i].kind] += 1;
+        }
+    }
+    ctx->prof_samples += 1;
+}
+
 static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const void* w2, const void* w3, int n_seg,
                      int Nout_seg, int K, void* X, void* out, int ldo) {
     memset(g, 0, sizeof(*g));
@@ -129,11 +173,17 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
     cudaStream_t st = ctx->st;
     const int rc = (sel == SEL_PREFILL) ? PREFILL_CHUNK : ctx->Qmax;
     const int dm = c.d_model, HD = ctx->HD, F = c.d_ffn, H = c.n_heads, dh = c.head_dim;
+    int pi = prof_open(ctx, PK_ROW);
     la_launch_embed(d, st, c.dtype, ctx->emb, ctx->x, dm, sel, rc);
+    prof_close(ctx, pi);
     for (int l = 0; l < c.n_layers; ++l) {
+        pi = prof_open(ctx, PK_ROW);
         la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->attn_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc);
+        prof_close(ctx, pi);
         if (ctx->tc) {
+            pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_qkv[l], ctx->work, sel));
+            prof_close(ctx, pi);
         } else {
             char* q = (char*)ctx->qkv;
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_STORE, ctx->xn, dm, ctx->wq[l], nullptr, dm, HD, q, 3 * HD, sel, rc);
@@ -147,8 +197,11 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
         void* vdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx)
                                           : layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax);
         int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ctx->Qmax;
+        pi = prof_open(ctx, PK_ROW);
         la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
                           stride, rc);
+        prof_close(ctx, pi);
+        pi = prof_open(ctx, PK_ATTN);
         if (ctx->bf16) {
             CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
                                         layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
@@ -162,15 +215,24 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
                                    layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, H, sel, ctx->Qcap,
                                    ctx->max_ctx, ctx->Qmax, rc));
         }
+        prof_close(ctx, pi);
         if (ctx->tc) {
+            pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_o[l], ctx->work, sel));
+            prof_close(ctx, pi);
         } else {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->attn, HD, ctx->wo[l], nullptr, HD, dm, ctx->x, dm, sel, rc);
         }
+        pi = prof_open(ctx, PK_ROW);
         la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->mlp_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc);
+        prof_close(ctx, pi);
         if (ctx->tc) {
+            pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel));
+            prof_close(ctx, pi);
+            pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_down[l], ctx->work, sel));
+            prof_close(ctx, pi);
         } else {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_SWIGLU, ctx->xn, dm, ctx->wg[l], ctx->wu[l], dm, F, ctx->act, F, sel, rc);
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->act, F, ctx->wd[l], nullptr, F, dm, ctx->x, dm, sel, rc);
@@ -186,13 +248,19 @@ static int enqueue_head(la_ctx* ctx, int keep_logits) {
     const LaDev& d = ctx->d;
     cudaStream_t st = ctx->st;
     const int rc = ctx->Qmax;
+    int pi = prof_open(ctx, PK_ROW);
     la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->fnorm, ctx->hn, c.d_model, c.rms_eps, SEL_NEED, 1, rc);
+    prof_close(ctx, pi);
     if (ctx->tc) {
         TcGemm g = ctx->g_head;
         g.logits = keep_logits ? ctx->logits : nullptr;
+        pi = prof_open(ctx, PK_GEMM);
         CK(la_launch_gemm_tc(d, st, g, ctx->work, SEL_NEED));
+        prof_close(ctx, pi);
+        pi = prof_open(ctx, PK_STATE);
         la_launch_argmax_reduce(d, st, ctx->work.part_v, ctx->work.part_i, c.vocab / 128, ctx->work.part_stride,
                                 SEL_NEED, rc);
+        prof_close(ctx, pi);
     } else {
         la_launch_gemm_ffma(d, st, c.dtype, GEMM_LOGITS, ctx->hn, c.d_model, ctx->head, nullptr, c.d_model, c.vocab,
                             ctx->logits, c.vocab, SEL_NEED, rc);
@@ -204,30 +272,42 @@ static int enqueue_head(la_ctx* ctx, int keep_logits) {
 
 static int enqueue_publish_commit(la_ctx* ctx, int verdict_given) {
     const la_model_cfg& c = ctx->cfg;
+    const int pi = prof_open(ctx, PK_STATE);
     la_launch_publish(ctx->d, ctx->st, verdict_given);
     la_launch_commit(ctx->d, ctx->st, ctx->cache, ctx->temp, c.n_layers * 2 * c.n_heads, c.n_heads,
                      (int)(c.head_dim * ctx->esz), ctx->max_ctx, ctx->Qmax);
+    prof_close(ctx, pi);
     CK(cudaGetLastError());
     return LA_OK;
 }
 
 static int enqueue_step(la_ctx* ctx) {
+    int pi = prof_open(ctx, PK_STATE);
     la_launch_pack(ctx->d, ctx->st);
+    prof_close(ctx, pi);
     int r = enqueue_forward(ctx, SEL_CALL);
     if (r) return r;
     r = enqueue_head(ctx, (ctx->debug & 1) | ctx->sampling);
     if (r) return r;
-    if (ctx->sampling) CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, ctx->cfg.vocab, 0));
+    if (ctx->sampling) {
+        pi = prof_open(ctx, PK_STATE);
+        CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, ctx->cfg.vocab, 0));
+        prof_close(ctx, pi);
+    }
     return enqueue_publish_commit(ctx, ctx->sampling);
 }
 
 static int get_graph(la_ctx* ctx, Graph** out) {
-    int key = (ctx->debug & 1) | (ctx->sampling << 1);
+    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     Graph g;
     CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
+    ctx->prof_capture = (ctx->debug & 4) != 0;
+    g.prof_begin = (int)ctx->prof.size();
     int r = enqueue_step(ctx);
+    ctx->prof_capture = false;
+    g.prof_end = (int)ctx->prof.size();
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
     if (r) { if (graph) cudaGraphDestroy(graph); return r; }
@@ -280,6 +360,10 @@ void la_free(la_ctx* ctx) {
     for (auto& kv : ctx->graphs) {
         if (kv.second.x) cudaGraphExecDestroy(kv.second.x);
         if (kv.second.g) cudaGraphDestroy(kv.second.g);
+    }
+    for (auto& pp : ctx->prof) {
+        if (pp.a) cudaEventDestroy(pp.a);
+        if (pp.b) cudaEventDestroy(pp.b);
     }
     for (void* p : ctx->allocs) cudaFree(p);
     if (ctx->own_stream && ctx->st) cudaStreamDestroy(ctx->st);
@@ -490,6 +574,19 @@ int la_set_debug(la_ctx* ctx, int flags) {
     return LA_OK;
 }
 
+int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* samples) {
+    if (!ctx || !ms4 || !launches4) return LA_EINVAL;
+    for (int k = 0; k < PK_KINDS; ++k) {
+        ms4[k] = ctx->prof_ms[k];
+        launches4[k] = ctx->prof_n[k];
+        ctx->prof_ms[k] = 0;
+        ctx->prof_n[k] = 0;
+    }
+    if (samples) *samples = ctx->prof_samples;
+    ctx->prof_samples = 0;
+    return LA_OK;
+}
+
 static int check_sampling(const la_sampling* s) {
     if (!s) return LA_OK;
     if (!(s->temperature > 0.f) || !(s->top_p > 0.f) || !(s->top_p <= 1.f)) return LA_EINVAL;
@@ -671,6 +768,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         for (int i = 0; i < launches; ++i) CK(cudaGraphLaunch(g->x, ctx->st));
         r = read_hdr(ctx, &h);
         if (r) return r;
+        prof_collect(ctx, *g);
         if (++guard > 4 * max_new + 16) return LA_EDEVICE;
     }
     CK(cudaEventRecord(e2, ctx->st));
