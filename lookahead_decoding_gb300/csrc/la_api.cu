@@ -117,6 +117,15 @@ static int read_hdr(la_ctx* ctx, LaHdr* h) {
     return LA_OK;
 }
 
+int la_pdl_enabled() {
+    static int on = -1;
+    if (on < 0) {
+        const char* e = getenv("LA_PDL");
+        on = (e && e[0] == '0') ? 0 : 1;
+    }
+    return on;
+}
+
 // Kernel-timing mode: while a timing graph is being captured, an event pair
 // brackets each timed launch on the context's stream.
 static int prof_open(la_ctx* ctx, int kind) {

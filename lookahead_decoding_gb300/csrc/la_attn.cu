@@ -82,6 +82,8 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
 __global__ void __launch_bounds__(256) k_attn_blocks(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
                                                      const __nv_bfloat16* vc, float* part, int sel, int Qcap,
                                                      int max_ctx, int TB, int NS, int H) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (h->err != 0 || (sel != SEL_PREFILL && h->done != 0)) return;
     const int rows = rows_sel(h, sel);
@@ -247,6 +249,8 @@ __global__ void __launch_bounds__(TW * 32) k_attn_tail(LaDev d, const float* par
                                                      const __nv_bfloat16* kt, const __nv_bfloat16* vt,
                                                      __nv_bfloat16* out, int sel, int Qcap, int max_ctx, int Qmax,
                                                      int TB, int NS, int H) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (h->err != 0 || (sel != SEL_PREFILL && h->done != 0)) return;
     const int rows = rows_sel(h, sel);
@@ -419,11 +423,11 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
         attr = true;
     }
     dim3 g1(H, NS, (rows_cap + RG - 1) / RG);
-    k_attn_blocks<<<g1, 256, smem, st>>>(d, (const __nv_bfloat16*)qbuf, (const __nv_bfloat16*)kc,
-                                         (const __nv_bfloat16*)vc, part, sel, Qcap, max_ctx, TB, NS, H);
+    cudaError_t e = la_launch_pdl(k_attn_blocks, g1, dim3(256), smem, st, d, (const __nv_bfloat16*)qbuf,
+                                  (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, part, sel, Qcap, max_ctx, TB, NS, H);
+    if (e != cudaSuccess) return e;
     dim3 g2(H, (rows_cap + TW - 1) / TW);
-    k_attn_tail<<<g2, TW * 32, 0, st>>>(d, part, (const __nv_bfloat16*)qbuf, (const __nv_bfloat16*)kc,
-                                       (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt, (const __nv_bfloat16*)vt,
-                                       (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, NS, H);
-    return cudaGetLastError();
+    return la_launch_pdl(k_attn_tail, g2, dim3(TW * 32), 0, st, d, (const float*)part, (const __nv_bfloat16*)qbuf,
+                         (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
+                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, NS, H);
 }

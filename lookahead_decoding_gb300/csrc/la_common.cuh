@@ -85,6 +85,35 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 
 __device__ __forceinline__ void la_set_err(LaHdr* h, int code) { atomicCAS(&h->err, 0, code); }
 
+// Programmatic dependent launch.  Kernels of the step are launched so that
+// each may start while its predecessor in the stream is still running; a
+// kernel calls la_pdl_wait() before its first access to anything an earlier
+// kernel wrote (it returns once the predecessor has completed and its writes
+// are visible), and la_pdl_trigger() to let its own successor launch.  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void la_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void la_pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 1 unless LA_PDL=0 (A/B runs): launches below carry the attribute
+int la_pdl_enabled();
+
+// kernel<<<grid, block, smem, st>>>(args...) with programmatic stream serialisation
+template <typename... KArgs, typename... Args>
+static inline cudaError_t la_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                        cudaStream_t st, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = la_pdl_enabled();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Spin limit of every bounded device wait (iterations of mbarrier.try_wait,
 // each of which suspends for a hardware-defined interval).
 #define LA_SPIN_LIMIT (1u << 22)

@@ -236,12 +236,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     // every stage layout below has at least this many stages
     const int n_pre = min(swiglu ? 2 : 3, n_units);
 
+    la_pdl_trigger();
     if (warp == 0) {
         int hdr_rows = 0;
         if (lane == 0) {
-            // header words: loaded now, first used after the first weight loads are issued
-            const int h_err = h->err, h_done = h->done;
-            const int h_n = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
             for (int s = 0; s < MAX_STAGES; ++s) {
                 mbar_init(bar_full + 8 * s, 1);
                 mbar_init(bar_empty + 8 * s, 1);
@@ -270,6 +268,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (++kt == p.k_tiles) { kt = 0; ++tile; }
                 }
             }
+            // everything above depends on no earlier kernel; the header and the
+            // activations are written by the kernels before this one
+            la_pdl_wait();
+            const int h_err = h->err, h_done = h->done;
+            const int h_n = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
             int rows = h_n;
             if (h_err != 0 || (p.sel != SEL_PREFILL && h_done != 0) || rows <= 0) rows = -1;
             if (rows > 0 && (rows + BN_MAX - 1) / BN_MAX > p.max_chunks) {
@@ -377,6 +380,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                          : "memory");
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
+        la_pdl_wait();
         tc_fence_before();
         asm volatile("bar.sync 2, 192;" ::: "memory");
         tc_fence_after();
@@ -763,7 +767,6 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     if (p.max_chunks < 1 || p.max_chunks > MAX_CHUNKS) return cudaErrorInvalidValue;
     const long long T = (long long)p.n_tiles * p.k_tiles;
     dim3 grid((unsigned)std::min<long long>(g.n_cta, T), 1);
-    k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES + 1024, st>>>(g.tmA, g.tmA2, g.tmA3, g.tmB, g.tmB32, g.tmB64, g.tmB128,
-                                                         g.tmB256, pf1, pf2, pf3, p);
-    return cudaGetLastError();
+    return la_launch_pdl(k_gemm_tc, grid, dim3(NTHREADS), (size_t)(SMEM_BYTES + 1024), st, g.tmA, g.tmA2, g.tmA3, g.tmB,
+                         g.tmB32, g.tmB64, g.tmB128, g.tmB256, pf1, pf2, pf3, p);
 }

@@ -41,6 +41,8 @@ __device__ __forceinline__ bool skip_call(const LaHdr* h, int sel) {
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     int q = blockIdx.x;
@@ -58,6 +60,8 @@ __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
 template <typename T>
 __global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const T* g, T* y, int dm, float eps, int sel,
                                                  int gather) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     int row = blockIdx.x;
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const 
 template <typename T>
 __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float* rsin, T* qbuf, T* kdst, T* vdst,
                           int H, int dh, int sel, int Qcap, int stride) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     int q = blockIdx.x;
@@ -365,6 +371,8 @@ __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
 }
 __global__ void k_argmax_rows(LaDev d, const float* logits, int V, int sel) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     int row = blockIdx.x;
@@ -391,6 +399,8 @@ __global__ void k_argmax_rows(LaDev d, const float* logits, int V, int sel) {
 
 // partial (value, index) per (vocab tile, row) -> argmax per row
 __global__ void k_argmax_reduce(LaDev d, const float* pv, const int* pi, int n_tiles, int stride, int sel) {
+    la_pdl_wait();
+    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     int row = blockIdx.x;
@@ -424,7 +434,7 @@ void la_launch_rope_table(float* rcos, float* rsin, int n_pos, int dh, double th
 
 template <typename T>
 void la_launch_embed_t(const LaDev& d, cudaStream_t st, const void* emb, float* x, int dm, int sel, int rows_cap) {
-    k_embed<T><<<rows_cap, 128, 0, st>>>(d, (const T*)emb, x, dm, sel);
+    la_launch_pdl(k_embed<T>, dim3(rows_cap), dim3(128), 0, st, d, (const T*)emb, x, dm, sel);
 }
 void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb, float* x, int dm, int sel, int rows_cap) {
     if (dtype == LA_F32) la_launch_embed_t<float>(d, st, emb, x, dm, sel, rows_cap);
@@ -433,8 +443,12 @@ void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb
 
 void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, const float* x, const void* g, void* y, int dm,
                        float eps, int sel, int gather, int rows_cap) {
-    if (dtype == LA_F32) k_rmsnorm<float><<<rows_cap, 256, 0, st>>>(d, x, (const float*)g, (float*)y, dm, eps, sel, gather);
-    else k_rmsnorm<__nv_bfloat16><<<rows_cap, 256, 0, st>>>(d, x, (const __nv_bfloat16*)g, (__nv_bfloat16*)y, dm, eps, sel, gather);
+    if (dtype == LA_F32)
+        la_launch_pdl(k_rmsnorm<float>, dim3(rows_cap), dim3(256), 0, st, d, x, (const float*)g, (float*)y, dm, eps, sel,
+                      gather);
+    else
+        la_launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows_cap), dim3(256), 0, st, d, x, (const __nv_bfloat16*)g,
+                      (__nv_bfloat16*)y, dm, eps, sel, gather);
 }
 
 void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
@@ -444,8 +458,8 @@ void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* q
         k_rope_kv<float><<<g, dh / 2, 0, st>>>(d, (const float*)qkv, rcos, rsin, (float*)qbuf, (float*)kdst, (float*)vdst,
                                                H, dh, sel, Qcap, stride);
     else
-        k_rope_kv<__nv_bfloat16><<<g, dh / 2, 0, st>>>(d, (const __nv_bfloat16*)qkv, rcos, rsin, (__nv_bfloat16*)qbuf,
-                                                       (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride);
+        la_launch_pdl(k_rope_kv<__nv_bfloat16>, g, dim3(dh / 2), 0, st, d, (const __nv_bfloat16*)qkv, rcos, rsin,
+                      (__nv_bfloat16*)qbuf, (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride);
 }
 
 template <typename T, int DH, int RPW>
@@ -502,5 +516,5 @@ void la_launch_argmax_rows(const LaDev& d, cudaStream_t st, const float* logits,
 }
 void la_launch_argmax_reduce(const LaDev& d, cudaStream_t st, const float* pv, const int* pi, int n_tiles, int stride,
                              int sel, int rows_cap) {
-    k_argmax_reduce<<<rows_cap, 256, 0, st>>>(d, pv, pi, n_tiles, stride, sel);
+    la_launch_pdl(k_argmax_reduce, dim3(rows_cap), dim3(256), 0, st, d, pv, pi, n_tiles, stride, sel);
 }

@@ -300,6 +300,8 @@ __device__ void sample_verify_core(const SvIn& in, float* p, Red& r, SvOut& o) {
 }
 
 __global__ void __launch_bounds__(NT) k_sample_verify(LaDev d, const float* logits, int V, int prefill) {
+    la_pdl_wait();
+    la_pdl_trigger();
     LaHdr* h = d.hdr;
     if (h->err || (!prefill && h->done)) return;
     extern __shared__ float p[];
@@ -369,6 +371,5 @@ cudaError_t la_launch_sample_verify(const LaDev& d, cudaStream_t st, const float
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    k_sample_verify<<<1, NT, smem, st>>>(d, logits, V, prefill);
-    return cudaGetLastError();
+    return la_launch_pdl(k_sample_verify, dim3(1), dim3(NT), smem, st, d, logits, V, prefill);
 }

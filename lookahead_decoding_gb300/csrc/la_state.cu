@@ -51,6 +51,8 @@ __global__ void k_begin(LaDev d, int mode, int W, int N, int G, int sampling,
 // pack: token ids, logical positions, metadata, key paths, needed rows
 // ---------------------------------------------------------------------------
 __global__ void k_pack(LaDev d) {
+    la_pdl_wait();
+    la_pdl_trigger();
     LaHdr* h = d.hdr;
     __shared__ int s_off[LA_MAX_R + 2];
     __shared__ int s_Q, s_Ct, s_vstart, s_ok, s_d, s_deep0;
@@ -176,6 +178,8 @@ __device__ void pool_upsert_warp(const LaDev& d, int key, const int* suffix, int
 }
 
 __global__ void k_publish(LaDev d, int verdict_given) {
+    la_pdl_wait();
+    la_pdl_trigger();
     LaHdr* h = d.hdr;
     __shared__ int s_best, s_emit[16], s_E, s_a, s_w;
     __shared__ int s_win[LA_MAX_R * LA_MAX_L];
@@ -305,6 +309,8 @@ __global__ void k_publish(LaDev d, int verdict_given) {
 // ---------------------------------------------------------------------------
 __global__ void k_commit_kv(LaDev d, char* cache, char* temp, int n_heads, int head_bytes,
                             int max_ctx, int Qmax) {
+    la_pdl_wait();
+    la_pdl_trigger();
     LaHdr* h = d.hdr;
     if (h->err) return;
     // `done` may have been set by this very call's publication: the copy still runs
@@ -379,13 +385,14 @@ void la_launch_begin(const LaDev& d, cudaStream_t st, int mode, int W, int N, in
     k_begin<<<1, 128, 0, st>>>(d, mode, W, N, G, sampling, temperature, top_p,
                                (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), max_out);
 }
-void la_launch_pack(const LaDev& d, cudaStream_t st) { k_pack<<<1, 256, 0, st>>>(d); }
+void la_launch_pack(const LaDev& d, cudaStream_t st) { la_launch_pdl(k_pack, dim3(1), dim3(256), 0, st, d); }
 void la_launch_publish(const LaDev& d, cudaStream_t st, int verdict_given) {
-    k_publish<<<1, 256, 0, st>>>(d, verdict_given);
+    la_launch_pdl(k_publish, dim3(1), dim3(256), 0, st, d, verdict_given);
 }
 void la_launch_commit(const LaDev& d, cudaStream_t st, void* cache, void* temp, int planes, int n_heads,
                       int head_bytes, int max_ctx, int Qmax) {
-    k_commit_kv<<<planes, 128, 0, st>>>(d, (char*)cache, (char*)temp, n_heads, head_bytes, max_ctx, Qmax);
+    la_launch_pdl(k_commit_kv, dim3(planes), dim3(128), 0, st, d, (char*)cache, (char*)temp, n_heads, head_bytes,
+                  max_ctx, Qmax);
 }
 void la_launch_inject_map(const LaDev& d, cudaStream_t st, const int32_t* argmax_rows, const float* logits_rows,
                           float* logits_need, int V) {
