@@ -165,7 +165,7 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     g->K = K;
     g->Nout = Nout_seg * n_seg;
     g->seg_tiles = n_seg > 1 ? Nout_seg / 128 : 0;
-    g->n_cta = la_tc_ctas();
+    g->n_cta = la_tc_pick_ctas(g->Nout / 128, K / 64);
     g->max_seg = la_tc_max_segments(g->Nout / 128, K / 64, g->n_cta);
     g->rows_cap = ctx->Qcap;
     g->out = out;
@@ -176,6 +176,16 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
 // ---------------------------------------------------------------------------
 // forward passes
 // ---------------------------------------------------------------------------
+// split tiles a GEMM leaves to its consumer (none for CUDA-core GEMMs)
+static LaSplit split_of(const la_ctx* ctx, const TcGemm* g) {
+    if (!ctx->tc || !g) {
+        LaSplit none{};
+        none.ws = nullptr;
+        return none;
+    }
+    return la_tc_split(*g, ctx->work);
+}
+
 static int enqueue_forward(la_ctx* ctx, int sel) {
     const la_model_cfg& c = ctx->cfg;
     const LaDev& d = ctx->d;
@@ -187,7 +197,8 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
     prof_close(ctx, pi);
     for (int l = 0; l < c.n_layers; ++l) {
         pi = prof_open(ctx, PK_ROW);
-        la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->attn_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc);
+        la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->attn_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc,
+                          split_of(ctx, (ctx->tc && l > 0) ? &ctx->g_down[l - 1] : nullptr));
         prof_close(ctx, pi);
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
@@ -208,7 +219,7 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
         int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ctx->Qmax;
         pi = prof_open(ctx, PK_ROW);
         la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
-                          stride, rc);
+                          stride, rc, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr));
         prof_close(ctx, pi);
         pi = prof_open(ctx, PK_ATTN);
         if (ctx->bf16) {
@@ -233,12 +244,18 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->attn, HD, ctx->wo[l], nullptr, HD, dm, ctx->x, dm, sel, rc);
         }
         pi = prof_open(ctx, PK_ROW);
-        la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->mlp_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc);
+        la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->mlp_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc,
+                          split_of(ctx, ctx->tc ? &ctx->g_o[l] : nullptr));
         prof_close(ctx, pi);
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel));
             prof_close(ctx, pi);
+            if (ctx->g_gu[l].defer) {
+                pi = prof_open(ctx, PK_ROW);
+                la_launch_swiglu_split(d, st, la_tc_split(ctx->g_gu[l], ctx->work), ctx->act, F, sel, rc);
+                prof_close(ctx, pi);
+            }
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_down[l], ctx->work, sel));
             prof_close(ctx, pi);
@@ -258,7 +275,8 @@ static int enqueue_head(la_ctx* ctx, int keep_logits) {
     cudaStream_t st = ctx->st;
     const int rc = ctx->Qmax;
     int pi = prof_open(ctx, PK_ROW);
-    la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->fnorm, ctx->hn, c.d_model, c.rms_eps, SEL_NEED, 1, rc);
+    la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->fnorm, ctx->hn, c.d_model, c.rms_eps, SEL_NEED, 1, rc,
+                      split_of(ctx, ctx->tc ? &ctx->g_down[c.n_layers - 1] : nullptr));
     prof_close(ctx, pi);
     if (ctx->tc) {
         TcGemm g = ctx->g_head;
@@ -530,6 +548,10 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
         }
         ctx->g_head.next = &ctx->g_qkv[0];
         ctx->g_head.pf_units = pf;
+        // the layer GEMMs leave their split tiles to RoPE, RMSNorm and SwiGLU
+        const int defer = la_tc_defer_default();
+        for (int l = 0; l < c.n_layers; ++l)
+            ctx->g_qkv[l].defer = ctx->g_o[l].defer = ctx->g_gu[l].defer = ctx->g_down[l].defer = defer;
         size_t wsf = 0;
         int qchunks = ctx->Qcap / 256;
         auto need_ws = [&](const TcGemm& g) {

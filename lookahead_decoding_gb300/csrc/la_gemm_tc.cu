@@ -59,6 +59,7 @@ struct TcParams {
     int max_chunks;
     // L2 prefetch of the next GEMM's first units (see la_launch_gemm_tc)
     int pf_units, pf_n_tiles, pf_k_tiles, pf_seg_tiles, pf_swiglu;
+    int defer;            // split tiles left as partials for the consumer
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -553,20 +554,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 tc_fence_before();
                 epi_sync();
-                if (quarter == 0 && lane == 0) {
-                    mbar_arrive(bar_acce + 8 * b);
-                    // arrival (release: the CTA's partial stores, ordered before it by
-                    // the barrier, are visible to whoever acquires the count).  The
-                    // count only grows: arrival k completes launch k / nseg.
-                    unsigned long long old;
-                    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;"
-                                 : "=l"(old)
-                                 : "l"(p.ctr + slot)
-                                 : "memory");
-                    d_target[nd] = (old / (unsigned long long)nseg + 1ull) * (unsigned long long)nseg;
+                if (p.defer) {
+                    // the consumer of this GEMM's output adds the segments
+                    if (quarter == 0 && lane == 0) mbar_arrive(bar_acce + 8 * b);
+                } else {
+                    if (quarter == 0 && lane == 0) {
+                        mbar_arrive(bar_acce + 8 * b);
+                        // arrival (release: the CTA's partial stores, ordered before it by
+                        // the barrier, are visible to whoever acquires the count).  The
+                        // count only grows: arrival k completes launch k / nseg.
+                        unsigned long long old;
+                        asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;"
+                                     : "=l"(old)
+                                     : "l"(p.ctr + slot)
+                                     : "memory");
+                        d_target[nd] = (old / (unsigned long long)nseg + 1ull) * (unsigned long long)nseg;
+                    }
+                    d_tile[nd] = tile; d_sg[nd] = sg; d_nseg[nd] = nseg; d_y[nd] = y;
+                    ++nd;
                 }
-                d_tile[nd] = tile; d_sg[nd] = sg; d_nseg[nd] = nseg; d_y[nd] = y;
-                ++nd;
             } else {
                 // a whole tile: straight from TMEM
                 for (int c0 = 0; c0 < nq; c0 += 16) {
@@ -682,11 +688,46 @@ int la_tc_pf_units() {
     return pf;
 }
 
+// 1 unless LA_TC_DEFER=0 (A/B runs): the layer GEMMs leave split tiles to their consumers
+int la_tc_defer_default() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("LA_TC_DEFER");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v;
+}
+
+LaSplit la_tc_split(const TcGemm& g, const TcWork& w) {
+    LaSplit s;
+    s.ws = g.defer ? w.ws : nullptr;
+    s.n_tiles = g.Nout / BM;
+    s.k_tiles = g.K / BK;
+    const long long T = (long long)s.n_tiles * s.k_tiles;
+    s.P = (int)std::min<long long>(g.n_cta, T);
+    s.max_seg = g.max_seg;
+    s.nA = g.mode == GEMM_SWIGLU ? 2 : 1;
+    return s;
+}
+
 // CTAs of the persistent kernel: one per SM of the current device
 int la_tc_ctas() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+    return sms;
+}
+
+// CTAs for a weight of n_tiles x k_tiles units: one per SM, except when a
+// whole number s of CTAs per tile keeps at least 80 % of the SMs busy — then
+// n_tiles * s, so every tile splits into s equal K ranges (no tile shared by
+// CTAs that also own parts of other tiles).
+int la_tc_pick_ctas(int n_tiles, int k_tiles) {
+    const int sms = la_tc_ctas();
+    if (n_tiles <= sms) {
+        const int s = std::min(sms / n_tiles, k_tiles);
+        if (s >= 2 && n_tiles * s * 5 >= sms * 4) return n_tiles * s;
+    }
     return sms;
 }
 
@@ -755,6 +796,7 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.part_i = w.part_i;
     p.part_stride = w.part_stride;
     p.max_chunks = (g.rows_cap + BN_MAX - 1) / BN_MAX;
+    p.defer = g.defer;
     const TcGemm* nx = (g.pf_units > 0) ? g.next : nullptr;
     p.pf_units = nx ? g.pf_units : 0;
     p.pf_n_tiles = nx ? nx->Nout / BM : 0;

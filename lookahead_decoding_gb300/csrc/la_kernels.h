@@ -29,12 +29,81 @@ void la_launch_prefill_rows(const LaDev& d, cudaStream_t st, int c0, int n);
 void la_launch_prefill_need(const LaDev& d, cudaStream_t st, int last_local);
 void la_launch_prefill_finish(const LaDev& d, cudaStream_t st, int P);
 
+// Split tiles of a tensor-core GEMM left for its consumer.  A GEMM launched
+// with `defer` writes each split tile's per-segment fp32 partials and stops;
+// the kernel that reads the GEMM's output adds the segments in K order
+// (starting from 0, the same additions the GEMM would have made) before its
+// own epilogue: RoPE after QKV, the residual add + RMSNorm after O and down,
+// SwiGLU after gate/up.  ws == nullptr: no split tiles to reduce.
+struct LaSplit {
+    const float* ws;      // partial records [tile + y * n_tiles][max_seg][nA][256][128]
+    int n_tiles, k_tiles, P, max_seg, nA;
+};
+
+// segments of tile t (1 = the GEMM wrote the tile itself)
+__host__ __device__ __forceinline__ int la_split_nseg(const LaSplit& s, int t) {
+    const long long T = (long long)s.n_tiles * s.k_tiles;
+    const long long u0 = (long long)t * s.k_tiles, u1 = u0 + s.k_tiles - 1;
+    const int c0 = (int)(((u0 + 1) * s.P - 1) / T), c1 = (int)(((u1 + 1) * s.P - 1) / T);
+    return c1 - c0 + 1;
+}
+// the record of segment sg, accumulator plane pl, row chunk y of tile t
+__host__ __device__ __forceinline__ const float* la_split_rec(const LaSplit& s, int t, int y, int sg, int pl) {
+    return s.ws + ((((size_t)t + (size_t)y * s.n_tiles) * s.max_seg + sg) * s.nA + pl) * (size_t)(256 * 128);
+}
+
+#ifdef __CUDACC__
+// Sum over the segments (K order, from 0) of the element at `off` of plane pl;
+// the loads of up to four segments are issued together.
+__device__ __forceinline__ float la_split_sum(const LaSplit& s, int t, int y, int pl, size_t off, int nseg) {
+    const float t0 = __ldcg(la_split_rec(s, t, y, 0, pl) + off);
+    const float t1 = __ldcg(la_split_rec(s, t, y, nseg > 1 ? 1 : 0, pl) + off);
+    const float t2 = __ldcg(la_split_rec(s, t, y, nseg > 2 ? 2 : 0, pl) + off);
+    const float t3 = __ldcg(la_split_rec(s, t, y, nseg > 3 ? 3 : 0, pl) + off);
+    float r = __fadd_rn(0.f, t0);
+    if (nseg > 1) r = __fadd_rn(r, t1);
+    if (nseg > 2) r = __fadd_rn(r, t2);
+    if (nseg > 3) r = __fadd_rn(r, t3);
+    for (int sg = 4; sg < nseg; ++sg) r = __fadd_rn(r, __ldcg(la_split_rec(s, t, y, sg, pl) + off));
+    return r;
+}
+// the same for four consecutive elements (off a multiple of 4)
+__device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, size_t off, int nseg) {
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k < nseg ? k : 0, 0) + off));
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (k < nseg) {
+            r.x = __fadd_rn(r.x, v[k].x);
+            r.y = __fadd_rn(r.y, v[k].y);
+            r.z = __fadd_rn(r.z, v[k].z);
+            r.w = __fadd_rn(r.w, v[k].w);
+        }
+    for (int sg = 4; sg < nseg; ++sg) {
+        const float4 p = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, sg, 0) + off));
+        r.x = __fadd_rn(r.x, p.x);
+        r.y = __fadd_rn(r.y, p.y);
+        r.z = __fadd_rn(r.z, p.z);
+        r.w = __fadd_rn(r.w, p.w);
+    }
+    return r;
+}
+#endif
+
 void la_launch_rope_table(float* rcos, float* rsin, int n_pos, int dh, double theta, cudaStream_t st);
 void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb, float* x, int dm, int sel, int rows_cap);
-void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, const float* x, const void* g, void* y, int dm,
-                       float eps, int sel, int gather, int rows_cap);
+// resid: split tiles of the GEMM that last added to x (O or down), summed into x first
+void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, float* x, const void* g, void* y, int dm,
+                       float eps, int sel, int gather, int rows_cap, const LaSplit& resid);
+// sp: split tiles of the QKV GEMM
 void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
-                       void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap);
+                       void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap,
+                       const LaSplit& sp);
+// act[q][n] = silu(gate) * up for the split tiles of the gate/up GEMM
+void la_launch_swiglu_split(const LaDev& d, cudaStream_t st, const LaSplit& sp, void* act, int ldo, int sel,
+                            int rows_cap);
 cudaError_t la_launch_attention(const LaDev& d, cudaStream_t st, int dtype, int dh, const void* qbuf, const void* kc,
                                 const void* vc, const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                 int max_ctx, int Qmax, int rows_cap);
@@ -60,6 +129,7 @@ struct TcGemm {
     // the GEMM launched after this one: each CTA prefetches the first pf_units
     // (128 x 64) weight tiles of its share of `next` into L2 while it drains
     const TcGemm* next; int pf_units;
+    int defer;            // 1: split tiles left as partials for the consumer (LaSplit)
     int ctr_off;          // first split-tile counter of this GEMM (counters are per GEMM)
 };
 #define LA_TC_CTR_PER_TILE 2   // ints per split-tile arrival counter (one 64-bit word)
@@ -76,9 +146,12 @@ int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_ro
 int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K);
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
 int la_tc_ctas();
+int la_tc_pick_ctas(int n_tiles, int k_tiles);
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
 cudaError_t la_tc_prepare_device();
 int la_tc_pf_units();
+int la_tc_defer_default();
+LaSplit la_tc_split(const TcGemm& g, const TcWork& w);
 void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t* ws_floats, size_t* n_counters);
 
 // exact sampling verifier (one CTA): reads the needed rows' fp32 logits and

@@ -55,11 +55,13 @@ __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
 
 // ---------------------------------------------------------------------------
 // RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, one block per row, fixed
-// reduction order.  gather=1 reads row need[i] and writes row i.
+// reduction order.  gather=1 reads row need[i] and writes row i.  First, the
+// split tiles the last residual GEMM left (resid) are added to x: x += the
+// segments' partials in K order, and x is written back.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const T* g, T* y, int dm, float eps, int sel,
-                                                 int gather) {
+__global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g, T* y, int dm, float eps, int sel,
+                                                 int gather, LaSplit resid) {
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
@@ -67,9 +69,10 @@ __global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const 
     int row = blockIdx.x;
     if (row >= rows_of(h, sel)) return;
     int src = gather ? d.need[row] : row;
-    const float* xr = x + (size_t)src * dm;
-    // the row stays in registers: up to 8 float4 per thread (d_model <= 8192)
-    constexpr int MAXV = 8;
+    float* xr = x + (size_t)src * dm;
+    // the row stays in registers: up to 2 float4 per thread (256 threads for
+    // d_model <= 2048, 1024 threads up to 8192)
+    constexpr int MAXV = 2;
     float4 v[MAXV];
     float ss = 0.f;
 #pragma unroll
@@ -77,6 +80,19 @@ __global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const 
         const int i = (k * blockDim.x + threadIdx.x) * 4;
         if (i < dm) {
             v[k] = *reinterpret_cast<const float4*>(xr + i);
+            if (resid.ws) {
+                const int tile = i >> 7;
+                const int nseg = la_split_nseg(resid, tile);
+                if (nseg > 1) {
+                    const size_t off = (size_t)(src & 255) * 128 + (i & 127);
+                    const float4 sum = la_split_sum4(resid, tile, src >> 8, off, nseg);
+                    v[k].x = v[k].x + sum.x;
+                    v[k].y = v[k].y + sum.y;
+                    v[k].z = v[k].z + sum.z;
+                    v[k].w = v[k].w + sum.w;
+                    *reinterpret_cast<float4*>(xr + i) = v[k];
+                }
+            }
             ss = fmaf(v[k].x, v[k].x, ss);
             ss = fmaf(v[k].y, v[k].y, ss);
             ss = fmaf(v[k].z, v[k].z, ss);
@@ -114,9 +130,17 @@ __global__ void __launch_bounds__(256) k_rmsnorm(LaDev d, const float* x, const 
 // packed index (temporary rows of the call) or, in a prefill, at its
 // position in the cache.
 // ---------------------------------------------------------------------------
+// value n of row q of the QKV output: stored, or the sum of a split tile's
+// segments rounded as the GEMM's store would round it
+template <typename T>
+__device__ __forceinline__ T qkv_at(const T* row, int q, int n, const LaSplit& sp, int nseg) {
+    if (nseg <= 1) return row[n];
+    return from_f<T>(la_split_sum(sp, n >> 7, q >> 8, 0, (size_t)(q & 255) * 128 + (n & 127), nseg));
+}
+
 template <typename T>
 __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float* rsin, T* qbuf, T* kdst, T* vdst,
-                          int H, int dh, int sel, int Qcap, int stride) {
+                          int H, int dh, int sel, int Qcap, int stride, LaSplit sp) {
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
@@ -128,9 +152,12 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     int pos = d.row_pos[q];
     float c = rcos[(size_t)pos * half + i], s = rsin[(size_t)pos * half + i];
     const int HD = H * dh;
-    const T* base = qkv + (size_t)q * 3 * HD + hh * dh;
-    float qa = to_f(base[i]), qb = to_f(base[i + half]);
-    float ka = to_f(base[HD + i]), kb = to_f(base[HD + i + half]);
+    const T* row = qkv + (size_t)q * 3 * HD;
+    const int nq = hh * dh, nk = HD + hh * dh, nv = 2 * HD + hh * dh;
+    const int sq = sp.ws ? la_split_nseg(sp, nq >> 7) : 1, sk = sp.ws ? la_split_nseg(sp, nk >> 7) : 1;
+    const int sv = sp.ws ? la_split_nseg(sp, nv >> 7) : 1;
+    float qa = to_f(qkv_at(row, q, nq + i, sp, sq)), qb = to_f(qkv_at(row, q, nq + i + half, sp, sq));
+    float ka = to_f(qkv_at(row, q, nk + i, sp, sk)), kb = to_f(qkv_at(row, q, nk + i + half, sp, sk));
     T* qo = qbuf + ((size_t)hh * Qcap + q) * dh;
     qo[i] = from_f<T>(qa * c - qb * s);
     qo[i + half] = from_f<T>(qb * c + qa * s);
@@ -139,8 +166,26 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     T* vo = vdst + ((size_t)hh * stride + slot) * dh;
     ko[i] = from_f<T>(ka * c - kb * s);
     ko[i + half] = from_f<T>(kb * c + ka * s);
-    vo[i] = base[2 * HD + i];
-    vo[i + half] = base[2 * HD + i + half];
+    vo[i] = qkv_at(row, q, nv + i, sp, sv);
+    vo[i + half] = qkv_at(row, q, nv + i + half, sp, sv);
+}
+
+// SwiGLU of the gate/up GEMM's split tiles: act = silu(gate) * up with gate
+// and up the sums of the segments' two accumulator planes (one CTA per row
+// and tile, one thread per output column)
+__global__ void __launch_bounds__(128) k_swiglu_split(LaDev d, LaSplit sp, __nv_bfloat16* act, int ldo, int sel) {
+    la_pdl_wait();
+    la_pdl_trigger();
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;
+    const int q = blockIdx.x, tile = blockIdx.y, e = threadIdx.x;
+    if (q >= rows_of(h, sel) || tile >= sp.n_tiles) return;
+    const int nseg = la_split_nseg(sp, tile);
+    if (nseg <= 1) return;
+    const size_t off = (size_t)(q & 255) * 128 + e;
+    const float v = la_split_sum(sp, tile, q >> 8, 0, off, nseg);
+    const float u = la_split_sum(sp, tile, q >> 8, 1, off, nseg);
+    act[(size_t)q * ldo + tile * 128 + e] = __float2bfloat16_rn(v / (1.0f + expf(-v)) * u);
 }
 
 // ---------------------------------------------------------------------------
@@ -441,25 +486,32 @@ void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb
     else la_launch_embed_t<__nv_bfloat16>(d, st, emb, x, dm, sel, rows_cap);
 }
 
-void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, const float* x, const void* g, void* y, int dm,
-                       float eps, int sel, int gather, int rows_cap) {
+void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, float* x, const void* g, void* y, int dm,
+                       float eps, int sel, int gather, int rows_cap, const LaSplit& resid) {
+    const dim3 threads(dm > 2048 ? 1024 : 256);
     if (dtype == LA_F32)
-        la_launch_pdl(k_rmsnorm<float>, dim3(rows_cap), dim3(256), 0, st, d, x, (const float*)g, (float*)y, dm, eps, sel,
-                      gather);
+        la_launch_pdl(k_rmsnorm<float>, dim3(rows_cap), threads, 0, st, d, x, (const float*)g, (float*)y, dm, eps, sel,
+                      gather, resid);
     else
-        la_launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows_cap), dim3(256), 0, st, d, x, (const __nv_bfloat16*)g,
-                      (__nv_bfloat16*)y, dm, eps, sel, gather);
+        la_launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows_cap), threads, 0, st, d, x, (const __nv_bfloat16*)g,
+                      (__nv_bfloat16*)y, dm, eps, sel, gather, resid);
 }
 
 void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
-                       void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap) {
+                       void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap,
+                       const LaSplit& sp) {
     dim3 g(rows_cap, H);
     if (dtype == LA_F32)
         k_rope_kv<float><<<g, dh / 2, 0, st>>>(d, (const float*)qkv, rcos, rsin, (float*)qbuf, (float*)kdst, (float*)vdst,
-                                               H, dh, sel, Qcap, stride);
+                                               H, dh, sel, Qcap, stride, sp);
     else
         la_launch_pdl(k_rope_kv<__nv_bfloat16>, g, dim3(dh / 2), 0, st, d, (const __nv_bfloat16*)qkv, rcos, rsin,
-                      (__nv_bfloat16*)qbuf, (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride);
+                      (__nv_bfloat16*)qbuf, (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride, sp);
+}
+
+void la_launch_swiglu_split(const LaDev& d, cudaStream_t st, const LaSplit& sp, void* act, int ldo, int sel,
+                            int rows_cap) {
+    la_launch_pdl(k_swiglu_split, dim3(rows_cap, sp.n_tiles), dim3(128), 0, st, d, sp, (__nv_bfloat16*)act, ldo, sel);
 }
 
 template <typename T, int DH, int RPW>
