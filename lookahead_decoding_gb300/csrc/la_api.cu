@@ -56,7 +56,6 @@ struct la_ctx {
     void *cache = nullptr, *temp = nullptr;
     float *rcos = nullptr, *rsin = nullptr;
     float* logits = nullptr;          // [Qcap][V] fp32
-    float* attn_part = nullptr;       // bf16 attention block partials [Qcap][H][blocks][record]
     int attn_TB = 0;
     float* logits_in = nullptr;       // [Qmax][V] staging for injected logits
     int32_t* argmax_in = nullptr;     // [Qcap]
@@ -165,7 +164,7 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     g->K = K;
     g->Nout = Nout_seg * n_seg;
     g->seg_tiles = n_seg > 1 ? Nout_seg / 128 : 0;
-    g->n_cta = la_tc_pick_ctas(g->Nout / 128, K / 64);
+    g->n_cta = la_tc_pick_ctas(g->Nout / 128, K / 64, mode);
     g->max_seg = la_tc_max_segments(g->Nout / 128, K / 64, g->n_cta);
     g->rows_cap = ctx->Qcap;
     g->out = out;
@@ -226,8 +225,8 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
             CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
                                         layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
                                         layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax),
-                                        layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, ctx->attn_part, H, sel,
-                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB));
+                                        layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, H, sel,
+                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX));
         } else {
             CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
                                    layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
@@ -251,7 +250,7 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel));
             prof_close(ctx, pi);
-            if (ctx->g_gu[l].defer) {
+            if (ctx->g_gu[l].defer && ctx->g_gu[l].max_seg > 1) {
                 pi = prof_open(ctx, PK_ROW);
                 la_launch_swiglu_split(d, st, la_tc_split(ctx->g_gu[l], ctx->work), ctx->act, F, sel, rc);
                 prof_close(ctx, pi);
@@ -510,8 +509,7 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
     A((void**)&ctx->logits_in, sizeof(float) * (size_t)ctx->Qmax * V);
     if (ctx->bf16) {
         ctx->attn_TB = la_attn_tail_blocks(ctx->PMAX);
-        A((void**)&ctx->attn_part,
-          sizeof(float) * Qc * c.n_heads * (size_t)la_attn_nblocks(max_ctx) * la_attn_record_floats());
+        if (la_attn_smem_bytes(ctx->attn_TB, ctx->Qmax, ctx->PMAX) > 227 * 1024) r = LA_ENOTSUP;
     }
     if (r) { la_free(ctx); return r; }
     la_launch_rope_table(ctx->rcos, ctx->rsin, ctx->rope_len, c.head_dim, (double)c.rope_theta, ctx->st);

@@ -1,22 +1,23 @@
-// Masked attention of the packed call for bf16 models, in two kernels.
+// Masked attention of the packed call for bf16 models: one kernel, one CTA
+// per (head, tile of 16 packed rows), 4 warps.
 //
 // Every row attends to one key per logical position 0..pos (M7.3 §0x04A:
 // the committed prefix, then the row's own branch path).  The positions are
 // split at t0(pos) = max(0, (floor(pos/32) - TB) * 32), a function of the
 // row's position alone (TB is fixed per context so that pos - t0 covers
 // every in-call offset):
-//   * k_attn_blocks — keys [0, t0) are committed K/V; one CTA per (head,
-//     128-position block) stages the block once (cp.async, [key][dim] bf16)
-//     and runs it for all rows on tensor cores (mma.sync m16n8k16 -> fp32):
-//     S = Q K^T in bf16, a per-row block maximum, P = exp(S - m) rounded to
-//     fp16, O = P V in fp16 (V fragments by ldmatrix.trans, converted exactly
-//     from bf16; P keeps 10 mantissa bits).  The partial (m, l, O) of each
-//     (row, head, block) goes to scratch.
-//   * k_attn_tail — one warp per (row, head) merges the row's block partials
-//     in block order, then takes the remaining positions [t0, pos] (at most
-//     128) as one softmax block on CUDA cores, one key per lane, each key
-//     from the cache (committed) or from the call's temporary rows on the
-//     row's path (in-call), and normalises.
+//   * committed keys [0, t0) — 128-position blocks of the cache stream
+//     through a double-buffered shared-memory ring (cp.async, [key][dim]
+//     bf16).  For each block the 4 warps split the keys for S = Q K^T
+//     (mma.sync m16n8k16 bf16 -> fp32), form the per-row block maximum m,
+//     P = exp(S - m) rounded to fp16 and its row sum l, then split the
+//     dimensions for O = P V (fp16 mma; V fragments by ldmatrix.trans,
+//     converted exactly from bf16).  (m, l, O) of the block merges into the
+//     row's running state in block order.
+//   * positions [t0, pos] — at most 128 keys per row, from the cache
+//     (committed) or the call's temporary rows on the row's path (in-call),
+//     staged in shared memory; one softmax block per row on CUDA cores, one
+//     key per lane, merged after the blocks, then normalised.
 // A row's arithmetic therefore depends only on its query, its position and
 // the keys it sees — the same whether it is decoded alone or packed.
 #include "la_common.cuh"
@@ -28,12 +29,12 @@
 namespace {
 
 constexpr int DH = 128;
-constexpr int BLK = 128;          // positions per block
-constexpr int RG = 128;           // rows per CTA (8 warps x 16)
+constexpr int BLK = 128;          // positions per committed block
+constexpr int FR = 16;            // packed rows per CTA (one m16 tile)
+constexpr int FW = 4;             // warps per CTA
 constexpr int PAD = 8;            // bf16 padding per smem row (16 B): conflict-free fragment loads
-constexpr int LDK = DH + PAD;     // K and V tiles [key][dim]
-constexpr int OOFF = 4;           // partial record: m, l, 2 pad, o[DH] (o 16-byte aligned)
-constexpr int PSTR = DH + OOFF;
+constexpr int LDK = DH + PAD;     // K, V, Q and P rows in shared memory
+constexpr int MAX_TAIL = 128;     // tail keys per row (TB <= 3)
 
 __device__ __forceinline__ int t0_of(int pos, int TB) {
     int b = (pos >> 5) - TB;
@@ -68,6 +69,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -79,152 +85,6 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
     return pack_f16(__low2float(b), __high2float(b));
 }
 
-__global__ void __launch_bounds__(256) k_attn_blocks(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
-                                                     const __nv_bfloat16* vc, float* part, int sel, int Qcap,
-                                                     int max_ctx, int TB, int NS, int H) {
-    la_pdl_wait();
-    la_pdl_trigger();
-    const LaHdr* h = d.hdr;
-    if (h->err != 0 || (sel != SEL_PREFILL && h->done != 0)) return;
-    const int rows = rows_sel(h, sel);
-    const int hh = blockIdx.x, blk = blockIdx.y, r0 = blockIdx.z * RG;
-    if (r0 >= rows) return;
-    const int key0 = blk * BLK;
-    const int r1 = min(rows, r0 + RG);
-    // skip the block if no row of this group sees committed keys in it
-    int t0max = 0;
-    for (int r = r0 + (int)threadIdx.x; r < r1; r += blockDim.x) t0max = max(t0max, t0_of(d.row_pos[r], TB));
-    t0max = __reduce_max_sync(0xffffffffu, t0max);
-    __shared__ int s_t0max[8];
-    if ((threadIdx.x & 31) == 0) s_t0max[threadIdx.x >> 5] = t0max;
-    __syncthreads();
-    t0max = 0;
-    for (int w = 0; w < 8; ++w) t0max = max(t0max, s_t0max[w]);
-    if (t0max <= key0) return;
-
-    extern __shared__ __align__(16) __nv_bfloat16 sm[];
-    __nv_bfloat16* ks = sm;                 // [BLK][LDK] bf16 keys
-    __nv_bfloat16* vs = sm + BLK * LDK;     // [BLK][LDK] bf16 values (same layout; fragments via ldmatrix.trans)
-    const __nv_bfloat16* kh = kc + (size_t)hh * max_ctx * DH;
-    const __nv_bfloat16* vh = vc + (size_t)hh * max_ctx * DH;
-    // stage the block with 16-byte asynchronous copies; positions past the cache read as zero
-    const uint32_t ks_a = (uint32_t)__cvta_generic_to_shared(ks), vs_a = (uint32_t)__cvta_generic_to_shared(vs);
-    for (int i = threadIdx.x; i < BLK * (DH / 8); i += blockDim.x) {
-        const int key = i >> 4, c8 = (i & 15) * 8;
-        const int p = key0 + key;
-        const int ok = p < max_ctx;
-        const size_t src = (size_t)(ok ? p : 0) * DH + c8;
-        const uint32_t off = (uint32_t)(key * LDK + c8) * 2u;
-        cp_async16(ks_a + off, kh + src, ok ? 16 : 0);
-        cp_async16(vs_a + off, vh + src, ok ? 16 : 0);
-    }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int rw = r0 + warp * 16;
-    if (rw >= r1) return;
-    const int ra = rw + g, rb = rw + g + 8;
-    const int ta = ra < r1 ? t0_of(d.row_pos[ra], TB) : 0;
-    const int tb = rb < r1 ? t0_of(d.row_pos[rb], TB) : 0;
-    if (__all_sync(0xffffffffu, ta <= key0 && tb <= key0)) return;
-
-    // Q fragments for 16 rows x 128 dims (8 k-steps)
-    uint32_t qa[8][4];
-    const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
-#pragma unroll
-    for (int ks8 = 0; ks8 < 8; ++ks8) {
-        const int c = ks8 * 16 + 2 * t;
-        qa[ks8][0] = ra < r1 ? *reinterpret_cast<const uint32_t*>(qh + (size_t)ra * DH + c) : 0u;
-        qa[ks8][1] = rb < r1 ? *reinterpret_cast<const uint32_t*>(qh + (size_t)rb * DH + c) : 0u;
-        qa[ks8][2] = ra < r1 ? *reinterpret_cast<const uint32_t*>(qh + (size_t)ra * DH + c + 8) : 0u;
-        qa[ks8][3] = rb < r1 ? *reinterpret_cast<const uint32_t*>(qh + (size_t)rb * DH + c + 8) : 0u;
-    }
-    // S = Q K^T over the 128 keys of the block (16 n-tiles of 8 keys)
-    float s[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-        const __nv_bfloat16* krow = ks + (n * 8 + g) * LDK + 2 * t;
-#pragma unroll
-        for (int ks8 = 0; ks8 < 8; ++ks8) {
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16 + 8);
-            mma16816(s[n], qa[ks8], b0, b1);
-        }
-    }
-    // mask (key position >= t0 of the row), scale, block maximum per row
-    const float scale = 0.08838834764831845f;   // 1/sqrt(128)
-    float ma = -INFINITY, mb = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        const int kp = key0 + n * 8 + 2 * t;
-        s[n][0] = (kp < ta) ? __fmul_rn(s[n][0], scale) : -INFINITY;
-        s[n][1] = (kp + 1 < ta) ? __fmul_rn(s[n][1], scale) : -INFINITY;
-        s[n][2] = (kp < tb) ? __fmul_rn(s[n][2], scale) : -INFINITY;
-        s[n][3] = (kp + 1 < tb) ? __fmul_rn(s[n][3], scale) : -INFINITY;
-        ma = fmaxf(ma, fmaxf(s[n][0], s[n][1]));
-        mb = fmaxf(mb, fmaxf(s[n][2], s[n][3]));
-    }
-    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
-    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-    // P = exp(S - m) rounded to fp16 (the values the P V product uses); l sums them
-    uint32_t pa[16][2];
-    float la = 0.f, lb = 0.f;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        const float p0 = (s[n][0] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][0], ma));
-        const float p1 = (s[n][1] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][1], ma));
-        const float p2 = (s[n][2] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][2], mb));
-        const float p3 = (s[n][3] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][3], mb));
-        pa[n][0] = pack_f16(p0, p1);
-        pa[n][1] = pack_f16(p2, p3);
-        const __half2 q0 = *reinterpret_cast<__half2*>(&pa[n][0]);
-        const __half2 q1 = *reinterpret_cast<__half2*>(&pa[n][1]);
-        la = __fadd_rn(la, __fadd_rn(__low2float(q0), __high2float(q0)));
-        lb = __fadd_rn(lb, __fadd_rn(__low2float(q1), __high2float(q1)));
-    }
-    la = __fadd_rn(la, __shfl_xor_sync(0xffffffffu, la, 1));
-    la = __fadd_rn(la, __shfl_xor_sync(0xffffffffu, la, 2));
-    lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 1));
-    lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 2));
-    // O = P V: 8 k-steps of 16 keys x 16 n-tiles of 8 dims; V fragments by
-    // transposing 8x8 tiles of the [key][dim] block, converted to fp16
-    float o[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    // lane -> (matrix, row): matrices {keys 0-7, keys 8-15} x {dims n*8, dims n*8+8}
-    const int mtx = lane >> 3, mrow = lane & 7;
-    const int key_off = (mtx & 1) * 8 + mrow, dim_off = (mtx >> 1) * 8;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a[4] = {pa[2 * kk][0], pa[2 * kk][1], pa[2 * kk + 1][0], pa[2 * kk + 1][1]};
-#pragma unroll
-        for (int n = 0; n < 16; n += 2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(vs_a + (uint32_t)((kk * 16 + key_off) * LDK + n * 8 + dim_off) * 2u, b0, b1, b2, b3);
-            mma16816_f16(o[n], a, bf2_to_h2(b0), bf2_to_h2(b1));
-            mma16816_f16(o[n + 1], a, bf2_to_h2(b2), bf2_to_h2(b3));
-        }
-    }
-    // partial records for rows that see committed keys in this block
-    if (ra < r1 && ta > key0) {
-        float* pr = part + (((size_t)ra * H + hh) * NS + blk) * PSTR;
-        if (t == 0) { pr[0] = ma; pr[1] = la; }
-#pragma unroll
-        for (int n = 0; n < 16; ++n) *reinterpret_cast<float2*>(pr + OOFF + n * 8 + 2 * t) = make_float2(o[n][0], o[n][1]);
-    }
-    if (rb < r1 && tb > key0) {
-        float* pr = part + (((size_t)rb * H + hh) * NS + blk) * PSTR;
-        if (t == 0) { pr[0] = mb; pr[1] = lb; }
-#pragma unroll
-        for (int n = 0; n < 16; ++n) *reinterpret_cast<float2*>(pr + OOFF + n * 8 + 2 * t) = make_float2(o[n][2], o[n][3]);
-    }
-}
-
 __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
@@ -234,200 +94,387 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One warp per (row, head): merges the row's committed-block partials in
-// block order, then the positions [t0, pos] — at most MAX_ROUNDS x 32 keys,
-// one key per lane per round, each taken from the cache (committed) or from
-// the call's temporary rows on the row's path (in-call) — as one softmax
-// block, and normalises.  Every load of a stage is issued before its first
-// use, so a warp spends a few memory round trips, not one per key.
-constexpr int TW = 4;                 // warps per tail CTA
-constexpr int MAX_ROUNDS = 4;         // tail keys <= 128 (TB <= 3)
-constexpr int MAX_BLK = 8;            // block partials merged per batch
+// shared memory (bytes): the K/V ring (reused for the tail keys), then fixed areas
+struct FusedLayout {
+    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, path, total;
+};
+__host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
+    FusedLayout L;
+    L.ring = 0;
+    L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;           // K and V rows, bf16
+    L.q = L.ring + L.ring_bytes;                                    // [FR][LDK] bf16
+    L.p = L.q + FR * LDK * 2;                                       // [FR][LDK] fp16
+    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32
+    L.wmax = L.o + FR * DH * 4;                                     // [FW][FR] fp32
+    L.wl = L.wmax + FW * FR * 4;                                    // [FW][FR] fp32
+    L.rpos = L.wl + FW * FR * 4;                                    // [FR] int
+    L.rt0 = L.rpos + FR * 4;                                        // [FR] int
+    L.pw = L.rt0 + FR * 4;                                          // [FW][MAX_TAIL] fp32
+    L.sw = L.pw + FW * MAX_TAIL * 4;                                // [FW][MAX_TAIL] int
+    L.path = L.sw + FW * MAX_TAIL * 4;                              // [FR][pmax] int
+    L.total = L.path + (uint32_t)FR * pmax * 4;
+    return L;
+}
 
-__global__ void __launch_bounds__(TW * 32) k_attn_tail(LaDev d, const float* part, const __nv_bfloat16* qbuf,
-                                                     const __nv_bfloat16* kc, const __nv_bfloat16* vc,
-                                                     const __nv_bfloat16* kt, const __nv_bfloat16* vt,
-                                                     __nv_bfloat16* out, int sel, int Qcap, int max_ctx, int Qmax,
-                                                     int TB, int NS, int H) {
+__global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
+                                                      const __nv_bfloat16* vc, const __nv_bfloat16* kt,
+                                                      const __nv_bfloat16* vt, __nv_bfloat16* out, int sel, int Qcap,
+                                                      int max_ctx, int Qmax, int TB, int H, int ring_keys) {
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (h->err != 0 || (sel != SEL_PREFILL && h->done != 0)) return;
     const int rows = rows_sel(h, sel);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hh = blockIdx.x;
-    const int r = blockIdx.y * TW + warp;
-    __shared__ __align__(16) float q_s[TW][DH];
-    if (r >= rows) return;
+    const int hh = blockIdx.x, r0 = blockIdx.y * FR;
+    if (r0 >= rows) return;
+    const int nr = min(FR, rows - r0);
     const int prefill = (sel == SEL_PREFILL);
-    const int pos = d.row_pos[r];
-    const int t0 = t0_of(pos, TB);
     const int K = prefill ? 0 : h->K;
-    const int Kr = prefill ? pos + 1 : K;        // positions below Kr are in the cache
+    const int Q = prefill ? 0 : h->Q;                 // the call's temporary K/V rows
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int PM = d.PMAX;
+
+    extern __shared__ __align__(16) uint8_t smem[];
+    const FusedLayout LY = fused_layout(ring_keys, PM);
+    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+    __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
+    __half* ps = reinterpret_cast<__half*>(smem + LY.p);
+    float* os = reinterpret_cast<float*>(smem + LY.o);
+    float* wmax = reinterpret_cast<float*>(smem + LY.wmax);
+    float* wl = reinterpret_cast<float*>(smem + LY.wl);
+    int* rpos = reinterpret_cast<int*>(smem + LY.rpos);
+    int* rt0 = reinterpret_cast<int*>(smem + LY.rt0);
+    float* pw = reinterpret_cast<float*>(smem + LY.pw);
+    int* sw = reinterpret_cast<int*>(smem + LY.sw);
+    int* spath = reinterpret_cast<int*>(smem + LY.path);
+
+    // rows of the tile: positions, split points, paths; queries (cp.async)
+    if (tid < FR) {
+        const int r = r0 + tid;
+        const int pos = tid < nr ? d.row_pos[r] : -1;
+        rpos[tid] = pos;
+        rt0[tid] = pos >= 0 ? t0_of(pos, TB) : 0;
+    }
+    if (!prefill)
+        for (int i = tid; i < nr * PM; i += blockDim.x) spath[i] = d.row_path[(size_t)(r0 + i / PM) * PM + i % PM];
+    const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
+    for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
+        const int r = i >> 4, c8 = (i & 15) * 8;
+        const int ok = r < nr;
+        cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(ok ? r0 + r : r0) * DH + c8, ok ? 16 : 0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    __syncthreads();
+    int t0max = 0, t0min = 0x7fffffff, posmax = 0;
+    for (int r = 0; r < nr; ++r) {
+        t0max = max(t0max, rt0[r]);
+        t0min = min(t0min, rt0[r]);
+        posmax = max(posmax, rpos[r]);
+    }
+    const int nb = (t0max + BLK - 1) / BLK;
+    const __nv_bfloat16* kh = kc + (size_t)hh * max_ctx * DH;
+    const __nv_bfloat16* vh = vc + (size_t)hh * max_ctx * DH;
+    const int ta = rt0[g], tb = rt0[g + 8];             // split points of this thread's two rows
+
+    // running state of rows g and g+8; O columns of this warp's dims
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    float o[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    auto stage_block = [&](int b, int buf) {
+        const uint32_t kb = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u);
+        const uint32_t vb = kb + BLK * LDK * 2u;
+        for (int i = tid; i < BLK * (DH / 8); i += blockDim.x) {
+            const int key = i >> 4, c8 = (i & 15) * 8;
+            const int p = b * BLK + key;
+            const int ok = p < max_ctx;
+            const size_t src = (size_t)(ok ? p : 0) * DH + c8;
+            const uint32_t off = (uint32_t)(key * LDK + c8) * 2u;
+            cp_async16(kb + off, kh + src, ok ? 16 : 0);
+            cp_async16(vb + off, vh + src, ok ? 16 : 0);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    // Q fragments (A operand of S = Q K^T) for the 8 k-steps, from shared memory
+    if (nb > 0) {
+        stage_block(0, 0);
+        asm volatile("cp.async.wait_group %0;" ::"n"(1) : "memory");     // the queries, not block 0
+    } else {
+        asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
+    }
+    __syncthreads();
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int ks8 = 0; ks8 < 8; ++ks8)
+        ldsm_x4(sbase + LY.q + (uint32_t)((lane & 15) * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qa[ks8]);
+
+    const float scale = 0.08838834764831845f;   // 1/sqrt(128)
+    for (int b = 0; b < nb; ++b) {
+        const int buf = b & 1;
+        if (b + 1 < nb) {
+            stage_block(b + 1, buf ^ 1);
+            asm volatile("cp.async.wait_group %0;" ::"n"(1) : "memory");
+        } else {
+            asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
+        }
+        __syncthreads();
+        const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring + (size_t)buf * (2 * BLK * LDK * 2));
+        const uint32_t vs_a = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u) + BLK * LDK * 2u;
+        const int key0 = b * BLK;
+        // S for this warp's 32 keys (4 n-tiles of 8)
+        float s[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+            const __nv_bfloat16* krow = ks + (warp * 32 + n * 8 + g) * LDK + 2 * t;
+#pragma unroll
+            for (int ks8 = 0; ks8 < 8; ++ks8) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16 + 8);
+                mma16816(s[n], qa[ks8], b0, b1);
+            }
+        }
+        float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int kp = key0 + warp * 32 + n * 8 + 2 * t;
+            s[n][0] = (kp < ta) ? __fmul_rn(s[n][0], scale) : -INFINITY;
+            s[n][1] = (kp + 1 < ta) ? __fmul_rn(s[n][1], scale) : -INFINITY;
+            s[n][2] = (kp < tb) ? __fmul_rn(s[n][2], scale) : -INFINITY;
+            s[n][3] = (kp + 1 < tb) ? __fmul_rn(s[n][3], scale) : -INFINITY;
+            ma = fmaxf(ma, fmaxf(s[n][0], s[n][1]));
+            mb = fmaxf(mb, fmaxf(s[n][2], s[n][3]));
+        }
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        if (t == 0) { wmax[warp * FR + g] = ma; wmax[warp * FR + g + 8] = mb; }
+        __syncthreads();
+        // block maximum per row over the four warps
+        ma = fmaxf(fmaxf(wmax[g], wmax[FR + g]), fmaxf(wmax[2 * FR + g], wmax[3 * FR + g]));
+        mb = fmaxf(fmaxf(wmax[g + 8], wmax[FR + g + 8]), fmaxf(wmax[2 * FR + g + 8], wmax[3 * FR + g + 8]));
+        // P = exp(S - m) rounded to fp16 into shared memory; l sums the rounded values
+        float la = 0.f, lb = 0.f;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const float p0 = (s[n][0] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][0], ma));
+            const float p1 = (s[n][1] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][1], ma));
+            const float p2 = (s[n][2] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][2], mb));
+            const float p3 = (s[n][3] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][3], mb));
+            const uint32_t ua = pack_f16(p0, p1), ub = pack_f16(p2, p3);
+            const int col = warp * 32 + n * 8 + 2 * t;
+            *reinterpret_cast<uint32_t*>(ps + g * LDK + col) = ua;
+            *reinterpret_cast<uint32_t*>(ps + (g + 8) * LDK + col) = ub;
+            const __half2 q0 = *reinterpret_cast<const __half2*>(&ua);
+            const __half2 q1 = *reinterpret_cast<const __half2*>(&ub);
+            la = __fadd_rn(la, __fadd_rn(__low2float(q0), __high2float(q0)));
+            lb = __fadd_rn(lb, __fadd_rn(__low2float(q1), __high2float(q1)));
+        }
+        la = __fadd_rn(la, __shfl_xor_sync(0xffffffffu, la, 1));
+        la = __fadd_rn(la, __shfl_xor_sync(0xffffffffu, la, 2));
+        lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 1));
+        lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 2));
+        if (t == 0) { wl[warp * FR + g] = la; wl[warp * FR + g + 8] = lb; }
+        __syncthreads();
+        la = __fadd_rn(__fadd_rn(__fadd_rn(wl[g], wl[FR + g]), wl[2 * FR + g]), wl[3 * FR + g]);
+        lb = __fadd_rn(__fadd_rn(__fadd_rn(wl[g + 8], wl[FR + g + 8]), wl[2 * FR + g + 8]), wl[3 * FR + g + 8]);
+        // O of the block for this warp's 32 dims: 8 k-steps of 16 keys x 4 n-tiles
+        float ob[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) ob[n][0] = ob[n][1] = ob[n][2] = ob[n][3] = 0.f;
+        const int mtx = lane >> 3, mrow = lane & 7;
+        const int key_off = (mtx & 1) * 8 + mrow, dim_off = (mtx >> 1) * 8;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(sbase + LY.p + (uint32_t)((lane & 15) * LDK + kk * 16 + (lane >> 4) * 8) * 2u, a);
+#pragma unroll
+            for (int n = 0; n < 4; n += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vs_a + (uint32_t)((kk * 16 + key_off) * LDK + warp * 32 + n * 8 + dim_off) * 2u, b0, b1, b2, b3);
+                mma16816_f16(ob[n], a, bf2_to_h2(b0), bf2_to_h2(b1));
+                mma16816_f16(ob[n + 1], a, bf2_to_h2(b2), bf2_to_h2(b3));
+            }
+        }
+        // merge the block into the running state (rows without committed keys here skip it)
+        if (ma != -INFINITY) {
+            const float mn = fmaxf(m_a, ma);
+            const float ca = (m_a == -INFINITY) ? 0.f : expf(__fsub_rn(m_a, mn));
+            const float cb = expf(__fsub_rn(ma, mn));
+            l_a = fmaf(l_a, ca, __fmul_rn(la, cb));
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                o[n][0] = fmaf(o[n][0], ca, __fmul_rn(ob[n][0], cb));
+                o[n][1] = fmaf(o[n][1], ca, __fmul_rn(ob[n][1], cb));
+            }
+            m_a = mn;
+        }
+        if (mb != -INFINITY) {
+            const float mn = fmaxf(m_b, mb);
+            const float ca = (m_b == -INFINITY) ? 0.f : expf(__fsub_rn(m_b, mn));
+            const float cb = expf(__fsub_rn(mb, mn));
+            l_b = fmaf(l_b, ca, __fmul_rn(lb, cb));
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                o[n][2] = fmaf(o[n][2], ca, __fmul_rn(ob[n][2], cb));
+                o[n][3] = fmaf(o[n][3], ca, __fmul_rn(ob[n][3], cb));
+            }
+            m_b = mn;
+        }
+        __syncthreads();      // P, the warp maxima/sums and this buffer are reused
+    }
+    // the committed state to shared memory: O by (row, dim), m and l per row
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        const int col = warp * 32 + n * 8 + 2 * t;
+        *reinterpret_cast<float2*>(os + g * DH + col) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(os + (g + 8) * DH + col) = make_float2(o[n][2], o[n][3]);
+    }
+    if (warp == 0 && t == 0) {
+        wmax[g] = m_a; wmax[g + 8] = m_b;
+        wl[g] = l_a; wl[g + 8] = l_b;
+    }
+
+    // tail keys: committed positions [t0min, Kc) then (in a call) the temporary rows
+    const int Kc = prefill ? posmax + 1 : K;
+    const int nc = (nr > 0 && Kc > t0min) ? Kc - t0min : 0;
+    const int nt = nc + Q;
     {
-        const uint2 qv = *reinterpret_cast<const uint2*>(qbuf + ((size_t)hh * Qcap + r) * DH + lane * 4);
-        const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qv.x);
-        const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qv.y);
-        *reinterpret_cast<float4*>(&q_s[warp][lane * 4]) =
-            make_float4(__low2float(q01), __high2float(q01), __low2float(q23), __high2float(q23));
-    }
-    // tail key sources: lane l owns the keys t0 + l + 32 i
-    const int n = pos - t0 + 1;
-    const __nv_bfloat16* kch = kc + (size_t)hh * max_ctx * DH;
-    const __nv_bfloat16* vch = vc + (size_t)hh * max_ctx * DH;
-    const __nv_bfloat16* kth = kt + (size_t)hh * Qmax * DH;
-    const __nv_bfloat16* vth = vt + (size_t)hh * Qmax * DH;
-    const int* path = d.row_path + (size_t)r * d.PMAX;
-    size_t srow[MAX_ROUNDS];                 // element offset of the key's row; bit 63: in-call
-#pragma unroll
-    for (int i = 0; i < MAX_ROUNDS; ++i) {
-        const int j = lane + 32 * i;
-        const int p = t0 + j;
-        srow[i] = 0;
-        if (j < n) {
-            if (p < Kr) srow[i] = (size_t)p * DH;
-            else srow[i] = ((size_t)path[p - K] * DH) | (1ull << 63);
+        const __nv_bfloat16* kth = kt + (size_t)hh * Qmax * DH;
+        const __nv_bfloat16* vth = vt + (size_t)hh * Qmax * DH;
+        const uint32_t tk = sbase + LY.ring, tv = tk + (uint32_t)ring_keys * LDK * 2u;
+        for (int i = tid; i < nt * (DH / 8); i += blockDim.x) {
+            const int j = i >> 4, c8 = (i & 15) * 8;
+            const __nv_bfloat16* ksrc;
+            const __nv_bfloat16* vsrc;
+            if (j < nc) { ksrc = kh + (size_t)(t0min + j) * DH; vsrc = vh + (size_t)(t0min + j) * DH; }
+            else { ksrc = kth + (size_t)(j - nc) * DH; vsrc = vth + (size_t)(j - nc) * DH; }
+            const uint32_t off = (uint32_t)(j * LDK + c8) * 2u;
+            cp_async16(tk + off, ksrc + c8, 16);
+            cp_async16(tv + off, vsrc + c8, 16);
         }
+        asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
-    // merge the committed blocks in block order (loads of a batch issued together)
-    float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-    const int nb = (t0 + BLK - 1) / BLK;
-    for (int b0 = 0; b0 < nb; b0 += MAX_BLK) {
-        float mj[MAX_BLK], lj[MAX_BLK];
-        float4 oj[MAX_BLK];
+    __syncthreads();
+    const __nv_bfloat16* TK = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring);
+    const __nv_bfloat16* TV = TK + (size_t)ring_keys * LDK;
+    float* pwr = pw + warp * MAX_TAIL;
+    int* swr = sw + warp * MAX_TAIL;
+    for (int r = warp; r < nr; r += FW) {
+        const int pos = rpos[r], t0 = rt0[r];
+        const int n = pos - t0 + 1;
+        const int Kr = prefill ? pos + 1 : K;
+        // scores: lane owns keys t0 + lane + 32 i
+        float sc[4], pj[4];
+        int slot[4];
 #pragma unroll
-        for (int k = 0; k < MAX_BLK; ++k) {
-            const int b = min(b0 + k, nb - 1);
-            const float* pr = part + (((size_t)r * H + hh) * NS + b) * PSTR;
-            mj[k] = pr[0];
-            lj[k] = pr[1];
-            oj[k] = *reinterpret_cast<const float4*>(pr + OOFF + lane * 4);
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            const int p = t0 + j;
+            slot[i] = 0;
+            sc[i] = -INFINITY;
+            if (j < n) slot[i] = (p < Kr) ? (p - t0min) : (nc + spath[r * PM + (p - K)]);
         }
 #pragma unroll
-        for (int k = 0; k < MAX_BLK; ++k) {
-            if (b0 + k >= nb) break;
-            const float mn = fmaxf(m, mj[k]);
-            const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
-            const float cb = expf(__fsub_rn(mj[k], mn));
-            l = fmaf(l, ca, __fmul_rn(lj[k], cb));
-            o[0] = fmaf(o[0], ca, __fmul_rn(oj[k].x, cb));
-            o[1] = fmaf(o[1], ca, __fmul_rn(oj[k].y, cb));
-            o[2] = fmaf(o[2], ca, __fmul_rn(oj[k].z, cb));
-            o[3] = fmaf(o[3], ca, __fmul_rn(oj[k].w, cb));
-            m = mn;
-        }
-    }
-    __syncwarp();
-    // scores of the tail keys: one key per lane per round, 16-byte loads issued together
-    const float scale = 0.08838834764831845f;
-    float sc[MAX_ROUNDS];
+        for (int i = 0; i < 4; ++i) {
+            if (32 * i >= n) continue;                       // warp-uniform
+            const bool valid = lane + 32 * i < n;
+            const __nv_bfloat16* kr = TK + (size_t)slot[i] * LDK;
+            float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < MAX_ROUNDS; ++i) {
-        sc[i] = -INFINITY;
-        if (32 * i >= n) continue;                       // warp-uniform
-        const bool valid = lane + 32 * i < n;
-        const __nv_bfloat16* kp = ((srow[i] >> 63) ? kth : kch) + (srow[i] & ~(1ull << 63));
-        int4 kv[DH / 8];
+            for (int c = 0; c < DH / 8; ++c) {
+                const int4 kv = *reinterpret_cast<const int4*>(kr + c * 8);
+                const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
+                const int4 qv = *reinterpret_cast<const int4*>(qs + r * LDK + c * 8);
+                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qv);
 #pragma unroll
-        for (int c = 0; c < DH / 8; ++c) kv[c] = valid ? *reinterpret_cast<const int4*>(kp + c * 8) : make_int4(0, 0, 0, 0);
-        float acc = 0.f;
-#pragma unroll
-        for (int c = 0; c < DH / 8; ++c) {
-            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv[c]);
-            const float4 qa = *reinterpret_cast<const float4*>(&q_s[warp][c * 8]);
-            const float4 qb = *reinterpret_cast<const float4*>(&q_s[warp][c * 8 + 4]);
-            acc = fmaf(qa.x, __low2float(k2[0]), acc);
-            acc = fmaf(qa.y, __high2float(k2[0]), acc);
-            acc = fmaf(qa.z, __low2float(k2[1]), acc);
-            acc = fmaf(qa.w, __high2float(k2[1]), acc);
-            acc = fmaf(qb.x, __low2float(k2[2]), acc);
-            acc = fmaf(qb.y, __high2float(k2[2]), acc);
-            acc = fmaf(qb.z, __low2float(k2[3]), acc);
-            acc = fmaf(qb.w, __high2float(k2[3]), acc);
-        }
-        if (valid) sc[i] = __fmul_rn(acc, scale);
-    }
-    // one softmax block over the tail
-    float tm = sc[0];
-#pragma unroll
-    for (int i = 1; i < MAX_ROUNDS; ++i) tm = fmaxf(tm, sc[i]);
-    tm = warp_max(tm);
-    float pj[MAX_ROUNDS], ps = 0.f;
-#pragma unroll
-    for (int i = 0; i < MAX_ROUNDS; ++i) {
-        pj[i] = (sc[i] == -INFINITY) ? 0.f : expf(__fsub_rn(sc[i], tm));
-        ps = __fadd_rn(ps, pj[i]);
-    }
-    const float tl = warp_sum(ps);
-    // P V in key order: each lane accumulates its 4 dims over the tail keys, 16 keys' values in flight
-    float to[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j0 = 0; j0 < n; j0 += 16) {
-        uint2 vv[16];
-        float pv[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int j = min(j0 + k, n - 1);
-            const int i = j >> 5, src_lane = j & 31;
-            size_t so = 0;
-            float pk = 0.f;
-#pragma unroll
-            for (int ii = 0; ii < MAX_ROUNDS; ++ii)
-                if (ii == i) {
-                    so = __shfl_sync(0xffffffffu, srow[ii], src_lane);
-                    pk = __shfl_sync(0xffffffffu, pj[ii], src_lane);
+                for (int e = 0; e < 4; ++e) {
+                    acc = fmaf(__low2float(q2[e]), __low2float(k2[e]), acc);
+                    acc = fmaf(__high2float(q2[e]), __high2float(k2[e]), acc);
                 }
-            const __nv_bfloat16* vp = ((so >> 63) ? vth : vch) + (so & ~(1ull << 63));
-            vv[k] = *reinterpret_cast<const uint2*>(vp + lane * 4);
-            pv[k] = (j0 + k < n) ? pk : 0.f;
+            }
+            if (valid) sc[i] = __fmul_rn(acc, scale);
         }
+        float tm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        tm = warp_max(tm);
+        float psum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (j0 + k >= n) break;
-            const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&vv[k].x);
-            const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&vv[k].y);
-            to[0] = fmaf(pv[k], __low2float(v01), to[0]);
-            to[1] = fmaf(pv[k], __high2float(v01), to[1]);
-            to[2] = fmaf(pv[k], __low2float(v23), to[2]);
-            to[3] = fmaf(pv[k], __high2float(v23), to[3]);
+        for (int i = 0; i < 4; ++i) {
+            pj[i] = (sc[i] == -INFINITY) ? 0.f : expf(__fsub_rn(sc[i], tm));
+            psum = __fadd_rn(psum, pj[i]);
         }
+        const float tl = warp_sum(psum);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            if (j < n) { pwr[j] = pj[i]; swr[j] = slot[i]; }
+        }
+        __syncwarp();
+        // P V in key order; lane owns dims 4 lane .. 4 lane + 3
+        float to[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < n; ++j) {
+            const float pv = pwr[j];
+            const uint2 vv = *reinterpret_cast<const uint2*>(TV + (size_t)swr[j] * LDK + lane * 4);
+            const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&vv.x);
+            const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&vv.y);
+            to[0] = fmaf(pv, __low2float(v01), to[0]);
+            to[1] = fmaf(pv, __high2float(v01), to[1]);
+            to[2] = fmaf(pv, __low2float(v23), to[2]);
+            to[3] = fmaf(pv, __high2float(v23), to[3]);
+        }
+        __syncwarp();
+        // merge the tail block after the committed blocks, normalise
+        const float m = wmax[r], l = wl[r];
+        const float4 oc = *reinterpret_cast<const float4*>(os + r * DH + lane * 4);
+        const float mn = fmaxf(m, tm);
+        const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
+        const float cb = expf(__fsub_rn(tm, mn));
+        const float lt = fmaf(l, ca, __fmul_rn(tl, cb));
+        const float o0 = fmaf(oc.x, ca, __fmul_rn(to[0], cb));
+        const float o1 = fmaf(oc.y, ca, __fmul_rn(to[1], cb));
+        const float o2 = fmaf(oc.z, ca, __fmul_rn(to[2], cb));
+        const float o3 = fmaf(oc.w, ca, __fmul_rn(to[3], cb));
+        const float inv = 1.0f / lt;
+        __nv_bfloat16* op = out + (size_t)(r0 + r) * H * DH + hh * DH + lane * 4;
+        *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(__fmul_rn(o0, inv), __fmul_rn(o1, inv));
+        *reinterpret_cast<__nv_bfloat162*>(op + 2) = __floats2bfloat162_rn(__fmul_rn(o2, inv), __fmul_rn(o3, inv));
     }
-    // merge the tail block, normalise
-    const float mn = fmaxf(m, tm);
-    const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
-    const float cb = expf(__fsub_rn(tm, mn));
-    l = fmaf(l, ca, __fmul_rn(tl, cb));
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = fmaf(o[e], ca, __fmul_rn(to[e], cb));
-    const float inv = 1.0f / l;
-    __nv_bfloat16* op = out + (size_t)r * H * DH + hh * DH + lane * 4;
-    *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(__fmul_rn(o[0], inv), __fmul_rn(o[1], inv));
-    *reinterpret_cast<__nv_bfloat162*>(op + 2) = __floats2bfloat162_rn(__fmul_rn(o[2], inv), __fmul_rn(o[3], inv));
 }
 
 }  // namespace
 
 int la_attn_tail_blocks(int pmax) { return (pmax + 31) / 32; }
-int la_attn_nblocks(int max_ctx) { return (max_ctx + BLK - 1) / BLK; }
-int la_attn_record_floats() { return PSTR; }
+
+// keys the ring must hold: two committed blocks, or the tail keys of a tile
+// (committed positions [t0min, K) or a prefill tile's span, plus the call's rows)
+static int ring_keys_for(int TB, int Qmax) {
+    const int tail = 32 * (TB + 1) + FR + Qmax;
+    return tail > 2 * BLK ? tail : 2 * BLK;
+}
+
+size_t la_attn_smem_bytes(int TB, int Qmax, int pmax) {
+    return fused_layout(ring_keys_for(TB, Qmax), pmax).total;
+}
 
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
-                                     const void* kt, const void* vt, void* out, float* part, int H, int sel, int Qcap,
-                                     int max_ctx, int Qmax, int rows_cap, int TB) {
-    if (TB + 1 > MAX_ROUNDS) return cudaErrorInvalidValue;
-    const int NS = la_attn_nblocks(max_ctx);
-    const size_t smem = (size_t)(2 * BLK * LDK) * sizeof(__nv_bfloat16);
+                                     const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
+                                     int max_ctx, int Qmax, int rows_cap, int TB, int pmax) {
+    if (TB + 1 > MAX_TAIL / 32) return cudaErrorInvalidValue;
+    const int ring_keys = ring_keys_for(TB, Qmax);
+    const size_t smem = fused_layout(ring_keys, pmax).total;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_attn_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 g1(H, NS, (rows_cap + RG - 1) / RG);
-    cudaError_t e = la_launch_pdl(k_attn_blocks, g1, dim3(256), smem, st, d, (const __nv_bfloat16*)qbuf,
-                                  (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, part, sel, Qcap, max_ctx, TB, NS, H);
-    if (e != cudaSuccess) return e;
-    dim3 g2(H, (rows_cap + TW - 1) / TW);
-    return la_launch_pdl(k_attn_tail, g2, dim3(TW * 32), 0, st, d, (const float*)part, (const __nv_bfloat16*)qbuf,
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    dim3 grid(H, (rows_cap + FR - 1) / FR);
+    return la_launch_pdl(k_attn_fused, grid, dim3(FW * 32), smem, st, d, (const __nv_bfloat16*)qbuf,
                          (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
-                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, NS, H);
+                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, H, ring_keys);
 }

@@ -68,10 +68,10 @@ __device__ __forceinline__ float la_split_sum(const LaSplit& s, int t, int y, in
     return r;
 }
 // the same for four consecutive elements (off a multiple of 4)
-__device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, size_t off, int nseg) {
+__device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, size_t off, int nseg, int pl = 0) {
     float4 v[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k < nseg ? k : 0, 0) + off));
+    for (int k = 0; k < 4; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k < nseg ? k : 0, pl) + off));
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -82,7 +82,7 @@ __device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, 
             r.w = __fadd_rn(r.w, v[k].w);
         }
     for (int sg = 4; sg < nseg; ++sg) {
-        const float4 p = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, sg, 0) + off));
+        const float4 p = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, sg, pl) + off));
         r.x = __fadd_rn(r.x, p.x);
         r.y = __fadd_rn(r.y, p.y);
         r.z = __fadd_rn(r.z, p.z);
@@ -146,7 +146,7 @@ int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_ro
 int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K);
 cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
 int la_tc_ctas();
-int la_tc_pick_ctas(int n_tiles, int k_tiles);
+int la_tc_pick_ctas(int n_tiles, int k_tiles, int mode);
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
 cudaError_t la_tc_prepare_device();
 int la_tc_pf_units();
@@ -163,8 +163,7 @@ cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V,
 
 // bf16 attention: committed 128-position blocks on tensor cores + combine/tail
 int la_attn_tail_blocks(int pmax);
-int la_attn_nblocks(int max_ctx);
-int la_attn_record_floats();
+size_t la_attn_smem_bytes(int TB, int Qmax, int pmax);
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
-                                     const void* kt, const void* vt, void* out, float* part, int H, int sel, int Qcap,
-                                     int max_ctx, int Qmax, int rows_cap, int TB);
+                                     const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
+                                     int max_ctx, int Qmax, int rows_cap, int TB, int pmax);

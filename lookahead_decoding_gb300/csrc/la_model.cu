@@ -147,8 +147,10 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     if (skip_call(h, sel)) return;
     int q = blockIdx.x;
     if (q >= rows_of(h, sel)) return;
-    int hh = blockIdx.y, i = threadIdx.x, half = dh >> 1;
-    if (i >= half) return;
+    const int half = dh >> 1;
+    // blockDim = RH heads x half threads
+    int hh = blockIdx.y * (blockDim.x / half) + threadIdx.x / half, i = threadIdx.x % half;
+    if (hh >= H) return;
     int pos = d.row_pos[q];
     float c = rcos[(size_t)pos * half + i], s = rsin[(size_t)pos * half + i];
     const int HD = H * dh;
@@ -171,21 +173,33 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
 }
 
 // SwiGLU of the gate/up GEMM's split tiles: act = silu(gate) * up with gate
-// and up the sums of the segments' two accumulator planes (one CTA per row
-// and tile, one thread per output column)
-__global__ void __launch_bounds__(128) k_swiglu_split(LaDev d, LaSplit sp, __nv_bfloat16* act, int ldo, int sel) {
+// and up the sums of the segments' two accumulator planes.  One thread per
+// four consecutive columns of a row (float4 partial loads, all in flight at once).
+__global__ void __launch_bounds__(256) k_swiglu_split(LaDev d, LaSplit sp, __nv_bfloat16* act, int ldo, int sel) {
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
-    const int q = blockIdx.x, tile = blockIdx.y, e = threadIdx.x;
-    if (q >= rows_of(h, sel) || tile >= sp.n_tiles) return;
-    const int nseg = la_split_nseg(sp, tile);
-    if (nseg <= 1) return;
-    const size_t off = (size_t)(q & 255) * 128 + e;
-    const float v = la_split_sum(sp, tile, q >> 8, 0, off, nseg);
-    const float u = la_split_sum(sp, tile, q >> 8, 1, off, nseg);
-    act[(size_t)q * ldo + tile * 128 + e] = __float2bfloat16_rn(v / (1.0f + expf(-v)) * u);
+    const int q = blockIdx.x;
+    if (q >= rows_of(h, sel)) return;
+    const int n_cols = sp.n_tiles * 128;
+    const int y = q >> 8;
+    const size_t rowoff = (size_t)(q & 255) * 128;
+    const int c4 = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+    if (c4 < n_cols) {
+        const int tile = c4 >> 7;
+        const int nseg = la_split_nseg(sp, tile);
+        if (nseg <= 1) return;
+        const size_t off = rowoff + (c4 & 127);
+        const float4 v = la_split_sum4(sp, tile, y, off, nseg, 0);
+        const float4 u = la_split_sum4(sp, tile, y, off, nseg, 1);
+        __nv_bfloat162 r01 = __floats2bfloat162_rn(v.x / (1.0f + expf(-v.x)) * u.x, v.y / (1.0f + expf(-v.y)) * u.y);
+        __nv_bfloat162 r23 = __floats2bfloat162_rn(v.z / (1.0f + expf(-v.z)) * u.z, v.w / (1.0f + expf(-v.w)) * u.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&r01);
+        pk.y = *reinterpret_cast<uint32_t*>(&r23);
+        *reinterpret_cast<uint2*>(act + (size_t)q * ldo + c4) = pk;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -500,18 +514,21 @@ void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, float* x, con
 void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
                        void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap,
                        const LaSplit& sp) {
-    dim3 g(rows_cap, H);
+    const int rh = (H % 4 == 0) ? 4 : 1;      // heads per CTA
+    dim3 g(rows_cap, H / rh);
     if (dtype == LA_F32)
-        k_rope_kv<float><<<g, dh / 2, 0, st>>>(d, (const float*)qkv, rcos, rsin, (float*)qbuf, (float*)kdst, (float*)vdst,
-                                               H, dh, sel, Qcap, stride, sp);
+        k_rope_kv<float><<<g, rh * dh / 2, 0, st>>>(d, (const float*)qkv, rcos, rsin, (float*)qbuf, (float*)kdst,
+                                                    (float*)vdst, H, dh, sel, Qcap, stride, sp);
     else
-        la_launch_pdl(k_rope_kv<__nv_bfloat16>, g, dim3(dh / 2), 0, st, d, (const __nv_bfloat16*)qkv, rcos, rsin,
+        la_launch_pdl(k_rope_kv<__nv_bfloat16>, g, dim3(rh * dh / 2), 0, st, d, (const __nv_bfloat16*)qkv, rcos, rsin,
                       (__nv_bfloat16*)qbuf, (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride, sp);
 }
 
 void la_launch_swiglu_split(const LaDev& d, cudaStream_t st, const LaSplit& sp, void* act, int ldo, int sel,
                             int rows_cap) {
-    la_launch_pdl(k_swiglu_split, dim3(rows_cap, sp.n_tiles), dim3(128), 0, st, d, sp, (__nv_bfloat16*)act, ldo, sel);
+    const int chunks = sp.n_tiles * 32;     // float4 columns per row
+    la_launch_pdl(k_swiglu_split, dim3(rows_cap, (chunks + 255) / 256), dim3(256), 0, st, d, sp, (__nv_bfloat16*)act, ldo,
+                  sel);
 }
 
 template <typename T, int DH, int RPW>
