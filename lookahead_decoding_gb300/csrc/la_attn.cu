@@ -1,5 +1,5 @@
 // Masked attention of the packed call for bf16 models: one kernel, one CTA
-// per (head, tile of 16 packed rows), 4 warps.
+// per (head, tile of 16 packed rows), 8 warps.
 //
 // Every row attends to one key per logical position 0..pos (M7.3 §0x04A:
 // the committed prefix, then the row's own branch path).  The positions are
@@ -8,7 +8,7 @@
 // every in-call offset):
 //   * committed keys [0, t0) — 128-position blocks of the cache stream
 //     through a double-buffered shared-memory ring (cp.async, [key][dim]
-//     bf16).  For each block the 4 warps split the keys for S = Q K^T
+//     bf16).  For each block the 8 warps split the keys for S = Q K^T
 //     (mma.sync m16n8k16 bf16 -> fp32), form the per-row block maximum m,
 //     P = exp(S - m) rounded to fp16 and its row sum l, then split the
 //     dimensions for O = P V (fp16 mma; V fragments by ldmatrix.trans,
@@ -16,8 +16,12 @@
 //     row's running state in block order.
 //   * positions [t0, pos] — at most 128 keys per row, from the cache
 //     (committed) or the call's temporary rows on the row's path (in-call),
-//     staged in shared memory; one softmax block per row on CUDA cores, one
-//     key per lane, merged after the blocks, then normalised.
+//     staged in shared memory once per tile; one softmax block per row:
+//     S = q K^T on tensor cores (the row's query fills an m16 tile and each
+//     lane's ldmatrix row address points at the staged key of its position,
+//     so the keys enter the products in position order); P in fp32, and
+//     P V on tensor cores with P as an fp16 value plus its fp16 residual;
+//     merged after the blocks, then normalised.
 // A row's arithmetic therefore depends only on its query, its position and
 // the keys it sees — the same whether it is decoded alone or packed.
 #include "la_common.cuh"
@@ -31,7 +35,10 @@ namespace {
 constexpr int DH = 128;
 constexpr int BLK = 128;          // positions per committed block
 constexpr int FR = 16;            // packed rows per CTA (one m16 tile)
-constexpr int FW = 4;             // warps per CTA
+constexpr int FW = 8;             // warps per CTA
+constexpr int KPW = BLK / FW;     // keys of a block per warp (S = Q K^T)
+constexpr int DPW = DH / FW;      // dimensions per warp (O = P V)
+constexpr int NTW = KPW / 8;      // n-tiles of 8 per warp (KPW == DPW)
 constexpr int PAD = 8;            // bf16 padding per smem row (16 B): conflict-free fragment loads
 constexpr int LDK = DH + PAD;     // K, V, Q and P rows in shared memory
 constexpr int MAX_TAIL = 128;     // tail keys per row (TB <= 3)
@@ -145,7 +152,6 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     float* wl = reinterpret_cast<float*>(smem + LY.wl);
     int* rpos = reinterpret_cast<int*>(smem + LY.rpos);
     int* rt0 = reinterpret_cast<int*>(smem + LY.rt0);
-    float* pw = reinterpret_cast<float*>(smem + LY.pw);
     int* sw = reinterpret_cast<int*>(smem + LY.sw);
     int* spath = reinterpret_cast<int*>(smem + LY.path);
 
@@ -179,9 +185,9 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
 
     // running state of rows g and g+8; O columns of this warp's dims
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    float o[4][4];
+    float o[NTW][4];
 #pragma unroll
-    for (int n = 0; n < 4; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < NTW; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     auto stage_block = [&](int b, int buf) {
         const uint32_t kb = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u);
@@ -224,12 +230,12 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring + (size_t)buf * (2 * BLK * LDK * 2));
         const uint32_t vs_a = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u) + BLK * LDK * 2u;
         const int key0 = b * BLK;
-        // S for this warp's 32 keys (4 n-tiles of 8)
-        float s[4][4];
+        // S for this warp's KPW keys (NTW n-tiles of 8)
+        float s[NTW][4];
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
+        for (int n = 0; n < NTW; ++n) {
             s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-            const __nv_bfloat16* krow = ks + (warp * 32 + n * 8 + g) * LDK + 2 * t;
+            const __nv_bfloat16* krow = ks + (warp * KPW + n * 8 + g) * LDK + 2 * t;
 #pragma unroll
             for (int ks8 = 0; ks8 < 8; ++ks8) {
                 const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16);
@@ -239,8 +245,8 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         }
         float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            const int kp = key0 + warp * 32 + n * 8 + 2 * t;
+        for (int n = 0; n < NTW; ++n) {
+            const int kp = key0 + warp * KPW + n * 8 + 2 * t;
             s[n][0] = (kp < ta) ? __fmul_rn(s[n][0], scale) : -INFINITY;
             s[n][1] = (kp + 1 < ta) ? __fmul_rn(s[n][1], scale) : -INFINITY;
             s[n][2] = (kp < tb) ? __fmul_rn(s[n][2], scale) : -INFINITY;
@@ -254,19 +260,24 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
         if (t == 0) { wmax[warp * FR + g] = ma; wmax[warp * FR + g + 8] = mb; }
         __syncthreads();
-        // block maximum per row over the four warps
-        ma = fmaxf(fmaxf(wmax[g], wmax[FR + g]), fmaxf(wmax[2 * FR + g], wmax[3 * FR + g]));
-        mb = fmaxf(fmaxf(wmax[g + 8], wmax[FR + g + 8]), fmaxf(wmax[2 * FR + g + 8], wmax[3 * FR + g + 8]));
+        // block maximum per row over the warps
+        ma = wmax[g];
+        mb = wmax[g + 8];
+#pragma unroll
+        for (int w = 1; w < FW; ++w) {
+            ma = fmaxf(ma, wmax[w * FR + g]);
+            mb = fmaxf(mb, wmax[w * FR + g + 8]);
+        }
         // P = exp(S - m) rounded to fp16 into shared memory; l sums the rounded values
         float la = 0.f, lb = 0.f;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
+        for (int n = 0; n < NTW; ++n) {
             const float p0 = (s[n][0] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][0], ma));
             const float p1 = (s[n][1] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][1], ma));
             const float p2 = (s[n][2] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][2], mb));
             const float p3 = (s[n][3] == -INFINITY) ? 0.f : expf(__fsub_rn(s[n][3], mb));
             const uint32_t ua = pack_f16(p0, p1), ub = pack_f16(p2, p3);
-            const int col = warp * 32 + n * 8 + 2 * t;
+            const int col = warp * KPW + n * 8 + 2 * t;
             *reinterpret_cast<uint32_t*>(ps + g * LDK + col) = ua;
             *reinterpret_cast<uint32_t*>(ps + (g + 8) * LDK + col) = ub;
             const __half2 q0 = *reinterpret_cast<const __half2*>(&ua);
@@ -280,12 +291,17 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 2));
         if (t == 0) { wl[warp * FR + g] = la; wl[warp * FR + g + 8] = lb; }
         __syncthreads();
-        la = __fadd_rn(__fadd_rn(__fadd_rn(wl[g], wl[FR + g]), wl[2 * FR + g]), wl[3 * FR + g]);
-        lb = __fadd_rn(__fadd_rn(__fadd_rn(wl[g + 8], wl[FR + g + 8]), wl[2 * FR + g + 8]), wl[3 * FR + g + 8]);
-        // O of the block for this warp's 32 dims: 8 k-steps of 16 keys x 4 n-tiles
-        float ob[4][4];
+        la = wl[g];
+        lb = wl[g + 8];
 #pragma unroll
-        for (int n = 0; n < 4; ++n) ob[n][0] = ob[n][1] = ob[n][2] = ob[n][3] = 0.f;
+        for (int w = 1; w < FW; ++w) {
+            la = __fadd_rn(la, wl[w * FR + g]);
+            lb = __fadd_rn(lb, wl[w * FR + g + 8]);
+        }
+        // O of the block for this warp's DPW dims: 8 k-steps of 16 keys x NTW n-tiles
+        float ob[NTW][4];
+#pragma unroll
+        for (int n = 0; n < NTW; ++n) ob[n][0] = ob[n][1] = ob[n][2] = ob[n][3] = 0.f;
         const int mtx = lane >> 3, mrow = lane & 7;
         const int key_off = (mtx & 1) * 8 + mrow, dim_off = (mtx >> 1) * 8;
 #pragma unroll
@@ -293,9 +309,9 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
             uint32_t a[4];
             ldsm_x4(sbase + LY.p + (uint32_t)((lane & 15) * LDK + kk * 16 + (lane >> 4) * 8) * 2u, a);
 #pragma unroll
-            for (int n = 0; n < 4; n += 2) {
+            for (int n = 0; n < NTW; n += 2) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vs_a + (uint32_t)((kk * 16 + key_off) * LDK + warp * 32 + n * 8 + dim_off) * 2u, b0, b1, b2, b3);
+                ldsm_x4_trans(vs_a + (uint32_t)((kk * 16 + key_off) * LDK + warp * DPW + n * 8 + dim_off) * 2u, b0, b1, b2, b3);
                 mma16816_f16(ob[n], a, bf2_to_h2(b0), bf2_to_h2(b1));
                 mma16816_f16(ob[n + 1], a, bf2_to_h2(b2), bf2_to_h2(b3));
             }
@@ -307,7 +323,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
             const float cb = expf(__fsub_rn(ma, mn));
             l_a = fmaf(l_a, ca, __fmul_rn(la, cb));
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
+            for (int n = 0; n < NTW; ++n) {
                 o[n][0] = fmaf(o[n][0], ca, __fmul_rn(ob[n][0], cb));
                 o[n][1] = fmaf(o[n][1], ca, __fmul_rn(ob[n][1], cb));
             }
@@ -319,7 +335,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
             const float cb = expf(__fsub_rn(mb, mn));
             l_b = fmaf(l_b, ca, __fmul_rn(lb, cb));
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
+            for (int n = 0; n < NTW; ++n) {
                 o[n][2] = fmaf(o[n][2], ca, __fmul_rn(ob[n][2], cb));
                 o[n][3] = fmaf(o[n][3], ca, __fmul_rn(ob[n][3], cb));
             }
@@ -329,8 +345,8 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     }
     // the committed state to shared memory: O by (row, dim), m and l per row
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
-        const int col = warp * 32 + n * 8 + 2 * t;
+    for (int n = 0; n < NTW; ++n) {
+        const int col = warp * DPW + n * 8 + 2 * t;
         *reinterpret_cast<float2*>(os + g * DH + col) = make_float2(o[n][0], o[n][1]);
         *reinterpret_cast<float2*>(os + (g + 8) * DH + col) = make_float2(o[n][2], o[n][3]);
     }
@@ -343,10 +359,10 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     const int Kc = prefill ? posmax + 1 : K;
     const int nc = (nr > 0 && Kc > t0min) ? Kc - t0min : 0;
     const int nt = nc + Q;
+    const uint32_t tk_a = sbase + LY.ring, tv_a = tk_a + (uint32_t)ring_keys * LDK * 2u;
     {
         const __nv_bfloat16* kth = kt + (size_t)hh * Qmax * DH;
         const __nv_bfloat16* vth = vt + (size_t)hh * Qmax * DH;
-        const uint32_t tk = sbase + LY.ring, tv = tk + (uint32_t)ring_keys * LDK * 2u;
         for (int i = tid; i < nt * (DH / 8); i += blockDim.x) {
             const int j = i >> 4, c8 = (i & 15) * 8;
             const __nv_bfloat16* ksrc;
@@ -354,94 +370,143 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
             if (j < nc) { ksrc = kh + (size_t)(t0min + j) * DH; vsrc = vh + (size_t)(t0min + j) * DH; }
             else { ksrc = kth + (size_t)(j - nc) * DH; vsrc = vth + (size_t)(j - nc) * DH; }
             const uint32_t off = (uint32_t)(j * LDK + c8) * 2u;
-            cp_async16(tk + off, ksrc + c8, 16);
-            cp_async16(tv + off, vsrc + c8, 16);
+            cp_async16(tk_a + off, ksrc + c8, 16);
+            cp_async16(tv_a + off, vsrc + c8, 16);
         }
         asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    const __nv_bfloat16* TK = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring);
-    const __nv_bfloat16* TV = TK + (size_t)ring_keys * LDK;
-    float* pwr = pw + warp * MAX_TAIL;
+    // tail values to fp16 in place (each element once; exact for |v| in the fp16 normal range)
+    {
+        uint32_t* tv32 = reinterpret_cast<uint32_t*>(smem + LY.ring + (size_t)ring_keys * LDK * 2);
+        for (int i = tid; i < nt * (DH / 2); i += blockDim.x) {
+            const int j = i / (DH / 2), c2 = (i % (DH / 2)) * 2;
+            uint32_t* w = tv32 + (j * LDK + c2) / 2;
+            *w = bf2_to_h2(*w);
+        }
+    }
+    __syncthreads();
     int* swr = sw + warp * MAX_TAIL;
     for (int r = warp; r < nr; r += FW) {
         const int pos = rpos[r], t0 = rt0[r];
-        const int n = pos - t0 + 1;
+        const int n = pos - t0 + 1;                  // tail keys, positions t0 .. pos
         const int Kr = prefill ? pos + 1 : K;
-        // scores: lane owns keys t0 + lane + 32 i
-        float sc[4], pj[4];
-        int slot[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = lane + 32 * i;
+        const int nkt = (n + 15) >> 4;               // 16-key tiles
+        // slot of each tail key in the staged rows (keys past n point at slot 0 and are masked)
+        for (int j = lane; j < nkt * 16; j += 32) {
             const int p = t0 + j;
-            slot[i] = 0;
-            sc[i] = -INFINITY;
-            if (j < n) slot[i] = (p < Kr) ? (p - t0min) : (nc + spath[r * PM + (p - K)]);
+            swr[j] = j < n ? ((p < Kr) ? (p - t0min) : (nc + spath[r * PM + (p - K)])) : 0;
         }
+        __syncwarp();
+        // S = q K^T with q in every row of the m16 tile (all rows of C equal), one
+        // 16-key tile at a time: keys in position order, dimensions in order
+        uint32_t qr[8][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (32 * i >= n) continue;                       // warp-uniform
-            const bool valid = lane + 32 * i < n;
-            const __nv_bfloat16* kr = TK + (size_t)slot[i] * LDK;
-            float acc = 0.f;
+        for (int ks8 = 0; ks8 < 8; ++ks8)
+            ldsm_x4(sbase + LY.q + (uint32_t)(r * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qr[ks8]);
+        float sc[MAX_TAIL / 16][2][2];               // [key tile][n-tile of 8][2 columns of this lane]
+        float tm = -INFINITY;
+        {
+            // all key tiles advance together through the 8 k-steps (independent accumulators)
+            float c[MAX_TAIL / 16][2][4];
+            uint32_t kaddr[MAX_TAIL / 16];
 #pragma unroll
-            for (int c = 0; c < DH / 8; ++c) {
-                const int4 kv = *reinterpret_cast<const int4*>(kr + c * 8);
-                const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
-                const int4 qv = *reinterpret_cast<const int4*>(qs + r * LDK + c * 8);
-                const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qv);
+            for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
+                // lane -> key row of the ldmatrix: keys kt16*16 + (lane & 7) [+8 for lanes 16-31], dims +8 for odd groups
+                const int krow = kt16 * 16 + (lane & 7) + ((lane >> 4) << 3);
+                kaddr[kt16] = tk_a + (uint32_t)(swr[kt16 < nkt ? krow : 0] * LDK + ((lane >> 3) & 1) * 8) * 2u;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc = fmaf(__low2float(q2[e]), __low2float(k2[e]), acc);
-                    acc = fmaf(__high2float(q2[e]), __high2float(k2[e]), acc);
+                for (int h8 = 0; h8 < 2; ++h8) c[kt16][h8][0] = c[kt16][h8][1] = c[kt16][h8][2] = c[kt16][h8][3] = 0.f;
+            }
+#pragma unroll
+            for (int ks8 = 0; ks8 < 8; ++ks8) {
+#pragma unroll
+                for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
+                    if (kt16 >= nkt) break;
+                    uint32_t bb[4];
+                    ldsm_x4(kaddr[kt16] + (uint32_t)(ks8 * 16) * 2u, bb);
+                    mma16816(c[kt16][0], qr[ks8], bb[0], bb[1]);
+                    mma16816(c[kt16][1], qr[ks8], bb[2], bb[3]);
                 }
             }
-            if (valid) sc[i] = __fmul_rn(acc, scale);
-        }
-        float tm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        tm = warp_max(tm);
-        float psum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            pj[i] = (sc[i] == -INFINITY) ? 0.f : expf(__fsub_rn(sc[i], tm));
-            psum = __fadd_rn(psum, pj[i]);
-        }
-        const float tl = warp_sum(psum);
+            for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
+                if (kt16 >= nkt) break;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = lane + 32 * i;
-            if (j < n) { pwr[j] = pj[i]; swr[j] = slot[i]; }
+                for (int e = 0; e < 2; ++e) {
+                    const int j0 = kt16 * 16 + 2 * t + e, j1 = j0 + 8;
+                    sc[kt16][0][e] = (j0 < n) ? __fmul_rn(c[kt16][0][e], scale) : -INFINITY;
+                    sc[kt16][1][e] = (j1 < n) ? __fmul_rn(c[kt16][1][e], scale) : -INFINITY;
+                    tm = fmaxf(tm, fmaxf(sc[kt16][0][e], sc[kt16][1][e]));
+                }
+            }
+        }
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+        // P = exp(S - tm) in fp32; tl sums them (every lane group holds the same
+        // row: the four lanes of a group cover it).  P V runs on tensor cores with
+        // P split into an fp16 value and its fp16 residual (about 22 bits of P).
+        float tl = 0.f;
+        uint32_t phi[MAX_TAIL / 16][2], plo[MAX_TAIL / 16][2];
+#pragma unroll
+        for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
+            if (kt16 >= nkt) break;
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float pv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    pv[e] = (sc[kt16][h8][e] == -INFINITY) ? 0.f : expf(__fsub_rn(sc[kt16][h8][e], tm));
+                    tl = __fadd_rn(tl, pv[e]);
+                }
+                const __half2 hi = __floats2half2_rn(pv[0], pv[1]);
+                const __half2 lo = __floats2half2_rn(__fsub_rn(pv[0], __low2float(hi)), __fsub_rn(pv[1], __high2float(hi)));
+                phi[kt16][h8] = *reinterpret_cast<const uint32_t*>(&hi);
+                plo[kt16][h8] = *reinterpret_cast<const uint32_t*>(&lo);
+            }
+        }
+        tl = __fadd_rn(tl, __shfl_xor_sync(0xffffffffu, tl, 1));
+        tl = __fadd_rn(tl, __shfl_xor_sync(0xffffffffu, tl, 2));
+        // O = P V over the key tiles; 16 dim tiles of 8 (lane group g holds row g: all equal)
+        float to[16][4];
+#pragma unroll
+        for (int n8 = 0; n8 < 16; ++n8) to[n8][0] = to[n8][1] = to[n8][2] = to[n8][3] = 0.f;
+#pragma unroll
+        for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
+            if (kt16 >= nkt) break;
+            const uint32_t ah[4] = {phi[kt16][0], phi[kt16][0], phi[kt16][1], phi[kt16][1]};
+            const uint32_t al[4] = {plo[kt16][0], plo[kt16][0], plo[kt16][1], plo[kt16][1]};
+            const int vrow = kt16 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const uint32_t vaddr = tv_a + (uint32_t)(swr[vrow] * LDK + (lane >> 4) * 8) * 2u;
+#pragma unroll
+            for (int n8 = 0; n8 < 16; n8 += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vaddr + (uint32_t)(n8 * 8) * 2u, b0, b1, b2, b3);
+                mma16816_f16(to[n8], ah, b0, b1);
+                mma16816_f16(to[n8 + 1], ah, b2, b3);
+                mma16816_f16(to[n8], al, b0, b1);
+                mma16816_f16(to[n8 + 1], al, b2, b3);
+            }
         }
         __syncwarp();
-        // P V in key order; lane owns dims 4 lane .. 4 lane + 3
-        float to[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < n; ++j) {
-            const float pv = pwr[j];
-            const uint2 vv = *reinterpret_cast<const uint2*>(TV + (size_t)swr[j] * LDK + lane * 4);
-            const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&vv.x);
-            const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&vv.y);
-            to[0] = fmaf(pv, __low2float(v01), to[0]);
-            to[1] = fmaf(pv, __high2float(v01), to[1]);
-            to[2] = fmaf(pv, __low2float(v23), to[2]);
-            to[3] = fmaf(pv, __high2float(v23), to[3]);
+        // merge the tail block after the committed blocks, normalise; lane group g = 0
+        // stores (lanes 0-3 hold row 0's columns 2t, 2t+1 of every dim tile)
+        if (g == 0) {
+            const float m = wmax[r], l = wl[r];
+            const float mn = fmaxf(m, tm);
+            const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
+            const float cb = expf(__fsub_rn(tm, mn));
+            const float inv = 1.0f / fmaf(l, ca, __fmul_rn(tl, cb));
+            __nv_bfloat16* op = out + (size_t)(r0 + r) * H * DH + hh * DH;
+#pragma unroll
+            for (int n8 = 0; n8 < 16; ++n8) {
+                const int col = n8 * 8 + 2 * t;
+                const float2 oc = *reinterpret_cast<const float2*>(os + r * DH + col);
+                const float o0 = fmaf(oc.x, ca, __fmul_rn(to[n8][0], cb));
+                const float o1 = fmaf(oc.y, ca, __fmul_rn(to[n8][1], cb));
+                *reinterpret_cast<__nv_bfloat162*>(op + col) = __floats2bfloat162_rn(__fmul_rn(o0, inv), __fmul_rn(o1, inv));
+            }
         }
-        __syncwarp();
-        // merge the tail block after the committed blocks, normalise
-        const float m = wmax[r], l = wl[r];
-        const float4 oc = *reinterpret_cast<const float4*>(os + r * DH + lane * 4);
-        const float mn = fmaxf(m, tm);
-        const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
-        const float cb = expf(__fsub_rn(tm, mn));
-        const float lt = fmaf(l, ca, __fmul_rn(tl, cb));
-        const float o0 = fmaf(oc.x, ca, __fmul_rn(to[0], cb));
-        const float o1 = fmaf(oc.y, ca, __fmul_rn(to[1], cb));
-        const float o2 = fmaf(oc.z, ca, __fmul_rn(to[2], cb));
-        const float o3 = fmaf(oc.w, ca, __fmul_rn(to[3], cb));
-        const float inv = 1.0f / lt;
-        __nv_bfloat16* op = out + (size_t)(r0 + r) * H * DH + hh * DH + lane * 4;
-        *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(__fmul_rn(o0, inv), __fmul_rn(o1, inv));
-        *reinterpret_cast<__nv_bfloat162*>(op + 2) = __floats2bfloat162_rn(__fmul_rn(o2, inv), __fmul_rn(o3, inv));
     }
 }
 
