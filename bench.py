@@ -63,9 +63,10 @@ def gemm_bytes_per_call(cfg, Q: float, need_rows: float) -> float:
 
 
 # DRAM bytes (read + write) of the GEMM launches of one packed call (32 layers
-# x (QKV + O + gate/up + down) + LM head), from the ncu captures of the current
-# kernel at 60 packed rows summarised in profiles/; None once the kernel changes.
-GEMM_TRAFFIC_PER_CALL = 13.856e9
+# x (QKV + O + gate/up + down) + LM head), from the ncu capture of the current
+# kernel's launches in a decode call summarised in profiles/; None once the
+# kernel changes.
+GEMM_TRAFFIC_PER_CALL = 13.715e9
 
 
 def measured_peaks():
