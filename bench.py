@@ -69,6 +69,19 @@ def gemm_bytes_per_call(cfg, Q: float, need_rows: float) -> float:
 GEMM_TRAFFIC_PER_CALL = 13.715e9
 
 
+def aggregate_replicas(new_tokens: float, decode_s: float, wall: float, device: str = "cpu"):
+    """Whole-job figures of independent replicas (one request per rank): tokens
+    summed over the ranks, decode and wall-clock times the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(new_tokens), float(decode_s), float(wall)
+    t = torch.tensor([new_tokens, decode_s, wall], dtype=torch.float64, device=device)
+    g = [torch.zeros_like(t) for _ in range(dist.get_world_size())]
+    dist.all_gather(g, t)
+    return sum(float(x[0]) for x in g), max(float(x[1]) for x in g), max(float(x[2]) for x in g)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -235,12 +248,7 @@ def main():
     call_ms = decode_s / calls * 1e3
     # aggregate over ranks: total tokens / max time
     if world > 1:
-        t = torch.tensor([new_tokens, decode_s, wall], dtype=torch.float64, device=f"cuda:{local}")
-        g = [torch.zeros_like(t) for _ in range(world)]
-        torch.distributed.all_gather(g, t)
-        tot_tok = sum(float(x[0]) for x in g)
-        max_dec = max(float(x[1]) for x in g)
-        wall = max(float(x[2]) for x in g)
+        tot_tok, max_dec, wall = aggregate_replicas(new_tokens, decode_s, wall, f"cuda:{local}")
         tps = tot_tok / max_dec
 
     # autoregressive decode on the same kernels
