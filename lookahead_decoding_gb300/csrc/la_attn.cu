@@ -16,12 +16,9 @@
 //     row's running state in block order.
 //   * positions [t0, pos] — at most 128 keys per row, from the cache
 //     (committed) or the call's temporary rows on the row's path (in-call),
-//     staged in shared memory once per tile; one softmax block per row:
-//     S = q K^T on tensor cores (the row's query fills an m16 tile and each
-//     lane's ldmatrix row address points at the staged key of its position,
-//     so the keys enter the products in position order); P in fp32, and
-//     P V on tensor cores with P as an fp16 value plus its fp16 residual;
-//     merged after the blocks, then normalised.
+//     staged in shared memory once per tile; one softmax block per row on
+//     CUDA cores in fp32 (a lane per key for S, four dimensions per lane for
+//     P V, keys in position order); merged after the blocks, then normalised.
 // A row's arithmetic therefore depends only on its query, its position and
 // the keys it sees — the same whether it is decoded alone or packed.
 #include "la_common.cuh"
@@ -111,8 +108,8 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;           // K and V rows, bf16
     L.q = L.ring + L.ring_bytes;                                    // [FR][LDK] bf16
     L.p = L.q + FR * LDK * 2;                                       // [FR][LDK] fp16
-    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32
-    L.wmax = L.o + FR * DH * 4;                                     // [FW][FR] fp32
+    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32, then [FW][DH] fp32 queries
+    L.wmax = L.o + (FR + FW) * DH * 4;                              // [FW][FR] fp32
     L.wl = L.wmax + FW * FR * 4;                                    // [FW][FR] fp32
     L.rpos = L.wl + FW * FR * 4;                                    // [FR] int
     L.rt0 = L.rpos + FR * 4;                                        // [FR] int
@@ -152,6 +149,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     float* wl = reinterpret_cast<float*>(smem + LY.wl);
     int* rpos = reinterpret_cast<int*>(smem + LY.rpos);
     int* rt0 = reinterpret_cast<int*>(smem + LY.rt0);
+    float* pw = reinterpret_cast<float*>(smem + LY.pw);
     int* sw = reinterpret_cast<int*>(smem + LY.sw);
     int* spath = reinterpret_cast<int*>(smem + LY.path);
 
@@ -376,137 +374,110 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    // tail values to fp16 in place (each element once; exact for |v| in the fp16 normal range)
-    {
-        uint32_t* tv32 = reinterpret_cast<uint32_t*>(smem + LY.ring + (size_t)ring_keys * LDK * 2);
-        for (int i = tid; i < nt * (DH / 2); i += blockDim.x) {
-            const int j = i / (DH / 2), c2 = (i % (DH / 2)) * 2;
-            uint32_t* w = tv32 + (j * LDK + c2) / 2;
-            *w = bf2_to_h2(*w);
-        }
-    }
-    __syncthreads();
+    const __nv_bfloat16* TK = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring);
+    const __nv_bfloat16* TV = TK + (size_t)ring_keys * LDK;
     int* swr = sw + warp * MAX_TAIL;
+    float* pwr = pw + warp * MAX_TAIL;
+    float* qf = os + FR * DH;                        // per-warp fp32 copy of the row's query (after O)
+    qf += warp * DH;
     for (int r = warp; r < nr; r += FW) {
         const int pos = rpos[r], t0 = rt0[r];
         const int n = pos - t0 + 1;                  // tail keys, positions t0 .. pos
         const int Kr = prefill ? pos + 1 : K;
-        const int nkt = (n + 15) >> 4;               // 16-key tiles
-        // slot of each tail key in the staged rows (keys past n point at slot 0 and are masked)
-        for (int j = lane; j < nkt * 16; j += 32) {
-            const int p = t0 + j;
-            swr[j] = j < n ? ((p < Kr) ? (p - t0min) : (nc + spath[r * PM + (p - K)])) : 0;
-        }
-        __syncwarp();
-        // S = q K^T with q in every row of the m16 tile (all rows of C equal), one
-        // 16-key tile at a time: keys in position order, dimensions in order
-        uint32_t qr[8][4];
-#pragma unroll
-        for (int ks8 = 0; ks8 < 8; ++ks8)
-            ldsm_x4(sbase + LY.q + (uint32_t)(r * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qr[ks8]);
-        float sc[MAX_TAIL / 16][2][2];               // [key tile][n-tile of 8][2 columns of this lane]
-        float tm = -INFINITY;
         {
-            // all key tiles advance together through the 8 k-steps (independent accumulators)
-            float c[MAX_TAIL / 16][2][4];
-            uint32_t kaddr[MAX_TAIL / 16];
-#pragma unroll
-            for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
-                // lane -> key row of the ldmatrix: keys kt16*16 + (lane & 7) [+8 for lanes 16-31], dims +8 for odd groups
-                const int krow = kt16 * 16 + (lane & 7) + ((lane >> 4) << 3);
-                kaddr[kt16] = tk_a + (uint32_t)(swr[kt16 < nkt ? krow : 0] * LDK + ((lane >> 3) & 1) * 8) * 2u;
-#pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) c[kt16][h8][0] = c[kt16][h8][1] = c[kt16][h8][2] = c[kt16][h8][3] = 0.f;
-            }
-#pragma unroll
-            for (int ks8 = 0; ks8 < 8; ++ks8) {
-#pragma unroll
-                for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
-                    if (kt16 >= nkt) break;
-                    uint32_t bb[4];
-                    ldsm_x4(kaddr[kt16] + (uint32_t)(ks8 * 16) * 2u, bb);
-                    mma16816(c[kt16][0], qr[ks8], bb[0], bb[1]);
-                    mma16816(c[kt16][1], qr[ks8], bb[2], bb[3]);
-                }
-            }
-#pragma unroll
-            for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
-                if (kt16 >= nkt) break;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j0 = kt16 * 16 + 2 * t + e, j1 = j0 + 8;
-                    sc[kt16][0][e] = (j0 < n) ? __fmul_rn(c[kt16][0][e], scale) : -INFINITY;
-                    sc[kt16][1][e] = (j1 < n) ? __fmul_rn(c[kt16][1][e], scale) : -INFINITY;
-                    tm = fmaxf(tm, fmaxf(sc[kt16][0][e], sc[kt16][1][e]));
-                }
-            }
+            const uint2 qv = *reinterpret_cast<const uint2*>(qs + r * LDK + lane * 4);
+            *reinterpret_cast<float4*>(qf + lane * 4) =
+                make_float4(__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xffff0000u),
+                            __uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xffff0000u));
         }
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
-        // P = exp(S - tm) in fp32; tl sums them (every lane group holds the same
-        // row: the four lanes of a group cover it).  P V runs on tensor cores with
-        // P split into an fp16 value and its fp16 residual (about 22 bits of P).
-        float tl = 0.f;
-        uint32_t phi[MAX_TAIL / 16][2], plo[MAX_TAIL / 16][2];
+        // scores: lane owns keys t0 + lane + 32 i; dimensions in order
+        float sc[MAX_TAIL / 32];
+        int slot[MAX_TAIL / 32];
 #pragma unroll
-        for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
-            if (kt16 >= nkt) break;
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                float pv[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    pv[e] = (sc[kt16][h8][e] == -INFINITY) ? 0.f : expf(__fsub_rn(sc[kt16][h8][e], tm));
-                    tl = __fadd_rn(tl, pv[e]);
-                }
-                const __half2 hi = __floats2half2_rn(pv[0], pv[1]);
-                const __half2 lo = __floats2half2_rn(__fsub_rn(pv[0], __low2float(hi)), __fsub_rn(pv[1], __high2float(hi)));
-                phi[kt16][h8] = *reinterpret_cast<const uint32_t*>(&hi);
-                plo[kt16][h8] = *reinterpret_cast<const uint32_t*>(&lo);
-            }
-        }
-        tl = __fadd_rn(tl, __shfl_xor_sync(0xffffffffu, tl, 1));
-        tl = __fadd_rn(tl, __shfl_xor_sync(0xffffffffu, tl, 2));
-        // O = P V over the key tiles; 16 dim tiles of 8 (lane group g holds row g: all equal)
-        float to[16][4];
-#pragma unroll
-        for (int n8 = 0; n8 < 16; ++n8) to[n8][0] = to[n8][1] = to[n8][2] = to[n8][3] = 0.f;
-#pragma unroll
-        for (int kt16 = 0; kt16 < MAX_TAIL / 16; ++kt16) {
-            if (kt16 >= nkt) break;
-            const uint32_t ah[4] = {phi[kt16][0], phi[kt16][0], phi[kt16][1], phi[kt16][1]};
-            const uint32_t al[4] = {plo[kt16][0], plo[kt16][0], plo[kt16][1], plo[kt16][1]};
-            const int vrow = kt16 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const uint32_t vaddr = tv_a + (uint32_t)(swr[vrow] * LDK + (lane >> 4) * 8) * 2u;
-#pragma unroll
-            for (int n8 = 0; n8 < 16; n8 += 2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vaddr + (uint32_t)(n8 * 8) * 2u, b0, b1, b2, b3);
-                mma16816_f16(to[n8], ah, b0, b1);
-                mma16816_f16(to[n8 + 1], ah, b2, b3);
-                mma16816_f16(to[n8], al, b0, b1);
-                mma16816_f16(to[n8 + 1], al, b2, b3);
-            }
+        for (int i = 0; i < MAX_TAIL / 32; ++i) {
+            const int j = lane + 32 * i;
+            const int p = t0 + j;
+            slot[i] = (j < n) ? ((p < Kr) ? (p - t0min) : (nc + spath[r * PM + (p - K)])) : 0;
         }
         __syncwarp();
-        // merge the tail block after the committed blocks, normalise; lane group g = 0
-        // stores (lanes 0-3 hold row 0's columns 2t, 2t+1 of every dim tile)
-        if (g == 0) {
-            const float m = wmax[r], l = wl[r];
-            const float mn = fmaxf(m, tm);
-            const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
-            const float cb = expf(__fsub_rn(tm, mn));
-            const float inv = 1.0f / fmaf(l, ca, __fmul_rn(tl, cb));
-            __nv_bfloat16* op = out + (size_t)(r0 + r) * H * DH + hh * DH;
 #pragma unroll
-            for (int n8 = 0; n8 < 16; ++n8) {
-                const int col = n8 * 8 + 2 * t;
-                const float2 oc = *reinterpret_cast<const float2*>(os + r * DH + col);
-                const float o0 = fmaf(oc.x, ca, __fmul_rn(to[n8][0], cb));
-                const float o1 = fmaf(oc.y, ca, __fmul_rn(to[n8][1], cb));
-                *reinterpret_cast<__nv_bfloat162*>(op + col) = __floats2bfloat162_rn(__fmul_rn(o0, inv), __fmul_rn(o1, inv));
+        for (int i = 0; i < MAX_TAIL / 32; ++i) {
+            sc[i] = -INFINITY;
+            if (32 * i >= n) continue;                   // warp-uniform
+            const __nv_bfloat16* kr = TK + (size_t)slot[i] * LDK;
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < DH / 8; ++c) {
+                const uint4 kv = *reinterpret_cast<const uint4*>(kr + c * 8);
+                const float4 qa = *reinterpret_cast<const float4*>(qf + c * 8);
+                const float4 qb = *reinterpret_cast<const float4*>(qf + c * 8 + 4);
+                acc = fmaf(qa.x, __uint_as_float(kv.x << 16), acc);
+                acc = fmaf(qa.y, __uint_as_float(kv.x & 0xffff0000u), acc);
+                acc = fmaf(qa.z, __uint_as_float(kv.y << 16), acc);
+                acc = fmaf(qa.w, __uint_as_float(kv.y & 0xffff0000u), acc);
+                acc = fmaf(qb.x, __uint_as_float(kv.z << 16), acc);
+                acc = fmaf(qb.y, __uint_as_float(kv.z & 0xffff0000u), acc);
+                acc = fmaf(qb.z, __uint_as_float(kv.w << 16), acc);
+                acc = fmaf(qb.w, __uint_as_float(kv.w & 0xffff0000u), acc);
+            }
+            if (lane + 32 * i < n) sc[i] = __fmul_rn(acc, scale);
+        }
+        float tm = sc[0];
+#pragma unroll
+        for (int i = 1; i < MAX_TAIL / 32; ++i) tm = fmaxf(tm, sc[i]);
+        tm = warp_max(tm);
+        float psum = 0.f;
+#pragma unroll
+        for (int i = 0; i < MAX_TAIL / 32; ++i) {
+            const float pv = (sc[i] == -INFINITY) ? 0.f : expf(__fsub_rn(sc[i], tm));
+            psum = __fadd_rn(psum, pv);
+            const int j = lane + 32 * i;
+            if (j < n) { pwr[j] = pv; swr[j] = slot[i]; }
+        }
+        const float tl = warp_sum(psum);
+        __syncwarp();
+        // P V in key order; lane owns dims 4 lane .. 4 lane + 3
+        float to[4] = {0.f, 0.f, 0.f, 0.f};
+        int j = 0;
+        for (; j + 4 <= n; j += 4) {
+            uint2 vv[4];
+            float pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                pk[u] = pwr[j + u];
+                vv[u] = *reinterpret_cast<const uint2*>(TV + (size_t)swr[j + u] * LDK + lane * 4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                to[0] = fmaf(pk[u], __uint_as_float(vv[u].x << 16), to[0]);
+                to[1] = fmaf(pk[u], __uint_as_float(vv[u].x & 0xffff0000u), to[1]);
+                to[2] = fmaf(pk[u], __uint_as_float(vv[u].y << 16), to[2]);
+                to[3] = fmaf(pk[u], __uint_as_float(vv[u].y & 0xffff0000u), to[3]);
             }
         }
+        for (; j < n; ++j) {
+            const float pk = pwr[j];
+            const uint2 vv = *reinterpret_cast<const uint2*>(TV + (size_t)swr[j] * LDK + lane * 4);
+            to[0] = fmaf(pk, __uint_as_float(vv.x << 16), to[0]);
+            to[1] = fmaf(pk, __uint_as_float(vv.x & 0xffff0000u), to[1]);
+            to[2] = fmaf(pk, __uint_as_float(vv.y << 16), to[2]);
+            to[3] = fmaf(pk, __uint_as_float(vv.y & 0xffff0000u), to[3]);
+        }
+        __syncwarp();
+        // merge the tail block after the committed blocks, normalise
+        const float m = wmax[r], l = wl[r];
+        const float4 oc = *reinterpret_cast<const float4*>(os + r * DH + lane * 4);
+        const float mn = fmaxf(m, tm);
+        const float ca = (m == -INFINITY) ? 0.f : expf(__fsub_rn(m, mn));
+        const float cb = expf(__fsub_rn(tm, mn));
+        const float inv = 1.0f / fmaf(l, ca, __fmul_rn(tl, cb));
+        const float o0 = fmaf(oc.x, ca, __fmul_rn(to[0], cb));
+        const float o1 = fmaf(oc.y, ca, __fmul_rn(to[1], cb));
+        const float o2 = fmaf(oc.z, ca, __fmul_rn(to[2], cb));
+        const float o3 = fmaf(oc.w, ca, __fmul_rn(to[3], cb));
+        __nv_bfloat16* op = out + (size_t)(r0 + r) * H * DH + hh * DH + lane * 4;
+        *reinterpret_cast<__nv_bfloat162*>(op) = __floats2bfloat162_rn(__fmul_rn(o0, inv), __fmul_rn(o1, inv));
+        *reinterpret_cast<__nv_bfloat162*>(op + 2) = __floats2bfloat162_rn(__fmul_rn(o2, inv), __fmul_rn(o3, inv));
     }
 }
 
