@@ -127,14 +127,8 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
-    if (h->err != 0 || (sel != SEL_PREFILL && h->done != 0)) return;
-    const int rows = rows_sel(h, sel);
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
-    if (r0 >= rows) return;
-    const int nr = min(FR, rows - r0);
     const int prefill = (sel == SEL_PREFILL);
-    const int K = prefill ? 0 : h->K;
-    const int Q = prefill ? 0 : h->Q;                 // the call's temporary K/V rows
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int PM = d.PMAX;
@@ -152,40 +146,8 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     float* pw = reinterpret_cast<float*>(smem + LY.pw);
     int* sw = reinterpret_cast<int*>(smem + LY.sw);
     int* spath = reinterpret_cast<int*>(smem + LY.path);
-
-    // rows of the tile: positions, split points, paths; queries (cp.async)
-    if (tid < FR) {
-        const int r = r0 + tid;
-        const int pos = tid < nr ? d.row_pos[r] : -1;
-        rpos[tid] = pos;
-        rt0[tid] = pos >= 0 ? t0_of(pos, TB) : 0;
-    }
-    if (!prefill)
-        for (int i = tid; i < nr * PM; i += blockDim.x) spath[i] = d.row_path[(size_t)(r0 + i / PM) * PM + i % PM];
-    const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
-    for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
-        const int r = i >> 4, c8 = (i & 15) * 8;
-        const int ok = r < nr;
-        cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(ok ? r0 + r : r0) * DH + c8, ok ? 16 : 0);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    __syncthreads();
-    int t0max = 0, t0min = 0x7fffffff, posmax = 0;
-    for (int r = 0; r < nr; ++r) {
-        t0max = max(t0max, rt0[r]);
-        t0min = min(t0min, rt0[r]);
-        posmax = max(posmax, rpos[r]);
-    }
-    const int nb = (t0max + BLK - 1) / BLK;
     const __nv_bfloat16* kh = kc + (size_t)hh * max_ctx * DH;
     const __nv_bfloat16* vh = vc + (size_t)hh * max_ctx * DH;
-    const int ta = rt0[g], tb = rt0[g + 8];             // split points of this thread's two rows
-
-    // running state of rows g and g+8; O columns of this warp's dims
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    float o[NTW][4];
-#pragma unroll
-    for (int n = 0; n < NTW; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     auto stage_block = [&](int b, int buf) {
         const uint32_t kb = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u);
@@ -202,11 +164,59 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
+    // Issued before the header is read, so the latencies overlap: the tile's
+    // row positions and paths and its queries (cp.async group 1); the first
+    // tile, which every call fills, also stages committed block 0 (group 2).
+    // Every grid row is below Qcap, and block 0 lies in the cache, so all of
+    // it is in bounds whatever the call's row count.
+    int pos_raw = 0;
+    if (tid < FR) pos_raw = d.row_pos[r0 + tid];
+    if (!prefill)
+        for (int i = tid; i < FR * PM; i += blockDim.x) spath[i] = d.row_path[(size_t)(r0 + i / PM) * PM + i % PM];
+    const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
+    for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
+        const int r = i >> 4, c8 = (i & 15) * 8;
+        cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(r0 + r) * DH + c8, 16);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const bool spec0 = (blockIdx.y == 0);
+    if (spec0) stage_block(0, 0);
+
+    const int h_err = h->err, h_done = h->done, rows = rows_sel(h, sel);
+    if (h_err != 0 || (sel != SEL_PREFILL && h_done != 0) || r0 >= rows) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");    // no copy outlives the CTA
+        return;
+    }
+    const int nr = min(FR, rows - r0);
+    const int K = prefill ? 0 : h->K;
+    const int Q = prefill ? 0 : h->Q;                 // the call's temporary K/V rows
+    if (tid < FR) {
+        const int pos = tid < nr ? pos_raw : -1;
+        rpos[tid] = pos;
+        rt0[tid] = pos >= 0 ? t0_of(pos, TB) : 0;
+    }
+    __syncthreads();
+    int t0max = 0, t0min = 0x7fffffff, posmax = 0;
+    for (int r = 0; r < nr; ++r) {
+        t0max = max(t0max, rt0[r]);
+        t0min = min(t0min, rt0[r]);
+        posmax = max(posmax, rpos[r]);
+    }
+    const int nb = (t0max + BLK - 1) / BLK;
+    if (!spec0 && nb > 0) stage_block(0, 0);
+    const int ta = rt0[g], tb = rt0[g + 8];             // split points of this thread's two rows
+
+    // running state of rows g and g+8; O columns of this warp's dims
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    float o[NTW][4];
+#pragma unroll
+    for (int n = 0; n < NTW; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
     // Q fragments (A operand of S = Q K^T) for the 8 k-steps, from shared memory
     if (nb > 0) {
-        stage_block(0, 0);
         asm volatile("cp.async.wait_group %0;" ::"n"(1) : "memory");     // the queries, not block 0
     } else {
+        // no committed block (block 0 of the first tile still lands before the ring is reused)
         asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
     }
     __syncthreads();

@@ -40,17 +40,43 @@ __device__ __forceinline__ bool skip_call(const LaHdr* h, int sel) {
 // embedding: x[q][:] = E[tok[q]]  (fp32 residual stream)
 // ---------------------------------------------------------------------------
 template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+
+template <typename T>
 __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
-    int q = blockIdx.x;
+    const int q = blockIdx.x;
     if (q >= rows_of(h, sel)) return;
-    int tok = d.row_tok[q];
+    const int tok = d.row_tok[q];
     if (tok < 0 || tok >= d.V) { la_set_err(d.hdr, LA_EDEVICE); return; }
     const T* e = emb + (size_t)tok * dm;
-    for (int i = threadIdx.x; i < dm; i += blockDim.x) x[(size_t)q * dm + i] = to_f(e[i]);
+    float* xr = x + (size_t)q * dm;
+    // four float4 groups a thread in flight, then their stores
+    constexpr int B = 4;
+    for (int i0 = threadIdx.x * 4; i0 < dm; i0 += B * blockDim.x * 4) {
+        float4 v[B];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int i = i0 + k * blockDim.x * 4;
+            if (i < dm) v[k] = load4<T>(e + i);
+        }
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int i = i0 + k * blockDim.x * 4;
+            if (i < dm) *reinterpret_cast<float4*>(xr + i) = v[k];
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -73,25 +99,38 @@ __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g,
     // the row stays in registers: up to 2 float4 per thread (256 threads for
     // d_model <= 2048, 1024 threads up to 8192)
     constexpr int MAXV = 2;
-    float4 v[MAXV];
+    float4 v[MAXV], add[MAXV], gv[MAXV];
+    bool upd[MAXV];
+    // every load (the row, the split partials, the gains) is issued before
+    // the first store of the updated row
+#pragma unroll
+    for (int k = 0; k < MAXV; ++k) {
+        const int i = (k * blockDim.x + threadIdx.x) * 4;
+        upd[k] = false;
+        if (i < dm) {
+            v[k] = *reinterpret_cast<const float4*>(xr + i);
+            gv[k] = load4<T>(g + i);
+            if (resid.ws) {
+                const int tile = i >> 7;
+                const int nseg = la_split_nseg(resid, tile);
+                if (nseg > 1) {
+                    add[k] = la_split_sum4(resid, tile, src >> 8, (size_t)(src & 255) * 128 + (i & 127), nseg);
+                    upd[k] = true;
+                }
+            }
+        }
+    }
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < MAXV; ++k) {
         const int i = (k * blockDim.x + threadIdx.x) * 4;
         if (i < dm) {
-            v[k] = *reinterpret_cast<const float4*>(xr + i);
-            if (resid.ws) {
-                const int tile = i >> 7;
-                const int nseg = la_split_nseg(resid, tile);
-                if (nseg > 1) {
-                    const size_t off = (size_t)(src & 255) * 128 + (i & 127);
-                    const float4 sum = la_split_sum4(resid, tile, src >> 8, off, nseg);
-                    v[k].x = v[k].x + sum.x;
-                    v[k].y = v[k].y + sum.y;
-                    v[k].z = v[k].z + sum.z;
-                    v[k].w = v[k].w + sum.w;
-                    *reinterpret_cast<float4*>(xr + i) = v[k];
-                }
+            if (upd[k]) {
+                v[k].x = v[k].x + add[k].x;
+                v[k].y = v[k].y + add[k].y;
+                v[k].z = v[k].z + add[k].z;
+                v[k].w = v[k].w + add[k].w;
+                *reinterpret_cast<float4*>(xr + i) = v[k];
             }
             ss = fmaf(v[k].x, v[k].x, ss);
             ss = fmaf(v[k].y, v[k].y, ss);
@@ -116,10 +155,10 @@ __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g,
     for (int k = 0; k < MAXV; ++k) {
         const int i = (k * blockDim.x + threadIdx.x) * 4;
         if (i < dm) {
-            yr[i + 0] = from_f<T>(v[k].x * r * to_f(g[i + 0]));
-            yr[i + 1] = from_f<T>(v[k].y * r * to_f(g[i + 1]));
-            yr[i + 2] = from_f<T>(v[k].z * r * to_f(g[i + 2]));
-            yr[i + 3] = from_f<T>(v[k].w * r * to_f(g[i + 3]));
+            yr[i + 0] = from_f<T>(v[k].x * r * gv[k].x);
+            yr[i + 1] = from_f<T>(v[k].y * r * gv[k].y);
+            yr[i + 2] = from_f<T>(v[k].z * r * gv[k].z);
+            yr[i + 3] = from_f<T>(v[k].w * r * gv[k].w);
         }
     }
 }
@@ -160,6 +199,8 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     const int sv = sp.ws ? la_split_nseg(sp, nv >> 7) : 1;
     float qa = to_f(qkv_at(row, q, nq + i, sp, sq)), qb = to_f(qkv_at(row, q, nq + i + half, sp, sq));
     float ka = to_f(qkv_at(row, q, nk + i, sp, sk)), kb = to_f(qkv_at(row, q, nk + i + half, sp, sk));
+    // all loads before the first store (the stores may alias them as far as the compiler knows)
+    const T va = qkv_at(row, q, nv + i, sp, sv), vb = qkv_at(row, q, nv + i + half, sp, sv);
     T* qo = qbuf + ((size_t)hh * Qcap + q) * dh;
     qo[i] = from_f<T>(qa * c - qb * s);
     qo[i + half] = from_f<T>(qb * c + qa * s);
@@ -168,8 +209,8 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     T* vo = vdst + ((size_t)hh * stride + slot) * dh;
     ko[i] = from_f<T>(ka * c - kb * s);
     ko[i + half] = from_f<T>(kb * c + ka * s);
-    vo[i] = qkv_at(row, q, nv + i, sp, sv);
-    vo[i + half] = qkv_at(row, q, nv + i + half, sp, sv);
+    vo[i] = va;
+    vo[i + half] = vb;
 }
 
 // SwiGLU of the gate/up GEMM's split tiles: act = silu(gate) * up with gate
@@ -493,7 +534,7 @@ void la_launch_rope_table(float* rcos, float* rsin, int n_pos, int dh, double th
 
 template <typename T>
 void la_launch_embed_t(const LaDev& d, cudaStream_t st, const void* emb, float* x, int dm, int sel, int rows_cap) {
-    la_launch_pdl(k_embed<T>, dim3(rows_cap), dim3(128), 0, st, d, (const T*)emb, x, dm, sel);
+    la_launch_pdl(k_embed<T>, dim3(rows_cap), dim3(256), 0, st, d, (const T*)emb, x, dm, sel);
 }
 void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb, float* x, int dm, int sel, int rows_cap) {
     if (dtype == LA_F32) la_launch_embed_t<float>(d, st, emb, x, dm, sel, rows_cap);
