@@ -124,8 +124,6 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
                                                       const __nv_bfloat16* vc, const __nv_bfloat16* kt,
                                                       const __nv_bfloat16* vt, __nv_bfloat16* out, int sel, int Qcap,
                                                       int max_ctx, int Qmax, int TB, int H, int ring_keys) {
-    la_pdl_wait();
-    la_pdl_trigger();
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
     const int prefill = (sel == SEL_PREFILL);
@@ -164,29 +162,31 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
-    // Issued before the header is read, so the latencies overlap: the tile's
-    // row positions and paths and its queries (cp.async group 1); the first
-    // tile, which every call fills, also stages committed block 0 (group 2).
-    // Every grid row is below Qcap, and block 0 lies in the cache, so all of
-    // it is in bounds whatever the call's row count.
+    // Before the wait (la_common.cuh): the header, and in a decode call the
+    // tile's row positions and paths (written by the pack kernel) and, for
+    // the first tile, which every call fills, committed block 0 of the cache
+    // (written by earlier calls; cp.async group 1).  After the wait: the
+    // queries, which the kernel before this one writes (group 2).  Every grid
+    // row is below Qcap and block 0 lies in the cache, so all of it is in
+    // bounds whatever the call's row count.
+    const int h_err = h->err, h_done = h->done, rows = rows_sel(h, sel);
+    if (h_err != 0 || (sel != SEL_PREFILL && h_done != 0) || r0 >= rows) return;
+    const bool spec0 = (blockIdx.y == 0) && !prefill;
     int pos_raw = 0;
-    if (tid < FR) pos_raw = d.row_pos[r0 + tid];
-    if (!prefill)
+    if (!prefill) {
+        if (tid < FR) pos_raw = d.row_pos[r0 + tid];
         for (int i = tid; i < FR * PM; i += blockDim.x) spath[i] = d.row_path[(size_t)(r0 + i / PM) * PM + i % PM];
+        if (spec0) stage_block(0, 0);
+    }
+    la_pdl_wait();
+    la_pdl_trigger();
+    if (prefill && tid < FR) pos_raw = d.row_pos[r0 + tid];
     const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
     for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
         const int r = i >> 4, c8 = (i & 15) * 8;
         cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(r0 + r) * DH + c8, 16);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    const bool spec0 = (blockIdx.y == 0);
-    if (spec0) stage_block(0, 0);
-
-    const int h_err = h->err, h_done = h->done, rows = rows_sel(h, sel);
-    if (h_err != 0 || (sel != SEL_PREFILL && h_done != 0) || r0 >= rows) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");    // no copy outlives the CTA
-        return;
-    }
     const int nr = min(FR, rows - r0);
     const int K = prefill ? 0 : h->K;
     const int Q = prefill ? 0 : h->Q;                 // the call's temporary K/V rows
@@ -213,10 +213,11 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     for (int n = 0; n < NTW; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     // Q fragments (A operand of S = Q K^T) for the 8 k-steps, from shared memory
-    if (nb > 0) {
+    if (nb > 0 && !spec0) {
         asm volatile("cp.async.wait_group %0;" ::"n"(1) : "memory");     // the queries, not block 0
     } else {
-        // no committed block (block 0 of the first tile still lands before the ring is reused)
+        // the first tile staged block 0 before its queries (so both land here);
+        // with no committed block, block 0 still lands before the ring is reused
         asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
     }
     __syncthreads();

@@ -91,6 +91,17 @@ __device__ __forceinline__ void la_set_err(LaHdr* h, int code) { atomicCAS(&h->e
 // kernel wrote (it returns once the predecessor has completed and its writes
 // are visible), and la_pdl_trigger() to let its own successor launch.  Both
 // are no-ops for a kernel launched without the attribute.
+//
+// Every kernel except the tensor-core GEMM waits before it triggers, the GEMM
+// triggers first, and no two GEMMs are adjacent in a step.  So when a kernel
+// launches, every kernel three or more launches before it has completed and
+// its writes are visible.  The header fields the layer kernels test (err,
+// done, K and the row counts Q, n_need, prefill_rows, written by the pack or
+// chunk kernels at the start of a call or by the publish kernel of the call
+// before) are therefore read before la_pdl_wait() by every kernel from the
+// first RMSNorm of a call on (an error flag a kernel sets in the same call
+// may be seen late; it still reaches the host).  The embedding, right after
+// the pack kernel, reads them after its wait.
 __device__ __forceinline__ void la_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void la_pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -269,9 +269,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (++kt == p.k_tiles) { kt = 0; ++tile; }
                 }
             }
-            // everything above depends on no earlier kernel; the header and the
-            // activations are written by the kernels before this one
-            la_pdl_wait();
+            // Everything above depends on no earlier kernel, and neither do the
+            // header fields read next (written at least three launches back,
+            // la_common.cuh); the activations, written by the kernel before
+            // this one, are loaded after the wait.
             const int h_err = h->err, h_done = h->done;
             const int h_n = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
             int rows = h_n;
@@ -280,6 +281,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if (blockIdx.x == 0) la_set_err(h, LA_EDEVICE);
                 rows = -1;
             }
+            la_pdl_wait();
             *s_rows = rows;
             hdr_rows = rows;
         }

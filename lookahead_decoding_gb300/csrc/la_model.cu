@@ -88,13 +88,13 @@ __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
 template <typename T>
 __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g, T* y, int dm, float eps, int sel,
                                                  int gather, LaSplit resid) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
+    const int row = blockIdx.x;
+    if (row >= rows_of(h, sel)) return;
     la_pdl_wait();
     la_pdl_trigger();
-    const LaHdr* h = d.hdr;
-    if (skip_call(h, sel)) return;
-    int row = blockIdx.x;
-    if (row >= rows_of(h, sel)) return;
-    int src = gather ? d.need[row] : row;
+    const int src = gather ? d.need[row] : row;
     float* xr = x + (size_t)src * dm;
     // the row stays in registers: up to 2 float4 per thread (256 threads for
     // d_model <= 2048, 1024 threads up to 8192)
@@ -180,12 +180,12 @@ __device__ __forceinline__ T qkv_at(const T* row, int q, int n, const LaSplit& s
 template <typename T>
 __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float* rsin, T* qbuf, T* kdst, T* vdst,
                           int H, int dh, int sel, int Qcap, int stride, LaSplit sp) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
+    const int q = blockIdx.x;
+    if (q >= rows_of(h, sel)) return;
     la_pdl_wait();
     la_pdl_trigger();
-    const LaHdr* h = d.hdr;
-    if (skip_call(h, sel)) return;
-    int q = blockIdx.x;
-    if (q >= rows_of(h, sel)) return;
     const int half = dh >> 1;
     // blockDim = RH heads x half threads
     int hh = blockIdx.y * (blockDim.x / half) + threadIdx.x / half, i = threadIdx.x % half;
@@ -217,12 +217,12 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
 // and up the sums of the segments' two accumulator planes.  One thread per
 // four consecutive columns of a row (float4 partial loads, all in flight at once).
 __global__ void __launch_bounds__(256) k_swiglu_split(LaDev d, LaSplit sp, __nv_bfloat16* act, int ldo, int sel) {
-    la_pdl_wait();
-    la_pdl_trigger();
     const LaHdr* h = d.hdr;
-    if (skip_call(h, sel)) return;
+    if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int q = blockIdx.x;
     if (q >= rows_of(h, sel)) return;
+    la_pdl_wait();
+    la_pdl_trigger();
     const int n_cols = sp.n_tiles * 128;
     const int y = q >> 8;
     const size_t rowoff = (size_t)(q & 255) * 128;

@@ -125,6 +125,9 @@ int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, c
 
     k_noalloc_reset<<<1, 256, 0, st>>>(hdr, counters, (int)n_counters, rows);
     if (cudaGetLastError() != cudaSuccess) return LA_ECUDA;
+    // the GEMM reads the header's row count before its dependency wait, so
+    // the reset must have completed before the GEMM launches
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ECUDA;
     if (la_launch_gemm_tc(d, st, g, wk, SEL_NEED) != cudaSuccess) return LA_ECUDA;
     int err = 0;
     if (cudaMemcpyAsync(&err, &hdr->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return LA_ECUDA;
