@@ -72,7 +72,11 @@ typedef struct {
  *   w_gate[l], w_up[l]         [d_ffn][d_model]
  *   w_down[l]                  [d_model][d_ffn]
  * Every matrix must be 16-byte aligned.  The caller keeps them alive and
- * unchanged until la_free.  The host pointer arrays are copied by la_init. */
+ * unchanged until la_free.  The host pointer arrays are copied by la_init.
+ * In bf16 mode la_init also copies every projection and the LM head into
+ * context-owned device memory (the same size again) in the order the
+ * tensor-core GEMM streams them: each 128 x 64 tile contiguous, already in
+ * its shared-memory layout. */
 typedef struct {
     const void* tok_emb;
     const void* lm_head;
@@ -238,6 +242,8 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
  * w [n_out][K], w2 [n_out][K] (swiglu only), x [rows][K]; y (host)
  * [rows][n_out] fp32 (bf16 results widened).  n_out a multiple of
  * 128 * n_seg (n_seg 1..3), K of 64, 1 <= rows <= 1024, 0 <= n_cta <= 4096.
+ * The weights are first packed into the unit-contiguous images the model's
+ * GEMMs stream (la_init does the same for every projection).
  * Uses the current device and allocates its own temporary device buffers.
  * Errors: LA_EINVAL, LA_ECUDA, LA_ETIMEOUT. */
 int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K,
@@ -247,12 +253,13 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
  * matrices of [n_out][K] (filled with small deterministic values) are used in
  * turn so that weights stream from HBM rather than L2; *us receives the mean
  * device time of one launch over `reps` launches after three warm-up
- * launches (CUDA events on the legacy default stream).  Each launch
- * prefetches into L2 the first pf_units weight tiles per CTA of the copy
- * used next (0: no prefetch).  Arguments as for la_debug_gemm;
- * 1 <= n_copies <= 64, pf_units >= 0.  Errors: LA_EINVAL, LA_ECUDA,
+ * launches (CUDA events on the legacy default stream).  packed = 1 streams
+ * the weights as the model's GEMMs do, from unit-contiguous images (one
+ * 16 KB bulk copy per 128 x 64 tile); 0 loads the row-major matrices through
+ * tensor maps, as la_gemm_noalloc does.  Arguments as for la_debug_gemm;
+ * 1 <= n_copies <= 64, packed 0 or 1.  Errors: LA_EINVAL, LA_ECUDA,
  * LA_ETIMEOUT. */
-int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, int pf_units,
+int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, int packed,
                   float* us);
 
 /* The tensor-core GEMM for callers that cannot allocate device memory.  The

@@ -299,10 +299,10 @@ def la_debug_gemm(w_bf16, x_bf16, n_cta: int = 0, mode: int = GEMM_LOGITS, w2_bf
 
 
 def la_bench_gemm(mode: int, n_out: int, K: int, rows: int, n_cta: int = 0, n_copies: int = 8,
-                  reps: int = 20, pf_units: int = 0) -> float:
+                  reps: int = 20, packed: int = 1) -> float:
     """Mean device microseconds of one tensor-core GEMM launch (see the header)."""
     us = C.c_float()
-    _check(LIB.la_bench_gemm(mode, n_out, K, rows, n_cta, n_copies, reps, pf_units, C.byref(us)), "la_bench_gemm")
+    _check(LIB.la_bench_gemm(mode, n_out, K, rows, n_cta, n_copies, reps, packed, C.byref(us)), "la_bench_gemm")
     return float(us.value)
 
 

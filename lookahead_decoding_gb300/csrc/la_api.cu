@@ -164,8 +164,8 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     g->K = K;
     g->Nout = Nout_seg * n_seg;
     g->seg_tiles = n_seg > 1 ? Nout_seg / 128 : 0;
-    g->n_cta = la_tc_pick_ctas(g->Nout / 128, K / 64, mode);
-    g->max_seg = la_tc_max_segments(g->Nout / 128, K / 64, g->n_cta);
+    g->n_cta = la_tc_pick_ctas(g->Nout / 128, la_tc_k_units(mode, K), mode);
+    g->max_seg = la_tc_max_segments(g->Nout / 128, la_tc_k_units(mode, K), g->n_cta);
     g->rows_cap = ctx->Qcap;
     g->out = out;
     g->ldo = ldo;
@@ -201,7 +201,7 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
         prof_close(ctx, pi);
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
-            CK(la_launch_gemm_tc(d, st, ctx->g_qkv[l], ctx->work, sel));
+            CK(la_launch_gemm_tc(d, st, ctx->g_qkv[l], ctx->work, sel, rc));
             prof_close(ctx, pi);
         } else {
             char* q = (char*)ctx->qkv;
@@ -237,7 +237,7 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
         prof_close(ctx, pi);
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
-            CK(la_launch_gemm_tc(d, st, ctx->g_o[l], ctx->work, sel));
+            CK(la_launch_gemm_tc(d, st, ctx->g_o[l], ctx->work, sel, rc));
             prof_close(ctx, pi);
         } else {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->attn, HD, ctx->wo[l], nullptr, HD, dm, ctx->x, dm, sel, rc);
@@ -248,7 +248,7 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
         prof_close(ctx, pi);
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
-            CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel));
+            CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel, rc));
             prof_close(ctx, pi);
             if (ctx->g_gu[l].defer && ctx->g_gu[l].max_seg > 1) {
                 pi = prof_open(ctx, PK_ROW);
@@ -256,7 +256,7 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
                 prof_close(ctx, pi);
             }
             pi = prof_open(ctx, PK_GEMM);
-            CK(la_launch_gemm_tc(d, st, ctx->g_down[l], ctx->work, sel));
+            CK(la_launch_gemm_tc(d, st, ctx->g_down[l], ctx->work, sel, rc));
             prof_close(ctx, pi);
         } else {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_SWIGLU, ctx->xn, dm, ctx->wg[l], ctx->wu[l], dm, F, ctx->act, F, sel, rc);
@@ -281,7 +281,7 @@ static int enqueue_head(la_ctx* ctx, int keep_logits) {
         TcGemm g = ctx->g_head;
         g.logits = keep_logits ? ctx->logits : nullptr;
         pi = prof_open(ctx, PK_GEMM);
-        CK(la_launch_gemm_tc(d, st, g, ctx->work, SEL_NEED));
+        CK(la_launch_gemm_tc(d, st, g, ctx->work, SEL_NEED, rc));
         prof_close(ctx, pi);
         pi = prof_open(ctx, PK_STATE);
         la_launch_argmax_reduce(d, st, ctx->work.part_v, ctx->work.part_i, c.vocab / 128, ctx->work.part_stride,
@@ -534,18 +534,26 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
                               nullptr, 0);
         if (r) { la_free(ctx); return r; }
         ctx->g_head.ld_logits = (int)V;
-        // every GEMM prefetches into L2 the first weight tiles of the GEMM launched
-        // after it (the head's successor is the first QKV of the next call)
-        const int pf = la_tc_pf_units();
-        for (int l = 0; l < c.n_layers; ++l) {
-            ctx->g_qkv[l].next = &ctx->g_o[l];
-            ctx->g_o[l].next = &ctx->g_gu[l];
-            ctx->g_gu[l].next = &ctx->g_down[l];
-            ctx->g_down[l].next = l + 1 < c.n_layers ? &ctx->g_qkv[l + 1] : &ctx->g_head;
-            ctx->g_qkv[l].pf_units = ctx->g_o[l].pf_units = ctx->g_gu[l].pf_units = ctx->g_down[l].pf_units = pf;
+        // unit-contiguous weight images (one bulk copy per unit); LA_TC_PACK=0
+        // (A/B runs) keeps the tensor-map loads of the row-major weights
+        const char* pe = getenv("LA_TC_PACK");
+        if (!(pe && pe[0] == '0')) {
+            auto pack = [&](TcGemm& g, const void* w1, const void* w2, const void* w3) {
+                if (r) return;
+                void* dst = nullptr;
+                r = dalloc(ctx, &dst, la_tc_packed_bytes(g));
+                if (!r && la_tc_pack(g, w1, w2, w3, dst, ctx->st) != cudaSuccess) r = LA_ECUDA;
+                if (!r) g.wpack = dst;
+            };
+            for (int l = 0; l < c.n_layers; ++l) {
+                pack(ctx->g_qkv[l], ctx->wq[l], ctx->wk[l], ctx->wv[l]);
+                pack(ctx->g_o[l], ctx->wo[l], nullptr, nullptr);
+                pack(ctx->g_gu[l], ctx->wg[l], ctx->wu[l], nullptr);
+                pack(ctx->g_down[l], ctx->wd[l], nullptr, nullptr);
+            }
+            pack(ctx->g_head, ctx->head, nullptr, nullptr);
+            if (r) { la_free(ctx); return r; }
         }
-        ctx->g_head.next = &ctx->g_qkv[0];
-        ctx->g_head.pf_units = pf;
         // the layer GEMMs leave their split tiles to RoPE, RMSNorm and SwiGLU
         const int defer = la_tc_defer_default();
         for (int l = 0; l < c.n_layers; ++l)
@@ -918,7 +926,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         n_out % (128 * n_seg) || K < 64 || K % 64 || rows < 1 || rows > 1024 || n_cta < 0 || n_cta > 4096)
         return LA_EINVAL;
     if (n_cta == 0) n_cta = la_tc_ctas();
-    const int max_seg = la_tc_max_segments(n_out / 128, K / 64, n_cta);
+    const int max_seg = la_tc_max_segments(n_out / 128, la_tc_k_units(mode, K), n_cta);
     if (mode == GEMM_SWIGLU && (!w2 || n_seg != 1)) return LA_EINVAL;
     if (mode == GEMM_LOGITS && n_seg != 1) return LA_EINVAL;
     const int rows_cap = ((rows + 255) / 256) * 256;
@@ -986,8 +994,14 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         LaDev d;
         memset(&d, 0, sizeof(d));
         d.hdr = hdr;
-        if (!rc && la_launch_gemm_tc(d, 0, g, wk, SEL_NEED) != cudaSuccess) rc = LA_ECUDA;
+        // the weights as the model's GEMMs read them: unit-contiguous images
+        void* wp = nullptr;
+        if (!rc && cudaMalloc(&wp, la_tc_packed_bytes(g)) != cudaSuccess) rc = LA_ECUDA;
+        if (!rc && la_tc_pack(g, dw[0], mode == GEMM_SWIGLU ? dw2 : dw[1], dw[2], wp, 0) != cudaSuccess) rc = LA_ECUDA;
+        g.wpack = wp;
+        if (!rc && la_launch_gemm_tc(d, 0, g, wk, SEL_NEED, rows) != cudaSuccess) rc = LA_ECUDA;
         if (!rc && cudaDeviceSynchronize() != cudaSuccess) rc = LA_ECUDA;
+        if (wp) cudaFree(wp);
         LaHdr h;
         if (!rc && cudaMemcpy(&h, hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) rc = LA_ECUDA;
         if (!rc && h.err) rc = h.err;
@@ -1020,12 +1034,12 @@ __global__ void k_fill_bf16(__nv_bfloat16* p, size_t n, uint32_t seed) {
     }
 }
 
-int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, int pf_units, float* us) {
+int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies, int reps, int packed, float* us) {
     if (!us || mode < GEMM_STORE || mode > GEMM_LOGITS || n_out < 128 || n_out % 128 || K < 64 || K % 64 ||
-        rows < 1 || rows > 1024 || n_cta < 0 || n_copies < 1 || n_copies > 64 || reps < 1 || pf_units < 0)
+        rows < 1 || rows > 1024 || n_cta < 0 || n_copies < 1 || n_copies > 64 || reps < 1 || packed < 0 || packed > 1)
         return LA_EINVAL;
     if (n_cta == 0) n_cta = la_tc_ctas();
-    const int max_seg = la_tc_max_segments(n_out / 128, K / 64, n_cta);
+    const int max_seg = la_tc_max_segments(n_out / 128, la_tc_k_units(mode, K), n_cta);
     const int rows_cap = ((rows + 255) / 256) * 256;
     const int tiles = n_out / 128, qchunks = rows_cap / 256;
     const int nA = mode == GEMM_SWIGLU ? 2 : 1;
@@ -1068,9 +1082,12 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
         g.mode = mode; g.K = K; g.Nout = n_out; g.n_cta = n_cta; g.max_seg = max_seg; g.rows_cap = rows_cap;
         g.out = dout; g.ldo = n_out; g.logits = nullptr; g.ld_logits = n_out;
     }
-    for (int i = 0; i < n_copies && !rc; ++i) {
-        gs[i].next = &gs[(i + 1) % n_copies];
-        gs[i].pf_units = pf_units;
+    std::vector<void*> wp(n_copies, nullptr);
+    for (int i = 0; i < n_copies && !rc && packed; ++i) {
+        if (cudaMalloc(&wp[i], la_tc_packed_bytes(gs[i])) != cudaSuccess ||
+            la_tc_pack(gs[i], w[i * nA], nA == 2 ? w[i * nA + 1] : nullptr, nullptr, wp[i], 0) != cudaSuccess)
+            rc = LA_ECUDA;
+        gs[i].wpack = wp[i];
     }
     TcWork wk;
     memset(&wk, 0, sizeof(wk));
@@ -1080,10 +1097,10 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
     d.hdr = hdr;
     if (!rc) {
         for (int i = 0; i < 3 && !rc; ++i)
-            if (la_launch_gemm_tc(d, 0, gs[i % n_copies], wk, SEL_NEED) != cudaSuccess) rc = LA_ECUDA;
+            if (la_launch_gemm_tc(d, 0, gs[i % n_copies], wk, SEL_NEED, rows) != cudaSuccess) rc = LA_ECUDA;
         if (!rc && cudaEventRecord(e0, 0) != cudaSuccess) rc = LA_ECUDA;
         for (int i = 0; i < reps && !rc; ++i)
-            if (la_launch_gemm_tc(d, 0, gs[i % n_copies], wk, SEL_NEED) != cudaSuccess) rc = LA_ECUDA;
+            if (la_launch_gemm_tc(d, 0, gs[i % n_copies], wk, SEL_NEED, rows) != cudaSuccess) rc = LA_ECUDA;
         if (!rc && cudaEventRecord(e1, 0) != cudaSuccess) rc = LA_ECUDA;
         if (!rc && cudaEventSynchronize(e1) != cudaSuccess) rc = LA_ECUDA;
         float ms = 0;
@@ -1095,6 +1112,7 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
     }
     if (e0) cudaEventDestroy(e0);
     if (e1) cudaEventDestroy(e1);
+    for (auto p : wp) if (p) cudaFree(p);
     for (auto p : w) cudaFree(p);
     cudaFree(dx); cudaFree(dout); cudaFree(ws); cudaFree(cnt); cudaFree(pv); cudaFree(pi); cudaFree(hdr);
     return rc;

@@ -44,21 +44,22 @@ constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int ROW_BYTES = BK * 2;         // 128 B per activation row per unit
 constexpr int BOX_ROWS = 16;
 constexpr int MAX_STAGES = 12;
-constexpr int SMEM_BYTES = 200 * 1024;
+constexpr int SMEM_BYTES = 220 * 1024;
 constexpr int NTHREADS = 192;             // producer, MMA, 4 epilogue warps
 constexpr int MAX_CHUNKS = 4;
 constexpr uint32_t TMEM_COLS = 512;       // two accumulators of up to 256 fp32 columns             // packed rows per launch <= MAX_CHUNKS * BN_MAX
 
 struct TcParams {
     LaHdr* hdr;
-    int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg, max_stages;
+    int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg;
+    int ns, max_ns, rows_cap;        // stages at rows_cap rows (issued before the header), stage limit, rows per launch at most
+    int ua, k_atoms;                 // 64-column atoms per unit (the last unit of a tile may hold fewer), K / 64
+    const uint8_t* wpack;            // unit-contiguous weight images (la_tc_pack), or null: the tensor maps
     void* out; int ldo;
     float* logits; int ld_logits;
     float* ws; unsigned long long* ctr;   // this GEMM's split-tile arrival counters
     float* part_v; int* part_i; int part_stride;
     int max_chunks;
-    // L2 prefetch of the next GEMM's first units (see la_launch_gemm_tc)
-    int pf_units, pf_n_tiles, pf_k_tiles, pf_seg_tiles, pf_swiglu;
     int defer;            // split tiles left as partials for the consumer
 };
 
@@ -90,17 +91,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* tm, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm), "r"(x), "r"(y)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y,
                                             uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(tm), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// contiguous global -> shared copy completing on an mbarrier (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -201,9 +205,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
           const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
-          const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB256,
-          const __grid_constant__ CUtensorMap pfA, const __grid_constant__ CUtensorMap pfA2,
-          const __grid_constant__ CUtensorMap pfA3, TcParams p) {
+          const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB256, TcParams p) {
     LaHdr* h = p.hdr;
     const int swiglu = (p.mode == GEMM_SWIGLU);
     const int nA = swiglu ? 2 : 1;
@@ -221,21 +223,51 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // [barriers][flags][reduction scratch 8 KB][weight ring][activation ring]
-    const uint32_t bar_full = base;                        // MAX_STAGES x 8 B
+    // [barriers][flags][reduction scratch 8 KB][stages: weights][stages: activations]
+    const uint32_t bar_full = base;                                   // MAX_STAGES x 8 B
     const uint32_t bar_empty = base + 8 * MAX_STAGES;
-    const uint32_t bar_accf = base + 16 * MAX_STAGES;      // 2 x 8 B
-    const uint32_t bar_acce = bar_accf + 16;               // 2 x 8 B
-    uint32_t* tmem_slot = (uint32_t*)(gbase + 16 * MAX_STAGES + 32);
-    int* s_flag = (int*)(gbase + 16 * MAX_STAGES + 40);
-    int* s_rows = (int*)(gbase + 16 * MAX_STAGES + 44);    // header broadcast: rows, or -1 to skip the call
-    float* rv = (float*)(gbase + 1024);                    // [4][BN_MAX] argmax values
-    int* ri = (int*)(gbase + 1024 + 4 * BN_MAX * 4);       // [4][BN_MAX] argmax ids
-    const uint32_t stage0 = base + 1024 + 8192;
-    const uint32_t a_stage = (uint32_t)nA * A_BYTES;
-    // weight tiles issued before the header is read (they depend on nothing);
-    // every stage layout below has at least this many stages
-    const int n_pre = min(swiglu ? 2 : 3, n_units);
+    const uint32_t bar_accf = base + 16 * MAX_STAGES;                 // 2 x 8 B
+    const uint32_t bar_acce = bar_accf + 16;                          // 2 x 8 B
+    uint8_t* flags = gbase + (bar_acce + 16 - base);
+    uint32_t* tmem_slot = (uint32_t*)flags;
+    int* s_flag = (int*)(flags + 8);
+    int* s_rows = (int*)(flags + 12);                                 // header broadcast: rows, or -1 to skip the call
+    float* rv = (float*)(gbase + 1024);                               // [4][BN_MAX] argmax values
+    int* ri = (int*)(gbase + 1024 + 4 * BN_MAX * 4);                  // [4][BN_MAX] argmax ids
+    const uint32_t a_stage = (uint32_t)(nA * p.ua) * A_BYTES;         // one unit's weight tiles (at most)
+    // Weight stage s starts at wring + s * a_stage whatever the row count;
+    // activation stage s ends at ring_end - s * b_stage, b_stage set by the
+    // call's rows.  ns(rows) * (a_stage + b_stage) fits, and ns(rows) >=
+    // p.ns = ns(rows_cap), so the weights of p.ns stages are issued before
+    // the header is read and before the dependency wait.
+    const uint32_t wring = base + 1024 + 8192;
+    const uint32_t ring_end = base + SMEM_BYTES;
+    const int n_pre = min(p.ns, n_units);
+
+    // unit u = (tile, kt) covers atoms kt * ua .. + atoms_of(u) - 1 of its tile
+    auto atoms_of = [&](long long u) { return min(p.ua, p.k_atoms - (int)(u % p.k_tiles) * p.ua); };
+    // weight tiles of unit u into stage s (the stage's barrier already expects
+    // them): atom i of matrix a at (i * nA + a) x 16 KB, the packed order
+    auto load_w = [&](int s, long long u, uint64_t pol) {
+        const uint32_t fb = bar_full + 8 * s, st = wring + (uint32_t)s * a_stage;
+        const int tile = (int)(u / p.k_tiles), at0 = (int)(u % p.k_tiles) * p.ua, na = atoms_of(u);
+        if (p.wpack) {
+            bulk_load(st, p.wpack + ((size_t)tile * p.k_atoms + at0) * nA * A_BYTES, (uint32_t)(na * nA) * A_BYTES, fb,
+                      pol);
+        } else {
+            const CUtensorMap* wmap = &tmA;
+            int wrow = tile * BM;
+            if (p.seg_tiles > 0) {
+                const int seg = tile / p.seg_tiles;
+                wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
+                wrow = (tile - seg * p.seg_tiles) * BM;
+            }
+            for (int i = 0; i < na; ++i) {
+                tma_load_2d(st + (uint32_t)(i * nA) * A_BYTES, wmap, fb, (at0 + i) * BK, wrow, pol);
+                if (swiglu) tma_load_2d(st + (uint32_t)(i * nA + 1) * A_BYTES, &tmA2, fb, (at0 + i) * BK, wrow, pol);
+            }
+        }
+    };
 
     la_pdl_trigger();
     if (warp == 0) {
@@ -252,24 +284,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             uint64_t pol_w;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
-            {
-                int tile = tile0, kt = kt0;
-                for (int i = 0; i < n_pre; ++i) {
-                    const uint32_t fb = bar_full + 8 * i, st = stage0 + (uint32_t)i * a_stage;
-                    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(a_stage) : "memory");
-                    const CUtensorMap* wmap = &tmA;
-                    int wrow = tile * BM;
-                    if (p.seg_tiles > 0) {
-                        const int seg = tile / p.seg_tiles;
-                        wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
-                        wrow = (tile - seg * p.seg_tiles) * BM;
-                    }
-                    tma_load_2d(st, wmap, fb, kt * BK, wrow, pol_w);
-                    if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kt * BK, wrow, pol_w);
-                    if (++kt == p.k_tiles) { kt = 0; ++tile; }
-                }
+            // expect_tx without arriving: a stage completes only once its
+            // activation rows (registered with the arrival below) have landed too
+            for (int i = 0; i < n_pre; ++i) {
+                const uint32_t wb = (uint32_t)(atoms_of(u_begin + i) * nA) * A_BYTES;
+                asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar_full + 8 * i), "r"(wb) : "memory");
+                load_w(i, u_begin + i, pol_w);
             }
-            // Everything above depends on no earlier kernel, and neither do the
+            // The weights depend on no earlier kernel, and neither do the
             // header fields read next (written at least three launches back,
             // la_common.cuh); the activations, written by the kernel before
             // this one, are loaded after the wait.
@@ -277,7 +299,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int h_n = p.sel == SEL_CALL ? h->Q : (p.sel == SEL_PREFILL ? h->prefill_rows : h->n_need);
             int rows = h_n;
             if (h_err != 0 || (p.sel != SEL_PREFILL && h_done != 0) || rows <= 0) rows = -1;
-            if (rows > 0 && (rows + BN_MAX - 1) / BN_MAX > p.max_chunks) {
+            if (rows > p.rows_cap || (rows > 0 && (rows + BN_MAX - 1) / BN_MAX > p.max_chunks)) {
                 if (blockIdx.x == 0) la_set_err(h, LA_EDEVICE);
                 rows = -1;
             }
@@ -299,81 +321,48 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             } else {
                 // TMA producer: every (chunk, unit) of this CTA, in order
                 const int n_chunks = (rows + BN_MAX - 1) / BN_MAX;
-                const int BN0 = (min(BN_MAX, rows) + 15) & ~15;
-                const uint32_t b_stage = (uint32_t)BN0 * ROW_BYTES;
-                int ns = (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage));
-                ns = ns > p.max_stages ? p.max_stages : ns;
-                const uint32_t bbase = stage0 + (uint32_t)ns * a_stage;
+                const uint32_t b_atom = (uint32_t)((min(BN_MAX, rows) + 15) & ~15) * ROW_BYTES;
+                const uint32_t b_stage = (uint32_t)p.ua * b_atom;
+                const int ns = min(p.max_ns, (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage)));
                 uint64_t pol_w, pol_x;
                 asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
                 asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
                 bool ok = true;
-                int y = 0, iu = 0, tile = tile0, kt = kt0, s = 0, r = 0;
+                int y = 0, iu = 0, s = 0, r = 0;
                 const int n_items = n_chunks * n_units;
                 for (int it = 0; it < n_items; ++it) {
                     const int q0 = y * BN_MAX;
                     const int BN = (min(BN_MAX, rows - q0) + 15) & ~15;
                     if (r > 0 && !mbar_wait(bar_empty + 8 * s, (uint32_t)((r - 1) & 1))) { ok = false; break; }
-                    const uint32_t st = stage0 + (uint32_t)s * a_stage;
-                    const uint32_t bst = bbase + (uint32_t)s * b_stage;
+                    const uint32_t bst = ring_end - (uint32_t)(s + 1) * b_stage;
                     const uint32_t fb = bar_full + 8 * s;
-                    const int kx = kt * BK;
+                    const long long u = u_begin + iu;
+                    const int at0 = (int)(u % p.k_tiles) * p.ua, na = atoms_of(u);
+                    const uint32_t xb = (uint32_t)(na * BN) * ROW_BYTES;
                     if (it < n_pre) {
-                        // the weight tile is already on its way
-                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                                     "r"((uint32_t)BN * ROW_BYTES)
-                                     : "memory");
+                        // the weight tiles are already on their way
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(xb) : "memory");
                     } else {
-                        mbar_expect_tx(fb, a_stage + (uint32_t)BN * ROW_BYTES);
-                        const CUtensorMap* wmap = &tmA;
-                        int wrow = tile * BM;
-                        if (p.seg_tiles > 0) {
-                            const int seg = tile / p.seg_tiles;
-                            wmap = seg == 0 ? &tmA : (seg == 1 ? &tmA2 : &tmA3);
-                            wrow = (tile - seg * p.seg_tiles) * BM;
+                        mbar_expect_tx(fb, (uint32_t)(na * nA) * A_BYTES + xb);
+                        load_w(s, u, pol_w);
+                    }
+                    // per atom, the activation rows in at most four boxes (256/128/64/32/16 rows)
+                    for (int i = 0; i < na; ++i) {
+                        int rr = 0;
+                        while (rr < BN) {
+                            const int left = BN - rr;
+                            const CUtensorMap* bm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128 : left >= 64 ? &tmB64
+                                                  : left >= 32 ? &tmB32 : &tmB;
+                            const int hgt = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : left >= 32 ? 32 : 16;
+                            tma_load_2d(bst + (uint32_t)i * b_atom + (uint32_t)rr * ROW_BYTES, bm, fb, (at0 + i) * BK,
+                                        q0 + rr, pol_x);
+                            rr += hgt;
                         }
-                        tma_load_2d(st, wmap, fb, kx, wrow, pol_w);
-                        if (swiglu) tma_load_2d(st + A_BYTES, &tmA2, fb, kx, wrow, pol_w);
                     }
-                    // activation rows in at most four boxes (256/128/64/32/16 rows)
-                    int rr = 0;
-                    while (rr < BN) {
-                        const int left = BN - rr;
-                        const CUtensorMap* bm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128 : left >= 64 ? &tmB64
-                                              : left >= 32 ? &tmB32 : &tmB;
-                        const int hgt = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : left >= 32 ? 32 : 16;
-                        tma_load_2d(bst + (uint32_t)rr * ROW_BYTES, bm, fb, kx, q0 + rr, pol_x);
-                        rr += hgt;
-                    }
-                    ++iu;
-                    if (++kt == p.k_tiles) { kt = 0; ++tile; }
-                    if (iu == n_units) { iu = 0; ++y; tile = tile0; kt = kt0; }
+                    if (++iu == n_units) { iu = 0; ++y; }
                     if (++s == ns) { s = 0; ++r; }
                 }
                 if (!ok) la_set_err(h, LA_ETIMEOUT);
-                // While this grid drains, pull the first units of the next GEMM's
-                // weights (the ones the same CTA index streams first) into L2.
-                if (ok && p.pf_units > 0) {
-                    const long long T2 = (long long)p.pf_n_tiles * p.pf_k_tiles;
-                    const int P2 = (int)(T2 < (long long)p.n_cta ? T2 : (long long)p.n_cta);
-                    if (c < P2) {
-                        const long long v0 = T2 * c / P2, v1 = T2 * (c + 1) / P2;
-                        const int npf = (int)((long long)p.pf_units < v1 - v0 ? (long long)p.pf_units : v1 - v0);
-                        int ptile = (int)(v0 / p.pf_k_tiles), pkt = (int)(v0 % p.pf_k_tiles);
-                        for (int i = 0; i < npf; ++i) {
-                            const CUtensorMap* m = &pfA;
-                            int row = ptile * BM;
-                            if (p.pf_seg_tiles > 0) {
-                                const int seg = ptile / p.pf_seg_tiles;
-                                m = seg == 0 ? &pfA : (seg == 1 ? &pfA2 : &pfA3);
-                                row = (ptile - seg * p.pf_seg_tiles) * BM;
-                            }
-                            tma_prefetch_l2(m, pkt * BK, row);
-                            if (p.pf_swiglu) tma_prefetch_l2(&pfA2, pkt * BK, row);
-                            if (++pkt == p.pf_k_tiles) { pkt = 0; ++ptile; }
-                        }
-                    }
-                }
             }
         }
     } else {
@@ -392,12 +381,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const uint32_t tmem = *tmem_slot;
     const int n_chunks = rows > 0 ? (rows + BN_MAX - 1) / BN_MAX : 0;
     const int BN0 = rows > 0 ? (min(BN_MAX, rows) + 15) & ~15 : 16;
-    const uint32_t b_stage = (uint32_t)BN0 * ROW_BYTES;
-    int ns = (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage));
-    ns = ns > p.max_stages ? p.max_stages : ns;
-    const uint32_t bbase = stage0 + (uint32_t)ns * a_stage;
     const int acc_cols = nA * BN0;                         // one accumulator: nA x BN fp32 columns
     const int nbuf = (2 * acc_cols <= TMEM_COLS) ? 2 : 1;
+    const uint32_t b_atom = (uint32_t)BN0 * ROW_BYTES, b_stage = (uint32_t)p.ua * b_atom;
+    const int ns = min(p.max_ns, (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage)));
 
     if (warp == 0) {
         // producer (above)
@@ -405,7 +392,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (lane == 0 && n_chunks > 0) {
             // MMA issuer: one accumulator per K segment, alternating buffers
             bool ok = true;
-            int y = 0, iu = 0, tile = tile0, kt = kt0, s = 0, r = 0, seg_i = 0;
+            int y = 0, iu = 0, kt = kt0, s = 0, r = 0, seg_i = 0;
             while (y < n_chunks && ok) {
                 const int seg_len = min(n_units - iu, p.k_tiles - kt);
                 const int BN = (min(BN_MAX, rows - y * BN_MAX) + 15) & ~15;
@@ -417,14 +404,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 for (int j = 0; j < seg_len; ++j) {
                     if (!mbar_wait(bar_full + 8 * s, (uint32_t)(r & 1))) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t st = stage0 + (uint32_t)s * a_stage;
-                    const uint32_t bst = bbase + (uint32_t)s * b_stage;
+                    const uint32_t st = wring + (uint32_t)s * a_stage;
+                    const uint32_t bst = ring_end - (uint32_t)(s + 1) * b_stage;
+                    const int na = min(p.ua, p.k_atoms - (kt + j) * p.ua);
+                    for (int i = 0; i < na; ++i) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t bdesc = sdesc(bst + kk * 32);
-                        const uint32_t accum = (j == 0 && kk == 0) ? 0u : 1u;
-                        mma_bf16(acc, sdesc(st + kk * 32), bdesc, id, accum);
-                        if (swiglu) mma_bf16(acc + (uint32_t)BN, sdesc(st + A_BYTES + kk * 32), bdesc, id, accum);
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t bdesc = sdesc(bst + (uint32_t)i * b_atom + kk * 32);
+                            const uint32_t accum = (j == 0 && i == 0 && kk == 0) ? 0u : 1u;
+                            const uint32_t sa = st + (uint32_t)(i * nA) * A_BYTES + kk * 32;
+                            mma_bf16(acc, sdesc(sa), bdesc, id, accum);
+                            if (swiglu) mma_bf16(acc + (uint32_t)BN, sdesc(sa + A_BYTES), bdesc, id, accum);
+                        }
                     }
                     mma_commit(bar_empty + 8 * s);
                     if (++s == ns) { s = 0; ++r; }
@@ -434,8 +425,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 ++seg_i;
                 iu += seg_len;
                 kt += seg_len;
-                if (kt == p.k_tiles) { kt = 0; ++tile; }
-                if (iu == n_units) { iu = 0; ++y; tile = tile0; kt = kt0; }
+                if (kt == p.k_tiles) kt = 0;
+                if (iu == n_units) { iu = 0; ++y; kt = kt0; }
             }
             if (!ok) la_set_err(h, LA_ETIMEOUT);
         }
@@ -677,19 +668,6 @@ int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K) {
     return 0;
 }
 
-// Weight tiles of the next GEMM each CTA prefetches into L2 (LA_TC_PF
-// overrides the default for tuning runs).
-int la_tc_pf_units() {
-    static int pf = -1;
-    if (pf < 0) {
-        const char* e = getenv("LA_TC_PF");
-        pf = e ? atoi(e) : 0;
-        if (pf < 0) pf = 0;
-        if (pf > 4096) pf = 4096;
-    }
-    return pf;
-}
-
 // 1 unless LA_TC_DEFER=0 (A/B runs): the layer GEMMs leave split tiles to their consumers
 int la_tc_defer_default() {
     static int v = -1;
@@ -700,11 +678,19 @@ int la_tc_defer_default() {
     return v;
 }
 
+// 64-column atoms per (tile, K) unit: two (one 32 KB copy) for a single
+// weight matrix, one for the gate/up pair (already two 16 KB tiles)
+static int unit_atoms(int mode) { return mode == GEMM_SWIGLU ? 1 : 2; }
+int la_tc_k_units(int mode, int K) {
+    const int atoms = K / BK, ua = unit_atoms(mode);
+    return (atoms + ua - 1) / ua;
+}
+
 LaSplit la_tc_split(const TcGemm& g, const TcWork& w) {
     LaSplit s;
     s.ws = g.defer ? w.ws : nullptr;
     s.n_tiles = g.Nout / BM;
-    s.k_tiles = g.K / BK;
+    s.k_tiles = la_tc_k_units(g.mode, g.K);
     const long long T = (long long)s.n_tiles * s.k_tiles;
     s.P = (int)std::min<long long>(g.n_cta, T);
     s.max_seg = g.max_seg;
@@ -763,39 +749,97 @@ cudaError_t la_tc_prepare_device() {
 // Scratch the kernel needs for one problem: the split-tile partial sums
 // (floats) and the per-tile arrival counters (ints).
 void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t* ws_floats, size_t* n_counters) {
-    const int tiles = n_out / BM, k_tiles = K / BK, n_y = (rows + BN_MAX - 1) / BN_MAX;
+    const int tiles = n_out / BM, k_tiles = la_tc_k_units(mode, K), n_y = (rows + BN_MAX - 1) / BN_MAX;
     const int nA = mode == GEMM_SWIGLU ? 2 : 1;
     const int max_seg = la_tc_max_segments(tiles, k_tiles, n_cta);
     *ws_floats = (size_t)tiles * n_y * max_seg * nA * BN_MAX * BM;
     *n_counters = (size_t)LA_TC_CTR_PER_TILE * tiles * n_y;
 }
 
-cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel) {
+// Ring stages at rows_cap rows (the weight stages issued before the header
+// is read; a call with fewer rows gets more stages) and the stage limit.
+// Each stage holds one unit's weight tiles and, per atom, the activation rows.
+static void ring_shape(int mode, int rows_cap, int* ns, int* max_ns) {
+    static int max_s = -1;
+    if (max_s < 0) {
+        const char* e = getenv("LA_TC_STAGES");   // pipeline-depth override for tuning runs
+        max_s = e ? atoi(e) : MAX_STAGES;
+        if (max_s < 2) max_s = 2;
+        if (max_s > MAX_STAGES) max_s = MAX_STAGES;
+    }
+    const int bn = (std::min(BN_MAX, std::max(rows_cap, 1)) + 15) & ~15;
+    const int ua = unit_atoms(mode);
+    const int a_stage = (mode == GEMM_SWIGLU ? 2 : 1) * ua * A_BYTES;
+    const int n = (SMEM_BYTES - 1024 - 8192) / (a_stage + ua * bn * ROW_BYTES);
+    *max_ns = max_s;
+    *ns = std::min(n, max_s);
+}
+
+size_t la_tc_packed_bytes(const TcGemm& g) {
+    return (size_t)g.Nout * g.K * 2 * (g.mode == GEMM_SWIGLU ? 2 : 1);
+}
+
+// Unit-contiguous weight images: unit (tile, kt) is nA blocks of 16 KB, each
+// the 128 x 64 bf16 tile as the 128-byte-swizzled TMA load would leave it in
+// shared memory (16-byte chunk c of row r at r * 128 + ((c ^ (r & 7)) * 16)).
+// w0..w2: the segments (or gate, up) with seg_rows rows each.
+__global__ void k_tc_pack(const uint4* w0, const uint4* w1, const uint4* w2, int seg_tiles, int nA, int n_tiles,
+                          int K, uint4* dst) {
+    const int k_tiles = K / BK;
+    const long long total = (long long)n_tiles * k_tiles * nA * BM * 8;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const int cc = (int)(i & 7), r = (int)((i >> 3) & 127);
+        const long long ua = i >> 10;                     // unit * nA + a
+        const int a = (int)(ua % nA);
+        const long long u = ua / nA;
+        const int tile = (int)(u / k_tiles), kt = (int)(u % k_tiles);
+        const uint4* src = w0;
+        int row = tile * BM + r;
+        if (nA == 2) {
+            src = a ? w1 : w0;
+        } else if (seg_tiles > 0) {
+            const int seg = tile / seg_tiles;
+            src = seg == 0 ? w0 : (seg == 1 ? w1 : w2);
+            row = (tile - seg * seg_tiles) * BM + r;
+        }
+        const uint4 v = src[((size_t)row * K + (size_t)kt * BK) / 8 + cc];
+        dst[(size_t)ua * (A_BYTES / 16) + r * 8 + (cc ^ (r & 7))] = v;
+    }
+}
+
+cudaError_t la_tc_pack(const TcGemm& g, const void* w1, const void* w2, const void* w3, void* dst, cudaStream_t st) {
+    const int nA = g.mode == GEMM_SWIGLU ? 2 : 1;
+    const int n_tiles = g.Nout / BM;
+    k_tc_pack<<<1024, 256, 0, st>>>((const uint4*)w1, (const uint4*)(w2 ? w2 : w1), (const uint4*)(w3 ? w3 : w1),
+                                    g.seg_tiles, nA, n_tiles, g.K, (uint4*)dst);
+    return cudaGetLastError();
+}
+
+cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel,
+                              int rows_cap) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES + 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    if (rows_cap < 1 || rows_cap > MAX_CHUNKS * BN_MAX) return cudaErrorInvalidValue;
     TcParams p;
     p.hdr = d.hdr;
     p.sel = sel;
     p.mode = g.mode;
     p.K = g.K;
     p.Nout = g.Nout;
-    p.k_tiles = g.K / BK;
+    p.k_tiles = la_tc_k_units(g.mode, g.K);
+    p.ua = unit_atoms(g.mode);
+    p.k_atoms = g.K / BK;
     p.n_tiles = g.Nout / BM;
     p.seg_tiles = g.seg_tiles;
     p.n_cta = g.n_cta;
     p.max_seg = g.max_seg;
-    static int stages = -1;
-    if (stages < 0) {
-        const char* e = getenv("LA_TC_STAGES");   // pipeline-depth override for tuning runs
-        stages = e ? atoi(e) : MAX_STAGES;
-        if (stages < 3) stages = 3;   // at least the weight tiles issued before the header
-        if (stages > MAX_STAGES) stages = MAX_STAGES;
-    }
-    p.max_stages = stages;
+    ring_shape(g.mode, rows_cap, &p.ns, &p.max_ns);
+    p.rows_cap = rows_cap;
+    p.wpack = (const uint8_t*)g.wpack;
     p.out = g.out;
     p.ldo = g.ldo;
     p.logits = g.logits;
@@ -805,20 +849,10 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.part_v = w.part_v;
     p.part_i = w.part_i;
     p.part_stride = w.part_stride;
-    p.max_chunks = (g.rows_cap + BN_MAX - 1) / BN_MAX;
+    p.max_chunks = (rows_cap + BN_MAX - 1) / BN_MAX;
     p.defer = g.defer;
-    const TcGemm* nx = (g.pf_units > 0) ? g.next : nullptr;
-    p.pf_units = nx ? g.pf_units : 0;
-    p.pf_n_tiles = nx ? nx->Nout / BM : 0;
-    p.pf_k_tiles = nx ? nx->K / BK : 0;
-    p.pf_seg_tiles = nx ? nx->seg_tiles : 0;
-    p.pf_swiglu = nx ? (nx->mode == GEMM_SWIGLU) : 0;
-    const CUtensorMap& pf1 = nx ? nx->tmA : g.tmA;
-    const CUtensorMap& pf2 = nx ? nx->tmA2 : g.tmA2;
-    const CUtensorMap& pf3 = nx ? nx->tmA3 : g.tmA3;
-    if (p.max_chunks < 1 || p.max_chunks > MAX_CHUNKS) return cudaErrorInvalidValue;
     const long long T = (long long)p.n_tiles * p.k_tiles;
     dim3 grid((unsigned)std::min<long long>(g.n_cta, T), 1);
     return la_launch_pdl(k_gemm_tc, grid, dim3(NTHREADS), (size_t)(SMEM_BYTES + 1024), st, g.tmA, g.tmA2, g.tmA3, g.tmB,
-                         g.tmB32, g.tmB64, g.tmB128, g.tmB256, pf1, pf2, pf3, p);
+                         g.tmB32, g.tmB64, g.tmB128, g.tmB256, p);
 }

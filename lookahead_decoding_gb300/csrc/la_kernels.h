@@ -126,9 +126,7 @@ struct TcGemm {
     int max_seg;          // largest number of CTAs sharing one tile's K range
     void* out; int ldo;
     float* logits; int ld_logits;   // GEMM_LOGITS: optional fp32 logits
-    // the GEMM launched after this one: each CTA prefetches the first pf_units
-    // (128 x 64) weight tiles of its share of `next` into L2 while it drains
-    const TcGemm* next; int pf_units;
+    void* wpack;          // unit-contiguous weight images (la_tc_pack), or null: the tensor maps
     int defer;            // 1: split tiles left as partials for the consumer (LaSplit)
     int ctr_off;          // first split-tile counter of this GEMM (counters are per GEMM)
 };
@@ -144,12 +142,18 @@ struct TcWork {
 };
 int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K);
-cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel);
+// rows_cap: the most rows any call of this launch (graph node) has
+cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, const TcWork& w, int sel,
+                              int rows_cap);
+// bytes of g's packed weights, and the packing of w1..w3 (the maps' matrices) into dst
+size_t la_tc_packed_bytes(const TcGemm& g);
+cudaError_t la_tc_pack(const TcGemm& g, const void* w1, const void* w2, const void* w3, void* dst, cudaStream_t st);
 int la_tc_ctas();
+// (tile, K) units per tile of a K-deep weight: 128-column units (64 for the gate/up pair)
+int la_tc_k_units(int mode, int K);
 int la_tc_pick_ctas(int n_tiles, int k_tiles, int mode);
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
 cudaError_t la_tc_prepare_device();
-int la_tc_pf_units();
 int la_tc_defer_default();
 LaSplit la_tc_split(const TcGemm& g, const TcWork& w);
 void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t* ws_floats, size_t* n_counters);

@@ -107,7 +107,7 @@ int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, c
     g.Nout = n_out;
     g.seg_tiles = 0;
     g.n_cta = n_cta;
-    g.max_seg = la_tc_max_segments(n_out / 128, K / 64, n_cta);
+    g.max_seg = la_tc_max_segments(n_out / 128, la_tc_k_units(mode, K), n_cta);
     g.rows_cap = ((rows + 255) / 256) * 256;
     g.out = y;
     g.ldo = n_out;
@@ -128,7 +128,7 @@ int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, c
     // the GEMM reads the header's row count before its dependency wait, so
     // the reset must have completed before the GEMM launches
     if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ECUDA;
-    if (la_launch_gemm_tc(d, st, g, wk, SEL_NEED) != cudaSuccess) return LA_ECUDA;
+    if (la_launch_gemm_tc(d, st, g, wk, SEL_NEED, rows) != cudaSuccess) return LA_ECUDA;
     int err = 0;
     if (cudaMemcpyAsync(&err, &hdr->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return LA_ECUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ECUDA;
