@@ -32,7 +32,8 @@ namespace {
 constexpr int DH = 128;
 constexpr int BLK = 128;          // positions per committed block
 constexpr int FR = 16;            // packed rows per CTA (one m16 tile)
-constexpr int FW = 8;             // warps per CTA
+constexpr int FW = 8;             // warps of the committed blocks (S, P V on tensor cores)
+constexpr int FT = 16;            // warps per CTA: the tail takes a row per warp
 constexpr int KPW = BLK / FW;     // keys of a block per warp (S = Q K^T)
 constexpr int DPW = DH / FW;      // dimensions per warp (O = P V)
 constexpr int NTW = KPW / 8;      // n-tiles of 8 per warp (KPW == DPW)
@@ -89,6 +90,9 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
     return pack_f16(__low2float(b), __high2float(b));
 }
 
+// barrier among the FW block warps (the helper warps are not in the block loop)
+__device__ __forceinline__ void bar_blocks() { asm volatile("bar.sync 1, %0;" ::"n"(FW * 32) : "memory"); }
+
 __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
@@ -108,19 +112,19 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;           // K and V rows, bf16
     L.q = L.ring + L.ring_bytes;                                    // [FR][LDK] bf16
     L.p = L.q + FR * LDK * 2;                                       // [FR][LDK] fp16
-    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32, then [FW][DH] fp32 queries
-    L.wmax = L.o + (FR + FW) * DH * 4;                              // [FW][FR] fp32
+    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32, then [FT][DH] fp32 queries
+    L.wmax = L.o + (FR + FT) * DH * 4;                              // [FW][FR] fp32
     L.wl = L.wmax + FW * FR * 4;                                    // [FW][FR] fp32
     L.rpos = L.wl + FW * FR * 4;                                    // [FR] int
     L.rt0 = L.rpos + FR * 4;                                        // [FR] int
-    L.pw = L.rt0 + FR * 4;                                          // [FW][MAX_TAIL] fp32
-    L.sw = L.pw + FW * MAX_TAIL * 4;                                // [FW][MAX_TAIL] int
-    L.path = L.sw + FW * MAX_TAIL * 4;                              // [FR][pmax] int
+    L.pw = L.rt0 + FR * 4;                                          // [FT][MAX_TAIL] fp32
+    L.sw = L.pw + FT * MAX_TAIL * 4;                                // [FT][MAX_TAIL] int
+    L.path = L.sw + FT * MAX_TAIL * 4;                              // [FR][pmax] int
     L.total = L.path + (uint32_t)FR * pmax * 4;
     return L;
 }
 
-__global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
+__global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
                                                       const __nv_bfloat16* vc, const __nv_bfloat16* kt,
                                                       const __nv_bfloat16* vt, __nv_bfloat16* out, int sel, int Qcap,
                                                       int max_ctx, int Qmax, int TB, int H, int ring_keys) {
@@ -147,10 +151,13 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     const __nv_bfloat16* kh = kc + (size_t)hh * max_ctx * DH;
     const __nv_bfloat16* vh = vc + (size_t)hh * max_ctx * DH;
 
+    // committed blocks are staged by the block warps alone (cp.async groups
+    // are per thread: the warps that wait on a block issued all of it)
     auto stage_block = [&](int b, int buf) {
         const uint32_t kb = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u);
         const uint32_t vb = kb + BLK * LDK * 2u;
-        for (int i = tid; i < BLK * (DH / 8); i += blockDim.x) {
+        if (warp >= FW) return;
+        for (int i = tid; i < BLK * (DH / 8); i += FW * 32) {
             const int key = i >> 4, c8 = (i & 15) * 8;
             const int p = b * BLK + key;
             const int ok = p < max_ctx;
@@ -227,7 +234,8 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         ldsm_x4(sbase + LY.q + (uint32_t)((lane & 15) * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qa[ks8]);
 
     const float scale = 0.08838834764831845f;   // 1/sqrt(128)
-    for (int b = 0; b < nb; ++b) {
+    // warps FW .. FT-1 wait for the blocks at the barrier before the tail
+    for (int b = 0; b < (warp < FW ? nb : 0); ++b) {
         const int buf = b & 1;
         if (b + 1 < nb) {
             stage_block(b + 1, buf ^ 1);
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         } else {
             asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
         }
-        __syncthreads();
+        bar_blocks();
         const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring + (size_t)buf * (2 * BLK * LDK * 2));
         const uint32_t vs_a = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u) + BLK * LDK * 2u;
         const int key0 = b * BLK;
@@ -268,7 +276,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
         mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
         if (t == 0) { wmax[warp * FR + g] = ma; wmax[warp * FR + g + 8] = mb; }
-        __syncthreads();
+        bar_blocks();
         // block maximum per row over the warps
         ma = wmax[g];
         mb = wmax[g + 8];
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 1));
         lb = __fadd_rn(lb, __shfl_xor_sync(0xffffffffu, lb, 2));
         if (t == 0) { wl[warp * FR + g] = la; wl[warp * FR + g + 8] = lb; }
-        __syncthreads();
+        bar_blocks();
         la = wl[g];
         lb = wl[g + 8];
 #pragma unroll
@@ -350,9 +358,10 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
             }
             m_b = mn;
         }
-        __syncthreads();      // P, the warp maxima/sums and this buffer are reused
+        bar_blocks();      // P, the warp maxima/sums and this buffer are reused
     }
     // the committed state to shared memory: O by (row, dim), m and l per row
+    if (warp < FW) {
 #pragma unroll
     for (int n = 0; n < NTW; ++n) {
         const int col = warp * DPW + n * 8 + 2 * t;
@@ -363,6 +372,8 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
         wmax[g] = m_a; wmax[g + 8] = m_b;
         wl[g] = l_a; wl[g + 8] = l_b;
     }
+    }
+    __syncthreads();      // the ring is free for the tail keys
 
     // tail keys: committed positions [t0min, Kc) then (in a call) the temporary rows
     const int Kc = prefill ? posmax + 1 : K;
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(FW * 32) k_attn_fused(LaDev d, const __nv_bflo
     float* pwr = pw + warp * MAX_TAIL;
     float* qf = os + FR * DH;                        // per-warp fp32 copy of the row's query (after O)
     qf += warp * DH;
-    for (int r = warp; r < nr; r += FW) {
+    for (int r = warp; r < nr; r += FT) {
         const int pos = rpos[r], t0 = rt0[r];
         const int n = pos - t0 + 1;                  // tail keys, positions t0 .. pos
         const int Kr = prefill ? pos + 1 : K;
@@ -521,7 +532,7 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
     }
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     dim3 grid(H, (rows_cap + FR - 1) / FR);
-    return la_launch_pdl(k_attn_fused, grid, dim3(FW * 32), smem, st, d, (const __nv_bfloat16*)qbuf,
+    return la_launch_pdl(k_attn_fused, grid, dim3(FT * 32), smem, st, d, (const __nv_bfloat16*)qbuf,
                          (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
                          (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, H, ring_keys);
 }
