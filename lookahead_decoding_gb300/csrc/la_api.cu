@@ -57,6 +57,7 @@ struct la_ctx {
     float *rcos = nullptr, *rsin = nullptr;
     float* logits = nullptr;          // [Qcap][V] fp32
     int attn_TB = 0;
+    CUtensorMap cache_map;            // the K/V cache as [L*2*H*max_ctx][head_dim] rows, 64 x 128 boxes, 128B swizzle
     float* logits_in = nullptr;       // [Qmax][V] staging for injected logits
     int32_t* argmax_in = nullptr;     // [Qcap]
     TcWork work{};
@@ -226,7 +227,8 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
                                         layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
                                         layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax),
                                         layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, H, sel,
-                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX));
+                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX, ctx->cache_map,
+                                        (l * 2 + 0) * H * ctx->max_ctx, (l * 2 + 1) * H * ctx->max_ctx));
         } else {
             CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
                                    layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
@@ -509,6 +511,8 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
     A((void**)&ctx->logits_in, sizeof(float) * (size_t)ctx->Qmax * V);
     if (ctx->bf16) {
         ctx->attn_TB = la_attn_tail_blocks(ctx->PMAX);
+        if (!r && la_tc_make_map(&ctx->cache_map, ctx->cache, c.n_layers * 2 * c.n_heads * max_ctx, c.head_dim, 128))
+            r = LA_ECUDA;
         if (la_attn_smem_bytes(ctx->attn_TB, ctx->Qmax, ctx->PMAX) > 227 * 1024) r = LA_ENOTSUP;
     }
     if (r) { la_free(ctx); return r; }

@@ -79,6 +79,38 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// bounded wait for phase `parity` of an mbarrier; false once the limit is spent
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < LA_SPIN_LIMIT; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+                 "l"(m), "r"(bar), "r"(x), "r"(y)
+                 : "memory");
+}
+// byte offset of (key, dimension pair start) in a TMA-staged block: two
+// 64-dimension boxes of BLK rows x 128 B, 16-byte chunks swizzled by key mod 8
+__device__ __forceinline__ uint32_t blk_off(int key, int dim) {
+    return (uint32_t)((dim >> 6) * (BLK * 128) + key * 128 + ((((dim & 63) >> 3) ^ (key & 7)) << 4) + ((dim & 7) << 1));
+}
+
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -103,13 +135,18 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // shared memory (bytes): the K/V ring (reused for the tail keys), then fixed areas
+// (offsets from the first 1024-byte boundary of the dynamic shared memory;
+// the launch adds 1024 bytes of slack).  The ring holds two committed blocks
+// as TMA leaves them (K then V, each two 64-dimension boxes of 128-byte rows,
+// 64 KB per block) or, after the blocks, the tail keys in padded rows.
 struct FusedLayout {
-    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, path, total;
+    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, bar, path, total;
 };
 __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     FusedLayout L;
     L.ring = 0;
     L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;           // K and V rows, bf16
+    if (L.ring_bytes < 2u * 4u * BLK * 128u) L.ring_bytes = 2u * 4u * BLK * 128u;
     L.q = L.ring + L.ring_bytes;                                    // [FR][LDK] bf16
     L.p = L.q + FR * LDK * 2;                                       // [FR][LDK] fp16
     L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32, then [FT][DH] fp32 queries
@@ -119,7 +156,8 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     L.rt0 = L.rpos + FR * 4;                                        // [FR] int
     L.pw = L.rt0 + FR * 4;                                          // [FT][MAX_TAIL] fp32
     L.sw = L.pw + FT * MAX_TAIL * 4;                                // [FT][MAX_TAIL] int
-    L.path = L.sw + FT * MAX_TAIL * 4;                              // [FR][pmax] int
+    L.bar = L.sw + FT * MAX_TAIL * 4;                               // 2 mbarriers
+    L.path = L.bar + 16;                                            // [FR][pmax] int
     L.total = L.path + (uint32_t)FR * pmax * 4;
     return L;
 }
@@ -127,7 +165,8 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
 __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
                                                       const __nv_bfloat16* vc, const __nv_bfloat16* kt,
                                                       const __nv_bfloat16* vt, __nv_bfloat16* out, int sel, int Qcap,
-                                                      int max_ctx, int Qmax, int TB, int H, int ring_keys) {
+                                                      int max_ctx, int Qmax, int TB, int H, int ring_keys,
+                                                      const __grid_constant__ CUtensorMap cmap, int krow0, int vrow0) {
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
     const int prefill = (sel == SEL_PREFILL);
@@ -135,9 +174,11 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const int g = lane >> 2, t = lane & 3;
     const int PM = d.PMAX;
 
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     const FusedLayout LY = fused_layout(ring_keys, PM);
-    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+    const uint32_t sraw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - sraw);
     __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
     __half* ps = reinterpret_cast<__half*>(smem + LY.p);
     float* os = reinterpret_cast<float*>(smem + LY.o);
@@ -151,23 +192,27 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const __nv_bfloat16* kh = kc + (size_t)hh * max_ctx * DH;
     const __nv_bfloat16* vh = vc + (size_t)hh * max_ctx * DH;
 
-    // committed blocks are staged by the block warps alone (cp.async groups
-    // are per thread: the warps that wait on a block issued all of it)
+    // Committed block b (positions b*BLK ..) into ring buffer buf by TMA,
+    // issued by thread 0, completing on barrier buf: rows krow0 + hh*max_ctx +
+    // position of the cache (rows past this head's range read masked keys or
+    // the zero fill past the end of the cache).
+    const uint32_t bar0 = sbase + LY.bar;
     auto stage_block = [&](int b, int buf) {
-        const uint32_t kb = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u);
-        const uint32_t vb = kb + BLK * LDK * 2u;
-        if (warp >= FW) return;
-        for (int i = tid; i < BLK * (DH / 8); i += FW * 32) {
-            const int key = i >> 4, c8 = (i & 15) * 8;
-            const int p = b * BLK + key;
-            const int ok = p < max_ctx;
-            const size_t src = (size_t)(ok ? p : 0) * DH + c8;
-            const uint32_t off = (uint32_t)(key * LDK + c8) * 2u;
-            cp_async16(kb + off, kh + src, ok ? 16 : 0);
-            cp_async16(vb + off, vh + src, ok ? 16 : 0);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (tid != 0) return;
+        const uint32_t kb = sbase + LY.ring + (uint32_t)buf * (4u * BLK * 128u);
+        const uint32_t vb = kb + 2u * BLK * 128u, bar = bar0 + 8u * buf;
+        const int y = b * BLK + hh * max_ctx;
+        mbar_arrive_tx(bar, 4u * BLK * 128u);
+        tma_2d(kb, &cmap, bar, 0, krow0 + y);
+        tma_2d(kb + BLK * 128u, &cmap, bar, 64, krow0 + y);
+        tma_2d(vb, &cmap, bar, 0, vrow0 + y);
+        tma_2d(vb + BLK * 128u, &cmap, bar, 64, vrow0 + y);
     };
+    if (tid == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
 
     // Before the wait (la_common.cuh): the header, and in a decode call the
     // tile's row positions and paths (written by the pack kernel) and, for
@@ -220,13 +265,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     for (int n = 0; n < NTW; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     // Q fragments (A operand of S = Q K^T) for the 8 k-steps, from shared memory
-    if (nb > 0 && !spec0) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(1) : "memory");     // the queries, not block 0
-    } else {
-        // the first tile staged block 0 before its queries (so both land here);
-        // with no committed block, block 0 still lands before the ring is reused
-        asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
-    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");     // the queries
     __syncthreads();
     uint32_t qa[8][4];
 #pragma unroll
@@ -237,26 +276,22 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     // warps FW .. FT-1 wait for the blocks at the barrier before the tail
     for (int b = 0; b < (warp < FW ? nb : 0); ++b) {
         const int buf = b & 1;
-        if (b + 1 < nb) {
-            stage_block(b + 1, buf ^ 1);
-            asm volatile("cp.async.wait_group %0;" ::"n"(1) : "memory");
-        } else {
-            asm volatile("cp.async.wait_group %0;" ::"n"(0) : "memory");
-        }
-        bar_blocks();
-        const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring + (size_t)buf * (2 * BLK * LDK * 2));
-        const uint32_t vs_a = sbase + LY.ring + (uint32_t)buf * (2u * BLK * LDK * 2u) + BLK * LDK * 2u;
+        // buffer buf ^ 1 held block b - 1, which every block warp has finished
+        if (b + 1 < nb) stage_block(b + 1, buf ^ 1);
+        if (!mbar_wait(bar0 + 8u * buf, (uint32_t)((b >> 1) & 1)) && lane == 0) la_set_err(d.hdr, LA_ETIMEOUT);
+        const uint8_t* kbb = smem + LY.ring + (size_t)buf * (4 * BLK * 128);
+        const uint32_t vs_a = sbase + LY.ring + (uint32_t)buf * (4u * BLK * 128u) + 2u * BLK * 128u;
         const int key0 = b * BLK;
         // S for this warp's KPW keys (NTW n-tiles of 8)
         float s[NTW][4];
 #pragma unroll
         for (int n = 0; n < NTW; ++n) {
             s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-            const __nv_bfloat16* krow = ks + (warp * KPW + n * 8 + g) * LDK + 2 * t;
+            const int key = warp * KPW + n * 8 + g;
 #pragma unroll
             for (int ks8 = 0; ks8 < 8; ++ks8) {
-                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16 + 8);
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kbb + blk_off(key, ks8 * 16 + 2 * t));
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kbb + blk_off(key, ks8 * 16 + 8 + 2 * t));
                 mma16816(s[n], qa[ks8], b0, b1);
             }
         }
@@ -328,7 +363,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
 #pragma unroll
             for (int n = 0; n < NTW; n += 2) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vs_a + (uint32_t)((kk * 16 + key_off) * LDK + warp * DPW + n * 8 + dim_off) * 2u, b0, b1, b2, b3);
+                ldsm_x4_trans(vs_a + blk_off(kk * 16 + key_off, warp * DPW + n * 8 + dim_off), b0, b1, b2, b3);
                 mma16816_f16(ob[n], a, bf2_to_h2(b0), bf2_to_h2(b1));
                 mma16816_f16(ob[n + 1], a, bf2_to_h2(b2), bf2_to_h2(b3));
             }
@@ -373,6 +408,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         wl[g] = l_a; wl[g + 8] = l_b;
     }
     }
+    // a first tile without committed blocks still had block 0 staged
+    if (tid == 0 && spec0 && nb == 0 && !mbar_wait(bar0, 0)) la_set_err(d.hdr, LA_ETIMEOUT);
     __syncthreads();      // the ring is free for the tail keys
 
     // tail keys: committed positions [t0min, Kc) then (in a call) the temporary rows
@@ -515,15 +552,16 @@ static int ring_keys_for(int TB, int Qmax) {
 }
 
 size_t la_attn_smem_bytes(int TB, int Qmax, int pmax) {
-    return fused_layout(ring_keys_for(TB, Qmax), pmax).total;
+    return fused_layout(ring_keys_for(TB, Qmax), pmax).total + 1024;   // + alignment slack
 }
 
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
-                                     int max_ctx, int Qmax, int rows_cap, int TB, int pmax) {
+                                     int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
+                                     int krow0, int vrow0) {
     if (TB + 1 > MAX_TAIL / 32) return cudaErrorInvalidValue;
     const int ring_keys = ring_keys_for(TB, Qmax);
-    const size_t smem = fused_layout(ring_keys, pmax).total;
+    const size_t smem = la_attn_smem_bytes(TB, Qmax, pmax);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_attn_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -534,5 +572,6 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
     dim3 grid(H, (rows_cap + FR - 1) / FR);
     return la_launch_pdl(k_attn_fused, grid, dim3(FT * 32), smem, st, d, (const __nv_bfloat16*)qbuf,
                          (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
-                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, H, ring_keys);
+                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, H, ring_keys,
+                         cmap, krow0, vrow0);
 }

@@ -170,4 +170,5 @@ int la_attn_tail_blocks(int pmax);
 size_t la_attn_smem_bytes(int TB, int Qmax, int pmax);
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
-                                     int max_ctx, int Qmax, int rows_cap, int TB, int pmax);
+                                     int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
+                                     int krow0, int vrow0);
