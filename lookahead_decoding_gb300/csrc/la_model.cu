@@ -92,24 +92,29 @@ __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g,
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int row = blockIdx.x;
     if (row >= rows_of(h, sel)) return;
-    la_pdl_wait();
-    la_pdl_trigger();
-    const int src = gather ? d.need[row] : row;
-    float* xr = x + (size_t)src * dm;
     // the row stays in registers: up to 2 float4 per thread (256 threads for
     // d_model <= 2048, 1024 threads up to 8192)
     constexpr int MAXV = 2;
     float4 v[MAXV], add[MAXV], gv[MAXV];
     bool upd[MAXV];
-    // every load (the row, the split partials, the gains) is issued before
-    // the first store of the updated row
+    // the gains (weights) are read before the wait, the row after it
+#pragma unroll
+    for (int k = 0; k < MAXV; ++k) {
+        const int i = (k * blockDim.x + threadIdx.x) * 4;
+        if (i < dm) gv[k] = load4<T>(g + i);
+    }
+    la_pdl_wait();
+    la_pdl_trigger();
+    const int src = gather ? d.need[row] : row;
+    float* xr = x + (size_t)src * dm;
+    // every load of the row and its split partials is issued before the
+    // first store of the updated row
 #pragma unroll
     for (int k = 0; k < MAXV; ++k) {
         const int i = (k * blockDim.x + threadIdx.x) * 4;
         upd[k] = false;
         if (i < dm) {
             v[k] = *reinterpret_cast<const float4*>(xr + i);
-            gv[k] = load4<T>(g + i);
             if (resid.ws) {
                 const int tile = i >> 7;
                 const int nseg = la_split_nseg(resid, tile);
@@ -184,14 +189,16 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int q = blockIdx.x;
     if (q >= rows_of(h, sel)) return;
-    la_pdl_wait();
-    la_pdl_trigger();
     const int half = dh >> 1;
     // blockDim = RH heads x half threads
-    int hh = blockIdx.y * (blockDim.x / half) + threadIdx.x / half, i = threadIdx.x % half;
+    const int hh = blockIdx.y * (blockDim.x / half) + threadIdx.x / half, i = threadIdx.x % half;
+    // the row's position (pack or chunk kernel) and its rotation (a table
+    // written at init) are read before the wait; the QKV output after it
+    const int pos = d.row_pos[q];
+    const float c = rcos[(size_t)pos * half + i], s = rsin[(size_t)pos * half + i];
+    la_pdl_wait();
+    la_pdl_trigger();
     if (hh >= H) return;
-    int pos = d.row_pos[q];
-    float c = rcos[(size_t)pos * half + i], s = rsin[(size_t)pos * half + i];
     const int HD = H * dh;
     const T* row = qkv + (size_t)q * 3 * HD;
     const int nq = hh * dh, nk = HD + hh * dh, nv = 2 * HD + hh * dh;
