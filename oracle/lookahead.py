@@ -32,6 +32,16 @@ Notation follows "M7.3 – Lookahead Decoding" (§0x01A, §0x03–§0x07):
   winner's first a verification rows are copied to K_in+1..K_in+a; the next
   ordinary input is the last emitted token.
 * Window advance, ALWAYS_FWD_ONE (§0x03C): [u^(1)[1:], u^(2), ..., u^(R-1), z].
+* Optional pool seeding (§0x03A POOL_FROM_PROMPT; §0x06A "optional
+  generated-prefix insertion"; Break the Sequential Dependency §5, prompt
+  lookup): the n-grams of the token sequence (prompt, then every output
+  token) are upserted into the same keyed LRU pool, the n-gram ending at
+  sequence position k keyed by token k-S with suffix tokens k-S+1..k, in
+  increasing k.  From the prompt: every n-gram that lies inside the prompt,
+  once, when the request starts.  From the output: every n-gram that ends at
+  an output token, when that token is appended (the first token at request
+  start, after any prompt n-grams; a call's tokens after that call's
+  trajectory n-grams).
 """
 from __future__ import annotations
 
@@ -184,6 +194,14 @@ def upsert_suffix_lru(pool: Dict[int, List[tuple]], key: int, suffix: tuple, G: 
     bucket.append(suffix)
 
 
+def upsert_sequence_ngrams(pool: Dict[int, List[tuple]], seq: Sequence[int], k_lo: int, k_hi: int,
+                           S: int, G: int) -> None:
+    """The n-grams of ``seq`` ending at positions k_lo <= k < k_hi (those with
+    k >= S): key seq[k-S], suffix seq[k-S+1..k], upserted in increasing k."""
+    for k in range(max(k_lo, S), k_hi):
+        upsert_suffix_lru(pool, int(seq[k - S]), tuple(int(t) for t in seq[k - S + 1:k + 1]), G)
+
+
 def lookup(pool: Dict[int, List[tuple]], key: int, G: int) -> List[tuple]:
     return list(pool.get(int(key), [])[:G])
 
@@ -282,7 +300,8 @@ class StepInfo:
 class LookaheadState:
     """Window, pool and frontier of one request between packed calls."""
 
-    def __init__(self, prompt: Sequence[int], first_token: int, W: int, N: int, G: int):
+    def __init__(self, prompt: Sequence[int], first_token: int, W: int, N: int, G: int,
+                 pool_from_prompt: bool = False, pool_from_output: bool = False):
         self.S = check_args(W, N, G)
         self.W, self.N, self.G = W, N, G
         self.levels = init_levels(prompt, W, N)
@@ -290,6 +309,13 @@ class LookaheadState:
         self.x_t = int(first_token)
         self.p = len(prompt)           # committed K/V length = position of x_t
         self.step = 0
+        self.pool_from_output = pool_from_output
+        self.seq = [int(t) for t in prompt] + [int(first_token)]   # prompt, then the output tokens
+        P = len(prompt)
+        if pool_from_prompt:
+            upsert_sequence_ngrams(self.pool, self.seq, 0, P, self.S, G)
+        if pool_from_output:
+            upsert_sequence_ngrams(self.pool, self.seq, P, P + 1, self.S, G)
 
     @property
     def steady(self) -> bool:
@@ -332,6 +358,10 @@ class LookaheadState:
         if steady:
             for key, suffix in extract_keyed_ngrams(self.x_t, self.levels, z, self.N, self.W):
                 upsert_suffix_lru(self.pool, key, suffix, self.G)
+        n0 = len(self.seq)
+        self.seq.extend(int(t) for t in emitted)
+        if self.pool_from_output:
+            upsert_sequence_ngrams(self.pool, self.seq, n0, len(self.seq), S, self.G)
         self.levels = advance_window(self.levels, z, steady)
         info = StepInfo(len(rows), len(guesses), steady, a, w, list(emitted), commit)
         self.x_t = int(emitted[-1])
@@ -431,12 +461,13 @@ def ar_generate(model: OracleModel, prompt: Sequence[int], max_new: int,
 
 def lookahead_generate(model: OracleModel, prompt: Sequence[int], max_new: int, W: int, N: int, G: int,
                        schedule: str = "meta", sampling: Optional[Sampling] = None,
-                       trace: Optional[list] = None) -> List[int]:
+                       trace: Optional[list] = None, pool_from_prompt: bool = False,
+                       pool_from_output: bool = False) -> List[int]:
     """Lookahead decoding (§0x06 loop) on one schedule of the packed call."""
     check_args(W, N, G)
     cache, logits = model.prefill(prompt)
     out = [_first_token(logits[-1], sampling)]
-    st = LookaheadState(prompt, out[0], W, N, G)
+    st = LookaheadState(prompt, out[0], W, N, G, pool_from_prompt, pool_from_output)
     runner = make_runner(model, cache, schedule)
     while len(out) < max_new:
         rows, guesses = st.plan()

@@ -206,3 +206,22 @@ def test_wrong_commit_row_breaks_equality():
             out.extend(info.emitted)
         diverged += out[:24] != ar
     assert diverged > 0
+
+
+@pytest.mark.parametrize("W,N,G", [(3, 3, 3), (5, 4, 2), (2, 5, 4)])
+def test_seeded_pool_lookahead_equals_ar(W, N, G):
+    """Seeding only changes which candidates are tried: the output stays the
+    greedy AR output, and a copy-heavy prompt gets candidates from the first
+    steady call on."""
+    offered = 0
+    for seed in range(8):
+        m = model_for(MICRO, 60 + seed)
+        base = list(synth.uniform_prompt(MICRO.vocab, 6, 200 + seed))
+        prompt = base + base + base
+        ar = la.ar_generate(m, prompt, 24)
+        tr = []
+        lk = la.lookahead_generate(m, prompt, 24, W, N, G, trace=tr, pool_from_prompt=True, pool_from_output=True)
+        assert lk == ar, (seed, lk, ar)
+        first_steady = next(i for i in tr if i.steady)
+        offered += first_steady.C_t
+    assert offered > 0

@@ -263,3 +263,41 @@ def test_pool_updates_only_after_outputs():
     assert g == []                                 # nothing in the pool yet
     st.publish(rows, g, [9] * len(rows))
     assert 9 in st.pool
+
+
+# ---- pool seeding (POOL_FROM_PROMPT, generated-prefix insertion) ------------
+
+def test_pool_from_prompt_hand_example():
+    """The prompt's n-grams, keyed by their first token, upserted in position
+    order under the per-key LRU rule (worked by hand, N=3, G=2)."""
+    p = [5, 6, 7, 5, 6, 8, 5, 6, 7]
+    st = la.LookaheadState(p, 9, 2, 3, 2, pool_from_prompt=True)
+    assert st.pool == {5: [(6, 8), (6, 7)], 6: [(7, 5), (8, 5)], 7: [(5, 6)], 8: [(5, 6)]}
+
+
+def test_pool_from_output_first_token():
+    """The n-gram ending at the first output token (sequence position P) goes
+    in after the prompt's: key 6 (position 7), suffix (7, 9) evicts (7, 5)."""
+    p = [5, 6, 7, 5, 6, 8, 5, 6, 7]
+    both = la.LookaheadState(p, 9, 2, 3, 2, pool_from_prompt=True, pool_from_output=True)
+    assert both.pool[6] == [(8, 5), (7, 9)]
+    only = la.LookaheadState(p, 9, 2, 3, 2, pool_from_output=True)
+    assert only.pool == {6: [(7, 9)]}
+
+
+def test_pool_from_output_after_a_call():
+    """A call's emitted tokens add the n-grams ending at them, after the
+    call's own trajectory n-grams (none in a warm-up call)."""
+    p = [5, 6, 7, 5, 6, 8, 5, 6, 7]
+    st = la.LookaheadState(p, 9, 2, 3, 2, pool_from_output=True)
+    rows, g = st.plan()
+    assert not st.steady
+    info = st.publish(rows, g, [4] * len(rows))
+    assert info.emitted == [4]
+    assert st.pool == {6: [(7, 9)], 7: [(9, 4)]}
+    assert st.seq == p + [9, 4]
+
+
+def test_unseeded_pool_starts_empty():
+    st = la.LookaheadState([5, 6, 7, 5, 6, 8], 9, 2, 3, 2)
+    assert st.pool == {}
