@@ -103,6 +103,23 @@ typedef struct {
     uint64_t seed;
 } la_sampling;
 
+/* Pool seeding options (la_set_options), off by default.  Both feed the
+ * same keyed LRU n-gram pool as the trajectory n-grams (M7.3 §0x03A
+ * POOL_FROM_PROMPT, §0x06A generated-prefix insertion; break the sequential
+ * dependency §5, prompt lookup).  The token sequence is the prompt followed
+ * by every output token; the n-gram ending at sequence position k is keyed by
+ * token k-(N-1) with suffix tokens k-(N-1)+1 .. k, upserted in increasing k.
+ *   LA_OPT_POOL_FROM_PROMPT  every n-gram inside the prompt, when a request
+ *                            starts
+ *   LA_OPT_POOL_FROM_OUTPUT  the n-gram ending at each output token as it is
+ *                            appended (the first token when the request
+ *                            starts, after the prompt's n-grams; a call's
+ *                            tokens after the call's trajectory n-grams)
+ * Outputs are unchanged (greedy: still the AR tokens); only which candidates
+ * are verified changes. */
+#define LA_OPT_POOL_FROM_PROMPT 1u
+#define LA_OPT_POOL_FROM_OUTPUT 2u
+
 /* Counters of the last la_generate / la_generate_ar call. */
 typedef struct {
     int64_t steps;              /* packed target calls after the prefill */
@@ -132,6 +149,11 @@ typedef struct {
  * Errors: LA_EINVAL, LA_ENOTSUP, LA_ECUDA. */
 int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
             int max_W, int max_N, int max_G, void* stream, la_ctx** out);
+
+/* Pool seeding options (LA_OPT_* bits) for the requests that start after
+ * this call (la_generate, or the first la_step after la_prefill).  Unknown
+ * bits: LA_EINVAL.  Host-only; does not synchronise. */
+int la_set_options(la_ctx* ctx, uint32_t flags);
 
 /* Prefill the prompt (host ids, n >= 1, each in [0, vocab)) with one causal
  * forward; resets the K/V cache, the window, the pool and the step counter.

@@ -22,7 +22,10 @@ LA_F32, LA_BF16 = 0, 1
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
            "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
-           "la_gemm_noalloc", "la_profile_read"]
+           "la_gemm_noalloc", "la_profile_read", "la_set_options"]
+
+# pool seeding options (la_set_options)
+LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT = 1, 2
 
 
 class la_model_cfg(C.Structure):
@@ -72,6 +75,7 @@ def _load() -> C.CDLL:
         "la_generate_ar": (C.c_int, [vp, i32p, C.c_int, C.c_int, C.POINTER(la_sampling), i32p, C.POINTER(C.c_int),
                                      C.POINTER(la_stats)]),
         "la_set_debug": (C.c_int, [vp, C.c_int]),
+        "la_set_options": (C.c_int, [vp, C.c_uint32]),
         "la_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
         "la_debug_logits": (C.c_int, [vp, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
         "la_debug_state": (C.c_int, [vp, i32p, i32p, i32p, i32p, i32p, i32p]),
@@ -136,6 +140,11 @@ def la_init(cfg: la_model_cfg, weights: la_weights, max_ctx: int, max_W: int, ma
                        C.byref(ctx))
     _check(code, "la_init")
     return ctx
+
+
+def la_set_options(ctx, flags: int) -> None:
+    """Pool seeding (LA_OPT_* bits) for requests started after this call."""
+    _check(LIB.la_set_options(ctx, flags), "la_set_options", ctx)
 
 
 def la_prefill(ctx, prompt: Sequence[int], sampling=None) -> int:

@@ -57,6 +57,7 @@ struct la_ctx {
     float *rcos = nullptr, *rsin = nullptr;
     float* logits = nullptr;          // [Qcap][V] fp32
     int attn_TB = 0;
+    uint32_t opts = 0;                // LA_OPT_* for requests started from now on
     CUtensorMap cache_map;            // the K/V cache as [L*2*H*max_ctx][head_dim] rows, 64 x 128 boxes, 128B swizzle
     float* logits_in = nullptr;       // [Qmax][V] staging for injected logits
     int32_t* argmax_in = nullptr;     // [Qcap]
@@ -688,6 +689,12 @@ int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, 
     return LA_OK;
 }
 
+int la_set_options(la_ctx* ctx, uint32_t flags) {
+    if (!ctx || (flags & ~(LA_OPT_POOL_FROM_PROMPT | LA_OPT_POOL_FROM_OUTPUT))) return LA_EINVAL;
+    ctx->opts = flags;
+    return LA_OK;
+}
+
 static int begin_request(la_ctx* ctx, int mode, int W, int N, int G, const la_sampling* s, int max_out) {
     if (mode == MODE_LOOKAHEAD) {
         if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
@@ -697,7 +704,7 @@ static int begin_request(la_ctx* ctx, int mode, int W, int N, int G, const la_sa
     ctx->W = W; ctx->N = N; ctx->G = G;
     ctx->sampling = s ? 1 : 0;
     la_launch_begin(ctx->d, ctx->st, mode, W, N, G, ctx->sampling, s ? s->temperature : 1.f, s ? s->top_p : 1.f,
-                    s ? s->seed : 0, max_out);
+                    s ? s->seed : 0, max_out, (int)ctx->opts);
     CK(cudaGetLastError());
     ctx->begun = true;
     return LA_OK;

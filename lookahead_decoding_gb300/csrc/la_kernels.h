@@ -18,7 +18,7 @@ struct LaDev;
 #define SEL_NEED 2     // rows whose logits are read
 
 void la_launch_begin(const LaDev& d, cudaStream_t st, int mode, int W, int N, int G, int sampling,
-                     float temperature, float top_p, uint64_t seed, int max_out);
+                     float temperature, float top_p, uint64_t seed, int max_out, int opts);
 void la_launch_pack(const LaDev& d, cudaStream_t st);
 void la_launch_publish(const LaDev& d, cudaStream_t st, int verdict_given);
 void la_launch_commit(const LaDev& d, cudaStream_t st, void* cache, void* temp, int planes, int n_heads,

@@ -19,11 +19,12 @@
 // request start: seed level 0 with W+N-3 prompt tokens (cyclic), §0x03A
 // ---------------------------------------------------------------------------
 __global__ void k_begin(LaDev d, int mode, int W, int N, int G, int sampling,
-                        float temperature, float top_p, uint32_t seed_lo, uint32_t seed_hi, int max_out) {
+                        float temperature, float top_p, uint32_t seed_lo, uint32_t seed_hi, int max_out, int opts) {
     LaHdr* h = d.hdr;
     int t = threadIdx.x;
     if (t == 0) {
         h->mode = mode;
+        h->opts = opts;
         h->sampling = sampling;
         h->W = W; h->N = N; h->G = G; h->S = N - 1;
         h->step = 0;
@@ -177,11 +178,42 @@ __device__ void pool_upsert_warp(const LaDev& d, int key, const int* suffix, int
     __syncwarp();
 }
 
+// token at position k of the request's sequence: the prompt, then the out ring
+__device__ __forceinline__ int seq_tok(const LaDev& d, int P, int k) { return k < P ? d.prompt[k] : d.out[k - P]; }
+
+// the n-gram ending at sequence position k (k >= S): key token k-S, suffix k-S+1 .. k
+__device__ __forceinline__ void upsert_seq_ngram_warp(const LaDev& d, int P, int k, int S, int G) {
+    int suf[LA_MAX_R];
+    const int key = seq_tok(d, P, k - S);
+    for (int s = 0; s < S; ++s) suf[s] = seq_tok(d, P, k - S + 1 + s);
+    pool_upsert_warp(d, key, suf, S, G);
+}
+
+// ---------------------------------------------------------------------------
+// request start, optional pool seeding (POOL_FROM_PROMPT of M7.3 §0x03A,
+// generated-prefix insertion of §0x06A): the n-grams ending at sequence
+// positions S .. P-1 (inside the prompt) and/or P (the first output token),
+// in increasing position.  Warp w applies the n-grams whose key is w modulo
+// the warp count, so each key's upserts keep their order.
+// ---------------------------------------------------------------------------
+__global__ void k_pool_seed(LaDev d) {
+    const LaHdr* h = d.hdr;
+    const int opts = h->opts, G = h->G, S = h->S, P = h->prompt_len;
+    if (h->err || h->mode != MODE_LOOKAHEAD || G <= 0) return;
+    const int k_lo = (opts & LA_OPT_POOL_FROM_PROMPT) ? S : P;
+    const int k_hi = (opts & LA_OPT_POOL_FROM_OUTPUT) ? P + 1 : P;
+    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int k = k_lo > S ? k_lo : S; k < k_hi; ++k) {
+        const int key = seq_tok(d, P, k - S);
+        if (key % nw == warp) upsert_seq_ngram_warp(d, P, k, S, G);
+    }
+}
+
 __global__ void k_publish(LaDev d, int verdict_given) {
     la_pdl_wait();
     la_pdl_trigger();
     LaHdr* h = d.hdr;
-    __shared__ int s_best, s_emit[16], s_E, s_a, s_w;
+    __shared__ int s_best, s_emit[16], s_E, s_a, s_w, s_nout0, s_take;
     __shared__ int s_win[LA_MAX_R * LA_MAX_L];
     __shared__ int s_len[LA_MAX_R];
     __shared__ int s_z[LA_MAX_L];
@@ -237,6 +269,8 @@ __global__ void k_publish(LaDev d, int verdict_given) {
         int room = h->max_out - n_out;
         int take = E < room ? E : room;
         for (int i = 0; i < take; ++i) d.out[n_out + i] = s_emit[i];
+        s_nout0 = n_out;
+        s_take = take;
         h->n_out = n_out + take;
         if (h->n_out >= h->max_out) h->done = 1;
         h->a = a; h->winner = w; h->E = E;
@@ -275,6 +309,14 @@ __global__ void k_publish(LaDev d, int verdict_given) {
                     if (s_key[k] == key) pool_upsert_warp(d, key, s_suf[k], S, G);
             }
         }
+    }
+    __syncthreads();
+    // generated-prefix insertion (§0x06A): the n-grams ending at the tokens
+    // this call appended, after the trajectory's, in increasing position
+    if ((h->opts & LA_OPT_POOL_FROM_OUTPUT) && G > 0 && tid < 32) {
+        const int P = h->prompt_len;
+        for (int k = P + s_nout0; k < P + s_nout0 + s_take; ++k)
+            if (k >= S) upsert_seq_ngram_warp(d, P, k, S, G);
     }
     __syncthreads();
     // window advance: steady §0x03C, warm-up §0x03A
@@ -381,9 +423,10 @@ __global__ void k_prefill_finish(LaDev d, int P, int sampled_token_valid) {
 // host launchers
 // ---------------------------------------------------------------------------
 void la_launch_begin(const LaDev& d, cudaStream_t st, int mode, int W, int N, int G, int sampling,
-                     float temperature, float top_p, uint64_t seed, int max_out) {
+                     float temperature, float top_p, uint64_t seed, int max_out, int opts) {
     k_begin<<<1, 128, 0, st>>>(d, mode, W, N, G, sampling, temperature, top_p,
-                               (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), max_out);
+                               (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), max_out, opts);
+    if (mode == MODE_LOOKAHEAD && opts) k_pool_seed<<<1, 1024, 0, st>>>(d);
 }
 void la_launch_pack(const LaDev& d, cudaStream_t st) { la_launch_pdl(k_pack, dim3(1), dim3(256), 0, st, d); }
 void la_launch_publish(const LaDev& d, cudaStream_t st, int verdict_given) {

@@ -141,6 +141,51 @@ def test_state_machine_with_injected_outputs(setup, W, N, G):
         assert total_a > 0
 
 
+@pytest.mark.parametrize("opts", [1, 2, 3])
+@pytest.mark.parametrize("W,N,G", [(5, 3, 5), (3, 4, 2), (2, 5, 8)])
+def test_pool_seeding_with_injected_outputs(setup, W, N, G, opts):
+    """Pool seeding (from the prompt, from the output, both): pack, verdicts,
+    pool, window and out ring bit-exact with the oracle's state machine."""
+    L, ctx, oracle, _ = setup
+    p = [1, 2, 3, 4, 5, 6, 7, 0, 1, 2, 3, 5, 6, 1, 2]
+    L.la_set_options(ctx.ctx, opts)
+    try:
+        first = L.la_prefill(ctx.ctx, p)
+        st = la.LookaheadState(p, first, W, N, G, bool(opts & 1), bool(opts & 2))
+        for step in range(40):
+            rows, guesses = st.plan()
+            outs = fake_outputs(rows)
+            em = L.la_step_inject(ctx.ctx, W, N, G, outs)
+            h, _, tok, pos, meta = L.la_debug_state(ctx.ctx)
+            check_rows(rows, tok, pos, meta)
+            info = st.publish(rows, guesses, outs)
+            assert em == info.emitted, step
+            check_state(L, ctx, st, set(range(8)) | {first})
+    finally:
+        L.la_set_options(ctx.ctx, 0)
+
+
+def test_generate_with_pool_seeding_equals_ar_and_oracle(setup):
+    """With both seeding options the output is still the AR output, and the
+    number of packed calls equals the oracle's (same candidates, same hits)."""
+    L, ctx, oracle, _ = setup
+    base = prompt(12, 5)
+    p = base + base + base
+    ar = L.la_generate_ar(ctx.ctx, p, 48)
+    assert ar == la.ar_generate(oracle, p, 48)
+    L.la_set_options(ctx.ctx, L.LA_OPT_POOL_FROM_PROMPT | L.LA_OPT_POOL_FROM_OUTPUT)
+    try:
+        for W, N, G in [(5, 3, 5), (4, 4, 3), (2, 5, 8)]:
+            st = L.la_stats()
+            got = L.la_generate(ctx.ctx, p, 48, W, N, G, stats=st)
+            assert got == ar, (W, N, G)
+            tr = []
+            la.lookahead_generate(oracle, p, 48, W, N, G, trace=tr, pool_from_prompt=True, pool_from_output=True)
+            assert st.steps == len(tr), (W, N, G)
+    finally:
+        L.la_set_options(ctx.ctx, 0)
+
+
 def test_generate_equals_ar_and_oracle(setup):
     L, ctx, oracle, _ = setup
     p = prompt(32, 1)
