@@ -706,12 +706,12 @@ int la_tc_ctas() {
     return sms;
 }
 
-// CTAs for a weight of n_tiles x k_tiles units: one per SM, except when a
-// whole number s of CTAs per tile keeps at least 80 % of the SMs busy — then
-// n_tiles * s, so every tile splits into s equal K ranges (no tile shared by
-// CTAs that also own parts of other tiles).  LA_TC_SWIGLU_UNSPLIT=1 (A/B
-// runs) gives a gate/up pair with at least half as many tiles as SMs one
-// CTA per tile instead.
+// CTAs for a weight of n_tiles x k_tiles units: one per SM.  LA_TC_ALIGN=1
+// (A/B runs) gives a weight whose tiles split into a whole number s of equal
+// K ranges with at least 80 % of the SMs busy n_tiles * s CTAs instead (O and
+// down: 128; measured 1.4 % slower per call than 152 with the packed-weight
+// stream); LA_TC_SWIGLU_UNSPLIT=1 gives a gate/up pair with at least half as
+// many tiles as SMs one CTA per tile.
 int la_tc_pick_ctas(int n_tiles, int k_tiles, int mode) {
     const int sms = la_tc_ctas();
     static int unsplit = -1;
@@ -720,7 +720,12 @@ int la_tc_pick_ctas(int n_tiles, int k_tiles, int mode) {
         unsplit = (e && e[0] == '1') ? 1 : 0;
     }
     if (unsplit && mode == GEMM_SWIGLU && n_tiles <= sms && 2 * n_tiles >= sms) return n_tiles;
-    if (n_tiles <= sms) {
+    static int align = -1;
+    if (align < 0) {
+        const char* e = getenv("LA_TC_ALIGN");
+        align = (e && e[0] == '1') ? 1 : 0;
+    }
+    if (align && n_tiles <= sms) {
         const int s = std::min(sms / n_tiles, k_tiles);
         if (s >= 2 && n_tiles * s * 5 >= sms * 4) return n_tiles * s;
     }
