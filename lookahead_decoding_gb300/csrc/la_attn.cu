@@ -16,9 +16,11 @@
 //     row's running state in block order.
 //   * positions [t0, pos] — at most 128 keys per row, from the cache
 //     (committed) or the call's temporary rows on the row's path (in-call),
-//     staged in shared memory once per tile; one softmax block per row on
-//     CUDA cores in fp32 (a lane per key for S, four dimensions per lane for
-//     P V, keys in position order); merged after the blocks, then normalised.
+//     staged in shared memory once per tile.  S on tensor cores for every
+//     (row, staged key) pair of the tile (an element of the mma depends only
+//     on its query and its key); then one softmax block per row on CUDA
+//     cores in fp32 over the row's own keys in position order (four
+//     dimensions per lane for P V); merged after the blocks, then normalised.
 // A row's arithmetic therefore depends only on its query, its position and
 // the keys it sees — the same whether it is decoded alone or packed.
 #include "la_common.cuh"
@@ -140,7 +142,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // as TMA leaves them (K then V, each two 64-dimension boxes of 128-byte rows,
 // 64 KB per block) or, after the blocks, the tail keys in padded rows.
 struct FusedLayout {
-    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, bar, path, total;
+    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, bar, ssc, ssp, path, total;
 };
 __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     FusedLayout L;
@@ -149,15 +151,17 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     if (L.ring_bytes < 2u * 4u * BLK * 128u) L.ring_bytes = 2u * 4u * BLK * 128u;
     L.q = L.ring + L.ring_bytes;                                    // [FR][LDK] bf16
     L.p = L.q + FR * LDK * 2;                                       // [FR][LDK] fp16
-    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32, then [FT][DH] fp32 queries
-    L.wmax = L.o + (FR + FT) * DH * 4;                              // [FW][FR] fp32
+    L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32
+    L.wmax = L.o + FR * DH * 4;                                     // [FW][FR] fp32
     L.wl = L.wmax + FW * FR * 4;                                    // [FW][FR] fp32
     L.rpos = L.wl + FW * FR * 4;                                    // [FR] int
     L.rt0 = L.rpos + FR * 4;                                        // [FR] int
     L.pw = L.rt0 + FR * 4;                                          // [FT][MAX_TAIL] fp32
     L.sw = L.pw + FT * MAX_TAIL * 4;                                // [FT][MAX_TAIL] int
     L.bar = L.sw + FT * MAX_TAIL * 4;                               // 2 mbarriers
-    L.path = L.bar + 16;                                            // [FR][pmax] int
+    L.ssp = (uint32_t)ring_keys + 4;                                // tail scores: [FR][ssp] fp32
+    L.ssc = L.bar + 16;
+    L.path = L.ssc + FR * L.ssp * 4;                                // [FR][pmax] int
     L.total = L.path + (uint32_t)FR * pmax * 4;
     return L;
 }
@@ -437,19 +441,32 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const __nv_bfloat16* TV = TK + (size_t)ring_keys * LDK;
     int* swr = sw + warp * MAX_TAIL;
     float* pwr = pw + warp * MAX_TAIL;
-    float* qf = os + FR * DH;                        // per-warp fp32 copy of the row's query (after O)
-    qf += warp * DH;
+    // Tail scores on tensor cores: S = Q K^T for the tile's rows against every
+    // staged tail key (the union of the rows' keys).  An output element of
+    // the mma depends only on its query row and its key, so S[r][key] is the
+    // same whichever rows share the tile; each row then reads its own keys.
+    float* ssc = reinterpret_cast<float*>(smem + LY.ssc);
+    const int SSP = (int)LY.ssp;
+    for (int nti = warp; nti * 8 < nt; nti += FT) {
+        float c4[4] = {0.f, 0.f, 0.f, 0.f};
+        const int kr = min(nti * 8 + g, nt - 1);
+        const __nv_bfloat16* krow = TK + (size_t)kr * LDK + 2 * t;
+#pragma unroll
+        for (int ks8 = 0; ks8 < 8; ++ks8) {
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16 + 8);
+            mma16816(c4, qa[ks8], b0, b1);
+        }
+        const int col = nti * 8 + 2 * t;
+        if (col < nt) { ssc[g * SSP + col] = c4[0]; ssc[(g + 8) * SSP + col] = c4[2]; }
+        if (col + 1 < nt) { ssc[g * SSP + col + 1] = c4[1]; ssc[(g + 8) * SSP + col + 1] = c4[3]; }
+    }
+    __syncthreads();
     for (int r = warp; r < nr; r += FT) {
         const int pos = rpos[r], t0 = rt0[r];
         const int n = pos - t0 + 1;                  // tail keys, positions t0 .. pos
         const int Kr = prefill ? pos + 1 : K;
-        {
-            const uint2 qv = *reinterpret_cast<const uint2*>(qs + r * LDK + lane * 4);
-            *reinterpret_cast<float4*>(qf + lane * 4) =
-                make_float4(__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xffff0000u),
-                            __uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xffff0000u));
-        }
-        // scores: lane owns keys t0 + lane + 32 i; dimensions in order
+        // scores: lane owns keys t0 + lane + 32 i
         float sc[MAX_TAIL / 32];
         int slot[MAX_TAIL / 32];
 #pragma unroll
@@ -460,27 +477,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < MAX_TAIL / 32; ++i) {
-            sc[i] = -INFINITY;
-            if (32 * i >= n) continue;                   // warp-uniform
-            const __nv_bfloat16* kr = TK + (size_t)slot[i] * LDK;
-            float acc = 0.f;
-#pragma unroll
-            for (int c = 0; c < DH / 8; ++c) {
-                const uint4 kv = *reinterpret_cast<const uint4*>(kr + c * 8);
-                const float4 qa = *reinterpret_cast<const float4*>(qf + c * 8);
-                const float4 qb = *reinterpret_cast<const float4*>(qf + c * 8 + 4);
-                acc = fmaf(qa.x, __uint_as_float(kv.x << 16), acc);
-                acc = fmaf(qa.y, __uint_as_float(kv.x & 0xffff0000u), acc);
-                acc = fmaf(qa.z, __uint_as_float(kv.y << 16), acc);
-                acc = fmaf(qa.w, __uint_as_float(kv.y & 0xffff0000u), acc);
-                acc = fmaf(qb.x, __uint_as_float(kv.z << 16), acc);
-                acc = fmaf(qb.y, __uint_as_float(kv.z & 0xffff0000u), acc);
-                acc = fmaf(qb.z, __uint_as_float(kv.w << 16), acc);
-                acc = fmaf(qb.w, __uint_as_float(kv.w & 0xffff0000u), acc);
-            }
-            if (lane + 32 * i < n) sc[i] = __fmul_rn(acc, scale);
-        }
+        for (int i = 0; i < MAX_TAIL / 32; ++i)
+            sc[i] = (lane + 32 * i < n) ? __fmul_rn(ssc[r * SSP + slot[i]], scale) : -INFINITY;
         float tm = sc[0];
 #pragma unroll
         for (int i = 1; i < MAX_TAIL / 32; ++i) tm = fmaxf(tm, sc[i]);
