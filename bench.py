@@ -66,7 +66,7 @@ def gemm_bytes_per_call(cfg, Q: float, need_rows: float) -> float:
 # x (QKV + O + gate/up + down) + LM head), from the ncu capture of the current
 # kernel's launches in a decode call summarised in profiles/; None once the
 # kernel changes.
-GEMM_TRAFFIC_PER_CALL = 13.617e9
+GEMM_TRAFFIC_PER_CALL = 13.608e9
 
 
 def aggregate_replicas(new_tokens: float, decode_s: float, wall: float, device: str = "cpu"):
