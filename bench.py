@@ -135,10 +135,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(cfg, weights, n_calls: int = 2, prompt_len: int = 24):
+def cpu_oracle_sample(cfg, weights, min_s: float = 10.0, max_calls: int = 64, prompt_len: int = 24):
     """The oracle (as it stands) on the host cores: a bounded sample of the same
-    workload — prefill of a short Markov prompt, then `n_calls` packed lookahead
-    calls at W=15, N=5, G=15; returns committed tokens/s of those calls."""
+    workload — prefill of a short Markov prompt (not timed), then packed
+    lookahead calls at W=15, N=5, G=15 until `min_s` seconds of them have run
+    (at most `max_calls`); returns committed tokens/s of those calls."""
     import numpy as np
     import synth
     from oracle import lookahead as la
@@ -150,12 +151,14 @@ def cpu_oracle_sample(cfg, weights, n_calls: int = 2, prompt_len: int = 24):
     run = la.make_runner(m, cache, "meta")
     t0 = time.perf_counter()
     toks = 0
-    for _ in range(n_calls):
+    n_calls = 0
+    while n_calls < max_calls and (n_calls == 0 or time.perf_counter() - t0 < min_s):
         rows, g = st.plan()
         out = run.run(rows)
         info = st.publish(rows, g, [argmax_lowest(x) for x in out])
         run.commit(rows, info.commit_rows)
         toks += len(info.emitted)
+        n_calls += 1
     dt = time.perf_counter() - t0
     return {"value": toks / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"oracle fp32 arithmetic, bf16 storage emulation; {n_calls} packed calls (W=15,N=5,G=15) "
@@ -198,7 +201,7 @@ def main():
         vals = []
         for _ in range(max(1, args.warmup)):
             pass          # the oracle has no warm-up state; warm-up runs would only repeat the sample
-        samples = [cpu_oracle_sample(cfg, w, n_calls=1) for _ in range(max(1, args.steps))]
+        samples = [cpu_oracle_sample(cfg, w, min_s=8.0) for _ in range(max(1, args.steps))]
         v = statistics.mean(s["value"] for s in samples)
         line = {"impl": "reference", "metric": "committed tokens/s", "value": v, "unit": "tokens/s",
                 "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
@@ -328,7 +331,7 @@ def main():
         "gpu_launches": launches,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(cfg, w, n_calls=1)
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, w)
     ctx.close()
     if rank == 0:
         print(json.dumps(line))
