@@ -32,6 +32,12 @@ Notation follows "M7.3 – Lookahead Decoding" (§0x01A, §0x03–§0x07):
   winner's first a verification rows are copied to K_in+1..K_in+a; the next
   ordinary input is the last emitted token.
 * Window advance, ALWAYS_FWD_ONE (§0x03C): [u^(1)[1:], u^(2), ..., u^(R-1), z].
+* Optional ALWAYS_FWD_ONE=False (§0x03C alternative; §0x06 sequence axis):
+  after a steady call that accepted a > 0 tokens, every level of the advanced
+  window also drops its first a cells, the rest move left and the vacated
+  tail cells are refilled, level 0 first, each level in column order, from
+  the seed source: the prompt cycle that seeded level 0, continued (the
+  refill cell numbered c takes prompt[(W+N-3+c) mod P]).
 * Optional pool seeding (§0x03A POOL_FROM_PROMPT; §0x06A "optional
   generated-prefix insertion"; Break the Sequential Dependency §5, prompt
   lookup): the n-grams of the token sequence (prompt, then every output
@@ -274,6 +280,20 @@ def advance_window(levels, z: Sequence[int], steady: bool):
     return new + [None] * (R - len(new))
 
 
+def slice_and_refill(levels, slide: int, seed_token):
+    """The ALWAYS_FWD_ONE=False alternative of §0x03C (sequence axis of §0x06):
+    applied after the one-column steady shift, it drops the first ``slide`` cells
+    of every level (the positions the ``slide`` accepted tokens consumed), moves
+    the rest left and refills the vacated tail, level 0 first and each level in
+    column order, with successive tokens of the seed source ``seed_token()``.
+    Level sizes [W-1, W, ..., W] are kept."""
+    out = []
+    for lv in levels:
+        keep = [int(t) for t in lv[slide:]]
+        out.append(keep + [int(seed_token()) for _ in range(len(lv) - len(keep))])
+    return out
+
+
 def init_levels(prompt: Sequence[int], W: int, N: int):
     """Level 0 of W+N-3 cells seeded by cycling the prompt; deeper levels empty."""
     R = N - 1
@@ -301,10 +321,14 @@ class LookaheadState:
     """Window, pool and frontier of one request between packed calls."""
 
     def __init__(self, prompt: Sequence[int], first_token: int, W: int, N: int, G: int,
-                 pool_from_prompt: bool = False, pool_from_output: bool = False):
+                 pool_from_prompt: bool = False, pool_from_output: bool = False,
+                 slice_window: bool = False):
         self.S = check_args(W, N, G)
         self.W, self.N, self.G = W, N, G
         self.levels = init_levels(prompt, W, N)
+        self.prompt = [int(t) for t in prompt]
+        self.slice_window = slice_window
+        self.seed_next = W + N - 3     # the prompt cycle continues after level 0's seed cells
         self.pool: Dict[int, List[tuple]] = {}
         self.x_t = int(first_token)
         self.p = len(prompt)           # committed K/V length = position of x_t
@@ -316,6 +340,12 @@ class LookaheadState:
             upsert_sequence_ngrams(self.pool, self.seq, 0, P, self.S, G)
         if pool_from_output:
             upsert_sequence_ngrams(self.pool, self.seq, P, P + 1, self.S, G)
+
+    def _seed_token(self) -> int:
+        """Next token of the seed source: the prompt, cycled (§0x03A)."""
+        t = self.prompt[self.seed_next % len(self.prompt)]
+        self.seed_next += 1
+        return t
 
     @property
     def steady(self) -> bool:
@@ -363,6 +393,8 @@ class LookaheadState:
         if self.pool_from_output:
             upsert_sequence_ngrams(self.pool, self.seq, n0, len(self.seq), S, self.G)
         self.levels = advance_window(self.levels, z, steady)
+        if steady and self.slice_window and a > 0:
+            self.levels = slice_and_refill(self.levels, a, self._seed_token)
         info = StepInfo(len(rows), len(guesses), steady, a, w, list(emitted), commit)
         self.x_t = int(emitted[-1])
         self.p += 1 + a
@@ -462,12 +494,12 @@ def ar_generate(model: OracleModel, prompt: Sequence[int], max_new: int,
 def lookahead_generate(model: OracleModel, prompt: Sequence[int], max_new: int, W: int, N: int, G: int,
                        schedule: str = "meta", sampling: Optional[Sampling] = None,
                        trace: Optional[list] = None, pool_from_prompt: bool = False,
-                       pool_from_output: bool = False) -> List[int]:
+                       pool_from_output: bool = False, slice_window: bool = False) -> List[int]:
     """Lookahead decoding (§0x06 loop) on one schedule of the packed call."""
     check_args(W, N, G)
     cache, logits = model.prefill(prompt)
     out = [_first_token(logits[-1], sampling)]
-    st = LookaheadState(prompt, out[0], W, N, G, pool_from_prompt, pool_from_output)
+    st = LookaheadState(prompt, out[0], W, N, G, pool_from_prompt, pool_from_output, slice_window)
     runner = make_runner(model, cache, schedule)
     while len(out) < max_new:
         rows, guesses = st.plan()

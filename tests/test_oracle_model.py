@@ -225,3 +225,21 @@ def test_seeded_pool_lookahead_equals_ar(W, N, G):
         first_steady = next(i for i in tr if i.steady)
         offered += first_steady.C_t
     assert offered > 0
+
+
+@pytest.mark.parametrize("W,N,G", [(3, 3, 3), (5, 4, 2), (2, 5, 4), (1, 3, 1)])
+def test_sliced_window_lookahead_equals_ar(W, N, G):
+    """The ALWAYS_FWD_ONE=False schedule only changes the proposals: the
+    output stays the greedy AR output, while the calls made differ from the
+    pinned schedule's on some seed."""
+    changed = 0
+    for seed in range(12):
+        m = model_for(MICRO, seed)
+        prompt = list(synth.uniform_prompt(MICRO.vocab, 5, 100 + seed))
+        ar = la.ar_generate(m, prompt, 24)
+        tr, tr0 = [], []
+        lk = la.lookahead_generate(m, prompt, 24, W, N, G, trace=tr, slice_window=True)
+        assert lk == ar, (seed, lk, ar)
+        la.lookahead_generate(m, prompt, 24, W, N, G, trace=tr0)
+        changed += [(i.Q, i.a) for i in tr] != [(i.Q, i.a) for i in tr0]
+    assert changed > 0

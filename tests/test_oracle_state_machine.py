@@ -301,3 +301,77 @@ def test_pool_from_output_after_a_call():
 def test_unseeded_pool_starts_empty():
     st = la.LookaheadState([5, 6, 7, 5, 6, 8], 9, 2, 3, 2)
     assert st.pool == {}
+
+
+# ---- ALWAYS_FWD_ONE=False: slice by the accepted count, refill -------------
+
+def _steady_hit_state(slice_window):
+    """W=3, N=4 (S=3), prompt [1..5]: level 0 was seeded with prompt[0..3], so
+    the refill continues the cycle at prompt[4].  The pool holds one suffix
+    for x_t=9 and the outputs accept two of its tokens."""
+    st = la.LookaheadState([1, 2, 3, 4, 5], 9, 3, 4, 2, slice_window=slice_window)
+    st.levels = [[10, 11], [20, 21, 22], [30, 31, 32]]
+    st.pool = {9: [(40, 41, 42)]}
+    rows, g = st.plan()
+    assert g == [(40, 41, 42)]
+    z = [50, 51, 52]
+    out = []
+    for r in rows:
+        if r.role == la.ORDINARY:
+            out.append(40)
+        elif r.role == la.VERIFY:
+            out.append({0: 41, 1: 99}.get(r.offset, 0))
+        elif r.level == 2:
+            out.append(z[r.column])
+        else:
+            out.append(0)
+    return st, st.publish(rows, g, out)
+
+
+def test_slice_window_hand_example():
+    """a = 2: the pinned shift gives [[21,22],[30,31,32],[50,51,52]]; each level
+    then drops two cells and takes 5,1 | 2,3 | 4,5 from the prompt cycle."""
+    st, info = _steady_hit_state(True)
+    assert (info.a, info.emitted) == (2, [40, 41, 99])
+    assert st.levels == [[5, 1], [32, 2, 3], [52, 4, 5]]
+    assert st.seed_next == 10
+    assert sizes(st.levels) == [2, 3, 3]
+
+
+def test_slice_window_off_is_the_pinned_shift():
+    st, info = _steady_hit_state(False)
+    assert info.a == 2
+    assert st.levels == [[21, 22], [30, 31, 32], [50, 51, 52]]
+
+
+def test_slice_window_without_a_hit_is_the_pinned_shift():
+    """a = 0 leaves nothing to slice: both schedules advance one column."""
+    runs = []
+    for flag in (False, True):
+        st = la.LookaheadState([1, 2, 3, 4, 5], 9, 3, 4, 2, slice_window=flag)
+        st.levels = [[10, 11], [20, 21, 22], [30, 31, 32]]
+        rows, g = st.plan()
+        st.publish(rows, g, [7] * len(rows))
+        runs.append((st.levels, st.seed_next))
+    assert runs[0] == runs[1] == ([[21, 22], [30, 31, 32], [7, 7, 7]], 4)
+
+
+def test_slice_window_wider_than_a_level():
+    """W=1, N=5 (S=4), a=3: level 0 is empty; levels of one cell are refilled
+    whole, in level order, from the prompt cycle (level 0's seed took
+    prompt[0..2], so the cycle goes on with 5, 6, 7)."""
+    st = la.LookaheadState([5, 6, 7], 9, 1, 5, 1, slice_window=True)
+    st.levels = [[], [20], [30], [40]]
+    st.pool = {9: [(1, 2, 3, 4)]}
+    rows, g = st.plan()
+    out = []
+    for r in rows:
+        if r.role == la.ORDINARY:
+            out.append(1)
+        elif r.role == la.VERIFY:
+            out.append({0: 2, 1: 3, 2: 8}.get(r.offset, 0))
+        else:
+            out.append(60 + r.level)
+    info = st.publish(rows, g, out)
+    assert (info.a, info.emitted) == (3, [1, 2, 3, 8])
+    assert st.levels == [[], [5], [6], [7]]
