@@ -120,6 +120,18 @@ typedef struct {
 #define LA_OPT_POOL_FROM_PROMPT 1u
 #define LA_OPT_POOL_FROM_OUTPUT 2u
 
+/* Window schedule option (la_set_options), off by default: ALWAYS_FWD_ONE=False
+ * (M7.3 §0x03C, the alternative to the pinned one-column advance; §0x06,
+ * sequence axis).  After a steady call that accepted a > 0 candidate tokens,
+ * every level of the advanced window [u1[1:], u2, ..., z] also drops its first
+ * a cells, the rest move left, and the vacated tail cells (level 0 first, each
+ * level in column order) take the next tokens of the prompt cycle that seeded
+ * level 0: refill cell c (counted from the request start) is
+ * prompt[(W+N-3+c) mod prompt_len].  Level sizes stay [W-1, W, ..., W].
+ * Outputs are unchanged (greedy: still the AR tokens); only the proposals
+ * change. */
+#define LA_OPT_SLICE_WINDOW 4u
+
 /* Counters of the last la_generate / la_generate_ar call. */
 typedef struct {
     int64_t steps;              /* packed target calls after the prefill */
@@ -150,7 +162,7 @@ typedef struct {
 int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
             int max_W, int max_N, int max_G, void* stream, la_ctx** out);
 
-/* Pool seeding options (LA_OPT_* bits) for the requests that start after
+/* Pool seeding and window options (LA_OPT_* bits) for the requests that start after
  * this call (la_generate, or the first la_step after la_prefill).  Unknown
  * bits: LA_EINVAL.  Host-only; does not synchronise. */
 int la_set_options(la_ctx* ctx, uint32_t flags);

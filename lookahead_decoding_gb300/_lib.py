@@ -25,7 +25,7 @@ EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", 
            "la_gemm_noalloc", "la_profile_read", "la_set_options"]
 
 # pool seeding options (la_set_options)
-LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT = 1, 2
+LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT, LA_OPT_SLICE_WINDOW = 1, 2, 4
 
 
 class la_model_cfg(C.Structure):
@@ -143,7 +143,7 @@ def la_init(cfg: la_model_cfg, weights: la_weights, max_ctx: int, max_W: int, ma
 
 
 def la_set_options(ctx, flags: int) -> None:
-    """Pool seeding (LA_OPT_* bits) for requests started after this call."""
+    """Pool seeding and window schedule (LA_OPT_* bits) for requests started after this call."""
     _check(LIB.la_set_options(ctx, flags), "la_set_options", ctx)
 
 

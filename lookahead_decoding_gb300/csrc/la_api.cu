@@ -690,7 +690,7 @@ int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, 
 }
 
 int la_set_options(la_ctx* ctx, uint32_t flags) {
-    if (!ctx || (flags & ~(LA_OPT_POOL_FROM_PROMPT | LA_OPT_POOL_FROM_OUTPUT))) return LA_EINVAL;
+    if (!ctx || (flags & ~(LA_OPT_POOL_FROM_PROMPT | LA_OPT_POOL_FROM_OUTPUT | LA_OPT_SLICE_WINDOW))) return LA_EINVAL;
     ctx->opts = flags;
     return LA_OK;
 }

@@ -56,8 +56,9 @@ struct LaHdr {
     float temperature, top_p;
     uint32_t seed_lo, seed_hi;
     int32_t prefill_rows;   // rows of the current prefill chunk
-    int32_t opts;           // LA_OPT_* pool seeding of the request
-    int32_t pad[2];
+    int32_t opts;           // LA_OPT_* options of the request
+    int32_t seed_next;      // next prompt index (mod prompt_len) of the refill cycle
+    int32_t pad[1];
 };
 
 // Device pointers and sizes of one context, passed by value to kernels.

@@ -38,6 +38,7 @@ __global__ void k_begin(LaDev d, int mode, int W, int N, int G, int sampling,
         if (mode == MODE_LOOKAHEAD) {
             h->n_levels = 1;
             h->level_len[0] = W + N - 3;
+            h->seed_next = (W + N - 3) % h->prompt_len;
         } else {
             h->n_levels = 0;
         }
@@ -321,14 +322,28 @@ __global__ void k_publish(LaDev d, int verdict_given) {
     __syncthreads();
     // window advance: steady §0x03C, warm-up §0x03A
     if (steady) {
-        // new[0] = old[1][1:], new[r] = old[r+1] (1 <= r <= R-2), new[R-1] = z
-        for (int i = tid; i < W - 1; i += blockDim.x) d.window[i] = s_win[1 * d.LMAX + 1 + i];
-        for (int r = 1; r <= R - 2; ++r)
-            for (int i = tid; i < W; i += blockDim.x) d.window[r * d.LMAX + i] = s_win[(r + 1) * d.LMAX + i];
-        for (int i = tid; i < W; i += blockDim.x) d.window[(R - 1) * d.LMAX + i] = s_z[i];
+        // new[0] = old[1][1:], new[r] = old[r+1] (1 <= r <= R-2), new[R-1] = z.
+        // ALWAYS_FWD_ONE=False (LA_OPT_SLICE_WINDOW): every new level also drops
+        // its first `sl` = a cells; the vacated tail cells, level 0 first and
+        // each level in column order, take the next tokens of the prompt cycle.
+        const int sl = (h->opts & LA_OPT_SLICE_WINDOW) ? a : 0;
+        const int n0 = sl < W - 1 ? sl : W - 1;     // refills of level 0
+        const int nr = sl < W ? sl : W;             // refills of each deeper level
+        const int P = h->prompt_len, seed0 = h->seed_next;
+        for (int i = tid; i < W - 1; i += blockDim.x)
+            d.window[i] = (i < W - 1 - n0) ? s_win[1 * d.LMAX + 1 + sl + i]
+                                           : d.prompt[(seed0 + i - (W - 1 - n0)) % P];
+        for (int r = 1; r < R; ++r)
+            for (int i = tid; i < W; i += blockDim.x) {
+                const int c = n0 + (r - 1) * nr + i - (W - nr);   // refill index of this cell
+                d.window[r * d.LMAX + i] = (i < W - nr) ? (r < R - 1 ? s_win[(r + 1) * d.LMAX + sl + i] : s_z[sl + i])
+                                                        : d.prompt[(seed0 + c) % P];
+            }
+        __syncthreads();   // every thread has read seed_next (steady is block-uniform)
         if (tid == 0) {
             h->level_len[0] = W - 1;
             for (int r = 1; r < R; ++r) h->level_len[r] = W;
+            h->seed_next = (seed0 + n0 + (R - 1) * nr) % P;
         }
     } else {
         int dl = nl - 1;

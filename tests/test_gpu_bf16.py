@@ -112,11 +112,17 @@ def test_generate_equals_ar_mid(mid):
     teacher_forced_check(oracle, p, ar)
 
 
-def test_generate_with_pool_seeding_equals_ar_mid(mid):
+@pytest.mark.parametrize("opts", ["seed", "seed+slice", "slice"])
+def test_generate_with_pool_seeding_equals_ar_mid(mid, opts):
     L, ctx, oracle = mid
     p = synth.markov_zipf_prompt(MID.vocab, 96, 8).tolist()
     ar = L.la_generate_ar(ctx.ctx, p, 96)
-    L.la_set_options(ctx.ctx, L.LA_OPT_POOL_FROM_PROMPT | L.LA_OPT_POOL_FROM_OUTPUT)
+    flags = 0
+    if "seed" in opts:
+        flags |= L.LA_OPT_POOL_FROM_PROMPT | L.LA_OPT_POOL_FROM_OUTPUT
+    if "slice" in opts:
+        flags |= L.LA_OPT_SLICE_WINDOW
+    L.la_set_options(ctx.ctx, flags)
     try:
         for W, N, G in [(15, 5, 15), (4, 3, 4)]:
             got = L.la_generate(ctx.ctx, p, 96, W, N, G)

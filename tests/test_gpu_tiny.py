@@ -141,17 +141,19 @@ def test_state_machine_with_injected_outputs(setup, W, N, G):
         assert total_a > 0
 
 
-@pytest.mark.parametrize("opts", [1, 2, 3])
-@pytest.mark.parametrize("W,N,G", [(5, 3, 5), (3, 4, 2), (2, 5, 8)])
+@pytest.mark.parametrize("opts", [1, 2, 3, 4, 7])
+@pytest.mark.parametrize("W,N,G", [(5, 3, 5), (3, 4, 2), (2, 5, 8), (1, 4, 3)])
 def test_pool_seeding_with_injected_outputs(setup, W, N, G, opts):
-    """Pool seeding (from the prompt, from the output, both): pack, verdicts,
-    pool, window and out ring bit-exact with the oracle's state machine."""
+    """Pool seeding (from the prompt, from the output, both) and the sliced
+    window schedule: pack, verdicts, pool, window and out ring bit-exact with
+    the oracle's state machine."""
     L, ctx, oracle, _ = setup
     p = [1, 2, 3, 4, 5, 6, 7, 0, 1, 2, 3, 5, 6, 1, 2]
     L.la_set_options(ctx.ctx, opts)
     try:
         first = L.la_prefill(ctx.ctx, p)
-        st = la.LookaheadState(p, first, W, N, G, bool(opts & 1), bool(opts & 2))
+        st = la.LookaheadState(p, first, W, N, G, bool(opts & 1), bool(opts & 2), bool(opts & 4))
+        total_a = 0
         for step in range(40):
             rows, guesses = st.plan()
             outs = fake_outputs(rows)
@@ -160,7 +162,9 @@ def test_pool_seeding_with_injected_outputs(setup, W, N, G, opts):
             check_rows(rows, tok, pos, meta)
             info = st.publish(rows, guesses, outs)
             assert em == info.emitted, step
+            total_a += info.a
             check_state(L, ctx, st, set(range(8)) | {first})
+        assert total_a > 0
     finally:
         L.la_set_options(ctx.ctx, 0)
 
@@ -181,6 +185,25 @@ def test_generate_with_pool_seeding_equals_ar_and_oracle(setup):
             assert got == ar, (W, N, G)
             tr = []
             la.lookahead_generate(oracle, p, 48, W, N, G, trace=tr, pool_from_prompt=True, pool_from_output=True)
+            assert st.steps == len(tr), (W, N, G)
+    finally:
+        L.la_set_options(ctx.ctx, 0)
+
+
+def test_generate_with_sliced_window_equals_ar_and_oracle(setup):
+    """ALWAYS_FWD_ONE=False: still the AR output, and the same number of
+    packed calls as the oracle running that schedule."""
+    L, ctx, oracle, _ = setup
+    p = prompt(32, 1)
+    ar = L.la_generate_ar(ctx.ctx, p, 64)
+    L.la_set_options(ctx.ctx, L.LA_OPT_SLICE_WINDOW)
+    try:
+        for W, N, G in [(5, 3, 5), (4, 4, 3), (1, 3, 1), (8, 5, 8)]:
+            st = L.la_stats()
+            got = L.la_generate(ctx.ctx, p, 64, W, N, G, stats=st)
+            assert got == ar, (W, N, G)
+            tr = []
+            la.lookahead_generate(oracle, p, 64, W, N, G, trace=tr, slice_window=True)
             assert st.steps == len(tr), (W, N, G)
     finally:
         L.la_set_options(ctx.ctx, 0)
