@@ -117,17 +117,21 @@ def fake_logits(rows, V, seed=5):
     return out
 
 
+@pytest.mark.parametrize("opts", [0, 4])
 @pytest.mark.parametrize("W,N,G", [(5, 3, 5), (3, 4, 2), (6, 5, 6)])
-def test_sampling_state_machine_with_injected_logits(W, N, G):
+def test_sampling_state_machine_with_injected_logits(W, N, G, opts):
+    """Sampling verdicts, frontier and window against the oracle, with the
+    pinned window schedule (opts 0) and ALWAYS_FWD_ONE=False (opts 4)."""
     cfg = synth.TINY
     w = {k: v.to("cuda:0") for k, v in synth.llama_weights(cfg, 0).items()}
     ctx = context(cfg, w, max_ctx=512, W=8, N=5, G=8)
     Lb = L()
     try:
+        Lb.la_set_options(ctx.ctx, opts)
         T, top_p, seed = 0.9, 0.95, 4242
         p = [1, 2, 3, 4, 5, 6, 7, 0]
         first = Lb.la_prefill(ctx.ctx, p, sampling=(T, top_p, seed))
-        st = la.LookaheadState(p, first, W, N, G)
+        st = la.LookaheadState(p, first, W, N, G, slice_window=bool(opts & 4))
         samp = la.Sampling(T, top_p, seed)
         mism = 0
         total_a = 0
