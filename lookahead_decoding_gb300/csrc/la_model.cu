@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g,
 // value n of row q of the QKV output: stored, or the sum of a split tile's
 // segments rounded as the GEMM's store would round it
 template <typename T>
-__device__ __forceinline__ T qkv_at(const T* row, int q, int n, const LaSplit& sp, int nseg) {
+__device__ __forceinline__ T qkv_at(const T* row, int q, int n, const LaSplit& sp) {
+    const int nseg = sp.ws ? la_split_nseg(sp, n >> 7) : 1;
     if (nseg <= 1) return row[n];
     return from_f<T>(la_split_sum(sp, n >> 7, q >> 8, 0, (size_t)(q & 255) * 128 + (n & 127), nseg));
 }
@@ -202,12 +203,10 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     const int HD = H * dh;
     const T* row = qkv + (size_t)q * 3 * HD;
     const int nq = hh * dh, nk = HD + hh * dh, nv = 2 * HD + hh * dh;
-    const int sq = sp.ws ? la_split_nseg(sp, nq >> 7) : 1, sk = sp.ws ? la_split_nseg(sp, nk >> 7) : 1;
-    const int sv = sp.ws ? la_split_nseg(sp, nv >> 7) : 1;
-    float qa = to_f(qkv_at(row, q, nq + i, sp, sq)), qb = to_f(qkv_at(row, q, nq + i + half, sp, sq));
-    float ka = to_f(qkv_at(row, q, nk + i, sp, sk)), kb = to_f(qkv_at(row, q, nk + i + half, sp, sk));
+    float qa = to_f(qkv_at(row, q, nq + i, sp)), qb = to_f(qkv_at(row, q, nq + i + half, sp));
+    float ka = to_f(qkv_at(row, q, nk + i, sp)), kb = to_f(qkv_at(row, q, nk + i + half, sp));
     // all loads before the first store (the stores may alias them as far as the compiler knows)
-    const T va = qkv_at(row, q, nv + i, sp, sv), vb = qkv_at(row, q, nv + i + half, sp, sv);
+    const T va = qkv_at(row, q, nv + i, sp), vb = qkv_at(row, q, nv + i + half, sp);
     T* qo = qbuf + ((size_t)hh * Qcap + q) * dh;
     qo[i] = from_f<T>(qa * c - qb * s);
     qo[i + half] = from_f<T>(qb * c + qa * s);
@@ -218,6 +217,78 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
     ko[i + half] = from_f<T>(kb * c + ka * s);
     vo[i] = va;
     vo[i + half] = vb;
+}
+
+// bf16 models: the same operation with eight dimensions per thread (four
+// consecutive ones of the first half and their rotation partners), all
+// partial loads as float4 and in flight before the first store, so the grid
+// (a quarter of the threads of k_rope_kv) is resident at once.  Every output
+// element takes the same arithmetic as in k_rope_kv.
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// four consecutive values n .. n+3 (n % 4 == 0) of row q of the QKV output
+// as the GEMM's bf16 store would have rounded them
+__device__ __forceinline__ float4 qkv_at4(const __nv_bfloat16* row, int q, int n, const LaSplit& sp, int nseg) {
+    if (nseg <= 1) {
+        const uint2 u = *reinterpret_cast<const uint2*>(row + n);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    const float4 s = la_split_sum4(sp, n >> 7, q >> 8, (size_t)(q & 255) * 128 + (n & 127), nseg);
+    return make_float4(bf16_round(s.x), bf16_round(s.y), bf16_round(s.z), bf16_round(s.w));
+}
+
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    return u;
+}
+
+// grid (rows, ceil(H / heads per CTA)); blockDim = heads per CTA x dh/8
+__global__ void __launch_bounds__(256) k_rope_kv4(LaDev d, const __nv_bfloat16* qkv, const float* rcos,
+                                                  const float* rsin, __nv_bfloat16* qbuf, __nv_bfloat16* kdst,
+                                                  __nv_bfloat16* vdst, int H, int dh, int sel, int Qcap, int stride,
+                                                  LaSplit sp) {
+    const LaHdr* h = d.hdr;
+    if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
+    const int q = blockIdx.x;
+    if (q >= rows_of(h, sel)) return;
+    const int half = dh >> 1, tph = dh >> 3;
+    const int hh = blockIdx.y * (blockDim.x / tph) + threadIdx.x / tph, i = (threadIdx.x % tph) * 4;
+    const int pos = d.row_pos[q];
+    const float4 c = *reinterpret_cast<const float4*>(rcos + (size_t)pos * half + i);
+    const float4 s = *reinterpret_cast<const float4*>(rsin + (size_t)pos * half + i);
+    // segments of the six column groups' tiles (the rotation partner sits in
+    // the next tile when a head is wider than a tile)
+    const int HD = H * dh, hc = hh < H ? hh : H - 1;
+    const int nq = hc * dh, nk = HD + hc * dh, nv = 2 * HD + hc * dh;
+    auto segs = [&](int n) { return sp.ws ? la_split_nseg(sp, n >> 7) : 1; };
+    const int sqa = segs(nq + i), ska = segs(nk + i), sva = segs(nv + i);
+    const int sqb = dh > 128 ? segs(nq + i + half) : sqa, skb = dh > 128 ? segs(nk + i + half) : ska;
+    const int svb = dh > 128 ? segs(nv + i + half) : sva;
+    la_pdl_wait();
+    la_pdl_trigger();
+    if (hh >= H) return;
+    const __nv_bfloat16* row = qkv + (size_t)q * 3 * HD;
+    const float4 qa = qkv_at4(row, q, nq + i, sp, sqa), qb = qkv_at4(row, q, nq + i + half, sp, sqb);
+    const float4 ka = qkv_at4(row, q, nk + i, sp, ska), kb = qkv_at4(row, q, nk + i + half, sp, skb);
+    const float4 va = qkv_at4(row, q, nv + i, sp, sva), vb = qkv_at4(row, q, nv + i + half, sp, svb);
+    __nv_bfloat16* qo = qbuf + ((size_t)hh * Qcap + q) * dh;
+    *reinterpret_cast<uint2*>(qo + i) = pack_bf16x4(qa.x * c.x - qb.x * s.x, qa.y * c.y - qb.y * s.y,
+                                                    qa.z * c.z - qb.z * s.z, qa.w * c.w - qb.w * s.w);
+    *reinterpret_cast<uint2*>(qo + i + half) = pack_bf16x4(qb.x * c.x + qa.x * s.x, qb.y * c.y + qa.y * s.y,
+                                                           qb.z * c.z + qa.z * s.z, qb.w * c.w + qa.w * s.w);
+    const int slot = (sel == 1) ? pos : q;
+    __nv_bfloat16* ko = kdst + ((size_t)hh * stride + slot) * dh;
+    __nv_bfloat16* vo = vdst + ((size_t)hh * stride + slot) * dh;
+    *reinterpret_cast<uint2*>(ko + i) = pack_bf16x4(ka.x * c.x - kb.x * s.x, ka.y * c.y - kb.y * s.y,
+                                                    ka.z * c.z - kb.z * s.z, ka.w * c.w - kb.w * s.w);
+    *reinterpret_cast<uint2*>(ko + i + half) = pack_bf16x4(kb.x * c.x + ka.x * s.x, kb.y * c.y + ka.y * s.y,
+                                                           kb.z * c.z + ka.z * s.z, kb.w * c.w + ka.w * s.w);
+    *reinterpret_cast<uint2*>(vo + i) = pack_bf16x4(va.x, va.y, va.z, va.w);
+    *reinterpret_cast<uint2*>(vo + i + half) = pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
 }
 
 // SwiGLU of the gate/up GEMM's split tiles: act = silu(gate) * up with gate
@@ -562,6 +633,13 @@ void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, float* x, con
 void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
                        void* qbuf, void* kdst, void* vdst, int H, int dh, int sel, int Qcap, int stride, int rows_cap,
                        const LaSplit& sp) {
+    if (dtype != LA_F32 && dh % 8 == 0 && dh <= 256) {
+        const int hpc = H < 256 / (dh / 8) ? H : 256 / (dh / 8);   // heads per CTA
+        la_launch_pdl(k_rope_kv4, dim3(rows_cap, (H + hpc - 1) / hpc), dim3(hpc * (dh / 8)), 0, st, d,
+                      (const __nv_bfloat16*)qkv, rcos, rsin, (__nv_bfloat16*)qbuf, (__nv_bfloat16*)kdst,
+                      (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride, sp);
+        return;
+    }
     const int rh = (H % 4 == 0) ? 4 : 1;      // heads per CTA
     dim3 g(rows_cap, H / rh);
     if (dtype == LA_F32)
