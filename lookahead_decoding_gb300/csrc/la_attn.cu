@@ -1,5 +1,6 @@
 // Masked attention of the packed call for bf16 models: one kernel, one CTA
-// per (head, tile of 16 packed rows), 8 warps.
+// per (head, tile of 16 packed rows), 16 warps (8 for the committed blocks,
+// all 16 for the tail).
 //
 // Every row attends to one key per logical position 0..pos (M7.3 §0x04A:
 // the committed prefix, then the row's own branch path).  The positions are
@@ -7,8 +8,10 @@
 // row's position alone (TB is fixed per context so that pos - t0 covers
 // every in-call offset):
 //   * committed keys [0, t0) — 128-position blocks of the cache stream
-//     through a double-buffered shared-memory ring (cp.async, [key][dim]
-//     bf16).  For each block the 8 warps split the keys for S = Q K^T
+//     through a double-buffered shared-memory ring (TMA from one tensor map
+//     over the whole cache: four 64-dimension boxes of 128-byte rows per
+//     block, 128-byte swizzle, an mbarrier per buffer).  For each block the
+//     8 block warps split the keys for S = Q K^T
 //     (mma.sync m16n8k16 bf16 -> fp32), form the per-row block maximum m,
 //     P = exp(S - m) rounded to fp16 and its row sum l, then split the
 //     dimensions for O = P V (fp16 mma; V fragments by ldmatrix.trans,

@@ -4,21 +4,27 @@
 // The call is a skinny contraction: Q packed rows against a weight matrix
 // that streams from HBM once per call, so the kernel is built to keep every
 // SM streaming weights:
-//   - persistent stream-K: one CTA per SM; the (128-row weight tile, 64-wide
-//     K slice) units of the whole matrix are split into equal contiguous
-//     ranges, one per CTA, so every SM moves the same number of bytes;
-//   - warp 0 streams units through a multi-stage TMA + mbarrier ring
-//     (128 x 64 bf16 weight tiles and q x 64 activation tiles, 128-byte
-//     swizzle); warp 1 issues tcgen05.mma (kind::f16, bf16 in, fp32 in TMEM,
-//     M = 128 weight rows, N = q rounded up to 16); warps 2-5 drain the
+//   - persistent stream-K: one CTA per SM; the (128-row weight tile, K slice
+//     of two 64-column atoms, one for gate/up) units of the whole matrix are
+//     split into equal contiguous ranges, one per CTA, so every SM moves the
+//     same number of bytes;
+//   - warp 0 streams units through a multi-stage mbarrier ring: the weights,
+//     repacked once at init into unit-contiguous 128-byte-swizzled images,
+//     by one bulk copy per unit (L2 evict-first), the q x 64 activation tiles
+//     by TMA (128-byte swizzle); weight stages sit at fixed offsets,
+//     activation stages are counted back from the ring's end and sized by
+//     the call's rows; warp 1 issues tcgen05.mma (kind::f16, bf16 in, fp32 in
+//     TMEM, M = 128 weight rows, N = q rounded up to 16); warps 2-5 drain the
 //     accumulator with tcgen05.ld;
 //   - two TMEM accumulators alternate between the K segments a CTA owns, so
 //     the MMA warp starts the next tile while the epilogue drains the last;
 //   - a tile whose K range spans several CTAs: each contributor publishes its
-//     fp32 partial (L2) and goes on streaming; after its last unit it waits
-//     (bounded) for the tile's other partials and finishes its own slice of
-//     the tile's packed rows, adding the partials in segment (K) order, so
-//     the reduction is spread over the contributors instead of one CTA;
+//     fp32 partial (L2) and goes on streaming.  The layer projections leave
+//     the partials to the kernel that reads their output (`defer`: RoPE,
+//     RMSNorm and SwiGLU add the segments in K order); otherwise (the LM
+//     head) a contributor waits (bounded) after its last unit for the tile's
+//     other partials and finishes its own slice of the tile's packed rows,
+//     adding the partials in segment (K) order;
 //   - all row chunks of a call (BN_MAX packed rows each) run inside the same
 //     grid of at most one CTA per SM, so the contributors of a tile are
 //     resident together.
@@ -46,8 +52,8 @@ constexpr int BOX_ROWS = 16;
 constexpr int MAX_STAGES = 12;
 constexpr int SMEM_BYTES = 220 * 1024;
 constexpr int NTHREADS = 192;             // producer, MMA, 4 epilogue warps
-constexpr int MAX_CHUNKS = 4;
-constexpr uint32_t TMEM_COLS = 512;       // two accumulators of up to 256 fp32 columns             // packed rows per launch <= MAX_CHUNKS * BN_MAX
+constexpr int MAX_CHUNKS = 4;             // packed rows per launch <= MAX_CHUNKS * BN_MAX
+constexpr uint32_t TMEM_COLS = 512;       // two accumulators of up to 256 fp32 columns
 
 struct TcParams {
     LaHdr* hdr;
