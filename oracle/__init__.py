@@ -18,6 +18,8 @@ Contents (each function cites the passage of the pages it restates):
   generate loops (autoregressive and lookahead, in three schedules).
 * ``sampling``  — temperature/top-p warping and the exact multi-draft
   verifier with disjoint one-hot proposals.
+* ``batch``     — several requests in one packed forward (each request's
+  rows against its own cache and rows only), and the batched generate loop.
 * ``philox``    — Philox4x32-10 counter-based generator.
 * ``jacobi``    — Jacobi and Gauss–Seidel sweeps over a triangular system.
 

@@ -15,9 +15,10 @@ Attention: softmax(q.k / sqrt(d_h)) over the keys a row may see.
 
 The visibility of the new rows is an explicit boolean relation (prefix keys
 are always visible), so the same forward serves the autoregressive step,
-the packed lookahead call with a dense mask (M7.3 §0x07A "Dense packed
-mask"), the packed call with a metadata predicate and the separate-forwards
-schedule (§0x07A "Separate forwards").
+the packed lookahead call with a dense mask (M7.3 §0x07A, dense packed
+mask), the packed call with a metadata predicate, the separate-forwards
+schedule (§0x07A, separate forwards) and, through ``forward_many``, several
+requests in one call (each request's rows against its own cache and rows).
 
 Arithmetic is float64 unless ``compute_dtype`` says otherwise.  With
 ``store="bf16"`` values are rounded to bf16 (round-to-nearest-even through
@@ -144,17 +145,35 @@ class OracleModel:
         new row i may see new row j (every row sees all committed rows).
         Returns (logits [Q, V], new_k [L][Q,H,dh], new_v [L][Q,H,dh]).
         """
+        return self.forward_many([(tokens, positions, cache, allowed_new)])[0]
+
+    def forward_many(self, calls):
+        """One forward over the rows of several independent requests.
+
+        ``calls`` is a list of (tokens, positions, cache, allowed_new), one per
+        request, each as in ``forward``.  The row-wise work (embedding, norms,
+        projections, SwiGLU, head) runs on the requests' rows stacked in call
+        order; attention runs per request, its rows against its own committed
+        cache and its own new rows only (no row sees another request).  With
+        one call this is exactly ``forward``.  Returns a list of
+        (logits, new_k, new_v) in call order.
+        """
         cfg = self.cfg
         H, dh = cfg.n_heads, cfg.head_dim
-        tokens = np.asarray(tokens, dtype=np.int64)
-        positions = np.asarray(positions, dtype=np.int64)
+        toks = [np.asarray(c[0], dtype=np.int64) for c in calls]
+        offs = np.cumsum([0] + [len(t) for t in toks])
+        tokens = np.concatenate(toks)
+        positions = np.concatenate([np.asarray(c[1], dtype=np.int64) for c in calls])
         Q = len(tokens)
-        K_in = len(cache)
-        allowed = np.concatenate([np.ones((Q, K_in), dtype=bool),
-                                  np.asarray(allowed_new, dtype=bool)], axis=1)
+        allowed = []
+        for (_, _, cache, allowed_new), b in zip(calls, range(len(calls))):
+            Qb = int(offs[b + 1] - offs[b])
+            allowed.append(np.concatenate([np.ones((Qb, len(cache)), dtype=bool),
+                                           np.asarray(allowed_new, dtype=bool)], axis=1))
         emb = self.w("tok_emb")
         x = emb[tokens].astype(self.dt)
-        new_k, new_v = [], []
+        new_k = [[] for _ in calls]
+        new_v = [[] for _ in calls]
         scale = 1.0 / math.sqrt(dh)
         for l in range(cfg.n_layers):
             xn = self._st(rmsnorm(x, self.w(f"l{l}.attn_norm"), cfg.rms_eps))
@@ -163,15 +182,18 @@ class OracleModel:
             v = self._st(xn @ self.w(f"l{l}.wv").T).reshape(Q, H, dh)
             q = self._st(rope(q, positions, cfg.rope_theta))
             k = self._st(rope(k, positions, cfg.rope_theta))
-            new_k.append(k)
-            new_v.append(v)
-            K = k if K_in == 0 else np.concatenate([cache.k[l], k], axis=0)
-            V = v if K_in == 0 else np.concatenate([cache.v[l], v], axis=0)
             o = np.empty((Q, H, dh), dtype=self.dt)
-            for h in range(H):
-                s = (q[:, h, :] @ K[:, h, :].T) * scale                 # [Q, K_in+Q]
-                s = np.where(allowed, s, -np.inf)
-                o[:, h, :] = softmax_rows(s) @ V[:, h, :]
+            for b, (_, _, cache, _) in enumerate(calls):
+                rows = slice(int(offs[b]), int(offs[b + 1]))
+                kb, vb = k[rows], v[rows]
+                new_k[b].append(kb)
+                new_v[b].append(vb)
+                K = kb if len(cache) == 0 else np.concatenate([cache.k[l], kb], axis=0)
+                V = vb if len(cache) == 0 else np.concatenate([cache.v[l], vb], axis=0)
+                for h in range(H):
+                    s = (q[rows, h, :] @ K[:, h, :].T) * scale             # [Q_b, K_b+Q_b]
+                    s = np.where(allowed[b], s, -np.inf)
+                    o[rows, h, :] = softmax_rows(s) @ V[:, h, :]
             o = self._st(o.reshape(Q, H * dh))
             x = x + o @ self.w(f"l{l}.wo").T
             hn = self._st(rmsnorm(x, self.w(f"l{l}.mlp_norm"), cfg.rms_eps))
@@ -179,7 +201,7 @@ class OracleModel:
             x = x + a @ self.w(f"l{l}.w_down").T
         xf = self._st(rmsnorm(x, self.w("final_norm"), cfg.rms_eps))
         logits = xf @ self.w("lm_head").T
-        return logits, new_k, new_v
+        return [(logits[int(offs[b]):int(offs[b + 1])], new_k[b], new_v[b]) for b in range(len(calls))]
 
     def causal(self, tokens, start_pos: int, cache: KVCache):
         """Plain causal forward of a token run at positions start_pos.."""
