@@ -365,11 +365,13 @@ cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V,
 
 cudaError_t la_launch_sample_verify(const LaDev& d, cudaStream_t st, const float* logits, int V, int prefill) {
     const size_t smem = sizeof(float) * (size_t)V;
-    static bool attr_done = false;
-    if (!attr_done) {
+    // the kernel's shared-memory allowance only grows: a context with a
+    // larger vocabulary than the ones before raises it
+    static size_t allowed = 0;
+    if (smem > allowed) {
         cudaError_t e = cudaFuncSetAttribute(k_sample_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        allowed = smem;
     }
     return la_launch_pdl(k_sample_verify, dim3(1), dim3(NT), smem, st, d, logits, V, prefill);
 }

@@ -173,3 +173,30 @@ def test_generate_sampling_runs_and_is_seeded():
         assert len(ar) == 48
     finally:
         ctx.close()
+
+
+def test_sampling_on_a_large_vocabulary_after_a_small_one():
+    """The sampling verifier holds one fp32 row of the vocabulary in shared
+    memory: after the 512-token model, a 32000-token one (128 KB) still
+    samples, in range and reproducibly per seed."""
+    Lb = L()
+    small = synth.TINY
+    ws = {k: v.to("cuda:0") for k, v in synth.llama_weights(small, 0).items()}
+    c0 = context(small, ws, max_ctx=128, W=4, N=3, G=4)
+    try:
+        p = synth.uniform_prompt(small.vocab, 8, 3).tolist()
+        assert len(Lb.la_generate(c0.ctx, p, 8, 4, 3, 4, sampling=(0.8, 0.9, 7))) == 8
+    finally:
+        c0.close()
+    big = synth.ModelConfig(n_layers=1, d_model=512, n_heads=4, head_dim=128, d_ffn=1408, vocab=32000, dtype="bf16")
+    wb = {k: v.to("cuda:0") for k, v in synth.llama_weights(big, 1).items()}
+    c1 = context(big, wb, max_ctx=128, W=4, N=3, G=4)
+    try:
+        p = synth.uniform_prompt(big.vocab, 8, 4).tolist()
+        a = Lb.la_generate(c1.ctx, p, 24, 4, 3, 4, sampling=(0.8, 0.9, 11))
+        b = Lb.la_generate(c1.ctx, p, 24, 4, 3, 4, sampling=(0.8, 0.9, 11))
+        c = Lb.la_generate(c1.ctx, p, 24, 4, 3, 4, sampling=(0.8, 0.9, 12))
+        assert a == b and a != c and len(a) == 24
+        assert all(0 <= t < big.vocab for t in a)
+    finally:
+        c1.close()
