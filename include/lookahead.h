@@ -200,6 +200,39 @@ int la_generate(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
 int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
                    const la_sampling* s, int32_t* out, int* n_out, la_stats* stats);
 
+/* ---- several requests in one packed call ---------------------------------- */
+
+/* As la_init, for contexts that also run batched calls of up to max_batch
+ * requests (bf16 models; max_batch x the largest call's rows rounded up to
+ * 16 must not exceed 1024).  Requests 1 .. max_batch-1 get their own
+ * header, window, pool, prompt, out ring and K/V cache (max_batch x the
+ * single-request cache).  la_init(...) is la_init_batch(..., 1, ...).
+ * Errors: those of la_init; LA_ENOTSUP for max_batch > 1 with fp32 weights
+ * or too many rows. */
+int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
+                  int max_W, int max_N, int max_G, int max_batch, void* stream,
+                  la_ctx** out);
+
+/* Greedy lookahead decoding of B prompts together (M7.3 runs one request
+ * per call in its pinned code, §0x04C, and calls that a property of the
+ * code; the state is per request, §0x03B, §0x07).  prompts (host) holds the
+ * B prompts back to back, lengths[b] (host) their lengths.  Each packed call
+ * stacks every live request's rows (request b at rows b*Qs .. , Qs the
+ * largest call's rows rounded up to 16; unused rows of a slice repeat the
+ * request's ordinary row), runs one forward and LM head over them (one
+ * weight stream for all requests), then verifies, publishes and advances
+ * each request on its own; a request with max_new tokens leaves the batch.
+ * Every request's rows see only its own cache and rows, so each output is
+ * that request's la_generate (and AR) output.  out (host, B x max_new) gets
+ * request b's tokens at out[b*max_new ..].  stats: steps = calls of the
+ * request that needed most, tokens = B*max_new.
+ * Errors: LA_EINVAL, LA_ECAPACITY (B > max_batch, a prompt + max_new >
+ * max_ctx, knobs above the context's), LA_ENOTSUP (a context from la_init),
+ * LA_ECUDA, device errors.  Resets request 0's single-request state: a
+ * later la_step needs la_prefill first. */
+int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t* lengths,
+                      int max_new, int W, int N, int G, int32_t* out, la_stats* stats);
+
 /* ---- inspection (tests) -------------------------------------------------- */
 
 /* flags bit 0: keep fp32 logits of the rows whose outputs the verifier reads

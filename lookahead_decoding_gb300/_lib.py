@@ -22,7 +22,7 @@ LA_F32, LA_BF16 = 0, 1
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
            "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
-           "la_gemm_noalloc", "la_profile_read", "la_set_options"]
+           "la_gemm_noalloc", "la_profile_read", "la_set_options", "la_init_batch", "la_generate_batch"]
 
 # pool seeding options (la_set_options)
 LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT, LA_OPT_SLICE_WINDOW = 1, 2, 4
@@ -68,6 +68,10 @@ def _load() -> C.CDLL:
     sig = {
         "la_init": (C.c_int, [C.POINTER(la_model_cfg), C.POINTER(la_weights), C.c_int, C.c_int, C.c_int, C.c_int, vp,
                               C.POINTER(vp)]),
+        "la_init_batch": (C.c_int, [C.POINTER(la_model_cfg), C.POINTER(la_weights), C.c_int, C.c_int, C.c_int,
+                                    C.c_int, C.c_int, vp, C.POINTER(vp)]),
+        "la_generate_batch": (C.c_int, [vp, C.c_int, i32p, i32p, C.c_int, C.c_int, C.c_int, C.c_int, i32p,
+                                        C.POINTER(la_stats)]),
         "la_prefill": (C.c_int, [vp, i32p, C.c_int, C.POINTER(la_sampling), i32p]),
         "la_step": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), i32p, C.POINTER(C.c_int)]),
         "la_generate": (C.c_int, [vp, i32p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), i32p,
@@ -134,12 +138,30 @@ def _sampling(s) -> Optional[la_sampling]:
 # ---------------------------------------------------------------------------
 
 def la_init(cfg: la_model_cfg, weights: la_weights, max_ctx: int, max_W: int, max_N: int, max_G: int,
-            stream: int = 0):
+            stream: int = 0, max_batch: int = 1):
     ctx = C.c_void_p()
-    code = LIB.la_init(C.byref(cfg), C.byref(weights), max_ctx, max_W, max_N, max_G, C.c_void_p(stream or None),
-                       C.byref(ctx))
+    if max_batch == 1:
+        code = LIB.la_init(C.byref(cfg), C.byref(weights), max_ctx, max_W, max_N, max_G, C.c_void_p(stream or None),
+                           C.byref(ctx))
+    else:
+        code = LIB.la_init_batch(C.byref(cfg), C.byref(weights), max_ctx, max_W, max_N, max_G, max_batch,
+                                 C.c_void_p(stream or None), C.byref(ctx))
     _check(code, "la_init")
     return ctx
+
+
+def la_generate_batch(ctx, prompts: Sequence[Sequence[int]], max_new: int, W: int, N: int, G: int,
+                      stats: Optional[la_stats] = None) -> List[List[int]]:
+    """Greedy lookahead of several prompts in batched packed calls."""
+    B = len(prompts)
+    flat = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in prompts]))
+    lengths = np.ascontiguousarray(np.asarray([len(p) for p in prompts], dtype=np.int32))
+    out = np.zeros(B * max_new, dtype=np.int32)
+    i32 = C.POINTER(C.c_int32)
+    _check(LIB.la_generate_batch(ctx, B, flat.ctypes.data_as(i32), lengths.ctypes.data_as(i32), max_new, W, N, G,
+                                 out.ctypes.data_as(i32), C.byref(stats) if stats is not None else None),
+           "la_generate_batch", ctx)
+    return [out[b * max_new:(b + 1) * max_new].tolist() for b in range(B)]
 
 
 def la_set_options(ctx, flags: int) -> None:
@@ -336,7 +358,7 @@ class Context:
     CUDA tensors in the model dtype (kept referenced for the context's life)."""
 
     def __init__(self, cfg, weights: Dict[str, "object"], max_ctx: int, max_W: int, max_N: int, max_G: int,
-                 stream: int = 0):
+                 stream: int = 0, max_batch: int = 1):
         dt = LA_F32 if cfg.dtype == "f32" else LA_BF16
         self.cfg = la_model_cfg(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.d_ffn,
                                 cfg.vocab, cfg.rms_eps, cfg.rope_theta, dt)
@@ -352,7 +374,7 @@ class Context:
         self.w = la_weights(weights["tok_emb"].data_ptr(), weights["lm_head"].data_ptr(),
                             weights["final_norm"].data_ptr(), ptrs("attn_norm"), ptrs("wq"), ptrs("wk"), ptrs("wv"),
                             ptrs("wo"), ptrs("mlp_norm"), ptrs("w_gate"), ptrs("w_up"), ptrs("w_down"))
-        self.ctx = la_init(self.cfg, self.w, max_ctx, max_W, max_N, max_G, stream)
+        self.ctx = la_init(self.cfg, self.w, max_ctx, max_W, max_N, max_G, stream, max_batch)
         self.vocab = cfg.vocab
 
     def close(self):

@@ -67,6 +67,16 @@ struct la_ctx {
     std::vector<TcGemm> g_qkv, g_o, g_gu, g_down;
     TcGemm g_head{};
 
+    // batched calls: up to max_batch requests stacked in slices of Qstride
+    // rows; request b's state and cache are its own (request 0's are the
+    // single-request ones above), `bd` carries the batch header
+    int max_batch = 1, Qstride = 0, temp_rows = 0;
+    std::vector<LaDev> req;            // per request, row arrays at its slice
+    std::vector<LaDev> req_pf;         // per request, row arrays at row 0 (prefill)
+    LaDev bd{};
+    const LaHdr** req_hdr = nullptr;   // device array of the requests' headers
+    size_t cache_bytes_req = 0;
+
     // request state on the host side
     bool prefilled = false, begun = false;
     int W = 0, N = 0, G = 0, mode = 0, sampling = 0;
@@ -187,11 +197,38 @@ static LaSplit split_of(const la_ctx* ctx, const TcGemm* g) {
     return la_tc_split(*g, ctx->work);
 }
 
-static int enqueue_forward(la_ctx* ctx, int sel) {
+// What a pass runs on: the device view whose header gives the row counts,
+// the K/V cache it reads (and a prefill writes), the temporary rows of a
+// call, and for a batched call the requests' headers and slice size.
+struct Lane {
+    const LaDev* d;
+    char* cache;                    // K/V cache [L][2][H][max_ctx][dh] of the lane's (first) request
+    int cache_row0;                 // that cache's first row in the cache tensor map
+    int temp_rows;                  // temporary K/V rows per (layer, k/v, head) plane
+    int rows_call;                  // rows of a call (all stacked slices in a batch)
+    const LaHdr* const* req_hdr;    // batched call: the requests' headers
+    int qstride;                    // batched call: rows per request slice (0: one request)
+};
+
+static Lane solo_lane(la_ctx* ctx) {
+    return Lane{&ctx->d, (char*)ctx->cache, 0, ctx->Qmax, ctx->Qmax, nullptr, 0};
+}
+// request b of a batched context, for its prefill (rows from row 0)
+static Lane prefill_lane(la_ctx* ctx, int b) {
     const la_model_cfg& c = ctx->cfg;
-    const LaDev& d = ctx->d;
+    return Lane{&ctx->req_pf[b], (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
+                b * c.n_layers * 2 * c.n_heads * ctx->max_ctx, ctx->Qmax, ctx->Qmax, nullptr, 0};
+}
+// a batched call of B requests
+static Lane batch_lane(la_ctx* ctx, int B) {
+    return Lane{&ctx->bd, (char*)ctx->cache, 0, ctx->temp_rows, B * ctx->Qstride, ctx->req_hdr, ctx->Qstride};
+}
+
+static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
+    const la_model_cfg& c = ctx->cfg;
+    const LaDev& d = *ln.d;
     cudaStream_t st = ctx->st;
-    const int rc = (sel == SEL_PREFILL) ? PREFILL_CHUNK : ctx->Qmax;
+    const int rc = (sel == SEL_PREFILL) ? PREFILL_CHUNK : ln.rows_call;
     const int dm = c.d_model, HD = ctx->HD, F = c.d_ffn, H = c.n_heads, dh = c.head_dim;
     int pi = prof_open(ctx, PK_ROW);
     la_launch_embed(d, st, c.dtype, ctx->emb, ctx->x, dm, sel, rc);
@@ -213,29 +250,32 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_STORE, ctx->xn, dm, ctx->wv[l], nullptr, dm, HD,
                                 q + 2 * HD * ctx->esz, 3 * HD, sel, rc);
         }
-        void* kdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx)
-                                          : layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax);
-        void* vdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx)
-                                          : layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax);
-        int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ctx->Qmax;
+        void* kdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx)
+                                          : layer_plane(ctx, ctx->temp, l, 0, ln.temp_rows);
+        void* vdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx)
+                                          : layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows);
+        int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ln.temp_rows;
         pi = prof_open(ctx, PK_ROW);
         la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
                           stride, rc, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr));
         prof_close(ctx, pi);
         pi = prof_open(ctx, PK_ATTN);
         if (ctx->bf16) {
-            CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
-                                        layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
-                                        layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax),
-                                        layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, H, sel,
-                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX, ctx->cache_map,
-                                        (l * 2 + 0) * H * ctx->max_ctx, (l * 2 + 1) * H * ctx->max_ctx));
+            CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
+                                        layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
+                                        layer_plane(ctx, ctx->temp, l, 0, ln.temp_rows),
+                                        layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows), ctx->attn, H, sel,
+                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX,
+                                        ctx->cache_map, ln.cache_row0 + (l * 2 + 0) * H * ctx->max_ctx,
+                                        ln.cache_row0 + (l * 2 + 1) * H * ctx->max_ctx, ln.req_hdr, ln.qstride,
+                                        (long long)(ctx->cache_bytes_req / ctx->esz),
+                                        c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows));
         } else {
-            CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ctx->cache, l, 0, ctx->max_ctx),
-                                   layer_plane(ctx, ctx->cache, l, 1, ctx->max_ctx),
-                                   layer_plane(ctx, ctx->temp, l, 0, ctx->Qmax),
-                                   layer_plane(ctx, ctx->temp, l, 1, ctx->Qmax), ctx->attn, H, sel, ctx->Qcap,
-                                   ctx->max_ctx, ctx->Qmax, rc));
+            CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
+                                   layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
+                                   layer_plane(ctx, ctx->temp, l, 0, ln.temp_rows),
+                                   layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows), ctx->attn, H, sel, ctx->Qcap,
+                                   ctx->max_ctx, ln.temp_rows, rc));
         }
         prof_close(ctx, pi);
         if (ctx->tc) {
@@ -271,11 +311,11 @@ static int enqueue_forward(la_ctx* ctx, int sel) {
 }
 
 // final norm on the needed rows, LM head, argmax (and fp32 logits when kept)
-static int enqueue_head(la_ctx* ctx, int keep_logits) {
+static int enqueue_head(la_ctx* ctx, int keep_logits, const Lane& ln) {
     const la_model_cfg& c = ctx->cfg;
-    const LaDev& d = ctx->d;
+    const LaDev& d = *ln.d;
     cudaStream_t st = ctx->st;
-    const int rc = ctx->Qmax;
+    const int rc = ln.rows_call;
     int pi = prof_open(ctx, PK_ROW);
     la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->fnorm, ctx->hn, c.d_model, c.rms_eps, SEL_NEED, 1, rc,
                       split_of(ctx, ctx->tc ? &ctx->g_down[c.n_layers - 1] : nullptr));
@@ -299,24 +339,32 @@ static int enqueue_head(la_ctx* ctx, int keep_logits) {
     return LA_OK;
 }
 
-static int enqueue_publish_commit(la_ctx* ctx, int verdict_given) {
+// publication and K/V commit of one request: `cache` is its cache, `temp`
+// the first of its temporary rows in each plane of temp_rows rows
+static int enqueue_publish_commit_req(la_ctx* ctx, const LaDev& d, int verdict_given, void* cache, char* temp,
+                                      int temp_rows) {
     const la_model_cfg& c = ctx->cfg;
     const int pi = prof_open(ctx, PK_STATE);
-    la_launch_publish(ctx->d, ctx->st, verdict_given);
-    la_launch_commit(ctx->d, ctx->st, ctx->cache, ctx->temp, c.n_layers * 2 * c.n_heads, c.n_heads,
-                     (int)(c.head_dim * ctx->esz), ctx->max_ctx, ctx->Qmax);
+    la_launch_publish(d, ctx->st, verdict_given);
+    la_launch_commit(d, ctx->st, cache, temp, c.n_layers * 2 * c.n_heads, c.n_heads, (int)(c.head_dim * ctx->esz),
+                     ctx->max_ctx, temp_rows);
     prof_close(ctx, pi);
     CK(cudaGetLastError());
     return LA_OK;
+}
+
+static int enqueue_publish_commit(la_ctx* ctx, int verdict_given) {
+    return enqueue_publish_commit_req(ctx, ctx->d, verdict_given, ctx->cache, (char*)ctx->temp, ctx->Qmax);
 }
 
 static int enqueue_step(la_ctx* ctx) {
     int pi = prof_open(ctx, PK_STATE);
     la_launch_pack(ctx->d, ctx->st);
     prof_close(ctx, pi);
-    int r = enqueue_forward(ctx, SEL_CALL);
+    const Lane ln = solo_lane(ctx);
+    int r = enqueue_forward(ctx, SEL_CALL, ln);
     if (r) return r;
-    r = enqueue_head(ctx, (ctx->debug & 1) | ctx->sampling);
+    r = enqueue_head(ctx, (ctx->debug & 1) | ctx->sampling, ln);
     if (r) return r;
     if (ctx->sampling) {
         pi = prof_open(ctx, PK_STATE);
@@ -401,7 +449,13 @@ void la_free(la_ctx* ctx) {
 
 int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W, int max_N, int max_G, void* stream,
             la_ctx** out) {
+    return la_init_batch(cfg, w, max_ctx, max_W, max_N, max_G, 1, stream, out);
+}
+
+int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W, int max_N, int max_G,
+                  int max_batch, void* stream, la_ctx** out) {
     if (!cfg || !w || !out) return LA_EINVAL;
+    if (max_batch < 1) return LA_EINVAL;
     *out = nullptr;
     const la_model_cfg& c = *cfg;
     if (c.n_layers < 1 || c.n_heads < 1 || c.vocab < 2 || c.d_model != c.n_heads * c.head_dim ||
@@ -443,7 +497,11 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
     int steadyQ = (max_W + max_G) * (max_N - 1);
     int warmQ = 1 + (max_N - 1) * (max_W + max_N - 3);
     ctx->Qmax = std::max(steadyQ, warmQ) + 16;
-    ctx->Qcap = ((std::max(ctx->Qmax, PREFILL_CHUNK) + 255) / 256) * 256;
+    ctx->max_batch = max_batch;
+    ctx->Qstride = (ctx->Qmax + 15) / 16 * 16;
+    if (max_batch > 1 && (c.dtype != LA_BF16 || max_batch * ctx->Qstride > 1024)) { delete ctx; return LA_ENOTSUP; }
+    ctx->temp_rows = max_batch > 1 ? max_batch * ctx->Qstride : ctx->Qmax;
+    ctx->Qcap = ((std::max(std::max(ctx->Qmax, PREFILL_CHUNK), max_batch > 1 ? ctx->temp_rows : 0) + 255) / 256) * 256;
     ctx->rope_len = max_ctx + ctx->PMAX + 1;
     ctx->out_cap = max_ctx + 32;
 
@@ -504,19 +562,66 @@ int la_init(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int max_W
     A(&ctx->attn, es * Qc * HD);
     A(&ctx->act, es * Qc * F);
     A(&ctx->hn, es * Qc * dm);
-    A(&ctx->cache, es * (size_t)c.n_layers * 2 * HD * max_ctx);
-    A(&ctx->temp, es * (size_t)c.n_layers * 2 * HD * ctx->Qmax);
+    ctx->cache_bytes_req = es * (size_t)c.n_layers * 2 * HD * max_ctx;
+    A(&ctx->cache, ctx->cache_bytes_req * max_batch);
+    A(&ctx->temp, es * (size_t)c.n_layers * 2 * HD * ctx->temp_rows);
     A((void**)&ctx->rcos, sizeof(float) * (size_t)ctx->rope_len * (c.head_dim / 2));
     A((void**)&ctx->rsin, sizeof(float) * (size_t)ctx->rope_len * (c.head_dim / 2));
     A((void**)&ctx->logits, sizeof(float) * Qc * V);
     A((void**)&ctx->logits_in, sizeof(float) * (size_t)ctx->Qmax * V);
     if (ctx->bf16) {
         ctx->attn_TB = la_attn_tail_blocks(ctx->PMAX);
-        if (!r && la_tc_make_map(&ctx->cache_map, ctx->cache, c.n_layers * 2 * c.n_heads * max_ctx, c.head_dim, 128))
+        if (!r && la_tc_make_map(&ctx->cache_map, ctx->cache, max_batch * c.n_layers * 2 * c.n_heads * max_ctx,
+                                 c.head_dim, 128))
             r = LA_ECUDA;
         if (la_attn_smem_bytes(ctx->attn_TB, ctx->Qmax, ctx->PMAX) > 227 * 1024) r = LA_ENOTSUP;
     }
+    // batched calls: request 0 keeps the state above; requests 1.. get their
+    // own header, window, pool, prompt, out ring and commit plan
+    ctx->req_pf.assign(max_batch, d);
+    for (int b = 1; b < max_batch && !r; ++b) {
+        LaDev& e = ctx->req_pf[b];
+        A((void**)&e.hdr, sizeof(LaHdr));
+        A((void**)&e.window, sizeof(int32_t) * ctx->Rmax * ctx->LMAX);
+        A((void**)&e.pool_tok, sizeof(int32_t) * V * ctx->Gmax * ctx->Smax);
+        A((void**)&e.pool_cnt, sizeof(int32_t) * V);
+        A((void**)&e.prompt, sizeof(int32_t) * max_ctx);
+        A((void**)&e.out, sizeof(int32_t) * ctx->out_cap);
+        A((void**)&e.commit_rows, sizeof(int32_t) * 16);
+    }
+    LaHdr* batch_hdr = nullptr;
+    if (max_batch > 1) {
+        A((void**)&batch_hdr, sizeof(LaHdr));
+        A((void**)&ctx->req_hdr, sizeof(LaHdr*) * max_batch);
+    }
     if (r) { la_free(ctx); return r; }
+    if (max_batch > 1) {
+        // the batch's view: shared rows and activations, the batch header
+        ctx->bd = d;
+        ctx->bd.hdr = batch_hdr;
+        // the requests' views: their own state, their slice of the rows
+        ctx->req = ctx->req_pf;
+        std::vector<const LaHdr*> hs(max_batch);
+        for (int b = 0; b < max_batch; ++b) {
+            LaDev& e = ctx->req[b];
+            const size_t o = (size_t)b * ctx->Qstride;
+            e.row_tok = d.row_tok + o;
+            e.row_pos = d.row_pos + o;
+            e.row_meta = d.row_meta + o;
+            e.row_path = d.row_path + o * ctx->PMAX;
+            e.need = d.need + o;
+            e.argmax = d.argmax + o;
+            e.row_base = (int)o;
+            e.pad_to = ctx->Qstride;
+            e.batch = batch_hdr;
+            hs[b] = e.hdr;
+        }
+        if (cudaMemcpyAsync(ctx->req_hdr, hs.data(), sizeof(LaHdr*) * max_batch, cudaMemcpyHostToDevice, ctx->st) !=
+            cudaSuccess) {
+            la_free(ctx);
+            return LA_ECUDA;
+        }
+    }
     la_launch_rope_table(ctx->rcos, ctx->rsin, ctx->rope_len, c.head_dim, (double)c.rope_theta, ctx->st);
 
     if (ctx->tc) {
@@ -635,15 +740,16 @@ static int check_sampling(const la_sampling* s) {
     return LA_OK;
 }
 
-static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s) {
+static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, const Lane& ln) {
     const la_model_cfg& c = ctx->cfg;
+    const LaDev& d = *ln.d;
     if (!prompt || n < 1) return LA_EINVAL;
     if (n > ctx->max_ctx - 1) return LA_ECAPACITY;
     for (int i = 0; i < n; ++i)
         if (prompt[i] < 0 || prompt[i] >= c.vocab) return LA_EINVAL;
     ctx->prefilled = false;
     ctx->begun = false;
-    CK(cudaMemcpyAsync(ctx->d.prompt, prompt, sizeof(int32_t) * n, cudaMemcpyHostToDevice, ctx->st));
+    CK(cudaMemcpyAsync(d.prompt, prompt, sizeof(int32_t) * n, cudaMemcpyHostToDevice, ctx->st));
     LaHdr h0;
     memset(&h0, 0, sizeof(h0));
     h0.prompt_len = n;
@@ -656,19 +762,19 @@ static int do_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampli
         h0.seed_lo = (uint32_t)(s->seed & 0xffffffffu);
         h0.seed_hi = (uint32_t)(s->seed >> 32);
     }
-    CK(cudaMemcpyAsync(ctx->d.hdr, &h0, sizeof(h0), cudaMemcpyHostToDevice, ctx->st));
-    CK(cudaMemsetAsync(ctx->d.pool_cnt, 0, sizeof(int32_t) * c.vocab, ctx->st));
+    CK(cudaMemcpyAsync(d.hdr, &h0, sizeof(h0), cudaMemcpyHostToDevice, ctx->st));
+    CK(cudaMemsetAsync(d.pool_cnt, 0, sizeof(int32_t) * c.vocab, ctx->st));
     for (int c0 = 0; c0 < n; c0 += PREFILL_CHUNK) {
         int m = std::min(PREFILL_CHUNK, n - c0);
-        la_launch_prefill_rows(ctx->d, ctx->st, c0, m);
-        int r = enqueue_forward(ctx, SEL_PREFILL);
+        la_launch_prefill_rows(d, ctx->st, c0, m);
+        int r = enqueue_forward(ctx, SEL_PREFILL, ln);
         if (r) return r;
     }
-    la_launch_prefill_need(ctx->d, ctx->st, (n - 1) % PREFILL_CHUNK);
-    int r = enqueue_head(ctx, (ctx->debug & 1) | (s ? 1 : 0));
+    la_launch_prefill_need(d, ctx->st, (n - 1) % PREFILL_CHUNK);
+    int r = enqueue_head(ctx, (ctx->debug & 1) | (s ? 1 : 0), ln);
     if (r) return r;
-    if (s) CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, c.vocab, 1));
-    la_launch_prefill_finish(ctx->d, ctx->st, n);
+    if (s) CK(la_launch_sample_verify(d, ctx->st, ctx->logits, c.vocab, 1));
+    la_launch_prefill_finish(d, ctx->st, n);
     CK(cudaGetLastError());
     ctx->prompt_len = n;
     return LA_OK;
@@ -678,7 +784,7 @@ int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, 
     if (!ctx || !first_token) return LA_EINVAL;
     int r = check_sampling(s);
     if (r) return r;
-    r = do_prefill(ctx, prompt, n, s);
+    r = do_prefill(ctx, prompt, n, s, solo_lane(ctx));
     if (r) return r;
     LaHdr h;
     r = read_hdr(ctx, &h);
@@ -794,7 +900,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
     CK(cudaEventCreate(&e1));
     CK(cudaEventCreate(&e2));
     CK(cudaEventRecord(e0, ctx->st));
-    int r = do_prefill(ctx, prompt, n, s);
+    int r = do_prefill(ctx, prompt, n, s, solo_lane(ctx));
     if (r) return r;
     ctx->prefilled = true;
     CK(cudaEventRecord(e1, ctx->st));
@@ -851,6 +957,126 @@ int la_generate(la_ctx* ctx, const int32_t* prompt, int n, int max_new, int W, i
 int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new, const la_sampling* s, int32_t* out,
                    int* n_out, la_stats* stats) {
     return run_generate(ctx, MODE_AR, prompt, n, max_new, 1, 3, 0, s, out, n_out, stats);
+}
+
+// One batched call of B requests as a graph: every request's pack, one
+// forward and LM head over the stacked slices, every request's publication
+// and commit.
+static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
+    const int key = 0x100 | B;
+    auto it = ctx->graphs.find(key);
+    if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
+    const la_model_cfg& c = ctx->cfg;
+    const size_t head_bytes = (size_t)c.head_dim * ctx->esz;
+    Graph g;
+    CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
+    int r = LA_OK;
+    for (int b = 0; b < B; ++b) la_launch_pack(ctx->req[b], ctx->st);
+    const Lane ln = batch_lane(ctx, B);
+    r = enqueue_forward(ctx, SEL_CALL, ln);
+    if (!r) r = enqueue_head(ctx, 0, ln);
+    for (int b = 0; b < B && !r; ++b)
+        r = enqueue_publish_commit_req(ctx, ctx->req[b], 0, (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
+                                       (char*)ctx->temp + (size_t)b * ctx->Qstride * head_bytes, ctx->temp_rows);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
+    if (r) { if (graph) cudaGraphDestroy(graph); return r; }
+    CK(e);
+    g.g = graph;
+    CK(cudaGraphInstantiate(&g.x, graph, 0));
+    ctx->graphs[key] = g;
+    *out = &ctx->graphs[key];
+    return LA_OK;
+}
+
+int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t* lengths, int max_new, int W, int N,
+                      int G, int32_t* out, la_stats* stats) {
+    if (!ctx || !prompts || !lengths || !out || B < 1 || max_new < 1) return LA_EINVAL;
+    if (ctx->max_batch < 2) return LA_ENOTSUP;
+    if (B > ctx->max_batch) return LA_ECAPACITY;
+    if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
+    if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    for (int b = 0; b < B; ++b) {
+        if (lengths[b] < 1) return LA_EINVAL;
+        if (lengths[b] + max_new > ctx->max_ctx) return LA_ECAPACITY;
+    }
+    // request 0's single-request state is reused: a later la_step needs a new prefill
+    ctx->prefilled = false;
+    ctx->begun = false;
+    cudaEvent_t e0, e1, e2;
+    CK(cudaEventCreate(&e0));
+    CK(cudaEventCreate(&e1));
+    CK(cudaEventCreate(&e2));
+    CK(cudaEventRecord(e0, ctx->st));
+    size_t off = 0;
+    for (int b = 0; b < B; ++b) {
+        int r = do_prefill(ctx, prompts + off, lengths[b], nullptr, prefill_lane(ctx, b));
+        if (r) return r;
+        off += (size_t)lengths[b];
+    }
+    CK(cudaEventRecord(e1, ctx->st));
+    for (int b = 0; b < B; ++b)
+        la_launch_begin(ctx->req[b], ctx->st, MODE_LOOKAHEAD, W, N, G, 0, 1.f, 1.f, 0, max_new, (int)ctx->opts);
+    CK(cudaGetLastError());
+    LaHdr hb;
+    memset(&hb, 0, sizeof(hb));
+    hb.mode = MODE_LOOKAHEAD;
+    hb.W = W; hb.N = N; hb.G = G; hb.S = N - 1;
+    hb.Q = B * ctx->Qstride;
+    hb.n_need = B * ctx->Qstride;
+    hb.active = B;
+    hb.done = (max_new <= 1);
+    CK(cudaMemcpyAsync(ctx->bd.hdr, &hb, sizeof(hb), cudaMemcpyHostToDevice, ctx->st));
+    if (ctx->work.counters) CK(cudaMemsetAsync(ctx->work.counters, 0, sizeof(int) * ctx->work.n_counters, ctx->st));
+    Graph* g = nullptr;
+    int r = get_batch_graph(ctx, B, &g);
+    if (r) return r;
+    LaHdr h;
+    CK(cudaMemcpyAsync(&h, ctx->bd.hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    int guard = 0, least = 1;     // tokens of the request that has the fewest
+    std::vector<LaHdr> hr(B);
+    while (!h.done && !h.err) {
+        // a call appends 1 .. N tokens to every live request
+        const int launches = std::max(1, (max_new - least + N - 1) / N);
+        for (int i = 0; i < launches; ++i) CK(cudaGraphLaunch(g->x, ctx->st));
+        CK(cudaMemcpyAsync(&h, ctx->bd.hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
+        for (int b = 0; b < B; ++b)
+            CK(cudaMemcpyAsync(&hr[b], ctx->req[b].hdr, sizeof(LaHdr), cudaMemcpyDeviceToHost, ctx->st));
+        CK(cudaStreamSynchronize(ctx->st));
+        least = max_new;
+        for (int b = 0; b < B; ++b) least = std::min(least, (int)hr[b].n_out);
+        if (++guard > 4 * max_new + 16) return LA_EDEVICE;
+    }
+    CK(cudaEventRecord(e2, ctx->st));
+    if (h.err) return h.err;
+    int64_t steps = 0;
+    for (int b = 0; b < B; ++b) {
+        CK(cudaMemcpyAsync(&hr[b], ctx->req[b].hdr, sizeof(LaHdr), cudaMemcpyDeviceToHost, ctx->st));
+        CK(cudaMemcpyAsync(out + (size_t)b * max_new, ctx->req[b].out, sizeof(int32_t) * max_new,
+                           cudaMemcpyDeviceToHost, ctx->st));
+    }
+    CK(cudaStreamSynchronize(ctx->st));
+    for (int b = 0; b < B; ++b) {
+        if (hr[b].err) return hr[b].err;
+        if (hr[b].n_out < max_new) return LA_EDEVICE;
+        steps = std::max<int64_t>(steps, hr[b].n_steps);
+    }
+    if (stats) {
+        float ms0 = 0, ms1 = 0;
+        cudaEventElapsedTime(&ms0, e0, e1);
+        cudaEventElapsedTime(&ms1, e1, e2);
+        memset(stats, 0, sizeof(*stats));
+        stats->steps = steps;
+        stats->tokens = (int64_t)B * max_new;
+        stats->prefill_ns = (int64_t)(ms0 * 1e6);
+        stats->decode_ns = (int64_t)(ms1 * 1e6);
+        stats->mean_rows = (double)B * ctx->Qstride;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaEventDestroy(e2);
+    return LA_OK;
 }
 
 int la_debug_logits(la_ctx* ctx, float* logits, int32_t* rows, int cap_rows, int* n_rows) {
@@ -1002,7 +1228,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         wk.part_v = pv;
         wk.part_i = pi;
         wk.part_stride = rows_cap;
-        LaDev d;
+        LaDev d{};
         memset(&d, 0, sizeof(d));
         d.hdr = hdr;
         // the weights as the model's GEMMs read them: unit-contiguous images
@@ -1103,7 +1329,7 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
     TcWork wk;
     memset(&wk, 0, sizeof(wk));
     wk.ws = ws; wk.counters = cnt; wk.part_v = pv; wk.part_i = pi; wk.part_stride = rows_cap;
-    LaDev d;
+    LaDev d{};
     memset(&d, 0, sizeof(d));
     d.hdr = hdr;
     if (!rc) {

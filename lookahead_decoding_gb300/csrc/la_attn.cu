@@ -172,10 +172,23 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
 __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bfloat16* qbuf, const __nv_bfloat16* kc,
                                                       const __nv_bfloat16* vc, const __nv_bfloat16* kt,
                                                       const __nv_bfloat16* vt, __nv_bfloat16* out, int sel, int Qcap,
-                                                      int max_ctx, int Qmax, int TB, int H, int ring_keys,
-                                                      const __grid_constant__ CUtensorMap cmap, int krow0, int vrow0) {
+                                                      int max_ctx, int temp_stride, int TB, int H, int ring_keys,
+                                                      const __grid_constant__ CUtensorMap cmap, int krow0, int vrow0,
+                                                      const LaHdr* const* req_hdr, int qstride,
+                                                      long long req_cache_elems, int req_cache_rows) {
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
+    // A batched call stacks its requests' rows in slices of qstride rows (a
+    // multiple of the tile): the tile's request has its own header
+    // (committed length, row count), cache and temporary rows.
+    const int req = qstride ? r0 / qstride : 0;
+    const LaHdr* hr = qstride ? req_hdr[req] : h;
+    krow0 += req * req_cache_rows;
+    vrow0 += req * req_cache_rows;
+    kc += (size_t)req * req_cache_elems;
+    vc += (size_t)req * req_cache_elems;
+    kt += (size_t)req * qstride * DH;
+    vt += (size_t)req * qstride * DH;
     const int prefill = (sel == SEL_PREFILL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     // row is below Qcap and block 0 lies in the cache, so all of it is in
     // bounds whatever the call's row count.
     const int h_err = h->err, h_done = h->done, rows = rows_sel(h, sel);
-    if (h_err != 0 || (sel != SEL_PREFILL && h_done != 0) || r0 >= rows) return;
+    if (h_err != 0 || (sel != SEL_PREFILL && (h_done != 0 || hr->done != 0)) || r0 >= rows) return;
     const bool spec0 = (blockIdx.y == 0) && !prefill;
     int pos_raw = 0;
     if (!prefill) {
@@ -247,8 +260,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     const int nr = min(FR, rows - r0);
-    const int K = prefill ? 0 : h->K;
-    const int Q = prefill ? 0 : h->Q;                 // the call's temporary K/V rows
+    const int K = prefill ? 0 : hr->K;
+    const int Q = prefill ? 0 : hr->Q;                // the request's temporary K/V rows
     if (tid < FR) {
         const int pos = tid < nr ? pos_raw : -1;
         rpos[tid] = pos;
@@ -425,8 +438,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const int nt = nc + Q;
     const uint32_t tk_a = sbase + LY.ring, tv_a = tk_a + (uint32_t)ring_keys * LDK * 2u;
     {
-        const __nv_bfloat16* kth = kt + (size_t)hh * Qmax * DH;
-        const __nv_bfloat16* vth = vt + (size_t)hh * Qmax * DH;
+        const __nv_bfloat16* kth = kt + (size_t)hh * temp_stride * DH;
+        const __nv_bfloat16* vth = vt + (size_t)hh * temp_stride * DH;
         for (int i = tid; i < nt * (DH / 8); i += blockDim.x) {
             const int j = i >> 4, c8 = (i & 15) * 8;
             const __nv_bfloat16* ksrc;
@@ -559,7 +572,8 @@ size_t la_attn_smem_bytes(int TB, int Qmax, int pmax) {
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
-                                     int krow0, int vrow0) {
+                                     int krow0, int vrow0, const LaHdr* const* req_hdr, int qstride,
+                                     long long req_cache_elems, int req_cache_rows, int temp_stride) {
     if (TB + 1 > MAX_TAIL / 32) return cudaErrorInvalidValue;
     const int ring_keys = ring_keys_for(TB, Qmax);
     const size_t smem = la_attn_smem_bytes(TB, Qmax, pmax);
@@ -573,6 +587,7 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
     dim3 grid(H, (rows_cap + FR - 1) / FR);
     return la_launch_pdl(k_attn_fused, grid, dim3(FT * 32), smem, st, d, (const __nv_bfloat16*)qbuf,
                          (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
-                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx, Qmax, TB, H, ring_keys,
-                         cmap, krow0, vrow0);
+                         (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx,
+                         temp_stride ? temp_stride : Qmax, TB, H, ring_keys,
+                         cmap, krow0, vrow0, req_hdr, qstride, req_cache_elems, req_cache_rows);
 }

@@ -58,7 +58,7 @@ struct LaHdr {
     int32_t prefill_rows;   // rows of the current prefill chunk
     int32_t opts;           // LA_OPT_* options of the request
     int32_t seed_next;      // next prompt index (mod prompt_len) of the refill cycle
-    int32_t pad[1];
+    int32_t active;         // batch header only: requests of the batch not yet done
 };
 
 // Device pointers and sizes of one context, passed by value to kernels.
@@ -77,6 +77,14 @@ struct LaDev {
     int32_t* out;          // [out_cap]
     int32_t* commit_rows;  // [16]
     int32_t V, Gmax, Smax, Rmax, LMAX, PMAX, Qmax, Qcap, max_ctx, out_cap;
+    // batched calls (several requests stacked in one call; all zero alone):
+    // the row arrays above then point at this request's slice of the stacked
+    // rows, need entries carry the slice's first stacked row, rows past the
+    // request's own up to pad_to are filled as copies of its ordinary row,
+    // and publication keeps the batch header's count of live requests.
+    int32_t row_base;
+    int32_t pad_to;
+    LaHdr* batch;
 };
 
 __device__ __forceinline__ float to_f(float x) { return x; }

@@ -171,4 +171,5 @@ size_t la_attn_smem_bytes(int TB, int Qmax, int pmax);
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
-                                     int krow0, int vrow0);
+                                     int krow0, int vrow0, const LaHdr* const* req_hdr = nullptr, int qstride = 0,
+                                     long long req_cache_elems = 0, int req_cache_rows = 0, int temp_stride = 0);

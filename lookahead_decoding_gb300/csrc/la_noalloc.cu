@@ -119,7 +119,7 @@ int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, c
     wk.ws_floats = ws_floats;
     wk.counters = counters;
     wk.n_counters = (int)n_counters;
-    LaDev d;
+    LaDev d{};
     memset(&d, 0, sizeof(d));
     d.hdr = hdr;
 

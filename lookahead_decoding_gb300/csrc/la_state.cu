@@ -58,8 +58,12 @@ __global__ void k_pack(LaDev d) {
     LaHdr* h = d.hdr;
     __shared__ int s_off[LA_MAX_R + 2];
     __shared__ int s_Q, s_Ct, s_vstart, s_ok, s_d, s_deep0;
-    if (h->err || h->done) return;
     const int tid = threadIdx.x;
+    if (h->err || h->done) {
+        // a finished request of a batch: nothing of this call is committed
+        if (tid == 0 && !h->err) h->commit_n = 0;
+        return;
+    }
     const int K = h->K, x_t = h->x_t, S = h->S;
     if (tid == 0) {
         int ok = 1;
@@ -95,7 +99,10 @@ __global__ void k_pack(LaDev d) {
             if (Q > d.Qmax || maxoff + 1 > d.PMAX || K + maxoff >= d.max_ctx + d.PMAX || K + 1 + S > d.max_ctx) ok = 0;
         }
         s_ok = ok;
-        if (!ok) la_set_err(h, LA_ECAPACITY);
+        if (!ok) {
+            la_set_err(h, LA_ECAPACITY);
+            if (d.batch) la_set_err(d.batch, LA_ECAPACITY);
+        }
     }
     __syncthreads();
     if (!s_ok) return;
@@ -132,20 +139,30 @@ __global__ void k_pack(LaDev d) {
         }
         d.row_tok[q] = tok; d.row_pos[q] = pos; d.row_meta[q] = meta;
     }
-    // needed rows: [0] + deepest level + verification rows
+    // batched call: the slice's remaining rows repeat the ordinary row
+    for (int q = Q + tid; q < d.pad_to; q += blockDim.x) {
+        d.row_tok[q] = x_t; d.row_pos[q] = K; d.row_meta[q] = la_meta(ROLE_ORDINARY, 0, 0, 0, 0);
+        d.row_path[(size_t)q * P] = 0;
+    }
+    // needed rows: [0] + deepest level + verification rows (stacked-row
+    // indices: the slice's first row added; a batch's slice padded with its
+    // ordinary row)
+    int n_need = 1;
     if (h->mode == MODE_AR) {
-        if (tid == 0) d.need[0] = 0;
+        if (tid == 0) d.need[0] = d.row_base;
     } else {
         int n_deep = h->level_len[dl];
         int nv = s_Ct * S;
-        for (int i = tid; i < 1 + n_deep + nv; i += blockDim.x) {
+        n_need = 1 + n_deep + nv;
+        for (int i = tid; i < n_need; i += blockDim.x) {
             int r;
             if (i == 0) r = 0;
             else if (i <= n_deep) r = s_deep0 + (i - 1);
             else r = vstart + (i - 1 - n_deep);
-            d.need[i] = r;
+            d.need[i] = d.row_base + r;
         }
     }
+    for (int i = n_need + tid; i < d.pad_to; i += blockDim.x) d.need[i] = d.row_base;
 }
 
 // ---------------------------------------------------------------------------
@@ -273,7 +290,11 @@ __global__ void k_publish(LaDev d, int verdict_given) {
         s_nout0 = n_out;
         s_take = take;
         h->n_out = n_out + take;
-        if (h->n_out >= h->max_out) h->done = 1;
+        if (h->n_out >= h->max_out) {
+            h->done = 1;
+            // the batch is done once its last live request is
+            if (d.batch && atomicSub(&d.batch->active, 1) == 1) d.batch->done = 1;
+        }
         h->a = a; h->winner = w; h->E = E;
         for (int i = 0; i < E; ++i) h->emitted[i] = s_emit[i];
         h->commit_base = h->K;
