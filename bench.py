@@ -165,6 +165,63 @@ def cpu_oracle_sample(cfg, weights, min_s: float = 10.0, max_calls: int = 64, pr
                       f"after a {prompt_len}-token prompt on the 7B shape; {toks} tokens in {dt:.1f} s"}
 
 
+def batch_prompts(vocab: int, B: int):
+    """B different 512-token Markov/Zipf prompts (seeds 2, 3, ..)."""
+    import synth
+    return [synth.markov_zipf_prompt(vocab, PROMPT_LEN, 2 + b).tolist() for b in range(B)]
+
+
+def run_batch(args, cfg, rank: int, local: int) -> None:
+    """Several requests per packed call on one GPU: committed tokens/s of all
+    requests (decode device time), each request checked against its AR output."""
+    if rank != 0:
+        return
+    import torch
+    import synth
+    torch.cuda.set_device(local)
+    from lookahead_decoding_gb300 import build
+    build()
+    from lookahead_decoding_gb300 import lib
+    L = lib()
+    B = args.batch
+    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}")
+    ctx = L.Context(cfg, w, max_ctx=1024, max_W=W_, max_N=N_, max_G=G_, max_batch=B)
+    prompts = batch_prompts(cfg.vocab, B)
+    for _ in range(args.warmup):
+        L.la_generate_batch(ctx.ctx, prompts, args.max_new, W_, N_, G_)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    stats, outs = [], []
+    for _ in range(args.steps):
+        st = L.la_stats()
+        outs.append(L.la_generate_batch(ctx.ctx, prompts, args.max_new, W_, N_, G_, stats=st))
+        stats.append(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    decode_s = sum(s.decode_ns for s in stats) * 1e-9
+    calls = sum(s.steps for s in stats)
+    new_tokens = sum(B * (args.max_new - 1) for _ in stats)
+    ar = [L.la_generate_ar(ctx.ctx, p, args.max_new) for p in prompts]
+    config = {"workload": f"llama-7b-shape bf16, {B} requests per packed call, prompts 512 Markov/Zipf(1.1), "
+                          f"{args.max_new} new tokens each, greedy, W=15 N=5 G=15",
+              "model": "llama-7b-shape (random init)", "global_batch": B, "seq_len": PROMPT_LEN + args.max_new,
+              "parallelism": "one GPU", "l2": "inputs larger than L2 (13 GB weights per call); no flush"}
+    line = {"metric": f"committed tokens/s @ batch {B} (7B-shape bf16)", "value": new_tokens / decode_s,
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "call_latency_ms": decode_s / calls * 1e3, "calls_per_request": calls / args.steps,
+            "batched_equals_ar": all(o == ar for o in outs),
+            "e2e": {"value": B * args.max_new * args.steps / wall, "unit": "tokens/s",
+                    "h2d_bytes_per_step": B * PROMPT_LEN * 4, "d2h_bytes_per_step": B * args.max_new * 4},
+            "clocks": clk}
+    ctx.close()
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -176,6 +233,8 @@ def main():
     ap.add_argument("--max-new", type=int, default=MAX_NEW, help="new tokens per request (profiling runs)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling runs: a model with this many layers of the same shapes (0 = all 32)")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="requests per packed call (la_generate_batch); 1 = the headline single-request bench")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -210,6 +269,9 @@ def main():
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
+
+    if args.batch > 1:
+        return run_batch(args, cfg, rank, local)
 
     if world > 1:
         import torch.distributed as dist

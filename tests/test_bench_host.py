@@ -15,3 +15,10 @@ def test_cpu_oracle_sample_is_bounded_and_reports_its_sample():
     assert s["kind"] == "oracle" and s["unit"] == "tokens/s" and s["value"] > 0
     assert s["cores"] >= 1
     assert "packed calls" in s["sample"]
+
+
+def test_batch_prompts_are_distinct_and_seeded():
+    import bench
+    a = bench.batch_prompts(32000, 4)
+    assert a == bench.batch_prompts(32000, 4)
+    assert len({tuple(p) for p in a}) == 4 and all(len(p) == bench.PROMPT_LEN for p in a)
