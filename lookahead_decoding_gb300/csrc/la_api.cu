@@ -269,7 +269,8 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
                                         ctx->cache_map, ln.cache_row0 + (l * 2 + 0) * H * ctx->max_ctx,
                                         ln.cache_row0 + (l * 2 + 1) * H * ctx->max_ctx, ln.req_hdr, ln.qstride,
                                         (long long)(ctx->cache_bytes_req / ctx->esz),
-                                        c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows));
+                                        c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows,
+                                        la_attn_tail_rows(ctx->max_W, ctx->max_N, ctx->Qmax)));
         } else {
             CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
                                    layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
@@ -574,7 +575,9 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         if (!r && la_tc_make_map(&ctx->cache_map, ctx->cache, max_batch * c.n_layers * 2 * c.n_heads * max_ctx,
                                  c.head_dim, 128))
             r = LA_ECUDA;
-        if (la_attn_smem_bytes(ctx->attn_TB, ctx->Qmax, ctx->PMAX) > 227 * 1024) r = LA_ENOTSUP;
+        if (la_attn_smem_bytes(ctx->attn_TB, la_attn_tail_rows(max_W, max_N, ctx->Qmax), ctx->PMAX, ctx->Qmax) >
+            227 * 1024)
+            r = LA_ENOTSUP;
     }
     // batched calls: request 0 keeps the state above; requests 1.. get their
     // own header, window, pool, prompt, out ring and commit plan

@@ -167,9 +167,18 @@ cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V,
 
 // bf16 attention: committed 128-position blocks on tensor cores + combine/tail
 int la_attn_tail_blocks(int pmax);
-size_t la_attn_smem_bytes(int TB, int Qmax, int pmax);
+size_t la_attn_smem_bytes(int TB, int tail_rows, int pmax, int qrows);
+// the most temporary rows the paths of one attention tile (16 consecutive
+// packed rows) can reach: base stripe and level 0 (<= W+N-3 cells), each
+// row's own trajectory cells (<= N-2), the verification cells of the
+// candidates the tile touches (<= 16 + N-1), bounded by the call's rows
+inline int la_attn_tail_rows(int max_W, int max_N, int Qmax) {
+    const int u = max_W + 20 * (max_N - 1);
+    return u < Qmax ? u : Qmax;
+}
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
                                      int krow0, int vrow0, const LaHdr* const* req_hdr = nullptr, int qstride = 0,
-                                     long long req_cache_elems = 0, int req_cache_rows = 0, int temp_stride = 0);
+                                     long long req_cache_elems = 0, int req_cache_rows = 0, int temp_stride = 0,
+                                     int tail_rows = 0);
