@@ -965,8 +965,8 @@ int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new, const
 // One batched call of B requests as a graph: every request's pack, one
 // forward and LM head over the stacked slices, every request's publication
 // and commit.
-static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
-    const int key = 0x100 | B;
+static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
+    const int key = 0x100 | B | (sampling << 12);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     const la_model_cfg& c = ctx->cfg;
@@ -977,9 +977,15 @@ static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
     for (int b = 0; b < B; ++b) la_launch_pack(ctx->req[b], ctx->st);
     const Lane ln = batch_lane(ctx, B);
     r = enqueue_forward(ctx, SEL_CALL, ln);
-    if (!r) r = enqueue_head(ctx, 0, ln);
+    if (!r) r = enqueue_head(ctx, sampling, ln);
+    // sampling: each request's verifier on the logits of its slice of the needed rows
+    for (int b = 0; b < B && !r && sampling; ++b)
+        if (la_launch_sample_verify(ctx->req[b], ctx->st, ctx->logits + (size_t)b * ctx->Qstride * c.vocab, c.vocab, 0) !=
+            cudaSuccess)
+            r = LA_ECUDA;
     for (int b = 0; b < B && !r; ++b)
-        r = enqueue_publish_commit_req(ctx, ctx->req[b], 0, (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
+        r = enqueue_publish_commit_req(ctx, ctx->req[b], sampling,
+                                       (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
                                        (char*)ctx->temp + (size_t)b * ctx->Qstride * head_bytes, ctx->temp_rows);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
@@ -993,8 +999,9 @@ static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
 }
 
 int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t* lengths, int max_new, int W, int N,
-                      int G, int32_t* out, la_stats* stats) {
+                      int G, const la_sampling* s, int32_t* out, la_stats* stats) {
     if (!ctx || !prompts || !lengths || !out || B < 1 || max_new < 1) return LA_EINVAL;
+    if (check_sampling(s)) return LA_EINVAL;
     if (ctx->max_batch < 2) return LA_ENOTSUP;
     if (B > ctx->max_batch) return LA_ECAPACITY;
     if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
@@ -1011,15 +1018,22 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     CK(cudaEventCreate(&e1));
     CK(cudaEventCreate(&e2));
     CK(cudaEventRecord(e0, ctx->st));
+    // sampling: request b draws with seed s->seed + b
+    std::vector<la_sampling> sb(B);
+    for (int b = 0; b < B && s; ++b) {
+        sb[b] = *s;
+        sb[b].seed = s->seed + (uint64_t)b;
+    }
     size_t off = 0;
     for (int b = 0; b < B; ++b) {
-        int r = do_prefill(ctx, prompts + off, lengths[b], nullptr, prefill_lane(ctx, b));
+        int r = do_prefill(ctx, prompts + off, lengths[b], s ? &sb[b] : nullptr, prefill_lane(ctx, b));
         if (r) return r;
         off += (size_t)lengths[b];
     }
     CK(cudaEventRecord(e1, ctx->st));
     for (int b = 0; b < B; ++b)
-        la_launch_begin(ctx->req[b], ctx->st, MODE_LOOKAHEAD, W, N, G, 0, 1.f, 1.f, 0, max_new, (int)ctx->opts);
+        la_launch_begin(ctx->req[b], ctx->st, MODE_LOOKAHEAD, W, N, G, s ? 1 : 0, s ? s->temperature : 1.f,
+                        s ? s->top_p : 1.f, s ? sb[b].seed : 0, max_new, (int)ctx->opts);
     CK(cudaGetLastError());
     LaHdr hb;
     memset(&hb, 0, sizeof(hb));
@@ -1032,7 +1046,7 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     CK(cudaMemcpyAsync(ctx->bd.hdr, &hb, sizeof(hb), cudaMemcpyHostToDevice, ctx->st));
     if (ctx->work.counters) CK(cudaMemsetAsync(ctx->work.counters, 0, sizeof(int) * ctx->work.n_counters, ctx->st));
     Graph* g = nullptr;
-    int r = get_batch_graph(ctx, B, &g);
+    int r = get_batch_graph(ctx, B, s ? 1 : 0, &g);
     if (r) return r;
     LaHdr h;
     CK(cudaMemcpyAsync(&h, ctx->bd.hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
