@@ -128,6 +128,15 @@ static int read_hdr(la_ctx* ctx, LaHdr* h) {
     return LA_OK;
 }
 
+int la_fuse_rope() {
+    static int on = -1;
+    if (on < 0) {
+        const char* e = getenv("LA_FUSE_ROPE");
+        on = (e && e[0] == '0') ? 0 : 1;
+    }
+    return on;
+}
+
 int la_pdl_enabled() {
     static int on = -1;
     if (on < 0) {
@@ -255,10 +264,16 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
         void* vdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx)
                                           : layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows);
         int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ln.temp_rows;
-        pi = prof_open(ctx, PK_ROW);
-        la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
-                          stride, rc, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr));
-        prof_close(ctx, pi);
+        // decode calls of bf16 models fold RoPE into the attention (LA_FUSE_ROPE=0: a kernel of its own)
+        const bool fuse = ctx->bf16 && ctx->tc && sel != SEL_PREFILL && la_fuse_rope();
+        const LaRope rope{(const __nv_bfloat16*)ctx->qkv, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr), ctx->rcos,
+                          ctx->rsin};
+        if (!fuse) {
+            pi = prof_open(ctx, PK_ROW);
+            la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel,
+                              ctx->Qcap, stride, rc, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr));
+            prof_close(ctx, pi);
+        }
         pi = prof_open(ctx, PK_ATTN);
         if (ctx->bf16) {
             CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
@@ -270,7 +285,7 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
                                         ln.cache_row0 + (l * 2 + 1) * H * ctx->max_ctx, ln.req_hdr, ln.qstride,
                                         (long long)(ctx->cache_bytes_req / ctx->esz),
                                         c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows,
-                                        la_attn_tail_rows(ctx->max_W, ctx->max_N, ctx->Qmax)));
+                                        la_attn_tail_rows(ctx->max_W, ctx->max_N, ctx->Qmax), fuse ? &rope : nullptr));
         } else {
             CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
                                    layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),

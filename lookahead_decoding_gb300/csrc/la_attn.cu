@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
                                                       int max_ctx, int temp_stride, int TB, int H, int ring_keys,
                                                       const __grid_constant__ CUtensorMap cmap, int krow0, int vrow0,
                                                       const LaHdr* const* req_hdr, int qstride,
-                                                      long long req_cache_elems, int req_cache_rows, int qrows) {
+                                                      long long req_cache_elems, int req_cache_rows, int qrows,
+                                                      LaRope rope) {
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
     // A batched call stacks its requests' rows in slices of qstride rows (a
@@ -256,13 +257,17 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     la_pdl_wait();
     la_pdl_trigger();
     if (prefill && tid < FR) pos_raw = d.row_pos[r0 + tid];
-    const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
-    for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
-        const int r = i >> 4, c8 = (i & 15) * 8;
-        cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(r0 + r) * DH + c8, 16);
+    const int nr = min(FR, rows - r0);
+    // decode with RoPE folded in: the queries are computed below from the QKV output
+    const bool fuse = rope.qkv != nullptr && !prefill;
+    if (!fuse) {
+        const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
+        for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
+            const int r = i >> 4, c8 = (i & 15) * 8;
+            cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(r0 + r) * DH + c8, 16);
+        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    const int nr = min(FR, rows - r0);
     const int K = prefill ? 0 : hr->K;
     const int Q = prefill ? 0 : hr->Q;                // the request's temporary K/V rows
     if (tid < FR) {
@@ -271,6 +276,44 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         rt0[tid] = pos >= 0 ? t0_of(pos, TB) : 0;
     }
     __syncthreads();
+    // RoPE folded in: the tile's queries of head hh into shared memory and,
+    // for the K/V commit, its rows' rotated K and V into the temporary rows
+    // (each (row, head) is written by exactly one CTA; no CTA of this kernel
+    // reads them).  Rows past the call's rows get zero queries.
+    const int HD = H * DH, half = DH / 2;
+    const int seg_q = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, hh) : 1;
+    const int seg_k = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, H + hh) : 1;
+    const int seg_v = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, 2 * H + hh) : 1;
+    if (fuse) {
+        __nv_bfloat16* qs_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
+        __nv_bfloat16* kt_w = const_cast<__nv_bfloat16*>(kt) + (size_t)hh * temp_stride * DH;
+        __nv_bfloat16* vt_w = const_cast<__nv_bfloat16*>(vt) + (size_t)hh * temp_stride * DH;
+        for (int i = tid; i < FR * (half / 4); i += blockDim.x) {
+            const int r = i / (half / 4), c4 = (i % (half / 4)) * 4;
+            __nv_bfloat16* qd = qs_w + r * LDK + c4;
+            if (r >= nr) {
+                *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
+                *reinterpret_cast<uint2*>(qd + half) = make_uint2(0u, 0u);
+                continue;
+            }
+            const int row = r0 + r, pos = rpos[r], lrow = row - req * qstride;
+            const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+            const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+            const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+            const float4 qa = la_qkv_at4(x, row, hh * DH + c4, rope.sp, seg_q);
+            const float4 qb = la_qkv_at4(x, row, hh * DH + c4 + half, rope.sp, seg_q);
+            const float4 ka = la_qkv_at4(x, row, HD + hh * DH + c4, rope.sp, seg_k);
+            const float4 kb = la_qkv_at4(x, row, HD + hh * DH + c4 + half, rope.sp, seg_k);
+            const float4 va = la_qkv_at4(x, row, 2 * HD + hh * DH + c4, rope.sp, seg_v);
+            const float4 vb = la_qkv_at4(x, row, 2 * HD + hh * DH + c4 + half, rope.sp, seg_v);
+            la_rope4_store(qd, qd + half, qa, qb, c, s);
+            __nv_bfloat16* ko = kt_w + (size_t)lrow * DH + c4;
+            __nv_bfloat16* vo = vt_w + (size_t)lrow * DH + c4;
+            la_rope4_store(ko, ko + half, ka, kb, c, s);
+            *reinterpret_cast<uint2*>(vo) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
+            *reinterpret_cast<uint2*>(vo + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+        }
+    }
     int t0max = 0, t0min = 0x7fffffff, posmax = 0;
     for (int r = 0; r < nr; ++r) {
         t0max = max(t0max, rt0[r]);
@@ -486,10 +529,33 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
             const __nv_bfloat16* ksrc;
             const __nv_bfloat16* vsrc;
             if (j < nc) { ksrc = kh + (size_t)(t0min + j) * DH; vsrc = vh + (size_t)(t0min + j) * DH; }
+            else if (fuse) continue;     // computed below from the QKV output
             else { const int row = urow[j - nc]; ksrc = kth + (size_t)row * DH; vsrc = vth + (size_t)row * DH; }
             const uint32_t off = (uint32_t)(j * LDK + c8) * 2u;
             cp_async16(tk_a + off, ksrc + c8, 16);
             cp_async16(tv_a + off, vsrc + c8, 16);
+        }
+        if (fuse) {
+            // the in-call keys on the tile's paths: rotated K and V of the
+            // request's row urow[s] at its position, head hh, into slot nc + s
+            __nv_bfloat16* tk_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.ring);
+            __nv_bfloat16* tv_w = tk_w + (size_t)ring_keys * LDK;
+            for (int i = tid; i < (nt - nc) * (half / 4); i += blockDim.x) {
+                const int sl = i / (half / 4), c4 = (i % (half / 4)) * 4;
+                const int row = req * qstride + urow[sl], pos = d.row_pos[row];
+                const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+                const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+                const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+                const float4 ka = la_qkv_at4(x, row, HD + hh * DH + c4, rope.sp, seg_k);
+                const float4 kb = la_qkv_at4(x, row, HD + hh * DH + c4 + half, rope.sp, seg_k);
+                const float4 va = la_qkv_at4(x, row, 2 * HD + hh * DH + c4, rope.sp, seg_v);
+                const float4 vb = la_qkv_at4(x, row, 2 * HD + hh * DH + c4 + half, rope.sp, seg_v);
+                __nv_bfloat16* kd = tk_w + (size_t)(nc + sl) * LDK + c4;
+                __nv_bfloat16* vd = tv_w + (size_t)(nc + sl) * LDK + c4;
+                la_rope4_store(kd, kd + half, ka, kb, c, s);
+                *reinterpret_cast<uint2*>(vd) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
+                *reinterpret_cast<uint2*>(vd + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+            }
         }
         asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
@@ -616,7 +682,8 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
                                      int krow0, int vrow0, const LaHdr* const* req_hdr, int qstride,
-                                     long long req_cache_elems, int req_cache_rows, int temp_stride, int tail_rows) {
+                                     long long req_cache_elems, int req_cache_rows, int temp_stride, int tail_rows,
+                                     const LaRope* rope) {
     if (TB + 1 > MAX_TAIL / 32) return cudaErrorInvalidValue;
     if (tail_rows <= 0 || tail_rows > Qmax) tail_rows = Qmax;
     const int ring_keys = ring_keys_for(TB, tail_rows);
@@ -633,5 +700,6 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
                          (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
                          (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx,
                          temp_stride ? temp_stride : Qmax, TB, H, ring_keys,
-                         cmap, krow0, vrow0, req_hdr, qstride, req_cache_elems, req_cache_rows, Qmax);
+                         cmap, krow0, vrow0, req_hdr, qstride, req_cache_elems, req_cache_rows, Qmax,
+                         rope ? *rope : LaRope{nullptr, LaSplit{}, nullptr, nullptr});
 }
