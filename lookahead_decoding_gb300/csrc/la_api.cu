@@ -752,6 +752,22 @@ int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* sampl
     return LA_OK;
 }
 
+// three timing events, destroyed on every return path
+struct Events3 {
+    cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
+    cudaError_t create() {
+        for (auto& x : e) {
+            cudaError_t r = cudaEventCreate(&x);
+            if (r != cudaSuccess) return r;
+        }
+        return cudaSuccess;
+    }
+    ~Events3() {
+        for (auto& x : e)
+            if (x) cudaEventDestroy(x);
+    }
+};
+
 static int check_sampling(const la_sampling* s) {
     if (!s) return LA_OK;
     if (!(s->temperature > 0.f) || !(s->top_p > 0.f) || !(s->top_p <= 1.f)) return LA_EINVAL;
@@ -913,10 +929,9 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
     }
     if (n + max_new > ctx->max_ctx) return LA_ECAPACITY;
-    cudaEvent_t e0, e1, e2;
-    CK(cudaEventCreate(&e0));
-    CK(cudaEventCreate(&e1));
-    CK(cudaEventCreate(&e2));
+    Events3 ev;
+    CK(ev.create());
+    cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
     CK(cudaEventRecord(e0, ctx->st));
     int r = do_prefill(ctx, prompt, n, s, solo_lane(ctx));
     if (r) return r;
@@ -961,9 +976,6 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         stats->mean_candidates = h.n_steady ? (double)h.sum_Ct / h.n_steady : 0.0;
         stats->mean_rows = h.n_steps ? (double)h.sum_Q / h.n_steps : 0.0;
     }
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaEventDestroy(e2);
     return LA_OK;
 }
 
@@ -1028,10 +1040,9 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     // request 0's single-request state is reused: a later la_step needs a new prefill
     ctx->prefilled = false;
     ctx->begun = false;
-    cudaEvent_t e0, e1, e2;
-    CK(cudaEventCreate(&e0));
-    CK(cudaEventCreate(&e1));
-    CK(cudaEventCreate(&e2));
+    Events3 ev;
+    CK(ev.create());
+    cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
     CK(cudaEventRecord(e0, ctx->st));
     // sampling: request b draws with seed s->seed + b
     std::vector<la_sampling> sb(B);
@@ -1105,9 +1116,6 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
         stats->decode_ns = (int64_t)(ms1 * 1e6);
         stats->mean_rows = (double)B * ctx->Qstride;
     }
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaEventDestroy(e2);
     return LA_OK;
 }
 
