@@ -177,6 +177,58 @@ def batch_prompts(vocab: int, B: int):
     return [synth.markov_zipf_prompt(vocab, PROMPT_LEN, 2 + b).tolist() for b in range(B)]
 
 
+SWEEP_W, SWEEP_N, SWEEP_PROMPT = (1, 3, 7, 15, 31), (3, 5, 7), 1024
+
+
+def run_sweep(args, cfg, rank: int, local: int) -> None:
+    """Per sweep point (W, N, G = W) on a 1024-token Markov prompt: packed-call
+    latency, committed tokens per call, the call's roofline fraction and the
+    autoregressive step latency on the same kernels; one context per point."""
+    if rank != 0:
+        return
+    import torch
+    import synth
+    torch.cuda.set_device(local)
+    from lookahead_decoding_gb300 import build
+    build()
+    from lookahead_decoding_gb300 import lib
+    L = lib()
+    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}")
+    prompt = synth.markov_zipf_prompt(cfg.vocab, SWEEP_PROMPT, 2).tolist()
+    peaks, src = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    max_ctx = SWEEP_PROMPT + args.max_new + 64
+    ar_ms, ar_out = None, None
+    points = []
+    for W in SWEEP_W:
+        for N in SWEEP_N:
+            try:
+                ctx = L.Context(cfg, w, max_ctx=max_ctx, max_W=W, max_N=N, max_G=W)
+            except L.LaError as e:
+                points.append({"W": W, "N": N, "G": W, "unsupported": str(e)})
+                continue
+            if ar_ms is None:
+                st = L.la_stats()
+                ar_out = L.la_generate_ar(ctx.ctx, prompt, args.max_new, stats=st)
+                ar_ms = st.decode_ns * 1e-6 / st.steps
+            L.la_generate(ctx.ctx, prompt, args.max_new, W, N, W)          # warm-up (graph capture)
+            st = L.la_stats()
+            out = L.la_generate(ctx.ctx, prompt, args.max_new, W, N, W, stats=st)
+            call_ms = st.decode_ns * 1e-6 / st.steps
+            K_mean = SWEEP_PROMPT + args.max_new / 2.0
+            bytes_call = algorithmic_bytes_per_call(cfg, K_mean, st.mean_rows)
+            points.append({"W": W, "N": N, "G": W, "call_ms": call_ms, "tokens_per_call": (st.tokens - 1) / st.steps,
+                           "tokens_per_s": (st.tokens - 1) / (st.decode_ns * 1e-9), "mean_rows": st.mean_rows,
+                           "step_roofline_frac": bytes_call / (call_ms * 1e-3) / 1e9 / peak,
+                           "equals_ar": out == ar_out})
+            ctx.close()
+    line = {"metric": "W x N sweep (7B-shape bf16, greedy)", "unit": "ms per packed call", "n_gpus": 1,
+            "config": {"workload": f"llama-7b-shape bf16, batch 1, prompt {SWEEP_PROMPT} Markov/Zipf(1.1), "
+                                   f"{args.max_new} new tokens, greedy, G = W", "model": "llama-7b-shape (random init)"},
+            "ar_ms_per_token": ar_ms, "peak_gbs": peak, "peak_source": src, "points": points}
+    print(json.dumps(line))
+
+
 def run_batch(args, cfg, rank: int, local: int) -> None:
     """Several requests per packed call on one GPU: committed tokens/s of all
     requests (decode device time), each request checked against its AR output."""
@@ -241,6 +293,8 @@ def main():
                     help="profiling runs: a model with this many layers of the same shapes (0 = all 32)")
     ap.add_argument("--batch", type=int, default=1,
                     help="requests per packed call (la_generate_batch); 1 = the headline single-request bench")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the W x N sweep on the 7B shape (W in 1,3,7,15,31; N in 3,5,7; G=W): one JSON line")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -276,6 +330,8 @@ def main():
         print(json.dumps(line))
         return
 
+    if args.sweep:
+        return run_sweep(args, cfg, rank, local)
     if args.batch > 1:
         return run_batch(args, cfg, rank, local)
 
