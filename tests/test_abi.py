@@ -40,3 +40,25 @@ def test_argument_errors_need_no_gpu():
     assert L.la_step(None, 5, 3, 5, None, None, None) == _lib.LA_EINVAL
     assert L.la_generate(None, None, 0, 1, 5, 3, 5, None, None, None, None) == _lib.LA_EINVAL
     assert L.la_free(None) is None
+
+
+def test_generate_batch_marshalling(monkeypatch):
+    """The binding passes the prompts back to back with their lengths and
+    cuts the B x max_new output into one list per request (a recording
+    stand-in replaces the library call; no GPU)."""
+    from lookahead_decoding_gb300 import _lib
+    seen = {}
+
+    class Stub:
+        def la_generate_batch(self, ctx, B, flat, lengths, max_new, W, N, G, out, stats):
+            seen.update(B=B, flat=[flat[i] for i in range(9)], lengths=[lengths[i] for i in range(B)],
+                        knobs=(max_new, W, N, G))
+            for b in range(B):
+                for i in range(max_new):
+                    out[b * max_new + i] = 100 * b + i
+            return 0
+
+    monkeypatch.setattr(_lib, "LIB", Stub())
+    got = _lib.la_generate_batch(None, [[1, 2], [3, 4, 5, 6], [7, 8, 9]], 3, 5, 4, 2)
+    assert seen == {"B": 3, "flat": [1, 2, 3, 4, 5, 6, 7, 8, 9], "lengths": [2, 4, 3], "knobs": (3, 5, 4, 2)}
+    assert got == [[0, 1, 2], [100, 101, 102], [200, 201, 202]]
