@@ -398,9 +398,11 @@ def main():
 
     # kernels of ours launched in the timed region: per request the prefill
     # (2 chunks x (rows + embed + 8 per layer) + need + head 3 + finish), begin,
-    # and per packed call pack + embed + 8 per layer + head 3 + publish + commit
+    # and per packed call pack + embed + 7 per layer (RoPE folded into the
+    # attention; 8 with LA_FUSE_ROPE=0) + head 3 + publish + commit
     chunks = (PROMPT_LEN + 255) // 256
-    per_call = 2 + 8 * cfg.n_layers + 3 + 2
+    per_layer_call = 8 if os.environ.get("LA_FUSE_ROPE", "1").startswith("0") else 7
+    per_call = 2 + per_layer_call * cfg.n_layers + 3 + 2
     per_request = chunks * (2 + 8 * cfg.n_layers) + 1 + 3 + 1 + 1
     launches = args.steps * per_request + calls * per_call
     peaks, src = measured_peaks()

@@ -213,7 +213,7 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
                   int max_W, int max_N, int max_G, int max_batch, void* stream,
                   la_ctx** out);
 
-/* Greedy lookahead decoding of B prompts together (M7.3 runs one request
+/* Lookahead decoding of B prompts together (M7.3 runs one request
  * per call in its pinned code, §0x04C, and calls that a property of the
  * code; the state is per request, §0x03B, §0x07).  prompts (host) holds the
  * B prompts back to back, lengths[b] (host) their lengths.  Each packed call
@@ -223,7 +223,10 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
  * weight stream for all requests), then verifies, publishes and advances
  * each request on its own; a request with max_new tokens leaves the batch.
  * Every request's rows see only its own cache and rows, so each output is
- * that request's la_generate (and AR) output.  out (host, B x max_new) gets
+ * that request's la_generate output (greedy: its AR output).  s: NULL for
+ * greedy, else every request samples with s's temperature and top-p and
+ * request b with seed s->seed + b (its la_generate output with that seed).
+ * out (host, B x max_new) gets
  * request b's tokens at out[b*max_new ..].  stats: steps = calls of the
  * request that needed most, tokens = B*max_new.
  * Errors: LA_EINVAL, LA_ECAPACITY (B > max_batch, a prompt + max_new >
@@ -231,7 +234,8 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx,
  * LA_ECUDA, device errors.  Resets request 0's single-request state: a
  * later la_step needs la_prefill first. */
 int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t* lengths,
-                      int max_new, int W, int N, int G, int32_t* out, la_stats* stats);
+                      int max_new, int W, int N, int G, const la_sampling* s, int32_t* out,
+                      la_stats* stats);
 
 /* ---- inspection (tests) -------------------------------------------------- */
 

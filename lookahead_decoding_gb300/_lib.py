@@ -70,8 +70,8 @@ def _load() -> C.CDLL:
                               C.POINTER(vp)]),
         "la_init_batch": (C.c_int, [C.POINTER(la_model_cfg), C.POINTER(la_weights), C.c_int, C.c_int, C.c_int,
                                     C.c_int, C.c_int, vp, C.POINTER(vp)]),
-        "la_generate_batch": (C.c_int, [vp, C.c_int, i32p, i32p, C.c_int, C.c_int, C.c_int, C.c_int, i32p,
-                                        C.POINTER(la_stats)]),
+        "la_generate_batch": (C.c_int, [vp, C.c_int, i32p, i32p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                        C.POINTER(la_sampling), i32p, C.POINTER(la_stats)]),
         "la_prefill": (C.c_int, [vp, i32p, C.c_int, C.POINTER(la_sampling), i32p]),
         "la_step": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), i32p, C.POINTER(C.c_int)]),
         "la_generate": (C.c_int, [vp, i32p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), i32p,
@@ -151,15 +151,17 @@ def la_init(cfg: la_model_cfg, weights: la_weights, max_ctx: int, max_W: int, ma
 
 
 def la_generate_batch(ctx, prompts: Sequence[Sequence[int]], max_new: int, W: int, N: int, G: int,
-                      stats: Optional[la_stats] = None) -> List[List[int]]:
-    """Greedy lookahead of several prompts in batched packed calls."""
+                      sampling=None, stats: Optional[la_stats] = None) -> List[List[int]]:
+    """Lookahead of several prompts in batched packed calls (request b samples with seed + b)."""
     B = len(prompts)
     flat = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in prompts]))
     lengths = np.ascontiguousarray(np.asarray([len(p) for p in prompts], dtype=np.int32))
     out = np.zeros(B * max_new, dtype=np.int32)
     i32 = C.POINTER(C.c_int32)
+    s = _sampling(sampling)
     _check(LIB.la_generate_batch(ctx, B, flat.ctypes.data_as(i32), lengths.ctypes.data_as(i32), max_new, W, N, G,
-                                 out.ctypes.data_as(i32), C.byref(stats) if stats is not None else None),
+                                 C.byref(s) if s else None, out.ctypes.data_as(i32),
+                                 C.byref(stats) if stats is not None else None),
            "la_generate_batch", ctx)
     return [out[b * max_new:(b + 1) * max_new].tolist() for b in range(B)]
 

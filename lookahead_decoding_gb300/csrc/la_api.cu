@@ -128,6 +128,15 @@ static int read_hdr(la_ctx* ctx, LaHdr* h) {
     return LA_OK;
 }
 
+int la_fuse_rope() {
+    static int on = -1;
+    if (on < 0) {
+        const char* e = getenv("LA_FUSE_ROPE");
+        on = (e && e[0] == '0') ? 0 : 1;
+    }
+    return on;
+}
+
 int la_pdl_enabled() {
     static int on = -1;
     if (on < 0) {
@@ -255,10 +264,16 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
         void* vdst = (sel == SEL_PREFILL) ? layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx)
                                           : layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows);
         int stride = (sel == SEL_PREFILL) ? ctx->max_ctx : ln.temp_rows;
-        pi = prof_open(ctx, PK_ROW);
-        la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel, ctx->Qcap,
-                          stride, rc, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr));
-        prof_close(ctx, pi);
+        // decode calls of bf16 models fold RoPE into the attention (LA_FUSE_ROPE=0: a kernel of its own)
+        const bool fuse = ctx->bf16 && ctx->tc && sel != SEL_PREFILL && la_fuse_rope();
+        const LaRope rope{(const __nv_bfloat16*)ctx->qkv, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr), ctx->rcos,
+                          ctx->rsin};
+        if (!fuse) {
+            pi = prof_open(ctx, PK_ROW);
+            la_launch_rope_kv(d, st, c.dtype, ctx->qkv, ctx->rcos, ctx->rsin, ctx->qbuf, kdst, vdst, H, dh, sel,
+                              ctx->Qcap, stride, rc, split_of(ctx, ctx->tc ? &ctx->g_qkv[l] : nullptr));
+            prof_close(ctx, pi);
+        }
         pi = prof_open(ctx, PK_ATTN);
         if (ctx->bf16) {
             CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
@@ -269,7 +284,8 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
                                         ctx->cache_map, ln.cache_row0 + (l * 2 + 0) * H * ctx->max_ctx,
                                         ln.cache_row0 + (l * 2 + 1) * H * ctx->max_ctx, ln.req_hdr, ln.qstride,
                                         (long long)(ctx->cache_bytes_req / ctx->esz),
-                                        c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows));
+                                        c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows,
+                                        la_attn_tail_rows(ctx->max_W, ctx->max_N, ctx->Qmax), fuse ? &rope : nullptr));
         } else {
             CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
                                    layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
@@ -574,7 +590,9 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         if (!r && la_tc_make_map(&ctx->cache_map, ctx->cache, max_batch * c.n_layers * 2 * c.n_heads * max_ctx,
                                  c.head_dim, 128))
             r = LA_ECUDA;
-        if (la_attn_smem_bytes(ctx->attn_TB, ctx->Qmax, ctx->PMAX) > 227 * 1024) r = LA_ENOTSUP;
+        if (la_attn_smem_bytes(ctx->attn_TB, la_attn_tail_rows(max_W, max_N, ctx->Qmax), ctx->PMAX, ctx->Qmax) >
+            227 * 1024)
+            r = LA_ENOTSUP;
     }
     // batched calls: request 0 keeps the state above; requests 1.. get their
     // own header, window, pool, prompt, out ring and commit plan
@@ -733,6 +751,22 @@ int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* sampl
     ctx->prof_samples = 0;
     return LA_OK;
 }
+
+// three timing events, destroyed on every return path
+struct Events3 {
+    cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
+    cudaError_t create() {
+        for (auto& x : e) {
+            cudaError_t r = cudaEventCreate(&x);
+            if (r != cudaSuccess) return r;
+        }
+        return cudaSuccess;
+    }
+    ~Events3() {
+        for (auto& x : e)
+            if (x) cudaEventDestroy(x);
+    }
+};
 
 static int check_sampling(const la_sampling* s) {
     if (!s) return LA_OK;
@@ -895,10 +929,9 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
     }
     if (n + max_new > ctx->max_ctx) return LA_ECAPACITY;
-    cudaEvent_t e0, e1, e2;
-    CK(cudaEventCreate(&e0));
-    CK(cudaEventCreate(&e1));
-    CK(cudaEventCreate(&e2));
+    Events3 ev;
+    CK(ev.create());
+    cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
     CK(cudaEventRecord(e0, ctx->st));
     int r = do_prefill(ctx, prompt, n, s, solo_lane(ctx));
     if (r) return r;
@@ -943,9 +976,6 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         stats->mean_candidates = h.n_steady ? (double)h.sum_Ct / h.n_steady : 0.0;
         stats->mean_rows = h.n_steps ? (double)h.sum_Q / h.n_steps : 0.0;
     }
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaEventDestroy(e2);
     return LA_OK;
 }
 
@@ -962,8 +992,8 @@ int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new, const
 // One batched call of B requests as a graph: every request's pack, one
 // forward and LM head over the stacked slices, every request's publication
 // and commit.
-static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
-    const int key = 0x100 | B;
+static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
+    const int key = 0x100 | B | (sampling << 12);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     const la_model_cfg& c = ctx->cfg;
@@ -974,9 +1004,15 @@ static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
     for (int b = 0; b < B; ++b) la_launch_pack(ctx->req[b], ctx->st);
     const Lane ln = batch_lane(ctx, B);
     r = enqueue_forward(ctx, SEL_CALL, ln);
-    if (!r) r = enqueue_head(ctx, 0, ln);
+    if (!r) r = enqueue_head(ctx, sampling, ln);
+    // sampling: each request's verifier on the logits of its slice of the needed rows
+    for (int b = 0; b < B && !r && sampling; ++b)
+        if (la_launch_sample_verify(ctx->req[b], ctx->st, ctx->logits + (size_t)b * ctx->Qstride * c.vocab, c.vocab, 0) !=
+            cudaSuccess)
+            r = LA_ECUDA;
     for (int b = 0; b < B && !r; ++b)
-        r = enqueue_publish_commit_req(ctx, ctx->req[b], 0, (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
+        r = enqueue_publish_commit_req(ctx, ctx->req[b], sampling,
+                                       (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
                                        (char*)ctx->temp + (size_t)b * ctx->Qstride * head_bytes, ctx->temp_rows);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
@@ -990,8 +1026,9 @@ static int get_batch_graph(la_ctx* ctx, int B, Graph** out) {
 }
 
 int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t* lengths, int max_new, int W, int N,
-                      int G, int32_t* out, la_stats* stats) {
+                      int G, const la_sampling* s, int32_t* out, la_stats* stats) {
     if (!ctx || !prompts || !lengths || !out || B < 1 || max_new < 1) return LA_EINVAL;
+    if (check_sampling(s)) return LA_EINVAL;
     if (ctx->max_batch < 2) return LA_ENOTSUP;
     if (B > ctx->max_batch) return LA_ECAPACITY;
     if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
@@ -1003,20 +1040,26 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     // request 0's single-request state is reused: a later la_step needs a new prefill
     ctx->prefilled = false;
     ctx->begun = false;
-    cudaEvent_t e0, e1, e2;
-    CK(cudaEventCreate(&e0));
-    CK(cudaEventCreate(&e1));
-    CK(cudaEventCreate(&e2));
+    Events3 ev;
+    CK(ev.create());
+    cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
     CK(cudaEventRecord(e0, ctx->st));
+    // sampling: request b draws with seed s->seed + b
+    std::vector<la_sampling> sb(B);
+    for (int b = 0; b < B && s; ++b) {
+        sb[b] = *s;
+        sb[b].seed = s->seed + (uint64_t)b;
+    }
     size_t off = 0;
     for (int b = 0; b < B; ++b) {
-        int r = do_prefill(ctx, prompts + off, lengths[b], nullptr, prefill_lane(ctx, b));
+        int r = do_prefill(ctx, prompts + off, lengths[b], s ? &sb[b] : nullptr, prefill_lane(ctx, b));
         if (r) return r;
         off += (size_t)lengths[b];
     }
     CK(cudaEventRecord(e1, ctx->st));
     for (int b = 0; b < B; ++b)
-        la_launch_begin(ctx->req[b], ctx->st, MODE_LOOKAHEAD, W, N, G, 0, 1.f, 1.f, 0, max_new, (int)ctx->opts);
+        la_launch_begin(ctx->req[b], ctx->st, MODE_LOOKAHEAD, W, N, G, s ? 1 : 0, s ? s->temperature : 1.f,
+                        s ? s->top_p : 1.f, s ? sb[b].seed : 0, max_new, (int)ctx->opts);
     CK(cudaGetLastError());
     LaHdr hb;
     memset(&hb, 0, sizeof(hb));
@@ -1029,7 +1072,7 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     CK(cudaMemcpyAsync(ctx->bd.hdr, &hb, sizeof(hb), cudaMemcpyHostToDevice, ctx->st));
     if (ctx->work.counters) CK(cudaMemsetAsync(ctx->work.counters, 0, sizeof(int) * ctx->work.n_counters, ctx->st));
     Graph* g = nullptr;
-    int r = get_batch_graph(ctx, B, &g);
+    int r = get_batch_graph(ctx, B, s ? 1 : 0, &g);
     if (r) return r;
     LaHdr h;
     CK(cudaMemcpyAsync(&h, ctx->bd.hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
@@ -1073,9 +1116,6 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
         stats->decode_ns = (int64_t)(ms1 * 1e6);
         stats->mean_rows = (double)B * ctx->Qstride;
     }
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaEventDestroy(e2);
     return LA_OK;
 }
 

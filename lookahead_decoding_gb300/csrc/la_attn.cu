@@ -145,9 +145,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // as TMA leaves them (K then V, each two 64-dimension boxes of 128-byte rows,
 // 64 KB per block) or, after the blocks, the tail keys in padded rows.
 struct FusedLayout {
-    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, bar, ssc, ssp, path, total;
+    uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, bar, ssc, ssp, path, uslot, urow, misc, total;
 };
-__host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
+__host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax, int qrows) {
     FusedLayout L;
     L.ring = 0;
     L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;           // K and V rows, bf16
@@ -165,7 +165,10 @@ __host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax) {
     L.ssp = (uint32_t)ring_keys + 4;                                // tail scores: [FR][ssp] fp32
     L.ssc = L.bar + 16;
     L.path = L.ssc + FR * L.ssp * 4;                                // [FR][pmax] int
-    L.total = L.path + (uint32_t)FR * pmax * 4;
+    L.uslot = L.path + (uint32_t)FR * pmax * 4;                     // [qrows] int: ring slot of a temporary row
+    L.urow = L.uslot + (uint32_t)qrows * 4;                         // [qrows] int: temporary row of a slot
+    L.misc = L.urow + (uint32_t)qrows * 4;                          // [4] int: the count of staged rows
+    L.total = L.misc + 16;
     return L;
 }
 
@@ -175,7 +178,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
                                                       int max_ctx, int temp_stride, int TB, int H, int ring_keys,
                                                       const __grid_constant__ CUtensorMap cmap, int krow0, int vrow0,
                                                       const LaHdr* const* req_hdr, int qstride,
-                                                      long long req_cache_elems, int req_cache_rows) {
+                                                      long long req_cache_elems, int req_cache_rows, int qrows,
+                                                      LaRope rope) {
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
     // A batched call stacks its requests' rows in slices of qstride rows (a
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const int PM = d.PMAX;
 
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    const FusedLayout LY = fused_layout(ring_keys, PM);
+    const FusedLayout LY = fused_layout(ring_keys, PM, qrows);
     const uint32_t sraw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - sraw);
@@ -253,13 +257,17 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     la_pdl_wait();
     la_pdl_trigger();
     if (prefill && tid < FR) pos_raw = d.row_pos[r0 + tid];
-    const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
-    for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
-        const int r = i >> 4, c8 = (i & 15) * 8;
-        cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(r0 + r) * DH + c8, 16);
+    const int nr = min(FR, rows - r0);
+    // decode with RoPE folded in: the queries are computed below from the QKV output
+    const bool fuse = rope.qkv != nullptr && !prefill;
+    if (!fuse) {
+        const __nv_bfloat16* qh = qbuf + (size_t)hh * Qcap * DH;
+        for (int i = tid; i < FR * (DH / 8); i += blockDim.x) {
+            const int r = i >> 4, c8 = (i & 15) * 8;
+            cp_async16(sbase + LY.q + (uint32_t)(r * LDK + c8) * 2u, qh + (size_t)(r0 + r) * DH + c8, 16);
+        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    const int nr = min(FR, rows - r0);
     const int K = prefill ? 0 : hr->K;
     const int Q = prefill ? 0 : hr->Q;                // the request's temporary K/V rows
     if (tid < FR) {
@@ -268,6 +276,44 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         rt0[tid] = pos >= 0 ? t0_of(pos, TB) : 0;
     }
     __syncthreads();
+    // RoPE folded in: the tile's queries of head hh into shared memory and,
+    // for the K/V commit, its rows' rotated K and V into the temporary rows
+    // (each (row, head) is written by exactly one CTA; no CTA of this kernel
+    // reads them).  Rows past the call's rows get zero queries.
+    const int HD = H * DH, half = DH / 2;
+    const int seg_q = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, hh) : 1;
+    const int seg_k = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, H + hh) : 1;
+    const int seg_v = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, 2 * H + hh) : 1;
+    if (fuse) {
+        __nv_bfloat16* qs_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
+        __nv_bfloat16* kt_w = const_cast<__nv_bfloat16*>(kt) + (size_t)hh * temp_stride * DH;
+        __nv_bfloat16* vt_w = const_cast<__nv_bfloat16*>(vt) + (size_t)hh * temp_stride * DH;
+        for (int i = tid; i < FR * (half / 4); i += blockDim.x) {
+            const int r = i / (half / 4), c4 = (i % (half / 4)) * 4;
+            __nv_bfloat16* qd = qs_w + r * LDK + c4;
+            if (r >= nr) {
+                *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
+                *reinterpret_cast<uint2*>(qd + half) = make_uint2(0u, 0u);
+                continue;
+            }
+            const int row = r0 + r, pos = rpos[r], lrow = row - req * qstride;
+            const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+            const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+            const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+            const float4 qa = la_qkv_at4(x, row, hh * DH + c4, rope.sp, seg_q);
+            const float4 qb = la_qkv_at4(x, row, hh * DH + c4 + half, rope.sp, seg_q);
+            const float4 ka = la_qkv_at4(x, row, HD + hh * DH + c4, rope.sp, seg_k);
+            const float4 kb = la_qkv_at4(x, row, HD + hh * DH + c4 + half, rope.sp, seg_k);
+            const float4 va = la_qkv_at4(x, row, 2 * HD + hh * DH + c4, rope.sp, seg_v);
+            const float4 vb = la_qkv_at4(x, row, 2 * HD + hh * DH + c4 + half, rope.sp, seg_v);
+            la_rope4_store(qd, qd + half, qa, qb, c, s);
+            __nv_bfloat16* ko = kt_w + (size_t)lrow * DH + c4;
+            __nv_bfloat16* vo = vt_w + (size_t)lrow * DH + c4;
+            la_rope4_store(ko, ko + half, ka, kb, c, s);
+            *reinterpret_cast<uint2*>(vo) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
+            *reinterpret_cast<uint2*>(vo + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+        }
+    }
     int t0max = 0, t0min = 0x7fffffff, posmax = 0;
     for (int r = 0; r < nr; ++r) {
         t0max = max(t0max, rt0[r]);
@@ -432,10 +478,48 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     if (tid == 0 && spec0 && nb == 0 && !mbar_wait(bar0, 0)) la_set_err(d.hdr, LA_ETIMEOUT);
     __syncthreads();      // the ring is free for the tail keys
 
-    // tail keys: committed positions [t0min, Kc) then (in a call) the temporary rows
+    // tail keys: committed positions [t0min, Kc), then (in a call) the
+    // temporary rows on the tile's rows' paths, each once, in row order
+    // (uslot: a temporary row's ring slot past the committed keys; urow: the
+    // inverse).  Which slot a key takes changes no arithmetic: every score
+    // depends only on its query and key, and each row reads its own keys in
+    // position order.
     const int Kc = prefill ? posmax + 1 : K;
     const int nc = (nr > 0 && Kc > t0min) ? Kc - t0min : 0;
-    const int nt = nc + Q;
+    int* uslot = reinterpret_cast<int*>(smem + LY.uslot);
+    int* urow = reinterpret_cast<int*>(smem + LY.urow);
+    int& s_nu = *reinterpret_cast<int*>(smem + LY.misc);
+    if (tid == 0) s_nu = 0;
+    if (Q > 0) {
+        for (int q = tid; q < Q; q += blockDim.x) uslot[q] = 0;
+        __syncthreads();
+        for (int i = tid; i < nr * PM; i += blockDim.x) {
+            const int r = i / PM, e = i % PM, pos = rpos[r];
+            if (pos >= K && e <= pos - K) {
+                const int pr = spath[i];
+                if (pr >= 0 && pr < Q) uslot[pr] = 1;
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {        // slots in row order: a ballot scan over the marks
+            int run = 0;
+            for (int base = 0; base < Q; base += 32) {
+                const int q = base + lane;
+                const bool m = q < Q && uslot[q] != 0;
+                const unsigned bal = __ballot_sync(0xffffffffu, m);
+                const int s = run + __popc(bal & ((1u << lane) - 1u));
+                if (m) { uslot[q] = s; urow[s] = q; }
+                run += __popc(bal);
+            }
+            if (lane == 0) s_nu = run;
+        }
+    }
+    __syncthreads();
+    const int nt = nc + s_nu;
+    if (nt > ring_keys) {       // beyond the ring the launch sized (bounded by construction)
+        if (tid == 0) la_set_err(d.hdr, LA_ECAPACITY);
+        return;
+    }
     const uint32_t tk_a = sbase + LY.ring, tv_a = tk_a + (uint32_t)ring_keys * LDK * 2u;
     {
         const __nv_bfloat16* kth = kt + (size_t)hh * temp_stride * DH;
@@ -445,10 +529,33 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
             const __nv_bfloat16* ksrc;
             const __nv_bfloat16* vsrc;
             if (j < nc) { ksrc = kh + (size_t)(t0min + j) * DH; vsrc = vh + (size_t)(t0min + j) * DH; }
-            else { ksrc = kth + (size_t)(j - nc) * DH; vsrc = vth + (size_t)(j - nc) * DH; }
+            else if (fuse) continue;     // computed below from the QKV output
+            else { const int row = urow[j - nc]; ksrc = kth + (size_t)row * DH; vsrc = vth + (size_t)row * DH; }
             const uint32_t off = (uint32_t)(j * LDK + c8) * 2u;
             cp_async16(tk_a + off, ksrc + c8, 16);
             cp_async16(tv_a + off, vsrc + c8, 16);
+        }
+        if (fuse) {
+            // the in-call keys on the tile's paths: rotated K and V of the
+            // request's row urow[s] at its position, head hh, into slot nc + s
+            __nv_bfloat16* tk_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.ring);
+            __nv_bfloat16* tv_w = tk_w + (size_t)ring_keys * LDK;
+            for (int i = tid; i < (nt - nc) * (half / 4); i += blockDim.x) {
+                const int sl = i / (half / 4), c4 = (i % (half / 4)) * 4;
+                const int row = req * qstride + urow[sl], pos = d.row_pos[row];
+                const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+                const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+                const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+                const float4 ka = la_qkv_at4(x, row, HD + hh * DH + c4, rope.sp, seg_k);
+                const float4 kb = la_qkv_at4(x, row, HD + hh * DH + c4 + half, rope.sp, seg_k);
+                const float4 va = la_qkv_at4(x, row, 2 * HD + hh * DH + c4, rope.sp, seg_v);
+                const float4 vb = la_qkv_at4(x, row, 2 * HD + hh * DH + c4 + half, rope.sp, seg_v);
+                __nv_bfloat16* kd = tk_w + (size_t)(nc + sl) * LDK + c4;
+                __nv_bfloat16* vd = tv_w + (size_t)(nc + sl) * LDK + c4;
+                la_rope4_store(kd, kd + half, ka, kb, c, s);
+                *reinterpret_cast<uint2*>(vd) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
+                *reinterpret_cast<uint2*>(vd + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+            }
         }
         asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
@@ -489,7 +596,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         for (int i = 0; i < MAX_TAIL / 32; ++i) {
             const int j = lane + 32 * i;
             const int p = t0 + j;
-            slot[i] = (j < n) ? ((p < Kr) ? (p - t0min) : (nc + spath[r * PM + (p - K)])) : 0;
+            slot[i] = (j < n) ? ((p < Kr) ? (p - t0min) : (nc + uslot[spath[r * PM + (p - K)]])) : 0;
         }
         __syncwarp();
 #pragma unroll
@@ -565,18 +672,22 @@ static int ring_keys_for(int TB, int Qmax) {
     return tail > 2 * BLK ? tail : 2 * BLK;
 }
 
-size_t la_attn_smem_bytes(int TB, int Qmax, int pmax) {
-    return fused_layout(ring_keys_for(TB, Qmax), pmax).total + 1024;   // + alignment slack
+// tail_rows: the most temporary rows a tile's paths reach (the ring's share
+// for them); qrows: the most temporary rows a request has
+size_t la_attn_smem_bytes(int TB, int tail_rows, int pmax, int qrows) {
+    return fused_layout(ring_keys_for(TB, tail_rows), pmax, qrows).total + 1024;   // + alignment slack
 }
 
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
                                      int krow0, int vrow0, const LaHdr* const* req_hdr, int qstride,
-                                     long long req_cache_elems, int req_cache_rows, int temp_stride) {
+                                     long long req_cache_elems, int req_cache_rows, int temp_stride, int tail_rows,
+                                     const LaRope* rope) {
     if (TB + 1 > MAX_TAIL / 32) return cudaErrorInvalidValue;
-    const int ring_keys = ring_keys_for(TB, Qmax);
-    const size_t smem = la_attn_smem_bytes(TB, Qmax, pmax);
+    if (tail_rows <= 0 || tail_rows > Qmax) tail_rows = Qmax;
+    const int ring_keys = ring_keys_for(TB, tail_rows);
+    const size_t smem = la_attn_smem_bytes(TB, tail_rows, pmax, Qmax);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_attn_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -589,5 +700,6 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
                          (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, (const __nv_bfloat16*)kt,
                          (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx,
                          temp_stride ? temp_stride : Qmax, TB, H, ring_keys,
-                         cmap, krow0, vrow0, req_hdr, qstride, req_cache_elems, req_cache_rows);
+                         cmap, krow0, vrow0, req_hdr, qstride, req_cache_elems, req_cache_rows, Qmax,
+                         rope ? *rope : LaRope{nullptr, LaSplit{}, nullptr, nullptr});
 }

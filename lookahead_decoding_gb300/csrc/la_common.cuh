@@ -117,6 +117,7 @@ __device__ __forceinline__ void la_pdl_trigger() { asm volatile("griddepcontrol.
 
 // 1 unless LA_PDL=0 (A/B runs): launches below carry the attribute
 int la_pdl_enabled();
+int la_fuse_rope();      // decode calls of bf16 models: RoPE folded into the attention
 
 // kernel<<<grid, block, smem, st>>>(args...) with programmatic stream serialisation
 template <typename... KArgs, typename... Args>

@@ -90,6 +90,47 @@ __device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, 
     }
     return r;
 }
+
+// RoPE of bf16 models on four consecutive dimensions i..i+3 (< dh/2) and
+// their rotation partners, shared by the RoPE kernel and the attention that
+// folds it in: values as the QKV GEMM's bf16 store would have rounded them,
+// rotation with explicit roundings (no contraction), so every kernel that
+// applies it gets the same bits.
+__device__ __forceinline__ float la_bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// four consecutive values n .. n+3 (n % 4 == 0) of row q of the QKV output
+__device__ __forceinline__ float4 la_qkv_at4(const __nv_bfloat16* row, int q, int n, const LaSplit& sp, int nseg) {
+    if (nseg <= 1) {
+        const uint2 u = *reinterpret_cast<const uint2*>(row + n);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    const float4 s = la_split_sum4(sp, n >> 7, q >> 8, (size_t)(q & 255) * 128 + (n & 127), nseg);
+    return make_float4(la_bf16_round(s.x), la_bf16_round(s.y), la_bf16_round(s.z), la_bf16_round(s.w));
+}
+
+__device__ __forceinline__ uint2 la_pack_bf16x4(float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    return u;
+}
+
+__device__ __forceinline__ float la_rope_lo(float a, float b, float c, float s) {
+    return __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+}
+__device__ __forceinline__ float la_rope_hi(float a, float b, float c, float s) {
+    return __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
+}
+// (a, b) = dimensions i.. and i+dh/2.. of one head; stores the rotated pair as bf16
+__device__ __forceinline__ void la_rope4_store(__nv_bfloat16* lo, __nv_bfloat16* hi, float4 a, float4 b, float4 c,
+                                               float4 s) {
+    *reinterpret_cast<uint2*>(lo) = la_pack_bf16x4(la_rope_lo(a.x, b.x, c.x, s.x), la_rope_lo(a.y, b.y, c.y, s.y),
+                                                   la_rope_lo(a.z, b.z, c.z, s.z), la_rope_lo(a.w, b.w, c.w, s.w));
+    *reinterpret_cast<uint2*>(hi) = la_pack_bf16x4(la_rope_hi(a.x, b.x, c.x, s.x), la_rope_hi(a.y, b.y, c.y, s.y),
+                                                   la_rope_hi(a.z, b.z, c.z, s.z), la_rope_hi(a.w, b.w, c.w, s.w));
+}
 #endif
 
 void la_launch_rope_table(float* rcos, float* rsin, int n_pos, int dh, double theta, cudaStream_t st);
@@ -167,9 +208,27 @@ cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V,
 
 // bf16 attention: committed 128-position blocks on tensor cores + combine/tail
 int la_attn_tail_blocks(int pmax);
-size_t la_attn_smem_bytes(int TB, int Qmax, int pmax);
+// RoPE folded into the attention of a decode call: the QKV GEMM's output
+// (and its split tiles) and the rotation tables; qkv == nullptr: the queries
+// and temporary K/V come from the RoPE kernel
+struct LaRope {
+    const __nv_bfloat16* qkv;
+    LaSplit sp;
+    const float* rcos;
+    const float* rsin;
+};
+size_t la_attn_smem_bytes(int TB, int tail_rows, int pmax, int qrows);
+// the most temporary rows the paths of one attention tile (16 consecutive
+// packed rows) can reach: base stripe and level 0 (<= W+N-3 cells), each
+// row's own trajectory cells (<= N-2), the verification cells of the
+// candidates the tile touches (<= 16 + N-1), bounded by the call's rows
+inline int la_attn_tail_rows(int max_W, int max_N, int Qmax) {
+    const int u = max_W + 20 * (max_N - 1);
+    return u < Qmax ? u : Qmax;
+}
 cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void* qbuf, const void* kc, const void* vc,
                                      const void* kt, const void* vt, void* out, int H, int sel, int Qcap,
                                      int max_ctx, int Qmax, int rows_cap, int TB, int pmax, const CUtensorMap& cmap,
                                      int krow0, int vrow0, const LaHdr* const* req_hdr = nullptr, int qstride = 0,
-                                     long long req_cache_elems = 0, int req_cache_rows = 0, int temp_stride = 0);
+                                     long long req_cache_elems = 0, int req_cache_rows = 0, int temp_stride = 0,
+                                     int tail_rows = 0, const LaRope* rope = nullptr);

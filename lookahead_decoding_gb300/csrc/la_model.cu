@@ -224,28 +224,6 @@ __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float*
 // partial loads as float4 and in flight before the first store, so the grid
 // (a quarter of the threads of k_rope_kv) is resident at once.  Every output
 // element takes the same arithmetic as in k_rope_kv.
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
-// four consecutive values n .. n+3 (n % 4 == 0) of row q of the QKV output
-// as the GEMM's bf16 store would have rounded them
-__device__ __forceinline__ float4 qkv_at4(const __nv_bfloat16* row, int q, int n, const LaSplit& sp, int nseg) {
-    if (nseg <= 1) {
-        const uint2 u = *reinterpret_cast<const uint2*>(row + n);
-        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-    }
-    const float4 s = la_split_sum4(sp, n >> 7, q >> 8, (size_t)(q & 255) * 128 + (n & 127), nseg);
-    return make_float4(bf16_round(s.x), bf16_round(s.y), bf16_round(s.z), bf16_round(s.w));
-}
-
-__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    return u;
-}
-
 // grid (rows, ceil(H / heads per CTA)); blockDim = heads per CTA x dh/8
 __global__ void __launch_bounds__(256) k_rope_kv4(LaDev d, const __nv_bfloat16* qkv, const float* rcos,
                                                   const float* rsin, __nv_bfloat16* qbuf, __nv_bfloat16* kdst,
@@ -272,23 +250,17 @@ __global__ void __launch_bounds__(256) k_rope_kv4(LaDev d, const __nv_bfloat16* 
     la_pdl_trigger();
     if (hh >= H) return;
     const __nv_bfloat16* row = qkv + (size_t)q * 3 * HD;
-    const float4 qa = qkv_at4(row, q, nq + i, sp, sqa), qb = qkv_at4(row, q, nq + i + half, sp, sqb);
-    const float4 ka = qkv_at4(row, q, nk + i, sp, ska), kb = qkv_at4(row, q, nk + i + half, sp, skb);
-    const float4 va = qkv_at4(row, q, nv + i, sp, sva), vb = qkv_at4(row, q, nv + i + half, sp, svb);
+    const float4 qa = la_qkv_at4(row, q, nq + i, sp, sqa), qb = la_qkv_at4(row, q, nq + i + half, sp, sqb);
+    const float4 ka = la_qkv_at4(row, q, nk + i, sp, ska), kb = la_qkv_at4(row, q, nk + i + half, sp, skb);
+    const float4 va = la_qkv_at4(row, q, nv + i, sp, sva), vb = la_qkv_at4(row, q, nv + i + half, sp, svb);
     __nv_bfloat16* qo = qbuf + ((size_t)hh * Qcap + q) * dh;
-    *reinterpret_cast<uint2*>(qo + i) = pack_bf16x4(qa.x * c.x - qb.x * s.x, qa.y * c.y - qb.y * s.y,
-                                                    qa.z * c.z - qb.z * s.z, qa.w * c.w - qb.w * s.w);
-    *reinterpret_cast<uint2*>(qo + i + half) = pack_bf16x4(qb.x * c.x + qa.x * s.x, qb.y * c.y + qa.y * s.y,
-                                                           qb.z * c.z + qa.z * s.z, qb.w * c.w + qa.w * s.w);
+    la_rope4_store(qo + i, qo + i + half, qa, qb, c, s);
     const int slot = (sel == 1) ? pos : q;
     __nv_bfloat16* ko = kdst + ((size_t)hh * stride + slot) * dh;
     __nv_bfloat16* vo = vdst + ((size_t)hh * stride + slot) * dh;
-    *reinterpret_cast<uint2*>(ko + i) = pack_bf16x4(ka.x * c.x - kb.x * s.x, ka.y * c.y - kb.y * s.y,
-                                                    ka.z * c.z - kb.z * s.z, ka.w * c.w - kb.w * s.w);
-    *reinterpret_cast<uint2*>(ko + i + half) = pack_bf16x4(kb.x * c.x + ka.x * s.x, kb.y * c.y + ka.y * s.y,
-                                                           kb.z * c.z + ka.z * s.z, kb.w * c.w + ka.w * s.w);
-    *reinterpret_cast<uint2*>(vo + i) = pack_bf16x4(va.x, va.y, va.z, va.w);
-    *reinterpret_cast<uint2*>(vo + i + half) = pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+    la_rope4_store(ko + i, ko + i + half, ka, kb, c, s);
+    *reinterpret_cast<uint2*>(vo + i) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
+    *reinterpret_cast<uint2*>(vo + i + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
 }
 
 // SwiGLU of the gate/up GEMM's split tiles: act = silu(gate) * up with gate

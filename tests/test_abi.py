@@ -50,7 +50,7 @@ def test_generate_batch_marshalling(monkeypatch):
     seen = {}
 
     class Stub:
-        def la_generate_batch(self, ctx, B, flat, lengths, max_new, W, N, G, out, stats):
+        def la_generate_batch(self, ctx, B, flat, lengths, max_new, W, N, G, sampling, out, stats):
             seen.update(B=B, flat=[flat[i] for i in range(9)], lengths=[lengths[i] for i in range(B)],
                         knobs=(max_new, W, N, G))
             for b in range(B):

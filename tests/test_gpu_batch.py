@@ -75,3 +75,17 @@ def test_batch_errors(batched):
         L.la_generate_batch(ctx.ctx, [p] * 4, 16, 4, 3, 4)           # more requests than the context holds
     with pytest.raises(LaError):
         L.la_generate_batch(ctx.ctx, [p, [1] * 500], 16, 4, 3, 4)    # prompt + max_new above max_ctx
+
+
+def test_batch_sampling_equals_each_request_alone(batched):
+    """Sampling in a batch: request b, drawing with seed + b, emits exactly its
+    solo sampled la_generate output with that seed (same logits rows, same
+    Philox counters)."""
+    L, ctx = batched
+    ps = prompts(51)
+    T, top_p, seed = 0.8, 0.9, 700
+    solo = [L.la_generate(ctx.ctx, p, 40, 8, 5, 8, sampling=(T, top_p, seed + b)) for b, p in enumerate(ps)]
+    got = L.la_generate_batch(ctx.ctx, ps, 40, 8, 5, 8, sampling=(T, top_p, seed))
+    assert got == solo
+    again = L.la_generate_batch(ctx.ctx, ps, 40, 8, 5, 8, sampling=(T, top_p, seed))
+    assert again == got

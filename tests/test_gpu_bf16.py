@@ -231,3 +231,92 @@ def test_7b_shapes_logits_against_oracle(shallow):
         run.commit(rows, info.commit_rows)
         assert em == info.emitted
     L.la_set_debug(ctx.ctx, 0)
+
+
+# ---- the W x N sweep (W in {1, 3, 7, 15, 31}, N in {3, 5, 7}, G = W) ----------
+
+@pytest.fixture(scope="module")
+def sweep():
+    """The small bf16 model in a context sized for the largest sweep point
+    (W = 31, N = 7, G = 31: up to 388 rows per call)."""
+    from lookahead_decoding_gb300 import lib
+    w = {k: v.to("cuda:0") for k, v in synth.llama_weights(MID, 0).items()}
+    ctx = context(MID, w, max_ctx=1400, W=31, N=7, G=31)
+    yield lib(), ctx
+    ctx.close()
+
+
+def test_sweep_points_equal_ar(sweep):
+    """Every sweep point on a 1024-token Markov prompt, 256 new tokens: the
+    lookahead output is the AR output."""
+    L, ctx = sweep
+    p = synth.markov_zipf_prompt(MID.vocab, 1024, 5).tolist()
+    ar = L.la_generate_ar(ctx.ctx, p, 256)
+    for W in (1, 3, 7, 15, 31):
+        for N in (3, 5, 7):
+            assert L.la_generate(ctx.ctx, p, 256, W, N, W) == ar, (W, N)
+
+
+# ---- the 13B shapes and the code-like workload -----------------------------
+
+@pytest.fixture(scope="module")
+def shallow13():
+    """One layer of the 13B shapes (d 5120, 40 heads of 128, FFN 13824, vocab 32000)."""
+    from lookahead_decoding_gb300 import lib
+    cfg = synth.ModelConfig(n_layers=1, d_model=5120, n_heads=40, head_dim=128, d_ffn=13824, vocab=32000)
+    w = synth.llama_weights(cfg, 0, device="cuda:0")
+    ctx = context(cfg, w, max_ctx=512, W=10, N=5, G=10)
+    yield lib(), ctx, cfg, w
+    ctx.close()
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_13b_shapes_logits_against_oracle(shallow13):
+    """Full-size 13B rows at 3e-2: the prefill row and every needed row of the
+    first packed calls of a code-like prompt (W=10, N=5, G=10)."""
+    L, ctx, cfg, w = shallow13
+    oracle = OracleModel(cfg, w, compute_dtype=np.float64, store="bf16")
+    p = synth.code_like_prompt(cfg.vocab, 48, 13).tolist()
+    L.la_set_debug(ctx.ctx, 1)
+    first = L.la_prefill(ctx.ctx, p)
+    lg, _ = L.la_debug_logits(ctx.ctx, 2, cfg.vocab)
+    cache, ref = oracle.prefill(p)
+    assert np.max(np.abs(lg[0] - ref[-1])) < LOGIT_TOL
+    st = la.LookaheadState(p, first, 10, 5, 10)
+    run = la.make_runner(oracle, cache, "meta")
+    for step in range(5):
+        rows, guesses = st.plan()
+        refl = run.run(rows)
+        em = L.la_step(ctx.ctx, 10, 5, 10)
+        lg, need = L.la_debug_logits(ctx.ctx, 1024, cfg.vocab)
+        assert need.tolist() == [r.packed_index for r in rows if r.request_logit]
+        err = np.max(np.abs(lg - refl[need]))
+        assert err < LOGIT_TOL, (step, err)
+        argmax = [int(np.argmax(x)) for x in refl]
+        for i, r in enumerate(need):
+            argmax[r] = int(np.argmax(lg[i]))
+        info = st.publish(rows, guesses, argmax)
+        run.commit(rows, info.commit_rows)
+        assert em == info.emitted
+    L.la_set_debug(ctx.ctx, 0)
+
+
+def test_13b_code_like_lookahead_equals_ar():
+    """The 13B code-like workload at full size: 40 layers, a 2048-token prompt
+    with 30 % copied spans, 512 new tokens, W=10, N=5, G=10."""
+    from lookahead_decoding_gb300 import lib
+    L = lib()
+    cfg = synth.LLAMA_13B
+    w = synth.llama_weights(cfg, 0, device="cuda:0")
+    ctx = context(cfg, w, max_ctx=2600, W=10, N=5, G=10)
+    try:
+        p = synth.code_like_prompt(cfg.vocab, 2048, 3).tolist()
+        ar = L.la_generate_ar(ctx.ctx, p, 512)
+        st = L.la_stats()
+        assert L.la_generate(ctx.ctx, p, 512, 10, 5, 10, stats=st) == ar
+        assert st.steps < 512
+    finally:
+        ctx.close()
+        del w
+        torch.cuda.empty_cache()
