@@ -49,6 +49,37 @@ def test_rope_properties():
     assert abs(d1 - d2) < 1e-12
 
 
+@pytest.mark.parametrize("dh,anchors", [
+    # dh = 8, theta = 1e4: the pair-i frequency theta^(-2i/dh) = 10^(-i), i = 0..3
+    (8, {0: 1.0, 1: 0.1, 2: 0.01, 3: 0.001}),
+    # dh = 128, theta = 1e4: 10^(-i/16); the decades fall at i = 16, 32, 48
+    (128, {0: 1.0, 1: 10 ** (-1 / 16), 2: 10 ** (-2 / 16), 3: 10 ** (-3 / 16),
+           16: 0.1, 32: 0.01, 48: 0.001, 63: 10 ** (-63 / 16)}),
+])
+@pytest.mark.parametrize("pos", [1, 5, 517])
+def test_rope_frequency_schedule_hand_values(dh, anchors, pos):
+    """RoFormer's rotary embedding (Su et al., eq. 15, rotate-half pairing as in
+    Llama): the unit vector on dimension i (< dh/2) at position pos becomes
+    cos(pos*f_i) on dimension i and sin(pos*f_i) on its partner i + dh/2, with
+    f_i = theta^(-2i/dh).  The frequencies are written out by hand above (for
+    theta = 10^4 they are powers of ten), so a wrong exponent such as -i/dh or
+    -2i/(dh-2), a swapped pair or a flipped sign fails here at every pos >= 1."""
+    half = dh // 2
+    for i, f in anchors.items():
+        e = np.zeros((1, 1, dh))
+        e[0, 0, i] = 1.0
+        y = rope(e, np.array([pos]), 10000.0)[0, 0]
+        want = np.zeros(dh)
+        want[i] = math.cos(pos * f)
+        want[i + half] = math.sin(pos * f)
+        assert np.allclose(y, want, rtol=0, atol=1e-12), (dh, i, pos)
+        # the partner dimension turns the other way: e_{i+half} -> (-sin, cos)
+        e2 = np.zeros((1, 1, dh))
+        e2[0, 0, i + half] = 1.0
+        y2 = rope(e2, np.array([pos]), 10000.0)[0, 0]
+        assert abs(y2[i] + math.sin(pos * f)) < 1e-12 and abs(y2[i + half] - math.cos(pos * f)) < 1e-12
+
+
 def test_bf16_round_matches_torch():
     x = np.random.default_rng(2).normal(size=4096) * 10.0 ** np.random.default_rng(3).integers(-8, 8, 4096)
     ours = bf16_round(x)
