@@ -144,6 +144,12 @@ typedef struct {
 } la_stats;
 
 /* Create a context on the current CUDA device.
+ * Defines the inputs of the method (break the sequential dependency, App. A,
+ * the lookahead decoding algorithm: a model, the n-gram size N, the window
+ * size W, the speculation limit G) and the state it keeps across calls
+ * (M7.3 §0x07: the stable K/V prefix, the ordinary frontier and the packed
+ * workspace of temporary rows; §0x03B: the keyed n-gram pool; §0x01A: the
+ * window, pool and backend manifest fixed for a round).
  *   cfg, w        : model (see above); weights are borrowed device memory.
  *   max_ctx       : largest committed length (prompt + generated tokens).
  *   max_W, max_N, max_G : largest lookahead knobs any later call may use
@@ -169,6 +175,10 @@ int la_set_options(la_ctx* ctx, uint32_t flags);
 
 /* Prefill the prompt (host ids, n >= 1, each in [0, vocab)) with one causal
  * forward; resets the K/V cache, the window, the pool and the step counter.
+ * This is the state before the first target call of M7.3 §0x03A (window and
+ * pool lifecycle) and §0x06B: the committed K/V covers the prompt and the
+ * first output token is one ahead of it, to be the next call's ordinary
+ * input.
  * *first_token (host) receives the first generated token (argmax of the last
  * prompt row, or a draw from it when `s` is not NULL).  Errors: LA_EINVAL,
  * LA_ECAPACITY (n > max_ctx - 1), LA_ECUDA, LA_EDEVICE. */
@@ -186,7 +196,12 @@ int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s,
 int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s,
             int32_t* out, int* n_out);
 
-/* Prefill + lookahead steps until max_new tokens (the prefill's token
+/* The whole decoding loop of M7.3 §0x06 (loop pseudocode; break the
+ * sequential dependency §3 and App. A, the lookahead decoding algorithm with
+ * prompt, model, N, W, G and a step limit): la_prefill, then the
+ * warm-up fills and steady calls of la_step (M7.3 §0x03A, steps 1-8, each
+ * published fail-closed, §0x06A, §0x07) until max_new tokens.
+ * Prefill + lookahead steps until max_new tokens (the prefill's token
  * included) have been produced; out (host, capacity >= max_new) receives
  * exactly max_new tokens (*n_out = max_new).  Steps run as captured CUDA
  * graphs without host synchronisation between them.  stats may be NULL. */
@@ -196,7 +211,11 @@ int la_generate(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
 
 /* The same as la_generate but with plain autoregressive decoding (one row
  * per call) on the same kernels: the baseline the method must equal
- * (greedy) and beat. */
+ * (greedy) and beat.  M7.3 §0x02A: greedy Jacobi iteration reaches the
+ * autoregressive greedy fixed point, so lookahead output must equal this
+ * call's output token for token; break the sequential dependency §1 and §5
+ * measure speedup against this decoding; §3.3 and App. B make sampled
+ * lookahead output follow this call's sampling distribution. */
 int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new,
                    const la_sampling* s, int32_t* out, int* n_out, la_stats* stats);
 
@@ -259,7 +278,13 @@ int la_set_debug(la_ctx* ctx, int flags);
 int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* samples);
 
 /* fp32 logits [*n_rows][vocab] of the last call's needed rows and their
- * packed row indices.  host buffers of capacity cap_rows rows. */
+ * packed row indices.  host buffers of capacity cap_rows rows.
+ * The needed rows are those whose outputs the step reads (M7.3 §0x04A row
+ * compiler output slices; §0x05C row ledger): the ordinary row, the deepest
+ * trajectory level's rows (the new n-gram ends) and every verification row.
+ * Requires la_set_debug bit 0 before the call; *n_rows is set even when
+ * the buffers are too small.  Errors: LA_EINVAL (null ctx or n_rows),
+ * LA_ESTATE (debug bit 0 off), LA_ECAPACITY (cap_rows < *n_rows), LA_ECUDA. */
 int la_debug_logits(la_ctx* ctx, float* logits, int32_t* rows, int cap_rows, int* n_rows);
 
 /* Snapshot of the request state after the last call (host buffers):
