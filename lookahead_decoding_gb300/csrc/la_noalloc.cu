@@ -10,17 +10,24 @@
 // byte it needs from a fixed array compiled into the library.
 //
 // The scratch is one file-scope __device__ array per device, of
-// LA_NOALLOC_SCRATCH_BYTES.  Its address is looked up once per device (the
-// first call made while that device is current), together with the kernel's
-// shared-memory opt-in; that first call should therefore come before any
-// stream capture on the device.  A problem whose split-tile partial sums do
-// not fit is rejected with LA_ECAPACITY before any device work.
+// LA_NOALLOC_SCRATCH_BYTES.  Host code cannot use the array's name as a
+// device address, so every call, with the caller's device current, asks the
+// runtime for the array's address on that device (cudaGetSymbolAddress) and
+// sets the kernel's shared-memory opt-in there.  Doing both on every call
+// rather than caching them keeps a call correct after the caller resets the
+// device (the module, and with it the array, may then load elsewhere).  The
+// first call on a device loads the library's device code there; make it
+// before any stream capture on that device.  A problem whose split-tile
+// partial sums do not fit is rejected with LA_ECAPACITY before any device
+// work.
 //
 // What must start at zero: the header's status word and the per-tile arrival
-// counters.  Each call zeroes both with a small kernel on the caller's stream
-// before the GEMM launch (the counters also return to zero at the end of a
-// successful launch); the partial-sum region needs no initialisation, since
-// every slot read in a launch is written earlier in the same launch.
+// counters.  The counters only grow during a launch (a tile's contributors
+// each add to its counter and wait for the full count), so each call must
+// zero both before its GEMM starts: a small kernel on the caller's stream
+// does that before every launch.  The partial-sum region needs no
+// initialisation, since every slot read in a launch is written earlier in
+// the same launch.
 //
 // One scratch region per device means two executions that overlap on a
 // device would race on its partial sums and counters.  The call therefore
@@ -44,7 +51,6 @@ static __device__ __align__(256) unsigned char g_scratch[LA_NOALLOC_SCRATCH_BYTE
 constexpr size_t HDR_BYTES = (sizeof(LaHdr) + 255) & ~(size_t)255;
 
 std::mutex g_lock;
-void* g_base[LA_NOALLOC_MAX_DEVICES];
 
 __global__ void k_noalloc_reset(LaHdr* h, int* counters, int n_counters, int rows) {
     int* w = (int*)h;
@@ -54,16 +60,14 @@ __global__ void k_noalloc_reset(LaHdr* h, int* counters, int n_counters, int row
     if (threadIdx.x == 0) h->n_need = rows;
 }
 
-// Once per device: the scratch address and the GEMM's shared-memory opt-in.
+// Per call, on the current device: the scratch array's device address and
+// the GEMM's shared-memory opt-in.
 int setup_device(int dev, void** base) {
     if (dev < 0 || dev >= LA_NOALLOC_MAX_DEVICES) return LA_ENOTSUP;
-    if (!g_base[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LA_ECUDA;
-        if (la_tc_prepare_device() != cudaSuccess) return LA_ECUDA;
-        g_base[dev] = p;
-    }
-    *base = g_base[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return LA_ECUDA;
+    if (la_tc_prepare_device() != cudaSuccess) return LA_ECUDA;
+    *base = p;
     return LA_OK;
 }
 
@@ -123,15 +127,22 @@ int la_gemm_noalloc(int mode, const void* w, const void* w2, int n_out, int K, c
     memset(&d, 0, sizeof(d));
     d.hdr = hdr;
 
+    // From the reset launch on, every return first waits for the stream, with
+    // the lock still held, so that no work of this call can still be running
+    // on the shared array when the next call resets it.
+    auto fail = [&]() {
+        cudaStreamSynchronize(st);
+        return LA_ECUDA;
+    };
     k_noalloc_reset<<<1, 256, 0, st>>>(hdr, counters, (int)n_counters, rows);
-    if (cudaGetLastError() != cudaSuccess) return LA_ECUDA;
+    if (cudaGetLastError() != cudaSuccess) return fail();
     // the GEMM reads the header's row count before its dependency wait, so
     // the reset must have completed before the GEMM launches
-    if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ECUDA;
-    if (la_launch_gemm_tc(d, st, g, wk, SEL_NEED, rows) != cudaSuccess) return LA_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return fail();
+    if (la_launch_gemm_tc(d, st, g, wk, SEL_NEED, rows) != cudaSuccess) return fail();
     int err = 0;
-    if (cudaMemcpyAsync(&err, &hdr->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return LA_ECUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ECUDA;
+    if (cudaMemcpyAsync(&err, &hdr->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return fail();
+    if (cudaStreamSynchronize(st) != cudaSuccess) return fail();
     return err ? err : LA_OK;
 }
 
