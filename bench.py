@@ -36,6 +36,8 @@ if ROOT not in sys.path:
 
 W_, N_, G_ = 15, 5, 15
 PROMPT_LEN, MAX_NEW = 512, 256
+# the headline metric, printed identically by both arms
+METRIC = "committed tokens/s @ batch 1 (7B-shape bf16), tokens/step, % step roofline"
 
 
 def algorithmic_bytes_per_call(cfg, K_in: float, Q: float) -> float:
@@ -62,11 +64,31 @@ def gemm_bytes_per_call(cfg, Q: float, need_rows: float) -> float:
     return L * per_layer + head
 
 
-# DRAM bytes (read + write) of the GEMM launches of one packed call (32 layers
-# x (QKV + O + gate/up + down) + LM head), from the ncu capture of the current
-# kernel's launches in a decode call summarised in profiles/; None once the
-# kernel changes.
-GEMM_TRAFFIC_PER_CALL = 13.608e9
+def kernel_source_digest(files) -> str:
+    """sha256 (first 16 hex digits) of the named CUDA sources, concatenated in
+    order: identifies the kernel build a DRAM-traffic capture belongs to."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "lookahead_decoding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(profile: str, files):
+    """DRAM bytes per call of the dominant kernel from the committed ncu summary
+    `profiles/<profile>`: its line `traffic_bytes_per_call: <bytes> source_digest:
+    <digest>`.  None when the file is missing or the kernel sources have changed
+    since the capture (the digest no longer matches)."""
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None, None
+    want = kernel_source_digest(files)
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and parts[0] == "traffic_bytes_per_call:" and parts[2] == "source_digest:":
+            return (float(parts[1]) if parts[3] == want else None), parts[3]
+    return None, None
 
 
 def aggregate_replicas(new_tokens: float, decode_s: float, wall: float, device: str = "cpu"):
@@ -97,11 +119,13 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int, path: str):
-        self.path = path
+    def __init__(self, index: int):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="la_clocks_", suffix=".csv")
+        os.close(fd)
         self.proc = None
         try:
-            self.f = open(path, "w")
+            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
@@ -117,7 +141,12 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        return parse_clocks(self.path)
+        out = parse_clocks(self.path)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        return out
 
 
 def parse_clocks(path: str):
@@ -141,16 +170,23 @@ def parse_clocks(path: str):
             "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(cfg, weights, min_s: float = 10.0, max_calls: int = 64, prompt_len: int = 24):
+def oracle_model(cfg, weights):
+    """The oracle transformer in the configuration the CPU baseline times
+    (fp32 arithmetic, bf16 storage emulation, weights converted once)."""
+    import numpy as np
+    from oracle.model import OracleModel
+    return OracleModel(cfg, weights, compute_dtype=np.float32, store="bf16", cache_weights=True)
+
+
+def cpu_oracle_sample(cfg, weights, min_s: float = 10.0, max_calls: int = 64, prompt_len: int = 24, model=None):
     """The oracle (as it stands) on the host cores: a bounded sample of the same
     workload — prefill of a short Markov prompt (not timed), then packed
     lookahead calls at W=15, N=5, G=15 until `min_s` seconds of them have run
     (at most `max_calls`); returns committed tokens/s of those calls."""
-    import numpy as np
     import synth
     from oracle import lookahead as la
-    from oracle.model import OracleModel, argmax_lowest
-    m = OracleModel(cfg, weights, compute_dtype=np.float32, store="bf16", cache_weights=True)
+    from oracle.model import argmax_lowest
+    m = model if model is not None else oracle_model(cfg, weights)
     p = synth.markov_zipf_prompt(cfg.vocab, prompt_len, 2).tolist()
     cache, lg = m.prefill(p)                    # also converts and caches the weights (not timed)
     st = la.LookaheadState(p, argmax_lowest(lg[-1]), W_, N_, G_)
@@ -207,9 +243,12 @@ def run_sweep(args, cfg, rank: int, local: int) -> None:
             except L.LaError as e:
                 points.append({"W": W, "N": N, "G": W, "unsupported": str(e)})
                 continue
+            # AR on the same context: the attention's key split is fixed per
+            # context by its largest path length, so outputs are compared
+            # within one context
+            st = L.la_stats()
+            ar_out = L.la_generate_ar(ctx.ctx, prompt, args.max_new, stats=st)
             if ar_ms is None:
-                st = L.la_stats()
-                ar_out = L.la_generate_ar(ctx.ctx, prompt, args.max_new, stats=st)
                 ar_ms = st.decode_ns * 1e-6 / st.steps
             L.la_generate(ctx.ctx, prompt, args.max_new, W, N, W)          # warm-up (graph capture)
             st = L.la_stats()
@@ -220,6 +259,7 @@ def run_sweep(args, cfg, rank: int, local: int) -> None:
             points.append({"W": W, "N": N, "G": W, "call_ms": call_ms, "tokens_per_call": (st.tokens - 1) / st.steps,
                            "tokens_per_s": (st.tokens - 1) / (st.decode_ns * 1e-9), "mean_rows": st.mean_rows,
                            "step_roofline_frac": bytes_call / (call_ms * 1e-3) / 1e9 / peak,
+                           "mean_candidates": st.mean_candidates, "emitted_hist": list(st.emitted_hist)[:N],
                            "equals_ar": out == ar_out})
             ctx.close()
     line = {"metric": "W x N sweep (7B-shape bf16, greedy)", "unit": "ms per packed call", "n_gpus": 1,
@@ -247,8 +287,7 @@ def run_batch(args, cfg, rank: int, local: int) -> None:
     prompts = batch_prompts(cfg.vocab, B)
     for _ in range(args.warmup):
         L.la_generate_batch(ctx.ctx, prompts, args.max_new, W_, N_, G_)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    clocks = ClockSampler(local)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     stats, outs = [], []
@@ -273,11 +312,174 @@ def run_batch(args, cfg, rank: int, local: int) -> None:
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
             "call_latency_ms": decode_s / calls * 1e3, "calls_per_request": calls / args.steps,
             "batched_equals_ar": all(o == ar for o in outs),
+            "gpu_launches": sum(s.kernel_launches for s in stats),
             "e2e": {"value": B * args.max_new * args.steps / wall, "unit": "tokens/s",
                     "h2d_bytes_per_step": B * PROMPT_LEN * 4, "d2h_bytes_per_step": B * args.max_new * 4},
             "clocks": clk}
     ctx.close()
     print(json.dumps(line))
+
+
+# The single-request workloads: the headline (the pages' plain configuration
+# on the 7B shape) and two where the n-gram pool retrieves candidates the
+# model accepts (pool seeding on the same prompt; the copy-heavy 13B prompt).
+WORKLOADS = {
+    "headline": {"desc": "llama-7b-shape bf16, batch 1, prompt 512 Markov/Zipf(1.1), 256 new tokens, greedy, "
+                         "W=15 N=5 G=15", "model": "llama-7b-shape (random init)", "prompt": "markov",
+                 "prompt_len": PROMPT_LEN, "max_new": MAX_NEW, "seed": 2, "knobs": (W_, N_, G_), "options": 0,
+                 "cfg": "LLAMA_7B"},
+    "pool-seeded": {"desc": "llama-7b-shape bf16, batch 1, prompt 512 Markov/Zipf(1.1), 256 new tokens, greedy, "
+                            "W=15 N=5 G=15, pool seeded from the prompt and every output token",
+                    "model": "llama-7b-shape (random init)", "prompt": "markov", "prompt_len": PROMPT_LEN,
+                    "max_new": MAX_NEW, "seed": 2, "knobs": (W_, N_, G_), "options": 3, "cfg": "LLAMA_7B"},
+    "code-13b": {"desc": "llama-13b-shape bf16, batch 1, code-like prompt 2048 (30% copied 8-32-token spans), "
+                         "512 new tokens, greedy, W=10 N=5 G=10", "model": "llama-13b-shape (random init)",
+                 "prompt": "code", "prompt_len": 2048, "max_new": 512, "seed": 4, "knobs": (10, 5, 10),
+                 "options": 0, "cfg": "LLAMA_13B"},
+}
+SPEC_HBM_GBS = 8000.0
+# the dominant kernel of a packed call: its kind in the kernel-timing totals,
+# the committed ncu summary holding its DRAM traffic, and the sources that
+# summary's digest covers
+DOMINANT = {"kind": "gemm", "profile": "k_gemm_tc_llama7b_decode_call.md",
+            "sources": ["la_gemm_tc.cu", "la_common.cuh", "la_kernels.h"],
+            "what": "k_gemm_tc (tcgen05 GEMMs: QKV, O, gate/up, down per layer + LM head), per call: "
+                    "algorithmic bytes / summed launch time"}      # the nominal HBM3e bandwidth the step roofline is also quoted against
+
+
+def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
+    """One request at a time through la_generate (graph per packed call):
+    committed tokens/s of the decode calls, acceptance, the step roofline, AR
+    on the same kernels, per-kind kernel times and the end-to-end rate."""
+    import torch
+    import synth
+    from lookahead_decoding_gb300 import lib
+    L = lib()
+    W, N, G = wl["knobs"]
+    max_new = args.max_new if args.workload == "headline" else wl["max_new"]
+    plen = wl["prompt_len"]
+    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}")
+    ctx = L.Context(cfg, w, max_ctx=max(1024, plen + max_new + 64), max_W=W, max_N=N, max_G=G)
+    if wl["options"]:
+        L.la_set_options(ctx.ctx, wl["options"])
+    if wl["prompt"] == "markov":
+        prompt = synth.markov_zipf_prompt(cfg.vocab, plen, wl["seed"]).tolist()
+    else:
+        prompt = synth.code_like_prompt(cfg.vocab, plen, wl["seed"]).tolist()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        L.la_generate(ctx.ctx, prompt, max_new, W, N, G)
+    clocks = ClockSampler(local)
+    barrier()
+    t0 = time.perf_counter()
+    stats = []
+    outs = []
+    for _ in range(args.steps):
+        st = L.la_stats()
+        outs.append(L.la_generate(ctx.ctx, prompt, max_new, W, N, G, stats=st))
+        stats.append(st)
+    barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+
+    decode_s = sum(s.decode_ns for s in stats) * 1e-9
+    calls = sum(s.steps for s in stats)
+    new_tokens = sum(s.tokens - 1 for s in stats)      # tokens of the packed calls (the first comes from the prefill)
+    tps = new_tokens / decode_s
+    call_ms = decode_s / calls * 1e3
+    if world > 1:
+        tot_tok, max_dec, wall = aggregate_replicas(new_tokens, decode_s, wall, f"cuda:{local}")
+        tps = tot_tok / max_dec
+
+    # autoregressive decode on the same kernels and context
+    ar_stats = []
+    for _ in range(args.ar_steps):
+        st = L.la_stats()
+        ar = L.la_generate_ar(ctx.ctx, prompt, max_new, stats=st)
+        ar_stats.append(st)
+    ar_tps = (sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)) if ar_stats else None
+    ar_ms = (sum(s.decode_ns for s in ar_stats) * 1e-6 / sum(s.steps for s in ar_stats)) if ar_stats else None
+    same = all(o == ar for o in outs) if ar_stats else None
+
+    # Live kernel timing of the same workload (one more request, with the
+    # step graph bracketing every launch by CUDA events on the library's
+    # stream).  The brackets serialise launches that otherwise overlap, so
+    # the per-kind figures are upper bounds that need not add up to a call.
+    L.la_set_debug(ctx.ctx, 4)
+    st_prof = L.la_stats()
+    L.la_generate(ctx.ctx, prompt, max_new, W, N, G, stats=st_prof)
+    prof = L.la_profile_read(ctx.ctx)
+    L.la_set_debug(ctx.ctx, 0)
+
+    launches = sum(s.kernel_launches for s in stats)        # counted by the library
+    peaks, src = measured_peaks()
+    mean_K = plen + max_new / 2.0
+    mean_Q = statistics.mean(s.mean_rows for s in stats)
+    mean_ct = statistics.mean(s.mean_candidates for s in stats)
+    hist = [sum(s.emitted_hist[i] for s in stats) for i in range(16)]
+    bytes_call = algorithmic_bytes_per_call(cfg, mean_K, mean_Q)
+    step_achieved = bytes_call / (call_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    samples = max(1, prof["samples"])
+    dom = DOMINANT
+    dom_ms_call = prof["ms"][dom["kind"]] / samples
+    dom_launches_call = prof["launches"][dom["kind"]] / samples
+    dom_bytes = gemm_bytes_per_call(cfg, mean_Q, 1 + W + mean_ct * (N - 1))
+    dom_achieved = dom_bytes / (dom_ms_call * 1e-3) / 1e9 if dom_ms_call > 0 else None
+    traffic, digest = captured_traffic(dom["profile"], dom["sources"]) if args.workload == "headline" else (None, None)
+    line = {
+        "metric": METRIC if args.workload == "headline" else f"{METRIC} [{args.workload}]",
+        "value": tps,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config,
+        "tokens_per_call": new_tokens / calls,
+        "accepted_tokens_per_step": new_tokens / calls,
+        "mean_candidates": mean_ct,
+        "emitted_hist": hist[:N],
+        "call_latency_ms": call_ms,
+        "prefill_ms": statistics.mean(s.prefill_ns for s in stats) * 1e-6,
+        "mean_rows_per_call": mean_Q,
+        "ar_tokens_per_s": ar_tps,
+        "ar_call_latency_ms": ar_ms,
+        "speedup_vs_ar": tps / ar_tps if (world == 1 and ar_tps) else None,
+        "lookahead_equals_ar": same,
+        "e2e": {"value": (max_new * args.steps * world) / wall, "unit": "tokens/s",
+                "h2d_bytes_per_step": plen * 4, "d2h_bytes_per_step": max_new * 4},
+        "roofline": {"bound": "hbm", "achieved": dom_achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (dom_achieved / peak) if dom_achieved else None,
+                     "traffic": traffic,
+                     "traffic_source": (f"ncu capture in profiles/{dom['profile']} (kernel sources {digest})"
+                                        if traffic else "no capture of this kernel build"),
+                     "kernel": dom["what"],
+                     "launches_per_call": dom_launches_call, "ms_per_call": dom_ms_call,
+                     "algorithmic_bytes_per_call": dom_bytes, "peak_source": src + " (copy bandwidth)",
+                     "timing": f"CUDA events around each launch in the step graph, {prof['samples']} sampled steps"},
+        "step_roofline": {"achieved": step_achieved, "frac": step_achieved / peak,
+                          "frac_of_spec_8tbs": step_achieved / SPEC_HBM_GBS,
+                          "algorithmic_bytes_per_call": bytes_call,
+                          "what": "whole packed call: weights once + committed K/V read + temporary K/V written"},
+        "kernel_ms_per_call": {k: v / samples for k, v in prof["ms"].items()},
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and not args.no_cpu_baseline and args.workload == "headline":
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, w)
+    ctx.close()
+    return line
 
 
 def main():
@@ -293,6 +495,8 @@ def main():
                     help="profiling runs: a model with this many layers of the same shapes (0 = all 32)")
     ap.add_argument("--batch", type=int, default=1,
                     help="requests per packed call (la_generate_batch); 1 = the headline single-request bench")
+    ap.add_argument("--workload", default="headline", choices=sorted(WORKLOADS),
+                    help="single-request workload: the headline, or one where the pool retrieves accepted candidates")
     ap.add_argument("--sweep", action="store_true",
                     help="the W x N sweep on the 7B shape (W in 1,3,7,15,31; N in 3,5,7; G=W): one JSON line")
     args = ap.parse_args()
@@ -317,12 +521,13 @@ def main():
             return
         dev = "cuda:0" if torch.cuda.is_available() else "cpu"
         w = synth.llama_weights(cfg, 0, device=dev)
-        vals = []
-        for _ in range(max(1, args.warmup)):
-            pass          # the oracle has no warm-up state; warm-up runs would only repeat the sample
-        samples = [cpu_oracle_sample(cfg, w, min_s=8.0) for _ in range(max(1, args.steps))]
+        m = oracle_model(cfg, w)
+        # warm-up steps: one packed call each (weights converted, caches warm)
+        for _ in range(args.warmup):
+            cpu_oracle_sample(cfg, w, min_s=0.0, max_calls=1, model=m)
+        samples = [cpu_oracle_sample(cfg, w, min_s=8.0, model=m) for _ in range(max(1, args.steps))]
         v = statistics.mean(s["value"] for s in samples)
-        line = {"impl": "reference", "metric": "committed tokens/s", "value": v, "unit": "tokens/s",
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
                 "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
                 "cpu_baseline": dict(samples[-1], value=v),
@@ -341,124 +546,14 @@ def main():
     torch.cuda.set_device(local)
     from lookahead_decoding_gb300 import build
     build()
-    from lookahead_decoding_gb300 import lib
-    L = lib()
-    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}")
-    ctx = L.Context(cfg, w, max_ctx=1024, max_W=W_, max_N=N_, max_G=G_)
-    prompt = synth.markov_zipf_prompt(cfg.vocab, PROMPT_LEN, 2).tolist()
-
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-
-    for _ in range(args.warmup):
-        L.la_generate(ctx.ctx, prompt, args.max_new, W_, N_, G_)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
-    barrier()
-    t0 = time.perf_counter()
-    stats = []
-    outs = []
-    for _ in range(args.steps):
-        st = L.la_stats()
-        outs.append(L.la_generate(ctx.ctx, prompt, args.max_new, W_, N_, G_, stats=st))
-        stats.append(st)
-    barrier()
-    wall = time.perf_counter() - t0
-    clk = clocks.stop()
-
-    decode_s = sum(s.decode_ns for s in stats) * 1e-9
-    calls = sum(s.steps for s in stats)
-    new_tokens = sum(s.tokens - 1 for s in stats)      # tokens of the packed calls (the first comes from the prefill)
-    tps = new_tokens / decode_s
-    call_ms = decode_s / calls * 1e3
-    # aggregate over ranks: total tokens / max time
-    if world > 1:
-        tot_tok, max_dec, wall = aggregate_replicas(new_tokens, decode_s, wall, f"cuda:{local}")
-        tps = tot_tok / max_dec
-
-    # autoregressive decode on the same kernels
-    ar_stats = []
-    for _ in range(args.ar_steps):
-        st = L.la_stats()
-        ar = L.la_generate_ar(ctx.ctx, prompt, args.max_new, stats=st)
-        ar_stats.append(st)
-    ar_tps = (sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)) if ar_stats else None
-    same = all(o == ar for o in outs) if ar_stats else None
-
-    # Live kernel timing of the same workload (one more request, with the
-    # step graph bracketing every launch by CUDA events on the library's
-    # stream): the GEMM family is the dominant kernel.
-    L.la_set_debug(ctx.ctx, 4)
-    st_prof = L.la_stats()
-    L.la_generate(ctx.ctx, prompt, args.max_new, W_, N_, G_, stats=st_prof)
-    prof = L.la_profile_read(ctx.ctx)
-    L.la_set_debug(ctx.ctx, 0)
-
-    # kernels of ours launched in the timed region: per request the prefill
-    # (2 chunks x (rows + embed + 8 per layer) + need + head 3 + finish), begin,
-    # and per packed call pack + embed + 7 per layer (RoPE folded into the
-    # attention; 8 with LA_FUSE_ROPE=0) + head 3 + publish + commit
-    chunks = (PROMPT_LEN + 255) // 256
-    per_layer_call = 8 if os.environ.get("LA_FUSE_ROPE", "1").startswith("0") else 7
-    per_call = 2 + per_layer_call * cfg.n_layers + 3 + 2
-    per_request = chunks * (2 + 8 * cfg.n_layers) + 1 + 3 + 1 + 1
-    launches = args.steps * per_request + calls * per_call
-    peaks, src = measured_peaks()
-    mean_K = PROMPT_LEN + args.max_new / 2.0
-    mean_Q = statistics.mean(s.mean_rows for s in stats)
-    mean_ct = statistics.mean(s.mean_candidates for s in stats)
-    bytes_call = algorithmic_bytes_per_call(cfg, mean_K, mean_Q)
-    step_achieved = bytes_call / (call_ms * 1e-3) / 1e9
-    peak = float(peaks["hbm_gbs"])
-    samples = max(1, prof["samples"])
-    gemm_ms_call = prof["ms"]["gemm"] / samples
-    gemm_launches_call = prof["launches"]["gemm"] / samples
-    gemm_bytes = gemm_bytes_per_call(cfg, mean_Q, 1 + W_ + mean_ct * (N_ - 1))
-    gemm_achieved = gemm_bytes / (gemm_ms_call * 1e-3) / 1e9 if gemm_ms_call > 0 else None
-    kernel_ms_call = {k: v / samples for k, v in prof["ms"].items()}
-    line = {
-        "metric": "committed tokens/s @ batch 1 (7B-shape bf16)",
-        "value": tps * (1 if world == 1 else 1),
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": wall / args.steps * 1e3,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": config,
-        "tokens_per_call": new_tokens / calls,
-        "call_latency_ms": call_ms,
-        "prefill_ms": statistics.mean(s.prefill_ns for s in stats) * 1e-6,
-        "mean_rows_per_call": mean_Q,
-        "ar_tokens_per_s": ar_tps,
-        "speedup_vs_ar": tps / ar_tps if (world == 1 and ar_tps) else None,
-        "lookahead_equals_ar": same,
-        "e2e": {"value": (args.max_new * args.steps * world) / wall, "unit": "tokens/s",
-                "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": args.max_new * 4},
-        "roofline": {"bound": "hbm", "achieved": gemm_achieved, "peak": peak, "unit": "GB/s",
-                     "frac": (gemm_achieved / peak) if gemm_achieved else None,
-                     "traffic": GEMM_TRAFFIC_PER_CALL,
-                     "kernel": "k_gemm_tc (tcgen05 GEMMs: QKV, O, gate/up, down per layer + LM head), "
-                               "per call: algorithmic bytes / summed launch time",
-                     "launches_per_call": gemm_launches_call, "ms_per_call": gemm_ms_call,
-                     "algorithmic_bytes_per_call": gemm_bytes, "peak_source": src + " (copy bandwidth)",
-                     "timing": f"CUDA events around each launch in the step graph, {prof['samples']} sampled steps"},
-        "step_roofline": {"achieved": step_achieved, "frac": step_achieved / peak,
-                          "algorithmic_bytes_per_call": bytes_call,
-                          "what": "whole packed call: weights once + committed K/V read + temporary K/V written"},
-        "kernel_ms_per_call": kernel_ms_call,
-        "clocks": clk,
-        "gpu_launches": launches,
-    }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(cfg, w)
-    ctx.close()
+    wl = WORKLOADS[args.workload]
+    if args.workload != "headline":
+        cfg = getattr(synth, wl["cfg"])
+        if args.layers:
+            import dataclasses
+            cfg = dataclasses.replace(cfg, n_layers=args.layers)
+        config = dict(config, workload=wl["desc"], model=wl["model"], seq_len=wl["prompt_len"] + wl["max_new"])
+    line = run_single(args, cfg, config, wl, rank, local, world)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

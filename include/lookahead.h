@@ -141,6 +141,8 @@ typedef struct {
     int32_t emitted_hist[16];   /* calls that emitted 1, 2, ... tokens (E_t = a+1) */
     double  mean_candidates;    /* mean C_t over steady calls */
     double  mean_rows;          /* mean Q over calls */
+    int64_t kernel_launches;    /* kernels of this library the call enqueued (a graph
+                                   execution counts every kernel node it runs) */
 } la_stats;
 
 /* Create a context on the current CUDA device.
@@ -268,6 +270,22 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
  * records add a little time to every step: time whole steps with it off. */
 int la_set_debug(la_ctx* ctx, int flags);
 
+/* flags bit 3: keep the residual stream of every layer for la_debug_hidden
+ * (the first call with it allocates (n_layers+1) x rows x d_model floats).
+ * Unknown bits: LA_EINVAL. */
+
+/* fp32 residual rows [rows][d_model] (host) of the last pass (prefill chunk
+ * or packed call) at the input of decoder layer `layer` (0 .. n_layers-1:
+ * the embedding plus every earlier layer's attention and MLP updates), or,
+ * for layer == n_layers, the final residual before the final RMSNorm, which
+ * is complete only on the rows whose logits the call reads.  This is the
+ * stream of the decoder of break the sequential dependency §2 that every
+ * packed row runs through unchanged (M7.3 §0x04); tests feed it to the
+ * oracle layer by layer.  Requires la_set_debug bit 3 before the pass.
+ * Errors: LA_EINVAL, LA_ESTATE (bit 3 off), LA_ECAPACITY (rows above the
+ * row buffers), LA_ECUDA. */
+int la_debug_hidden(la_ctx* ctx, int layer, float* host, int rows);
+
 /* Per-kind kernel-timing totals since the last read (then reset):
  *   ms4[k], launches4[k] (host, 4 entries each): k = 0 tensor-core GEMMs,
  *   1 attention (block and combine kernels, timed together per layer),
@@ -376,11 +394,12 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
  *   y     (device) as above, 4-byte aligned
  *   stream  cudaStream_t the work is ordered on (NULL: the legacy stream)
  * n_out a multiple of 128, K a multiple of 64 (>= 64), 1 <= rows <= 1024.  The call
- * returns once the result is in y.  The first call on a device (the current
- * one) looks up the workspace address and sets the kernel's shared-memory
- * limit there; make it before any stream capture on that device.  The
- * counters and status word must be zero when the GEMM starts: the call zeroes
- * them itself on `stream` before each launch.  There is one workspace per
+ * returns once the result is in y.  Every call looks up the workspace's
+ * address on the current device and sets the kernel's shared-memory limit
+ * there; the first call on a device also loads the library's device code
+ * there, so make it before any stream capture on that device.  The counters
+ * and status word must be zero when the GEMM starts: the call zeroes them
+ * itself on `stream` before each launch.  There is one workspace per
  * device, so two executions overlapping on a device would race on it; calls
  * hold a process-wide lock until their work has finished, which keeps them
  * from overlapping.  Errors: LA_EINVAL (argument, alignment), LA_ECAPACITY

@@ -22,7 +22,8 @@ LA_F32, LA_BF16 = 0, 1
 EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", "la_set_debug", "la_debug_logits",
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
            "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
-           "la_gemm_noalloc", "la_profile_read", "la_set_options", "la_init_batch", "la_generate_batch"]
+           "la_gemm_noalloc", "la_profile_read", "la_set_options", "la_init_batch", "la_generate_batch",
+           "la_debug_hidden"]
 
 # pool seeding options (la_set_options)
 LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT, LA_OPT_SLICE_WINDOW = 1, 2, 4
@@ -49,7 +50,8 @@ class la_sampling(C.Structure):
 
 class la_stats(C.Structure):
     _fields_ = [("steps", C.c_int64), ("tokens", C.c_int64), ("prefill_ns", C.c_int64), ("decode_ns", C.c_int64),
-                ("emitted_hist", C.c_int32 * 16), ("mean_candidates", C.c_double), ("mean_rows", C.c_double)]
+                ("emitted_hist", C.c_int32 * 16), ("mean_candidates", C.c_double), ("mean_rows", C.c_double),
+                ("kernel_launches", C.c_int64)]
 
 
 class LaError(RuntimeError):
@@ -82,6 +84,7 @@ def _load() -> C.CDLL:
         "la_set_options": (C.c_int, [vp, C.c_uint32]),
         "la_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
         "la_debug_logits": (C.c_int, [vp, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
+        "la_debug_hidden": (C.c_int, [vp, C.c_int, f32p, C.c_int]),
         "la_debug_state": (C.c_int, [vp, i32p, i32p, i32p, i32p, i32p, i32p]),
         "la_debug_pool": (C.c_int, [vp, C.c_int, i32p, C.POINTER(C.c_int)]),
         "la_step_inject": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), C.c_int, i32p, f32p, i32p,
@@ -240,6 +243,14 @@ def la_debug_logits(ctx, cap_rows: int, vocab: int):
     _check(LIB.la_debug_logits(ctx, logits.ctypes.data_as(C.POINTER(C.c_float)),
                                rows.ctypes.data_as(C.POINTER(C.c_int32)), cap_rows, C.byref(n)), "la_debug_logits", ctx)
     return logits[: n.value], rows[: n.value]
+
+
+def la_debug_hidden(ctx, layer: int, rows: int, d_model: int):
+    """fp32 residual rows [rows][d_model] at the input of `layer` in the last
+    pass (layer == n_layers: the final residual); needs debug bit 3."""
+    x = np.zeros((rows, d_model), dtype=np.float32)
+    _check(LIB.la_debug_hidden(ctx, layer, x.ctypes.data_as(C.POINTER(C.c_float)), rows), "la_debug_hidden", ctx)
+    return x
 
 
 HDR_KEYS = ["K", "x_t", "W", "N", "G", "n_levels", "step", "Q", "C_t", "a", "winner", "n_out", "err", "steady",

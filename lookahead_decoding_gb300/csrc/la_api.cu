@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <string>
@@ -20,6 +21,7 @@ struct Graph {
     cudaGraph_t g = nullptr;
     cudaGraphExec_t x = nullptr;
     int prof_begin = 0, prof_end = 0;   // the graph's timing event pairs (kernel-timing graphs)
+    long long n_kernels = 0;            // kernel launches one execution runs
 };
 
 // kernel kinds of the kernel-timing mode
@@ -30,7 +32,12 @@ struct ProfPair {
     int kind = 0;
 };
 
+std::atomic<unsigned long long> g_launches{0};
+
 }  // namespace
+
+void la_note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+unsigned long long la_launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 struct la_ctx {
     la_model_cfg cfg{};
@@ -82,6 +89,7 @@ struct la_ctx {
     int W = 0, N = 0, G = 0, mode = 0, sampling = 0;
     int prompt_len = 0;
     int debug = 0;
+    float* dbg_hidden = nullptr;      // [n_layers + 1][Qcap][d_model] fp32 (debug bit 3)
     std::map<int, Graph> graphs;
 
     // kernel-timing mode (debug bit 2): event pairs recorded inside the step graph
@@ -247,6 +255,9 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
         la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->attn_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc,
                           split_of(ctx, (ctx->tc && l > 0) ? &ctx->g_down[l - 1] : nullptr));
         prof_close(ctx, pi);
+        if ((ctx->debug & 8) && ctx->dbg_hidden)     // layer l's input residual rows (complete after this RMSNorm)
+            CK(cudaMemcpyAsync(ctx->dbg_hidden + (size_t)l * ctx->Qcap * dm, ctx->x, sizeof(float) * (size_t)rc * dm,
+                               cudaMemcpyDeviceToDevice, st));
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_qkv[l], ctx->work, sel, rc));
@@ -336,6 +347,9 @@ static int enqueue_head(la_ctx* ctx, int keep_logits, const Lane& ln) {
     la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->fnorm, ctx->hn, c.d_model, c.rms_eps, SEL_NEED, 1, rc,
                       split_of(ctx, ctx->tc ? &ctx->g_down[c.n_layers - 1] : nullptr));
     prof_close(ctx, pi);
+    if ((ctx->debug & 8) && ctx->dbg_hidden)         // the final residual (complete on the needed rows)
+        CK(cudaMemcpyAsync(ctx->dbg_hidden + (size_t)c.n_layers * ctx->Qcap * c.d_model, ctx->x,
+                           sizeof(float) * (size_t)std::min(rc, ctx->Qcap) * c.d_model, cudaMemcpyDeviceToDevice, st));
     if (ctx->tc) {
         TcGemm g = ctx->g_head;
         g.logits = keep_logits ? ctx->logits : nullptr;
@@ -391,14 +405,16 @@ static int enqueue_step(la_ctx* ctx) {
 }
 
 static int get_graph(la_ctx* ctx, Graph** out) {
-    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4);
+    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4) | (ctx->debug & 8);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     Graph g;
     CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
     ctx->prof_capture = (ctx->debug & 4) != 0;
     g.prof_begin = (int)ctx->prof.size();
+    const unsigned long long n0 = la_launch_count();
     int r = enqueue_step(ctx);
+    g.n_kernels = (long long)(la_launch_count() - n0);
     ctx->prof_capture = false;
     g.prof_end = (int)ctx->prof.size();
     cudaGraph_t graph = nullptr;
@@ -734,8 +750,24 @@ int la_query(la_ctx* ctx, int32_t* s) {
 }
 
 int la_set_debug(la_ctx* ctx, int flags) {
-    if (!ctx) return LA_EINVAL;
+    if (!ctx || (flags & ~(1 | 4 | 8))) return LA_EINVAL;
+    if ((flags & 8) && !ctx->dbg_hidden) {
+        const size_t bytes = sizeof(float) * (size_t)(ctx->cfg.n_layers + 1) * ctx->Qcap * ctx->cfg.d_model;
+        int r = dalloc(ctx, (void**)&ctx->dbg_hidden, bytes);
+        if (r) return r;
+    }
     ctx->debug = flags;
+    return LA_OK;
+}
+
+int la_debug_hidden(la_ctx* ctx, int layer, float* host, int rows) {
+    if (!ctx || !host || layer < 0 || layer > ctx->cfg.n_layers || rows < 1) return LA_EINVAL;
+    if (!(ctx->debug & 8) || !ctx->dbg_hidden) return LA_ESTATE;
+    if (rows > ctx->Qcap) return LA_ECAPACITY;
+    const size_t dm = ctx->cfg.d_model;
+    CK(cudaMemcpyAsync(host, ctx->dbg_hidden + (size_t)layer * ctx->Qcap * dm, sizeof(float) * (size_t)rows * dm,
+                       cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
     return LA_OK;
 }
 
@@ -933,6 +965,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
     CK(ev.create());
     cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
     CK(cudaEventRecord(e0, ctx->st));
+    const unsigned long long n0 = la_launch_count();
     int r = do_prefill(ctx, prompt, n, s, solo_lane(ctx));
     if (r) return r;
     ctx->prefilled = true;
@@ -945,6 +978,8 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
     r = get_graph(ctx, &g);
     if (r) return r;
     const int per_step_max = (mode == MODE_LOOKAHEAD) ? N : 1;
+    const long long direct = (long long)(la_launch_count() - n0);
+    long long graph_runs = 0;
     LaHdr h;
     r = read_hdr(ctx, &h);
     if (r) return r;
@@ -953,6 +988,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         int remaining = max_new - h.n_out;
         int launches = std::max(1, (remaining + per_step_max - 1) / per_step_max);
         for (int i = 0; i < launches; ++i) CK(cudaGraphLaunch(g->x, ctx->st));
+        graph_runs += launches;
         r = read_hdr(ctx, &h);
         if (r) return r;
         prof_collect(ctx, *g);
@@ -975,6 +1011,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         for (int i = 0; i < 16; ++i) stats->emitted_hist[i] = h.hist[i];
         stats->mean_candidates = h.n_steady ? (double)h.sum_Ct / h.n_steady : 0.0;
         stats->mean_rows = h.n_steps ? (double)h.sum_Q / h.n_steps : 0.0;
+        stats->kernel_launches = direct + graph_runs * g->n_kernels;
     }
     return LA_OK;
 }
@@ -1000,6 +1037,7 @@ static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
     const size_t head_bytes = (size_t)c.head_dim * ctx->esz;
     Graph g;
     CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
+    const unsigned long long n0 = la_launch_count();
     int r = LA_OK;
     for (int b = 0; b < B; ++b) la_launch_pack(ctx->req[b], ctx->st);
     const Lane ln = batch_lane(ctx, B);
@@ -1014,6 +1052,7 @@ static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
         r = enqueue_publish_commit_req(ctx, ctx->req[b], sampling,
                                        (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
                                        (char*)ctx->temp + (size_t)b * ctx->Qstride * head_bytes, ctx->temp_rows);
+    g.n_kernels = (long long)(la_launch_count() - n0);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
     if (r) { if (graph) cudaGraphDestroy(graph); return r; }
@@ -1044,6 +1083,7 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     CK(ev.create());
     cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
     CK(cudaEventRecord(e0, ctx->st));
+    const unsigned long long n0 = la_launch_count();
     // sampling: request b draws with seed s->seed + b
     std::vector<la_sampling> sb(B);
     for (int b = 0; b < B && s; ++b) {
@@ -1071,6 +1111,8 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     hb.done = (max_new <= 1);
     CK(cudaMemcpyAsync(ctx->bd.hdr, &hb, sizeof(hb), cudaMemcpyHostToDevice, ctx->st));
     if (ctx->work.counters) CK(cudaMemsetAsync(ctx->work.counters, 0, sizeof(int) * ctx->work.n_counters, ctx->st));
+    const long long direct = (long long)(la_launch_count() - n0);
+    long long graph_runs = 0;
     Graph* g = nullptr;
     int r = get_batch_graph(ctx, B, s ? 1 : 0, &g);
     if (r) return r;
@@ -1083,6 +1125,7 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
         // a call appends 1 .. N tokens to every live request
         const int launches = std::max(1, (max_new - least + N - 1) / N);
         for (int i = 0; i < launches; ++i) CK(cudaGraphLaunch(g->x, ctx->st));
+        graph_runs += launches;
         CK(cudaMemcpyAsync(&h, ctx->bd.hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
         for (int b = 0; b < B; ++b)
             CK(cudaMemcpyAsync(&hr[b], ctx->req[b].hdr, sizeof(LaHdr), cudaMemcpyDeviceToHost, ctx->st));
@@ -1115,6 +1158,7 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
         stats->prefill_ns = (int64_t)(ms0 * 1e6);
         stats->decode_ns = (int64_t)(ms1 * 1e6);
         stats->mean_rows = (double)B * ctx->Qstride;
+        stats->kernel_launches = direct + graph_runs * g->n_kernels;
     }
     return LA_OK;
 }

@@ -119,6 +119,11 @@ __device__ __forceinline__ void la_pdl_trigger() { asm volatile("griddepcontrol.
 int la_pdl_enabled();
 int la_fuse_rope();      // decode calls of bf16 models: RoPE folded into the attention
 
+// Process-wide count of kernel launches the library has enqueued (a launch
+// recorded into a CUDA graph counts once, at capture).
+void la_note_launch();
+unsigned long long la_launch_count();
+
 // kernel<<<grid, block, smem, st>>>(args...) with programmatic stream serialisation
 template <typename... KArgs, typename... Args>
 static inline cudaError_t la_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -133,7 +138,9 @@ static inline cudaError_t la_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) la_note_launch();
+    return e;
 }
 
 // Spin limit of every bounded device wait (iterations of mbarrier.try_wait,

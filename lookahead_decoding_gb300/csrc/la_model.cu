@@ -614,10 +614,11 @@ void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* q
     }
     const int rh = (H % 4 == 0) ? 4 : 1;      // heads per CTA
     dim3 g(rows_cap, H / rh);
-    if (dtype == LA_F32)
+    if (dtype == LA_F32) {
         k_rope_kv<float><<<g, rh * dh / 2, 0, st>>>(d, (const float*)qkv, rcos, rsin, (float*)qbuf, (float*)kdst,
                                                     (float*)vdst, H, dh, sel, Qcap, stride, sp);
-    else
+        la_note_launch();
+    } else
         la_launch_pdl(k_rope_kv<__nv_bfloat16>, g, dim3(rh * dh / 2), 0, st, d, (const __nv_bfloat16*)qkv, rcos, rsin,
                       (__nv_bfloat16*)qbuf, (__nv_bfloat16*)kdst, (__nv_bfloat16*)vdst, H, dh, sel, Qcap, stride, sp);
 }
@@ -645,6 +646,7 @@ static cudaError_t attn_t(const LaDev& d, cudaStream_t st, const void* qbuf, con
     dim3 g(H, (rows_cap + RPC - 1) / RPC);
     kern<<<g, 256, smem, st>>>(d, (const T*)qbuf, (const T*)kc, (const T*)vc, (const T*)kt, (const T*)vt, (T*)out, H,
                                 sel, Qcap, max_ctx, Qmax, 1.0f / sqrtf((float)DH));
+    la_note_launch();
     return cudaGetLastError();
 }
 
@@ -671,6 +673,7 @@ static void gemm_ffma_t(const LaDev& d, cudaStream_t st, int mode, const void* X
         case GEMM_SWIGLU: k_gemm_ffma<T, GEMM_SWIGLU><<<g, 256, 0, st>>>(d, (const T*)X, ldx, (const T*)Wm, (const T*)W2, K, Nout, out, ldo, sel); break;
         case GEMM_LOGITS: k_gemm_ffma<T, GEMM_LOGITS><<<g, 256, 0, st>>>(d, (const T*)X, ldx, (const T*)Wm, nullptr, K, Nout, out, ldo, sel); break;
     }
+    la_note_launch();
 }
 void la_launch_gemm_ffma(const LaDev& d, cudaStream_t st, int dtype, int mode, const void* X, int ldx, const void* Wm,
                          const void* W2, int K, int Nout, void* out, int ldo, int sel, int rows_cap) {
@@ -680,6 +683,7 @@ void la_launch_gemm_ffma(const LaDev& d, cudaStream_t st, int dtype, int mode, c
 
 void la_launch_argmax_rows(const LaDev& d, cudaStream_t st, const float* logits, int V, int sel, int rows_cap) {
     k_argmax_rows<<<rows_cap, 256, 0, st>>>(d, logits, V, sel);
+    la_note_launch();
 }
 void la_launch_argmax_reduce(const LaDev& d, cudaStream_t st, const float* pv, const int* pi, int n_tiles, int stride,
                              int sel, int rows_cap) {

@@ -461,8 +461,11 @@ __global__ void k_prefill_finish(LaDev d, int P, int sampled_token_valid) {
 void la_launch_begin(const LaDev& d, cudaStream_t st, int mode, int W, int N, int G, int sampling,
                      float temperature, float top_p, uint64_t seed, int max_out, int opts) {
     k_begin<<<1, 128, 0, st>>>(d, mode, W, N, G, sampling, temperature, top_p,
-                               (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), max_out, opts);
-    if (mode == MODE_LOOKAHEAD && opts) k_pool_seed<<<1, 1024, 0, st>>>(d);
+                               (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), max_out, opts); la_note_launch();
+    if (mode == MODE_LOOKAHEAD && opts) {
+        k_pool_seed<<<1, 1024, 0, st>>>(d);
+        la_note_launch();
+    }
 }
 void la_launch_pack(const LaDev& d, cudaStream_t st) { la_launch_pdl(k_pack, dim3(1), dim3(256), 0, st, d); }
 void la_launch_publish(const LaDev& d, cudaStream_t st, int verdict_given) {
@@ -475,14 +478,14 @@ void la_launch_commit(const LaDev& d, cudaStream_t st, void* cache, void* temp, 
 }
 void la_launch_inject_map(const LaDev& d, cudaStream_t st, const int32_t* argmax_rows, const float* logits_rows,
                           float* logits_need, int V) {
-    k_inject_map<<<logits_rows ? 64 : 1, 256, 0, st>>>(d, argmax_rows, logits_rows, logits_need, V);
+    k_inject_map<<<logits_rows ? 64 : 1, 256, 0, st>>>(d, argmax_rows, logits_rows, logits_need, V); la_note_launch();
 }
 void la_launch_prefill_rows(const LaDev& d, cudaStream_t st, int c0, int n) {
-    k_prefill_rows<<<(n + 255) / 256, 256, 0, st>>>(d, c0, n);
+    k_prefill_rows<<<(n + 255) / 256, 256, 0, st>>>(d, c0, n); la_note_launch();
 }
 void la_launch_prefill_need(const LaDev& d, cudaStream_t st, int last_local) {
-    k_prefill_need<<<1, 1, 0, st>>>(d, last_local);
+    k_prefill_need<<<1, 1, 0, st>>>(d, last_local); la_note_launch();
 }
 void la_launch_prefill_finish(const LaDev& d, cudaStream_t st, int P) {
-    k_prefill_finish<<<1, 1, 0, st>>>(d, P, 1);
+    k_prefill_finish<<<1, 1, 0, st>>>(d, P, 1); la_note_launch();
 }

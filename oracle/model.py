@@ -159,49 +159,70 @@ class OracleModel:
         (logits, new_k, new_v) in call order.
         """
         cfg = self.cfg
-        H, dh = cfg.n_heads, cfg.head_dim
         toks = [np.asarray(c[0], dtype=np.int64) for c in calls]
         offs = np.cumsum([0] + [len(t) for t in toks])
         tokens = np.concatenate(toks)
         positions = np.concatenate([np.asarray(c[1], dtype=np.int64) for c in calls])
-        Q = len(tokens)
-        allowed = []
+        groups = []
         for (_, _, cache, allowed_new), b in zip(calls, range(len(calls))):
             Qb = int(offs[b + 1] - offs[b])
-            allowed.append(np.concatenate([np.ones((Qb, len(cache)), dtype=bool),
-                                           np.asarray(allowed_new, dtype=bool)], axis=1))
+            allowed = np.concatenate([np.ones((Qb, len(cache)), dtype=bool),
+                                      np.asarray(allowed_new, dtype=bool)], axis=1)
+            groups.append((slice(int(offs[b]), int(offs[b + 1])), cache, allowed))
         emb = self.w("tok_emb")
         x = emb[tokens].astype(self.dt)
         new_k = [[] for _ in calls]
         new_v = [[] for _ in calls]
-        scale = 1.0 / math.sqrt(dh)
         for l in range(cfg.n_layers):
-            xn = self._st(rmsnorm(x, self.w(f"l{l}.attn_norm"), cfg.rms_eps))
-            q = self._st(xn @ self.w(f"l{l}.wq").T).reshape(Q, H, dh)
-            k = self._st(xn @ self.w(f"l{l}.wk").T).reshape(Q, H, dh)
-            v = self._st(xn @ self.w(f"l{l}.wv").T).reshape(Q, H, dh)
-            q = self._st(rope(q, positions, cfg.rope_theta))
-            k = self._st(rope(k, positions, cfg.rope_theta))
-            o = np.empty((Q, H, dh), dtype=self.dt)
-            for b, (_, _, cache, _) in enumerate(calls):
-                rows = slice(int(offs[b]), int(offs[b + 1]))
-                kb, vb = k[rows], v[rows]
-                new_k[b].append(kb)
-                new_v[b].append(vb)
-                K = kb if len(cache) == 0 else np.concatenate([cache.k[l], kb], axis=0)
-                V = vb if len(cache) == 0 else np.concatenate([cache.v[l], vb], axis=0)
-                for h in range(H):
-                    s = (q[rows, h, :] @ K[:, h, :].T) * scale             # [Q_b, K_b+Q_b]
-                    s = np.where(allowed[b], s, -np.inf)
-                    o[rows, h, :] = softmax_rows(s) @ V[:, h, :]
-            o = self._st(o.reshape(Q, H * dh))
-            x = x + o @ self.w(f"l{l}.wo").T
-            hn = self._st(rmsnorm(x, self.w(f"l{l}.mlp_norm"), cfg.rms_eps))
-            a = self._st(silu(hn @ self.w(f"l{l}.w_gate").T) * (hn @ self.w(f"l{l}.w_up").T))
-            x = x + a @ self.w(f"l{l}.w_down").T
-        xf = self._st(rmsnorm(x, self.w("final_norm"), cfg.rms_eps))
-        logits = xf @ self.w("lm_head").T
+            x, kl, vl = self.block(l, x, positions, groups)
+            for b in range(len(calls)):
+                new_k[b].append(kl[b])
+                new_v[b].append(vl[b])
+        logits = self.head(x)
         return [(logits[int(offs[b]):int(offs[b + 1])], new_k[b], new_v[b]) for b in range(len(calls))]
+
+    def block(self, l: int, x: np.ndarray, positions, groups):
+        """Decoder layer ``l`` on the residual rows ``x`` [Q, d] at ``positions``.
+
+        ``groups`` lists, per request, (row slice, committed cache, visibility
+        [Q_b, len(cache) + Q_b]); a request's rows attend to its own cache at
+        layer ``l`` and its own new rows only.  Returns (x after the layer,
+        per-request new K rows [Q_b, H, dh], per-request new V rows).
+        """
+        cfg = self.cfg
+        H, dh = cfg.n_heads, cfg.head_dim
+        Q = x.shape[0]
+        scale = 1.0 / math.sqrt(dh)
+        xn = self._st(rmsnorm(x, self.w(f"l{l}.attn_norm"), cfg.rms_eps))
+        q = self._st(xn @ self.w(f"l{l}.wq").T).reshape(Q, H, dh)
+        k = self._st(xn @ self.w(f"l{l}.wk").T).reshape(Q, H, dh)
+        v = self._st(xn @ self.w(f"l{l}.wv").T).reshape(Q, H, dh)
+        q = self._st(rope(q, positions, cfg.rope_theta))
+        k = self._st(rope(k, positions, cfg.rope_theta))
+        o = np.empty((Q, H, dh), dtype=self.dt)
+        ks, vs = [], []
+        for rows, cache, allowed in groups:
+            kb, vb = k[rows], v[rows]
+            ks.append(kb)
+            vs.append(vb)
+            K = kb if len(cache) == 0 else np.concatenate([cache.k[l], kb], axis=0)
+            V = vb if len(cache) == 0 else np.concatenate([cache.v[l], vb], axis=0)
+            for h in range(H):
+                s = (q[rows, h, :] @ K[:, h, :].T) * scale             # [Q_b, K_b+Q_b]
+                s = np.where(allowed, s, -np.inf)
+                o[rows, h, :] = softmax_rows(s) @ V[:, h, :]
+        o = self._st(o.reshape(Q, H * dh))
+        x = x + o @ self.w(f"l{l}.wo").T
+        hn = self._st(rmsnorm(x, self.w(f"l{l}.mlp_norm"), cfg.rms_eps))
+        a = self._st(silu(hn @ self.w(f"l{l}.w_gate").T) * (hn @ self.w(f"l{l}.w_up").T))
+        x = x + a @ self.w(f"l{l}.w_down").T
+        return x, ks, vs
+
+    def head(self, x: np.ndarray) -> np.ndarray:
+        """Final RMSNorm and LM head of residual rows ``x`` [Q, d]: logits [Q, V]."""
+        cfg = self.cfg
+        xf = self._st(rmsnorm(x, self.w("final_norm"), cfg.rms_eps))
+        return xf @ self.w("lm_head").T
 
     def causal(self, tokens, start_pos: int, cache: KVCache):
         """Plain causal forward of a token run at positions start_pos.."""
