@@ -121,8 +121,10 @@ def sample_verify(cands: Sequence[Sequence[int]], out_probs, row_probs: Callable
     cands[c] is candidate c's suffix (S tokens).  row_probs(c, s) is the
     target distribution of the row whose input is cands[c][s] (it predicts
     the token after it).  Returns (emitted, a, winner) where a is the number
-    of accepted candidate tokens and winner the lowest-index survivor
-    (meaningful when a > 0).
+    of accepted candidate tokens and winner the lowest-index survivor of the
+    accepted prefix (-1 when a = 0): its rows v_{w,0..a-1} are the ones whose
+    K/V the call commits, whether the next offset was rejected or all S
+    offsets were accepted.
     """
     S = len(cands[0]) if cands else 0
     survivors = list(range(len(cands)))
@@ -133,7 +135,7 @@ def sample_verify(cands: Sequence[Sequence[int]], out_probs, row_probs: Callable
         tok, acc = verify_position(p, offered, chooser, off)
         emitted.append(tok)
         if not acc:
-            return emitted, off, -1
+            return emitted, off, (survivors[0] if off > 0 else -1)
         survivors = [c for c in survivors if cands[c][off] == tok]
         p = row_probs(survivors[0], off)
     emitted.append(chooser.categorical(p, S, philox.PLAIN))

@@ -142,6 +142,70 @@ def test_multistep_joint_law_equals_ar():
         assert law.get(seq, 0) == ar, seq
 
 
+def test_winner_is_the_lowest_survivor_of_the_accepted_prefix():
+    """Over every outcome of the verifier (exact enumeration): with a > 0 the
+    winner is the lowest-index candidate whose first a tokens are the emitted
+    ones (its rows v_{w,0..a-1} carry the K/V the call commits), also when
+    the next offset is rejected; with a = 0 there is none (-1)."""
+    V = 3
+    rnd = np.random.default_rng(11)
+    table = {}
+
+    def cond(prefix):
+        if prefix not in table:
+            w = rnd.integers(1, 6, size=V)
+            table[prefix] = [Fraction(int(x), int(w.sum())) for x in w]
+        return table[prefix]
+
+    cands = [(1, 2, 0), (0, 1, 1), (0, 1, 2), (1, 2, 2), (0, 2, 0)]     # S = 3, shared prefixes
+    seen = []
+
+    def run(ch):
+        em, a, w = smp.sample_verify(cands, cond(()), lambda c, s: cond(tuple(cands[c][: s + 1])), ch)
+        want = min((c for c in range(len(cands)) if list(cands[c][:a]) == list(em[:a])), default=-1) if a else -1
+        seen.append((a, w, want))
+        return (a, w)
+
+    smp.enumerate_law(run)
+    assert all(w == want for _, w, want in seen)
+    assert any(0 < a < 3 for a, _, _ in seen) and any(a == 3 for a, _, _ in seen)
+
+
+def test_sampled_lookahead_commits_the_verified_rows():
+    """A sampled lookahead decode of a tiny model (vocabulary 5, peaked
+    logits, so candidates are accepted and rejected at every offset): after
+    each call the committed K/V equals that of one causal forward over the
+    prompt and the emitted tokens (every committed row is the row of an
+    emitted token at its position), so the next call reads the same prefix
+    AR sampling would."""
+    from oracle import lookahead as la
+    from oracle.model import KVCache, OracleModel
+    import synth
+    cfg = synth.ModelConfig(n_layers=1, d_model=16, n_heads=2, head_dim=8, d_ffn=32, vocab=5, dtype="f32",
+                            init_std=0.8)
+    m = OracleModel(cfg, synth.llama_weights(cfg, 7))
+    prompt = [1, 2, 3, 1, 2, 3, 1, 2]
+    samp = la.Sampling(1.0, 1.0, 55)
+    cache, lg = m.prefill(prompt)
+    out = [la._first_token(lg[-1], samp)]
+    st = la.LookaheadState(prompt, out[0], 3, 4, 3)
+    run = la.make_runner(m, cache, "meta")
+    partial = 0
+    while len(out) < 60:
+        rows, guesses = st.plan()
+        logits = run.run(rows)
+        verdict = la.sample_step(logits, rows, guesses, st, samp)
+        info = st.publish(rows, guesses, [int(np.argmax(x)) for x in logits], verdict)
+        run.commit(rows, info.commit_rows)
+        partial += 0 < info.a < st.S and len(guesses) > 0
+        out.extend(info.emitted)
+        _, rk, rv = m.forward(prompt + out[:-1], list(range(len(prompt) + len(out) - 1)), KVCache(1),
+                              np.tril(np.ones((len(prompt) + len(out) - 1,) * 2, dtype=bool)))
+        assert np.allclose(run.cache.k[0], rk[0], rtol=0, atol=1e-9)
+        assert np.allclose(run.cache.v[0], rv[0], rtol=0, atol=1e-9)
+    assert partial > 0          # some call accepted part of a suffix and rejected the rest
+
+
 # ---- warping ---------------------------------------------------------------------
 
 def test_warp_temperature_and_top_p():
