@@ -33,6 +33,10 @@ class BatchStep:
     requests: List[int]
     rows: List[int]            # packed rows per request
     infos: List[StepInfo]
+    logits: List[object]       # per request, the logits of its packed rows [rows, V]
+    needed: List[List[int]]    # per request, the packed rows whose logits the step reads
+    tokens: List[List[int]]    # per request, the input token of every packed row
+    positions: List[List[int]] # per request, the logical position of every packed row
 
 
 class BatchedLookahead:
@@ -55,8 +59,12 @@ class BatchedLookahead:
     def active(self, max_new: int) -> List[int]:
         return [b for b, o in enumerate(self.out) if len(o) < max_new]
 
-    def step(self, max_new: int) -> Optional[BatchStep]:
-        """One batched call over the requests that still need tokens."""
+    def step(self, max_new: int, choose=None) -> Optional[BatchStep]:
+        """One batched call over the requests that still need tokens.
+
+        ``choose(b, logits, needed)``, if given, returns request b's argmax per
+        packed row in place of the greedy selector (a test feeds another
+        implementation's decisions to keep the two state machines in step)."""
         live = self.active(max_new)
         if not live:
             return None
@@ -64,15 +72,20 @@ class BatchedLookahead:
         calls = [([r.token for r in rows], [r.position for r in rows], self.caches[b], meta_mask(rows))
                  for b, (rows, _) in zip(live, plans)]
         results = self.model.forward_many(calls)
-        infos = []
+        infos, all_logits, needed = [], [], []
         for b, (rows, guesses), (logits, new_k, new_v) in zip(live, plans, results):
-            argmax = [argmax_lowest(logits[i]) for i in range(len(rows))]
+            all_logits.append(logits)
+            needed.append([r.packed_index for r in rows if r.request_logit])
+            need = [r.packed_index for r in rows if r.request_logit]
+            argmax = (choose(b, logits, need) if choose is not None
+                      else [argmax_lowest(logits[i]) for i in range(len(rows))])
             info = self.states[b].publish(rows, guesses, argmax)
             idx = list(info.commit_rows)
             self.caches[b].append([k[idx] for k in new_k], [v[idx] for v in new_v])
             self.out[b].extend(info.emitted)
             infos.append(info)
-        return BatchStep(live, [len(rows) for rows, _ in plans], infos)
+        return BatchStep(live, [len(rows) for rows, _ in plans], infos, all_logits, needed,
+                         [[r.token for r in rows] for rows, _ in plans], [[r.position for r in rows] for rows, _ in plans])
 
 
 def lookahead_generate_batch(model: OracleModel, prompts: Sequence[Sequence[int]], max_new: int,

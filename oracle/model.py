@@ -187,8 +187,17 @@ class OracleModel:
         ``groups`` lists, per request, (row slice, committed cache, visibility
         [Q_b, len(cache) + Q_b]); a request's rows attend to its own cache at
         layer ``l`` and its own new rows only.  Returns (x after the layer,
-        per-request new K rows [Q_b, H, dh], per-request new V rows).
+        per-request new K rows [Q_b, H, dh], per-request new V rows).  The
+        stages below, in order, are the whole layer.
         """
+        o, ks, vs = self.attention(l, x, positions, groups)
+        x = self.o_residual(l, x, o)
+        a = self.mlp_act(l, self.mlp_input(l, x))
+        return self.down_residual(l, x, a), ks, vs
+
+    def attention(self, l: int, x: np.ndarray, positions, groups):
+        """RMSNorm, Q/K/V projections, RoPE and masked attention of layer l:
+        (attention output [Q, H*dh] as stored, new K rows, new V rows)."""
         cfg = self.cfg
         H, dh = cfg.n_heads, cfg.head_dim
         Q = x.shape[0]
@@ -211,12 +220,23 @@ class OracleModel:
                 s = (q[rows, h, :] @ K[:, h, :].T) * scale             # [Q_b, K_b+Q_b]
                 s = np.where(allowed, s, -np.inf)
                 o[rows, h, :] = softmax_rows(s) @ V[:, h, :]
-        o = self._st(o.reshape(Q, H * dh))
-        x = x + o @ self.w(f"l{l}.wo").T
-        hn = self._st(rmsnorm(x, self.w(f"l{l}.mlp_norm"), cfg.rms_eps))
-        a = self._st(silu(hn @ self.w(f"l{l}.w_gate").T) * (hn @ self.w(f"l{l}.w_up").T))
-        x = x + a @ self.w(f"l{l}.w_down").T
-        return x, ks, vs
+        return self._st(o.reshape(Q, H * dh)), ks, vs
+
+    def o_residual(self, l: int, x: np.ndarray, o: np.ndarray) -> np.ndarray:
+        """The residual after the attention: x + Wo . o."""
+        return x + o @ self.w(f"l{l}.wo").T
+
+    def mlp_input(self, l: int, x: np.ndarray) -> np.ndarray:
+        """RMSNorm of the residual before the MLP, as stored."""
+        return self._st(rmsnorm(x, self.w(f"l{l}.mlp_norm"), self.cfg.rms_eps))
+
+    def mlp_act(self, l: int, hn: np.ndarray) -> np.ndarray:
+        """SwiGLU of the normalised rows, as stored: silu(Wgate . hn) * (Wup . hn)."""
+        return self._st(silu(hn @ self.w(f"l{l}.w_gate").T) * (hn @ self.w(f"l{l}.w_up").T))
+
+    def down_residual(self, l: int, x: np.ndarray, a: np.ndarray) -> np.ndarray:
+        """The residual after the MLP: x + Wdown . a."""
+        return x + a @ self.w(f"l{l}.w_down").T
 
     def head(self, x: np.ndarray) -> np.ndarray:
         """Final RMSNorm and LM head of residual rows ``x`` [Q, d]: logits [Q, V]."""
