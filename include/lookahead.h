@@ -258,6 +258,21 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
                       int max_new, int W, int N, int G, const la_sampling* s, int32_t* out,
                       la_stats* stats);
 
+/* fp32 logits [*n_rows][vocab] of request b's needed rows in the last
+ * batched call (la_set_debug bit 0 set before la_generate_batch) and their
+ * packed row indices within the request's own rows.  A request that left the
+ * batch before the last call keeps no logits of that call.  Errors:
+ * LA_EINVAL, LA_ENOTSUP (a context from la_init), LA_ESTATE (bit 0 off),
+ * LA_ECAPACITY (cap_rows < *n_rows), LA_ECUDA. */
+int la_debug_batch_logits(la_ctx* ctx, int b, float* logits, int32_t* rows, int cap_rows, int* n_rows);
+
+/* la_debug_state for request b of a batched context after the last batched
+ * call: its header, window and its own packed rows (packed indices within
+ * the request).  Errors: LA_EINVAL, LA_ENOTSUP (a context from la_init),
+ * LA_ECUDA. */
+int la_debug_batch_state(la_ctx* ctx, int b, int32_t* hdr, int32_t* levels, int32_t* level_len, int32_t* row_tok,
+                         int32_t* row_pos, int32_t* row_meta);
+
 /* ---- inspection (tests) -------------------------------------------------- */
 
 /* flags bit 0: keep fp32 logits of the rows whose outputs the verifier reads
@@ -270,21 +285,26 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
  * records add a little time to every step: time whole steps with it off. */
 int la_set_debug(la_ctx* ctx, int flags);
 
-/* flags bit 3: keep the residual stream of every layer for la_debug_hidden
- * (the first call with it allocates (n_layers+1) x rows x d_model floats).
- * Unknown bits: LA_EINVAL. */
+/* flags bit 3: keep, for la_debug_layer, every layer's values at the points
+ * where the decoder stores them (the first call with it allocates them:
+ * (n_layers+1) x rows x d_model floats and n_layers x rows x (HD + d_model +
+ * d_ffn) elements of the model dtype).  Unknown bits: LA_EINVAL. */
 
-/* fp32 residual rows [rows][d_model] (host) of the last pass (prefill chunk
- * or packed call) at the input of decoder layer `layer` (0 .. n_layers-1:
- * the embedding plus every earlier layer's attention and MLP updates), or,
- * for layer == n_layers, the final residual before the final RMSNorm, which
- * is complete only on the rows whose logits the call reads.  This is the
- * stream of the decoder of break the sequential dependency §2 that every
- * packed row runs through unchanged (M7.3 §0x04); tests feed it to the
- * oracle layer by layer.  Requires la_set_debug bit 3 before the pass.
- * Errors: LA_EINVAL, LA_ESTATE (bit 3 off), LA_ECAPACITY (rows above the
- * row buffers), LA_ECUDA. */
-int la_debug_hidden(la_ctx* ctx, int layer, float* host, int rows);
+/* Rows [0, rows) of the last pass (prefill chunk or packed call) of decoder
+ * layer `layer`, at one of its storage points (host buffer of rows x width):
+ *   what 0  the fp32 residual at the layer's input (width d_model); layer ==
+ *           n_layers: the final residual before the final RMSNorm, complete
+ *           only on the rows whose logits the call reads
+ *   what 1  the attention output (width n_heads*head_dim, model dtype)
+ *   what 2  the RMSNorm output that enters the gate/up projection (width
+ *           d_model, model dtype)
+ *   what 3  the SwiGLU output that enters the down projection (width d_ffn,
+ *           model dtype)
+ * Every packed row runs through the same decoder (break the sequential
+ * dependency §2; M7.3 §0x04); tests feed these values to the oracle stage by
+ * stage.  Requires la_set_debug bit 3 before the pass.  Errors: LA_EINVAL,
+ * LA_ESTATE (bit 3 off), LA_ECAPACITY (rows above the row buffers), LA_ECUDA. */
+int la_debug_layer(la_ctx* ctx, int layer, int what, void* host, int rows);
 
 /* Per-kind kernel-timing totals since the last read (then reset):
  *   ms4[k], launches4[k] (host, 4 entries each): k = 0 tensor-core GEMMs,

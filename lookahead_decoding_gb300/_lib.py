@@ -23,7 +23,7 @@ EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", 
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
            "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
            "la_gemm_noalloc", "la_profile_read", "la_set_options", "la_init_batch", "la_generate_batch",
-           "la_debug_hidden"]
+           "la_debug_layer", "la_debug_batch_logits", "la_debug_batch_state"]
 
 # pool seeding options (la_set_options)
 LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT, LA_OPT_SLICE_WINDOW = 1, 2, 4
@@ -84,8 +84,10 @@ def _load() -> C.CDLL:
         "la_set_options": (C.c_int, [vp, C.c_uint32]),
         "la_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
         "la_debug_logits": (C.c_int, [vp, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
-        "la_debug_hidden": (C.c_int, [vp, C.c_int, f32p, C.c_int]),
+        "la_debug_layer": (C.c_int, [vp, C.c_int, C.c_int, vp, C.c_int]),
+        "la_debug_batch_logits": (C.c_int, [vp, C.c_int, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
         "la_debug_state": (C.c_int, [vp, i32p, i32p, i32p, i32p, i32p, i32p]),
+        "la_debug_batch_state": (C.c_int, [vp, C.c_int, i32p, i32p, i32p, i32p, i32p, i32p]),
         "la_debug_pool": (C.c_int, [vp, C.c_int, i32p, C.POINTER(C.c_int)]),
         "la_step_inject": (C.c_int, [vp, C.c_int, C.c_int, C.c_int, C.POINTER(la_sampling), C.c_int, i32p, f32p, i32p,
                                      C.POINTER(C.c_int)]),
@@ -245,19 +247,45 @@ def la_debug_logits(ctx, cap_rows: int, vocab: int):
     return logits[: n.value], rows[: n.value]
 
 
-def la_debug_hidden(ctx, layer: int, rows: int, d_model: int):
-    """fp32 residual rows [rows][d_model] at the input of `layer` in the last
-    pass (layer == n_layers: the final residual); needs debug bit 3."""
-    x = np.zeros((rows, d_model), dtype=np.float32)
-    _check(LIB.la_debug_hidden(ctx, layer, x.ctypes.data_as(C.POINTER(C.c_float)), rows), "la_debug_hidden", ctx)
+def la_debug_batch_logits(ctx, b: int, cap_rows: int, vocab: int):
+    """Request b's needed-row logits of the last batched call and their packed
+    indices within the request (needs debug bit 0)."""
+    logits = np.zeros((cap_rows, vocab), dtype=np.float32)
+    rows = np.zeros(cap_rows, dtype=np.int32)
+    n = C.c_int()
+    _check(LIB.la_debug_batch_logits(ctx, b, logits.ctypes.data_as(C.POINTER(C.c_float)),
+                                     rows.ctypes.data_as(C.POINTER(C.c_int32)), cap_rows, C.byref(n)),
+           "la_debug_batch_logits", ctx)
+    return logits[: n.value], rows[: n.value]
+
+
+def la_debug_layer(ctx, layer: int, what: int, rows: int, width: int, bf16: bool = True):
+    """Rows of one storage point of `layer` in the last pass (see the header):
+    what 0 the fp32 residual input (float32 array), 1 the attention output,
+    2 the normalised MLP input, 3 the SwiGLU output (float64 arrays of the
+    stored bf16 values, or float32 for an fp32 model); needs debug bit 3."""
+    if what == 0:
+        x = np.zeros((rows, width), dtype=np.float32)
+    else:
+        x = np.zeros((rows, width), dtype=np.uint16 if bf16 else np.float32)
+    _check(LIB.la_debug_layer(ctx, layer, what, x.ctypes.data, rows), "la_debug_layer", ctx)
+    if what != 0 and bf16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return x
+
+
+def la_debug_hidden(ctx, layer: int, rows: int, d_model: int):
+    """fp32 residual rows [rows][d_model] at the input of `layer` (debug bit 3)."""
+    return la_debug_layer(ctx, layer, 0, rows, d_model)
 
 
 HDR_KEYS = ["K", "x_t", "W", "N", "G", "n_levels", "step", "Q", "C_t", "a", "winner", "n_out", "err", "steady",
             "n_need", "n_deep"]
 
 
-def la_debug_state(ctx):
+def la_debug_state(ctx, b: Optional[int] = None):
+    """Header, window levels and the last call's rows (tokens, positions,
+    metadata); b: request b of a batched context."""
     q = la_query(ctx)
     R = q["max_N"] - 1
     hdr = np.zeros(16, dtype=np.int32)
@@ -267,7 +295,11 @@ def la_debug_state(ctx):
     pos = np.zeros(q["Qmax"], dtype=np.int32)
     meta = np.zeros(q["Qmax"], dtype=np.int32)
     P = lambda a: a.ctypes.data_as(C.POINTER(C.c_int32))
-    _check(LIB.la_debug_state(ctx, P(hdr), P(levels), P(lens), P(tok), P(pos), P(meta)), "la_debug_state", ctx)
+    if b is None:
+        _check(LIB.la_debug_state(ctx, P(hdr), P(levels), P(lens), P(tok), P(pos), P(meta)), "la_debug_state", ctx)
+    else:
+        _check(LIB.la_debug_batch_state(ctx, b, P(hdr), P(levels), P(lens), P(tok), P(pos), P(meta)),
+               "la_debug_batch_state", ctx)
     h = dict(zip(HDR_KEYS, hdr.tolist()))
     lv = [levels[r, : lens[r]].tolist() if r < h["n_levels"] else None for r in range(R)]
     Q = h["Q"]

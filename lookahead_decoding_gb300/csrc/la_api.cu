@@ -73,6 +73,10 @@ struct la_ctx {
     // tensor-core GEMM descriptors (bf16 models)
     std::vector<TcGemm> g_qkv, g_o, g_gu, g_down;
     TcGemm g_head{};
+    // decode calls through the layer-chain kernel (la_mega.cu): one launch
+    // per stretch between two attention launches; a phase counter each
+    int mega = 0;
+    unsigned long long* mg_bar = nullptr;   // [n_layers + 1][MG_MAX_PHASES]
 
     // batched calls: up to max_batch requests stacked in slices of Qstride
     // rows; request b's state and cache are its own (request 0's are the
@@ -90,6 +94,9 @@ struct la_ctx {
     int prompt_len = 0;
     int debug = 0;
     float* dbg_hidden = nullptr;      // [n_layers + 1][Qcap][d_model] fp32 (debug bit 3)
+    // debug bit 3: per layer, the attention output, the normalised MLP input
+    // and the SwiGLU output ([n_layers][Qcap][HD | d_model | d_ffn], model dtype)
+    void *dbg_attn = nullptr, *dbg_hn = nullptr, *dbg_act = nullptr;
     std::map<int, Graph> graphs;
 
     // kernel-timing mode (debug bit 2): event pairs recorded inside the step graph
@@ -198,6 +205,7 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     g->rows_cap = ctx->Qcap;
     g->out = out;
     g->ldo = ldo;
+    g->act = X;
     return LA_OK;
 }
 
@@ -239,6 +247,146 @@ static Lane prefill_lane(la_ctx* ctx, int b) {
 // a batched call of B requests
 static Lane batch_lane(la_ctx* ctx, int B) {
     return Lane{&ctx->bd, (char*)ctx->cache, 0, ctx->temp_rows, B * ctx->Qstride, ctx->req_hdr, ctx->Qstride};
+}
+
+// attention of layer l for a bf16 model (RoPE folded in when `rope` is given)
+static int enqueue_attention_bf16(la_ctx* ctx, int l, int sel, const Lane& ln, int rc, const LaRope* rope) {
+    const la_model_cfg& c = ctx->cfg;
+    const int H = c.n_heads;
+    CK(la_launch_attention_bf16(*ln.d, ctx->st, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
+                                layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
+                                layer_plane(ctx, ctx->temp, l, 0, ln.temp_rows),
+                                layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows), ctx->attn, H, sel, ctx->Qcap,
+                                ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX, ctx->cache_map,
+                                ln.cache_row0 + (l * 2 + 0) * H * ctx->max_ctx,
+                                ln.cache_row0 + (l * 2 + 1) * H * ctx->max_ctx, ln.req_hdr, ln.qstride,
+                                (long long)(ctx->cache_bytes_req / ctx->esz), c.n_layers * 2 * H * ctx->max_ctx,
+                                ln.temp_rows, la_attn_tail_rows(ctx->max_W, ctx->max_N, ctx->Qmax), rope));
+    return LA_OK;
+}
+
+// ---- layer-chain kernel ---------------------------------------------------------
+
+static MgGemm mg_gemm(la_ctx* ctx, const TcGemm& g, int sel) {
+    MgGemm m;
+    memset(&m, 0, sizeof(m));
+    m.wpack = (const uint8_t*)g.wpack;
+    m.act = (const __nv_bfloat16*)g.act;
+    m.mode = g.mode;
+    m.K = g.K;
+    m.n_tiles = g.Nout / 128;
+    m.k_tiles = la_tc_k_units(g.mode, g.K);
+    m.ua = la_tc_unit_atoms(g.mode);
+    m.k_atoms = g.K / 64;
+    m.nA = g.mode == GEMM_SWIGLU ? 2 : 1;
+    m.max_seg = g.max_seg;
+    m.sel = sel;
+    m.defer = g.defer;
+    m.n_cta = g.n_cta;
+    m.ws = ctx->work.ws;
+    m.ctr = (unsigned long long*)ctx->work.counters + g.ctr_off;
+    m.out = g.out;
+    m.ldo = g.ldo;
+    m.logits = g.logits;
+    m.ld_logits = g.ld_logits;
+    m.part_v = ctx->work.part_v;
+    m.part_i = ctx->work.part_i;
+    m.part_stride = ctx->work.part_stride;
+    return m;
+}
+static MgRows mg_rms(la_ctx* ctx, int kind, int sel, const void* gain, void* y, const TcGemm* prev) {
+    MgRows r;
+    memset(&r, 0, sizeof(r));
+    r.kind = kind;
+    r.sel = sel;
+    r.dm = ctx->cfg.d_model;
+    r.eps = ctx->cfg.rms_eps;
+    r.x = ctx->x;
+    r.g = (const __nv_bfloat16*)gain;
+    r.y = (__nv_bfloat16*)y;
+    r.split = split_of(ctx, prev);
+    return r;
+}
+struct MgChain {
+    MgParams p;
+    int ng = 0, nr = 0;
+    explicit MgChain(la_ctx* ctx, unsigned long long* bar) {
+        memset(&p, 0, sizeof(p));
+        p.hdr = ctx->d.hdr;
+        p.need = ctx->d.need;
+        p.bar = bar;
+        p.rows_cap = ctx->Qmax;
+        p.ns_pre = la_mega_ring_stages(ctx->Qmax);
+    }
+    void gemm(const MgGemm& g) { p.ph_kind[p.n_ph] = MG_PH_GEMM; p.ph_idx[p.n_ph++] = ng; p.g[ng++] = g; }
+    void rows(const MgRows& r) { p.ph_kind[p.n_ph] = MG_PH_ROWS; p.ph_idx[p.n_ph++] = nr; p.r[nr++] = r; }
+};
+
+
+// A decode call of a single-request bf16 context: embedding, then per layer
+// one layer-chain launch and the attention, then the last chain (down of the
+// last layer, final RMSNorm of the needed rows, LM head), then the argmax
+// over the head's tiles.  The chains compute exactly what enqueue_forward and
+// enqueue_head compute for SEL_CALL.
+static int enqueue_call_mega(la_ctx* ctx, int keep_logits) {
+    const la_model_cfg& c = ctx->cfg;
+    const LaDev& d = ctx->d;
+    cudaStream_t st = ctx->st;
+    const int L = c.n_layers;
+    const Lane ln = solo_lane(ctx);
+    const int rc = ln.rows_call;
+    CK(cudaMemsetAsync(ctx->mg_bar, 0, sizeof(unsigned long long) * (L + 1) * MG_MAX_PHASES, st));
+    int pi = prof_open(ctx, PK_ROW);
+    la_launch_embed(d, st, c.dtype, ctx->emb, ctx->x, c.d_model, SEL_CALL, rc);
+    prof_close(ctx, pi);
+    {
+        MgChain ch(ctx, ctx->mg_bar);
+        ch.rows(mg_rms(ctx, MG_RMS, SEL_CALL, ctx->attn_norm[0], ctx->xn, nullptr));
+        ch.gemm(mg_gemm(ctx, ctx->g_qkv[0], SEL_CALL));
+        pi = prof_open(ctx, PK_GEMM);
+        CK(la_launch_mega(ch.p, st));
+        prof_close(ctx, pi);
+    }
+    for (int l = 0; l < L; ++l) {
+        const LaRope rope{(const __nv_bfloat16*)ctx->qkv, split_of(ctx, &ctx->g_qkv[l]), ctx->rcos, ctx->rsin};
+        pi = prof_open(ctx, PK_ATTN);
+        int r = enqueue_attention_bf16(ctx, l, SEL_CALL, ln, rc, &rope);
+        prof_close(ctx, pi);
+        if (r) return r;
+        MgChain ch(ctx, ctx->mg_bar + (size_t)(l + 1) * MG_MAX_PHASES);
+        ch.gemm(mg_gemm(ctx, ctx->g_o[l], SEL_CALL));
+        ch.rows(mg_rms(ctx, MG_RMS, SEL_CALL, ctx->mlp_norm[l], ctx->xn, &ctx->g_o[l]));
+        ch.gemm(mg_gemm(ctx, ctx->g_gu[l], SEL_CALL));
+        if (ctx->g_gu[l].defer && ctx->g_gu[l].max_seg > 1) {
+            MgRows sw;
+            memset(&sw, 0, sizeof(sw));
+            sw.kind = MG_SWIGLU;
+            sw.sel = SEL_CALL;
+            sw.y = (__nv_bfloat16*)ctx->act;
+            sw.ldo = c.d_ffn;
+            sw.split = la_tc_split(ctx->g_gu[l], ctx->work);
+            ch.rows(sw);
+        }
+        ch.gemm(mg_gemm(ctx, ctx->g_down[l], SEL_CALL));
+        if (l + 1 < L) {
+            ch.rows(mg_rms(ctx, MG_RMS, SEL_CALL, ctx->attn_norm[l + 1], ctx->xn, &ctx->g_down[l]));
+            ch.gemm(mg_gemm(ctx, ctx->g_qkv[l + 1], SEL_CALL));
+        } else {
+            ch.rows(mg_rms(ctx, MG_RMS_GATHER, SEL_NEED, ctx->fnorm, ctx->hn, &ctx->g_down[l]));
+            TcGemm hg = ctx->g_head;
+            hg.logits = keep_logits ? ctx->logits : nullptr;
+            ch.gemm(mg_gemm(ctx, hg, SEL_NEED));
+        }
+        pi = prof_open(ctx, PK_GEMM);
+        CK(la_launch_mega(ch.p, st));
+        prof_close(ctx, pi);
+    }
+    pi = prof_open(ctx, PK_STATE);
+    la_launch_argmax_reduce(d, st, ctx->work.part_v, ctx->work.part_i, c.vocab / 128, ctx->work.part_stride, SEL_NEED,
+                            rc);
+    prof_close(ctx, pi);
+    CK(cudaGetLastError());
+    return LA_OK;
 }
 
 static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
@@ -287,16 +435,8 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
         }
         pi = prof_open(ctx, PK_ATTN);
         if (ctx->bf16) {
-            CK(la_launch_attention_bf16(d, st, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
-                                        layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
-                                        layer_plane(ctx, ctx->temp, l, 0, ln.temp_rows),
-                                        layer_plane(ctx, ctx->temp, l, 1, ln.temp_rows), ctx->attn, H, sel,
-                                        ctx->Qcap, ctx->max_ctx, ctx->Qmax, rc, ctx->attn_TB, ctx->PMAX,
-                                        ctx->cache_map, ln.cache_row0 + (l * 2 + 0) * H * ctx->max_ctx,
-                                        ln.cache_row0 + (l * 2 + 1) * H * ctx->max_ctx, ln.req_hdr, ln.qstride,
-                                        (long long)(ctx->cache_bytes_req / ctx->esz),
-                                        c.n_layers * 2 * H * ctx->max_ctx, ln.temp_rows,
-                                        la_attn_tail_rows(ctx->max_W, ctx->max_N, ctx->Qmax), fuse ? &rope : nullptr));
+            int r = enqueue_attention_bf16(ctx, l, sel, ln, rc, fuse ? &rope : nullptr);
+            if (r) return r;
         } else {
             CK(la_launch_attention(d, st, c.dtype, dh, ctx->qbuf, layer_plane(ctx, ln.cache, l, 0, ctx->max_ctx),
                                    layer_plane(ctx, ln.cache, l, 1, ctx->max_ctx),
@@ -305,6 +445,10 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
                                    ctx->max_ctx, ln.temp_rows, rc));
         }
         prof_close(ctx, pi);
+        const bool keep = (ctx->debug & 8) && ctx->dbg_attn;
+        if (keep)
+            CK(cudaMemcpyAsync((char*)ctx->dbg_attn + (size_t)l * ctx->Qcap * HD * ctx->esz, ctx->attn,
+                               (size_t)rc * HD * ctx->esz, cudaMemcpyDeviceToDevice, st));
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_o[l], ctx->work, sel, rc));
@@ -316,6 +460,9 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
         la_launch_rmsnorm(d, st, c.dtype, ctx->x, ctx->mlp_norm[l], ctx->xn, dm, c.rms_eps, sel, 0, rc,
                           split_of(ctx, ctx->tc ? &ctx->g_o[l] : nullptr));
         prof_close(ctx, pi);
+        if (keep)
+            CK(cudaMemcpyAsync((char*)ctx->dbg_hn + (size_t)l * ctx->Qcap * dm * ctx->esz, ctx->xn,
+                               (size_t)rc * dm * ctx->esz, cudaMemcpyDeviceToDevice, st));
         if (ctx->tc) {
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_gu[l], ctx->work, sel, rc));
@@ -325,11 +472,17 @@ static int enqueue_forward(la_ctx* ctx, int sel, const Lane& ln) {
                 la_launch_swiglu_split(d, st, la_tc_split(ctx->g_gu[l], ctx->work), ctx->act, F, sel, rc);
                 prof_close(ctx, pi);
             }
+            if (keep)
+                CK(cudaMemcpyAsync((char*)ctx->dbg_act + (size_t)l * ctx->Qcap * F * ctx->esz, ctx->act,
+                                   (size_t)rc * F * ctx->esz, cudaMemcpyDeviceToDevice, st));
             pi = prof_open(ctx, PK_GEMM);
             CK(la_launch_gemm_tc(d, st, ctx->g_down[l], ctx->work, sel, rc));
             prof_close(ctx, pi);
         } else {
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_SWIGLU, ctx->xn, dm, ctx->wg[l], ctx->wu[l], dm, F, ctx->act, F, sel, rc);
+            if (keep)
+                CK(cudaMemcpyAsync((char*)ctx->dbg_act + (size_t)l * ctx->Qcap * F * ctx->esz, ctx->act,
+                                   (size_t)rc * F * ctx->esz, cudaMemcpyDeviceToDevice, st));
             la_launch_gemm_ffma(d, st, c.dtype, GEMM_RESID, ctx->act, F, ctx->wd[l], nullptr, F, dm, ctx->x, dm, sel, rc);
         }
     }
@@ -392,10 +545,18 @@ static int enqueue_step(la_ctx* ctx) {
     la_launch_pack(ctx->d, ctx->st);
     prof_close(ctx, pi);
     const Lane ln = solo_lane(ctx);
-    int r = enqueue_forward(ctx, SEL_CALL, ln);
-    if (r) return r;
-    r = enqueue_head(ctx, (ctx->debug & 1) | ctx->sampling, ln);
-    if (r) return r;
+    int r;
+    if (ctx->mega && !(ctx->debug & (8 | 16))) {
+        // the layer-chain schedule (debug bit 3 needs the per-layer hooks of
+        // the multi-launch path; bit 4 forces it for comparisons)
+        r = enqueue_call_mega(ctx, (ctx->debug & 1) | ctx->sampling);
+        if (r) return r;
+    } else {
+        r = enqueue_forward(ctx, SEL_CALL, ln);
+        if (r) return r;
+        r = enqueue_head(ctx, (ctx->debug & 1) | ctx->sampling, ln);
+        if (r) return r;
+    }
     if (ctx->sampling) {
         pi = prof_open(ctx, PK_STATE);
         CK(la_launch_sample_verify(ctx->d, ctx->st, ctx->logits, ctx->cfg.vocab, 0));
@@ -405,7 +566,7 @@ static int enqueue_step(la_ctx* ctx) {
 }
 
 static int get_graph(la_ctx* ctx, Graph** out) {
-    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4) | (ctx->debug & 8);
+    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4) | (ctx->debug & 8) | (ctx->debug & 16);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     Graph g;
@@ -732,6 +893,23 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         A((void**)&ctx->work.part_v, sizeof(float) * (V / 128) * ctx->Qcap);
         A((void**)&ctx->work.part_i, sizeof(int) * (V / 128) * ctx->Qcap);
         if (r) { la_free(ctx); return r; }
+        // decode calls through the layer-chain kernel: single-request bf16
+        // contexts whose calls fit its accumulators, with packed weights, the
+        // deferred split tiles and one GEMM CTA per SM (LA_MEGA=0: the
+        // multi-launch schedule, for A/B runs)
+        const char* me = getenv("LA_MEGA");
+        bool mega = (me && me[0] == '1') && ctx->bf16 && max_batch == 1 && ctx->Qmax <= MG_MAX_ROWS_PER_CALL &&
+                    defer && la_fuse_rope() && c.head_dim == 128;
+        const int sms = la_tc_ctas();
+        auto fits = [&](const TcGemm& g) { return g.wpack != nullptr && g.n_cta == sms; };
+        for (int l = 0; l < c.n_layers && mega; ++l)
+            mega = fits(ctx->g_qkv[l]) && fits(ctx->g_o[l]) && fits(ctx->g_gu[l]) && fits(ctx->g_down[l]);
+        mega = mega && fits(ctx->g_head);
+        if (mega) {
+            A((void**)&ctx->mg_bar, sizeof(unsigned long long) * (c.n_layers + 1) * MG_MAX_PHASES);
+            if (r) { la_free(ctx); return r; }
+            ctx->mega = 1;
+        }
     }
     if (cudaStreamSynchronize(ctx->st) != cudaSuccess) {
         ctx->last_err = cudaGetErrorString(cudaGetLastError());
@@ -750,22 +928,31 @@ int la_query(la_ctx* ctx, int32_t* s) {
 }
 
 int la_set_debug(la_ctx* ctx, int flags) {
-    if (!ctx || (flags & ~(1 | 4 | 8))) return LA_EINVAL;
+    if (!ctx || (flags & ~(1 | 4 | 8 | 16))) return LA_EINVAL;
     if ((flags & 8) && !ctx->dbg_hidden) {
-        const size_t bytes = sizeof(float) * (size_t)(ctx->cfg.n_layers + 1) * ctx->Qcap * ctx->cfg.d_model;
-        int r = dalloc(ctx, (void**)&ctx->dbg_hidden, bytes);
+        const la_model_cfg& c = ctx->cfg;
+        const size_t rows = (size_t)ctx->Qcap;
+        int r = dalloc(ctx, (void**)&ctx->dbg_hidden, sizeof(float) * (size_t)(c.n_layers + 1) * rows * c.d_model);
+        if (!r) r = dalloc(ctx, &ctx->dbg_attn, ctx->esz * (size_t)c.n_layers * rows * ctx->HD);
+        if (!r) r = dalloc(ctx, &ctx->dbg_hn, ctx->esz * (size_t)c.n_layers * rows * c.d_model);
+        if (!r) r = dalloc(ctx, &ctx->dbg_act, ctx->esz * (size_t)c.n_layers * rows * c.d_ffn);
         if (r) return r;
     }
     ctx->debug = flags;
     return LA_OK;
 }
 
-int la_debug_hidden(la_ctx* ctx, int layer, float* host, int rows) {
-    if (!ctx || !host || layer < 0 || layer > ctx->cfg.n_layers || rows < 1) return LA_EINVAL;
+int la_debug_layer(la_ctx* ctx, int layer, int what, void* host, int rows) {
+    if (!ctx || !host || layer < 0 || layer > ctx->cfg.n_layers || rows < 1 || what < 0 || what > 3) return LA_EINVAL;
+    if (what > 0 && layer == ctx->cfg.n_layers) return LA_EINVAL;
     if (!(ctx->debug & 8) || !ctx->dbg_hidden) return LA_ESTATE;
     if (rows > ctx->Qcap) return LA_ECAPACITY;
-    const size_t dm = ctx->cfg.d_model;
-    CK(cudaMemcpyAsync(host, ctx->dbg_hidden + (size_t)layer * ctx->Qcap * dm, sizeof(float) * (size_t)rows * dm,
+    const la_model_cfg& c = ctx->cfg;
+    const size_t width[4] = {(size_t)c.d_model, (size_t)ctx->HD, (size_t)c.d_model, (size_t)c.d_ffn};
+    const size_t esz = what == 0 ? sizeof(float) : ctx->esz;
+    const char* base = what == 0 ? (const char*)ctx->dbg_hidden
+                     : (const char*)(what == 1 ? ctx->dbg_attn : what == 2 ? ctx->dbg_hn : ctx->dbg_act);
+    CK(cudaMemcpyAsync(host, base + (size_t)layer * ctx->Qcap * width[what] * esz, esz * (size_t)rows * width[what],
                        cudaMemcpyDeviceToHost, ctx->st));
     CK(cudaStreamSynchronize(ctx->st));
     return LA_OK;
@@ -1030,7 +1217,8 @@ int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new, const
 // forward and LM head over the stacked slices, every request's publication
 // and commit.
 static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
-    const int key = 0x100 | B | (sampling << 12);
+    const int keep = sampling | (ctx->debug & 1);
+    const int key = 0x100 | B | (sampling << 12) | ((ctx->debug & 1) << 13);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
     const la_model_cfg& c = ctx->cfg;
@@ -1042,7 +1230,7 @@ static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
     for (int b = 0; b < B; ++b) la_launch_pack(ctx->req[b], ctx->st);
     const Lane ln = batch_lane(ctx, B);
     r = enqueue_forward(ctx, SEL_CALL, ln);
-    if (!r) r = enqueue_head(ctx, sampling, ln);
+    if (!r) r = enqueue_head(ctx, keep, ln);
     // sampling: each request's verifier on the logits of its slice of the needed rows
     for (int b = 0; b < B && !r && sampling; ++b)
         if (la_launch_sample_verify(ctx->req[b], ctx->st, ctx->logits + (size_t)b * ctx->Qstride * c.vocab, c.vocab, 0) !=
@@ -1178,25 +1366,60 @@ int la_debug_logits(la_ctx* ctx, float* logits, int32_t* rows, int cap_rows, int
     return LA_OK;
 }
 
-int la_debug_state(la_ctx* ctx, int32_t* hdr, int32_t* levels, int32_t* level_len, int32_t* row_tok, int32_t* row_pos,
-                   int32_t* row_meta) {
-    if (!ctx) return LA_EINVAL;
+int la_debug_batch_logits(la_ctx* ctx, int b, float* logits, int32_t* rows, int cap_rows, int* n_rows) {
+    if (!ctx || !n_rows || b < 0) return LA_EINVAL;
+    if (ctx->max_batch < 2) return LA_ENOTSUP;
+    if (b >= ctx->max_batch) return LA_EINVAL;
+    if (!(ctx->debug & 1)) return LA_ESTATE;
     LaHdr h;
-    int r = read_hdr(ctx, &h);
-    if (r) return r;
+    CK(cudaMemcpyAsync(&h, ctx->req[b].hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    const int n = h.n_need;
+    *n_rows = n;
+    if (n > cap_rows) return LA_ECAPACITY;
+    const size_t o = (size_t)b * ctx->Qstride;
+    if (logits)
+        CK(cudaMemcpyAsync(logits, ctx->logits + o * ctx->cfg.vocab, sizeof(float) * (size_t)n * ctx->cfg.vocab,
+                           cudaMemcpyDeviceToHost, ctx->st));
+    if (rows) CK(cudaMemcpyAsync(rows, ctx->req[b].need, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
+    if (rows)
+        for (int i = 0; i < n; ++i) rows[i] -= (int32_t)o;
+    return LA_OK;
+}
+
+static int debug_state_of(la_ctx* ctx, const LaDev& v, int32_t* hdr, int32_t* levels, int32_t* level_len,
+                          int32_t* row_tok, int32_t* row_pos, int32_t* row_meta) {
+    LaHdr h;
+    CK(cudaMemcpyAsync(&h, v.hdr, sizeof(h), cudaMemcpyDeviceToHost, ctx->st));
+    CK(cudaStreamSynchronize(ctx->st));
     if (hdr) {
         int32_t v[16] = {h.K, h.x_t, h.W, h.N, h.G, h.n_levels, h.step, h.Q, h.C_t, h.a, h.winner, h.n_out,
                          h.err, h.steady, h.n_need, h.n_deep};
         memcpy(hdr, v, sizeof(v));
     }
-    if (levels) CK(cudaMemcpyAsync(levels, ctx->d.window, sizeof(int32_t) * ctx->Rmax * ctx->LMAX, cudaMemcpyDeviceToHost, ctx->st));
+    if (levels) CK(cudaMemcpyAsync(levels, v.window, sizeof(int32_t) * ctx->Rmax * ctx->LMAX, cudaMemcpyDeviceToHost, ctx->st));
     if (level_len)
         for (int i = 0; i < ctx->Rmax; ++i) level_len[i] = h.level_len[i];
-    if (row_tok) CK(cudaMemcpyAsync(row_tok, ctx->d.row_tok, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
-    if (row_pos) CK(cudaMemcpyAsync(row_pos, ctx->d.row_pos, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
-    if (row_meta) CK(cudaMemcpyAsync(row_meta, ctx->d.row_meta, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
+    if (row_tok) CK(cudaMemcpyAsync(row_tok, v.row_tok, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
+    if (row_pos) CK(cudaMemcpyAsync(row_pos, v.row_pos, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
+    if (row_meta) CK(cudaMemcpyAsync(row_meta, v.row_meta, sizeof(int32_t) * ctx->Qmax, cudaMemcpyDeviceToHost, ctx->st));
     CK(cudaStreamSynchronize(ctx->st));
     return LA_OK;
+}
+
+int la_debug_state(la_ctx* ctx, int32_t* hdr, int32_t* levels, int32_t* level_len, int32_t* row_tok, int32_t* row_pos,
+                   int32_t* row_meta) {
+    if (!ctx) return LA_EINVAL;
+    return debug_state_of(ctx, ctx->d, hdr, levels, level_len, row_tok, row_pos, row_meta);
+}
+
+int la_debug_batch_state(la_ctx* ctx, int b, int32_t* hdr, int32_t* levels, int32_t* level_len, int32_t* row_tok,
+                         int32_t* row_pos, int32_t* row_meta) {
+    if (!ctx || b < 0) return LA_EINVAL;
+    if (ctx->max_batch < 2) return LA_ENOTSUP;
+    if (b >= ctx->max_batch) return LA_EINVAL;
+    return debug_state_of(ctx, ctx->req[b], hdr, levels, level_len, row_tok, row_pos, row_meta);
 }
 
 int la_debug_pool(la_ctx* ctx, int key, int32_t* suffixes, int* count) {
