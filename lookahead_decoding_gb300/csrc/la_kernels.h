@@ -2,9 +2,11 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 struct LaDev;
+struct LaHdr;
 
 // epilogues of the GEMMs
 #define GEMM_STORE 0   // out[q][n] = acc                       (element type of the model)
@@ -170,6 +172,7 @@ struct TcGemm {
     void* wpack;          // unit-contiguous weight images (la_tc_pack), or null: the tensor maps
     int defer;            // 1: split tiles left as partials for the consumer (LaSplit)
     int ctr_off;          // first split-tile counter of this GEMM (counters are per GEMM)
+    const void* act;      // the activation rows [rows_alloc][K] the tensor maps cover
 };
 #define LA_TC_CTR_PER_TILE 2   // ints per split-tile arrival counter (one 64-bit word)
 struct TcWork {
@@ -232,3 +235,49 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
                                      int krow0, int vrow0, const LaHdr* const* req_hdr = nullptr, int qstride = 0,
                                      long long req_cache_elems = 0, int req_cache_rows = 0, int temp_stride = 0,
                                      int tail_rows = 0, const LaRope* rope = nullptr);
+
+// ---------------------------------------------------------------------------
+// Layer-chain kernel (la_mega.cu): one launch runs a chain of GEMM and row
+// phases of a decode call on one CTA per SM (see la_mega.cu).
+// ---------------------------------------------------------------------------
+#define MG_MAX_PHASES 8
+#define MG_MAX_GEMMS 4
+#define MG_MAX_ROWS 4
+#define MG_MAX_ROWS_PER_CALL 256      // packed rows a chain supports (one 256-row chunk)
+enum { MG_PH_GEMM = 0, MG_PH_ROWS = 1 };
+enum { MG_RMS = 0, MG_RMS_GATHER = 1, MG_SWIGLU = 2 };
+
+struct MgGemm {
+    const uint8_t* wpack;                 // unit-contiguous weight images (la_tc_pack)
+    const __nv_bfloat16* act;             // activation rows [rows][K] (row stride K)
+    int mode, K, n_tiles, k_tiles, ua, k_atoms, nA, max_seg, sel, defer, n_cta;
+    float* ws;                            // split-tile partial records (LaSplit layout)
+    unsigned long long* ctr;              // split-tile arrival counters (non-deferred GEMMs)
+    void* out; int ldo;
+    float* logits; int ld_logits;         // GEMM_LOGITS: optional fp32 logits
+    float* part_v; int* part_i; int part_stride;   // GEMM_LOGITS: argmax partials per tile
+};
+struct MgRows {
+    int kind, sel, dm;
+    float eps;
+    float* x;                             // RMS: the fp32 residual rows (updated in place)
+    const __nv_bfloat16* g;               // RMS: gains
+    __nv_bfloat16* y;                     // RMS: normalised rows; SWIGLU: the activation rows
+    int ldo;                              // SWIGLU: row stride of y
+    LaSplit split;                        // partials of the GEMM that wrote x (RMS) or gate/up (SWIGLU)
+};
+struct MgParams {
+    LaHdr* hdr;
+    const int32_t* need;                  // needed rows (MG_RMS_GATHER)
+    unsigned long long* bar;              // this launch's phase counters [MG_MAX_PHASES] (zero at launch)
+    int n_ph;
+    int ph_kind[MG_MAX_PHASES], ph_idx[MG_MAX_PHASES];
+    MgGemm g[MG_MAX_GEMMS];
+    MgRows r[MG_MAX_ROWS];
+    int rows_cap;                         // the most rows any call of this launch has
+    int ns_pre;                           // ring stages whose weights are issued before the header is read
+};
+cudaError_t la_launch_mega(const MgParams& p, cudaStream_t st);
+int la_mega_ring_stages(int rows);        // ring stages at `rows` packed rows
+int la_tc_unit_atoms(int mode);
+
