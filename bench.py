@@ -337,6 +337,7 @@ WORKLOADS = {
                  "prompt": "code", "prompt_len": 2048, "max_new": 512, "seed": 4, "knobs": (10, 5, 10),
                  "options": 0, "cfg": "LLAMA_13B"},
 }
+# the nominal HBM3e bandwidth the step roofline is also quoted against
 SPEC_HBM_GBS = 8000.0
 # the dominant kernel of a packed call: its kind in the kernel-timing totals,
 # the committed ncu summary holding its DRAM traffic, and the sources that
@@ -344,7 +345,7 @@ SPEC_HBM_GBS = 8000.0
 DOMINANT = {"kind": "gemm", "profile": "k_gemm_tc_llama7b_decode_call.md",
             "sources": ["la_gemm_tc.cu", "la_common.cuh", "la_kernels.h"],
             "what": "k_gemm_tc (tcgen05 GEMMs: QKV, O, gate/up, down per layer + LM head), per call: "
-                    "algorithmic bytes / summed launch time"}      # the nominal HBM3e bandwidth the step roofline is also quoted against
+                    "algorithmic bytes / summed launch time"}
 
 
 def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
