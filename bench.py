@@ -321,8 +321,11 @@ def run_batch(args, cfg, rank: int, local: int) -> None:
 
 
 # The single-request workloads: the headline (the pages' plain configuration
-# on the 7B shape) and two where the n-gram pool retrieves candidates the
-# model accepts (pool seeding on the same prompt; the copy-heavy 13B prompt).
+# on the 7B shape); pool seeding on the same prompt and the copy-heavy 13B
+# prompt, where a trained model would accept the pool's candidates (a
+# random-init one does not continue the prompt's n-grams); and a 7B-shape
+# model whose greedy next token is nearly a function of the current token,
+# where the collected n-grams come true and calls commit several tokens.
 WORKLOADS = {
     "headline": {"desc": "llama-7b-shape bf16, batch 1, prompt 512 Markov/Zipf(1.1), 256 new tokens, greedy, "
                          "W=15 N=5 G=15", "model": "llama-7b-shape (random init)", "prompt": "markov",
@@ -336,6 +339,12 @@ WORKLOADS = {
                          "512 new tokens, greedy, W=10 N=5 G=10", "model": "llama-13b-shape (random init)",
                  "prompt": "code", "prompt_len": 2048, "max_new": 512, "seed": 4, "knobs": (10, 5, 10),
                  "options": 0, "cfg": "LLAMA_13B"},
+    "predictable-7b": {"desc": "llama-7b-shape bf16 with attention output projections scaled by 2^-10 (next token "
+                               "nearly a function of the current one), batch 1, prompt 512 Markov/Zipf(1.1), "
+                               "256 new tokens, greedy, W=15 N=5 G=15",
+                       "model": "llama-7b-shape (random init, wo x 2^-10)", "prompt": "markov",
+                       "prompt_len": PROMPT_LEN, "max_new": MAX_NEW, "seed": 2, "knobs": (W_, N_, G_), "options": 0,
+                       "cfg": "LLAMA_7B", "wo_scale": 2.0 ** -10},
 }
 # the nominal HBM3e bandwidth the step roofline is also quoted against
 SPEC_HBM_GBS = 8000.0
@@ -346,6 +355,30 @@ DOMINANT = {"kind": "gemm", "profile": "k_gemm_tc_llama7b_decode_call.md",
             "sources": ["la_gemm_tc.cu", "la_common.cuh", "la_kernels.h"],
             "what": "k_gemm_tc (tcgen05 GEMMs: QKV, O, gate/up, down per layer + LM head), per call: "
                     "algorithmic bytes / summed launch time"}
+
+
+def timeline_per_call(L, ctx, prompt, W: int, N: int, G: int, calls: int = 16):
+    """Per-kind device time of a packed call from the library's kernel
+    timeline (global-timer stamps per CTA, no events in the graph): one more
+    request, prefill untimed, then `calls` packed calls one by one; every
+    instant is charged to the running CTA that finishes next, so the kinds
+    add up to the calls' device time (host gaps between calls are left out)."""
+    import numpy as np
+    cap = 120_000 * calls
+    L.la_prefill(ctx.ctx, prompt)
+    L.la_timeline_start(cap)
+    try:
+        for _ in range(calls):
+            L.la_step(ctx.ctx, W, N, G)
+    finally:
+        rec = L.la_timeline_stop(cap)
+    split = L.timeline_split(rec)
+    ms = {k: v * 1e-6 / calls for k, v in split["ns"].items() if v}
+    return {"ms": ms, "by_kernel_ms": {k: v * 1e-6 / calls for k, v in split["by_kernel_ns"].items()},
+            "launches_per_call": float(np.sum(1.0 / rec[:, 4])) / calls if len(rec) else 0.0,
+            "what": ("split of %d packed calls' device time from per-CTA global-timer stamps (every instant "
+                     "charged to the running CTA that finishes next); the kinds add up to the calls' device "
+                     "time, host gaps between the calls left out" % calls)}
 
 
 def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
@@ -359,7 +392,7 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
     W, N, G = wl["knobs"]
     max_new = args.max_new if args.workload == "headline" else wl["max_new"]
     plen = wl["prompt_len"]
-    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}")
+    w = synth.llama_weights(cfg, 0, device=f"cuda:{local}", wo_scale=wl.get("wo_scale", 1.0))
     ctx = L.Context(cfg, w, max_ctx=max(1024, plen + max_new + 64), max_W=W, max_N=N, max_G=G)
     if wl["options"]:
         L.la_set_options(ctx.ctx, wl["options"])
@@ -416,6 +449,7 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
     L.la_generate(ctx.ctx, prompt, max_new, W, N, G, stats=st_prof)
     prof = L.la_profile_read(ctx.ctx)
     L.la_set_debug(ctx.ctx, 0)
+    tl = timeline_per_call(L, ctx, prompt, W, N, G)
 
     launches = sum(s.kernel_launches for s in stats)        # counted by the library
     peaks, src = measured_peaks()
@@ -473,7 +507,11 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
                           "frac_of_spec_8tbs": step_achieved / SPEC_HBM_GBS,
                           "algorithmic_bytes_per_call": bytes_call,
                           "what": "whole packed call: weights once + committed K/V read + temporary K/V written"},
-        "kernel_ms_per_call": {k: v / samples for k, v in prof["ms"].items()},
+        "kernel_ms_per_call": tl["ms"],
+        "kernel_timing": tl["what"],
+        "kernel_ms_per_call_by_kernel": tl["by_kernel_ms"],
+        "kernel_ms_per_call_sum": sum(tl["ms"].values()),
+        "kernel_ms_bracketed_per_call": {k: v / samples for k, v in prof["ms"].items()},
         "clocks": clk,
         "gpu_launches": launches,
     }

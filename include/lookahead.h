@@ -315,6 +315,29 @@ int la_debug_layer(la_ctx* ctx, int layer, int what, void* host, int rows);
  * Errors: LA_EINVAL. */
 int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* samples);
 
+/* Kernel timeline (process-wide; every context's kernels are recorded).
+ * la_timeline_start opens a table for up to max_ctas CTA records (32 bytes
+ * each, device memory the library owns until la_timeline_stop); from then on
+ * every CTA of every library kernel records its start and end on the GPU's
+ * global nanosecond timer, the kernel's id, its linear CTA index and the
+ * grid's CTA count.  Ids: 0 tensor-core GEMM, 1 CUDA-core GEMM, 2 fused
+ * attention, 3 CUDA-core attention, 4 embedding, 5 RMSNorm, 6 and 7 RoPE,
+ * 8 SwiGLU, 9 and 10 argmax, 11 sampling verifier, 12 request begin, 13 pack,
+ * 14 pool seeding, 15 publish, 16 K/V commit, 17 injected outputs,
+ * 18-20 prefill rows / needed row / finish, 21 layer chain.  The call
+ * synchronises the device before and after.
+ * la_timeline_stop synchronises, closes the table and writes up to cap
+ * records to rec (host, 5 int64 each: start ns, end ns, id, CTA, CTAs of the
+ * grid), ordered by start; *n (host) = CTAs that took a record, also when
+ * above max_ctas or cap (the records beyond are lost).
+ * Charging every instant of the device time to the running CTA that
+ * finishes next splits the time of a call into kernels on its critical path
+ * and adds up to that time.
+ * Errors: LA_EINVAL (max_ctas < 1, null n, a second start), LA_ESTATE
+ * (stop without start), LA_ECUDA. */
+int la_timeline_start(int64_t max_ctas);
+int la_timeline_stop(int64_t* rec, int64_t cap, int64_t* n);
+
 /* fp32 logits [*n_rows][vocab] of the last call's needed rows and their
  * packed row indices.  host buffers of capacity cap_rows rows.
  * The needed rows are those whose outputs the step reads (M7.3 §0x04A row

@@ -23,7 +23,8 @@ EXPORTS = ["la_init", "la_prefill", "la_step", "la_generate", "la_generate_ar", 
            "la_debug_state", "la_debug_pool", "la_step_inject", "la_query", "la_free", "la_strerror",
            "la_last_cuda_error", "la_debug_sample_verify", "la_debug_gemm", "la_bench_gemm",
            "la_gemm_noalloc", "la_profile_read", "la_set_options", "la_init_batch", "la_generate_batch",
-           "la_debug_layer", "la_debug_batch_logits", "la_debug_batch_state"]
+           "la_debug_layer", "la_debug_batch_logits", "la_debug_batch_state", "la_timeline_start",
+           "la_timeline_stop"]
 
 # pool seeding options (la_set_options)
 LA_OPT_POOL_FROM_PROMPT, LA_OPT_POOL_FROM_OUTPUT, LA_OPT_SLICE_WINDOW = 1, 2, 4
@@ -83,6 +84,8 @@ def _load() -> C.CDLL:
         "la_set_debug": (C.c_int, [vp, C.c_int]),
         "la_set_options": (C.c_int, [vp, C.c_uint32]),
         "la_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+        "la_timeline_start": (C.c_int, [C.c_int64]),
+        "la_timeline_stop": (C.c_int, [C.POINTER(C.c_int64), C.c_int64, C.POINTER(C.c_int64)]),
         "la_debug_logits": (C.c_int, [vp, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
         "la_debug_layer": (C.c_int, [vp, C.c_int, C.c_int, vp, C.c_int]),
         "la_debug_batch_logits": (C.c_int, [vp, C.c_int, f32p, i32p, C.c_int, C.POINTER(C.c_int)]),
@@ -236,6 +239,76 @@ def la_profile_read(ctx) -> Dict[str, object]:
     _check(LIB.la_profile_read(ctx, ms, n, C.byref(samples)), "la_profile_read", ctx)
     return {"ms": dict(zip(PROFILE_KINDS, list(ms))), "launches": dict(zip(PROFILE_KINDS, list(n))),
             "samples": int(samples.value)}
+
+
+TIMELINE_KINDS = ("gemm", "attention", "rowwise", "state", "chain")
+# kernel ids of the timeline records and the kind of each
+TIMELINE_IDS = (("k_gemm_tc", "gemm"), ("k_gemm_ffma", "gemm"), ("k_attn_fused", "attention"),
+                ("k_attention", "attention"), ("k_embed", "rowwise"), ("k_rmsnorm", "rowwise"),
+                ("k_rope_kv", "rowwise"), ("k_rope_kv4", "rowwise"), ("k_swiglu_split", "rowwise"),
+                ("k_argmax_rows", "rowwise"), ("k_argmax_reduce", "rowwise"), ("k_sample_verify", "state"),
+                ("k_begin", "state"), ("k_pack", "state"), ("k_pool_seed", "state"), ("k_publish", "state"),
+                ("k_commit_kv", "state"), ("k_inject_map", "state"), ("k_prefill_rows", "state"),
+                ("k_prefill_need", "state"), ("k_prefill_finish", "state"), ("k_mega", "chain"))
+
+
+def la_timeline_start(max_ctas: int) -> None:
+    """Opens the process-wide kernel timeline for up to max_ctas CTA records."""
+    _check(LIB.la_timeline_start(int(max_ctas)), "la_timeline_start")
+
+
+def la_timeline_stop(cap: int) -> np.ndarray:
+    """Closes the timeline: int64 [CTAs, 5] = (start ns, end ns, kernel id,
+    CTA, CTAs of the grid), in start order.  Raises if records were lost."""
+    rec = np.zeros((max(1, cap), 5), dtype=np.int64)
+    n = C.c_int64()
+    _check(LIB.la_timeline_stop(rec.ctypes.data_as(C.POINTER(C.c_int64)), int(cap), C.byref(n)), "la_timeline_stop")
+    if n.value > cap:
+        raise RuntimeError(f"la_timeline_stop: {n.value} CTAs recorded, room for {cap}")
+    return rec[:n.value]
+
+
+def timeline_split(rec: np.ndarray) -> Dict[str, object]:
+    """Splits the device time of a timeline (rows in start order) by kernel:
+    every instant at which some CTA runs is charged to the running CTA that
+    finishes next; instants with none running are idle.  The charges plus
+    idle add up to the span from the first start to the last end."""
+    import heapq
+    by_id = {name: 0 for name, _ in TIMELINE_IDS}
+    ctas = {name: 0 for name, _ in TIMELINE_IDS}
+    idle = 0
+    rows = [(int(a), max(int(a), int(b)), int(k)) for a, b, k in rec[:, :3].tolist()] if len(rec) else []
+    heap: List[tuple] = []
+    i, n = 0, len(rows)
+    t = rows[0][0] if n else 0
+    while i < n or heap:
+        if not heap:
+            if rows[i][0] > t:
+                idle += rows[i][0] - t
+                t = rows[i][0]
+        while i < n and rows[i][0] <= t:
+            heapq.heappush(heap, (rows[i][1], rows[i][2]))
+            ctas[TIMELINE_IDS[rows[i][2]][0]] += 1
+            i += 1
+        if not heap:
+            continue
+        end, k = heap[0]
+        nxt = rows[i][0] if i < n else None
+        if nxt is not None and nxt < end:
+            by_id[TIMELINE_IDS[k][0]] += nxt - t
+            t = nxt
+        else:
+            by_id[TIMELINE_IDS[k][0]] += end - t
+            t = end
+            heapq.heappop(heap)
+            while heap and heap[0][0] <= t:
+                heapq.heappop(heap)
+    ns = {k: 0 for k in TIMELINE_KINDS}
+    for name, kind in TIMELINE_IDS:
+        ns[kind] += by_id[name]
+    span = (max(r[1] for r in rows) - rows[0][0]) if n else 0
+    return {"ns": ns, "by_kernel_ns": {k: v for k, v in by_id.items() if ctas[k]},
+            "ctas": {k: v for k, v in ctas.items() if v}, "idle_ns": idle, "span_ns": span}
 
 
 def la_debug_logits(ctx, cap_rows: int, vocab: int):

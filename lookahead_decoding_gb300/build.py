@@ -15,7 +15,7 @@ OUT = os.path.join(HERE, "liblookahead.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = ["la_api.cu", "la_state.cu", "la_model.cu", "la_gemm_tc.cu", "la_sample.cu", "la_attn.cu",
            "la_noalloc.cu", "la_mega.cu"]
-HEADERS = ["la_common.cuh", "la_kernels.h", "la_tc.cuh", os.path.join("..", "..", "include", "lookahead.h")]
+HEADERS = ["la_common.cuh", "la_kernels.h", "la_tc.cuh", "la_timeline.cuh", os.path.join("..", "..", "include", "lookahead.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-diag-suppress", "177"]
 

@@ -10,6 +10,7 @@
 #include <atomic>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -22,6 +23,7 @@ struct Graph {
     cudaGraphExec_t x = nullptr;
     int prof_begin = 0, prof_end = 0;   // the graph's timing event pairs (kernel-timing graphs)
     long long n_kernels = 0;            // kernel launches one execution runs
+    unsigned long long tl_epoch = 0;    // timeline session the graph's kernels record into (timeline graphs)
 };
 
 // kernel kinds of the kernel-timing mode
@@ -34,9 +36,17 @@ struct ProfPair {
 
 std::atomic<unsigned long long> g_launches{0};
 
+// the open kernel timeline (la_timeline_start), process-wide
+std::mutex g_tl_mu;
+LaTlRec* g_tl_table = nullptr;
+unsigned int g_tl_cap = 0;
+unsigned long long g_tl_epoch = 0;      // changes at every open and close
+
 }  // namespace
 
 void la_note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+// launches recorded into a graph at capture run only when it is launched
+static void la_unnote_launches(unsigned long long n) { g_launches.fetch_sub(n, std::memory_order_relaxed); }
 unsigned long long la_launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 struct la_ctx {
@@ -313,6 +323,7 @@ struct MgChain {
     explicit MgChain(la_ctx* ctx, unsigned long long* bar) {
         memset(&p, 0, sizeof(p));
         p.hdr = ctx->d.hdr;
+        p.tl = ctx->d.tl;
         p.need = ctx->d.need;
         p.bar = bar;
         p.rows_cap = ctx->Qmax;
@@ -565,17 +576,42 @@ static int enqueue_step(la_ctx* ctx) {
     return enqueue_publish_commit(ctx, ctx->sampling);
 }
 
+// Points every kernel-argument block of the context at the open timeline
+// table (nullptr when none), before anything is launched or captured.
+static void tl_sync(la_ctx* ctx) {
+    LaTlRec* t = g_tl_table;
+    ctx->d.tl = t;
+    ctx->bd.tl = t;
+    for (auto& e : ctx->req) e.tl = t;
+    for (auto& e : ctx->req_pf) e.tl = t;
+}
+
+static void drop_graph(Graph& g) {
+    if (g.x) cudaGraphExecDestroy(g.x);
+    if (g.g) cudaGraphDestroy(g.g);
+    g.x = nullptr;
+    g.g = nullptr;
+}
+
 static int get_graph(la_ctx* ctx, Graph** out) {
-    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4) | (ctx->debug & 8) | (ctx->debug & 16);
+    int key = (ctx->debug & 1) | (ctx->sampling << 1) | (ctx->debug & 4) | (ctx->debug & 8) | (ctx->debug & 16) |
+              (g_tl_table ? 32 : 0);
     auto it = ctx->graphs.find(key);
-    if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
+    if (it != ctx->graphs.end()) {
+        if (!g_tl_table || it->second.tl_epoch == g_tl_epoch) { *out = &it->second; return LA_OK; }
+        drop_graph(it->second);     // captured into an earlier timeline's table
+        ctx->graphs.erase(it);
+    }
+    tl_sync(ctx);
     Graph g;
+    g.tl_epoch = g_tl_epoch;
     CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
     ctx->prof_capture = (ctx->debug & 4) != 0;
     g.prof_begin = (int)ctx->prof.size();
     const unsigned long long n0 = la_launch_count();
     int r = enqueue_step(ctx);
     g.n_kernels = (long long)(la_launch_count() - n0);
+    la_unnote_launches((unsigned long long)g.n_kernels);
     ctx->prof_capture = false;
     g.prof_end = (int)ctx->prof.size();
     cudaGraph_t graph = nullptr;
@@ -627,10 +663,7 @@ const char* la_last_cuda_error(la_ctx* ctx) { return ctx ? ctx->last_err.c_str()
 void la_free(la_ctx* ctx) {
     if (!ctx) return;
     if (ctx->st) cudaStreamSynchronize(ctx->st);
-    for (auto& kv : ctx->graphs) {
-        if (kv.second.x) cudaGraphExecDestroy(kv.second.x);
-        if (kv.second.g) cudaGraphDestroy(kv.second.g);
-    }
+    for (auto& kv : ctx->graphs) drop_graph(kv.second);
     for (auto& pp : ctx->prof) {
         if (pp.a) cudaEventDestroy(pp.a);
         if (pp.b) cudaEventDestroy(pp.b);
@@ -971,6 +1004,58 @@ int la_profile_read(la_ctx* ctx, double* ms4, int64_t* launches4, int64_t* sampl
     return LA_OK;
 }
 
+// ---- kernel timeline (process-wide) ----
+int la_timeline_start(int64_t max_ctas) {
+    if (max_ctas < 1 || max_ctas > (int64_t(1) << 30)) return LA_EINVAL;
+    std::lock_guard<std::mutex> lk(g_tl_mu);
+    if (g_tl_table) return LA_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LA_ECUDA;
+    LaTlRec* t = nullptr;
+    const size_t bytes = sizeof(LaTlRec) * (size_t)(max_ctas + 1);
+    if (cudaMalloc(&t, bytes) != cudaSuccess) return LA_ECUDA;
+    const LaTlHead head{0u, (unsigned int)max_ctas};
+    if (cudaMemset(t, 0, bytes) != cudaSuccess || cudaMemcpy(t, &head, sizeof(head), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(t);
+        return LA_ECUDA;
+    }
+    g_tl_table = t;
+    g_tl_cap = (unsigned int)max_ctas;
+    ++g_tl_epoch;
+    return LA_OK;
+}
+
+int la_timeline_stop(int64_t* rec, int64_t cap, int64_t* n) {
+    if (!n || cap < 0 || (cap > 0 && !rec)) return LA_EINVAL;
+    std::lock_guard<std::mutex> lk(g_tl_mu);
+    if (!g_tl_table) return LA_ESTATE;
+    std::vector<LaTlRec> h((size_t)g_tl_cap + 1);
+    const cudaError_t e1 = cudaDeviceSynchronize();
+    const cudaError_t e2 = cudaMemcpy(h.data(), g_tl_table, sizeof(LaTlRec) * h.size(), cudaMemcpyDeviceToHost);
+    cudaFree(g_tl_table);
+    g_tl_table = nullptr;
+    g_tl_cap = 0;
+    ++g_tl_epoch;
+    if (e1 != cudaSuccess || e2 != cudaSuccess) return LA_ECUDA;
+    LaTlHead head;
+    std::memcpy(&head, &h[0], sizeof(head));
+    const unsigned int kept = std::min(head.count, head.cap);
+    std::vector<const LaTlRec*> used;
+    used.reserve(kept);
+    for (unsigned int i = 0; i < kept; ++i) used.push_back(&h[1 + i]);
+    std::stable_sort(used.begin(), used.end(),
+                     [](const LaTlRec* a, const LaTlRec* b) { return a->start < b->start; });
+    *n = (int64_t)head.count;
+    for (int64_t i = 0; i < (int64_t)used.size() && i < cap; ++i) {
+        const LaTlRec* x = used[i];
+        rec[5 * i + 0] = (int64_t)x->start;
+        rec[5 * i + 1] = (int64_t)x->end;
+        rec[5 * i + 2] = (int64_t)x->id;
+        rec[5 * i + 3] = (int64_t)x->block;
+        rec[5 * i + 4] = (int64_t)x->blocks;
+    }
+    return LA_OK;
+}
+
 // three timing events, destroyed on every return path
 struct Events3 {
     cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
@@ -1037,6 +1122,7 @@ int la_prefill(la_ctx* ctx, const int32_t* prompt, int n, const la_sampling* s, 
     if (!ctx || !first_token) return LA_EINVAL;
     int r = check_sampling(s);
     if (r) return r;
+    tl_sync(ctx);
     r = do_prefill(ctx, prompt, n, s, solo_lane(ctx));
     if (r) return r;
     LaHdr h;
@@ -1075,6 +1161,7 @@ int la_step(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int32_t* out
     if (!ctx->prefilled) return LA_ESTATE;
     if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
     if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    tl_sync(ctx);
     int r;
     if (!ctx->begun) {
         r = begin_request(ctx, MODE_LOOKAHEAD, W, N, G, s, ctx->out_cap);
@@ -1103,6 +1190,7 @@ int la_step_inject(la_ctx* ctx, int W, int N, int G, const la_sampling* s, int Q
     if (!ctx->prefilled) return LA_ESTATE;
     if (N < 3 || W < 1 || G < 0) return LA_EINVAL;
     if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
+    tl_sync(ctx);
     int r;
     if (!ctx->begun) {
         r = begin_request(ctx, MODE_LOOKAHEAD, W, N, G, s, ctx->out_cap);
@@ -1148,6 +1236,7 @@ static int run_generate(la_ctx* ctx, int mode, const int32_t* prompt, int n, int
         if (N > ctx->max_N || W > ctx->max_W || G > ctx->max_G) return LA_ECAPACITY;
     }
     if (n + max_new > ctx->max_ctx) return LA_ECAPACITY;
+    tl_sync(ctx);
     Events3 ev;
     CK(ev.create());
     cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];
@@ -1218,12 +1307,18 @@ int la_generate_ar(la_ctx* ctx, const int32_t* prompt, int n, int max_new, const
 // and commit.
 static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
     const int keep = sampling | (ctx->debug & 1);
-    const int key = 0x100 | B | (sampling << 12) | ((ctx->debug & 1) << 13);
+    const int key = 0x100 | B | (sampling << 12) | ((ctx->debug & 1) << 13) | (g_tl_table ? (1 << 14) : 0);
     auto it = ctx->graphs.find(key);
-    if (it != ctx->graphs.end()) { *out = &it->second; return LA_OK; }
+    if (it != ctx->graphs.end()) {
+        if (!g_tl_table || it->second.tl_epoch == g_tl_epoch) { *out = &it->second; return LA_OK; }
+        drop_graph(it->second);     // captured into an earlier timeline's table
+        ctx->graphs.erase(it);
+    }
+    tl_sync(ctx);
     const la_model_cfg& c = ctx->cfg;
     const size_t head_bytes = (size_t)c.head_dim * ctx->esz;
     Graph g;
+    g.tl_epoch = g_tl_epoch;
     CK(cudaStreamBeginCapture(ctx->st, cudaStreamCaptureModeRelaxed));
     const unsigned long long n0 = la_launch_count();
     int r = LA_OK;
@@ -1241,6 +1336,7 @@ static int get_batch_graph(la_ctx* ctx, int B, int sampling, Graph** out) {
                                        (char*)ctx->cache + (size_t)b * ctx->cache_bytes_req,
                                        (char*)ctx->temp + (size_t)b * ctx->Qstride * head_bytes, ctx->temp_rows);
     g.n_kernels = (long long)(la_launch_count() - n0);
+    la_unnote_launches((unsigned long long)g.n_kernels);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(ctx->st, &graph);
     if (r) { if (graph) cudaGraphDestroy(graph); return r; }
@@ -1267,6 +1363,7 @@ int la_generate_batch(la_ctx* ctx, int B, const int32_t* prompts, const int32_t*
     // request 0's single-request state is reused: a later la_step needs a new prefill
     ctx->prefilled = false;
     ctx->begun = false;
+    tl_sync(ctx);
     Events3 ev;
     CK(ev.create());
     cudaEvent_t e0 = ev.e[0], e1 = ev.e[1], e2 = ev.e[2];

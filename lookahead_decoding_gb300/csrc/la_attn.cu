@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
                                                       const LaHdr* const* req_hdr, int qstride,
                                                       long long req_cache_elems, int req_cache_rows, int qrows,
                                                       LaRope rope) {
+    LaTl la_tl_(LA_TL_ATTN_FUSED, d.tl);
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
     // A batched call stacks its requests' rows in slices of qstride rows (a

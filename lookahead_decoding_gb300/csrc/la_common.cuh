@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/lookahead.h"
+#include "la_timeline.cuh"
 
 #define LA_MAX_R 8            // trajectory levels: N <= 9
 #define LA_MAX_G 32           // candidates per key (one warp lane each)
@@ -85,6 +86,7 @@ struct LaDev {
     int32_t row_base;
     int32_t pad_to;
     LaHdr* batch;
+    LaTlRec* tl;           // kernel timeline table (la_timeline.cuh), or nullptr
 };
 
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -119,8 +121,9 @@ __device__ __forceinline__ void la_pdl_trigger() { asm volatile("griddepcontrol.
 int la_pdl_enabled();
 int la_fuse_rope();      // decode calls of bf16 models: RoPE folded into the attention
 
-// Process-wide count of kernel launches the library has enqueued (a launch
-// recorded into a CUDA graph counts once, at capture).
+// Process-wide count of kernel launches the library has enqueued outside
+// graph capture (the launches recorded into a graph are taken back out once
+// captured: they run, and are counted, with each launch of the graph).
 void la_note_launch();
 unsigned long long la_launch_count();
 

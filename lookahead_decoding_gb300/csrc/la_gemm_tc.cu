@@ -54,6 +54,7 @@ constexpr int MAX_CHUNKS = 4;             // packed rows per launch <= MAX_CHUNK
 
 struct TcParams {
     LaHdr* hdr;
+    LaTlRec* tl;                     // kernel timeline table, or nullptr
     int sel, mode, K, Nout, k_tiles, n_tiles, seg_tiles, n_cta, max_seg;
     int ns, max_ns, rows_cap;        // stages at rows_cap rows (issued before the header), stage limit, rows per launch at most
     int ua, k_atoms;                 // 64-column atoms per unit (the last unit of a tile may hold fewer), K / 64
@@ -71,6 +72,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
           const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmB256, TcParams p) {
+    LaTl la_tl_(LA_TL_GEMM_TC, p.tl);
     LaHdr* h = p.hdr;
     const int swiglu = (p.mode == GEMM_SWIGLU);
     const int nA = swiglu ? 2 : 1;
@@ -137,6 +139,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     la_pdl_trigger();
     if (warp == 0) {
         int hdr_rows = 0;
+        int n_pre_all = n_pre;      // weight stages issued before the wait
         if (lane == 0) {
             for (int s = 0; s < MAX_STAGES; ++s) {
                 mbar_init(bar_full + 8 * s, 1);
@@ -167,6 +170,19 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             if (rows > p.rows_cap || (rows > 0 && (rows + BN_MAX - 1) / BN_MAX > p.max_chunks)) {
                 if (blockIdx.x == 0) la_set_err(h, LA_EDEVICE);
                 rows = -1;
+            }
+            // a call with fewer rows than rows_cap has a deeper ring: its
+            // further weight stages go out before the wait too
+            if (rows > 0) {
+                const uint32_t b_stage0 = (uint32_t)p.ua * (uint32_t)((min(BN_MAX, rows) + 15) & ~15) * ROW_BYTES;
+                const int ns0 = min(p.max_ns, (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage0)));
+                const int n_pre2 = min(ns0, n_units);
+                for (int i = n_pre; i < n_pre2; ++i) {
+                    const uint32_t wb = (uint32_t)(atoms_of(u_begin + i) * nA) * A_BYTES;
+                    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar_full + 8 * i), "r"(wb) : "memory");
+                    load_w(i, u_begin + i, pol_w);
+                }
+                n_pre_all = max(n_pre, n_pre2);
             }
             la_pdl_wait();
             *s_rows = rows;
@@ -204,7 +220,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     const long long u = u_begin + iu;
                     const int at0 = (int)(u % p.k_tiles) * p.ua, na = atoms_of(u);
                     const uint32_t xb = (uint32_t)(na * BN) * ROW_BYTES;
-                    if (it < n_pre) {
+                    if (it < n_pre_all) {
                         // the weight tiles are already on their way
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(xb) : "memory");
                     } else {
@@ -697,6 +713,7 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     if (rows_cap < 1 || rows_cap > MAX_CHUNKS * BN_MAX) return cudaErrorInvalidValue;
     TcParams p;
     p.hdr = d.hdr;
+    p.tl = d.tl;
     p.sel = sel;
     p.mode = g.mode;
     p.K = g.K;

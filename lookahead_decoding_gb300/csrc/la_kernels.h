@@ -7,6 +7,7 @@
 
 struct LaDev;
 struct LaHdr;
+struct LaTlRec;
 
 // epilogues of the GEMMs
 #define GEMM_STORE 0   // out[q][n] = acc                       (element type of the model)
@@ -184,6 +185,7 @@ struct TcWork {
     int* part_i;
     int part_stride;
 };
+
 int la_tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 int la_tc_make_act_maps(TcGemm* g, const void* base, int rows, int K);
 // rows_cap: the most rows any call of this launch (graph node) has
@@ -268,6 +270,7 @@ struct MgRows {
 };
 struct MgParams {
     LaHdr* hdr;
+    LaTlRec* tl;                          // kernel timeline table, or nullptr
     const int32_t* need;                  // needed rows (MG_RMS_GATHER)
     unsigned long long* bar;              // this launch's phase counters [MG_MAX_PHASES] (zero at launch)
     int n_ph;

@@ -120,6 +120,7 @@ __device__ __forceinline__ void arrive_count(unsigned long long* c) {
 }
 
 __global__ void __launch_bounds__(MG_THREADS, 1) k_mega(const __grid_constant__ MgParams p) {
+    LaTl la_tl_(LA_TL_CHAIN, p.tl);
     LaHdr* h = p.hdr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, NC = gridDim.x;

@@ -52,6 +52,7 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 
 template <typename T>
 __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
+    LaTl la_tl_(LA_TL_EMBED, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
@@ -88,6 +89,7 @@ __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
 template <typename T>
 __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g, T* y, int dm, float eps, int sel,
                                                  int gather, LaSplit resid) {
+    LaTl la_tl_(LA_TL_RMSNORM, d.tl);
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int row = blockIdx.x;
@@ -186,6 +188,7 @@ __device__ __forceinline__ T qkv_at(const T* row, int q, int n, const LaSplit& s
 template <typename T>
 __global__ void k_rope_kv(LaDev d, const T* qkv, const float* rcos, const float* rsin, T* qbuf, T* kdst, T* vdst,
                           int H, int dh, int sel, int Qcap, int stride, LaSplit sp) {
+    LaTl la_tl_(LA_TL_ROPE_KV, d.tl);
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int q = blockIdx.x;
@@ -229,6 +232,7 @@ __global__ void __launch_bounds__(256) k_rope_kv4(LaDev d, const __nv_bfloat16* 
                                                   const float* rsin, __nv_bfloat16* qbuf, __nv_bfloat16* kdst,
                                                   __nv_bfloat16* vdst, int H, int dh, int sel, int Qcap, int stride,
                                                   LaSplit sp) {
+    LaTl la_tl_(LA_TL_ROPE_KV4, d.tl);
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int q = blockIdx.x;
@@ -267,6 +271,7 @@ __global__ void __launch_bounds__(256) k_rope_kv4(LaDev d, const __nv_bfloat16* 
 // and up the sums of the segments' two accumulator planes.  One thread per
 // four consecutive columns of a row (float4 partial loads, all in flight at once).
 __global__ void __launch_bounds__(256) k_swiglu_split(LaDev d, LaSplit sp, __nv_bfloat16* act, int ldo, int sel) {
+    LaTl la_tl_(LA_TL_SWIGLU, d.tl);
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int q = blockIdx.x;
@@ -343,6 +348,7 @@ template <typename T, int DH, int RPW>
 __global__ void __launch_bounds__(256) k_attention(LaDev d, const T* qbuf, const T* kc, const T* vc, const T* kt,
                                                    const T* vt, T* out, int H, int sel, int Qcap, int max_ctx,
                                                    int Qmax, float scale) {
+    LaTl la_tl_(LA_TL_ATTENTION, d.tl);
     constexpr int DPL = DH / 32;
     constexpr int NW = 8;
     constexpr int RPC = NW * RPW;
@@ -463,6 +469,7 @@ __global__ void __launch_bounds__(256) k_attention(LaDev d, const T* qbuf, const
 template <typename T, int MODE>
 __global__ void __launch_bounds__(256) k_gemm_ffma(LaDev d, const T* X, int ldx, const T* Wm, const T* W2, int K,
                                                    int Nout, void* out, int ldo, int sel) {
+    LaTl la_tl_(LA_TL_GEMM_FFMA, d.tl);
     const LaHdr* h = d.hdr;
     if (skip_call(h, sel)) return;
     const int rows = rows_of(h, sel);
@@ -521,6 +528,7 @@ __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
     if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
 }
 __global__ void k_argmax_rows(LaDev d, const float* logits, int V, int sel) {
+    LaTl la_tl_(LA_TL_ARGMAX_ROWS, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;
@@ -549,6 +557,7 @@ __global__ void k_argmax_rows(LaDev d, const float* logits, int V, int sel) {
 
 // partial (value, index) per (vocab tile, row) -> argmax per row
 __global__ void k_argmax_reduce(LaDev d, const float* pv, const int* pi, int n_tiles, int stride, int sel) {
+    LaTl la_tl_(LA_TL_ARGMAX_REDUCE, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     const LaHdr* h = d.hdr;

@@ -300,6 +300,7 @@ __device__ void sample_verify_core(const SvIn& in, float* p, Red& r, SvOut& o) {
 }
 
 __global__ void __launch_bounds__(NT) k_sample_verify(LaDev d, const float* logits, int V, int prefill) {
+    LaTl la_tl_(LA_TL_SAMPLE_VERIFY, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     LaHdr* h = d.hdr;

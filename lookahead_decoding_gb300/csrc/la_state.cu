@@ -20,6 +20,7 @@
 // ---------------------------------------------------------------------------
 __global__ void k_begin(LaDev d, int mode, int W, int N, int G, int sampling,
                         float temperature, float top_p, uint32_t seed_lo, uint32_t seed_hi, int max_out, int opts) {
+    LaTl la_tl_(LA_TL_BEGIN, d.tl);
     LaHdr* h = d.hdr;
     int t = threadIdx.x;
     if (t == 0) {
@@ -53,6 +54,7 @@ __global__ void k_begin(LaDev d, int mode, int W, int N, int G, int sampling,
 // pack: token ids, logical positions, metadata, key paths, needed rows
 // ---------------------------------------------------------------------------
 __global__ void k_pack(LaDev d) {
+    LaTl la_tl_(LA_TL_PACK, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     LaHdr* h = d.hdr;
@@ -215,6 +217,7 @@ __device__ __forceinline__ void upsert_seq_ngram_warp(const LaDev& d, int P, int
 // the warp count, so each key's upserts keep their order.
 // ---------------------------------------------------------------------------
 __global__ void k_pool_seed(LaDev d) {
+    LaTl la_tl_(LA_TL_POOL_SEED, d.tl);
     const LaHdr* h = d.hdr;
     const int opts = h->opts, G = h->G, S = h->S, P = h->prompt_len;
     if (h->err || h->mode != MODE_LOOKAHEAD || G <= 0) return;
@@ -228,6 +231,7 @@ __global__ void k_pool_seed(LaDev d) {
 }
 
 __global__ void k_publish(LaDev d, int verdict_given) {
+    LaTl la_tl_(LA_TL_PUBLISH, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     LaHdr* h = d.hdr;
@@ -387,6 +391,7 @@ __global__ void k_publish(LaDev d, int verdict_given) {
 // ---------------------------------------------------------------------------
 __global__ void k_commit_kv(LaDev d, char* cache, char* temp, int n_heads, int head_bytes,
                             int max_ctx, int Qmax) {
+    LaTl la_tl_(LA_TL_COMMIT_KV, d.tl);
     la_pdl_wait();
     la_pdl_trigger();
     LaHdr* h = d.hdr;
@@ -411,6 +416,7 @@ __global__ void k_commit_kv(LaDev d, char* cache, char* temp, int n_heads, int h
 // ---------------------------------------------------------------------------
 __global__ void k_inject_map(LaDev d, const int32_t* argmax_rows, const float* logits_rows,
                              float* logits_need, int V) {
+    LaTl la_tl_(LA_TL_INJECT_MAP, d.tl);
     LaHdr* h = d.hdr;
     if (h->err || h->done) return;
     int n = h->n_need;
@@ -428,6 +434,7 @@ __global__ void k_inject_map(LaDev d, const int32_t* argmax_rows, const float* l
 // prefill rows of chunk [c0, c0+n): tokens and positions 0..P-1
 // ---------------------------------------------------------------------------
 __global__ void k_prefill_rows(LaDev d, int c0, int n) {
+    LaTl la_tl_(LA_TL_PREFILL_ROWS, d.tl);
     LaHdr* h = d.hdr;
     if (threadIdx.x == 0 && blockIdx.x == 0) { h->Q = n; h->prefill_rows = n; }
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -439,6 +446,7 @@ __global__ void k_prefill_rows(LaDev d, int c0, int n) {
 
 // the last prompt row is the only needed row of a prefill
 __global__ void k_prefill_need(LaDev d, int last_local) {
+    LaTl la_tl_(LA_TL_PREFILL_NEED, d.tl);
     LaHdr* h = d.hdr;
     h->n_need = 1;
     d.need[0] = last_local;
@@ -446,6 +454,7 @@ __global__ void k_prefill_need(LaDev d, int last_local) {
 
 // after the prefill: the frontier is the prompt, x_t the first token
 __global__ void k_prefill_finish(LaDev d, int P, int sampled_token_valid) {
+    LaTl la_tl_(LA_TL_PREFILL_FINISH, d.tl);
     LaHdr* h = d.hdr;
     if (h->err) return;
     h->K = P;

@@ -157,8 +157,21 @@ def make_weight(cfg: ModelConfig, name: str, seed: int = 0, device="cpu",
     return out.view(shape)
 
 
-def llama_weights(cfg: ModelConfig, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
-    return {n: make_weight(cfg, n, seed, device) for n in weight_names(cfg)}
+def llama_weights(cfg: ModelConfig, seed: int = 0, device="cpu", wo_scale: float = 1.0) -> Dict[str, torch.Tensor]:
+    """Every weight of the model.  ``wo_scale`` (a power of two, so the
+    stored values are the unscaled ones scaled exactly) multiplies the
+    attention output projections: at 2**-10 the attention adds almost
+    nothing to the residual stream, and the greedy next token becomes nearly
+    a function of the current token alone -- a random map whose walks run
+    into cycles, so the n-grams a lookahead window collects come true."""
+    m, e = math.frexp(wo_scale)
+    assert m == 0.5 and -40 < e <= 1, "wo_scale must be a power of two"
+    w = {n: make_weight(cfg, n, seed, device) for n in weight_names(cfg)}
+    if wo_scale != 1.0:
+        for n in w:
+            if n.endswith(".wo"):
+                w[n].mul_(wo_scale)
+    return w
 
 
 # --------------------------------------------------------------------------

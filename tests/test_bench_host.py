@@ -35,3 +35,31 @@ def test_parse_clocks(tmp_path):
                  "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
     c = bench.parse_clocks(str(p))
     assert c == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_timeline_split_adds_up_to_the_span():
+    """Every instant goes to the running CTA that finishes next (a CTA that
+    runs inside another's lifetime takes its own stretch), a gap with no CTA
+    is idle, and the charges plus idle equal the span."""
+    import numpy as np
+    from lookahead_decoding_gb300._lib import timeline_split
+    # start, end, kernel id, CTA, CTAs  (ns; ids 13 pack, 0 tensor-core GEMM, 5 RMSNorm, 2 fused attention)
+    rec = np.array([[0, 100, 13, 0, 1],
+                    [90, 300, 0, 0, 152],
+                    [250, 280, 5, 0, 64],
+                    [295, 400, 2, 0, 128],
+                    [450, 470, 0, 1, 152]], dtype=np.int64)
+    s = timeline_split(rec)
+    assert s["ns"] == {"gemm": 190, "attention": 100, "rowwise": 30, "state": 100, "chain": 0}
+    assert s["by_kernel_ns"] == {"k_gemm_tc": 190, "k_attn_fused": 100, "k_rmsnorm": 30, "k_pack": 100}
+    assert s["ctas"] == {"k_gemm_tc": 2, "k_attn_fused": 1, "k_rmsnorm": 1, "k_pack": 1}
+    assert s["idle_ns"] == 50 and s["span_ns"] == 470
+    assert sum(s["ns"].values()) + s["idle_ns"] == s["span_ns"]
+    assert timeline_split(rec[:0])["span_ns"] == 0
+    # random intervals: the identity holds whatever the overlap
+    rng = np.random.default_rng(1)
+    st = np.sort(rng.integers(0, 10_000, 300))
+    r = np.stack([st, st + rng.integers(0, 500, 300), rng.integers(0, 22, 300), np.zeros(300, int),
+                  np.ones(300, int)], axis=1).astype(np.int64)
+    q = timeline_split(r)
+    assert sum(q["ns"].values()) + q["idle_ns"] == q["span_ns"] == int(r[:, 1].max() - r[0, 0])

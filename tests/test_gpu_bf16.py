@@ -83,6 +83,73 @@ def test_step_by_step_mid(mid, W, N, G):
     L.la_set_debug(ctx.ctx, 0)
 
 
+@pytest.fixture(scope="module")
+def mid_pred():
+    """MID with the attention output projections scaled by 2**-10: the greedy
+    next token is nearly a function of the current one, so the pool's
+    n-grams come true and calls accept candidates on real logits."""
+    from lookahead_decoding_gb300 import lib
+    w = synth.llama_weights(MID, 0, device="cuda:0", wo_scale=2.0 ** -10)
+    ctx = context(MID, w, max_ctx=640, W=15, N=5, G=15)
+    oracle = OracleModel(MID, {k: v.cpu() for k, v in w.items()}, store="bf16")
+    yield lib(), ctx, oracle
+    ctx.close()
+
+
+def test_accepting_calls_against_oracle_mid(mid_pred):
+    """Call by call against the oracle on a model whose candidates are
+    accepted: rows, needed-row logits within 3e-2, the verdict and the
+    emitted tokens (the GPU's argmax followed where the oracle's top-2 gap is
+    under TIE); the run must include calls that commit several tokens (the
+    accepted rows' K/V then feed every later call's logits)."""
+    L, ctx, oracle = mid_pred
+    W, N, G = 15, 5, 15
+    p = synth.markov_zipf_prompt(MID.vocab, 64, 5).tolist()
+    L.la_set_debug(ctx.ctx, 1)
+    first = L.la_prefill(ctx.ctx, p)
+    cache, _ = oracle.prefill(p)
+    st = la.LookaheadState(p, first, W, N, G)
+    run = la.make_runner(oracle, cache, "meta")
+    multi = 0
+    for step in range(60):
+        rows, guesses = st.plan()
+        ref = run.run(rows)
+        em = L.la_step(ctx.ctx, W, N, G)
+        h, _, tok, pos, _ = L.la_debug_state(ctx.ctx)
+        assert tok == [r.token for r in rows] and pos == [r.position for r in rows]
+        lg, need = L.la_debug_logits(ctx.ctx, 1024, MID.vocab)
+        assert need.tolist() == [r.packed_index for r in rows if r.request_logit]
+        err = np.max(np.abs(lg - ref[need]))
+        assert err < LOGIT_TOL, (step, err)
+        argmax = [argmax_lowest(x) for x in ref]
+        for i, r in enumerate(need):
+            g = int(np.argmax(lg[i]))
+            assert g == argmax[r] or top2_gap(ref[r]) < TIE
+            argmax[r] = g
+        info = st.publish(rows, guesses, argmax)
+        run.commit(rows, info.commit_rows)
+        assert em == info.emitted, step
+        multi += len(em) > 1
+    L.la_set_debug(ctx.ctx, 0)
+    assert multi >= 5, multi
+
+
+def test_accepting_generate_equals_ar_mid(mid_pred):
+    """Whole requests with accepted candidates: lookahead == AR token for
+    token, more than one token per call, and the oracle's greedy choice
+    given the GPU's prefix (teacher forced)."""
+    L, ctx, oracle = mid_pred
+    p = synth.markov_zipf_prompt(MID.vocab, 96, 7).tolist()
+    ar = L.la_generate_ar(ctx.ctx, p, 160)
+    for W, N, G in [(15, 5, 15), (7, 4, 7)]:
+        st = L.la_stats()
+        got = L.la_generate(ctx.ctx, p, 160, W, N, G, stats=st)
+        assert got == ar, (W, N, G)
+        assert (st.tokens - 1) / st.steps > 1.2, (W, N, G, st.tokens, st.steps)
+        assert sum(st.emitted_hist[1:]) > 0
+    teacher_forced_check(oracle, p, ar)
+
+
 def teacher_forced_check(oracle, prompt, tokens):
     """Every GPU token equals the oracle's greedy choice given the GPU's own prefix,
     except where the oracle's top-2 gap is below TIE.  Returns the number of ties."""

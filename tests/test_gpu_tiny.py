@@ -283,3 +283,34 @@ def test_error_contract(setup):
         assert (h1["K"], h1["n_out"], lv1) == (h2["K"], h2["n_out"], lv2)
     finally:
         c2.close()
+
+
+def test_kernel_timeline_records_every_launch(setup):
+    """The timeline holds one record per CTA of every kernel the library
+    launched: each launch contributes its grid's CTA count of records (so the
+    records weighted by 1/CTAs add up to the library's own launch count),
+    every record ends after it starts, with a known kernel id and a CTA index
+    inside its grid; a second start while open and a stop without one fail;
+    the outputs are those of an untimed run."""
+    L, ctx, _, _ = setup
+    p = prompt(24, 5)
+    ref = L.la_generate(ctx.ctx, p, 20, 8, 5, 8)
+    st = L.la_stats()
+    L.la_timeline_start(1 << 20)
+    try:
+        with pytest.raises(RuntimeError):
+            L.la_timeline_start(16)
+        out = L.la_generate(ctx.ctx, p, 20, 8, 5, 8, stats=st)
+    finally:
+        rec = L.la_timeline_stop(1 << 20)
+    with pytest.raises(RuntimeError):
+        L.la_timeline_stop(16)
+    assert list(out) == list(ref)
+    assert st.kernel_launches > 0
+    assert abs(float(np.sum(1.0 / rec[:, 4])) - st.kernel_launches) < 1e-6 * st.kernel_launches
+    assert np.all(rec[:, 1] >= rec[:, 0]) and np.all(rec[:, 0] > 0)
+    assert np.all((rec[:, 2] >= 0) & (rec[:, 2] < len(L.TIMELINE_IDS)))
+    assert np.all((rec[:, 3] >= 0) & (rec[:, 3] < rec[:, 4]))
+    split = L.timeline_split(rec)
+    assert sum(split["ns"].values()) + split["idle_ns"] == split["span_ns"]
+    assert split["ns"]["gemm"] > 0 and split["ns"]["attention"] > 0 and split["ns"]["state"] > 0

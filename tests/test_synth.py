@@ -43,3 +43,22 @@ def test_markov_rank_law():
     n = 20000
     r1 = sum(int(np.searchsorted(mc.cdf, mc._u(), side="left")) == 0 for _ in range(n))
     assert abs(r1 / n - mc.cdf[0]) < 4 * np.sqrt(mc.cdf[0] * (1 - mc.cdf[0]) / n)
+
+
+def test_wo_scale_scales_only_the_attention_output_exactly():
+    """A power-of-two scale changes the wo tensors by exactly that factor
+    (bf16 and fp32 storage) and leaves every other tensor alone; other
+    scales are refused."""
+    import dataclasses
+    import pytest
+    import torch
+    for cfg in (synth.TINY, dataclasses.replace(synth.TINY, dtype="bf16")):
+        a = synth.llama_weights(cfg, 3)
+        b = synth.llama_weights(cfg, 3, wo_scale=2.0 ** -10)
+        for n in a:
+            if n.endswith(".wo"):
+                assert torch.equal(b[n].float(), a[n].float() * 2.0 ** -10)
+            else:
+                assert torch.equal(a[n], b[n])
+    with pytest.raises(AssertionError):
+        synth.llama_weights(synth.TINY, 0, wo_scale=0.001)
