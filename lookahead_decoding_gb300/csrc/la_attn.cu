@@ -289,30 +289,35 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         __nv_bfloat16* qs_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
         __nv_bfloat16* kt_w = const_cast<__nv_bfloat16*>(kt) + (size_t)hh * temp_stride * DH;
         __nv_bfloat16* vt_w = const_cast<__nv_bfloat16*>(vt) + (size_t)hh * temp_stride * DH;
-        for (int i = tid; i < FR * (half / 4); i += blockDim.x) {
-            const int r = i / (half / 4), c4 = (i % (half / 4)) * 4;
-            __nv_bfloat16* qd = qs_w + r * LDK + c4;
+        // one item per (part, row, four dimensions): part 0 the query, 1 the
+        // key, 2 the value (no rotation), so every thread has one short chain
+        for (int i = tid; i < 3 * FR * (half / 4); i += blockDim.x) {
+            const int part = i / (FR * (half / 4)), j = i % (FR * (half / 4));
+            const int r = j / (half / 4), c4 = (j % (half / 4)) * 4;
             if (r >= nr) {
-                *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
-                *reinterpret_cast<uint2*>(qd + half) = make_uint2(0u, 0u);
+                if (part == 0) {
+                    __nv_bfloat16* qd = qs_w + r * LDK + c4;
+                    *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
+                    *reinterpret_cast<uint2*>(qd + half) = make_uint2(0u, 0u);
+                }
                 continue;
             }
             const int row = r0 + r, pos = rpos[r], lrow = row - req * qstride;
+            const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+            const int seg = part == 0 ? seg_q : (part == 1 ? seg_k : seg_v);
+            const int n0 = part * HD + hh * DH + c4;
+            const float4 a = la_qkv_at4(x, row, n0, rope.sp, seg);
+            const float4 b = la_qkv_at4(x, row, n0 + half, rope.sp, seg);
+            if (part == 2) {
+                __nv_bfloat16* vo = vt_w + (size_t)lrow * DH + c4;
+                *reinterpret_cast<uint2*>(vo) = la_pack_bf16x4(a.x, a.y, a.z, a.w);
+                *reinterpret_cast<uint2*>(vo + half) = la_pack_bf16x4(b.x, b.y, b.z, b.w);
+                continue;
+            }
             const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
             const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
-            const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
-            const float4 qa = la_qkv_at4(x, row, hh * DH + c4, rope.sp, seg_q);
-            const float4 qb = la_qkv_at4(x, row, hh * DH + c4 + half, rope.sp, seg_q);
-            const float4 ka = la_qkv_at4(x, row, HD + hh * DH + c4, rope.sp, seg_k);
-            const float4 kb = la_qkv_at4(x, row, HD + hh * DH + c4 + half, rope.sp, seg_k);
-            const float4 va = la_qkv_at4(x, row, 2 * HD + hh * DH + c4, rope.sp, seg_v);
-            const float4 vb = la_qkv_at4(x, row, 2 * HD + hh * DH + c4 + half, rope.sp, seg_v);
-            la_rope4_store(qd, qd + half, qa, qb, c, s);
-            __nv_bfloat16* ko = kt_w + (size_t)lrow * DH + c4;
-            __nv_bfloat16* vo = vt_w + (size_t)lrow * DH + c4;
-            la_rope4_store(ko, ko + half, ka, kb, c, s);
-            *reinterpret_cast<uint2*>(vo) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
-            *reinterpret_cast<uint2*>(vo + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+            __nv_bfloat16* dst = part == 0 ? qs_w + r * LDK + c4 : kt_w + (size_t)lrow * DH + c4;
+            la_rope4_store(dst, dst + half, a, b, c, s);
         }
     }
     int t0max = 0, t0min = 0x7fffffff, posmax = 0;
@@ -541,21 +546,28 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
             // request's row urow[s] at its position, head hh, into slot nc + s
             __nv_bfloat16* tk_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.ring);
             __nv_bfloat16* tv_w = tk_w + (size_t)ring_keys * LDK;
-            for (int i = tid; i < (nt - nc) * (half / 4); i += blockDim.x) {
-                const int sl = i / (half / 4), c4 = (i % (half / 4)) * 4;
-                const int row = req * qstride + urow[sl], pos = d.row_pos[row];
+            // one item per (part, slot, four dimensions): part 0 the key
+            // (rotated at the row's position), 1 the value
+            const int nk = (nt - nc) * (half / 4);
+            for (int i = tid; i < 2 * nk; i += blockDim.x) {
+                const int part = i / nk, j = i % nk;
+                const int sl = j / (half / 4), c4 = (j % (half / 4)) * 4;
+                const int row = req * qstride + urow[sl];
+                const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+                const int n0 = (part + 1) * HD + hh * DH + c4;
+                const float4 a = la_qkv_at4(x, row, n0, rope.sp, part == 0 ? seg_k : seg_v);
+                const float4 b = la_qkv_at4(x, row, n0 + half, rope.sp, part == 0 ? seg_k : seg_v);
+                if (part == 1) {
+                    __nv_bfloat16* vd = tv_w + (size_t)(nc + sl) * LDK + c4;
+                    *reinterpret_cast<uint2*>(vd) = la_pack_bf16x4(a.x, a.y, a.z, a.w);
+                    *reinterpret_cast<uint2*>(vd + half) = la_pack_bf16x4(b.x, b.y, b.z, b.w);
+                    continue;
+                }
+                const int pos = d.row_pos[row];
                 const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
                 const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
-                const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
-                const float4 ka = la_qkv_at4(x, row, HD + hh * DH + c4, rope.sp, seg_k);
-                const float4 kb = la_qkv_at4(x, row, HD + hh * DH + c4 + half, rope.sp, seg_k);
-                const float4 va = la_qkv_at4(x, row, 2 * HD + hh * DH + c4, rope.sp, seg_v);
-                const float4 vb = la_qkv_at4(x, row, 2 * HD + hh * DH + c4 + half, rope.sp, seg_v);
                 __nv_bfloat16* kd = tk_w + (size_t)(nc + sl) * LDK + c4;
-                __nv_bfloat16* vd = tv_w + (size_t)(nc + sl) * LDK + c4;
-                la_rope4_store(kd, kd + half, ka, kb, c, s);
-                *reinterpret_cast<uint2*>(vd) = la_pack_bf16x4(va.x, va.y, va.z, va.w);
-                *reinterpret_cast<uint2*>(vd + half) = la_pack_bf16x4(vb.x, vb.y, vb.z, vb.w);
+                la_rope4_store(kd, kd + half, a, b, c, s);
             }
         }
         asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");

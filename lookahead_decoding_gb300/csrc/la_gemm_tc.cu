@@ -139,7 +139,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     la_pdl_trigger();
     if (warp == 0) {
         int hdr_rows = 0;
-        int n_pre_all = n_pre;      // weight stages issued before the wait
         if (lane == 0) {
             for (int s = 0; s < MAX_STAGES; ++s) {
                 mbar_init(bar_full + 8 * s, 1);
@@ -170,19 +169,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             if (rows > p.rows_cap || (rows > 0 && (rows + BN_MAX - 1) / BN_MAX > p.max_chunks)) {
                 if (blockIdx.x == 0) la_set_err(h, LA_EDEVICE);
                 rows = -1;
-            }
-            // a call with fewer rows than rows_cap has a deeper ring: its
-            // further weight stages go out before the wait too
-            if (rows > 0) {
-                const uint32_t b_stage0 = (uint32_t)p.ua * (uint32_t)((min(BN_MAX, rows) + 15) & ~15) * ROW_BYTES;
-                const int ns0 = min(p.max_ns, (int)((SMEM_BYTES - 1024 - 8192) / (a_stage + b_stage0)));
-                const int n_pre2 = min(ns0, n_units);
-                for (int i = n_pre; i < n_pre2; ++i) {
-                    const uint32_t wb = (uint32_t)(atoms_of(u_begin + i) * nA) * A_BYTES;
-                    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar_full + 8 * i), "r"(wb) : "memory");
-                    load_w(i, u_begin + i, pol_w);
-                }
-                n_pre_all = max(n_pre, n_pre2);
             }
             la_pdl_wait();
             *s_rows = rows;
@@ -220,7 +206,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     const long long u = u_begin + iu;
                     const int at0 = (int)(u % p.k_tiles) * p.ua, na = atoms_of(u);
                     const uint32_t xb = (uint32_t)(na * BN) * ROW_BYTES;
-                    if (it < n_pre_all) {
+                    if (it < n_pre) {
                         // the weight tiles are already on their way
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(xb) : "memory");
                     } else {

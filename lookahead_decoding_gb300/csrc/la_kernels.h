@@ -57,12 +57,13 @@ __host__ __device__ __forceinline__ const float* la_split_rec(const LaSplit& s, 
 
 #ifdef __CUDACC__
 // Sum over the segments (K order, from 0) of the element at `off` of plane pl;
-// the loads of up to four segments are issued together.
+// the loads of up to four segments are issued together (only the tile's own
+// segments: every request goes to L2).
 __device__ __forceinline__ float la_split_sum(const LaSplit& s, int t, int y, int pl, size_t off, int nseg) {
     const float t0 = __ldcg(la_split_rec(s, t, y, 0, pl) + off);
-    const float t1 = __ldcg(la_split_rec(s, t, y, nseg > 1 ? 1 : 0, pl) + off);
-    const float t2 = __ldcg(la_split_rec(s, t, y, nseg > 2 ? 2 : 0, pl) + off);
-    const float t3 = __ldcg(la_split_rec(s, t, y, nseg > 3 ? 3 : 0, pl) + off);
+    const float t1 = nseg > 1 ? __ldcg(la_split_rec(s, t, y, 1, pl) + off) : 0.f;
+    const float t2 = nseg > 2 ? __ldcg(la_split_rec(s, t, y, 2, pl) + off) : 0.f;
+    const float t3 = nseg > 3 ? __ldcg(la_split_rec(s, t, y, 3, pl) + off) : 0.f;
     float r = __fadd_rn(0.f, t0);
     if (nseg > 1) r = __fadd_rn(r, t1);
     if (nseg > 2) r = __fadd_rn(r, t2);
@@ -74,7 +75,8 @@ __device__ __forceinline__ float la_split_sum(const LaSplit& s, int t, int y, in
 __device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, size_t off, int nseg, int pl = 0) {
     float4 v[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k < nseg ? k : 0, pl) + off));
+    for (int k = 0; k < 4; ++k)
+        if (k < nseg) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k, pl) + off));
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
