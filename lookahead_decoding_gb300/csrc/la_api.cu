@@ -200,7 +200,7 @@ static void prof_collect(la_ctx* ctx, const Graph& g) {
 }
 
 static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const void* w2, const void* w3, int n_seg,
-                     int Nout_seg, int K, void* X, void* out, int ldo) {
+                     int Nout_seg, int K, void* X, void* out, int ldo, int pair = 0) {
     memset(g, 0, sizeof(*g));
     if (la_tc_make_map(&g->tmA, w1, Nout_seg, K, 128)) return LA_ECUDA;
     if (la_tc_make_map(&g->tmA2, w2 ? w2 : w1, Nout_seg, K, 128)) return LA_ECUDA;
@@ -210,8 +210,10 @@ static int make_gemm(la_ctx* ctx, TcGemm* g, int mode, const void* w1, const voi
     g->K = K;
     g->Nout = Nout_seg * n_seg;
     g->seg_tiles = n_seg > 1 ? Nout_seg / 128 : 0;
-    g->n_cta = la_tc_pick_ctas(g->Nout / 128, la_tc_k_units(mode, K), mode);
-    g->max_seg = la_tc_max_segments(g->Nout / 128, la_tc_k_units(mode, K), g->n_cta);
+    g->pair = (pair && (g->Nout / 128) % 2 == 0 && g->seg_tiles % 2 == 0) ? 1 : 0;
+    const int utiles = g->Nout / 128 / (g->pair ? 2 : 1), ku = la_tc_k_units(mode, K, g->pair);
+    g->n_cta = la_tc_pick_ctas(utiles, ku, mode);
+    g->max_seg = la_tc_max_segments(utiles, ku, g->n_cta);
     g->rows_cap = ctx->Qcap;
     g->out = out;
     g->ldo = ldo;
@@ -858,18 +860,26 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         ctx->g_o.resize(c.n_layers);
         ctx->g_gu.resize(c.n_layers);
         ctx->g_down.resize(c.n_layers);
+        // QKV, O, down and the LM head stream units of two adjacent output tiles (one
+        // 32 KB copy of one 64-column atom each, as gate/up does), which
+        // halves a stage's activation bytes; packed weights only, and not
+        // in the layer-chain kernel (LA_TC_PAIR=0: single-tile units)
+        const char* pp = getenv("LA_TC_PAIR");      // bit 0 QKV, bit 1 O, bit 2 down, bit 3 LM head
+        const char* pk = getenv("LA_TC_PACK");
+        const char* mg = getenv("LA_MEGA");
+        const int pmask = (!(pk && pk[0] == '0') && !(mg && mg[0] == '1')) ? (pp ? atoi(pp) : 15) : 0;
         for (int l = 0; l < c.n_layers && !r; ++l) {
             r = make_gemm(ctx, &ctx->g_qkv[l], GEMM_STORE, ctx->wq[l], ctx->wk[l], ctx->wv[l], 3, (int)HD, (int)dm,
-                          ctx->xn, ctx->qkv, (int)(3 * HD));
+                          ctx->xn, ctx->qkv, (int)(3 * HD), pmask & 1);
             if (!r) r = make_gemm(ctx, &ctx->g_o[l], GEMM_RESID, ctx->wo[l], nullptr, nullptr, 1, (int)dm, (int)HD,
-                                  ctx->attn, ctx->x, (int)dm);
+                                  ctx->attn, ctx->x, (int)dm, (pmask >> 1) & 1);
             if (!r) r = make_gemm(ctx, &ctx->g_gu[l], GEMM_SWIGLU, ctx->wg[l], ctx->wu[l], nullptr, 1, (int)F, (int)dm,
                                   ctx->xn, ctx->act, (int)F);
             if (!r) r = make_gemm(ctx, &ctx->g_down[l], GEMM_RESID, ctx->wd[l], nullptr, nullptr, 1, (int)dm, (int)F,
-                                  ctx->act, ctx->x, (int)dm);
+                                  ctx->act, ctx->x, (int)dm, (pmask >> 2) & 1);
         }
         if (!r) r = make_gemm(ctx, &ctx->g_head, GEMM_LOGITS, ctx->head, nullptr, nullptr, 1, (int)V, (int)dm, ctx->hn,
-                              nullptr, 0);
+                              nullptr, 0, (pmask >> 3) & 1);
         if (r) { la_free(ctx); return r; }
         ctx->g_head.ld_logits = (int)V;
         // unit-contiguous weight images (one bulk copy per unit); LA_TC_PACK=0
@@ -899,8 +909,9 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         size_t wsf = 0;
         int qchunks = ctx->Qcap / 256;
         auto need_ws = [&](const TcGemm& g) {
-            const size_t planes = (g.mode == GEMM_SWIGLU) ? 2 : 1;
-            if (g.max_seg > 1) wsf = std::max(wsf, (size_t)(g.Nout / 128) * qchunks * g.max_seg * planes * 256 * 128);
+            const size_t planes = (g.mode == GEMM_SWIGLU || g.pair) ? 2 : 1;
+            const size_t utiles = (size_t)(g.Nout / 128) / (g.pair ? 2 : 1);
+            if (g.max_seg > 1) wsf = std::max(wsf, utiles * qchunks * g.max_seg * planes * 256 * 128);
         };
         need_ws(ctx->g_qkv[0]);
         need_ws(ctx->g_o[0]);

@@ -65,6 +65,7 @@ struct TcParams {
     float* part_v; int* part_i; int part_stride;
     int max_chunks;
     int defer;            // split tiles left as partials for the consumer
+    int pair;             // units of two adjacent output tiles (planes 0, 1) x one atom
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -75,7 +76,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     LaTl la_tl_(LA_TL_GEMM_TC, p.tl);
     LaHdr* h = p.hdr;
     const int swiglu = (p.mode == GEMM_SWIGLU);
-    const int nA = swiglu ? 2 : 1;
+    const int nA = (swiglu || p.pair) ? 2 : 1;     // weight matrices of a unit (accumulators)
     const long long T = (long long)p.n_tiles * p.k_tiles;
     // never more CTAs than units: every CTA then owns at least one unit and the
     // owners of one tile are consecutive CTAs
@@ -281,7 +282,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                             const uint32_t accum = (j == 0 && i == 0 && kk == 0) ? 0u : 1u;
                             const uint32_t sa = st + (uint32_t)(i * nA) * A_BYTES + kk * 32;
                             mma_bf16(acc, sdesc(sa), bdesc, id, accum);
-                            if (swiglu) mma_bf16(acc + (uint32_t)BN, sdesc(sa + A_BYTES), bdesc, id, accum);
+                            if (nA == 2) mma_bf16(acc + (uint32_t)BN, sdesc(sa + A_BYTES), bdesc, id, accum);
                         }
                     }
                     mma_commit(bar_empty + 8 * s);
@@ -405,7 +406,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         if (c0 + j < nq) __stcg(wsb + (size_t)(c0 + j) * BM + et, got ? v[j] : 0.f);
-                    if (swiglu) {
+                    if (nA == 2) {
                         tmem_ld16(acc + BN + c0, v);
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
@@ -435,16 +436,28 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
             } else {
                 // a whole tile: straight from TMEM
-                for (int c0 = 0; c0 < nq; c0 += 16) {
-                    float v[16], w2[16];
-                    tmem_ld16(acc + c0, v);
-                    if (swiglu) tmem_ld16(acc + BN + c0, w2);
-                    emit_group(tile, q0, c0, min(16, nq - c0), v, w2, got);
+                if (p.pair) {
+                    // the unit's two output tiles in turn (the argmax scratch holds one)
+                    for (int a = 0; a < 2; ++a) {
+                        for (int c0 = 0; c0 < nq; c0 += 16) {
+                            float v[16];
+                            tmem_ld16(acc + (uint32_t)(a * BN) + c0, v);
+                            emit_group(2 * tile + a, q0, c0, min(16, nq - c0), v, v, got);
+                        }
+                        if (a == 0) argmax_out(2 * tile, q0, 0, nq, got);
+                    }
+                } else {
+                    for (int c0 = 0; c0 < nq; c0 += 16) {
+                        float v[16], w2[16];
+                        tmem_ld16(acc + c0, v);
+                        if (nA == 2) tmem_ld16(acc + BN + c0, w2);
+                        emit_group(tile, q0, c0, min(16, nq - c0), v, w2, got);
+                    }
                 }
                 tc_fence_before();
                 epi_sync();
                 if (quarter == 0 && lane == 0) mbar_arrive(bar_acce + 8 * b);
-                argmax_out(tile, q0, 0, nq, got);
+                argmax_out(p.pair ? 2 * tile + 1 : tile, q0, 0, nq, got);
             }
             iu += seg_len;
             kt += seg_len;
@@ -471,21 +484,36 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int c_lo = nq * sg / nseg, c_hi = nq * (sg + 1) / nseg;
             const float* wst = p.ws + (slot * p.max_seg * nA) * plane + et;
             const size_t seg_stride = (size_t)nA * plane;
-            for (int cb = c_lo; cb < c_hi; cb += 16) {
-                float v[16], w2[16];
-                if (nseg == 2) {
-                    sum_segments<2, 16>(wst, seg_stride, nseg, cb, c_hi, v);
-                    if (swiglu) sum_segments<2, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
-                } else if (nseg == 3) {
-                    sum_segments<3, 16>(wst, seg_stride, nseg, cb, c_hi, v);
-                    if (swiglu) sum_segments<3, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
-                } else {
-                    sum_segments<4, 16>(wst, seg_stride, nseg, cb, c_hi, v);
-                    if (swiglu) sum_segments<4, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
+            if (p.pair) {
+                // the unit's two output tiles in turn, each from its own plane
+                for (int a = 0; a < 2; ++a) {
+                    for (int cb = c_lo; cb < c_hi; cb += 16) {
+                        float v[16];
+                        const float* wa = wst + (size_t)a * plane;
+                        if (nseg == 2) sum_segments<2, 16>(wa, seg_stride, nseg, cb, c_hi, v);
+                        else if (nseg == 3) sum_segments<3, 16>(wa, seg_stride, nseg, cb, c_hi, v);
+                        else sum_segments<4, 16>(wa, seg_stride, nseg, cb, c_hi, v);
+                        emit_group(2 * tile + a, q0, cb, min(16, c_hi - cb), v, v, ok);
+                    }
+                    argmax_out(2 * tile + a, q0, c_lo, c_hi, ok);
                 }
-                emit_group(tile, q0, cb, min(16, c_hi - cb), v, w2, ok);
+            } else {
+                for (int cb = c_lo; cb < c_hi; cb += 16) {
+                    float v[16], w2[16];
+                    if (nseg == 2) {
+                        sum_segments<2, 16>(wst, seg_stride, nseg, cb, c_hi, v);
+                        if (nA == 2) sum_segments<2, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
+                    } else if (nseg == 3) {
+                        sum_segments<3, 16>(wst, seg_stride, nseg, cb, c_hi, v);
+                        if (nA == 2) sum_segments<3, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
+                    } else {
+                        sum_segments<4, 16>(wst, seg_stride, nseg, cb, c_hi, v);
+                        if (nA == 2) sum_segments<4, 16>(wst + plane, seg_stride, nseg, cb, c_hi, w2);
+                    }
+                    emit_group(tile, q0, cb, min(16, c_hi - cb), v, w2, ok);
+                }
+                argmax_out(tile, q0, c_lo, c_hi, ok);
             }
-            argmax_out(tile, q0, c_lo, c_hi, ok);
             // s_flag is rewritten by the next tile's leader only after this barrier
             epi_sync();
         }
@@ -547,22 +575,23 @@ int la_tc_defer_default() {
 
 // 64-column atoms per (tile, K) unit: two (one 32 KB copy) for a single
 // weight matrix, one for the gate/up pair (already two 16 KB tiles)
-static int unit_atoms(int mode) { return mode == GEMM_SWIGLU ? 1 : 2; }
-int la_tc_unit_atoms(int mode) { return unit_atoms(mode); }
-int la_tc_k_units(int mode, int K) {
-    const int atoms = K / BK, ua = unit_atoms(mode);
+static int unit_atoms(int mode, int pair = 0) { return (mode == GEMM_SWIGLU || pair) ? 1 : 2; }
+int la_tc_unit_atoms(int mode, int pair) { return unit_atoms(mode, pair); }
+int la_tc_k_units(int mode, int K, int pair) {
+    const int atoms = K / BK, ua = unit_atoms(mode, pair);
     return (atoms + ua - 1) / ua;
 }
 
 LaSplit la_tc_split(const TcGemm& g, const TcWork& w) {
     LaSplit s;
     s.ws = g.defer ? w.ws : nullptr;
-    s.n_tiles = g.Nout / BM;
-    s.k_tiles = la_tc_k_units(g.mode, g.K);
+    s.n_tiles = g.Nout / BM / (g.pair ? 2 : 1);
+    s.k_tiles = la_tc_k_units(g.mode, g.K, g.pair);
     const long long T = (long long)s.n_tiles * s.k_tiles;
     s.P = (int)std::min<long long>(g.n_cta, T);
     s.max_seg = g.max_seg;
-    s.nA = g.mode == GEMM_SWIGLU ? 2 : 1;
+    s.nA = (g.mode == GEMM_SWIGLU || g.pair) ? 2 : 1;
+    s.pair = g.pair;
     return s;
 }
 
@@ -632,7 +661,7 @@ void la_tc_scratch_need(int mode, int n_out, int K, int rows, int n_cta, size_t*
 // Ring stages at rows_cap rows (the weight stages issued before the header
 // is read; a call with fewer rows gets more stages) and the stage limit.
 // Each stage holds one unit's weight tiles and, per atom, the activation rows.
-static void ring_shape(int mode, int rows_cap, int* ns, int* max_ns) {
+static void ring_shape(int mode, int pair, int rows_cap, int* ns, int* max_ns) {
     static int max_s = -1;
     if (max_s < 0) {
         const char* e = getenv("LA_TC_STAGES");   // pipeline-depth override for tuning runs
@@ -641,11 +670,16 @@ static void ring_shape(int mode, int rows_cap, int* ns, int* max_ns) {
         if (max_s > MAX_STAGES) max_s = MAX_STAGES;
     }
     const int bn = (std::min(BN_MAX, std::max(rows_cap, 1)) + 15) & ~15;
-    const int ua = unit_atoms(mode);
-    const int a_stage = (mode == GEMM_SWIGLU ? 2 : 1) * ua * A_BYTES;
+    const int ua = unit_atoms(mode, pair);
+    const int a_stage = ((mode == GEMM_SWIGLU || pair) ? 2 : 1) * ua * A_BYTES;
     const int n = (SMEM_BYTES - 1024 - 8192) / (a_stage + ua * bn * ROW_BYTES);
+    static int pre = -1;
+    if (pre < 0) {
+        const char* e = getenv("LA_TC_PRE");       // cap on the stages issued before the dependency wait (tuning runs)
+        pre = e ? std::max(0, atoi(e)) : MAX_STAGES;
+    }
     *max_ns = max_s;
-    *ns = std::min(n, max_s);
+    *ns = std::min(std::min(n, max_s), pre);
 }
 
 size_t la_tc_packed_bytes(const TcGemm& g) {
@@ -655,9 +689,10 @@ size_t la_tc_packed_bytes(const TcGemm& g) {
 // Unit-contiguous weight images: unit (tile, kt) is nA blocks of 16 KB, each
 // the 128 x 64 bf16 tile as the 128-byte-swizzled TMA load would leave it in
 // shared memory (16-byte chunk c of row r at r * 128 + ((c ^ (r & 7)) * 16)).
-// w0..w2: the segments (or gate, up) with seg_rows rows each.
+// w0..w2: the segments (or gate, up) with seg_rows rows each.  pair: unit
+// tile u holds output tiles 2u (block 0) and 2u + 1 (block 1).
 __global__ void k_tc_pack(const uint4* w0, const uint4* w1, const uint4* w2, int seg_tiles, int nA, int n_tiles,
-                          int K, uint4* dst) {
+                          int K, int pair, uint4* dst) {
     const int k_tiles = K / BK;
     const long long total = (long long)n_tiles * k_tiles * nA * BM * 8;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
@@ -666,14 +701,15 @@ __global__ void k_tc_pack(const uint4* w0, const uint4* w1, const uint4* w2, int
         const int a = (int)(ua % nA);
         const long long u = ua / nA;
         const int tile = (int)(u / k_tiles), kt = (int)(u % k_tiles);
+        const int out_tile = pair ? 2 * tile + a : tile;
         const uint4* src = w0;
-        int row = tile * BM + r;
-        if (nA == 2) {
+        int row = out_tile * BM + r;
+        if (nA == 2 && !pair) {
             src = a ? w1 : w0;
         } else if (seg_tiles > 0) {
-            const int seg = tile / seg_tiles;
+            const int seg = out_tile / seg_tiles;
             src = seg == 0 ? w0 : (seg == 1 ? w1 : w2);
-            row = (tile - seg * seg_tiles) * BM + r;
+            row = (out_tile - seg * seg_tiles) * BM + r;
         }
         const uint4 v = src[((size_t)row * K + (size_t)kt * BK) / 8 + cc];
         dst[(size_t)ua * (A_BYTES / 16) + r * 8 + (cc ^ (r & 7))] = v;
@@ -681,10 +717,11 @@ __global__ void k_tc_pack(const uint4* w0, const uint4* w1, const uint4* w2, int
 }
 
 cudaError_t la_tc_pack(const TcGemm& g, const void* w1, const void* w2, const void* w3, void* dst, cudaStream_t st) {
-    const int nA = g.mode == GEMM_SWIGLU ? 2 : 1;
-    const int n_tiles = g.Nout / BM;
+    const int nA = (g.mode == GEMM_SWIGLU || g.pair) ? 2 : 1;
+    const int n_tiles = g.Nout / BM / (g.pair ? 2 : 1);
+    if (g.pair && (g.mode == GEMM_SWIGLU || (g.Nout / BM) % 2 || (g.seg_tiles % 2))) return cudaErrorInvalidValue;
     k_tc_pack<<<1024, 256, 0, st>>>((const uint4*)w1, (const uint4*)(w2 ? w2 : w1), (const uint4*)(w3 ? w3 : w1),
-                                    g.seg_tiles, nA, n_tiles, g.K, (uint4*)dst);
+                                    g.seg_tiles, nA, n_tiles, g.K, g.pair, (uint4*)dst);
     return cudaGetLastError();
 }
 
@@ -704,14 +741,17 @@ cudaError_t la_launch_gemm_tc(const LaDev& d, cudaStream_t st, const TcGemm& g, 
     p.mode = g.mode;
     p.K = g.K;
     p.Nout = g.Nout;
-    p.k_tiles = la_tc_k_units(g.mode, g.K);
-    p.ua = unit_atoms(g.mode);
+    if (g.pair && (!g.wpack || g.mode == GEMM_SWIGLU || (g.Nout / BM) % 2))
+        return cudaErrorInvalidValue;
+    p.pair = g.pair;
+    p.k_tiles = la_tc_k_units(g.mode, g.K, g.pair);
+    p.ua = unit_atoms(g.mode, g.pair);
     p.k_atoms = g.K / BK;
-    p.n_tiles = g.Nout / BM;
+    p.n_tiles = g.Nout / BM / (g.pair ? 2 : 1);
     p.seg_tiles = g.seg_tiles;
     p.n_cta = g.n_cta;
     p.max_seg = g.max_seg;
-    ring_shape(g.mode, rows_cap, &p.ns, &p.max_ns);
+    ring_shape(g.mode, g.pair, rows_cap, &p.ns, &p.max_ns);
     p.rows_cap = rows_cap;
     p.wpack = (const uint8_t*)g.wpack;
     p.out = g.out;

@@ -39,20 +39,24 @@ void la_launch_prefill_finish(const LaDev& d, cudaStream_t st, int P);
 // own epilogue: RoPE after QKV, the residual add + RMSNorm after O and down,
 // SwiGLU after gate/up.  ws == nullptr: no split tiles to reduce.
 struct LaSplit {
-    const float* ws;      // partial records [tile + y * n_tiles][max_seg][nA][256][128]
+    const float* ws;      // partial records [unit tile + y * n_tiles][max_seg][nA][256][128]
     int n_tiles, k_tiles, P, max_seg, nA;
+    int pair;             // 1: a unit tile is two adjacent output tiles (planes 0 and 1)
 };
 
-// segments of tile t (1 = the GEMM wrote the tile itself)
+// segments of output tile t (1 = the GEMM wrote the tile itself)
 __host__ __device__ __forceinline__ int la_split_nseg(const LaSplit& s, int t) {
+    const int ut = s.pair ? (t >> 1) : t;
     const long long T = (long long)s.n_tiles * s.k_tiles;
-    const long long u0 = (long long)t * s.k_tiles, u1 = u0 + s.k_tiles - 1;
+    const long long u0 = (long long)ut * s.k_tiles, u1 = u0 + s.k_tiles - 1;
     const int c0 = (int)(((u0 + 1) * s.P - 1) / T), c1 = (int)(((u1 + 1) * s.P - 1) / T);
     return c1 - c0 + 1;
 }
-// the record of segment sg, accumulator plane pl, row chunk y of tile t
+// the record of segment sg, accumulator plane pl, row chunk y of output tile
+// t (a unit of two tiles: the plane is the tile's place in it)
 __host__ __device__ __forceinline__ const float* la_split_rec(const LaSplit& s, int t, int y, int sg, int pl) {
-    return s.ws + ((((size_t)t + (size_t)y * s.n_tiles) * s.max_seg + sg) * s.nA + pl) * (size_t)(256 * 128);
+    const int ut = s.pair ? (t >> 1) : t, plane = s.pair ? (t & 1) : pl;
+    return s.ws + ((((size_t)ut + (size_t)y * s.n_tiles) * s.max_seg + sg) * s.nA + plane) * (size_t)(256 * 128);
 }
 
 #ifdef __CUDACC__
@@ -176,6 +180,8 @@ struct TcGemm {
     int defer;            // 1: split tiles left as partials for the consumer (LaSplit)
     int ctr_off;          // first split-tile counter of this GEMM (counters are per GEMM)
     const void* act;      // the activation rows [rows_alloc][K] the tensor maps cover
+    int pair;             // 1: units of two adjacent 128-row output tiles x one 64-column atom
+                          // (packed weights only; not with GEMM_SWIGLU or GEMM_LOGITS)
 };
 #define LA_TC_CTR_PER_TILE 2   // ints per split-tile arrival counter (one 64-bit word)
 struct TcWork {
@@ -198,7 +204,7 @@ size_t la_tc_packed_bytes(const TcGemm& g);
 cudaError_t la_tc_pack(const TcGemm& g, const void* w1, const void* w2, const void* w3, void* dst, cudaStream_t st);
 int la_tc_ctas();
 // (tile, K) units per tile of a K-deep weight: 128-column units (64 for the gate/up pair)
-int la_tc_k_units(int mode, int K);
+int la_tc_k_units(int mode, int K, int pair = 0);
 int la_tc_pick_ctas(int n_tiles, int k_tiles, int mode);
 int la_tc_max_segments(int n_tiles, int k_tiles, int n_cta);
 cudaError_t la_tc_prepare_device();
@@ -284,5 +290,5 @@ struct MgParams {
 };
 cudaError_t la_launch_mega(const MgParams& p, cudaStream_t st);
 int la_mega_ring_stages(int rows);        // ring stages at `rows` packed rows
-int la_tc_unit_atoms(int mode);
+int la_tc_unit_atoms(int mode, int pair = 0);
 
