@@ -61,27 +61,28 @@ __host__ __device__ __forceinline__ const float* la_split_rec(const LaSplit& s, 
 
 #ifdef __CUDACC__
 // Sum over the segments (K order, from 0) of the element at `off` of plane pl;
-// the loads of up to four segments are issued together (only the tile's own
-// segments: every request goes to L2).
+// the loads of the segments go out four at a time (only the tile's own
+// segments: every request goes to L2), each group added in order.
 __device__ __forceinline__ float la_split_sum(const LaSplit& s, int t, int y, int pl, size_t off, int nseg) {
-    const float t0 = __ldcg(la_split_rec(s, t, y, 0, pl) + off);
-    const float t1 = nseg > 1 ? __ldcg(la_split_rec(s, t, y, 1, pl) + off) : 0.f;
-    const float t2 = nseg > 2 ? __ldcg(la_split_rec(s, t, y, 2, pl) + off) : 0.f;
-    const float t3 = nseg > 3 ? __ldcg(la_split_rec(s, t, y, 3, pl) + off) : 0.f;
-    float r = __fadd_rn(0.f, t0);
-    if (nseg > 1) r = __fadd_rn(r, t1);
-    if (nseg > 2) r = __fadd_rn(r, t2);
-    if (nseg > 3) r = __fadd_rn(r, t3);
-    for (int sg = 4; sg < nseg; ++sg) r = __fadd_rn(r, __ldcg(la_split_rec(s, t, y, sg, pl) + off));
+    float r = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += 4) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k < nseg) v[k] = __ldcg(la_split_rec(s, t, y, s0 + k, pl) + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k < nseg) r = __fadd_rn(r, v[k]);
+    }
     return r;
 }
 // the same for four consecutive elements (off a multiple of 4)
 __device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, size_t off, int nseg, int pl = 0) {
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
         if (k < nseg) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k, pl) + off));
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
         if (k < nseg) {
@@ -90,12 +91,18 @@ __device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, 
             r.z = __fadd_rn(r.z, v[k].z);
             r.w = __fadd_rn(r.w, v[k].w);
         }
-    for (int sg = 4; sg < nseg; ++sg) {
-        const float4 p = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, sg, pl) + off));
-        r.x = __fadd_rn(r.x, p.x);
-        r.y = __fadd_rn(r.y, p.y);
-        r.z = __fadd_rn(r.z, p.z);
-        r.w = __fadd_rn(r.w, p.w);
+    for (int s0 = 4; s0 < nseg; s0 += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k < nseg) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, s0 + k, pl) + off));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k < nseg) {
+                r.x = __fadd_rn(r.x, v[k].x);
+                r.y = __fadd_rn(r.y, v[k].y);
+                r.z = __fadd_rn(r.z, v[k].z);
+                r.w = __fadd_rn(r.w, v[k].w);
+            }
     }
     return r;
 }
