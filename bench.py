@@ -352,7 +352,7 @@ SPEC_HBM_GBS = 8000.0
 # the committed ncu summary holding its DRAM traffic, and the sources that
 # summary's digest covers
 DOMINANT = {"kind": "gemm", "profile": "k_gemm_tc_llama7b_decode_call.md",
-            "sources": ["la_gemm_tc.cu", "la_common.cuh", "la_kernels.h"],
+            "sources": ["la_gemm_tc.cu", "la_tc.cuh", "la_common.cuh", "la_kernels.h", "la_timeline.cuh"],
             "what": "k_gemm_tc (tcgen05 GEMMs: QKV, O, gate/up, down per layer + LM head), per call: "
                     "algorithmic bytes / summed launch time"}
 
