@@ -867,7 +867,11 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         const char* pp = getenv("LA_TC_PAIR");      // bit 0 QKV, bit 1 O, bit 2 down, bit 3 LM head
         const char* pk = getenv("LA_TC_PACK");
         const char* mg = getenv("LA_MEGA");
-        const int pmask = (!(pk && pk[0] == '0') && !(mg && mg[0] == '1')) ? (pp ? atoi(pp) : 15) : 0;
+        // (only where a decode call stacks at most 128 rows: at more, a unit's
+        // two accumulators fill TMEM and the kernel cannot double-buffer them)
+        const int call_rows = max_batch * ((ctx->Qmax + 15) / 16 * 16);
+        const int pmask = (!(pk && pk[0] == '0') && !(mg && mg[0] == '1') && call_rows <= 128)
+                              ? (pp ? atoi(pp) : 15) : 0;
         for (int l = 0; l < c.n_layers && !r; ++l) {
             r = make_gemm(ctx, &ctx->g_qkv[l], GEMM_STORE, ctx->wq[l], ctx->wk[l], ctx->wv[l], 3, (int)HD, (int)dm,
                           ctx->xn, ctx->qkv, (int)(3 * HD), pmask & 1);

@@ -285,41 +285,44 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const int seg_q = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, hh) : 1;
     const int seg_k = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, H + hh) : 1;
     const int seg_v = (fuse && rope.sp.ws) ? la_split_nseg(rope.sp, 2 * H + hh) : 1;
-    if (fuse) {
-        __nv_bfloat16* qs_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
-        __nv_bfloat16* kt_w = const_cast<__nv_bfloat16*>(kt) + (size_t)hh * temp_stride * DH;
-        __nv_bfloat16* vt_w = const_cast<__nv_bfloat16*>(vt) + (size_t)hh * temp_stride * DH;
-        // one item per (part, row, four dimensions): part 0 the query, 1 the
-        // key, 2 the value (no rotation), so every thread has one short chain
-        for (int i = tid; i < 3 * FR * (half / 4); i += blockDim.x) {
-            const int part = i / (FR * (half / 4)), j = i % (FR * (half / 4));
-            const int r = j / (half / 4), c4 = (j % (half / 4)) * 4;
-            if (r >= nr) {
-                if (part == 0) {
-                    __nv_bfloat16* qd = qs_w + r * LDK + c4;
-                    *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
-                    *reinterpret_cast<uint2*>(qd + half) = make_uint2(0u, 0u);
-                }
-                continue;
+    // item j of part 0 (the query: rotated into shared memory), 1 (the key:
+    // rotated) or 2 (the value) of the tile's rows; keys and values go to the
+    // temporary rows for the commit (no CTA of this kernel reads them)
+    __nv_bfloat16* qs_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.q);
+    __nv_bfloat16* kt_w = const_cast<__nv_bfloat16*>(kt) + (size_t)hh * temp_stride * DH;
+    __nv_bfloat16* vt_w = const_cast<__nv_bfloat16*>(vt) + (size_t)hh * temp_stride * DH;
+    constexpr int RI = FR * (DH / 2 / 4);              // items of one part
+    auto rope_item = [&](int part, int j) {
+        const int r = j / (half / 4), c4 = (j % (half / 4)) * 4;
+        if (r >= nr) {
+            if (part == 0) {
+                __nv_bfloat16* qd = qs_w + r * LDK + c4;
+                *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
+                *reinterpret_cast<uint2*>(qd + half) = make_uint2(0u, 0u);
             }
-            const int row = r0 + r, pos = rpos[r], lrow = row - req * qstride;
-            const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
-            const int seg = part == 0 ? seg_q : (part == 1 ? seg_k : seg_v);
-            const int n0 = part * HD + hh * DH + c4;
-            const float4 a = la_qkv_at4(x, row, n0, rope.sp, seg);
-            const float4 b = la_qkv_at4(x, row, n0 + half, rope.sp, seg);
-            if (part == 2) {
-                __nv_bfloat16* vo = vt_w + (size_t)lrow * DH + c4;
-                *reinterpret_cast<uint2*>(vo) = la_pack_bf16x4(a.x, a.y, a.z, a.w);
-                *reinterpret_cast<uint2*>(vo + half) = la_pack_bf16x4(b.x, b.y, b.z, b.w);
-                continue;
-            }
-            const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
-            const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
-            __nv_bfloat16* dst = part == 0 ? qs_w + r * LDK + c4 : kt_w + (size_t)lrow * DH + c4;
-            la_rope4_store(dst, dst + half, a, b, c, s);
+            return;
         }
-    }
+        const int row = r0 + r, pos = rpos[r], lrow = row - req * qstride;
+        const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+        const int seg = part == 0 ? seg_q : (part == 1 ? seg_k : seg_v);
+        const int n0 = part * HD + hh * DH + c4;
+        const float4 a = la_qkv_at4(x, row, n0, rope.sp, seg);
+        const float4 b = la_qkv_at4(x, row, n0 + half, rope.sp, seg);
+        if (part == 2) {
+            __nv_bfloat16* vo = vt_w + (size_t)lrow * DH + c4;
+            *reinterpret_cast<uint2*>(vo) = la_pack_bf16x4(a.x, a.y, a.z, a.w);
+            *reinterpret_cast<uint2*>(vo + half) = la_pack_bf16x4(b.x, b.y, b.z, b.w);
+            return;
+        }
+        const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+        const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+        __nv_bfloat16* dst = part == 0 ? qs_w + r * LDK + c4 : kt_w + (size_t)lrow * DH + c4;
+        la_rope4_store(dst, dst + half, a, b, c, s);
+    };
+    // the queries now; the keys and values for the commit by the warps that
+    // wait out the committed blocks
+    if (fuse)
+        for (int j = tid; j < RI; j += blockDim.x) rope_item(0, j);
     int t0max = 0, t0min = 0x7fffffff, posmax = 0;
     for (int r = 0; r < nr; ++r) {
         t0max = max(t0max, rt0[r]);
@@ -345,6 +348,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         ldsm_x4(sbase + LY.q + (uint32_t)((lane & 15) * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qa[ks8]);
 
     const float scale = 0.08838834764831845f;   // 1/sqrt(128)
+    if (fuse && warp >= FW)
+        for (int i = tid - FW * 32; i < 2 * RI; i += (FT - FW) * 32) rope_item(1 + i / RI, i % RI);
     // warps FW .. FT-1 wait for the blocks at the barrier before the tail
     for (int b = 0; b < (warp < FW ? nb : 0); ++b) {
         const int buf = b & 1;
