@@ -440,7 +440,7 @@ int la_bench_gemm(int mode, int n_out, int K, int rows, int n_cta, int n_copies,
  * returns once the result is in y.  Every call looks up the workspace's
  * address on the current device and sets the kernel's shared-memory limit
  * there; the first call on a device also loads the library's device code
- * there, so make it before any stream capture on that device.  The counters
+ * there.  The counters
  * and status word must be zero when the GEMM starts: the call zeroes them
  * itself on `stream` before each launch.  There is one workspace per
  * device, so two executions overlapping on a device would race on it; calls

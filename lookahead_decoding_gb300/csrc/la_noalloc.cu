@@ -16,10 +16,9 @@
 // sets the kernel's shared-memory opt-in there.  Doing both on every call
 // rather than caching them keeps a call correct after the caller resets the
 // device (the module, and with it the array, may then load elsewhere).  The
-// first call on a device loads the library's device code there; make it
-// before any stream capture on that device.  A problem whose split-tile
-// partial sums do not fit is rejected with LA_ECAPACITY before any device
-// work.
+// first call on a device loads the library's device code there.  A problem
+// whose split-tile partial sums do not fit is rejected with LA_ECAPACITY
+// before any device work.
 //
 // What must start at zero: the header's status word and the per-tile arrival
 // counters.  The counters only grow during a launch (a tile's contributors
