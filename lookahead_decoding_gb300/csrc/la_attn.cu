@@ -146,25 +146,54 @@ __device__ __forceinline__ float warp_sum(float v) {
 // 64 KB per block) or, after the blocks, the tail keys in padded rows.
 struct FusedLayout {
     uint32_t ring, ring_bytes, q, p, o, wmax, wl, rpos, rt0, pw, sw, bar, ssc, ssp, path, uslot, urow, misc, total;
+    uint32_t tk, tv, ik, iv, ring_used;   // tail keys: committed (tk, tv) and, apart, in-call (ik, iv)
 };
-__host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax, int qrows) {
+// ck: the committed tail keys a tile can stage (32 (TB + 1)).  sep: the
+// in-call keys get a region of their own beside the block ring, so the warps
+// that wait out the committed blocks can stage them meanwhile; the committed
+// tail keys, the per-warp softmax rows and the tail scores then move into
+// the ring, free once the blocks are done.
+__host__ __device__ inline FusedLayout fused_layout(int ring_keys, int pmax, int qrows, int sep = 0, int ck = 0) {
     FusedLayout L;
     L.ring = 0;
-    L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;           // K and V rows, bf16
-    if (L.ring_bytes < 2u * 4u * BLK * 128u) L.ring_bytes = 2u * 4u * BLK * 128u;
-    L.q = L.ring + L.ring_bytes;                                    // [FR][LDK] bf16
+    L.ssp = (uint32_t)ring_keys + 4;                                // tail scores: [FR][ssp] fp32
+    if (!sep) {
+        L.ring_bytes = (uint32_t)ring_keys * 2u * LDK * 2u;       // K and V rows, bf16
+        if (L.ring_bytes < 2u * 4u * BLK * 128u) L.ring_bytes = 2u * 4u * BLK * 128u;
+        L.tk = L.ring;
+        L.tv = L.tk + (uint32_t)ring_keys * LDK * 2u;
+        L.ik = L.tk;                                                // in-call keys follow the committed ones
+        L.iv = L.tv;
+        L.q = L.ring + L.ring_bytes;
+    } else {
+        L.ring_bytes = 2u * 4u * BLK * 128u;
+        L.tk = L.ring;                                              // [ck][LDK] bf16, after the blocks
+        L.tv = L.tk + (uint32_t)ck * LDK * 2u;
+        L.pw = L.tv + (uint32_t)ck * LDK * 2u;                      // [FT][MAX_TAIL] fp32
+        L.sw = L.pw + FT * MAX_TAIL * 4;                            // [FT][MAX_TAIL] int
+        L.ssc = L.sw + FT * MAX_TAIL * 4;
+        L.ring_used = L.ssc + FR * L.ssp * 4;                       // <= ring_bytes (checked by the launch)
+        L.ik = L.ring + L.ring_bytes;                               // [ring_keys - ck][LDK] bf16
+        L.iv = L.ik + (uint32_t)(ring_keys - ck) * LDK * 2u;
+        L.q = L.iv + (uint32_t)(ring_keys - ck) * LDK * 2u;
+    }
     L.p = L.q + FR * LDK * 2;                                       // [FR][LDK] fp16
     L.o = L.p + FR * LDK * 2;                                       // [FR][DH] fp32
     L.wmax = L.o + FR * DH * 4;                                     // [FW][FR] fp32
     L.wl = L.wmax + FW * FR * 4;                                    // [FW][FR] fp32
     L.rpos = L.wl + FW * FR * 4;                                    // [FR] int
     L.rt0 = L.rpos + FR * 4;                                        // [FR] int
-    L.pw = L.rt0 + FR * 4;                                          // [FT][MAX_TAIL] fp32
-    L.sw = L.pw + FT * MAX_TAIL * 4;                                // [FT][MAX_TAIL] int
-    L.bar = L.sw + FT * MAX_TAIL * 4;                               // 2 mbarriers
-    L.ssp = (uint32_t)ring_keys + 4;                                // tail scores: [FR][ssp] fp32
-    L.ssc = L.bar + 16;
-    L.path = L.ssc + FR * L.ssp * 4;                                // [FR][pmax] int
+    if (!sep) {
+        L.pw = L.rt0 + FR * 4;                                      // [FT][MAX_TAIL] fp32
+        L.sw = L.pw + FT * MAX_TAIL * 4;                            // [FT][MAX_TAIL] int
+        L.bar = L.sw + FT * MAX_TAIL * 4;                           // 2 mbarriers
+        L.ssc = L.bar + 16;
+        L.path = L.ssc + FR * L.ssp * 4;                            // [FR][pmax] int
+        L.ring_used = L.ring_bytes;
+    } else {
+        L.bar = L.rt0 + FR * 4;
+        L.path = L.bar + 16;
+    }
     L.uslot = L.path + (uint32_t)FR * pmax * 4;                     // [qrows] int: ring slot of a temporary row
     L.urow = L.uslot + (uint32_t)qrows * 4;                         // [qrows] int: temporary row of a slot
     L.misc = L.urow + (uint32_t)qrows * 4;                          // [4] int: the count of staged rows
@@ -179,7 +208,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
                                                       const __grid_constant__ CUtensorMap cmap, int krow0, int vrow0,
                                                       const LaHdr* const* req_hdr, int qstride,
                                                       long long req_cache_elems, int req_cache_rows, int qrows,
-                                                      LaRope rope) {
+                                                      LaRope rope, int sep, int ck) {
     LaTl la_tl_(LA_TL_ATTN_FUSED, d.tl);
     const LaHdr* h = d.hdr;
     const int hh = blockIdx.x, r0 = blockIdx.y * FR;
@@ -200,7 +229,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const int PM = d.PMAX;
 
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    const FusedLayout LY = fused_layout(ring_keys, PM, qrows);
+    const FusedLayout LY = fused_layout(ring_keys, PM, qrows, sep, ck);
     const uint32_t sraw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - sraw);
@@ -333,6 +362,75 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     if (!spec0 && nb > 0) stage_block(0, 0);
     const int ta = rt0[g], tb = rt0[g + 8];             // split points of this thread's two rows
 
+    const bool sepm = sep && fuse;
+    const int Kc = prefill ? posmax + 1 : K;
+    const int nc = (nr > 0 && Kc > t0min) ? Kc - t0min : 0;
+    int* uslot = reinterpret_cast<int*>(smem + LY.uslot);
+    int* urow = reinterpret_cast<int*>(smem + LY.urow);
+    int& s_nu = *reinterpret_cast<int*>(smem + LY.misc);
+    const uint32_t tk_a = sbase + LY.tk, tv_a = sbase + LY.tv;
+    // the temporary rows on the tile's rows' paths, each once, in row order
+    // (uslot: a temporary row's slot among them; urow: the inverse; s_nu:
+    // their count).  Every thread of the CTA calls it.
+    auto mark_paths = [&]() {
+        if (tid == 0) s_nu = 0;
+        if (Q > 0) {
+            for (int q = tid; q < Q; q += blockDim.x) uslot[q] = 0;
+            __syncthreads();
+            for (int i = tid; i < nr * PM; i += blockDim.x) {
+                const int r = i / PM, e = i % PM, pos = rpos[r];
+                if (pos >= K && e <= pos - K) {
+                    const int pr = spath[i];
+                    if (pr >= 0 && pr < Q) uslot[pr] = 1;
+                }
+            }
+            __syncthreads();
+            if (warp == 0) {        // slots in row order: a ballot scan over the marks
+                int run = 0;
+                for (int base = 0; base < Q; base += 32) {
+                    const int q = base + lane;
+                    const bool m = q < Q && uslot[q] != 0;
+                    const unsigned bal = __ballot_sync(0xffffffffu, m);
+                    const int sl = run + __popc(bal & ((1u << lane) - 1u));
+                    if (m) { uslot[q] = sl; urow[sl] = q; }
+                    run += __popc(bal);
+                }
+                if (lane == 0) s_nu = run;
+            }
+        }
+        __syncthreads();
+    };
+    // the in-call keys: rotated K and V of the request's row urow[s] at its
+    // position, head hh, into in-call slot s (row nc + s of the tail keys, or
+    // row s of the separate region), items from i0 in steps of di; one item
+    // per (part, slot, four dimensions): part 0 the key, 1 the value
+    auto stage_incall = [&](int i0, int di) {
+        __nv_bfloat16* ik_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.ik) + (sepm ? 0 : (size_t)nc * LDK);
+        __nv_bfloat16* iv_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.iv) + (sepm ? 0 : (size_t)nc * LDK);
+        const int nk = s_nu * (half / 4);
+        for (int i = i0; i < 2 * nk; i += di) {
+            const int part = i / nk, j = i % nk;
+            const int sl = j / (half / 4), c4 = (j % (half / 4)) * 4;
+            const int row = req * qstride + urow[sl];
+            const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+            const int n0 = (part + 1) * HD + hh * DH + c4;
+            const float4 a = la_qkv_at4(x, row, n0, rope.sp, part == 0 ? seg_k : seg_v);
+            const float4 b = la_qkv_at4(x, row, n0 + half, rope.sp, part == 0 ? seg_k : seg_v);
+            if (part == 1) {
+                __nv_bfloat16* vd = iv_w + (size_t)sl * LDK + c4;
+                *reinterpret_cast<uint2*>(vd) = la_pack_bf16x4(a.x, a.y, a.z, a.w);
+                *reinterpret_cast<uint2*>(vd + half) = la_pack_bf16x4(b.x, b.y, b.z, b.w);
+                continue;
+            }
+            const int pos = d.row_pos[row];
+            const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+            const float4 sn = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+            __nv_bfloat16* kd = ik_w + (size_t)sl * LDK + c4;
+            la_rope4_store(kd, kd + half, a, b, c, sn);
+        }
+    };
+    if (sepm) mark_paths();
+
     // running state of rows g and g+8; O columns of this warp's dims
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     float o[NTW][4];
@@ -348,8 +446,10 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         ldsm_x4(sbase + LY.q + (uint32_t)((lane & 15) * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qa[ks8]);
 
     const float scale = 0.08838834764831845f;   // 1/sqrt(128)
-    if (fuse && warp >= FW)
+    if (fuse && warp >= FW) {
         for (int i = tid - FW * 32; i < 2 * RI; i += (FT - FW) * 32) rope_item(1 + i / RI, i % RI);
+        if (sepm && s_nu <= ring_keys - ck) stage_incall(tid - FW * 32, (FT - FW) * 32);
+    }
     // warps FW .. FT-1 wait for the blocks at the barrier before the tail
     for (int b = 0; b < (warp < FW ? nb : 0); ++b) {
         const int buf = b & 1;
@@ -490,52 +590,23 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     __syncthreads();      // the ring is free for the tail keys
 
     // tail keys: committed positions [t0min, Kc), then (in a call) the
-    // temporary rows on the tile's rows' paths, each once, in row order
-    // (uslot: a temporary row's ring slot past the committed keys; urow: the
-    // inverse).  Which slot a key takes changes no arithmetic: every score
-    // depends only on its query and key, and each row reads its own keys in
-    // position order.
-    const int Kc = prefill ? posmax + 1 : K;
-    const int nc = (nr > 0 && Kc > t0min) ? Kc - t0min : 0;
-    int* uslot = reinterpret_cast<int*>(smem + LY.uslot);
-    int* urow = reinterpret_cast<int*>(smem + LY.urow);
-    int& s_nu = *reinterpret_cast<int*>(smem + LY.misc);
-    if (tid == 0) s_nu = 0;
-    if (Q > 0) {
-        for (int q = tid; q < Q; q += blockDim.x) uslot[q] = 0;
-        __syncthreads();
-        for (int i = tid; i < nr * PM; i += blockDim.x) {
-            const int r = i / PM, e = i % PM, pos = rpos[r];
-            if (pos >= K && e <= pos - K) {
-                const int pr = spath[i];
-                if (pr >= 0 && pr < Q) uslot[pr] = 1;
-            }
-        }
-        __syncthreads();
-        if (warp == 0) {        // slots in row order: a ballot scan over the marks
-            int run = 0;
-            for (int base = 0; base < Q; base += 32) {
-                const int q = base + lane;
-                const bool m = q < Q && uslot[q] != 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, m);
-                const int s = run + __popc(bal & ((1u << lane) - 1u));
-                if (m) { uslot[q] = s; urow[s] = q; }
-                run += __popc(bal);
-            }
-            if (lane == 0) s_nu = run;
-        }
-    }
-    __syncthreads();
+    // temporary rows on the tile's rows' paths, each once, in row order.
+    // Which slot a key takes changes no arithmetic: every score depends only
+    // on its query and key, and each row reads its own keys in position
+    // order.  Separate layout: the in-call keys were marked and staged while
+    // the blocks ran.
+    if (!sepm) mark_paths();
     const int nt = nc + s_nu;
-    if (nt > ring_keys) {       // beyond the ring the launch sized (bounded by construction)
+    if (nt > ring_keys || (sepm && (nc > ck || s_nu > ring_keys - ck))) {
+        // beyond the ring the launch sized (bounded by construction)
         if (tid == 0) la_set_err(d.hdr, LA_ECAPACITY);
         return;
     }
-    const uint32_t tk_a = sbase + LY.ring, tv_a = tk_a + (uint32_t)ring_keys * LDK * 2u;
     {
         const __nv_bfloat16* kth = kt + (size_t)hh * temp_stride * DH;
         const __nv_bfloat16* vth = vt + (size_t)hh * temp_stride * DH;
-        for (int i = tid; i < nt * (DH / 8); i += blockDim.x) {
+        const int nstage = sepm ? nc : nt;
+        for (int i = tid; i < nstage * (DH / 8); i += blockDim.x) {
             const int j = i >> 4, c8 = (i & 15) * 8;
             const __nv_bfloat16* ksrc;
             const __nv_bfloat16* vsrc;
@@ -546,40 +617,18 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
             cp_async16(tk_a + off, ksrc + c8, 16);
             cp_async16(tv_a + off, vsrc + c8, 16);
         }
-        if (fuse) {
-            // the in-call keys on the tile's paths: rotated K and V of the
-            // request's row urow[s] at its position, head hh, into slot nc + s
-            __nv_bfloat16* tk_w = reinterpret_cast<__nv_bfloat16*>(smem + LY.ring);
-            __nv_bfloat16* tv_w = tk_w + (size_t)ring_keys * LDK;
-            // one item per (part, slot, four dimensions): part 0 the key
-            // (rotated at the row's position), 1 the value
-            const int nk = (nt - nc) * (half / 4);
-            for (int i = tid; i < 2 * nk; i += blockDim.x) {
-                const int part = i / nk, j = i % nk;
-                const int sl = j / (half / 4), c4 = (j % (half / 4)) * 4;
-                const int row = req * qstride + urow[sl];
-                const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
-                const int n0 = (part + 1) * HD + hh * DH + c4;
-                const float4 a = la_qkv_at4(x, row, n0, rope.sp, part == 0 ? seg_k : seg_v);
-                const float4 b = la_qkv_at4(x, row, n0 + half, rope.sp, part == 0 ? seg_k : seg_v);
-                if (part == 1) {
-                    __nv_bfloat16* vd = tv_w + (size_t)(nc + sl) * LDK + c4;
-                    *reinterpret_cast<uint2*>(vd) = la_pack_bf16x4(a.x, a.y, a.z, a.w);
-                    *reinterpret_cast<uint2*>(vd + half) = la_pack_bf16x4(b.x, b.y, b.z, b.w);
-                    continue;
-                }
-                const int pos = d.row_pos[row];
-                const float4 c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
-                const float4 s = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
-                __nv_bfloat16* kd = tk_w + (size_t)(nc + sl) * LDK + c4;
-                la_rope4_store(kd, kd + half, a, b, c, s);
-            }
-        }
+        if (fuse && !sepm) stage_incall(tid, (int)blockDim.x);
         asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    const __nv_bfloat16* TK = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ring);
-    const __nv_bfloat16* TV = TK + (size_t)ring_keys * LDK;
+    const __nv_bfloat16* TK = reinterpret_cast<const __nv_bfloat16*>(smem + LY.tk);
+    const __nv_bfloat16* TV = reinterpret_cast<const __nv_bfloat16*>(smem + LY.tv);
+    const __nv_bfloat16* IK = reinterpret_cast<const __nv_bfloat16*>(smem + LY.ik);
+    const __nv_bfloat16* IV = reinterpret_cast<const __nv_bfloat16*>(smem + LY.iv);
+    // row of tail slot j: committed keys first, then the in-call keys (in the
+    // separate region in the separate layout)
+    auto key_row = [&](int j) { return (sepm && j >= nc) ? IK + (size_t)(j - nc) * LDK : TK + (size_t)j * LDK; };
+    auto val_row = [&](int j) { return (sepm && j >= nc) ? IV + (size_t)(j - nc) * LDK : TV + (size_t)j * LDK; };
     int* swr = sw + warp * MAX_TAIL;
     float* pwr = pw + warp * MAX_TAIL;
     // Tail scores on tensor cores: S = Q K^T for the tile's rows against every
@@ -591,7 +640,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     for (int nti = warp; nti * 8 < nt; nti += FT) {
         float c4[4] = {0.f, 0.f, 0.f, 0.f};
         const int kr = min(nti * 8 + g, nt - 1);
-        const __nv_bfloat16* krow = TK + (size_t)kr * LDK + 2 * t;
+        const __nv_bfloat16* krow = key_row(kr) + 2 * t;
 #pragma unroll
         for (int ks8 = 0; ks8 < 8; ++ks8) {
             const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks8 * 16);
@@ -643,7 +692,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 pk[u] = pwr[j + u];
-                vv[u] = *reinterpret_cast<const uint2*>(TV + (size_t)swr[j + u] * LDK + lane * 4);
+                vv[u] = *reinterpret_cast<const uint2*>(val_row(swr[j + u]) + lane * 4);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -655,7 +704,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         }
         for (; j < n; ++j) {
             const float pk = pwr[j];
-            const uint2 vv = *reinterpret_cast<const uint2*>(TV + (size_t)swr[j] * LDK + lane * 4);
+            const uint2 vv = *reinterpret_cast<const uint2*>(val_row(swr[j]) + lane * 4);
             to[0] = fmaf(pk, __uint_as_float(vv.x << 16), to[0]);
             to[1] = fmaf(pk, __uint_as_float(vv.x & 0xffff0000u), to[1]);
             to[2] = fmaf(pk, __uint_as_float(vv.y << 16), to[2]);
@@ -704,8 +753,24 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
                                      const LaRope* rope) {
     if (TB + 1 > MAX_TAIL / 32) return cudaErrorInvalidValue;
     if (tail_rows <= 0 || tail_rows > Qmax) tail_rows = Qmax;
-    const int ring_keys = ring_keys_for(TB, tail_rows);
-    const size_t smem = la_attn_smem_bytes(TB, tail_rows, pmax, Qmax);
+    int ring_keys = ring_keys_for(TB, tail_rows);
+    size_t smem = la_attn_smem_bytes(TB, tail_rows, pmax, Qmax);
+    // the separate layout (in-call keys staged while the blocks run) where
+    // it fits: decode calls with RoPE folded in (LA_ATTN_SEP=0: never)
+    const char* sep_e = getenv("LA_ATTN_SEP");       // read per launch (graphs record it at capture)
+    const int sep_env = (sep_e && sep_e[0] == '0') ? 0 : 1;
+    // committed tail keys of a tile: K - t0min <= 31 + 32 TB; in-call keys:
+    // at most tail_rows, plus a tile's slack
+    const int ck = 32 * (TB + 1), keys_sep = ck + FR + tail_rows;
+    int sep = 0;
+    if (sep_env && rope && sel != SEL_PREFILL) {
+        const FusedLayout L = fused_layout(keys_sep, pmax, Qmax, 1, ck);
+        if (L.ring_used <= L.ring_bytes && (size_t)L.total + 1024 <= 227 * 1024) {
+            sep = 1;
+            smem = (size_t)L.total + 1024;
+            ring_keys = keys_sep;
+        }
+    }
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_attn_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -719,5 +784,5 @@ cudaError_t la_launch_attention_bf16(const LaDev& d, cudaStream_t st, const void
                          (const __nv_bfloat16*)vt, (__nv_bfloat16*)out, sel, Qcap, max_ctx,
                          temp_stride ? temp_stride : Qmax, TB, H, ring_keys,
                          cmap, krow0, vrow0, req_hdr, qstride, req_cache_elems, req_cache_rows, Qmax,
-                         rope ? *rope : LaRope{nullptr, LaSplit{}, nullptr, nullptr});
+                         rope ? *rope : LaRope{nullptr, LaSplit{}, nullptr, nullptr}, sep, ck);
 }

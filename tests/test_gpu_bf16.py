@@ -197,6 +197,41 @@ def test_generate_with_pool_seeding_equals_ar_mid(mid, opts):
         L.la_set_options(ctx.ctx, 0)
 
 
+@pytest.mark.parametrize("W,N,G", [(15, 5, 15), (7, 4, 7)])
+def test_attention_layouts_bitwise_equal_mid(monkeypatch, W, N, G):
+    """The attention's two shared-memory layouts (in-call keys staged after
+    the committed blocks in the ring, or during them in a region of their
+    own) compute the same bits: every call's needed-row logits and every
+    layer's attention output (W=15: including calls that accept)."""
+    from lookahead_decoding_gb300 import lib
+    L = lib()
+    w = synth.llama_weights(MID, 0, device="cuda:0", wo_scale=2.0 ** -10)
+    p = synth.markov_zipf_prompt(MID.vocab, 64, 5).tolist()
+    runs = []
+    for sep in ("0", "1"):
+        monkeypatch.setenv("LA_ATTN_SEP", sep)
+        ctx = context(MID, w, max_ctx=640, W=15, N=5, G=15)
+        L.la_set_debug(ctx.ctx, 1 | 8)
+        L.la_prefill(ctx.ctx, p)
+        calls = []
+        for _ in range(24):
+            em = L.la_step(ctx.ctx, W, N, G)
+            lg, need = L.la_debug_logits(ctx.ctx, 1024, MID.vocab)
+            h = L.la_debug_state(ctx.ctx)[0]
+            Q = int(h["Q"])
+            attn = [L.la_debug_layer(ctx.ctx, l, 1, Q, MID.n_heads * MID.head_dim) for l in range(MID.n_layers)]
+            calls.append((em, lg.copy(), need.copy(), attn))
+        ctx.close()
+        runs.append(calls)
+    for (e0, l0, n0, a0), (e1, l1, n1, a1) in zip(*runs):
+        assert e0 == e1 and np.array_equal(n0, n1)
+        assert np.array_equal(l0.view(np.uint32), l1.view(np.uint32))
+        for x, y in zip(a0, a1):
+            assert np.array_equal(x, y)
+    if W == 15:
+        assert any(len(c[0]) > 1 for c in runs[1]), "no accepting call"
+
+
 def test_row_invariance_probe_mid(mid):
     L, ctx, oracle = mid
     p = synth.markov_zipf_prompt(MID.vocab, 200, 9).tolist()
