@@ -371,21 +371,27 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     const uint32_t tk_a = sbase + LY.tk, tv_a = sbase + LY.tv;
     // the temporary rows on the tile's rows' paths, each once, in row order
     // (uslot: a temporary row's slot among them; urow: the inverse; s_nu:
-    // their count).  Every thread of the CTA calls it.
-    auto mark_paths = [&]() {
-        if (tid == 0) s_nu = 0;
+    // their count).  Called by every thread of the CTA (group 0) or by the
+    // warps FW .. FT-1 alone (group 1, while the blocks run).
+    auto mark_paths = [&](int group) {
+        const int t = group ? tid - FW * 32 : tid, nthr = group ? (FT - FW) * 32 : (int)blockDim.x;
+        auto sync = [&]() {
+            if (group) asm volatile("bar.sync 2, %0;" ::"n"((FT - FW) * 32) : "memory");
+            else __syncthreads();
+        };
+        if (t == 0) s_nu = 0;
         if (Q > 0) {
-            for (int q = tid; q < Q; q += blockDim.x) uslot[q] = 0;
-            __syncthreads();
-            for (int i = tid; i < nr * PM; i += blockDim.x) {
+            for (int q = t; q < Q; q += nthr) uslot[q] = 0;
+            sync();
+            for (int i = t; i < nr * PM; i += nthr) {
                 const int r = i / PM, e = i % PM, pos = rpos[r];
                 if (pos >= K && e <= pos - K) {
                     const int pr = spath[i];
                     if (pr >= 0 && pr < Q) uslot[pr] = 1;
                 }
             }
-            __syncthreads();
-            if (warp == 0) {        // slots in row order: a ballot scan over the marks
+            sync();
+            if (t < 32) {        // slots in row order: a ballot scan over the marks
                 int run = 0;
                 for (int base = 0; base < Q; base += 32) {
                     const int q = base + lane;
@@ -398,8 +404,9 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
                 if (lane == 0) s_nu = run;
             }
         }
-        __syncthreads();
+        sync();
     };
+    if (sepm) mark_paths(0);
     // the in-call keys: rotated K and V of the request's row urow[s] at its
     // position, head hh, into in-call slot s (row nc + s of the tail keys, or
     // row s of the separate region), items from i0 in steps of di; one item
@@ -429,7 +436,6 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
             la_rope4_store(kd, kd + half, a, b, c, sn);
         }
     };
-    if (sepm) mark_paths();
 
     // running state of rows g and g+8; O columns of this warp's dims
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
@@ -446,6 +452,8 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
         ldsm_x4(sbase + LY.q + (uint32_t)((lane & 15) * LDK + ks8 * 16 + (lane >> 4) * 8) * 2u, qa[ks8]);
 
     const float scale = 0.08838834764831845f;   // 1/sqrt(128)
+    // (the paths are marked by the whole CTA first: the warps below would
+    // otherwise outlast the blocks)
     if (fuse && warp >= FW) {
         for (int i = tid - FW * 32; i < 2 * RI; i += (FT - FW) * 32) rope_item(1 + i / RI, i % RI);
         if (sepm && s_nu <= ring_keys - ck) stage_incall(tid - FW * 32, (FT - FW) * 32);
@@ -595,7 +603,7 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     // on its query and key, and each row reads its own keys in position
     // order.  Separate layout: the in-call keys were marked and staged while
     // the blocks ran.
-    if (!sepm) mark_paths();
+    if (!sepm) mark_paths(0);
     const int nt = nc + s_nu;
     if (nt > ring_keys || (sepm && (nc > ck || s_nu > ring_keys - ck))) {
         // beyond the ring the launch sized (bounded by construction)

@@ -86,7 +86,40 @@ __global__ void k_embed(LaDev d, const T* emb, float* x, int dm, int sel) {
 // split tiles the last residual GEMM left (resid) are added to x: x += the
 // segments' partials in K order, and x is written back.
 // ---------------------------------------------------------------------------
-template <typename T>
+// the segments of a split tile summed in K order like la_split_sum4, the
+// first eight loads issued together (a row of at most one float4 a thread
+// has the registers for them)
+__device__ __forceinline__ float4 split_sum4_wide(const LaSplit& s, int t, int y, size_t off, int nseg) {
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nseg) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k, 0) + off));
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nseg) {
+            r.x = __fadd_rn(r.x, v[k].x);
+            r.y = __fadd_rn(r.y, v[k].y);
+            r.z = __fadd_rn(r.z, v[k].z);
+            r.w = __fadd_rn(r.w, v[k].w);
+        }
+    for (int s0 = 8; s0 < nseg; s0 += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k < nseg) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, s0 + k, 0) + off));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k < nseg) {
+                r.x = __fadd_rn(r.x, v[k].x);
+                r.y = __fadd_rn(r.y, v[k].y);
+                r.z = __fadd_rn(r.z, v[k].z);
+                r.w = __fadd_rn(r.w, v[k].w);
+            }
+    }
+    return r;
+}
+
+template <typename T, int MAXV>
 __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g, T* y, int dm, float eps, int sel,
                                                  int gather, LaSplit resid) {
     LaTl la_tl_(LA_TL_RMSNORM, d.tl);
@@ -94,9 +127,8 @@ __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g,
     if (skip_call(h, sel)) return;       // header fields: readable before the wait (la_common.cuh)
     const int row = blockIdx.x;
     if (row >= rows_of(h, sel)) return;
-    // the row stays in registers: up to 2 float4 per thread (256 threads for
-    // d_model <= 2048, 1024 threads up to 8192)
-    constexpr int MAXV = 2;
+    // the row stays in registers: up to MAXV float4 per thread (256 threads
+    // for d_model <= 2048, 1024 threads up to 8192)
     float4 v[MAXV], add[MAXV], gv[MAXV];
     bool upd[MAXV];
     // the gains (weights) are read before the wait, the row after it
@@ -121,7 +153,9 @@ __global__ void __launch_bounds__(1024) k_rmsnorm(LaDev d, float* x, const T* g,
                 const int tile = i >> 7;
                 const int nseg = la_split_nseg(resid, tile);
                 if (nseg > 1) {
-                    add[k] = la_split_sum4(resid, tile, src >> 8, (size_t)(src & 255) * 128 + (i & 127), nseg);
+                    const size_t off = (size_t)(src & 255) * 128 + (i & 127);
+                    add[k] = MAXV == 1 ? split_sum4_wide(resid, tile, src >> 8, off, nseg)
+                                       : la_split_sum4(resid, tile, src >> 8, off, nseg);
                     upd[k] = true;
                 }
             }
@@ -603,12 +637,13 @@ void la_launch_embed(const LaDev& d, cudaStream_t st, int dtype, const void* emb
 void la_launch_rmsnorm(const LaDev& d, cudaStream_t st, int dtype, float* x, const void* g, void* y, int dm,
                        float eps, int sel, int gather, int rows_cap, const LaSplit& resid) {
     const dim3 threads(dm > 2048 ? 1024 : 256);
+    const bool one = dm <= 4 * (int)threads.x;           // one float4 a thread
     if (dtype == LA_F32)
-        la_launch_pdl(k_rmsnorm<float>, dim3(rows_cap), threads, 0, st, d, x, (const float*)g, (float*)y, dm, eps, sel,
-                      gather, resid);
+        la_launch_pdl(one ? k_rmsnorm<float, 1> : k_rmsnorm<float, 2>, dim3(rows_cap), threads, 0, st, d, x,
+                      (const float*)g, (float*)y, dm, eps, sel, gather, resid);
     else
-        la_launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows_cap), threads, 0, st, d, x, (const __nv_bfloat16*)g,
-                      (__nv_bfloat16*)y, dm, eps, sel, gather, resid);
+        la_launch_pdl(one ? k_rmsnorm<__nv_bfloat16, 1> : k_rmsnorm<__nv_bfloat16, 2>, dim3(rows_cap), threads, 0,
+                      st, d, x, (const __nv_bfloat16*)g, (__nv_bfloat16*)y, dm, eps, sel, gather, resid);
 }
 
 void la_launch_rope_kv(const LaDev& d, cudaStream_t st, int dtype, const void* qkv, const float* rcos, const float* rsin,
