@@ -466,7 +466,9 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
     dom_launches_call = prof["launches"][dom["kind"]] / samples
     dom_bytes = gemm_bytes_per_call(cfg, mean_Q, 1 + W + mean_ct * (N - 1))
     dom_achieved = dom_bytes / (dom_ms_call * 1e-3) / 1e9 if dom_ms_call > 0 else None
-    traffic, digest = captured_traffic(dom["profile"], dom["sources"]) if args.workload == "headline" else (None, None)
+    # the capture is of the full headline model's calls
+    full = args.workload == "headline" and not args.layers
+    traffic, digest = captured_traffic(dom["profile"], dom["sources"]) if full else (None, None)
     line = {
         "metric": METRIC if args.workload == "headline" else f"{METRIC} [{args.workload}]",
         "value": tps,

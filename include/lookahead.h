@@ -396,6 +396,9 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
  *   mode 1 resid   y[q][n] += acc                     (y holds the input, fp32)
  *   mode 2 swiglu  y[q][n] = bf16(silu(acc_w) * acc_w2)
  *   mode 3 logits  y[q][n] = acc (fp32)
+ * mode | LA_GEMM_PAIR (not with swiglu): the GEMM streams units of one
+ * 64-column atom of two adjacent 128-row output tiles, as the model's QKV,
+ * O, down and LM head GEMMs do (n_out / n_seg a multiple of 256).
  * w [n_out][K], w2 [n_out][K] (swiglu only), x [rows][K]; y (host)
  * [rows][n_out] fp32 (bf16 results widened).  n_out a multiple of
  * 128 * n_seg (n_seg 1..3), K of 64, 1 <= rows <= 1024, 0 <= n_cta <= 4096.
@@ -403,6 +406,7 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
  * GEMMs stream (la_init does the same for every projection).
  * Uses the current device and allocates its own temporary device buffers.
  * Errors: LA_EINVAL, LA_ECUDA, LA_ETIMEOUT. */
+#define LA_GEMM_PAIR 16
 int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K,
                   const uint16_t* x, int rows, int n_cta, float* y);
 

@@ -1578,11 +1578,14 @@ int la_debug_sample_verify(const float* logits, int rows, int V, const int32_t* 
 
 int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, int n_out, int K, const uint16_t* x,
                   int rows, int n_cta, float* y) {
+    const int pair = (mode & LA_GEMM_PAIR) ? 1 : 0;
+    mode &= ~LA_GEMM_PAIR;
     if (!w || !x || !y || mode < GEMM_STORE || mode > GEMM_LOGITS || n_seg < 1 || n_seg > 3 || n_out < 128 ||
         n_out % (128 * n_seg) || K < 64 || K % 64 || rows < 1 || rows > 1024 || n_cta < 0 || n_cta > 4096)
         return LA_EINVAL;
+    if (pair && (mode == GEMM_SWIGLU || (n_out / n_seg) % 256)) return LA_EINVAL;
     if (n_cta == 0) n_cta = la_tc_ctas();
-    const int max_seg = la_tc_max_segments(n_out / 128, la_tc_k_units(mode, K), n_cta);
+    const int max_seg = la_tc_max_segments(n_out / 128 / (pair ? 2 : 1), la_tc_k_units(mode, K, pair), n_cta);
     if (mode == GEMM_SWIGLU && (!w2 || n_seg != 1)) return LA_EINVAL;
     if (mode == GEMM_LOGITS && n_seg != 1) return LA_EINVAL;
     const int rows_cap = ((rows + 255) / 256) * 256;
@@ -1633,6 +1636,7 @@ int la_debug_gemm(int mode, const uint16_t* w, const uint16_t* w2, int n_seg, in
         g.K = K;
         g.Nout = n_out;
         g.seg_tiles = n_seg > 1 ? n_seg_out / 128 : 0;
+        g.pair = pair;
         g.n_cta = n_cta;
         g.max_seg = max_seg;
         g.rows_cap = rows_cap;
