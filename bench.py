@@ -323,9 +323,10 @@ def run_batch(args, cfg, rank: int, local: int) -> None:
 # The single-request workloads: the headline (the pages' plain configuration
 # on the 7B shape); pool seeding on the same prompt and the copy-heavy 13B
 # prompt, where a trained model would accept the pool's candidates (a
-# random-init one does not continue the prompt's n-grams); and a 7B-shape
+# random-init one does not continue the prompt's n-grams); a 7B-shape
 # model whose greedy next token is nearly a function of the current token,
-# where the collected n-grams come true and calls commit several tokens.
+# where the collected n-grams come true and calls commit several tokens; and
+# sampled decoding of 16 prompts (the verifier's exact rejection scheme).
 WORKLOADS = {
     "headline": {"desc": "llama-7b-shape bf16, batch 1, prompt 512 Markov/Zipf(1.1), 256 new tokens, greedy, "
                          "W=15 N=5 G=15", "model": "llama-7b-shape (random init)", "prompt": "markov",
@@ -345,6 +346,12 @@ WORKLOADS = {
                        "model": "llama-7b-shape (random init, wo x 2^-10)", "prompt": "markov",
                        "prompt_len": PROMPT_LEN, "max_new": MAX_NEW, "seed": 2, "knobs": (W_, N_, G_), "options": 0,
                        "cfg": "LLAMA_7B", "wo_scale": 2.0 ** -10},
+    "sampled-7b": {"desc": "llama-7b-shape bf16, sampling (temperature 0.8, top-p 0.9, exact verification of the "
+                           "candidates), 16 prompts of 256 Markov/Zipf(1.1) tokens one after another, 256 new "
+                           "tokens each, W=15 N=5 G=15",
+                   "model": "llama-7b-shape (random init)", "prompt": "markov", "prompt_len": 256, "max_new": 256,
+                   "seed": 40, "knobs": (W_, N_, G_), "options": 0, "cfg": "LLAMA_7B", "n_prompts": 16,
+                   "sampling": (0.8, 0.9)},
 }
 # the nominal HBM3e bandwidth the step roofline is also quoted against
 SPEC_HBM_GBS = 8000.0
@@ -357,7 +364,7 @@ DOMINANT = {"kind": "gemm", "profile": "k_gemm_tc_llama7b_decode_call.md",
                     "algorithmic bytes / summed launch time"}
 
 
-def timeline_per_call(L, ctx, prompt, W: int, N: int, G: int, calls: int = 16):
+def timeline_per_call(L, ctx, prompt, W: int, N: int, G: int, calls: int = 16, sampling=None):
     """Per-kind device time of a packed call from the library's kernel
     timeline (global-timer stamps per CTA, no events in the graph): one more
     request, prefill untimed, then `calls` packed calls one by one; every
@@ -365,11 +372,11 @@ def timeline_per_call(L, ctx, prompt, W: int, N: int, G: int, calls: int = 16):
     add up to the calls' device time (host gaps between calls are left out)."""
     import numpy as np
     cap = 120_000 * calls
-    L.la_prefill(ctx.ctx, prompt)
+    L.la_prefill(ctx.ctx, prompt, sampling=sampling)
     L.la_timeline_start(cap)
     try:
         for _ in range(calls):
-            L.la_step(ctx.ctx, W, N, G)
+            L.la_step(ctx.ctx, W, N, G, sampling=sampling)
     finally:
         rec = L.la_timeline_stop(cap)
     split = L.timeline_split(rec)
@@ -396,27 +403,34 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
     ctx = L.Context(cfg, w, max_ctx=max(1024, plen + max_new + 64), max_W=W, max_N=N, max_G=G)
     if wl["options"]:
         L.la_set_options(ctx.ctx, wl["options"])
+    n_prompts = wl.get("n_prompts", 1)
     if wl["prompt"] == "markov":
-        prompt = synth.markov_zipf_prompt(cfg.vocab, plen, wl["seed"]).tolist()
+        prompts = [synth.markov_zipf_prompt(cfg.vocab, plen, wl["seed"] + i).tolist() for i in range(n_prompts)]
     else:
-        prompt = synth.code_like_prompt(cfg.vocab, plen, wl["seed"]).tolist()
+        prompts = [synth.code_like_prompt(cfg.vocab, plen, wl["seed"] + i).tolist() for i in range(n_prompts)]
+    prompt = prompts[0]
+    temp_top_p = wl.get("sampling")       # (temperature, top_p): request i of step k draws with seed 1000 k + i
+
+    def samp(step: int, i: int):
+        return None if temp_top_p is None else (temp_top_p[0], temp_top_p[1], 1000 * step + i)
 
     def barrier():
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
 
-    for _ in range(args.warmup):
-        L.la_generate(ctx.ctx, prompt, max_new, W, N, G)
+    for k in range(args.warmup):
+        L.la_generate(ctx.ctx, prompt, max_new, W, N, G, sampling=samp(k + 100, 0))
     clocks = ClockSampler(local)
     barrier()
     t0 = time.perf_counter()
     stats = []
     outs = []
-    for _ in range(args.steps):
-        st = L.la_stats()
-        outs.append(L.la_generate(ctx.ctx, prompt, max_new, W, N, G, stats=st))
-        stats.append(st)
+    for k in range(args.steps):
+        for i, pr in enumerate(prompts):
+            st = L.la_stats()
+            outs.append(L.la_generate(ctx.ctx, pr, max_new, W, N, G, sampling=samp(k, i), stats=st))
+            stats.append(st)
     barrier()
     wall = time.perf_counter() - t0
     clk = clocks.stop()
@@ -432,13 +446,18 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
 
     # autoregressive decode on the same kernels and context
     ar_stats = []
-    for _ in range(args.ar_steps):
-        st = L.la_stats()
-        ar = L.la_generate_ar(ctx.ctx, prompt, max_new, stats=st)
-        ar_stats.append(st)
+    ars = []
+    for k in range(args.ar_steps):
+        for i, pr in enumerate(prompts):
+            st = L.la_stats()
+            ars.append(L.la_generate_ar(ctx.ctx, pr, max_new, sampling=samp(k, i), stats=st))
+            ar_stats.append(st)
     ar_tps = (sum(s.tokens - 1 for s in ar_stats) / (sum(s.decode_ns for s in ar_stats) * 1e-9)) if ar_stats else None
     ar_ms = (sum(s.decode_ns for s in ar_stats) * 1e-6 / sum(s.steps for s in ar_stats)) if ar_stats else None
-    same = all(o == ar for o in outs) if ar_stats else None
+    # greedy: every request's lookahead output equals its AR output (sampled
+    # outputs draw differently; the verifier's law is checked by the tests)
+    same = (all(outs[k * n_prompts + i] == ars[i] for k in range(args.steps) for i in range(n_prompts))
+            if ar_stats and temp_top_p is None else None)
 
     # Live kernel timing of the same workload (one more request, with the
     # step graph bracketing every launch by CUDA events on the library's
@@ -446,10 +465,10 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
     # the per-kind figures are upper bounds that need not add up to a call.
     L.la_set_debug(ctx.ctx, 4)
     st_prof = L.la_stats()
-    L.la_generate(ctx.ctx, prompt, max_new, W, N, G, stats=st_prof)
+    L.la_generate(ctx.ctx, prompt, max_new, W, N, G, sampling=samp(200, 0), stats=st_prof)
     prof = L.la_profile_read(ctx.ctx)
     L.la_set_debug(ctx.ctx, 0)
-    tl = timeline_per_call(L, ctx, prompt, W, N, G)
+    tl = timeline_per_call(L, ctx, prompt, W, N, G, sampling=samp(300, 0))
 
     launches = sum(s.kernel_launches for s in stats)        # counted by the library
     peaks, src = measured_peaks()
@@ -494,8 +513,8 @@ def run_single(args, cfg, config, wl, rank: int, local: int, world: int):
         "ar_call_latency_ms": ar_ms,
         "speedup_vs_ar": tps / ar_tps if (world == 1 and ar_tps) else None,
         "lookahead_equals_ar": same,
-        "e2e": {"value": (max_new * args.steps * world) / wall, "unit": "tokens/s",
-                "h2d_bytes_per_step": plen * 4, "d2h_bytes_per_step": max_new * 4},
+        "e2e": {"value": (max_new * n_prompts * args.steps * world) / wall, "unit": "tokens/s",
+                "h2d_bytes_per_step": n_prompts * plen * 4, "d2h_bytes_per_step": n_prompts * max_new * 4},
         "roofline": {"bound": "hbm", "achieved": dom_achieved, "peak": peak, "unit": "GB/s",
                      "frac": (dom_achieved / peak) if dom_achieved else None,
                      "traffic": traffic,

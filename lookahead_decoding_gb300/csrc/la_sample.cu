@@ -40,6 +40,17 @@ __device__ __forceinline__ float philox_uniform(uint32_t k0, uint32_t k1, uint32
     return (float)(c0 >> 8) * (1.0f / 16777216.0f);
 }
 
+// The distribution lives in shared memory in the blocked id layout (thread
+// t owns ids [t per, (t + 1) per)), each thread's run starting at t * pstride
+// with pstride odd: a warp's 32 threads stepping through their runs touch 32
+// different banks (runs at t * per for even per hit one bank 32 times).
+__host__ __device__ __forceinline__ int p_per(int V) { return (V + NT - 1) / NT; }
+__host__ __device__ __forceinline__ int p_stride(int V) { return p_per(V) | 1; }
+__device__ __forceinline__ int pidx(int i, int V) {
+    const int per = p_per(V), q = i / per;
+    return q * p_stride(V) + (i - q * per);
+}
+
 struct Red {
     float f[NW];
     int i[NW];
@@ -117,9 +128,10 @@ __device__ float block_excl_scan(float v, Red& r, float* total) {
 }
 
 // p[] <- nucleus-restricted softmax(logits / T), normalised (blocked id layout)
-__device__ void warp_distribution(const float* logits, float* p, int V, float T, float top_p, Red& r) {
-    const int per = (V + NT - 1) / NT;
+__device__ void warp_distribution(const float* logits, float* pall, int V, float T, float top_p, Red& r) {
+    const int per = p_per(V);
     const int i0 = threadIdx.x * per, i1 = min(V, i0 + per);
+    float* p = pall + threadIdx.x * p_stride(V) - i0;   // p[i] for this thread's ids
     float m = -INFINITY;
     for (int i = i0; i < i1; ++i) m = fmaxf(m, logits[i] / T);
     m = block_max(m, r);
@@ -184,9 +196,10 @@ __device__ void warp_distribution(const float* logits, float* p, int V, float T,
 }
 
 // inverse CDF in id order: the first id whose cumulative mass exceeds u * total
-__device__ int draw_index(const float* p, int V, float u, Red& r) {
-    const int per = (V + NT - 1) / NT;
+__device__ int draw_index(const float* pall, int V, float u, Red& r) {
+    const int per = p_per(V);
     const int i0 = threadIdx.x * per, i1 = min(V, i0 + per);
+    const float* p = pall + threadIdx.x * p_stride(V) - i0;
     float s = 0.f;
     int last_nz = -1;
     for (int i = i0; i < i1; ++i) {
@@ -265,8 +278,9 @@ __device__ void sample_verify_core(const SvIn& in, float* p, Red& r, SvOut& o) {
                 s_tested[t] = tok;
                 const float rem = 1.0f - s_removed;
                 const float u = philox_uniform(in.k0, in.k1, in.step, (uint32_t)off, (uint32_t)t, PURPOSE_ACCEPT);
-                if (u < p[tok] / rem) { s_acc = tok; break; }
-                s_removed += p[tok];
+                const float pt = p[pidx(tok, V)];
+                if (u < pt / rem) { s_acc = tok; break; }
+                s_removed += pt;
                 if (!(1.0f - s_removed > 0.f)) { s_acc = tok; break; }   // all remaining mass was this token's
             }
         }
@@ -288,7 +302,7 @@ __device__ void sample_verify_core(const SvIn& in, float* p, Red& r, SvOut& o) {
         }
         // every offered token rejected: draw from the residual and stop
         if (threadIdx.x == 0)
-            for (int t = 0; t < s_ntested; ++t) p[s_tested[t]] = 0.f;
+            for (int t = 0; t < s_ntested; ++t) p[pidx(s_tested[t], V)] = 0.f;
         __syncthreads();
         const float u = philox_uniform(in.k0, in.k1, in.step, (uint32_t)off, 0u, PURPOSE_RESIDUAL);
         const int tok = draw_index(p, V, u, r);
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__(NT) k_sample_verify_trials(const float* logits
 
 cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V, const int32_t* cand, int Ct, int S,
                                     float T, float top_p, uint64_t seed, int n_trials, int32_t* out) {
-    const size_t smem = sizeof(float) * (size_t)V;
+    const size_t smem = sizeof(float) * (size_t)NT * p_stride(V);
     cudaError_t e = cudaFuncSetAttribute(k_sample_verify_trials, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int grid = n_trials < 4096 ? n_trials : 4096;
@@ -365,7 +379,7 @@ cudaError_t la_launch_sample_trials(cudaStream_t st, const float* logits, int V,
 }
 
 cudaError_t la_launch_sample_verify(const LaDev& d, cudaStream_t st, const float* logits, int V, int prefill) {
-    const size_t smem = sizeof(float) * (size_t)V;
+    const size_t smem = sizeof(float) * (size_t)NT * p_stride(V);
     // the kernel's shared-memory allowance only grows: a context with a
     // larger vocabulary than the ones before raises it
     static size_t allowed = 0;

@@ -63,3 +63,15 @@ def test_timeline_split_adds_up_to_the_span():
                   np.ones(300, int)], axis=1).astype(np.int64)
     q = timeline_split(r)
     assert sum(q["ns"].values()) + q["idle_ns"] == q["span_ns"] == int(r[:, 1].max() - r[0, 0])
+
+
+def test_workloads_are_complete():
+    """Every single-request workload names its model shape, prompt kind and
+    knobs; the sampled one runs 16 prompts at temperature 0.8, top-p 0.9."""
+    import synth
+    for name, wl in bench.WORKLOADS.items():
+        for key in ("desc", "model", "prompt", "prompt_len", "max_new", "seed", "knobs", "options", "cfg"):
+            assert key in wl, (name, key)
+        assert hasattr(synth, wl["cfg"]) and wl["prompt"] in ("markov", "code")
+    s = bench.WORKLOADS["sampled-7b"]
+    assert s["n_prompts"] == 16 and s["sampling"] == (0.8, 0.9) and s["prompt_len"] == 256
