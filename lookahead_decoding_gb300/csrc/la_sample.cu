@@ -56,6 +56,7 @@ struct Red {
     int i[NW];
     float bcast_f;
     int bcast_i;
+    float f2[2][NW];      // the one-barrier sums of a loop, alternating by iteration
 };
 
 __device__ float block_sum(float v, Red& r) {
@@ -71,6 +72,19 @@ __device__ float block_sum(float v, Red& r) {
     }
     __syncthreads();
     return r.bcast_f;
+}
+// The same sum as block_sum with one barrier: every warp adds the 32 warp
+// partials in the same shuffle tree.  Consecutive calls must alternate ph (a
+// warp cannot rewrite a slot until every warp has passed the next call's
+// barrier, i.e. finished reading it).
+__device__ float block_sum_1(float v, Red& r, int ph) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) r.f2[ph][w] = v;
+    __syncthreads();
+    float x = r.f2[ph][l];
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
 }
 __device__ float block_max(float v, Red& r) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -132,12 +146,16 @@ __device__ void warp_distribution(const float* logits, float* pall, int V, float
     const int per = p_per(V);
     const int i0 = threadIdx.x * per, i1 = min(V, i0 + per);
     float* p = pall + threadIdx.x * p_stride(V) - i0;   // p[i] for this thread's ids
+    // logits / T staged by coalesced reads (a thread's run of ids would
+    // touch 32 lines a warp instruction, and the runs outgrow L1)
+    for (int i = threadIdx.x; i < V; i += NT) pall[pidx(i, V)] = logits[i] / T;
+    __syncthreads();
     float m = -INFINITY;
-    for (int i = i0; i < i1; ++i) m = fmaxf(m, logits[i] / T);
+    for (int i = i0; i < i1; ++i) m = fmaxf(m, p[i]);
     m = block_max(m, r);
     float s = 0.f;
     for (int i = i0; i < i1; ++i) {
-        const float e = expf(logits[i] / T - m);
+        const float e = expf(p[i] - m);
         p[i] = e;
         s += e;
     }
@@ -151,14 +169,16 @@ __device__ void warp_distribution(const float* logits, float* pall, int V, float
     pmax = block_max(pmax, r);
     // largest threshold tau (a float bit pattern) whose mass at-or-above reaches top_p
     uint32_t lo = 0u, hi = __float_as_uint(pmax) + 1u;
+    int ph = 0;
     while (hi - lo > 1u) {
         const uint32_t mid = lo + ((hi - lo) >> 1);
         const float b = __uint_as_float(mid);
         float g = 0.f;
         for (int i = i0; i < i1; ++i)
             if (p[i] >= b) g += p[i];
-        if (block_sum(g, r) >= top_p) lo = mid;
+        if (block_sum_1(g, r, ph) >= top_p) lo = mid;
         else hi = mid;
+        ph ^= 1;
     }
     const float tau = __uint_as_float(lo);
     float a = 0.f;
