@@ -350,8 +350,39 @@ __global__ void __launch_bounds__(FT * 32) k_attn_fused(LaDev d, const __nv_bflo
     };
     // the queries now; the keys and values for the commit by the warps that
     // wait out the committed blocks
-    if (fuse)
-        for (int j = tid; j < RI; j += blockDim.x) rope_item(0, j);
+    if (fuse) {
+        // the queries: two lanes an item, one rotation partner each (its
+        // segments' loads in one round), the pair exchanged by a shuffle
+        for (int j = tid; j < 2 * RI; j += blockDim.x) {
+            const int item = j >> 1, hf = j & 1;
+            const int r = item / (half / 4), c4 = (item % (half / 4)) * 4;
+            const bool live = r < nr;
+            float4 own = make_float4(0.f, 0.f, 0.f, 0.f), c = own, sn = own;
+            if (live) {
+                const int row = r0 + r, pos = rpos[r];
+                const __nv_bfloat16* x = rope.qkv + (size_t)row * 3 * HD;
+                own = la_qkv_at4_w8(x, row, hh * DH + c4 + hf * half, rope.sp, seg_q);
+                c = *reinterpret_cast<const float4*>(rope.rcos + (size_t)pos * half + c4);
+                sn = *reinterpret_cast<const float4*>(rope.rsin + (size_t)pos * half + c4);
+            }
+            float4 oth;
+            oth.x = __shfl_xor_sync(0xffffffffu, own.x, 1);
+            oth.y = __shfl_xor_sync(0xffffffffu, own.y, 1);
+            oth.z = __shfl_xor_sync(0xffffffffu, own.z, 1);
+            oth.w = __shfl_xor_sync(0xffffffffu, own.w, 1);
+            const float4 a = hf ? oth : own, b = hf ? own : oth;
+            __nv_bfloat16* qd = qs_w + r * LDK + c4 + hf * half;
+            if (!live) {
+                *reinterpret_cast<uint2*>(qd) = make_uint2(0u, 0u);
+            } else if (hf == 0) {
+                *reinterpret_cast<uint2*>(qd) = la_pack_bf16x4(la_rope_lo(a.x, b.x, c.x, sn.x), la_rope_lo(a.y, b.y, c.y, sn.y),
+                                                               la_rope_lo(a.z, b.z, c.z, sn.z), la_rope_lo(a.w, b.w, c.w, sn.w));
+            } else {
+                *reinterpret_cast<uint2*>(qd) = la_pack_bf16x4(la_rope_hi(a.x, b.x, c.x, sn.x), la_rope_hi(a.y, b.y, c.y, sn.y),
+                                                               la_rope_hi(a.z, b.z, c.z, sn.z), la_rope_hi(a.w, b.w, c.w, sn.w));
+            }
+        }
+    }
     int t0max = 0, t0min = 0x7fffffff, posmax = 0;
     for (int r = 0; r < nr; ++r) {
         t0max = max(t0max, rt0[r]);
