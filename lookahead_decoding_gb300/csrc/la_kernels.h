@@ -107,32 +107,6 @@ __device__ __forceinline__ float4 la_split_sum4(const LaSplit& s, int t, int y, 
     return r;
 }
 
-// la_split_sum4 with the first eight segments' loads issued together (same
-// additions, K order), for callers with the registers for them
-__device__ __forceinline__ float4 la_split_sum4_w8(const LaSplit& s, int t, int y, size_t off, int nseg) {
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (k < nseg) v[k] = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, k, 0) + off));
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (k < nseg) {
-            r.x = __fadd_rn(r.x, v[k].x);
-            r.y = __fadd_rn(r.y, v[k].y);
-            r.z = __fadd_rn(r.z, v[k].z);
-            r.w = __fadd_rn(r.w, v[k].w);
-        }
-    for (int s0 = 8; s0 < nseg; ++s0) {
-        const float4 q = __ldcg(reinterpret_cast<const float4*>(la_split_rec(s, t, y, s0, 0) + off));
-        r.x = __fadd_rn(r.x, q.x);
-        r.y = __fadd_rn(r.y, q.y);
-        r.z = __fadd_rn(r.z, q.z);
-        r.w = __fadd_rn(r.w, q.w);
-    }
-    return r;
-}
-
 // RoPE of bf16 models on four consecutive dimensions i..i+3 (< dh/2) and
 // their rotation partners, shared by the RoPE kernel and the attention that
 // folds it in: values as the QKV GEMM's bf16 store would have rounded them,
@@ -148,17 +122,6 @@ __device__ __forceinline__ float4 la_qkv_at4(const __nv_bfloat16* row, int q, in
                            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
     }
     const float4 s = la_split_sum4(sp, n >> 7, q >> 8, (size_t)(q & 255) * 128 + (n & 127), nseg);
-    return make_float4(la_bf16_round(s.x), la_bf16_round(s.y), la_bf16_round(s.z), la_bf16_round(s.w));
-}
-
-// la_qkv_at4 with the wide segment loads
-__device__ __forceinline__ float4 la_qkv_at4_w8(const __nv_bfloat16* row, int q, int n, const LaSplit& sp, int nseg) {
-    if (nseg <= 1) {
-        const uint2 u = *reinterpret_cast<const uint2*>(row + n);
-        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-    }
-    const float4 s = la_split_sum4_w8(sp, n >> 7, q >> 8, (size_t)(q & 255) * 128 + (n & 127), nseg);
     return make_float4(la_bf16_round(s.x), la_bf16_round(s.y), la_bf16_round(s.z), la_bf16_round(s.w));
 }
 
