@@ -302,6 +302,7 @@ def run_batch(args, cfg, rank: int, local: int) -> None:
     calls = sum(s.steps for s in stats)
     new_tokens = sum(B * (args.max_new - 1) for _ in stats)
     ar = [L.la_generate_ar(ctx.ctx, p, args.max_new) for p in prompts]
+    tl = batch_timeline_per_call(L, ctx, prompts, W_, N_, G_)
     config = {"workload": f"llama-7b-shape bf16, {B} requests per packed call, prompts 512 Markov/Zipf(1.1), "
                           f"{args.max_new} new tokens each, greedy, W=15 N=5 G=15",
               "model": "llama-7b-shape (random init)", "global_batch": B, "seq_len": PROMPT_LEN + args.max_new,
@@ -315,7 +316,8 @@ def run_batch(args, cfg, rank: int, local: int) -> None:
             "gpu_launches": sum(s.kernel_launches for s in stats),
             "e2e": {"value": B * args.max_new * args.steps / wall, "unit": "tokens/s",
                     "h2d_bytes_per_step": B * PROMPT_LEN * 4, "d2h_bytes_per_step": B * args.max_new * 4},
-            "clocks": clk}
+            "kernel_ms_per_call": tl["ms"], "kernel_ms_per_call_by_kernel": tl["by_kernel_ms"],
+            "kernel_timing": tl["what"], "clocks": clk}
     ctx.close()
     print(json.dumps(line))
 
@@ -386,6 +388,41 @@ def timeline_per_call(L, ctx, prompt, W: int, N: int, G: int, calls: int = 16, s
             "what": ("split of %d packed calls' device time from per-CTA global-timer stamps (every instant "
                      "charged to the running CTA that finishes next); the kinds add up to the calls' device "
                      "time, host gaps between the calls left out" % calls)}
+
+
+def split_difference(long_split, short_split, calls: int):
+    """Per-call device time of the calls that separate two kernel timelines of
+    the same work (`timeline_split` results): the longer run's charges minus
+    the shorter run's, per kind and per kernel, over `calls` calls.  Kernels
+    whose charge does not grow between the runs (the prefill's, which both
+    runs share up to the timer's jitter) are left out."""
+    def diff(a, b):
+        return {k: (v - b.get(k, 0)) * 1e-6 / calls for k, v in a.items() if v > b.get(k, 0)}
+    return {"ms": diff(long_split["ns"], short_split["ns"]),
+            "by_kernel_ms": diff(long_split["by_kernel_ns"], short_split["by_kernel_ns"])}
+
+
+def batch_timeline_per_call(L, ctx, prompts, W: int, N: int, G: int, short: int = 2, long: int = 18):
+    """Per-kind device time of a batched packed call: the kernel timeline of
+    the request set generated to `long` tokens minus the same set generated
+    to `short` (the prefills and first calls are the same and cancel), over
+    the calls between them."""
+    splits, steps = {}, {}
+    for mn in (short, long):
+        cap = 200_000 * (mn + 8) * len(prompts)
+        st = L.la_stats()
+        L.la_timeline_start(cap)
+        try:
+            L.la_generate_batch(ctx.ctx, prompts, mn, W, N, G, stats=st)
+        finally:
+            rec = L.la_timeline_stop(cap)
+        splits[mn], steps[mn] = L.timeline_split(rec), st.steps
+    calls = steps[long] - steps[short]
+    out = split_difference(splits[long], splits[short], calls)
+    out["what"] = ("split of %d batched calls' device time from per-CTA global-timer stamps (a run to %d "
+                   "tokens minus a run to %d, prefills cancelling); every instant charged to the running "
+                   "CTA that finishes next" % (calls, long, short))
+    return out
 
 
 def run_single(args, cfg, config, wl, rank: int, local: int, world: int):

@@ -2,6 +2,8 @@
 import os
 import sys
 
+import pytest
+
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 import bench  # noqa: E402
@@ -63,6 +65,21 @@ def test_timeline_split_adds_up_to_the_span():
                   np.ones(300, int)], axis=1).astype(np.int64)
     q = timeline_split(r)
     assert sum(q["ns"].values()) + q["idle_ns"] == q["span_ns"] == int(r[:, 1].max() - r[0, 0])
+
+
+def test_split_difference_is_per_call():
+    """The batched line's per-call split: the longer timeline's charges minus
+    the shorter one's, per kind and per kernel, over the calls between them
+    (a kind absent from the shorter run counts from zero; a kernel whose
+    charge does not grow, like a shared prefill's, is left out)."""
+    long = {"ns": {"gemm": 5_000_000, "attention": 1_000_000, "rowwise": 0, "state": 300_000},
+            "by_kernel_ns": {"k_gemm_tc": 5_000_000, "k_attn_fused": 1_000_000, "k_pack": 300_000,
+                             "k_prefill_rows": 999}}
+    short = {"ns": {"gemm": 1_000_000, "attention": 200_000, "rowwise": 0},
+             "by_kernel_ns": {"k_gemm_tc": 1_000_000, "k_attn_fused": 200_000, "k_prefill_rows": 1000}}
+    d = bench.split_difference(long, short, 4)
+    assert d["ms"] == pytest.approx({"gemm": 1.0, "attention": 0.2, "state": 0.075}, rel=1e-12)
+    assert d["by_kernel_ms"] == pytest.approx({"k_gemm_tc": 1.0, "k_attn_fused": 0.2, "k_pack": 0.075}, rel=1e-12)
 
 
 def test_workloads_are_complete():
