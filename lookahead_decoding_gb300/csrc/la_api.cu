@@ -867,9 +867,12 @@ int la_init_batch(const la_model_cfg* cfg, const la_weights* w, int max_ctx, int
         const char* pp = getenv("LA_TC_PAIR");      // bit 0 QKV, bit 1 O, bit 2 down, bit 3 LM head
         const char* pk = getenv("LA_TC_PACK");
         const char* mg = getenv("LA_MEGA");
-        // (only where a decode call stacks at most 128 rows: at more, a unit's
-        // two accumulators fill TMEM and the kernel cannot double-buffer them)
-        const int call_rows = max_batch * ((ctx->Qmax + 15) / 16 * 16);
+        // (only where the rows every decode call stacks fit 128: above, a
+        // unit's two accumulators fill TMEM and the kernel keeps one buffer.
+        // A request's calls always carry the lookahead branch's W (N - 1)
+        // rows and the ordinary row, and candidates add rows only to the calls
+        // that have them; a batched call stacks every request's whole slice.)
+        const int call_rows = max_batch > 1 ? max_batch * ctx->Qstride : max_W * (max_N - 1) + 1;
         const int pmask = (!(pk && pk[0] == '0') && !(mg && mg[0] == '1') && call_rows <= 128)
                               ? (pp ? atoi(pp) : 15) : 0;
         for (int l = 0; l < c.n_layers && !r; ++l) {
